@@ -1,0 +1,128 @@
+"""fp64 CPU oracle for batched speculative-decoding verification.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg (and its reference arm) may import this package.
+The product library never imports, links or executes it, and the two share no
+code: this side is plain C in ``oracle.c`` compiled with gcc.
+
+Citations ([P1]-[P3], page title and section) are listed in ``oracle.h``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_HDR = os.path.join(_HERE, "oracle.h")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+OK, TOKEN_RANGE, NONFINITE, UNIFORM_RANGE = 0, 4, 5, 7
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def build(force: bool = False, src: str = _SRC, out: str = _LIB) -> str:
+    """Compile an oracle source into a shared library (skipped when up to date)."""
+    newest = max(os.path.getmtime(src), os.path.getmtime(_HDR))
+    if force or not os.path.exists(out) or os.path.getmtime(out) < newest:
+        tmp = out + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-ffp-contract=off", "-std=c99", "-Wall",
+                               "-I", _HERE, "-shared", "-fPIC", "-o", tmp, src, "-lm"])
+        os.replace(tmp, out)
+    return out
+
+
+def _bind(path: str) -> ctypes.CDLL:
+    lib = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    lib.oracle_verify.restype = ctypes.c_int
+    lib.oracle_verify.argtypes = [P, ctypes.c_int, P, P, P, ctypes.c_int64, ctypes.c_int,
+                                  ctypes.c_int64, ctypes.c_float] + [P] * 10
+    lib.oracle_softmax_row.restype = ctypes.c_int
+    lib.oracle_softmax_row.argtypes = [P, ctypes.c_int, ctypes.c_int64, ctypes.c_double,
+                                       P, P, P]
+    return lib
+
+
+def _load() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        _lib = _bind(build())
+    return _lib
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _dtype_code(dtype: str) -> int:
+    if dtype not in ("f32", "bf16"):
+        raise ValueError(f"unknown logits dtype {dtype!r}")
+    return 0 if dtype == "f32" else 1
+
+
+def softmax_row(row: np.ndarray, dtype: str, T: float):
+    """(status, p, m, s) for one stored logits row."""
+    lib = _load()
+    row = np.ascontiguousarray(row, dtype=np.float32 if dtype == "f32" else np.uint16)
+    V = row.shape[-1]
+    p = np.empty(V, dtype=np.float64)
+    m = ctypes.c_double()
+    s = ctypes.c_double()
+    st = lib.oracle_softmax_row(_ptr(row), _dtype_code(dtype), V, float(T), _ptr(p),
+                                ctypes.byref(m), ctypes.byref(s))
+    return st, p, m.value, s.value
+
+
+def verify(logits: np.ndarray, dtype: str, q: np.ndarray, tokens: np.ndarray,
+           uniforms: np.ndarray, T: float, lib: Optional[ctypes.CDLL] = None) -> dict:
+    """Run the oracle over a batch.  Shapes: logits [B, K+1, V] (float32, or uint16
+    bf16 bits), q [B, K, V] float32, tokens [B, K] int32, uniforms [B, K+1] float32.
+
+    Returns a dict of numpy arrays: accept_len, out_tokens, accept_mask, status,
+    row_m, row_s, p_draft, accept_margin, sample_margin, sample_alt.
+    ``lib`` selects another build of the oracle (used to show that the pins
+    catch planted mistakes); by default the oracle next to this file."""
+    lib = lib or _load()
+    logits = np.ascontiguousarray(logits, dtype=np.float32 if dtype == "f32" else np.uint16)
+    B, K1, V = logits.shape
+    K = K1 - 1
+    q = np.ascontiguousarray(q, dtype=np.float32).reshape(B, K, V)
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32).reshape(B, K)
+    uniforms = np.ascontiguousarray(uniforms, dtype=np.float32).reshape(B, K + 1)
+    out = {
+        "accept_len": np.empty(B, np.int32),
+        "out_tokens": np.empty((B, K + 1), np.int32),
+        "accept_mask": np.empty((B, K), np.uint8),
+        "status": np.empty(B, np.int32),
+        "row_m": np.empty((B, K + 1), np.float64),
+        "row_s": np.empty((B, K + 1), np.float64),
+        "p_draft": np.empty((B, K), np.float64),
+        "accept_margin": np.empty(B, np.float64),
+        "sample_margin": np.empty(B, np.float64),
+        "sample_alt": np.empty(B, np.int32),
+    }
+    rc = lib.oracle_verify(_ptr(logits), _dtype_code(dtype), _ptr(q), _ptr(tokens),
+                           _ptr(uniforms), B, K, V, float(T), _ptr(out["accept_len"]),
+                           _ptr(out["out_tokens"]), _ptr(out["accept_mask"]),
+                           _ptr(out["status"]), _ptr(out["row_m"]), _ptr(out["row_s"]),
+                           _ptr(out["p_draft"]), _ptr(out["accept_margin"]),
+                           _ptr(out["sample_margin"]), _ptr(out["sample_alt"]))
+    if rc != 0:
+        raise ValueError(f"oracle_verify rejected its arguments (rc={rc})")
+    return out
+
+
+def verify_inputs(inp, lib: Optional[ctypes.CDLL] = None) -> dict:
+    """verify() on a workloads.Inputs bundle."""
+    return verify(inp.logits, inp.dtype, inp.q, inp.tokens, inp.uniforms, inp.T, lib=lib)
+
+
+def load_variant(src_path: str, out_path: str) -> ctypes.CDLL:
+    """Build and bind another oracle source (a copy with a planted mistake)."""
+    return _bind(build(force=True, src=src_path, out=out_path))

@@ -1,0 +1,301 @@
+/*
+ * oracle.c -- fp64 CPU reference for batched speculative-decoding verification.
+ *
+ * TEST INFRASTRUCTURE ONLY (see oracle.h for the citations [P1]-[P3]).  It is
+ * slow and plain on purpose: one sequence at a time, one row at a time, every
+ * sum a left-to-right loop in double precision.  It follows the method step by
+ * step as the pages state it; where the pages leave a step open, the reading
+ * taken is stated next to the step.
+ *
+ * Build: gcc -O2 -ffp-contract=off -shared -fPIC oracle.c -lm
+ */
+#include "oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* One stored logit as an exact double.  bf16 widens to fp32 by placing its 16
+ * bits in the high half of the word; both widen exactly to double. */
+static double logit_at(const void* base, int dtype, int64_t idx)
+{
+    if (dtype == 0)
+        return (double)((const float*)base)[idx];
+    uint32_t bits = (uint32_t)((const uint16_t*)base)[idx] << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+/* [P1] "Speculative decoding: draft first, then verify": each target row is
+ * turned into a distribution by a softmax of logits / T.  Written out: z = l/T,
+ * m = max z, s = sum exp(z - m), p = exp(z - m) / s.  A NaN, a +inf, or a row
+ * with no finite-or-smaller value (all -inf) has no distribution; the pages are
+ * silent, and the reading taken is that such a sequence is an error. */
+int oracle_softmax_row(const void* row, int dtype, int64_t V, double T,
+                       double* p, double* m_out, double* s_out)
+{
+    double m = -INFINITY;
+    for (int64_t v = 0; v < V; ++v) {
+        double z = logit_at(row, dtype, v) / T;
+        if (isnan(z))
+            return ORACLE_NONFINITE;
+        if (z > m)
+            m = z;
+    }
+    if (!isfinite(m))
+        return ORACLE_NONFINITE;
+    double s = 0.0;
+    for (int64_t v = 0; v < V; ++v) {
+        double e = exp(logit_at(row, dtype, v) / T - m);
+        p[v] = e;
+        s += e;
+    }
+    for (int64_t v = 0; v < V; ++v)
+        p[v] /= s;
+    *m_out = m;
+    *s_out = s;
+    return ORACLE_OK;
+}
+
+static int q_value_ok(float x)
+{
+    return x >= 0.0f && isfinite(x);
+}
+
+/* Inverse-CDF draw from weights w[0..V) with the single uniform u: the first
+ * token whose running sum exceeds u * S, tokens taken in ascending id order.
+ * The pages call torch.multinomial and do not fix which exact sampler it is;
+ * any exact sampler has the right law, and this one is the plain definition.
+ * A weight of zero can never be drawn.  If rounding leaves u * S at or past the
+ * last running sum, the last positive-weight token is taken.
+ * Also reports the tie margin: the distance from u to the normalised running
+ * sums just below and at the drawn token, each counted only when a
+ * positive-weight token lies on the far side of that boundary. */
+static int64_t draw_inverse_cdf(const double* w, int64_t V, double S, double u,
+                                double* margin, int32_t* alt)
+{
+    const double t = u * S;
+    double run = 0.0, before = 0.0;
+    int64_t tok = -1;
+    for (int64_t v = 0; v < V; ++v) {
+        before = run;
+        run += w[v];
+        if (run > t) {
+            tok = v;
+            break;
+        }
+    }
+    if (tok < 0) {
+        for (int64_t v = V - 1; v >= 0; --v)
+            if (w[v] > 0.0) {
+                tok = v;
+                break;
+            }
+        before = 0.0;
+        for (int64_t v = 0; v < tok; ++v)
+            before += w[v];
+        run = before + w[tok];
+    }
+    int64_t prev = -1, next = -1;
+    for (int64_t v = tok - 1; v >= 0; --v)
+        if (w[v] > 0.0) {
+            prev = v;
+            break;
+        }
+    for (int64_t v = tok + 1; v < V; ++v)
+        if (w[v] > 0.0) {
+            next = v;
+            break;
+        }
+    double m_lo = prev >= 0 ? fabs(u - before / S) : INFINITY;
+    double m_hi = next >= 0 ? fabs(u - run / S) : INFINITY;
+    if (m_lo <= m_hi) {
+        *margin = m_lo;
+        *alt = (int32_t)prev;
+    } else {
+        *margin = m_hi;
+        *alt = (int32_t)next;
+    }
+    return tok;
+}
+
+/* One sequence.  p and w are scratch rows of V doubles. */
+static int verify_one(const void* logits, int dtype, const float* q, const int32_t* x,
+                      const float* u, int K, int64_t V, double T, double* p, double* w,
+                      int32_t* out_tok, uint8_t* mask, double* rm, double* rs, double* pd,
+                      double* a_margin, double* s_margin, int32_t* s_alt, int32_t* len)
+{
+    const size_t esz = dtype == 0 ? 4 : 2;
+    const char* lbase = (const char*)logits;
+
+    /* Every draft token must name a vocabulary entry and every uniform must lie
+     * in [0, 1) (the pages draw them with torch.rand, which has that range). */
+    for (int i = 0; i < K; ++i)
+        if (x[i] < 0 || (int64_t)x[i] >= V)
+            return ORACLE_TOKEN_RANGE;
+    for (int i = 0; i <= K; ++i)
+        if (!(u[i] >= 0.0f && u[i] < 1.0f))
+            return ORACLE_UNIFORM_RANGE;
+
+    /* [P1] verify loop: positions in order, stop at the first rejection.
+     * Acceptance probability is min(1, p(x)/q(x)) ([P1]; [P2] "Speculative
+     * decoding").  The test "u < min(1, p/q)" with u in [0, 1) is written as
+     * u * q(x) < p(x): identical for q(x) > 0, and for q(x) = 0 it accepts
+     * exactly when p(x) > 0.  The pages' prior-art code adds 1e-9 to q(x) as a
+     * guard; the method itself has no such term and it is left out. */
+    int j = K;
+    double m = 0.0, s = 0.0;
+    for (int i = 0; i < K; ++i) {
+        int st = oracle_softmax_row(lbase + (size_t)i * (size_t)V * esz, dtype, V, T, p, &m, &s);
+        if (st != ORACLE_OK)
+            return st;
+        rm[i] = m;
+        rs[i] = s;
+        const double px = p[x[i]];
+        const float qf = q[(size_t)i * (size_t)V + (size_t)x[i]];
+        if (!q_value_ok(qf))
+            return ORACLE_NONFINITE;
+        const double qx = (double)qf;
+        pd[i] = px;
+        if (qx > 0.0) {
+            double mg = fabs((double)u[i] - px / qx);
+            if (mg < *a_margin)
+                *a_margin = mg;
+        }
+        if ((double)u[i] * qx < px)
+            continue; /* accepted */
+        j = i;
+        break;
+    }
+
+    double S = 0.0;
+    if (j < K) {
+        /* [P1] rejection at position j: the corrected token comes from
+         * relu(p_j - q_j) normalised by its sum. */
+        const float* qj = q + (size_t)j * (size_t)V;
+        for (int64_t v = 0; v < V; ++v) {
+            if (!q_value_ok(qj[v]))
+                return ORACLE_NONFINITE;
+            const double d = p[v] - (double)qj[v];
+            w[v] = d > 0.0 ? d : 0.0;
+            S += w[v];
+        }
+        /* Exact arithmetic cannot reject with S = 0 when both rows sum to one;
+         * rounding or an unnormalised q can.  The pages are silent; the reading
+         * taken is to draw from p_j itself with the same uniform. */
+        if (S == 0.0) {
+            for (int64_t v = 0; v < V; ++v) {
+                w[v] = p[v];
+                S += w[v];
+            }
+        }
+    } else {
+        /* [P1] every draft accepted: the bonus token comes from the softmax of
+         * the last target row. */
+        int st = oracle_softmax_row(lbase + (size_t)K * (size_t)V * esz, dtype, V, T, p, &m, &s);
+        if (st != ORACLE_OK)
+            return st;
+        rm[K] = m;
+        rs[K] = s;
+        for (int64_t v = 0; v < V; ++v) {
+            w[v] = p[v];
+            S += w[v];
+        }
+    }
+
+    /* One uniform for the one sample of the pass: u[K]. */
+    const int64_t tok = draw_inverse_cdf(w, V, S, (double)u[K], s_margin, s_alt);
+
+    /* [P3] the accepted length counts the accepted drafts plus the one token
+     * the target always adds: AL in [1, 1 + D]. */
+    *len = j + 1;
+    for (int i = 0; i < j; ++i) {
+        out_tok[i] = x[i];
+        mask[i] = 1;
+    }
+    out_tok[j] = (int32_t)tok;
+    return ORACLE_OK;
+}
+
+int oracle_verify(const void* logits, int dtype, const float* q, const int32_t* tokens,
+                  const float* uniforms, int64_t B, int K, int64_t V, float temperature,
+                  int32_t* accept_len, int32_t* out_tokens, uint8_t* accept_mask,
+                  int32_t* status, double* row_m, double* row_s, double* p_draft,
+                  double* accept_margin, double* sample_margin, int32_t* sample_alt)
+{
+    if (!logits || !uniforms || !accept_len || !out_tokens || B < 0 || K < 0 || V < 1 ||
+        (K > 0 && (!q || !tokens || !accept_mask)) || (dtype != 0 && dtype != 1) ||
+        !(temperature > 0.0f) || !isfinite(temperature))
+        return -1;
+    /* scratch: two rows of V doubles, plus the per-row results of one sequence */
+    double* p = (double*)malloc((size_t)V * sizeof(double));
+    double* w = (double*)malloc((size_t)V * sizeof(double));
+    double* rm = (double*)malloc((size_t)(K + 1) * sizeof(double));
+    double* rs = (double*)malloc((size_t)(K + 1) * sizeof(double));
+    double* pd = (double*)malloc((size_t)(K + 1) * sizeof(double));
+    if (!p || !w || !rm || !rs || !pd) {
+        free(p); free(w); free(rm); free(rs); free(pd);
+        return -2;
+    }
+    const size_t esz = dtype == 0 ? 4 : 2;
+    const double T = (double)temperature;
+
+    for (int64_t b = 0; b < B; ++b) {
+        int32_t* ot = out_tokens + (size_t)b * (size_t)(K + 1);
+        uint8_t* mk = K > 0 ? accept_mask + (size_t)b * (size_t)K : 0;
+        uint8_t mk_dummy[1];
+        for (int i = 0; i <= K; ++i) {
+            ot[i] = -1;
+            rm[i] = NAN;
+            rs[i] = NAN;
+            if (i < K) {
+                mk[i] = 0;
+                pd[i] = NAN;
+            }
+        }
+        double a_mg = INFINITY, s_mg = INFINITY;
+        int32_t s_alt = -1, len = 0;
+        int st = verify_one((const char*)logits + (size_t)b * (size_t)(K + 1) * (size_t)V * esz,
+                            dtype, K > 0 ? q + (size_t)b * (size_t)K * (size_t)V : 0,
+                            K > 0 ? tokens + (size_t)b * (size_t)K : 0,
+                            uniforms + (size_t)b * (size_t)(K + 1), K, V, T, p, w, ot,
+                            mk ? mk : mk_dummy, rm, rs, pd, &a_mg, &s_mg, &s_alt, &len);
+        if (st != ORACLE_OK) {
+            /* an erroneous sequence reports nothing but its status */
+            len = 0;
+            for (int i = 0; i <= K; ++i) {
+                ot[i] = -1;
+                rm[i] = NAN;
+                rs[i] = NAN;
+                if (i < K) {
+                    mk[i] = 0;
+                    pd[i] = NAN;
+                }
+            }
+            a_mg = INFINITY;
+            s_mg = INFINITY;
+            s_alt = -1;
+        }
+        accept_len[b] = len;
+        if (status)
+            status[b] = st;
+        if (row_m)
+            for (int i = 0; i <= K; ++i)
+                row_m[(size_t)b * (size_t)(K + 1) + (size_t)i] = rm[i];
+        if (row_s)
+            for (int i = 0; i <= K; ++i)
+                row_s[(size_t)b * (size_t)(K + 1) + (size_t)i] = rs[i];
+        if (p_draft)
+            for (int i = 0; i < K; ++i)
+                p_draft[(size_t)b * (size_t)K + (size_t)i] = pd[i];
+        if (accept_margin)
+            accept_margin[b] = a_mg;
+        if (sample_margin)
+            sample_margin[b] = s_mg;
+        if (sample_alt)
+            sample_alt[b] = s_alt;
+    }
+    free(p); free(w); free(rm); free(rs); free(pd);
+    return 0;
+}

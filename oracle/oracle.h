@@ -1,0 +1,84 @@
+/*
+ * oracle.h -- fp64 CPU reference for batched speculative-decoding verification.
+ *
+ * TEST INFRASTRUCTURE ONLY.  The tests, the package smoke check and the
+ * benchmark's CPU-baseline leg call it; the product library never links it and
+ * shares no code, header or constant with it.
+ *
+ * Citations (page title, then section):
+ *  [P1] reactapp.top, "Speculative decoding and early exit: speeding up
+ *       autoregressive decode" -- section "Speculative decoding: draft first,
+ *       then verify" (the conceptual PyTorch loop: softmax of each target row at
+ *       temperature T, acceptance min(1, p(x)/q(x)), stop at the first
+ *       rejection, corrected token from relu(p - q) normalised, bonus token from
+ *       the last row when every draft token is accepted).
+ *  [P2] trefon.com, "Decode is memory-bound: a ~59 tok/s ceiling on an RTX 4090
+ *       and how speculative decoding breaks it" -- section "Speculative
+ *       decoding" (accept x with probability min(1, p(x)/q(x)); the output law
+ *       equals the target's; expected tokens per pass (1 - a^(k+1))/(1 - a) and
+ *       its table) and section "Two things that follow from the math"
+ *       (expected acceptance = sum_x min(p(x), q(x))).
+ *  [P3] agentnet.co.il, "New technical post reveals how speculative decoding
+ *       speeds up LLM inference without hurting accuracy" -- section "How it
+ *       works in practice" (draft length D; acceptance length AL in [1, 1 + D]).
+ */
+#ifndef SV_ORACLE_H
+#define SV_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Per-sequence status codes (the numbers the product library also reports). */
+#define ORACLE_OK 0
+#define ORACLE_TOKEN_RANGE 4   /* a draft token outside [0, V)                       */
+#define ORACLE_NONFINITE 5     /* NaN / +inf / all -inf target row, or bad q value    */
+#define ORACLE_UNIFORM_RANGE 7 /* a uniform outside [0, 1) or NaN                     */
+
+/* Softmax of one target row at temperature T, in double precision.
+ *   row: V stored logits (dtype 0 = float32, 1 = bfloat16 bit patterns).
+ *   p: out, V probabilities.  m_out = max_v row[v]/T, s_out = sum_v exp(row[v]/T - m).
+ * Returns ORACLE_OK, or ORACLE_NONFINITE when a value is NaN, a value is +inf,
+ * or every value is -inf (p is then left unspecified). */
+int oracle_softmax_row(const void* row, int dtype, int64_t V, double T,
+                       double* p, double* m_out, double* s_out);
+
+/* Batched verification, sequence by sequence, in the order the pages give.
+ *
+ * Inputs (host, row-major, V innermost):
+ *   logits   [B, K+1, V]  float32 or bf16 bits (dtype 0 / 1); row i is the
+ *                         target's distribution at draft position i, row K the
+ *                         bonus row
+ *   q        [B, K, V]    float32 draft probabilities, used as given
+ *   tokens   [B, K]       int32 draft tokens
+ *   uniforms [B, K+1]     float32; u[b,i] drives the test at position i and
+ *                         u[b,K] the single corrected-or-bonus sample
+ * Outputs (any of the optional ones may be NULL):
+ *   accept_len [B]        accepted drafts + 1, in [1, K+1]; 0 on a sequence error
+ *   out_tokens [B, K+1]   accepted prefix, then the sampled token, then -1
+ *   accept_mask [B, K]    1 for accepted positions, else 0
+ *   status [B]            ORACLE_* code of the sequence
+ *   row_m, row_s [B, K+1] softmax max and normaliser of the rows the loop
+ *                         reached; NaN for rows it never reached (optional)
+ *   p_draft [B, K]        p_i(x_i) for the tests that ran; NaN otherwise (optional)
+ *   accept_margin [B]     min over the tests that ran of |u_i - p/q| (inf when
+ *                         none ran or q(x) = 0) (optional)
+ *   sample_margin [B]     distance of u[b,K] to the nearer normalised CDF
+ *                         boundary around the sampled token, counting only
+ *                         boundaries that have a positive-weight token on the
+ *                         far side (inf when neither does) (optional)
+ *   sample_alt [B]        the positive-weight token across that nearer
+ *                         boundary, or -1 (optional)
+ */
+int oracle_verify(const void* logits, int dtype, const float* q, const int32_t* tokens,
+                  const float* uniforms, int64_t B, int K, int64_t V, float temperature,
+                  int32_t* accept_len, int32_t* out_tokens, uint8_t* accept_mask,
+                  int32_t* status, double* row_m, double* row_s, double* p_draft,
+                  double* accept_margin, double* sample_margin, int32_t* sample_alt);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

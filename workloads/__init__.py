@@ -1,0 +1,289 @@
+"""Seeded synthetic inputs for batched draft verification.
+
+This module serves both sides of every parity check: the CUDA library and the
+fp64 oracle read the very same arrays.  It draws random numbers and builds the
+*inputs* of the verify step (target logits, draft distributions, draft tokens,
+uniforms).  It holds none of the verification arithmetic: no acceptance test,
+no residual distribution, no inverse-CDF sampling of the corrected or bonus
+token.  The draft side (``q = softmax(draft_logits / T)`` and ``x ~ q``) is part
+of producing inputs, exactly as the draft model produces them before the target
+verifies (see the pages' draft loop in "Speculative decoding: draft first, then
+verify").
+
+Random streams: every draw uses ``numpy.random.Generator(Philox(seed).jumped(k))``
+with one ``k`` per field (0 target, 1 draft noise, 2 boost positions / mixture
+rows, 3 draft tokens, 4 uniforms).  Uniforms are float32 in [0, 1).
+
+bf16 logits are produced by rounding the fp64 draw to fp32 (round to nearest
+even) and then to bf16 (round to nearest even).  Both sides read the rounded
+values; the oracle upcasts them exactly.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional
+
+import numpy as np
+
+__all__ = [
+    "Inputs", "SweepCell", "CONFIGS", "SWEEP_ALPHAS", "SWEEP_KS",
+    "make_config", "make_random", "make_sweep_cell", "sample_tokens",
+    "softmax64", "f32_to_bf16_bits", "bf16_bits_to_f32", "logits_as_f64",
+    "draft_from_target", "uniforms",
+]
+
+
+# ----------------------------------------------------------------------------
+# dtype helpers
+# ----------------------------------------------------------------------------
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to bfloat16 (nearest, ties to even); return uint16 bits."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    bits = x.view(np.uint32).astype(np.uint64)
+    rounded = (bits + 0x7FFF + ((bits >> 16) & 1)) >> 16
+    out = rounded.astype(np.uint16)
+    nan = np.isnan(x)
+    if nan.any():
+        out[nan] = 0x7FC0
+    return out
+
+
+def bf16_bits_to_f32(h: np.ndarray) -> np.ndarray:
+    """Exact widening of bfloat16 bit patterns to float32."""
+    h = np.ascontiguousarray(h, dtype=np.uint16)
+    return (h.astype(np.uint32) << 16).view(np.float32)
+
+
+def logits_as_f64(logits: np.ndarray, dtype: str) -> np.ndarray:
+    """The stored logits as exact float64 values."""
+    if dtype == "bf16":
+        return bf16_bits_to_f32(logits).astype(np.float64)
+    return np.asarray(logits, dtype=np.float32).astype(np.float64)
+
+
+def _cast(x64: np.ndarray, dtype: str) -> np.ndarray:
+    x32 = x64.astype(np.float32)
+    return f32_to_bf16_bits(x32) if dtype == "bf16" else x32
+
+
+def softmax64(z: np.ndarray) -> np.ndarray:
+    """Row-wise softmax in float64, used to build draft distributions."""
+    z = np.asarray(z, dtype=np.float64)
+    m = np.max(z, axis=-1, keepdims=True)
+    e = np.exp(z - m)
+    return e / np.sum(e, axis=-1, keepdims=True)
+
+
+def _rng(seed: int, k: int) -> np.random.Generator:
+    return np.random.Generator(np.random.Philox(seed).jumped(k))
+
+
+# ----------------------------------------------------------------------------
+# the input bundle
+# ----------------------------------------------------------------------------
+
+@dataclasses.dataclass
+class Inputs:
+    """One verify call's inputs, host-resident.
+
+    logits   [B, K+1, V]  float32, or uint16 bf16 bit patterns when dtype == "bf16"
+    q        [B, K, V]    float32 draft probabilities
+    tokens   [B, K]       int32 draft tokens
+    uniforms [B, K+1]     float32 in [0, 1): u[b, i] for the test at position i,
+                          u[b, K] for the one corrected-or-bonus sample
+    """
+    name: str
+    B: int
+    K: int
+    V: int
+    dtype: str
+    T: float
+    logits: np.ndarray
+    q: np.ndarray
+    tokens: np.ndarray
+    uniforms: np.ndarray
+
+    @property
+    def logit_bytes(self) -> int:
+        return 2 if self.dtype == "bf16" else 4
+
+    def nominal_bytes(self) -> int:
+        """Logits + all of q + tokens + uniforms + outputs, read/written once."""
+        B, K, V = self.B, self.K, self.V
+        return (B * (K + 1) * V * self.logit_bytes + B * K * V * 4 + B * K * 4
+                + B * (K + 1) * 4 + B * 4 + B * (K + 1) * 4 + B * K)
+
+
+# ----------------------------------------------------------------------------
+# the five workloads of the verify step
+# ----------------------------------------------------------------------------
+
+@dataclasses.dataclass(frozen=True)
+class Config:
+    name: str
+    B: int
+    K: int
+    V: int
+    dtype: str
+    T: float
+    sigma: float           # target logits ~ N(0, sigma^2)
+    sigma_draft: float     # draft logits = target + N(0, sigma_draft^2)
+    boost_frac: float = 0.0
+    boost: float = 0.0
+    zipf_s: float = 0.0    # additive bias -s * ln(v + 1) over token ids
+    seed: int = 0
+
+
+CONFIGS = {
+    "b1_k4_v32000_f32": Config("b1_k4_v32000_f32", 1, 4, 32000, "f32", 1.0, 2.0, 1.0, seed=0),
+    "b8_k4_v32000_bf16_peaked": Config("b8_k4_v32000_bf16_peaked", 8, 4, 32000, "bf16", 0.6,
+                                       3.0, 0.5, boost_frac=0.01, boost=8.0, seed=1),
+    "b64_k3_v151936_bf16": Config("b64_k3_v151936_bf16", 64, 3, 151936, "bf16", 0.6, 2.5, 0.8,
+                                  seed=2),
+    "b256_k7_v128256_bf16_zipf": Config("b256_k7_v128256_bf16_zipf", 256, 7, 128256, "bf16", 1.0,
+                                        2.0, 0.7, zipf_s=1.1, seed=3),
+}
+CONFIG_ORDER = list(CONFIGS)
+SWEEP_ALPHAS = (0.35, 0.5, 0.6, 0.7, 0.8, 0.9)
+SWEEP_KS = (1, 3, 5)
+
+
+def sample_tokens(q_rows: np.ndarray, r: np.ndarray) -> np.ndarray:
+    """Draft tokens x ~ q by inverse CDF: first v whose running sum exceeds r * total.
+
+    q_rows [..., V] float32; r [..., n] float64 in [0, 1) -> int32 [..., n].
+    This is the draft model's own sampler, part of producing the inputs.
+    """
+    q_rows = np.asarray(q_rows)
+    lead = q_rows.shape[:-1]
+    V = q_rows.shape[-1]
+    qf = q_rows.reshape(-1, V)
+    rf = np.asarray(r, dtype=np.float64).reshape(qf.shape[0], -1)
+    out = np.empty(rf.shape, dtype=np.int32)
+    for row in range(qf.shape[0]):
+        cum = np.cumsum(qf[row].astype(np.float64))
+        idx = np.searchsorted(cum, rf[row] * cum[-1], side="right")
+        out[row] = np.minimum(idx, V - 1)
+    return out.reshape(lead + (rf.shape[1],))
+
+
+def draft_from_target(target_f64: np.ndarray, sigma_draft: float, T: float,
+                      rng: np.random.Generator) -> np.ndarray:
+    """q = softmax((target + N(0, sigma_draft^2)) / T), computed in fp64, rounded to fp32."""
+    d = target_f64 + sigma_draft * rng.standard_normal(target_f64.shape)
+    return softmax64(d / T).astype(np.float32)
+
+
+def uniforms(seed: int, B: int, K: int) -> np.ndarray:
+    return _rng(seed, 4).random((B, K + 1), dtype=np.float32)
+
+
+def make_config(name: str, seed: Optional[int] = None, B: Optional[int] = None) -> Inputs:
+    """Build one of the named workloads.  ``seed`` overrides the config's seed;
+    ``B`` builds only the first B sequences (same streams, a prefix of the batch)."""
+    cfg = CONFIGS[name]
+    seed = cfg.seed if seed is None else seed
+    B_full = cfg.B
+    B = B_full if B is None else min(B, B_full)
+    K, V, T = cfg.K, cfg.V, cfg.T
+    rt, rn, rb, rx = _rng(seed, 0), _rng(seed, 1), _rng(seed, 2), _rng(seed, 3)
+    # the first workload takes its uniforms from Philox seed 0 itself
+    ru = np.random.Generator(np.random.Philox(0)) if name == "b1_k4_v32000_f32" and seed == 0 \
+        else _rng(seed, 4)
+
+    store_dtype = np.uint16 if cfg.dtype == "bf16" else np.float32
+    logits = np.empty((B, K + 1, V), dtype=store_dtype)
+    q = np.empty((B, K, V), dtype=np.float32)
+    tokens = np.empty((B, K), dtype=np.int32)
+    bias = None
+    if cfg.zipf_s:
+        bias = -cfg.zipf_s * np.log(np.arange(V, dtype=np.float64) + 1.0)
+    n_boost = int(np.floor(cfg.boost_frac * V))
+    for b in range(B):
+        t = cfg.sigma * rt.standard_normal((K + 1, V))
+        if n_boost:
+            for i in range(K + 1):
+                t[i, rb.choice(V, size=n_boost, replace=False)] += cfg.boost
+        if bias is not None:
+            t += bias
+        logits[b] = _cast(t, cfg.dtype)
+        up = logits_as_f64(logits[b, :K], cfg.dtype)
+        if K:
+            q[b] = draft_from_target(up, cfg.sigma_draft, T, rn)
+            tokens[b] = sample_tokens(q[b], rx.random((K, 1)))[:, 0]
+    u = ru.random((B_full, K + 1), dtype=np.float32)[:B]
+    return Inputs(name, B, K, V, cfg.dtype, T, logits, q, tokens, np.ascontiguousarray(u))
+
+
+def make_random(B: int, K: int, V: int, dtype: str = "f32", T: float = 1.0, sigma: float = 2.0,
+                sigma_draft: float = 1.0, seed: int = 0, name: str = "random") -> Inputs:
+    """Small random instance with the value distribution of the first workload."""
+    rt, rn, rx, ru = _rng(seed, 0), _rng(seed, 1), _rng(seed, 3), _rng(seed, 4)
+    t = sigma * rt.standard_normal((B, K + 1, V))
+    logits = _cast(t, dtype)
+    up = logits_as_f64(logits, dtype)
+    q = draft_from_target(up[:, :K], sigma_draft, T, rn) if K else np.zeros((B, 0, V), np.float32)
+    tokens = sample_tokens(q, rx.random((B, K, 1)))[..., 0] if K else np.zeros((B, 0), np.int32)
+    u = ru.random((B, K + 1), dtype=np.float32)
+    return Inputs(name, B, K, V, dtype, T, np.ascontiguousarray(logits), np.ascontiguousarray(q),
+                  np.ascontiguousarray(tokens.astype(np.int32)), u)
+
+
+# ----------------------------------------------------------------------------
+# acceptance sweep: draft rows with a controlled overlap alpha = sum_v min(p, q)
+# ----------------------------------------------------------------------------
+
+@dataclasses.dataclass
+class SweepCell:
+    """Fixed target logits and draft rows for one (alpha, K) cell, plus `rounds`
+    fresh draws of draft tokens and uniforms.
+
+    logits [B, K+1, V] f32, q [B, K, V] f32, tokens [R, B, K], uniforms [R, B, K+1].
+    """
+    alpha: float
+    B: int
+    K: int
+    V: int
+    T: float
+    logits: np.ndarray
+    q: np.ndarray
+    tokens: np.ndarray
+    uniforms: np.ndarray
+
+    def round_inputs(self, r: int) -> Inputs:
+        return Inputs(f"sweep_a{self.alpha}_k{self.K}_r{r}", self.B, self.K, self.V, "f32", self.T,
+                      self.logits, self.q, np.ascontiguousarray(self.tokens[r]),
+                      np.ascontiguousarray(self.uniforms[r]))
+
+
+def make_sweep_cell(alpha: float, K: int, B: int = 32, V: int = 32000, rounds: int = 10 ** 4,
+                    seed: int = 4, sigma: float = 2.0, dirichlet: float = 0.1) -> SweepCell:
+    """Target rows softmax(N(0, sigma^2)) at T = 1; each draft row is the mixture
+    (1 - w) p + w r with r ~ Dirichlet(dirichlet) and w = (1 - alpha) / TV(p, r),
+    so that sum_v min(p, q) = 1 - w * TV(p, r) = alpha (r is redrawn while
+    TV(p, r) < 1 - alpha).  Draft tokens and uniforms are fresh in every round."""
+    cell_seed = seed * 1000 + int(round(alpha * 100)) * 10 + K
+    rt, rm, rx, ru = _rng(cell_seed, 0), _rng(cell_seed, 2), _rng(cell_seed, 3), _rng(cell_seed, 4)
+    logits = (sigma * rt.standard_normal((B, K + 1, V))).astype(np.float32)
+    p = softmax64(logits.astype(np.float64))
+    q = np.empty((B, K, V), dtype=np.float32)
+    for b in range(B):
+        for i in range(K):
+            while True:
+                g = rm.standard_gamma(dirichlet, V)
+                s = g.sum()
+                if s <= 0:
+                    continue
+                r = g / s
+                tv = np.maximum(p[b, i] - r, 0.0).sum()
+                if tv >= 1.0 - alpha:
+                    break
+            w = (1.0 - alpha) / tv
+            q[b, i] = ((1.0 - w) * p[b, i] + w * r).astype(np.float32)
+    tokens = np.empty((rounds, B, K), dtype=np.int32)
+    if K:
+        draws = rx.random((B, K, rounds))
+        tokens[:] = np.moveaxis(sample_tokens(q, draws), -1, 0)
+    u = ru.random((rounds, B, K + 1), dtype=np.float32)
+    return SweepCell(alpha, B, K, V, 1.0, logits, q, tokens, u)
