@@ -1,0 +1,413 @@
+#!/usr/bin/env python
+"""Benchmark of the batched draft-verification step on GB300.
+
+One step = one spec_verify_run call over one batch of the workload (the whole
+hot path: row softmax statistics, accept tests, first-rejection scan, residual
+or bonus draw).  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Metric: verified rows/s, rows = B*(K+1) per step, with inputs resident in HBM
+(value), plus tokens/s, algorithmic HBM GB/s and its fraction of the measured
+copy bandwidth (roofline), the fp64 CPU oracle on a bounded sample
+(cpu_baseline), and the same metric through the host-buffer entry point with
+the copies inside the timed region (e2e).  Several copies of the inputs are
+rotated so that no step finds the previous step's data in L2 (each copy is
+larger than L2).  Under torchrun every rank verifies its own batch (weak
+scaling, no collective besides the timing barrier and max).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "verified rows/s and HBM GB/s (% of GB300 peak) for B×(K+1)×V verify"
+DEFAULT_WORKLOAD = "b256_k7_v128256_bf16_zipf"
+L2_BYTES = 129 * 1024 * 1024
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=workloads.CONFIG_ORDER)
+    ap.add_argument("--sets", type=int, default=3, help="input copies rotated between steps")
+    ap.add_argument("--e2e-steps", type=int, default=8)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--clock-window", type=float, default=2.0,
+                    help="seconds of untimed load, sampled for clocks, before the timed steps")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def profile_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary, if it covers this
+    workload and the current kernel (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d.get(workload)
+        return float(e["dram_bytes_per_launch"]) if e else None
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------ byte counts -----
+
+def algorithmic_bytes(inp, accept_len: np.ndarray) -> int:
+    """Bytes the method must move for one verify, from its outputs.
+
+    Per sequence b with accepted length n = accept_len[b] (rows 0..n-1 reached):
+      n rows of logits (V * sizeof(logit) each)             -- the test loop reads
+                                                               rows in order and
+                                                               stops at the first
+                                                               rejection
+      + V * 4 for the draft row q_j when a draft was rejected (n <= K)
+      + 4 per test that ran (q(x_i) gathered), min(n, K) tests
+      + K * 4 (draft tokens) + (K + 1) * 4 (uniforms)
+      + outputs: 4 + (K + 1) * 4 + K
+    The logits of row j are re-used for the draw from shared memory, not re-read.
+    """
+    B, K, V, es = inp.B, inp.K, inp.V, inp.logit_bytes
+    n = accept_len.astype(np.int64)
+    rows = int(n.sum())
+    rejected = int((n <= K).sum())
+    tests = int(np.minimum(n, K).sum())
+    return (rows * V * es + rejected * V * 4 + tests * 4 + B * K * 4 + B * (K + 1) * 4
+            + B * (4 + (K + 1) * 4 + K))
+
+
+# ---------------------------------------------------------------- clocks -----
+
+class ClockSampler:
+    def __init__(self, device: int):
+        self.device = device
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            self.fh = os.fdopen(fd, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.device)], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# -------------------------------------------------------------- our arm -----
+
+def run_ours(args):
+    import torch
+    import speculative_decoding_verification_14_gb300 as sv
+
+    world, rank, local = dist_env()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.cuda.current_device()
+
+    cfg = workloads.CONFIGS[args.workload]
+    inp = workloads.make_config(args.workload, seed=cfg.seed + rank)
+    B, K, V, T = inp.B, inp.K, inp.V, inp.T
+    dcode = sv.SV_BF16 if inp.dtype == "bf16" else sv.SV_F32
+    per_set = inp.nominal_bytes()
+    nsets = max(1, args.sets)
+
+    def dev_logits():
+        if inp.dtype == "bf16":
+            return torch.from_numpy(inp.logits.view(np.int16)).cuda().view(torch.bfloat16)
+        return torch.from_numpy(inp.logits).cuda()
+
+    sets = []
+    for s in range(nsets):
+        sets.append((dev_logits(), torch.from_numpy(inp.q).cuda(), torch.from_numpy(inp.tokens).cuda(),
+                     torch.from_numpy(inp.uniforms).cuda()))
+    outs = {"accept_len": torch.empty(B, dtype=torch.int32, device="cuda"),
+            "out_tokens": torch.empty(B, K + 1, dtype=torch.int32, device="cuda"),
+            "accept_mask": torch.empty(B, K, dtype=torch.uint8, device="cuda")}
+    verifier = sv.Verifier(B, K, V)
+    stream = torch.cuda.current_stream()
+    lib = sv.library()
+    calls = []
+    for (lg, q, x, u) in sets:
+        calls.append((verifier.ctx, lg.data_ptr(), dcode, q.data_ptr(), x.data_ptr(), u.data_ptr(),
+                      B, K, V, ctypes.c_float(T), outs["accept_len"].data_ptr(),
+                      outs["out_tokens"].data_ptr(), outs["accept_mask"].data_ptr(), None, None,
+                      None, stream.cuda_stream))
+    run = lib.spec_verify_run
+
+    def step(k):
+        rc = run(*calls[k % nsets])
+        if rc != 0:
+            raise sv.SpecVerifyError(rc, "spec_verify_run")
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    # warm-up, then an untimed sampled window for the clock record
+    for k in range(args.warmup):
+        step(k)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev)
+    clocks.start()
+    t_end = time.time() + args.clock_window
+    k = 0
+    while time.time() < t_end:
+        for _ in range(64):
+            step(k)
+            k += 1
+        torch.cuda.synchronize()
+
+    # timed region: K steps, an event pair around every launch on its stream
+    barrier()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(args.steps):
+        ev[k][0].record(stream)
+        step(k)
+        ev[k][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    total_ms = t0.elapsed_time(t1)
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    if dist is not None:
+        tt = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+
+    err, _ = verifier.error()
+    if err != sv.SV_OK:
+        raise sv.SpecVerifyError(err, "device error during the benchmark")
+    acc = outs["accept_len"].cpu().numpy()
+    alg = algorithmic_bytes(inp, acc)
+    avg_launch_s = statistics.mean(launch_ms) / 1e3
+    rows_per_step = B * (K + 1)
+    value = world * rows_per_step * args.steps / (total_ms / 1e3)
+    tokens_per_step = int(acc.sum())
+    peak, peak_kind = measured_peak()
+    achieved = alg / avg_launch_s / 1e9
+    plan = verifier.plan(B, K, V, dcode)
+
+    # end to end through the host-buffer entry point, copies inside the region
+    e2e = None
+    if not args.no_e2e and args.e2e_steps > 0:
+        def pinned(a):
+            t = torch.empty(a.shape, dtype={np.float32: torch.float32, np.uint16: torch.int16,
+                                            np.int32: torch.int32, np.uint8: torch.uint8}[a.dtype.type],
+                            pin_memory=True)
+            arr = t.numpy()
+            arr[...] = a.view(arr.dtype) if a.dtype != arr.dtype else a
+            return t, arr
+        keep = []
+        h = {}
+        for name, a in (("logits", inp.logits), ("q", inp.q), ("tokens", inp.tokens),
+                        ("uniforms", inp.uniforms)):
+            t, arr = pinned(a)
+            keep.append(t)
+            h[name] = arr
+        hout = {}
+        for name, shape, dt in (("accept_len", (B,), np.int32), ("out_tokens", (B, K + 1), np.int32),
+                                ("accept_mask", (B, K), np.uint8)):
+            t, arr = pinned(np.zeros(shape, dt))
+            keep.append(t)
+            hout[name] = arr
+        rc = verifier.run_host(h["logits"], dcode, h["q"], h["tokens"], h["uniforms"], T, hout,
+                               stream=stream.cuda_stream)  # first call allocates staging
+        assert rc == sv.SV_OK, sv.spec_verify_strerror(rc)
+        barrier()
+        ts = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            rc = verifier.run_host(h["logits"], dcode, h["q"], h["tokens"], h["uniforms"], T, hout,
+                                   stream=stream.cuda_stream)
+            assert rc == sv.SV_OK
+        el = time.perf_counter() - ts
+        if dist is not None:
+            tt = torch.tensor([el], device="cuda", dtype=torch.float64)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            el = float(tt.item())
+        assert np.array_equal(hout["accept_len"], acc)
+        h2d = inp.logits.nbytes + inp.q.nbytes + inp.tokens.nbytes + inp.uniforms.nbytes
+        d2h = hout["accept_len"].nbytes + hout["out_tokens"].nbytes + hout["accept_mask"].nbytes + 4
+        e2e = {"value": world * rows_per_step * args.e2e_steps / el, "unit": "rows/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "steps": args.e2e_steps, "api": "spec_verify_run_host (pinned host buffers)"}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(inp, args.cpu_seconds)
+
+    if rank != 0:
+        return None
+    line = {
+        "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "B": B, "K": K, "V": V, "logits_dtype": inp.dtype,
+                   "T": T, "l2": f"{nsets} input copies of {per_set / 1e9:.2f} GB rotated "
+                                 f"(each larger than the {L2_BYTES >> 20} MB L2)",
+                   "plan": plan},
+        "tokens_per_s": world * tokens_per_step * args.steps / (total_ms / 1e3),
+        "mean_accept_len": float(acc.mean()),
+        "hbm_gbs_algorithmic": achieved,
+        "hbm_gbs_nominal": inp.nominal_bytes() / avg_launch_s / 1e9,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": profile_traffic(args.workload),
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind ==
+                     "measured" else "fallback 6.8 TB/s",
+                     "algorithmic_bytes_per_launch": alg, "avg_launch_us": avg_launch_s * 1e6},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+    return line
+
+
+def cpu_baseline(inp, seconds: float) -> dict:
+    """The fp64 oracle as it stands, single thread, on whole passes over the
+    workload's sequences until `seconds` of CPU work have accumulated."""
+    import oracle
+    oracle.build()
+    # one sequence first, to size the sample
+    t = time.perf_counter()
+    oracle.verify(inp.logits[:1], inp.dtype, inp.q[:1], inp.tokens[:1], inp.uniforms[:1], inp.T)
+    per_seq = max(time.perf_counter() - t, 1e-6)
+    n = int(min(inp.B, max(1, seconds / per_seq)))
+    reps = max(1, int(seconds / (per_seq * n)))
+    t = time.perf_counter()
+    for _ in range(reps):
+        oracle.verify(inp.logits[:n], inp.dtype, inp.q[:n], inp.tokens[:n], inp.uniforms[:n], inp.T)
+    el = time.perf_counter() - t
+    return {"value": reps * n * (inp.K + 1) / el, "unit": "rows/s", "cores": 1, "kind": "oracle",
+            "sample": f"{reps} pass(es) over the first {n} of {inp.B} sequences ({el:.1f} s)"}
+
+
+# -------------------------------------------------------- reference arm -----
+
+def run_reference(args):
+    """The oracle (fp64 CPU) timed as the reference arm on a bounded sample of
+    the same workload per step."""
+    world, rank, local = dist_env()
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    inp = workloads.make_config(args.workload)
+    t = time.perf_counter()
+    oracle.verify(inp.logits[:1], inp.dtype, inp.q[:1], inp.tokens[:1], inp.uniforms[:1], inp.T)
+    per_seq = max(time.perf_counter() - t, 1e-6)
+    budget = 120.0 / max(1, args.steps + args.warmup)   # whole run within ~2 minutes
+    n = int(min(inp.B, max(1, budget / per_seq)))
+    sl = slice(0, n)
+    for _ in range(args.warmup):
+        oracle.verify(inp.logits[sl], inp.dtype, inp.q[sl], inp.tokens[sl], inp.uniforms[sl], inp.T)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.verify(inp.logits[sl], inp.dtype, inp.q[sl], inp.tokens[sl], inp.uniforms[sl], inp.T)
+    el = time.perf_counter() - t
+    value = args.steps * n * (inp.K + 1) / el
+    sample = f"first {n} of {inp.B} sequences per step"
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": args.workload, "B": inp.B, "K": inp.K,
+                                            "V": inp.V, "logits_dtype": inp.dtype, "T": inp.T},
+            "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def main():
+    args = parse_args()
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

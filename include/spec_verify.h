@@ -1,0 +1,164 @@
+/*
+ * spec_verify.h -- C ABI of a GB300 (sm_103a) library for the batched
+ * draft-verification step of speculative decoding.
+ *
+ * The operation (sources are web pages, cited by title and section):
+ *  [P1] reactapp.top, "Speculative decoding and early exit: speeding up
+ *       autoregressive decode", section "Speculative decoding: draft first,
+ *       then verify": the target scores the K drafted positions plus one more
+ *       in a single pass; each target row becomes p = softmax(logits / T);
+ *       positions are tested in order and the first rejection ends the pass;
+ *       a rejection is replaced by a token drawn from relu(p - q) normalised;
+ *       when all K drafts pass, one bonus token is drawn from the last row.
+ *  [P2] trefon.com, "Decode is memory-bound: a ~59 tok/s ceiling on an RTX
+ *       4090 and how speculative decoding breaks it", section "Speculative
+ *       decoding": draft token x is kept with probability min(1, p(x)/q(x)),
+ *       which makes the output follow the target distribution exactly.
+ *  [P3] agentnet.co.il, "New technical post reveals how speculative decoding
+ *       speeds up LLM inference without hurting accuracy", section "How it
+ *       works in practice": with D drafts the accepted length AL is in
+ *       [1, 1 + D].
+ *
+ * Conventions shared by every entry point:
+ *  - Arrays are row-major and dense with the vocabulary (V) innermost.
+ *  - logits [B, K+1, V]: row i < K scores draft position i, row K is the bonus
+ *    row.  dtype SV_F32 (float) or SV_BF16 (bfloat16 bit patterns).
+ *  - q [B, K, V] float: the draft's probabilities, already at the draft's
+ *    temperature; used as given (not renormalised).
+ *  - draft_tokens [B, K] int32.
+ *  - uniforms [B, K+1] float in [0, 1): u[b, i] drives the test at position i
+ *    (accept iff u * q(x) < p(x), i.e. u < min(1, p/q)); u[b, K] drives the
+ *    one corrected-or-bonus draw, an inverse-CDF draw over token ids in
+ *    ascending order (the first token whose running weight exceeds u * S).
+ *    Uniforms are inputs so that results are reproducible and testable.
+ *  - Outputs: accept_len [B] int32 = accepted drafts + 1 in [1, K+1] (0 marks
+ *    a sequence error); out_tokens [B, K+1] int32 = accepted drafts, then the
+ *    drawn token, then -1; accept_mask [B, K] uint8 = 1 on accepted positions.
+ *  - Optional outputs (pass NULL to skip): row_stats [B, K+1, 2] float =
+ *    (max_v logits/T, sum_v exp(logits/T - max)) for every row the pass
+ *    reached, NaN for rows it never needed; p_draft [B, K] float = p_i(x_i)
+ *    for the tests that ran, NaN otherwise; status [B] int32 = SV_* code of
+ *    each sequence.
+ *  - Rows after the first rejection are never read: the test loop of [P1]
+ *    stops there, and so does the kernel.
+ *  - Shapes: 1 <= B, 0 <= K <= 32 (K = 0 draws one token from row 0),
+ *    1 <= V, B*(K+1)*V < 2^40.  Every pointer must be aligned to its element
+ *    size.  16-byte aligned logits with V*sizeof(element) a multiple of 16 take
+ *    the bulk-copy path; other layouts take a slower element-wise path.
+ *
+ * Ownership and threading: the caller owns every array.  A context owns only
+ * its own small device state (an error word) and, after the first host-buffer
+ * call, staging buffers sized to the context's maxima.  spec_verify_run
+ * allocates nothing and never synchronises.  One context serves one stream at
+ * a time; calls on one context from several host threads must be serialised
+ * by the caller.
+ *
+ * Errors: host-detectable problems return at once and launch nothing.  Errors
+ * found on the device (a draft token outside [0, V), a uniform outside [0, 1),
+ * a NaN / +inf / all -inf target row that the pass reaches, a NaN, infinite or
+ * negative q value that the pass reads) mark only that sequence (accept_len 0,
+ * out_tokens -1, mask 0, stats NaN, status code) and set a bit in the
+ * context's sticky error word, read with spec_verify_get_error.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
+
+typedef enum {
+    SV_OK = 0,
+    SV_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad shape, T <= 0 or not finite   */
+    SV_ERR_UNSUPPORTED = 2,   /* shape beyond what one launch plan can hold                  */
+    SV_ERR_CUDA = 3,          /* a CUDA runtime call failed                                   */
+    SV_ERR_TOKEN_RANGE = 4,   /* device: a draft token outside [0, V)                         */
+    SV_ERR_NONFINITE = 5,     /* device: NaN/+inf/all -inf logits row, or NaN/inf/negative q  */
+    SV_ERR_TIMEOUT = 6,       /* device: a bounded wait for a bulk copy ran out               */
+    SV_ERR_UNIFORM_RANGE = 7  /* device: a uniform outside [0, 1)                             */
+} sv_status;
+
+/* Opaque context: device id, limits, launch-plan cache, error word. */
+typedef struct sv_ctx sv_ctx;
+
+/* Launch plan the library picks for a shape (reported for tests and tuning). */
+typedef struct {
+    int cluster;       /* CTAs per sequence, one thread-block cluster (1..16)          */
+    int group;         /* target rows a cluster loads before deciding (1..K+1)         */
+    int threads;       /* threads per CTA                                              */
+    int smem_bytes;    /* dynamic shared memory per CTA                                */
+    int64_t slice;     /* vocabulary entries per CTA (a multiple of 8)                 */
+    int64_t grid;      /* CTAs in the launch = B * cluster                             */
+    int bulk_copy;     /* 1: row slices move with cp.async.bulk; 0: element-wise loads */
+} sv_plan;
+
+/* Create a context on `device` for calls with B <= max_B, K <= max_K (<= 32)
+ * and V <= max_V.  Queries the device, sets kernel attributes, allocates the
+ * 4-byte device error word.  *out is set only on success.
+ * Returns SV_OK, SV_ERR_INVALID_ARG or SV_ERR_CUDA (no usable device). */
+int spec_verify_init(sv_ctx** out, int device, int max_B, int max_K, int64_t max_V);
+
+/* One batched verify on `stream` (a cudaStream_t; NULL = legacy default
+ * stream), device pointers throughout, asynchronous.  Layouts, meaning and
+ * error behaviour as described at the top of this file.  `stream` must belong
+ * to the context's device.  Safe to capture in a CUDA graph. */
+int spec_verify_run(sv_ctx* ctx,
+                    const void* target_logits, int logits_dtype,
+                    const float* q, const int32_t* draft_tokens, const float* uniforms,
+                    int B, int K, int64_t V, float temperature,
+                    int32_t* accept_len, int32_t* out_tokens, uint8_t* accept_mask,
+                    float* row_stats, float* p_draft, int32_t* status,
+                    void* stream);
+
+/* The same verify with HOST buffers for every array (pinned memory gives the
+ * fastest copies).  Copies the inputs to context-owned device staging buffers
+ * (allocated on the first call, sized to the context maxima, kept until
+ * destroy), runs, copies the outputs back and synchronises `stream` before
+ * returning.  Returns the launch status, or the lowest device error code seen
+ * by this call (the sticky error word is cleared). */
+int spec_verify_run_host(sv_ctx* ctx,
+                         const void* target_logits, int logits_dtype,
+                         const float* q, const int32_t* draft_tokens, const float* uniforms,
+                         int B, int K, int64_t V, float temperature,
+                         int32_t* accept_len, int32_t* out_tokens, uint8_t* accept_mask,
+                         float* row_stats, float* p_draft, int32_t* status,
+                         void* stream);
+
+/* Synchronise `stream`, read and clear the context's sticky device error
+ * word.  *mask (if not NULL) receives a bit (1 << code) per error kind seen
+ * since the last read.  Returns SV_OK or the lowest code present. */
+int spec_verify_get_error(sv_ctx* ctx, void* stream, uint32_t* mask);
+
+/* Launch plan for a shape on the context's device (no launch). */
+int spec_verify_get_plan(sv_ctx* ctx, int B, int K, int64_t V, int logits_dtype, sv_plan* out);
+
+/* Force parts of the plan (0 = automatic): cluster size 1..16, rows per group
+ * 1..K+1 (clamped), threads per CTA 128/256/512.  Used by tests to cover every
+ * plan and by tuning sweeps.  Returns SV_ERR_INVALID_ARG on values outside those sets. */
+int spec_verify_set_plan_override(sv_ctx* ctx, int cluster, int group, int threads);
+
+/* The planner as a pure host function of the device limits, for tests:
+ * num_sms, max dynamic shared memory per CTA, largest cluster the device
+ * allows, and the same overrides.  No CUDA call is made. */
+int spec_verify_plan_for(int num_sms, int smem_per_cta, int max_cluster,
+                         int B, int K, int64_t V, int logits_dtype,
+                         int ovr_cluster, int ovr_group, int ovr_threads, sv_plan* out);
+
+/* Release the context and everything it owns. */
+int spec_verify_destroy(sv_ctx* ctx);
+
+/* Static text for a status code. */
+const char* spec_verify_strerror(int code);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int spec_verify_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPEC_VERIFY_H */

@@ -10,9 +10,11 @@ of producing inputs, exactly as the draft model produces them before the target
 verifies (see the pages' draft loop in "Speculative decoding: draft first, then
 verify").
 
-Random streams: every draw uses ``numpy.random.Generator(Philox(seed).jumped(k))``
-with one ``k`` per field (0 target, 1 draft noise, 2 boost positions / mixture
-rows, 3 draft tokens, 4 uniforms).  Uniforms are float32 in [0, 1).
+Random streams: ``numpy.random.Generator(PCG64(SeedSequence(key)))`` with one key
+per field and sequence: [seed, k, b] for the named workloads (k = 0 target
+logits, 1 draft noise, 2 boost positions, 3 draft tokens; b the sequence) and
+[seed, 4] for the uniforms; the first workload takes its uniforms from
+``Philox(0)`` as its recipe states.  Uniforms are float32 in [0, 1).
 
 bf16 logits are produced by rounding the fp64 draw to fp32 (round to nearest
 even) and then to bf16 (round to nearest even).  Both sides read the rounded
@@ -21,6 +23,7 @@ values; the oracle upcasts them exactly.
 from __future__ import annotations
 
 import dataclasses
+import os
 from typing import Optional
 
 import numpy as np
@@ -40,9 +43,13 @@ __all__ = [
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """Round float32 values to bfloat16 (nearest, ties to even); return uint16 bits."""
     x = np.ascontiguousarray(x, dtype=np.float32)
-    bits = x.view(np.uint32).astype(np.uint64)
-    rounded = (bits + 0x7FFF + ((bits >> 16) & 1)) >> 16
-    out = rounded.astype(np.uint16)
+    bits = x.view(np.uint32)
+    # the largest finite or infinite pattern plus the rounding bias stays below 2^32
+    lsb = (bits >> 16) & np.uint32(1)
+    lsb += np.uint32(0x7FFF)
+    lsb += bits
+    lsb >>= 16
+    out = lsb.astype(np.uint16)
     nan = np.isnan(x)
     if nan.any():
         out[nan] = 0x7FC0
@@ -76,7 +83,11 @@ def softmax64(z: np.ndarray) -> np.ndarray:
 
 
 def _rng(seed: int, k: int) -> np.random.Generator:
-    return np.random.Generator(np.random.Philox(seed).jumped(k))
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, k])))
+
+
+def _rng3(seed: int, k: int, b: int) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, k, b])))
 
 
 # ----------------------------------------------------------------------------
@@ -179,28 +190,16 @@ def uniforms(seed: int, B: int, K: int) -> np.ndarray:
     return _rng(seed, 4).random((B, K + 1), dtype=np.float32)
 
 
-def make_config(name: str, seed: Optional[int] = None, B: Optional[int] = None) -> Inputs:
-    """Build one of the named workloads.  ``seed`` overrides the config's seed;
-    ``B`` builds only the first B sequences (same streams, a prefix of the batch)."""
+def _sequences_into(name: str, seed: int, b0: int, b1: int, logits, q, tokens):
+    """Fill logits, draft rows and draft tokens of sequences b0..b1-1 (arrays
+    indexed by sequence).  Every sequence has its own streams, so any split of
+    the batch gives the same arrays."""
     cfg = CONFIGS[name]
-    seed = cfg.seed if seed is None else seed
-    B_full = cfg.B
-    B = B_full if B is None else min(B, B_full)
     K, V, T = cfg.K, cfg.V, cfg.T
-    rt, rn, rb, rx = _rng(seed, 0), _rng(seed, 1), _rng(seed, 2), _rng(seed, 3)
-    # the first workload takes its uniforms from Philox seed 0 itself
-    ru = np.random.Generator(np.random.Philox(0)) if name == "b1_k4_v32000_f32" and seed == 0 \
-        else _rng(seed, 4)
-
-    store_dtype = np.uint16 if cfg.dtype == "bf16" else np.float32
-    logits = np.empty((B, K + 1, V), dtype=store_dtype)
-    q = np.empty((B, K, V), dtype=np.float32)
-    tokens = np.empty((B, K), dtype=np.int32)
-    bias = None
-    if cfg.zipf_s:
-        bias = -cfg.zipf_s * np.log(np.arange(V, dtype=np.float64) + 1.0)
+    bias = -cfg.zipf_s * np.log(np.arange(V, dtype=np.float64) + 1.0) if cfg.zipf_s else None
     n_boost = int(np.floor(cfg.boost_frac * V))
-    for b in range(B):
+    for b in range(b0, b1):
+        rt, rn, rb, rx = (_rng3(seed, k, b) for k in range(4))
         t = cfg.sigma * rt.standard_normal((K + 1, V))
         if n_boost:
             for i in range(K + 1):
@@ -208,10 +207,72 @@ def make_config(name: str, seed: Optional[int] = None, B: Optional[int] = None) 
         if bias is not None:
             t += bias
         logits[b] = _cast(t, cfg.dtype)
-        up = logits_as_f64(logits[b, :K], cfg.dtype)
         if K:
+            up = logits_as_f64(logits[b, :K], cfg.dtype)
             q[b] = draft_from_target(up, cfg.sigma_draft, T, rn)
             tokens[b] = sample_tokens(q[b], rx.random((K, 1)))[:, 0]
+
+
+def _worker(args):
+    from multiprocessing import shared_memory
+    name, seed, b0, b1, B, shm_names = args
+    cfg = CONFIGS[name]
+    shapes = _shapes(cfg, B)
+    blocks = [shared_memory.SharedMemory(name=n) for n in shm_names]
+    try:
+        arrs = [np.ndarray(shp, dtype=dt, buffer=blk.buf) for (shp, dt), blk in zip(shapes, blocks)]
+        _sequences_into(name, seed, b0, b1, *arrs)
+        del arrs
+    finally:
+        for blk in blocks:
+            blk.close()
+    return b1 - b0
+
+
+def _shapes(cfg, B):
+    store = np.uint16 if cfg.dtype == "bf16" else np.float32
+    return [((B, cfg.K + 1, cfg.V), store), ((B, cfg.K, cfg.V), np.float32), ((B, cfg.K), np.int32)]
+
+
+def make_config(name: str, seed: Optional[int] = None, B: Optional[int] = None,
+                workers: Optional[int] = None) -> Inputs:
+    """Build one of the named workloads.  ``seed`` overrides the config's seed;
+    ``B`` builds only the first B sequences (a prefix of the full batch).
+    Large batches are generated by a spawn-started process pool writing into
+    shared memory; the arrays do not depend on the number of workers."""
+    cfg = CONFIGS[name]
+    seed = cfg.seed if seed is None else seed
+    B_full = cfg.B
+    B = B_full if B is None else min(B, B_full)
+    K, V, T = cfg.K, cfg.V, cfg.T
+    shapes = _shapes(cfg, B)
+    if workers is None:
+        workers = min(16, os.cpu_count() or 1) if B * (2 * K + 1) * V > 50_000_000 else 1
+    if workers > 1 and B > 1:
+        import concurrent.futures
+        import multiprocessing
+        from multiprocessing import shared_memory
+        blocks = [shared_memory.SharedMemory(create=True, size=max(1, int(np.prod(shp)) * np.dtype(dt).itemsize))
+                  for shp, dt in shapes]
+        try:
+            step = -(-B // workers)
+            jobs = [(name, seed, lo, min(B, lo + step), B, [b.name for b in blocks])
+                    for lo in range(0, B, step)]
+            with concurrent.futures.ProcessPoolExecutor(
+                    max_workers=len(jobs), mp_context=multiprocessing.get_context("spawn")) as ex:
+                assert sum(ex.map(_worker, jobs)) == B
+            logits, q, tokens = (np.ndarray(shp, dtype=dt, buffer=blk.buf).copy()
+                                 for (shp, dt), blk in zip(shapes, blocks))
+        finally:
+            for blk in blocks:
+                blk.close()
+                blk.unlink()
+    else:
+        logits, q, tokens = (np.empty(shp, dtype=dt) for shp, dt in shapes)
+        _sequences_into(name, seed, 0, B, logits, q, tokens)
+    # the first workload takes its uniforms from Philox seed 0 itself
+    ru = np.random.Generator(np.random.Philox(0)) if name == "b1_k4_v32000_f32" and seed == 0 \
+        else _rng(seed, 4)
     u = ru.random((B_full, K + 1), dtype=np.float32)[:B]
     return Inputs(name, B, K, V, cfg.dtype, T, logits, q, tokens, np.ascontiguousarray(u))
 
