@@ -48,7 +48,7 @@
  *
  * Ownership and threading: the caller owns every array.  A context owns only
  * its own small device state (an error word) and, after the first host-buffer
- * call, staging buffers sized to the context's maxima.  spec_verify_run
+ * call, staging buffers sized to the largest host-buffer call so far.  spec_verify_run
  * allocates nothing and never synchronises.  One context serves one stream at
  * a time; calls on one context from several host threads must be serialised
  * by the caller.
@@ -117,10 +117,10 @@ int spec_verify_run(sv_ctx* ctx,
 
 /* The same verify with HOST buffers for every array (pinned memory gives the
  * fastest copies).  Copies the inputs to context-owned device staging buffers
- * (allocated on the first call, sized to the context maxima, kept until
- * destroy), runs, copies the outputs back and synchronises `stream` before
- * returning.  Returns the launch status, or the lowest device error code seen
- * by this call (the sticky error word is cleared). */
+ * (allocated by the first call, re-allocated only when a later call needs
+ * more, kept until destroy), runs, copies the outputs back and synchronises
+ * `stream` before returning.  Returns the launch status, or the lowest device
+ * error code seen by this call (the sticky error word is cleared). */
 int spec_verify_run_host(sv_ctx* ctx,
                          const void* target_logits, int logits_dtype,
                          const float* q, const int32_t* draft_tokens, const float* uniforms,

@@ -176,6 +176,13 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// l - m for the exponent d*c_hi + d*c_lo.  A -inf logit (or -inf padding)
+// would give d = -inf and, when c_lo < 0, -inf + inf = NaN; clamping d to a
+// finite floor keeps the product with c_lo finite while d*c_hi still
+// overflows to -inf, so the entry weighs exactly 0.  (NaN logits never reach
+// this point: the row max propagates them and the row is rejected first.)
+__device__ __forceinline__ float exp_arg_diff(float l, float m) { return fmaxf(l - m, -3.0e38f); }
+
 // max that returns NaN when either input is NaN (IEEE maxNum would drop it)
 __device__ __forceinline__ float fmax_nan(float a, float b) {
     float d;
@@ -303,7 +310,7 @@ __device__ float slice_sumexp(const unsigned char* buf, int nvec, float m, float
         Elem<ES>::unpack(reinterpret_cast<const uint4*>(buf)[vi], f);
 #pragma unroll
         for (int k = 0; k < E; k += 2) {
-            const float d0 = f[k] - m, d1 = f[k + 1] - m;
+            const float d0 = exp_arg_diff(f[k], m), d1 = exp_arg_diff(f[k + 1], m);
             s0 += ex2_approx(fmaf(d0, c_hi, d0 * c_lo));
             s1 += ex2_approx(fmaf(d1, c_hi, d1 * c_lo));
         }
@@ -369,7 +376,7 @@ __device__ __forceinline__ void vec_weights(const unsigned char* buf, int vi, in
     }
 #pragma unroll
     for (int k = 0; k < E; ++k) {
-        const float d = f[k] - M;
+        const float d = exp_arg_diff(f[k], M);
         const float e = ex2_approx(fmaf(d, c_hi, d * c_lo));
         float wk;
         if (mode == kModeResidual) {
@@ -1148,14 +1155,22 @@ int spec_verify_run_host(sv_ctx* ctx, const void* target_logits, int logits_dtyp
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const size_t es = logits_dtype == SV_BF16 ? 2 : 4;
     auto al = [](size_t n) { return (n + 255) & ~(size_t)255; };
-    // staging layout sized to the context maxima
-    const size_t mB = (size_t)ctx->max_B, mK = (size_t)ctx->max_K, mV = (size_t)ctx->max_V;
+    // staging layout sized to this call; a larger later call replaces it
+    const size_t mB = (size_t)B, mK = (size_t)K, mV = (size_t)V;
     const size_t cap_logits = al(mB * (mK + 1) * mV * 4), cap_q = al(mB * mK * mV * 4);
     const size_t cap_tok = al(mB * mK * 4), cap_u = al(mB * (mK + 1) * 4);
     const size_t cap_len = al(mB * 4), cap_out = al(mB * (mK + 1) * 4), cap_mask = al(mB * mK);
     const size_t cap_stats = al(mB * (mK + 1) * 8), cap_pd = al(mB * mK * 4), cap_st = al(mB * 4);
     const size_t need = cap_logits + cap_q + cap_tok + cap_u + cap_len + cap_out + cap_mask +
                         cap_stats + cap_pd + cap_st;
+    if (ctx->d_stage && ctx->stage_bytes < need) {
+        if (cudaStreamSynchronize(s) != cudaSuccess || cudaFree(ctx->d_stage) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return SV_ERR_CUDA;
+        }
+        ctx->d_stage = nullptr;
+        ctx->stage_bytes = 0;
+    }
     if (!ctx->d_stage) {
         if (cudaMalloc(&ctx->d_stage, need) != cudaSuccess) {
             (void)cudaGetLastError();

@@ -299,7 +299,7 @@ def test_host_buffer_entry_matches_device_entry():
 
 @pytest.mark.parametrize("V,K,T,seed", [(4, 1, 1.0, 1), (8, 3, 1.3, 3)])
 def test_gpu_output_law(V, K, T, seed):
-    pins.check_output_law(gh.gpu_verify, V, K, T, seed)
+    pins.check_output_law(gh.gpu_verify, V, K, T, seed, margin=2e-6)
 
 
 @pytest.mark.parametrize("V,K", [(4, 1), (6, 3), (8, 3)])

@@ -245,3 +245,16 @@ def test_workload_recipes_have_the_stated_overlap():
     p = pins.p_rows(cell.logits, 1.0)
     ov = np.minimum(p[:, :3], cell.q.astype(np.float64)).sum(-1)
     np.testing.assert_allclose(ov, 0.7, atol=1e-6)
+
+
+def test_inverse_transform_convention():
+    """The draw maps u to the first token whose cumulative weight exceeds u
+    (inverse-transform sampling over ascending ids): weights 0.1, 0.2, 0.3, 0.4
+    have cumulative sums 0.1, 0.3, 0.6, 1.0."""
+    logits = np.log(np.array([[0.1, 0.2, 0.3, 0.4]])).astype(np.float32)
+    us = np.array([0.0, 0.05, 0.0999, 0.1001, 0.2999, 0.3001, 0.5999, 0.6001, 0.99999994], np.float32)
+    want = [0, 0, 0, 1, 1, 2, 2, 3, 3]
+    n = us.size
+    out = oracle.verify(np.broadcast_to(logits, (n, 1, 4)), "f32", np.zeros((n, 0, 4), np.float32),
+                        np.zeros((n, 0), np.int32), us.reshape(n, 1), 1.0)
+    assert list(out["out_tokens"][:, 0]) == want
