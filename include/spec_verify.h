@@ -95,6 +95,7 @@ typedef struct {
     int64_t slice;     /* vocabulary entries per CTA (a multiple of 8)                 */
     int64_t grid;      /* CTAs in the launch = B * cluster                             */
     int bulk_copy;     /* 1: row slices move with cp.async.bulk; 0: element-wise loads */
+    int prefetch_next; /* 1: the next row slice is prefetched into L2 while one is reduced */
 } sv_plan;
 
 /* Create a context on `device` for calls with B <= max_B, K <= max_K (<= 32)

@@ -70,6 +70,7 @@ int plan_impl(int num_sms, int smem_per_cta, int max_cluster, int B, int K, int6
             out->slice = slice;
             out->grid = (int64_t)B * C;
             out->bulk_copy = ((V * es) % 16) == 0 ? 1 : 0;
+            out->prefetch_next = 0;
             return SV_OK;
         }
         if (ovr_cluster || C >= cmax)

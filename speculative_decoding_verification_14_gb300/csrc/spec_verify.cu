@@ -17,17 +17,21 @@
 //  * one thread-block cluster of C CTAs per sequence; CTA r owns a contiguous
 //    vocabulary slice of every row of that sequence;
 //  * a row slice moves HBM -> shared memory with one cp.async.bulk (the TMA
-//    bulk-copy engine) completing on an mbarrier, then two passes over shared
-//    memory give the slice's max and sum of exponentials;
-//  * the C partial (max, sum) pairs are combined through distributed shared
-//    memory after a cluster barrier, in the same fixed order in every CTA, so
-//    every CTA reaches the same accept/reject decision without broadcast;
+//    bulk-copy engine) completing on an mbarrier; each warp reduces the
+//    vectors it owns to a (max, sum of exponentials) pair with packed f32x2
+//    arithmetic and publishes it -- no CTA-wide barrier inside a row step;
+//  * after one cluster barrier, warp 0 of every CTA reads the C x warps
+//    partial pairs through distributed shared memory and merges them in a
+//    fixed order in double precision, so every CTA reaches the same
+//    accept/reject decision without a broadcast;
 //  * rows are consumed in order and the loop stops at the first rejection,
 //    like the pages' loop, so rows after it are never read;
-//  * the residual (or bonus) draw is split across the cluster too: each CTA
-//    sums max(0, p - q) over its slice (q streamed from HBM, logits still in
-//    shared memory), the per-CTA sums meet in distributed shared memory, and
-//    only the CTA holding the crossing point re-scans one warp-sized stretch.
+//  * the residual (or bonus) draw is split across the cluster: the rejected
+//    draft row is bulk-prefetched into L2 as soon as the rejection is known,
+//    each CTA weighs its slice (logits still in shared memory), per-warp scans
+//    give tile and warp totals, the per-CTA totals meet in distributed shared
+//    memory, and the crossing is located by warp-parallel scans down to one
+//    entry in the owning CTA.
 #include <cuda_runtime.h>
 #include <cooperative_groups.h>
 
@@ -47,6 +51,7 @@ using sv::kMaxK;
 using sv::kMaxRows;
 
 constexpr unsigned kFull = 0xffffffffu;
+constexpr int kMaxWarps = 16;
 constexpr int kStateRun = 0, kStateSample = 1, kStateError = 2;
 constexpr int kModeResidual = 0, kModeBonus = 1, kModeTargetRow = 2;
 
@@ -66,24 +71,25 @@ struct SvArgs {
     int64_t slice;
     int B, K, C, G;
     int rowbuf_bytes;
+    int part_offset;        // bytes from the fixed state to the per-warp partials
+    int wt_offset;          // bytes from the fixed state to the tile/warp totals
     int bulk;
     int qvec;
-    float c_hi, c_lo;       // log2(e)/T split into two floats (hi + lo)
+    int prefetch_next;      // 1: L2-prefetch the next row slice while this one is processed
+    float c_hi, c_lo;       // log2(e)/T = c_hi + c_lo with c_lo > 0
     double c_d;             // log2(e)/T in double
     double T_d;
     unsigned long long wait_ns;
 };
 
-// Fixed shared state of one CTA.  The part_* and samp_* members are read by
-// the other CTAs of the cluster through distributed shared memory.
+// Fixed shared state of one CTA.  samp_* is read by the other CTAs of the
+// cluster through distributed shared memory (so are the per-warp partials,
+// which live after this struct).
 struct __align__(16) SvShared {
     unsigned long long mbar;
-    float part_m[2][kMaxRows];
-    float part_s[2][kMaxRows];
-    int part_flag[2];
     double samp_tot[2];
-    int samp_last[2];
     int samp_bad[2];
+    double wtot[kMaxWarps];
     int x[kMaxK];
     float u[kMaxRows];
     float lx[kMaxK];
@@ -91,13 +97,9 @@ struct __align__(16) SvShared {
     float rs_m[kMaxRows];
     float rs_s[kMaxRows];
     float pd[kMaxK];
-    float red_f[32];
-    int red_i[32];
-    int state, j, code, ndec, mode, tok, owner;
+    int state, j, code, ndec, mode, tok, owner, take_last, loc_tile, loc_warp;
     float rowM;
-    double rowS;
-    int loc_warp, loc_tile;
-    double loc_rem;
+    double rowS, loc_rem;
 };
 static_assert(sizeof(SvShared) + 64 <= sv::kFixedSmem, "fixed shared state outgrew its reservation");
 
@@ -134,6 +136,11 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
             smem_addr(dst)),
         "l"(src), "r"(bytes), "r"(smem_addr(bar))
         : "memory");
+}
+
+// Bulk prefetch of a global range into L2 (no destination, no completion).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t parity) {
@@ -176,13 +183,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
-// l - m for the exponent d*c_hi + d*c_lo.  A -inf logit (or -inf padding)
-// would give d = -inf and, when c_lo < 0, -inf + inf = NaN; clamping d to a
-// finite floor keeps the product with c_lo finite while d*c_hi still
-// overflows to -inf, so the entry weighs exactly 0.  (NaN logits never reach
-// this point: the row max propagates them and the row is rejected first.)
-__device__ __forceinline__ float exp_arg_diff(float l, float m) { return fmaxf(l - m, -3.0e38f); }
-
 // max that returns NaN when either input is NaN (IEEE maxNum would drop it)
 __device__ __forceinline__ float fmax_nan(float a, float b) {
     float d;
@@ -199,6 +199,16 @@ __device__ __forceinline__ uint32_t bf16x2_max_nan(uint32_t a, uint32_t b) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+// 2^((l - m) * log2(e)/T) for a pair of entries.  The exponent is formed as
+// d*c_hi + d*c_lo with d = l - m (exact for bf16 inputs), so the only
+// roundings are the final one and the ex2 approximation.  c_lo > 0 keeps a
+// -inf entry at -inf (-inf*c_lo = -inf), so it weighs exactly 0.
+__device__ __forceinline__ float2 exp2_pair(float2 l, float2 neg_m, float2 chi, float2 clo) {
+    const float2 d = __fadd2_rn(l, neg_m);
+    const float2 y = __ffma2_rn(d, chi, __fmul2_rn(d, clo));
+    return make_float2(ex2_approx(y.x), ex2_approx(y.y));
+}
+
 // ------------------------------------------------------------ elements -----
 
 template <int ES>
@@ -207,11 +217,9 @@ template <>
 struct Elem<4> {
     static constexpr int E = 4;  // entries per 16-byte vector
     static constexpr uint32_t kNegInf = 0xff800000u;
-    __device__ static __forceinline__ void unpack(const uint4 w, float (&f)[4]) {
-        f[0] = __uint_as_float(w.x);
-        f[1] = __uint_as_float(w.y);
-        f[2] = __uint_as_float(w.z);
-        f[3] = __uint_as_float(w.w);
+    __device__ static __forceinline__ void unpack(const uint4 w, float2 (&f)[2]) {
+        f[0] = make_float2(__uint_as_float(w.x), __uint_as_float(w.y));
+        f[1] = make_float2(__uint_as_float(w.z), __uint_as_float(w.w));
     }
     __device__ static __forceinline__ float load(const void* base, int64_t idx) {
         return __ldg(static_cast<const float*>(base) + idx);
@@ -222,20 +230,20 @@ struct Elem<4> {
     __device__ static __forceinline__ uint32_t load_raw(const void* base, int64_t idx) {
         return __ldg(static_cast<const uint32_t*>(base) + idx);
     }
+    __device__ static __forceinline__ float vec_max(const uint4 w, float m) {
+        return fmax_nan(m, fmax_nan(fmax_nan(__uint_as_float(w.x), __uint_as_float(w.y)),
+                                    fmax_nan(__uint_as_float(w.z), __uint_as_float(w.w))));
+    }
 };
 template <>
 struct Elem<2> {
     static constexpr int E = 8;
     static constexpr uint32_t kNegInf = 0xff80u;
-    __device__ static __forceinline__ void unpack(const uint4 w, float (&f)[8]) {
-        f[0] = bf16_lo(w.x);
-        f[1] = bf16_hi(w.x);
-        f[2] = bf16_lo(w.y);
-        f[3] = bf16_hi(w.y);
-        f[4] = bf16_lo(w.z);
-        f[5] = bf16_hi(w.z);
-        f[6] = bf16_lo(w.w);
-        f[7] = bf16_hi(w.w);
+    __device__ static __forceinline__ void unpack(const uint4 w, float2 (&f)[4]) {
+        f[0] = make_float2(bf16_lo(w.x), bf16_hi(w.x));
+        f[1] = make_float2(bf16_lo(w.y), bf16_hi(w.y));
+        f[2] = make_float2(bf16_lo(w.z), bf16_hi(w.z));
+        f[3] = make_float2(bf16_lo(w.w), bf16_hi(w.w));
     }
     __device__ static __forceinline__ float load(const void* base, int64_t idx) {
         const unsigned short h = __ldg(static_cast<const unsigned short*>(base) + idx);
@@ -249,9 +257,8 @@ struct Elem<2> {
     }
 };
 
-// ------------------------------------------------------- block helpers -----
+// ------------------------------------------------------- warp helpers -----
 
-template <int NT>
 __device__ __forceinline__ float warp_max_nan(float v) {
 #pragma unroll
     for (int o = 16; o; o >>= 1)
@@ -259,75 +266,20 @@ __device__ __forceinline__ float warp_max_nan(float v) {
     return v;
 }
 
-// Max over a staged row slice (nvec 16-byte vectors, padded with -inf).
-// Every thread returns the same value.
-template <int ES, int NT>
-__device__ float slice_max(const unsigned char* buf, int nvec, SvShared& sh) {
-    const int tid = threadIdx.x;
-    float m;
-    if constexpr (ES == 2) {
-        uint32_t acc = 0xff80ff80u;
-        for (int vi = tid; vi < nvec; vi += NT) {
-            const uint4 w = reinterpret_cast<const uint4*>(buf)[vi];
-            acc = bf16x2_max_nan(acc, w.x);
-            acc = bf16x2_max_nan(acc, w.y);
-            acc = bf16x2_max_nan(acc, w.z);
-            acc = bf16x2_max_nan(acc, w.w);
-        }
-        m = fmax_nan(bf16_lo(acc), bf16_hi(acc));
-    } else {
-        m = -INFINITY;
-        for (int vi = tid; vi < nvec; vi += NT) {
-            const uint4 w = reinterpret_cast<const uint4*>(buf)[vi];
-            m = fmax_nan(m, fmax_nan(fmax_nan(__uint_as_float(w.x), __uint_as_float(w.y)),
-                                     fmax_nan(__uint_as_float(w.z), __uint_as_float(w.w))));
-        }
-    }
-    m = warp_max_nan<NT>(m);
-    if ((tid & 31) == 0)
-        sh.red_f[tid >> 5] = m;
-    __syncthreads();
-    float r = sh.red_f[0];
-#pragma unroll
-    for (int w = 1; w < NT / 32; ++w)
-        r = fmax_nan(r, sh.red_f[w]);
-    __syncthreads();
-    return r;
-}
-
-// sum_v 2^((l_v - m) * log2(e)/T) over a staged slice.  The exponent is formed
-// as d*c_hi + d*c_lo with d = l - m exact for bf16 inputs, so the only
-// rounding per entry is the final one and the ex2 approximation.
-// Result valid in thread 0.
-template <int ES, int NT>
-__device__ float slice_sumexp(const unsigned char* buf, int nvec, float m, float c_hi, float c_lo,
-                              SvShared& sh) {
-    constexpr int E = Elem<ES>::E;
-    const int tid = threadIdx.x;
-    float s0 = 0.f, s1 = 0.f;
-    for (int vi = tid; vi < nvec; vi += NT) {
-        float f[E];
-        Elem<ES>::unpack(reinterpret_cast<const uint4*>(buf)[vi], f);
-#pragma unroll
-        for (int k = 0; k < E; k += 2) {
-            const float d0 = exp_arg_diff(f[k], m), d1 = exp_arg_diff(f[k + 1], m);
-            s0 += ex2_approx(fmaf(d0, c_hi, d0 * c_lo));
-            s1 += ex2_approx(fmaf(d1, c_hi, d1 * c_lo));
-        }
-    }
-    float s = s0 + s1;
+// Sum over the warp, result in every lane (reduced in one fixed order, then
+// broadcast from lane 0 so that all lanes hold the same bits).
+__device__ __forceinline__ float warp_sum_bcast(float v) {
 #pragma unroll
     for (int o = 16; o; o >>= 1)
-        s += __shfl_down_sync(kFull, s, o);
-    if ((tid & 31) == 0)
-        sh.red_f[tid >> 5] = s;
-    __syncthreads();
-    float r = 0.f;
-    if (tid == 0)
-        for (int w = 0; w < NT / 32; ++w)
-            r += sh.red_f[w];
-    __syncthreads();
-    return r;
+        v += __shfl_down_sync(kFull, v, o);
+    return __shfl_sync(kFull, v, 0);
+}
+
+__device__ __forceinline__ double warp_sum_bcast(double v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1)
+        v += __shfl_down_sync(kFull, v, o);
+    return __shfl_sync(kFull, v, 0);
 }
 
 __device__ __forceinline__ float warp_incl_scan(float v) {
@@ -341,73 +293,159 @@ __device__ __forceinline__ float warp_incl_scan(float v) {
     return v;
 }
 
-// Weights of one 16-byte vector of the staged row: residual max(0, p - q)
-// (mode 0), unnormalised target weights exp(z - max) (modes 1 and 2).
-// Entries at or past L weigh 0.  `bad` is raised by a NaN, infinite or
-// negative q value.
-template <int ES>
-__device__ __forceinline__ void vec_weights(const unsigned char* buf, int vi, int64_t L,
-                                            const float* qrow, int qvec, int mode, float M,
-                                            float c_hi, float c_lo, float inv_s,
-                                            float (&w)[Elem<ES>::E], bool& bad) {
+__device__ __forceinline__ double warp_incl_scan(double v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const double n = __shfl_up_sync(kFull, v, o);
+        if (lane >= o)
+            v += n;
+    }
+    return v;
+}
+
+// First lane whose inclusive running total exceeds `rem`; when none does (a
+// rounding corner), the last lane with a positive part and take_last = 1.
+// Lanes beyond `n` must hold part = 0.  Returns -1 only if every part is 0.
+__device__ __forceinline__ int pick_lane(double part, double incl, double rem, int n,
+                                         int& take_last) {
+    const int lane = threadIdx.x & 31;
+    const unsigned cross = __ballot_sync(kFull, lane < n && !take_last && incl > rem);
+    if (cross)
+        return __ffs(cross) - 1;
+    const unsigned pos = __ballot_sync(kFull, lane < n && part > 0.0);
+    take_last = 1;
+    return pos ? 31 - __clz(pos) : -1;
+}
+
+// Per-warp (max, sum of exponentials relative to that max) over the vectors of
+// one staged row slice this warp owns (vectors warp*32 + lane + k*NT).  The
+// same value is returned in every lane.
+template <int ES, int NT>
+__device__ __forceinline__ float2 warp_slice_stats(const unsigned char* buf, int nvec, float c_hi,
+                                                   float c_lo) {
     constexpr int E = Elem<ES>::E;
-    float f[E];
-    Elem<ES>::unpack(reinterpret_cast<const uint4*>(buf)[vi], f);
-    const int64_t base = (int64_t)vi * E;
-    float qq[E];
+    const int tid = threadIdx.x;
+    const uint4* vbuf = reinterpret_cast<const uint4*>(buf);
+    float m;
+    if constexpr (ES == 2) {
+        uint32_t acc = 0xff80ff80u;
+        for (int vi = tid; vi < nvec; vi += NT) {
+            const uint4 w = vbuf[vi];
+            acc = bf16x2_max_nan(bf16x2_max_nan(acc, w.x), bf16x2_max_nan(w.y, w.z));
+            acc = bf16x2_max_nan(acc, w.w);
+        }
+        m = fmax_nan(bf16_lo(acc), bf16_hi(acc));
+    } else {
+        m = -INFINITY;
+        for (int vi = tid; vi < nvec; vi += NT)
+            m = Elem<4>::vec_max(vbuf[vi], m);
+    }
+    m = warp_max_nan(m);
+    float s = 0.f;
+    if (m > -INFINITY && m < INFINITY) {  // uniform within the warp
+        const float2 neg_m = make_float2(-m, -m), chi = make_float2(c_hi, c_hi),
+                     clo = make_float2(c_lo, c_lo);
+        float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+        for (int vi = tid; vi < nvec; vi += NT) {
+            float2 f[E / 2];
+            Elem<ES>::unpack(vbuf[vi], f);
 #pragma unroll
-    for (int k = 0; k < E; ++k)
-        qq[k] = 0.f;
-    if (mode == kModeResidual) {
-        if (qvec && base + E <= L) {
-#pragma unroll
-            for (int k = 0; k < E; k += 4) {
-                const float4 t = __ldg(reinterpret_cast<const float4*>(qrow + base + k));
-                qq[k] = t.x;
-                qq[k + 1] = t.y;
-                qq[k + 2] = t.z;
-                qq[k + 3] = t.w;
+            for (int k = 0; k < E / 2; k += 2) {
+                a0 = __fadd2_rn(a0, exp2_pair(f[k], neg_m, chi, clo));
+                a1 = __fadd2_rn(a1, exp2_pair(f[k + 1], neg_m, chi, clo));
             }
-        } else {
+        }
+        s = warp_sum_bcast((a0.x + a0.y) + (a1.x + a1.y));
+    }
+    return make_float2(m, s);
+}
+
+// Draft probabilities for one 16-byte vector of the slice (E entries); entries
+// at or past L read as 0.
+template <int ES>
+__device__ __forceinline__ void load_q_vec(const float* qrow, int vi, int64_t L, int qvec,
+                                           float (&qq)[Elem<ES>::E]) {
+    constexpr int E = Elem<ES>::E;
+    const int64_t base = (int64_t)vi * E;
+    if (qvec && base + E <= L) {
 #pragma unroll
-            for (int k = 0; k < E; ++k)
-                qq[k] = base + k < L ? __ldg(qrow + base + k) : 0.f;
+        for (int k = 0; k < E; k += 4) {
+            const float4 t = __ldg(reinterpret_cast<const float4*>(qrow + base + k));
+            qq[k] = t.x;
+            qq[k + 1] = t.y;
+            qq[k + 2] = t.z;
+            qq[k + 3] = t.w;
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < E; ++k)
+            qq[k] = base + k < L ? __ldg(qrow + base + k) : 0.f;
+    }
+}
+
+// Draw weights of one vector: residual max(0, p - q) (mode 0) or the
+// unnormalised target weights exp(z - max) (modes 1 and 2).  Entries at or
+// past L weigh 0.  `bad` is raised by a NaN, infinite or negative q value.
+template <int ES>
+__device__ __forceinline__ float vec_weights(const unsigned char* buf, int vi, int64_t L,
+                                             const float (&qq)[Elem<ES>::E], int mode, float M,
+                                             float c_hi, float c_lo, float inv_s,
+                                             float (&w)[Elem<ES>::E], bool& bad) {
+    constexpr int E = Elem<ES>::E;
+    float2 f[E / 2];
+    Elem<ES>::unpack(reinterpret_cast<const uint4*>(buf)[vi], f);
+    const float2 neg_m = make_float2(-M, -M), chi = make_float2(c_hi, c_hi),
+                 clo = make_float2(c_lo, c_lo);
+    const int64_t base = (int64_t)vi * E;
+    float ts = 0.f;
+#pragma unroll
+    for (int k = 0; k < E / 2; ++k) {
+        const float2 e = exp2_pair(f[k], neg_m, chi, clo);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int idx = 2 * k + h;
+            const float ev = h ? e.y : e.x;
+            float wk;
+            if (mode == kModeResidual) {
+                const float qv = qq[idx];
+                if (base + idx < L && !(qv >= 0.f && qv < INFINITY))
+                    bad = true;
+                wk = fmaxf(__fmaf_rn(ev, inv_s, -qv), 0.f);
+            } else {
+                wk = ev;
+            }
+            w[idx] = base + idx < L ? wk : 0.f;
+            ts += w[idx];
         }
     }
-#pragma unroll
-    for (int k = 0; k < E; ++k) {
-        const float d = exp_arg_diff(f[k], M);
-        const float e = ex2_approx(fmaf(d, c_hi, d * c_lo));
-        float wk;
-        if (mode == kModeResidual) {
-            const float qv = qq[k];
-            if (base + k < L && !(qv >= 0.f && qv < INFINITY))
-                bad = true;
-            wk = fmaxf(e * inv_s - qv, 0.f);
-        } else {
-            wk = e;
-        }
-        w[k] = base + k < L ? wk : 0.f;
-    }
+    return ts;
 }
 
 // --------------------------------------------------------------- kernel -----
 
+// Residency target: 1536 threads per SM (registers capped accordingly).
 template <int ES, int NT>
-__global__ void __launch_bounds__(NT) sv_verify_kernel(const __grid_constant__ SvArgs a) {
+__global__ void __launch_bounds__(NT, 1536 / NT) sv_verify_kernel(const __grid_constant__ SvArgs a) {
     constexpr int E = Elem<ES>::E;
     constexpr int NW = NT / 32;
+    static_assert(NW <= kMaxWarps, "too many warps");
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = (int)cluster.block_rank();
     const int b = (int)(blockIdx.x / (unsigned)a.C);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int K = a.K;
     const int64_t V = a.V;
+    const int C = a.C;
+    const int G = a.G;
 
     extern __shared__ __align__(128) unsigned char smem_raw[];
     unsigned char* bufs = smem_raw;
-    SvShared& sh = *reinterpret_cast<SvShared*>(smem_raw + (size_t)a.G * a.rowbuf_bytes);
-    float* wt = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(&sh) + sizeof(SvShared));
+    unsigned char* fixed = smem_raw + (size_t)G * a.rowbuf_bytes;
+    SvShared& sh = *reinterpret_cast<SvShared*>(fixed);
+    float2* part = reinterpret_cast<float2*>(fixed + a.part_offset);  // [2][G][NW] (max, sum)
+    int* part_flag = reinterpret_cast<int*>(part + 2 * G * NW);       // [2][NW]
+    float* wt = reinterpret_cast<float*>(fixed + a.wt_offset);          // [tiles][NW]
 
     // this CTA's vocabulary slice
     const int64_t v0 = (int64_t)rank * a.slice;
@@ -418,13 +456,15 @@ __global__ void __launch_bounds__(NT) sv_verify_kernel(const __grid_constant__ S
     if (tid == 0) {
         mbar_init(&sh.mbar, 1);
         fence_mbar_init();
-        sh.part_flag[0] = sh.part_flag[1] = 0;
     }
     __syncthreads();
 
     uint32_t phase = 0;
-    bool timed_out = false;
+    bool timed_out = false;  // per thread; published per warp
 
+    auto row_src = [&](int row) {
+        return static_cast<const unsigned char*>(a.logits) + ((row0 + row) * V + v0) * ES;
+    };
     // Moves rows g0 .. g0+ng-1 of this sequence's slice into shared memory.
     auto load_group = [&](int g0, int ng) {
         if (L == 0)
@@ -434,11 +474,12 @@ __global__ void __launch_bounds__(NT) sv_verify_kernel(const __grid_constant__ S
                 fence_proxy_async();
                 const uint32_t bytes = (uint32_t)(L * ES);
                 mbar_arrive_expect_tx(&sh.mbar, bytes * (uint32_t)ng);
-                for (int r = 0; r < ng; ++r) {
-                    const unsigned char* src = static_cast<const unsigned char*>(a.logits) +
-                                               ((row0 + g0 + r) * V + v0) * ES;
-                    bulk_copy_g2s(bufs + (size_t)r * a.rowbuf_bytes, src, bytes, &sh.mbar);
-                }
+                for (int r = 0; r < ng; ++r)
+                    bulk_copy_g2s(bufs + (size_t)r * a.rowbuf_bytes, row_src(g0 + r), bytes,
+                                  &sh.mbar);
+                if (a.prefetch_next)
+                    for (int r = g0 + ng; r < g0 + 2 * ng && r <= K; ++r)
+                        bulk_prefetch_l2(row_src(r), bytes);
             }
         } else {
             const int64_t lpad = (int64_t)nvec * E;
@@ -456,17 +497,15 @@ __global__ void __launch_bounds__(NT) sv_verify_kernel(const __grid_constant__ S
         if (L == 0)
             return;
         if (a.bulk) {
-            const bool ok = mbar_wait_bounded(&sh.mbar, phase, a.wait_ns);
-            phase ^= 1u;
-            if (__syncthreads_or(!ok))
+            if (!mbar_wait_bounded(&sh.mbar, phase, a.wait_ns))
                 timed_out = true;
+            phase ^= 1u;
         } else {
             __syncthreads();
         }
     };
 
     // first group's copy goes out before anything else
-    const int G = a.G;
     load_group(0, G < K + 1 ? G : K + 1);
 
     // per-sequence inputs: drafts, uniforms, and the gathered p/q inputs at the drafts
@@ -494,7 +533,7 @@ __global__ void __launch_bounds__(NT) sv_verify_kernel(const __grid_constant__ S
         sh.lx[tid] = Elem<ES>::load(a.logits, (row0 + tid) * V + x);
         sh.qx[tid] = __ldg(a.q + ((int64_t)b * K + tid) * V + x);
     }
-    // (made visible to thread 0 by the barriers below)
+    // (made visible to warp 0 by the cluster barrier below)
 
     // ---- test loop over groups of rows, in order ([P1]) ----
     int par = 0;
@@ -507,49 +546,58 @@ __global__ void __launch_bounds__(NT) sv_verify_kernel(const __grid_constant__ S
         if (sh.state != kStateRun)
             break;
         for (int r = 0; r < ng; ++r) {
-            const unsigned char* buf = bufs + (size_t)r * a.rowbuf_bytes;
-            const float m = L ? slice_max<ES, NT>(buf, nvec, sh) : -INFINITY;
-            float s = 0.f;
-            if (m > -INFINITY && m < INFINITY)
-                s = slice_sumexp<ES, NT>(buf, nvec, m, a.c_hi, a.c_lo, sh);
-            if (tid == 0) {
-                sh.part_m[par][r] = m;
-                sh.part_s[par][r] = s;
-            }
+            const float2 ms = L ? warp_slice_stats<ES, NT>(bufs + (size_t)r * a.rowbuf_bytes, nvec,
+                                                           a.c_hi, a.c_lo)
+                                : make_float2(-INFINITY, 0.f);
+            if (lane == 0)
+                part[(par * G + r) * NW + warp] = ms;
         }
-        if (tid == 0)
-            sh.part_flag[par] = timed_out ? 1 : 0;
+        {
+            const int anyto = __any_sync(kFull, timed_out);
+            if (lane == 0)
+                part_flag[par * NW + warp] = anyto;
+        }
         cluster.sync();
 
-        // combine the C partials of each row in rank order, then decide
+        // combine the C * NW partial pairs of each row in a fixed order, then decide
         if (warp == 0) {
+            constexpr int kPer = sv::kMaxCluster * NW / 32;  // partials per lane, at most
+            const int P = C * NW;
+            int anyflag = 0;
+            for (int p = lane; p < P; p += 32)
+                anyflag |= cluster.map_shared_rank(part_flag, p / NW)[par * NW + (p % NW)];
+            anyflag = __any_sync(kFull, anyflag != 0);
             for (int r = 0; r < ng; ++r) {
-                float mr = -INFINITY, sr = 0.f;
-                int fr = 0;
-                if (lane < a.C) {
-                    const SvShared* rs = cluster.map_shared_rank(&sh, lane);
-                    mr = rs->part_m[par][r];
-                    sr = rs->part_s[par][r];
-                    fr = rs->part_flag[par];
-                }
-                const float M = warp_max_nan<NT>(mr);
-                double term = 0.0;
-                if (lane < a.C && sr > 0.f && M > -INFINITY && M < INFINITY)
-                    term = (double)sr * exp2(((double)mr - (double)M) * a.c_d);
+                float2 pv[kPer];
+                float mloc = -INFINITY;
 #pragma unroll
-                for (int o = 16; o; o >>= 1)
-                    term += __shfl_down_sync(kFull, term, o);
-                const int anyflag = __any_sync(kFull, fr != 0);
+                for (int t = 0; t < kPer; ++t) {
+                    const int p = lane + 32 * t;
+                    pv[t] = make_float2(-INFINITY, 0.f);
+                    if (p < P) {
+                        pv[t] = cluster.map_shared_rank(part, p / NW)[(par * G + r) * NW + (p % NW)];
+                        mloc = fmax_nan(mloc, pv[t].x);
+                    }
+                }
+                const float M = warp_max_nan(mloc);
+                const bool finite = M > -INFINITY && M < INFINITY;
+                double acc = 0.0;
+                if (finite) {
+#pragma unroll
+                    for (int t = 0; t < kPer; ++t)
+                        if (pv[t].y > 0.f)
+                            acc += (double)pv[t].y * exp2(((double)pv[t].x - (double)M) * a.c_d);
+                }
+                const double S = warp_sum_bcast(acc);
                 if (lane == 0 && sh.state == kStateRun) {
                     const int i = g0 + r;
                     if (anyflag) {
                         sh.state = kStateError;
                         sh.code = SV_ERR_TIMEOUT;
-                    } else if (!(M > -INFINITY && M < INFINITY)) {
+                    } else if (!finite) {
                         sh.state = kStateError;
                         sh.code = SV_ERR_NONFINITE;
                     } else {
-                        const double S = term;
                         sh.rs_m[i] = (float)((double)M / a.T_d);
                         sh.rs_s[i] = (float)S;
                         sh.ndec = i + 1;
@@ -567,6 +615,10 @@ __global__ void __launch_bounds__(NT) sv_verify_kernel(const __grid_constant__ S
                                     sh.mode = kModeResidual;
                                     sh.rowM = M;
                                     sh.rowS = S;
+                                    // the draft row is needed now: start pulling it into L2
+                                    if (a.qvec && L > 0)
+                                        bulk_prefetch_l2(a.q + ((int64_t)b * K + i) * V + v0,
+                                                         (uint32_t)(L * 4));
                                 }
                             }
                         } else {
@@ -586,7 +638,6 @@ __global__ void __launch_bounds__(NT) sv_verify_kernel(const __grid_constant__ S
         if (sh.state != kStateRun)
             break;
         g0 += ng;
-        __syncthreads();  // every thread is done with the staged rows
         load_group(g0, G < K + 1 - g0 ? G : K + 1 - g0);
     }
 
@@ -601,92 +652,88 @@ __global__ void __launch_bounds__(NT) sv_verify_kernel(const __grid_constant__ S
         const int ntiles = (nvec + NT - 1) / NT;
         int mode = sh.mode;
         int sp = 0;
-        double S = 0.0, t = 0.0;
-        double tots[sv::kMaxCluster];
-        int lasts[sv::kMaxCluster];
         for (int round = 0; round < 2; ++round) {
-            int last = -1;
             bool bad = false;
-            for (int k = 0; k < ntiles; ++k) {
-                const int vi = k * NT + tid;
-                float ts = 0.f;
-                if (vi < nvec) {
-                    float w[E];
-                    vec_weights<ES>(buf, vi, L, qrow, a.qvec, mode, M, a.c_hi, a.c_lo, inv_s, w,
-                                    bad);
+            double wacc = 0.0;  // this warp's total over all tiles (meaningful in lane 31)
+            for (int k = 0; k < ntiles; k += 2) {
+                // two tiles in flight: both q loads go out before either is used
+                const int vi0 = k * NT + tid, vi1 = vi0 + NT;
+                float q0[E], q1[E], w[E];
 #pragma unroll
-                    for (int e = 0; e < E; ++e) {
-                        ts += w[e];
-                        if (w[e] > 0.f)
-                            last = vi * E + e;
+                for (int e = 0; e < E; ++e)
+                    q0[e] = q1[e] = 0.f;
+                if (mode == kModeResidual) {
+                    if (vi0 < nvec)
+                        load_q_vec<ES>(qrow, vi0, L, a.qvec, q0);
+                    if (vi1 < nvec)
+                        load_q_vec<ES>(qrow, vi1, L, a.qvec, q1);
+                }
+                const float ts0 = vi0 < nvec ? vec_weights<ES>(buf, vi0, L, q0, mode, M, a.c_hi,
+                                                               a.c_lo, inv_s, w, bad)
+                                             : 0.f;
+                const float ts1 = vi1 < nvec ? vec_weights<ES>(buf, vi1, L, q1, mode, M, a.c_hi,
+                                                               a.c_lo, inv_s, w, bad)
+                                             : 0.f;
+                const float in0 = warp_incl_scan(ts0);
+                const float in1 = warp_incl_scan(ts1);
+                if (lane == 31) {
+                    wt[k * NW + warp] = in0;
+                    wacc += (double)in0;
+                    if (k + 1 < ntiles) {
+                        wt[(k + 1) * NW + warp] = in1;
+                        wacc += (double)in1;
                     }
                 }
-                const float incl = warp_incl_scan(ts);
-                if (lane == 31)
-                    wt[k * NW + warp] = incl;
             }
-            // block: any bad q, last positive entry, slice total
-#pragma unroll
-            for (int o = 16; o; o >>= 1)
-                last = max(last, __shfl_xor_sync(kFull, last, o));
-            if (lane == 0)
-                sh.red_i[warp] = last;
+            if (lane == 31)
+                sh.wtot[warp] = wacc;
             const int anybad = __syncthreads_or(bad);
             if (tid == 0) {
-                int lb = -1;
-                for (int w = 0; w < NW; ++w)
-                    lb = max(lb, sh.red_i[w]);
                 double tot = 0.0;
-                for (int k = 0; k < ntiles; ++k)
-                    for (int w = 0; w < NW; ++w)
-                        tot += (double)wt[k * NW + w];
+                for (int w2 = 0; w2 < NW; ++w2)
+                    tot += sh.wtot[w2];
                 sh.samp_tot[sp] = tot;
-                sh.samp_last[sp] = lb >= 0 ? (int)(v0 + lb) : -1;
                 sh.samp_bad[sp] = anybad;
             }
             cluster.sync();
-            if (tid == 0) {
+            if (warp == 0) {
+                double tot = 0.0;
                 int cbad = 0;
-                S = 0.0;
-                for (int c = 0; c < a.C; ++c) {
-                    const SvShared* rs = cluster.map_shared_rank(&sh, c);
-                    tots[c] = rs->samp_tot[sp];
-                    lasts[c] = rs->samp_last[sp];
-                    cbad |= rs->samp_bad[sp];
-                    S += tots[c];
+                if (lane < C) {
+                    const SvShared* rs = cluster.map_shared_rank(&sh, lane);
+                    tot = rs->samp_tot[sp];
+                    cbad = rs->samp_bad[sp];
                 }
-                if (cbad) {
-                    sh.state = kStateError;
-                    sh.code = SV_ERR_NONFINITE;
-                    sh.mode = -1;
-                } else if (S == 0.0 && mode == kModeResidual) {
-                    // max(0, p - q) vanished (rounding or an unnormalised q):
-                    // draw from p_j itself with the same uniform
-                    sh.mode = kModeTargetRow;
-                } else {
-                    sh.mode = -1;  // done
-                    t = uK * S;
-                    int owner = -1;
-                    double run = 0.0;
-                    for (int c = 0; c < a.C; ++c) {
-                        if (run + tots[c] > t) {
-                            owner = c;
-                            break;
-                        }
-                        run += tots[c];
+                cbad = __any_sync(kFull, cbad != 0);
+                const double incl = warp_incl_scan(tot);
+                const double S = __shfl_sync(kFull, incl, C - 1);
+                const double t = uK * S;
+                int take_last = 0;
+                const int owner = pick_lane(tot, incl, t, C, take_last);
+                double prev = __shfl_up_sync(kFull, incl, 1);
+                if (lane == 0)
+                    prev = 0.0;
+                const double excl = __shfl_sync(kFull, prev, owner < 0 ? 0 : owner);
+                if (lane == 0) {
+                    if (cbad) {
+                        sh.state = kStateError;
+                        sh.code = SV_ERR_NONFINITE;
+                        sh.mode = -1;
+                    } else if (S == 0.0 && mode == kModeResidual) {
+                        // max(0, p - q) vanished (rounding or an unnormalised q):
+                        // draw from p_j itself with the same uniform
+                        sh.mode = kModeTargetRow;
+                    } else if (owner < 0) {
+                        // no positive weight anywhere: unreachable when the row max is finite
+                        sh.state = kStateError;
+                        sh.code = SV_ERR_NONFINITE;
+                        sh.mode = -1;
+                    } else {
+                        sh.mode = -1;  // done
+                        sh.owner = owner;
+                        sh.take_last = take_last;
+                        sh.loc_rem = t - excl;
                     }
-                    sh.tok = -1;
-                    if (owner < 0) {
-                        // rounding left t at or past the total: last positive entry
-                        for (int c = a.C - 1; c >= 0; --c)
-                            if (lasts[c] >= 0) {
-                                sh.tok = lasts[c];
-                                break;
-                            }
-                        owner = 0;
-                    }
-                    sh.owner = owner;
-                    sh.loc_rem = t - run;
                 }
             }
             __syncthreads();
@@ -697,83 +744,88 @@ __global__ void __launch_bounds__(NT) sv_verify_kernel(const __grid_constant__ S
         }
 
         if (sh.state == kStateSample && rank == sh.owner) {
-            // locate the crossing inside this CTA's slice: tile, then warp
-            if (tid == 0 && sh.tok < 0) {
-                const double rem = sh.loc_rem;
-                double acc = 0.0;
-                int kk = -1, ww = -1;
-                for (int k = 0; k < ntiles && kk < 0; ++k) {
+            // tile, then warp, by warp-parallel scans over the stored totals
+            if (warp == 0) {
+                int take_last = sh.take_last;
+                double rem = sh.loc_rem;
+                int kk = -1, klast = -1;
+                double carry = 0.0, carry_last = 0.0, acc_at = 0.0;
+                for (int c0 = 0; c0 < ntiles && kk < 0; c0 += 32) {
+                    const int k = c0 + lane;
                     double tk = 0.0;
-                    for (int w = 0; w < NW; ++w)
-                        tk += (double)wt[k * NW + w];
-                    if (acc + tk > rem) {
-                        for (int w = 0; w < NW; ++w) {
-                            const double tw = (double)wt[k * NW + w];
-                            if (acc + tw > rem) {
-                                kk = k;
-                                ww = w;
-                                break;
-                            }
-                            acc += tw;
-                        }
-                        if (kk < 0)
-                            break;  // rounding: no warp crosses inside the tile
-                    } else {
-                        acc += tk;
+                    if (k < ntiles)
+                        for (int w2 = 0; w2 < NW; ++w2)
+                            tk += (double)wt[k * NW + w2];
+                    const double incl = warp_incl_scan(tk) + carry;
+                    int tl = take_last;
+                    const int pick = pick_lane(tk, incl, rem, ntiles - c0, tl);
+                    if (!tl && pick >= 0) {
+                        kk = c0 + pick;
+                        acc_at = __shfl_sync(kFull, incl - tk, pick);
+                    } else if (pick >= 0) {
+                        klast = c0 + pick;
+                        carry_last = __shfl_sync(kFull, incl - tk, pick);
                     }
+                    carry = __shfl_sync(kFull, incl, 31);
                 }
                 if (kk < 0) {
-                    sh.tok = sh.samp_last[sp];
-                } else {
+                    take_last = 1;
+                    kk = klast;
+                    acc_at = carry_last;
+                }
+                double tw = 0.0;
+                if (kk >= 0 && lane < NW)
+                    tw = (double)wt[kk * NW + lane];
+                const double inclw = warp_incl_scan(tw);
+                const int ww = pick_lane(tw, inclw + acc_at, rem, NW, take_last);
+                const double accw = __shfl_sync(kFull, inclw - tw, ww < 0 ? 0 : ww);
+                if (lane == 0) {
                     sh.loc_tile = kk;
                     sh.loc_warp = ww;
-                    sh.loc_rem = rem - acc;
+                    sh.take_last = take_last;
+                    sh.loc_rem = rem - acc_at - accw;
                 }
             }
             __syncthreads();
-            if (sh.tok < 0 && warp == sh.loc_warp) {
-                // this warp re-derives the same weights and scan, then finds
-                // the lane and the entry where the running sum passes the rest
+            if (warp == sh.loc_warp && sh.loc_tile >= 0) {
+                // this warp re-derives the same weights and scan, then finds the
+                // lane and the entry where the running sum passes the remainder
+                int take_last = sh.take_last;
                 const double rem = sh.loc_rem;
                 const int vi = sh.loc_tile * NT + tid;
-                float w[E];
-                float ts = 0.f;
+                float qq[E], w[E];
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    qq[e] = 0.f;
+                    w[e] = 0.f;
+                }
                 bool dummy = false;
+                float ts = 0.f;
                 if (vi < nvec) {
-                    vec_weights<ES>(buf, vi, L, qrow, a.qvec, mode, M, a.c_hi, a.c_lo, inv_s, w,
-                                    dummy);
-#pragma unroll
-                    for (int e = 0; e < E; ++e)
-                        ts += w[e];
-                } else {
-#pragma unroll
-                    for (int e = 0; e < E; ++e)
-                        w[e] = 0.f;
+                    if (mode == kModeResidual)
+                        load_q_vec<ES>(qrow, vi, L, a.qvec, qq);
+                    ts = vec_weights<ES>(buf, vi, L, qq, mode, M, a.c_hi, a.c_lo, inv_s, w, dummy);
                 }
                 const float incl = warp_incl_scan(ts);
-                float excl = __shfl_up_sync(kFull, incl, 1);
+                const int pick = pick_lane((double)ts, (double)incl, rem, 32, take_last);
+                float prev = __shfl_up_sync(kFull, incl, 1);
                 if (lane == 0)
-                    excl = 0.f;
-                const unsigned cross = __ballot_sync(kFull, (double)incl > rem);
-                const unsigned pos = __ballot_sync(kFull, ts > 0.f);
-                int pick = cross ? __ffs(cross) - 1 : (pos ? 31 - __clz(pos) : -1);
+                    prev = 0.f;
+                const double excl = (double)__shfl_sync(kFull, prev, pick < 0 ? 0 : pick);
                 if (lane == pick) {
                     int e_hit = -1, e_last = -1;
-                    double acc = (double)excl;
+                    double acc = excl;
 #pragma unroll
                     for (int e = 0; e < E; ++e) {
                         if (w[e] > 0.f)
                             e_last = e;
                         acc += (double)w[e];
-                        if (e_hit < 0 && cross && acc > rem)
+                        if (e_hit < 0 && !take_last && acc > rem)
                             e_hit = e;
                     }
                     const int e = e_hit >= 0 ? e_hit : e_last;
-                    sh.tok = e >= 0 ? (int)(v0 + (int64_t)vi * E + e) : sh.samp_last[sp];
+                    sh.tok = (int)(v0 + (int64_t)vi * E + (e >= 0 ? e : 0));
                 }
-                __syncwarp();
-                if (lane == 0 && pick < 0)
-                    sh.tok = sh.samp_last[sp];
             }
             __syncthreads();
             // outputs of a finished sequence
@@ -863,6 +915,7 @@ struct sv_ctx {
     int num_sms = 0, smem_optin = 0, max_cluster = 8;
     uint32_t* d_err = nullptr;
     int ovr_cluster = 0, ovr_group = 0, ovr_threads = 0;
+    int ovr_prefetch = -1;  // -1: the planner decides
     unsigned long long wait_ns = 2000000000ull;
     // staging for the host-buffer entry point
     unsigned char* d_stage = nullptr;
@@ -905,8 +958,12 @@ int validate(const sv_ctx* ctx, const void* logits, int dtype, const float* q, c
 }
 
 int make_plan(const sv_ctx* ctx, int B, int K, int64_t V, int dtype, sv_plan* plan) {
-    return spec_verify_plan_for(ctx->num_sms, ctx->smem_optin, ctx->max_cluster, B, K, V, dtype,
-                                ctx->ovr_cluster, ctx->ovr_group, ctx->ovr_threads, plan);
+    const int rc = spec_verify_plan_for(ctx->num_sms, ctx->smem_optin, ctx->max_cluster, B, K, V,
+                                        dtype, ctx->ovr_cluster, ctx->ovr_group, ctx->ovr_threads,
+                                        plan);
+    if (rc == SV_OK && ctx->ovr_prefetch >= 0)
+        plan->prefetch_next = ctx->ovr_prefetch ? 1 : 0;
+    return rc;
 }
 
 int launch(sv_ctx* ctx, const void* logits, int dtype, const float* q, const int32_t* tokens,
@@ -942,11 +999,18 @@ int launch(sv_ctx* ctx, const void* logits, int dtype, const float* q, const int
     args.C = plan.cluster;
     args.G = plan.group;
     args.rowbuf_bytes = (int)sv::round_up(plan.slice * es, sv::kRowBufAlign);
+    args.part_offset = (int)sv::round_up(sizeof(SvShared), 16);
+    args.wt_offset = args.part_offset + (int)sv::partial_bytes(plan.group, plan.threads);
     args.bulk = plan.bulk_copy && aligned(logits, 16) ? 1 : 0;
+    args.prefetch_next = plan.prefetch_next && args.bulk ? 1 : 0;
     args.qvec = (V % 4 == 0) && q && aligned(q, 16) ? 1 : 0;
     args.T_d = (double)T;
     args.c_d = 1.4426950408889634074 / args.T_d;  // log2(e) / T
+    // c_hi just below c_d so that c_lo = c_d - c_hi is strictly positive: a
+    // -inf logit then gives -inf * c_lo = -inf instead of NaN
     args.c_hi = (float)args.c_d;
+    if ((double)args.c_hi >= args.c_d)
+        args.c_hi = std::nextafter(args.c_hi, 0.0f);
     args.c_lo = (float)(args.c_d - (double)args.c_hi);
     args.wait_ns = ctx->wait_ns;
 
@@ -1066,6 +1130,7 @@ int spec_verify_init(sv_ctx** out, int device, int max_B, int max_K, int64_t max
     ctx->ovr_cluster = env_int("SV_CLUSTER", 0);
     ctx->ovr_group = env_int("SV_GROUP", 0);
     ctx->ovr_threads = env_int("SV_THREADS", 0);
+    ctx->ovr_prefetch = env_int("SV_PREFETCH", -1);
     if (cudaMalloc(&ctx->d_err, sizeof(uint32_t)) != cudaSuccess ||
         cudaMemset(ctx->d_err, 0, sizeof(uint32_t)) != cudaSuccess) {
         (void)cudaGetLastError();
