@@ -77,8 +77,7 @@ struct SvArgs {
     int qvec;
     int prefetch_next;      // 1: L2-prefetch the next row slice while this one is processed
     float c_hi, c_lo;       // log2(e)/T = c_hi + c_lo with c_lo > 0
-    double c_d;             // log2(e)/T in double
-    double T_d;
+    float T;
     unsigned long long wait_ns;
 };
 
@@ -207,6 +206,36 @@ __device__ __forceinline__ float2 exp2_pair(float2 l, float2 neg_m, float2 chi, 
     const float2 d = __fadd2_rn(l, neg_m);
     const float2 y = __ffma2_rn(d, chi, __fmul2_rn(d, clo));
     return make_float2(ex2_approx(y.x), ex2_approx(y.y));
+}
+
+// 2^x for x <= 0 (x may be -inf) to about one ulp, on the FMA pipe: GB300's
+// double-precision units are far too slow for per-row use, and ex2.approx is
+// a little less accurate than this path needs for the few values it feeds
+// (merge weights and p(x)).  x = n + f with n = rint(x) and |f| <= 1/2;
+// 2^f = e^(f ln 2) by its Taylor series to degree 7 in (f ln 2), whose
+// truncation error on that interval is below 1e-8 relative; 2^n is applied
+// with ldexpf.
+__device__ __forceinline__ float exp2_accurate(float x) {
+    if (!(x > -160.f))
+        return 0.f;
+    const float n = rintf(x);
+    const float f = x - n;  // exact
+    // coefficients (ln 2)^k / k!, k = 7 .. 0
+    float p = 1.5252733804059840e-05f;
+    p = fmaf(p, f, 1.5403530393381606e-04f);
+    p = fmaf(p, f, 1.3333558146428443e-03f);
+    p = fmaf(p, f, 9.6181291076284772e-03f);
+    p = fmaf(p, f, 5.5504108664821580e-02f);
+    p = fmaf(p, f, 2.4022650695910071e-01f);
+    p = fmaf(p, f, 6.9314718055994531e-01f);
+    p = fmaf(p, f, 1.0f);
+    return ldexpf(p, (int)n);
+}
+
+// (l - m) * log2(e)/T with the split constant, for one value.
+__device__ __forceinline__ float exp2_arg(float l, float m, float c_hi, float c_lo) {
+    const float d = l - m;
+    return fmaf(d, c_hi, d * c_lo);
 }
 
 // ------------------------------------------------------------ elements -----
@@ -586,9 +615,15 @@ __global__ void __launch_bounds__(NT, 1536 / NT) sv_verify_kernel(const __grid_c
 #pragma unroll
                     for (int t = 0; t < kPer; ++t)
                         if (pv[t].y > 0.f)
-                            acc += (double)pv[t].y * exp2(((double)pv[t].x - (double)M) * a.c_d);
+                            acc += (double)pv[t].y *
+                                   (double)exp2_accurate(exp2_arg(pv[t].x, M, a.c_hi, a.c_lo));
                 }
                 const double S = warp_sum_bcast(acc);
+                // p(x) numerator 2^((l_x - M) log2e/T), on a lane of its own
+                float num = 0.f;
+                if (lane == 1 && finite && g0 + r < K)
+                    num = exp2_accurate(exp2_arg(sh.lx[g0 + r], M, a.c_hi, a.c_lo));
+                num = __shfl_sync(kFull, num, 1);
                 if (lane == 0 && sh.state == kStateRun) {
                     const int i = g0 + r;
                     if (anyflag) {
@@ -598,8 +633,9 @@ __global__ void __launch_bounds__(NT, 1536 / NT) sv_verify_kernel(const __grid_c
                         sh.state = kStateError;
                         sh.code = SV_ERR_NONFINITE;
                     } else {
-                        sh.rs_m[i] = (float)((double)M / a.T_d);
-                        sh.rs_s[i] = (float)S;
+                        const float Sf = (float)S;
+                        sh.rs_m[i] = __fdiv_rn(M, a.T);
+                        sh.rs_s[i] = Sf;
                         sh.ndec = i + 1;
                         if (i < K) {
                             const float qxf = sh.qx[i];
@@ -607,9 +643,10 @@ __global__ void __launch_bounds__(NT, 1536 / NT) sv_verify_kernel(const __grid_c
                                 sh.state = kStateError;
                                 sh.code = SV_ERR_NONFINITE;
                             } else {
-                                const double px = exp2(((double)sh.lx[i] - (double)M) * a.c_d) / S;
-                                sh.pd[i] = (float)px;
-                                if (!((double)sh.u[i] * (double)qxf < px)) {
+                                sh.pd[i] = __fdiv_rn(num, Sf);
+                                // u < p(x)/q(x) as u * q(x) * S < 2^((l_x - M) log2e/T):
+                                // products only, in double
+                                if (!((double)sh.u[i] * (double)qxf * S < (double)num)) {
                                     sh.state = kStateSample;
                                     sh.j = i;
                                     sh.mode = kModeResidual;
@@ -647,7 +684,7 @@ __global__ void __launch_bounds__(NT, 1536 / NT) sv_verify_kernel(const __grid_c
         const unsigned char* buf = bufs + (size_t)(j - gcur) * a.rowbuf_bytes;
         const float* qrow = j < K ? a.q + ((int64_t)b * K + j) * V + v0 : nullptr;
         const float M = sh.rowM;
-        const float inv_s = (float)(1.0 / sh.rowS);
+        const float inv_s = __frcp_rn((float)sh.rowS);
         const double uK = (double)sh.u[K];
         const int ntiles = (nvec + NT - 1) / NT;
         int mode = sh.mode;
@@ -1004,14 +1041,14 @@ int launch(sv_ctx* ctx, const void* logits, int dtype, const float* q, const int
     args.bulk = plan.bulk_copy && aligned(logits, 16) ? 1 : 0;
     args.prefetch_next = plan.prefetch_next && args.bulk ? 1 : 0;
     args.qvec = (V % 4 == 0) && q && aligned(q, 16) ? 1 : 0;
-    args.T_d = (double)T;
-    args.c_d = 1.4426950408889634074 / args.T_d;  // log2(e) / T
+    args.T = T;
+    const double c_d = 1.4426950408889634074 / (double)T;  // log2(e) / T
     // c_hi just below c_d so that c_lo = c_d - c_hi is strictly positive: a
     // -inf logit then gives -inf * c_lo = -inf instead of NaN
-    args.c_hi = (float)args.c_d;
-    if ((double)args.c_hi >= args.c_d)
+    args.c_hi = (float)c_d;
+    if ((double)args.c_hi >= c_d)
         args.c_hi = std::nextafter(args.c_hi, 0.0f);
-    args.c_lo = (float)(args.c_d - (double)args.c_hi);
+    args.c_lo = (float)(c_d - (double)args.c_hi);
     args.wait_ns = ctx->wait_ns;
 
     cudaLaunchConfig_t cfg;
