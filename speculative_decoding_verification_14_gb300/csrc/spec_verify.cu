@@ -84,11 +84,15 @@ struct SvArgs {
 // Fixed shared state of one CTA.  samp_* is read by the other CTAs of the
 // cluster through distributed shared memory (so are the per-warp partials,
 // which live after this struct).
+struct FF {  // hi + lo, see the double-float helpers below
+    float hi, lo;
+};
+
 struct __align__(16) SvShared {
     unsigned long long mbar;
-    double samp_tot[2];
+    FF samp_tot[2];
     int samp_bad[2];
-    double wtot[kMaxWarps];
+    FF wtot[kMaxWarps];
     int x[kMaxK];
     float u[kMaxRows];
     float lx[kMaxK];
@@ -98,7 +102,7 @@ struct __align__(16) SvShared {
     float pd[kMaxK];
     int state, j, code, ndec, mode, tok, owner, take_last, loc_tile, loc_warp;
     float rowM;
-    double rowS, loc_rem;
+    FF rowS, loc_rem;
 };
 static_assert(sizeof(SvShared) + 64 <= sv::kFixedSmem, "fixed shared state outgrew its reservation");
 
@@ -208,18 +212,85 @@ __device__ __forceinline__ float2 exp2_pair(float2 l, float2 neg_m, float2 chi, 
     return make_float2(ex2_approx(y.x), ex2_approx(y.y));
 }
 
-// 2^x for x <= 0 (x may be -inf) to about one ulp, on the FMA pipe: GB300's
-// double-precision units are far too slow for per-row use, and ex2.approx is
-// a little less accurate than this path needs for the few values it feeds
-// (merge weights and p(x)).  x = n + f with n = rint(x) and |f| <= 1/2;
-// 2^f = e^(f ln 2) by its Taylor series to degree 7 in (f ln 2), whose
-// truncation error on that interval is below 1e-8 relative; 2^n is applied
-// with ldexpf.
-__device__ __forceinline__ float exp2_accurate(float x) {
-    if (!(x > -160.f))
+// ------------------------------------------ double-float (fp32 pairs) -----
+// A value hi + lo with |lo| <= ulp(hi)/2, built from exact fp32
+// transformations (two-sum, two-product): about 44 significant bits, enough
+// for every running total and threshold here, all on the FP32 pipe (GB300's
+// FP64 units are far too slow to use per row).
+
+__device__ __forceinline__ FF two_sum(float a, float b) {
+    const float s = a + b;
+    const float bb = s - a;
+    return {s, (a - (s - bb)) + (b - bb)};
+}
+
+__device__ __forceinline__ FF fast_two_sum(float a, float b) {  // needs |a| >= |b| or a == 0
+    const float s = a + b;
+    return {s, b - (s - a)};
+}
+
+__device__ __forceinline__ FF two_prod(float a, float b) {
+    const float p = a * b;
+    return {p, fmaf(a, b, -p)};
+}
+
+__device__ __forceinline__ FF ff_add(FF x, FF y) {
+    FF t = two_sum(x.hi, y.hi);
+    t.lo += x.lo + y.lo;
+    return fast_two_sum(t.hi, t.lo);
+}
+
+__device__ __forceinline__ FF ff_add(FF x, float y) {
+    FF t = two_sum(x.hi, y);
+    t.lo += x.lo;
+    return fast_two_sum(t.hi, t.lo);
+}
+
+__device__ __forceinline__ FF ff_neg(FF x) { return {-x.hi, -x.lo}; }
+
+__device__ __forceinline__ FF ff_mul(FF x, FF y) {
+    FF p = two_prod(x.hi, y.hi);
+    p.lo = fmaf(x.hi, y.lo, fmaf(x.lo, y.hi, p.lo));
+    return fast_two_sum(p.hi, p.lo);
+}
+
+// x > y for double-float values
+__device__ __forceinline__ bool ff_gt(FF x, FF y) {
+    const FF d = ff_add(x, ff_neg(y));
+    return d.hi > 0.f || (d.hi == 0.f && d.lo > 0.f);
+}
+
+__device__ __forceinline__ FF shfl_ff(FF v, int src) {
+    return {__shfl_sync(0xffffffffu, v.hi, src), __shfl_sync(0xffffffffu, v.lo, src)};
+}
+
+__device__ __forceinline__ FF shfl_up_ff(FF v, int d) {
+    return {__shfl_up_sync(0xffffffffu, v.hi, d), __shfl_up_sync(0xffffffffu, v.lo, d)};
+}
+
+__device__ __forceinline__ FF shfl_down_ff(FF v, int d) {
+    return {__shfl_down_sync(0xffffffffu, v.hi, d), __shfl_down_sync(0xffffffffu, v.lo, d)};
+}
+
+// (l - m) * log2(e)/T as hi + lo, with the difference and the product formed
+// exactly (two-sum, two-product).  Needs finite l and m.
+__device__ __forceinline__ FF exp2_arg_ff(float l, float m, float c_hi, float c_lo) {
+    const FF d = two_sum(l, -m);
+    FF p = two_prod(d.hi, c_hi);
+    p.lo = fmaf(d.hi, c_lo, fmaf(d.lo, c_hi, p.lo));
+    return fast_two_sum(p.hi, p.lo);
+}
+
+// 2^y for y = hi + lo <= 0 to about one ulp, on the FMA pipe (used for the
+// few values that must be accurate: merge weights and p(x)).  y = n + f with
+// n = rint(hi) and |f| <= 1/2 (lo folded into f); 2^f = e^(f ln 2) by its
+// Taylor series to degree 7 in (f ln 2), whose truncation error on that
+// interval is below 1e-8 relative; 2^n is applied with ldexpf.
+__device__ __forceinline__ float exp2_accurate(FF y) {
+    if (!(y.hi > -160.f))
         return 0.f;
-    const float n = rintf(x);
-    const float f = x - n;  // exact
+    const float n = rintf(y.hi);
+    const float f = (y.hi - n) + y.lo;
     // coefficients (ln 2)^k / k!, k = 7 .. 0
     float p = 1.5252733804059840e-05f;
     p = fmaf(p, f, 1.5403530393381606e-04f);
@@ -232,10 +303,11 @@ __device__ __forceinline__ float exp2_accurate(float x) {
     return ldexpf(p, (int)n);
 }
 
-// (l - m) * log2(e)/T with the split constant, for one value.
-__device__ __forceinline__ float exp2_arg(float l, float m, float c_hi, float c_lo) {
-    const float d = l - m;
-    return fmaf(d, c_hi, d * c_lo);
+// 2^((l - m) log2e/T) accurately; 0 for l = -inf.
+__device__ __forceinline__ float exp2_diff_accurate(float l, float m, float c_hi, float c_lo) {
+    if (!(l > -INFINITY))
+        return 0.f;
+    return exp2_accurate(exp2_arg_ff(l, m, c_hi, c_lo));
 }
 
 // ------------------------------------------------------------ elements -----
@@ -304,11 +376,11 @@ __device__ __forceinline__ float warp_sum_bcast(float v) {
     return __shfl_sync(kFull, v, 0);
 }
 
-__device__ __forceinline__ double warp_sum_bcast(double v) {
+__device__ __forceinline__ FF warp_sum_bcast(FF v) {
 #pragma unroll
     for (int o = 16; o; o >>= 1)
-        v += __shfl_down_sync(kFull, v, o);
-    return __shfl_sync(kFull, v, 0);
+        v = ff_add(v, shfl_down_ff(v, o));
+    return shfl_ff(v, 0);
 }
 
 __device__ __forceinline__ float warp_incl_scan(float v) {
@@ -322,27 +394,32 @@ __device__ __forceinline__ float warp_incl_scan(float v) {
     return v;
 }
 
-__device__ __forceinline__ double warp_incl_scan(double v) {
+__device__ __forceinline__ FF warp_incl_scan(FF v) {
     const int lane = threadIdx.x & 31;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const double n = __shfl_up_sync(kFull, v, o);
+        const FF n = shfl_up_ff(v, o);
         if (lane >= o)
-            v += n;
+            v = ff_add(v, n);
     }
     return v;
+}
+
+// Exclusive prefix from an inclusive scan: the previous lane's value, `first` in lane 0.
+__device__ __forceinline__ FF warp_excl_from_incl(FF incl, FF first) {
+    const FF prev = shfl_up_ff(incl, 1);
+    return (threadIdx.x & 31) ? prev : first;
 }
 
 // First lane whose inclusive running total exceeds `rem`; when none does (a
 // rounding corner), the last lane with a positive part and take_last = 1.
 // Lanes beyond `n` must hold part = 0.  Returns -1 only if every part is 0.
-__device__ __forceinline__ int pick_lane(double part, double incl, double rem, int n,
-                                         int& take_last) {
+__device__ __forceinline__ int pick_lane(float part, FF incl, FF rem, int n, int& take_last) {
     const int lane = threadIdx.x & 31;
-    const unsigned cross = __ballot_sync(kFull, lane < n && !take_last && incl > rem);
+    const unsigned cross = __ballot_sync(kFull, lane < n && !take_last && ff_gt(incl, rem));
     if (cross)
         return __ffs(cross) - 1;
-    const unsigned pos = __ballot_sync(kFull, lane < n && part > 0.0);
+    const unsigned pos = __ballot_sync(kFull, lane < n && part > 0.f);
     take_last = 1;
     return pos ? 31 - __clz(pos) : -1;
 }
@@ -610,19 +687,19 @@ __global__ void __launch_bounds__(NT, 1536 / NT) sv_verify_kernel(const __grid_c
                 }
                 const float M = warp_max_nan(mloc);
                 const bool finite = M > -INFINITY && M < INFINITY;
-                double acc = 0.0;
+                FF acc = {0.f, 0.f};
                 if (finite) {
 #pragma unroll
                     for (int t = 0; t < kPer; ++t)
                         if (pv[t].y > 0.f)
-                            acc += (double)pv[t].y *
-                                   (double)exp2_accurate(exp2_arg(pv[t].x, M, a.c_hi, a.c_lo));
+                            acc = ff_add(acc, two_prod(pv[t].y, exp2_diff_accurate(
+                                                                    pv[t].x, M, a.c_hi, a.c_lo)));
                 }
-                const double S = warp_sum_bcast(acc);
+                const FF S = warp_sum_bcast(acc);
                 // p(x) numerator 2^((l_x - M) log2e/T), on a lane of its own
                 float num = 0.f;
                 if (lane == 1 && finite && g0 + r < K)
-                    num = exp2_accurate(exp2_arg(sh.lx[g0 + r], M, a.c_hi, a.c_lo));
+                    num = exp2_diff_accurate(sh.lx[g0 + r], M, a.c_hi, a.c_lo);
                 num = __shfl_sync(kFull, num, 1);
                 if (lane == 0 && sh.state == kStateRun) {
                     const int i = g0 + r;
@@ -633,7 +710,7 @@ __global__ void __launch_bounds__(NT, 1536 / NT) sv_verify_kernel(const __grid_c
                         sh.state = kStateError;
                         sh.code = SV_ERR_NONFINITE;
                     } else {
-                        const float Sf = (float)S;
+                        const float Sf = S.hi;
                         sh.rs_m[i] = __fdiv_rn(M, a.T);
                         sh.rs_s[i] = Sf;
                         sh.ndec = i + 1;
@@ -645,8 +722,9 @@ __global__ void __launch_bounds__(NT, 1536 / NT) sv_verify_kernel(const __grid_c
                             } else {
                                 sh.pd[i] = __fdiv_rn(num, Sf);
                                 // u < p(x)/q(x) as u * q(x) * S < 2^((l_x - M) log2e/T):
-                                // products only, in double
-                                if (!((double)sh.u[i] * (double)qxf * S < (double)num)) {
+                                // products only, in double-float
+                                const FF lhs = ff_mul(two_prod(sh.u[i], qxf), S);
+                                if (!ff_gt(FF{num, 0.f}, lhs)) {
                                     sh.state = kStateSample;
                                     sh.j = i;
                                     sh.mode = kModeResidual;
@@ -684,14 +762,14 @@ __global__ void __launch_bounds__(NT, 1536 / NT) sv_verify_kernel(const __grid_c
         const unsigned char* buf = bufs + (size_t)(j - gcur) * a.rowbuf_bytes;
         const float* qrow = j < K ? a.q + ((int64_t)b * K + j) * V + v0 : nullptr;
         const float M = sh.rowM;
-        const float inv_s = __frcp_rn((float)sh.rowS);
-        const double uK = (double)sh.u[K];
+        const float inv_s = __frcp_rn(sh.rowS.hi);
+        const float uK = sh.u[K];
         const int ntiles = (nvec + NT - 1) / NT;
         int mode = sh.mode;
         int sp = 0;
         for (int round = 0; round < 2; ++round) {
             bool bad = false;
-            double wacc = 0.0;  // this warp's total over all tiles (meaningful in lane 31)
+            FF wacc = {0.f, 0.f};  // this warp's total over all tiles (meaningful in lane 31)
             for (int k = 0; k < ntiles; k += 2) {
                 // two tiles in flight: both q loads go out before either is used
                 const int vi0 = k * NT + tid, vi1 = vi0 + NT;
@@ -715,10 +793,10 @@ __global__ void __launch_bounds__(NT, 1536 / NT) sv_verify_kernel(const __grid_c
                 const float in1 = warp_incl_scan(ts1);
                 if (lane == 31) {
                     wt[k * NW + warp] = in0;
-                    wacc += (double)in0;
+                    wacc = ff_add(wacc, in0);
                     if (k + 1 < ntiles) {
                         wt[(k + 1) * NW + warp] = in1;
-                        wacc += (double)in1;
+                        wacc = ff_add(wacc, in1);
                     }
                 }
             }
@@ -726,15 +804,15 @@ __global__ void __launch_bounds__(NT, 1536 / NT) sv_verify_kernel(const __grid_c
                 sh.wtot[warp] = wacc;
             const int anybad = __syncthreads_or(bad);
             if (tid == 0) {
-                double tot = 0.0;
+                FF tot = {0.f, 0.f};
                 for (int w2 = 0; w2 < NW; ++w2)
-                    tot += sh.wtot[w2];
+                    tot = ff_add(tot, sh.wtot[w2]);
                 sh.samp_tot[sp] = tot;
                 sh.samp_bad[sp] = anybad;
             }
             cluster.sync();
             if (warp == 0) {
-                double tot = 0.0;
+                FF tot = {0.f, 0.f};
                 int cbad = 0;
                 if (lane < C) {
                     const SvShared* rs = cluster.map_shared_rank(&sh, lane);
@@ -742,21 +820,18 @@ __global__ void __launch_bounds__(NT, 1536 / NT) sv_verify_kernel(const __grid_c
                     cbad = rs->samp_bad[sp];
                 }
                 cbad = __any_sync(kFull, cbad != 0);
-                const double incl = warp_incl_scan(tot);
-                const double S = __shfl_sync(kFull, incl, C - 1);
-                const double t = uK * S;
+                const FF incl = warp_incl_scan(tot);
+                const FF S = shfl_ff(incl, C - 1);
+                const FF t = ff_mul(FF{uK, 0.f}, S);
                 int take_last = 0;
-                const int owner = pick_lane(tot, incl, t, C, take_last);
-                double prev = __shfl_up_sync(kFull, incl, 1);
-                if (lane == 0)
-                    prev = 0.0;
-                const double excl = __shfl_sync(kFull, prev, owner < 0 ? 0 : owner);
+                const int owner = pick_lane(tot.hi, incl, t, C, take_last);
+                const FF excl = shfl_ff(warp_excl_from_incl(incl, FF{0.f, 0.f}), owner < 0 ? 0 : owner);
                 if (lane == 0) {
                     if (cbad) {
                         sh.state = kStateError;
                         sh.code = SV_ERR_NONFINITE;
                         sh.mode = -1;
-                    } else if (S == 0.0 && mode == kModeResidual) {
+                    } else if (S.hi == 0.f && mode == kModeResidual) {
                         // max(0, p - q) vanished (rounding or an unnormalised q):
                         // draw from p_j itself with the same uniform
                         sh.mode = kModeTargetRow;
@@ -769,7 +844,7 @@ __global__ void __launch_bounds__(NT, 1536 / NT) sv_verify_kernel(const __grid_c
                         sh.mode = -1;  // done
                         sh.owner = owner;
                         sh.take_last = take_last;
-                        sh.loc_rem = t - excl;
+                        sh.loc_rem = ff_add(t, ff_neg(excl));
                     }
                 }
             }
@@ -784,43 +859,45 @@ __global__ void __launch_bounds__(NT, 1536 / NT) sv_verify_kernel(const __grid_c
             // tile, then warp, by warp-parallel scans over the stored totals
             if (warp == 0) {
                 int take_last = sh.take_last;
-                double rem = sh.loc_rem;
+                const FF rem = sh.loc_rem;
                 int kk = -1, klast = -1;
-                double carry = 0.0, carry_last = 0.0, acc_at = 0.0;
+                FF carry = {0.f, 0.f}, carry_last = {0.f, 0.f}, acc_at = {0.f, 0.f};
                 for (int c0 = 0; c0 < ntiles && kk < 0; c0 += 32) {
                     const int k = c0 + lane;
-                    double tk = 0.0;
+                    FF tk = {0.f, 0.f};
                     if (k < ntiles)
                         for (int w2 = 0; w2 < NW; ++w2)
-                            tk += (double)wt[k * NW + w2];
-                    const double incl = warp_incl_scan(tk) + carry;
+                            tk = ff_add(tk, wt[k * NW + w2]);
+                    const FF incl = ff_add(warp_incl_scan(tk), carry);
+                    const FF excl = warp_excl_from_incl(incl, carry);
                     int tl = take_last;
-                    const int pick = pick_lane(tk, incl, rem, ntiles - c0, tl);
+                    const int pick = pick_lane(tk.hi, incl, rem, ntiles - c0, tl);
                     if (!tl && pick >= 0) {
                         kk = c0 + pick;
-                        acc_at = __shfl_sync(kFull, incl - tk, pick);
+                        acc_at = shfl_ff(excl, pick);
                     } else if (pick >= 0) {
                         klast = c0 + pick;
-                        carry_last = __shfl_sync(kFull, incl - tk, pick);
+                        carry_last = shfl_ff(excl, pick);
                     }
-                    carry = __shfl_sync(kFull, incl, 31);
+                    carry = shfl_ff(incl, 31);
                 }
                 if (kk < 0) {
                     take_last = 1;
                     kk = klast;
                     acc_at = carry_last;
                 }
-                double tw = 0.0;
+                float tw = 0.f;
                 if (kk >= 0 && lane < NW)
-                    tw = (double)wt[kk * NW + lane];
-                const double inclw = warp_incl_scan(tw);
-                const int ww = pick_lane(tw, inclw + acc_at, rem, NW, take_last);
-                const double accw = __shfl_sync(kFull, inclw - tw, ww < 0 ? 0 : ww);
+                    tw = wt[kk * NW + lane];
+                const FF inclw = ff_add(warp_incl_scan(FF{tw, 0.f}), acc_at);
+                const FF exclw = warp_excl_from_incl(inclw, acc_at);
+                const int ww = pick_lane(tw, inclw, rem, NW, take_last);
+                const FF accw = shfl_ff(exclw, ww < 0 ? 0 : ww);
                 if (lane == 0) {
                     sh.loc_tile = kk;
                     sh.loc_warp = ww;
                     sh.take_last = take_last;
-                    sh.loc_rem = rem - acc_at - accw;
+                    sh.loc_rem = ff_add(rem, ff_neg(accw));
                 }
             }
             __syncthreads();
@@ -828,7 +905,7 @@ __global__ void __launch_bounds__(NT, 1536 / NT) sv_verify_kernel(const __grid_c
                 // this warp re-derives the same weights and scan, then finds the
                 // lane and the entry where the running sum passes the remainder
                 int take_last = sh.take_last;
-                const double rem = sh.loc_rem;
+                const FF rem = sh.loc_rem;
                 const int vi = sh.loc_tile * NT + tid;
                 float qq[E], w[E];
 #pragma unroll
@@ -844,20 +921,20 @@ __global__ void __launch_bounds__(NT, 1536 / NT) sv_verify_kernel(const __grid_c
                     ts = vec_weights<ES>(buf, vi, L, qq, mode, M, a.c_hi, a.c_lo, inv_s, w, dummy);
                 }
                 const float incl = warp_incl_scan(ts);
-                const int pick = pick_lane((double)ts, (double)incl, rem, 32, take_last);
+                const int pick = pick_lane(ts, FF{incl, 0.f}, rem, 32, take_last);
                 float prev = __shfl_up_sync(kFull, incl, 1);
                 if (lane == 0)
                     prev = 0.f;
-                const double excl = (double)__shfl_sync(kFull, prev, pick < 0 ? 0 : pick);
+                const float excl = __shfl_sync(kFull, prev, pick < 0 ? 0 : pick);
                 if (lane == pick) {
                     int e_hit = -1, e_last = -1;
-                    double acc = excl;
+                    FF acc = {excl, 0.f};
 #pragma unroll
                     for (int e = 0; e < E; ++e) {
                         if (w[e] > 0.f)
                             e_last = e;
-                        acc += (double)w[e];
-                        if (e_hit < 0 && !take_last && acc > rem)
+                        acc = ff_add(acc, w[e]);
+                        if (e_hit < 0 && !take_last && ff_gt(acc, rem))
                             e_hit = e;
                     }
                     const int e = e_hit >= 0 ? e_hit : e_last;
