@@ -1,21 +1,28 @@
 // planner.cpp -- maps one batched verify onto thread-block clusters.
 //
 // Work unit: one sequence b (its K+1 target rows, K draft rows, K tokens and
-// K+1 uniforms) is verified by one cluster of C CTAs.  CTA r of the cluster
-// owns the vocabulary slice [r*slice, (r+1)*slice) of every row of b, so the
-// split-vocab partial softmax statistics of a row are combined inside the
-// cluster through distributed shared memory; no global workspace and no
-// second launch.
+// K+1 uniforms) is verified by one cluster of C CTAs.  CTA r owns the
+// vocabulary slice [r*slice, (r+1)*slice) of every row of b and each warp a
+// contiguous stretch of that slice, streamed through a small private ring of
+// shared memory; the partial softmax statistics of a row meet inside the
+// cluster through distributed shared memory.
 //
-// Rows are loaded `group` at a time.  group = 1 reads only the rows the test
-// loop reaches ([P1] "Speculative decoding: draft first, then verify": the
-// loop stops at the first rejection), which minimises HBM bytes; it is chosen
-// when the batch alone fills the GPU.  For small batches the pass is latency
-// bound, so all K+1 rows are loaded at once (group = K+1) and decided from one
-// cluster barrier.
+// Choice of C: the sequences' rows are consumed one after another (the test
+// loop of [P1] stops at the first rejection, so later rows are not read), so
+// a sequence is a chain of dependent steps and throughput comes from running
+// many sequences at once.  The planner takes the largest cluster that still
+// lets every sequence of the batch be resident at the same time (more CTAs per
+// sequence shorten each step), while keeping at least half a ring stage of
+// work per warp; batches too large to be resident get C = 1.
+//
+// Rows per step (group): 1 when the batch fills the GPU (only rows the loop
+// reaches are read; the first chunks of the next row are prefetched while a
+// row is decided); all K+1 for batches too small to fill it, where latency
+// rules and one barrier decides every row.
 //
 // [P1] = reactapp.top, "Speculative decoding and early exit: speeding up
-// autoregressive decode".
+// autoregressive decode", section "Speculative decoding: draft first, then
+// verify".
 #include "../../include/spec_verify.h"
 #include "sv_internal.h"
 
@@ -25,7 +32,7 @@ int plan_impl(int num_sms, int smem_per_cta, int max_cluster, int B, int K, int6
               int ovr_cluster, int ovr_group, int ovr_threads, sv_plan* out) {
     using namespace sv;
     if (!out || num_sms < 1 || smem_per_cta < 1 || max_cluster < 1 || B < 1 || K < 0 ||
-        K > kMaxK || V < 1 || (dtype != SV_F32 && dtype != SV_BF16))
+        K > kMaxK || V < 1 || V > ((int64_t)1 << 31) || (dtype != SV_F32 && dtype != SV_BF16))
         return SV_ERR_INVALID_ARG;
     if (ovr_cluster < 0 || ovr_cluster > kMaxCluster || ovr_group < 0 ||
         (ovr_threads != 0 && ovr_threads != 128 && ovr_threads != 256 && ovr_threads != 512))
@@ -33,52 +40,58 @@ int plan_impl(int num_sms, int smem_per_cta, int max_cluster, int B, int K, int6
     if (ovr_cluster > max_cluster)
         return SV_ERR_UNSUPPORTED;
     const int es = dtype == SV_BF16 ? 2 : 4;
+    const int E = 16 / es;
     const int rows = K + 1;
+    const int threads = ovr_threads ? ovr_threads : 128;
+    const int nw = threads / 32;
     const int cmax = max_cluster < kMaxCluster ? max_cluster : kMaxCluster;
-    const int threads = ovr_threads ? ovr_threads : 256;
+    const int64_t min_slice = (int64_t)nw * (kChunkBytes / 16) * E / 2;  // half a stage per warp
+
+    // resident CTAs per SM with a single-row plan (threads and shared memory)
+    const int64_t smem1 = layout_for(round_up(ceil_div(V, 4), kSliceAlign), es, 1, threads).total;
+    int64_t per_sm = (int64_t)kSmemPerSM / (smem1 + kSmemPerCtaReserved);
+    const int64_t by_threads = 1024 / threads;  // the kernels' launch bounds
+    if (per_sm > by_threads)
+        per_sm = by_threads;
+    if (per_sm < 1)
+        per_sm = 1;
+    const int64_t capacity = per_sm * num_sms;
 
     int C;
     if (ovr_cluster) {
         C = ovr_cluster;
     } else {
-        // big clusters when the batch is small, so that a sequence's rows are
-        // spread over many SMs; 8 (the portable size) otherwise
-        C = (int64_t)B * 8 < 2 * (int64_t)num_sms ? 16 : 8;
-        if (C > cmax)
-            C = cmax;
-        while (C > 1 && ceil_div(V, C) < kMinSlice)
-            C /= 2;
+        C = 1;
+        for (int c = cmax >= 16 ? 16 : cmax; c >= 1; c /= 2) {
+            if ((int64_t)B * c <= capacity && (c == 1 || ceil_div(V, c) >= min_slice)) {
+                C = c;
+                break;
+            }
+        }
     }
     int G;
     if (ovr_group)
         G = ovr_group < rows ? ovr_group : rows;
     else
-        G = (int64_t)B * C >= 2 * (int64_t)num_sms ? 1 : rows;
+        G = (int64_t)B * C >= num_sms ? 1 : rows;
 
-    for (;;) {
-        const int64_t slice = round_up(ceil_div(V, C), kSliceAlign);
-        int64_t smem = smem_bytes_for(slice, es, G, threads);
-        while (smem > smem_per_cta && G > 1 && !ovr_group) {
-            G = (G + 1) / 2;
-            smem = smem_bytes_for(slice, es, G, threads);
-        }
-        if (smem <= smem_per_cta) {
-            out->cluster = C;
-            out->group = G;
-            out->threads = threads;
-            out->smem_bytes = (int)smem;
-            out->slice = slice;
-            out->grid = (int64_t)B * C;
-            out->bulk_copy = ((V * es) % 16) == 0 ? 1 : 0;
-            out->prefetch_next = 0;
-            return SV_OK;
-        }
-        if (ovr_cluster || C >= cmax)
-            return SV_ERR_UNSUPPORTED;
-        C *= 2;
-        if (C > cmax)
-            C = cmax;
+    const int64_t slice = round_up(ceil_div(V, C), kSliceAlign);
+    Layout l = layout_for(slice, es, G, threads);
+    while (l.total > smem_per_cta && G > 1 && !ovr_group) {
+        G = (G + 1) / 2;
+        l = layout_for(slice, es, G, threads);
     }
+    if (l.total > smem_per_cta)
+        return SV_ERR_UNSUPPORTED;
+    out->cluster = C;
+    out->group = G;
+    out->threads = threads;
+    out->smem_bytes = (int)l.total;
+    out->slice = slice;
+    out->grid = (int64_t)B * C;
+    out->bulk_copy = ((V * es) % 16) == 0 ? 1 : 0;
+    out->prefetch_next = G == 1 ? 1 : 0;
+    return SV_OK;
 }
 
 }  // namespace

@@ -13,25 +13,27 @@
 //       speeds up LLM inference without hurting accuracy", section "How it
 //       works in practice": accepted length in [1, 1 + D].
 //
-// Design (one launch per call, no global workspace besides a 4-byte error word):
+// Design (one launch per call; no global workspace besides a 4-byte error word):
 //  * one thread-block cluster of C CTAs per sequence; CTA r owns a contiguous
-//    vocabulary slice of every row of that sequence;
-//  * a row slice moves HBM -> shared memory with one cp.async.bulk (the TMA
-//    bulk-copy engine) completing on an mbarrier; each warp reduces the
-//    vectors it owns to a (max, sum of exponentials) pair with packed f32x2
-//    arithmetic and publishes it -- no CTA-wide barrier inside a row step;
-//  * after one cluster barrier, warp 0 of every CTA reads the C x warps
-//    partial pairs through distributed shared memory and merges them in a
-//    fixed order in double precision, so every CTA reaches the same
-//    accept/reject decision without a broadcast;
+//    vocabulary slice of every row, and each warp of the CTA owns a contiguous
+//    stretch of that slice;
+//  * every warp streams its stretch through a private ring of shared-memory
+//    stages filled by cp.async.bulk (the TMA bulk-copy engine), each stage
+//    completing on its own mbarrier -- warps never wait for one another inside
+//    a row, and shared memory does not grow with the vocabulary;
+//  * lanes keep a running (max, sum of exponentials) with packed f32x2
+//    arithmetic; each warp publishes one partial per row;
+//  * after one cluster barrier, every warp reads the C x warps partials through
+//    distributed shared memory, merges them in a fixed order (double-float
+//    accumulation, accurate exp2) and takes the accept/reject decision itself,
+//    so no broadcast is needed;
 //  * rows are consumed in order and the loop stops at the first rejection,
-//    like the pages' loop, so rows after it are never read;
-//  * the residual (or bonus) draw is split across the cluster: the rejected
-//    draft row is bulk-prefetched into L2 as soon as the rejection is known,
-//    each CTA weighs its slice (logits still in shared memory), per-warp scans
-//    give tile and warp totals, the per-CTA totals meet in distributed shared
-//    memory, and the crossing is located by warp-parallel scans down to one
-//    entry in the owning CTA.
+//    like the pages' loop; the first chunks of the next row are already in
+//    flight while a row is decided;
+//  * the residual (or bonus) draw streams the rejected draft row through the
+//    same rings, records per-tile totals, meets the other CTAs' totals in
+//    distributed shared memory, and one warp of the owning CTA locates the
+//    token by warp-parallel scans.
 #include <cuda_runtime.h>
 #include <cooperative_groups.h>
 
@@ -49,9 +51,14 @@ namespace {
 
 using sv::kMaxK;
 using sv::kMaxRows;
+using sv::kStages;
+using sv::kChunkBytes;
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kMaxWarps = 16;
+constexpr int kChunkVecs = kChunkBytes / 16;  // 16-byte vectors per ring stage
+constexpr int kVecPerLane = kChunkVecs / 32;
+constexpr int kQChunk = kChunkBytes / 4;      // draft probabilities per ring stage
 constexpr int kStateRun = 0, kStateSample = 1, kStateError = 2;
 constexpr int kModeResidual = 0, kModeBonus = 1, kModeTargetRow = 2;
 
@@ -68,31 +75,30 @@ struct SvArgs {
     int32_t* status;
     uint32_t* err_word;
     int64_t V;
-    int64_t slice;
+    int64_t slice;          // vocabulary entries per CTA (multiple of 8)
     int B, K, C, G;
-    int rowbuf_bytes;
-    int part_offset;        // bytes from the fixed state to the per-warp partials
-    int wt_offset;          // bytes from the fixed state to the tile/warp totals
-    int bulk;
-    int qvec;
-    int prefetch_next;      // 1: L2-prefetch the next row slice while this one is processed
+    int wvec;               // 16-byte vectors per warp stretch
+    int ntw;                // draw tiles per warp stretch (capacity of the tile-total table)
+    int off_fixed, off_bar, off_part, off_tt;  // shared-memory layout
+    int bulk;               // 1: rows move with cp.async.bulk (16-byte aligned rows)
+    int qvec;               // 1: draft rows move with cp.async.bulk as well
+    int speculate;          // 1: first chunks of the next row are issued before the decision
     float c_hi, c_lo;       // log2(e)/T = c_hi + c_lo with c_lo > 0
     float T;
     unsigned long long wait_ns;
 };
 
-// Fixed shared state of one CTA.  samp_* is read by the other CTAs of the
-// cluster through distributed shared memory (so are the per-warp partials,
-// which live after this struct).
 struct FF {  // hi + lo, see the double-float helpers below
     float hi, lo;
 };
 
+// Fixed shared state of one CTA.  samp_* is read by the other CTAs of the
+// cluster through distributed shared memory (so are the per-warp partials).
 struct __align__(16) SvShared {
-    unsigned long long mbar;
     FF samp_tot[2];
     int samp_bad[2];
     FF wtot[kMaxWarps];
+    int wbad[kMaxWarps];
     int x[kMaxK];
     float u[kMaxRows];
     float lx[kMaxK];
@@ -100,9 +106,6 @@ struct __align__(16) SvShared {
     float rs_m[kMaxRows];
     float rs_s[kMaxRows];
     float pd[kMaxK];
-    int state, j, code, ndec, mode, tok, owner, take_last, loc_tile, loc_warp;
-    float rowM;
-    FF rowS, loc_rem;
 };
 static_assert(sizeof(SvShared) + 64 <= sv::kFixedSmem, "fixed shared state outgrew its reservation");
 
@@ -141,19 +144,16 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
         : "memory");
 }
 
-// Bulk prefetch of a global range into L2 (no destination, no completion).
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
+// One bounded poll: the waiting thread may be suspended (up to about 50 us)
+// until the phase completes, so waiting warps do not spin on issue slots.
 __device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(50000u)
         : "memory");
     return ok != 0;
 }
@@ -174,7 +174,7 @@ __device__ bool mbar_wait_bounded(unsigned long long* bar, uint32_t parity,
     for (uint32_t it = 0; it < (1u << 26); ++it) {
         if (mbar_try_wait(bar, parity))
             return true;
-        if ((it & 63u) == 0 && global_ns() - t0 > limit_ns)
+        if (global_ns() - t0 > limit_ns)
             return false;
     }
     return false;
@@ -190,6 +190,13 @@ __device__ __forceinline__ float ex2_approx(float x) {
 __device__ __forceinline__ float fmax_nan(float a, float b) {
     float d;
     asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+    return d;
+}
+
+// min that returns NaN when either input is NaN
+__device__ __forceinline__ float fmin_nan(float a, float b) {
+    float d;
+    asm("min.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
     return d;
 }
 
@@ -356,6 +363,10 @@ struct Elem<2> {
     __device__ static __forceinline__ uint32_t load_raw(const void* base, int64_t idx) {
         return __ldg(static_cast<const unsigned short*>(base) + idx);
     }
+    __device__ static __forceinline__ float vec_max(const uint4 w, float m) {
+        const uint32_t p = bf16x2_max_nan(bf16x2_max_nan(w.x, w.y), bf16x2_max_nan(w.z, w.w));
+        return fmax_nan(m, fmax_nan(bf16_lo(p), bf16_hi(p)));
+    }
 };
 
 // ------------------------------------------------------- warp helpers -----
@@ -367,8 +378,8 @@ __device__ __forceinline__ float warp_max_nan(float v) {
     return v;
 }
 
-// Sum over the warp, result in every lane (reduced in one fixed order, then
-// broadcast from lane 0 so that all lanes hold the same bits).
+// Sums over the warp, reduced in one fixed order and broadcast from lane 0 so
+// that every lane (and every warp doing the same reduction) holds the same bits.
 __device__ __forceinline__ float warp_sum_bcast(float v) {
 #pragma unroll
     for (int o = 16; o; o >>= 1)
@@ -413,7 +424,7 @@ __device__ __forceinline__ FF warp_excl_from_incl(FF incl, FF first) {
 
 // First lane whose inclusive running total exceeds `rem`; when none does (a
 // rounding corner), the last lane with a positive part and take_last = 1.
-// Lanes beyond `n` must hold part = 0.  Returns -1 only if every part is 0.
+// Only lanes below `n` take part.  Returns -1 only if every part is 0.
 __device__ __forceinline__ int pick_lane(float part, FF incl, FF rem, int n, int& take_last) {
     const int lane = threadIdx.x & 31;
     const unsigned cross = __ballot_sync(kFull, lane < n && !take_last && ff_gt(incl, rem));
@@ -424,104 +435,97 @@ __device__ __forceinline__ int pick_lane(float part, FF incl, FF rem, int n, int
     return pos ? 31 - __clz(pos) : -1;
 }
 
-// Per-warp (max, sum of exponentials relative to that max) over the vectors of
-// one staged row slice this warp owns (vectors warp*32 + lane + k*NT).  The
-// same value is returned in every lane.
-template <int ES, int NT>
-__device__ __forceinline__ float2 warp_slice_stats(const unsigned char* buf, int nvec, float c_hi,
-                                                   float c_lo) {
+// One 16-byte vector of the slice from global memory with element loads,
+// entries at or past `lim` reading as -inf (used when rows are not 16-byte
+// aligned).
+template <int ES>
+__device__ __forceinline__ uint4 load_vec_elems(const void* logits, int64_t gbase, int64_t e,
+                                                int64_t lim) {
     constexpr int E = Elem<ES>::E;
-    const int tid = threadIdx.x;
-    const uint4* vbuf = reinterpret_cast<const uint4*>(buf);
-    float m;
-    if constexpr (ES == 2) {
-        uint32_t acc = 0xff80ff80u;
-        for (int vi = tid; vi < nvec; vi += NT) {
-            const uint4 w = vbuf[vi];
-            acc = bf16x2_max_nan(bf16x2_max_nan(acc, w.x), bf16x2_max_nan(w.y, w.z));
-            acc = bf16x2_max_nan(acc, w.w);
+    uint32_t r[E];
+#pragma unroll
+    for (int k = 0; k < E; ++k)
+        r[k] = e + k < lim ? Elem<ES>::load_raw(logits, gbase + e + k) : Elem<ES>::kNegInf;
+    if constexpr (ES == 4)
+        return make_uint4(r[0], r[1], r[2], r[3]);
+    else
+        return make_uint4(r[0] | (r[1] << 16), r[2] | (r[3] << 16), r[4] | (r[5] << 16),
+                          r[6] | (r[7] << 16));
+}
+
+// Folds this lane's vectors of one chunk (vector k*32 + lane of `buf`, for
+// k*32 + lane < nv) into the lane's running (max, sum of 2^((l - max)
+// log2e/T)): a max pass, one rescale if the max moved, then a sum pass, with
+// one vector live at a time.  mchk collects the NaN-propagating max so that a
+// NaN or +inf anywhere poisons the row.
+template <int ES, typename Src>
+__device__ __forceinline__ void lane_fold(const Src& src, int nv, float& m, float& s, float& mchk,
+                                          float c_hi, float c_lo) {
+    constexpr int E = Elem<ES>::E;
+    const int lane = threadIdx.x & 31;
+    float cm = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < kVecPerLane; ++k)
+        if (k * 32 + lane < nv)
+            cm = Elem<ES>::vec_max(src(k * 32 + lane), cm);
+    mchk = fmax_nan(mchk, cm);
+    if (cm > m) {  // a new running max: rescale what was summed so far
+        if (s > 0.f) {
+            const float d = m - cm;
+            s *= ex2_approx(fmaf(d, c_hi, d * c_lo));
         }
-        m = fmax_nan(bf16_lo(acc), bf16_hi(acc));
-    } else {
-        m = -INFINITY;
-        for (int vi = tid; vi < nvec; vi += NT)
-            m = Elem<4>::vec_max(vbuf[vi], m);
+        m = cm;
     }
-    m = warp_max_nan(m);
-    float s = 0.f;
-    if (m > -INFINITY && m < INFINITY) {  // uniform within the warp
+    if (m > -INFINITY && m < INFINITY) {
         const float2 neg_m = make_float2(-m, -m), chi = make_float2(c_hi, c_hi),
                      clo = make_float2(c_lo, c_lo);
         float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
-        for (int vi = tid; vi < nvec; vi += NT) {
-            float2 f[E / 2];
-            Elem<ES>::unpack(vbuf[vi], f);
+#pragma unroll 1
+        for (int k = 0; k < kVecPerLane; ++k) {
+            if (k * 32 + lane < nv) {
+                float2 f[E / 2];
+                Elem<ES>::unpack(src(k * 32 + lane), f);
 #pragma unroll
-            for (int k = 0; k < E / 2; k += 2) {
-                a0 = __fadd2_rn(a0, exp2_pair(f[k], neg_m, chi, clo));
-                a1 = __fadd2_rn(a1, exp2_pair(f[k + 1], neg_m, chi, clo));
+                for (int h = 0; h < E / 2; h += 2) {
+                    a0 = __fadd2_rn(a0, exp2_pair(f[h], neg_m, chi, clo));
+                    a1 = __fadd2_rn(a1, exp2_pair(f[h + 1], neg_m, chi, clo));
+                }
             }
         }
-        s = warp_sum_bcast((a0.x + a0.y) + (a1.x + a1.y));
-    }
-    return make_float2(m, s);
-}
-
-// Draft probabilities for one 16-byte vector of the slice (E entries); entries
-// at or past L read as 0.
-template <int ES>
-__device__ __forceinline__ void load_q_vec(const float* qrow, int vi, int64_t L, int qvec,
-                                           float (&qq)[Elem<ES>::E]) {
-    constexpr int E = Elem<ES>::E;
-    const int64_t base = (int64_t)vi * E;
-    if (qvec && base + E <= L) {
-#pragma unroll
-        for (int k = 0; k < E; k += 4) {
-            const float4 t = __ldg(reinterpret_cast<const float4*>(qrow + base + k));
-            qq[k] = t.x;
-            qq[k + 1] = t.y;
-            qq[k + 2] = t.z;
-            qq[k + 3] = t.w;
-        }
-    } else {
-#pragma unroll
-        for (int k = 0; k < E; ++k)
-            qq[k] = base + k < L ? __ldg(qrow + base + k) : 0.f;
+        s += (a0.x + a0.y) + (a1.x + a1.y);
     }
 }
 
-// Draw weights of one vector: residual max(0, p - q) (mode 0) or the
+// Draw weights of E entries: residual max(0, p - q) (mode 0) or the
 // unnormalised target weights exp(z - max) (modes 1 and 2).  Entries at or
-// past L weigh 0.  `bad` is raised by a NaN, infinite or negative q value.
+// past `n` weigh 0.  q range checks fold into qmin (NaN-propagating) / qmax.
 template <int ES>
-__device__ __forceinline__ float vec_weights(const unsigned char* buf, int vi, int64_t L,
-                                             const float (&qq)[Elem<ES>::E], int mode, float M,
-                                             float c_hi, float c_lo, float inv_s,
-                                             float (&w)[Elem<ES>::E], bool& bad) {
+__device__ __forceinline__ float entry_weights(const float2 (&f)[Elem<ES>::E / 2],
+                                               const float (&qq)[Elem<ES>::E], int n, int mode,
+                                               float M, float c_hi, float c_lo, float inv_s,
+                                               float (&w)[Elem<ES>::E], float& qmin,
+                                               float& qmax) {
     constexpr int E = Elem<ES>::E;
-    float2 f[E / 2];
-    Elem<ES>::unpack(reinterpret_cast<const uint4*>(buf)[vi], f);
     const float2 neg_m = make_float2(-M, -M), chi = make_float2(c_hi, c_hi),
                  clo = make_float2(c_lo, c_lo);
-    const int64_t base = (int64_t)vi * E;
     float ts = 0.f;
 #pragma unroll
-    for (int k = 0; k < E / 2; ++k) {
-        const float2 e = exp2_pair(f[k], neg_m, chi, clo);
+    for (int h = 0; h < E / 2; ++h) {
+        const float2 e = exp2_pair(f[h], neg_m, chi, clo);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int idx = 2 * k + h;
-            const float ev = h ? e.y : e.x;
-            float wk;
+        for (int g = 0; g < 2; ++g) {
+            const int idx = 2 * h + g;
+            const float ev = g ? e.y : e.x;
+            float wk = ev;
             if (mode == kModeResidual) {
                 const float qv = qq[idx];
-                if (base + idx < L && !(qv >= 0.f && qv < INFINITY))
-                    bad = true;
+                if (idx < n) {
+                    qmin = fmin_nan(qmin, qv);
+                    qmax = fmaxf(qmax, qv);
+                }
                 wk = fmaxf(__fmaf_rn(ev, inv_s, -qv), 0.f);
-            } else {
-                wk = ev;
             }
-            w[idx] = base + idx < L ? wk : 0.f;
+            w[idx] = idx < n ? wk : 0.f;
             ts += w[idx];
         }
     }
@@ -530,12 +534,13 @@ __device__ __forceinline__ float vec_weights(const unsigned char* buf, int vi, i
 
 // --------------------------------------------------------------- kernel -----
 
-// Residency target: 1536 threads per SM (registers capped accordingly).
+// Residency target: 1024 threads per SM (registers capped accordingly).
 template <int ES, int NT>
-__global__ void __launch_bounds__(NT, 1536 / NT) sv_verify_kernel(const __grid_constant__ SvArgs a) {
+__global__ void __launch_bounds__(NT, 1024 / NT) sv_verify_kernel(const __grid_constant__ SvArgs a) {
     constexpr int E = Elem<ES>::E;
     constexpr int NW = NT / 32;
     static_assert(NW <= kMaxWarps, "too many warps");
+    constexpr int kPer = (sv::kMaxCluster * NW + 31) / 32;  // merge partials per lane, at most
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = (int)cluster.block_rank();
     const int b = (int)(blockIdx.x / (unsigned)a.C);
@@ -546,410 +551,445 @@ __global__ void __launch_bounds__(NT, 1536 / NT) sv_verify_kernel(const __grid_c
     const int G = a.G;
 
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    unsigned char* bufs = smem_raw;
-    unsigned char* fixed = smem_raw + (size_t)G * a.rowbuf_bytes;
-    SvShared& sh = *reinterpret_cast<SvShared*>(fixed);
-    float2* part = reinterpret_cast<float2*>(fixed + a.part_offset);  // [2][G][NW] (max, sum)
-    int* part_flag = reinterpret_cast<int*>(part + 2 * G * NW);       // [2][NW]
-    float* wt = reinterpret_cast<float*>(fixed + a.wt_offset);          // [tiles][NW]
+    SvShared& sh = *reinterpret_cast<SvShared*>(smem_raw + a.off_fixed);
+    unsigned long long* bar = reinterpret_cast<unsigned long long*>(smem_raw + a.off_bar);
+    float2* part = reinterpret_cast<float2*>(smem_raw + a.off_part);  // [2][G][NW] (max, sum)
+    float* tt = reinterpret_cast<float*>(smem_raw + a.off_tt);          // [NW][ntw] draw tile totals
+    unsigned char* ring = smem_raw + (size_t)warp * kStages * kChunkBytes;
+    unsigned long long* wbar = bar + warp * kStages;
 
-    // this CTA's vocabulary slice
+    // this CTA's slice and this warp's stretch of it (in 16-byte vectors)
     const int64_t v0 = (int64_t)rank * a.slice;
     const int64_t L = v0 < V ? (V - v0 < a.slice ? V - v0 : a.slice) : 0;
     const int nvec = (int)((L + E - 1) / E);
-    const int64_t row0 = (int64_t)b * (K + 1);  // first logits row of this sequence
+    const int wv0 = min(nvec, warp * a.wvec);
+    const int wv1 = min(nvec, wv0 + a.wvec);
+    const int wn = wv1 - wv0;
+    const int nch = (wn + kChunkVecs - 1) / kChunkVecs;  // ring chunks per row
+    const int64_t row0 = (int64_t)b * (K + 1);
 
-    if (tid == 0) {
-        mbar_init(&sh.mbar, 1);
+    if (lane == 0) {
+        for (int st = 0; st < kStages; ++st)
+            mbar_init(&wbar[st], 1);
         fence_mbar_init();
     }
-    __syncthreads();
-
-    uint32_t phase = 0;
-    bool timed_out = false;  // per thread; published per warp
-
-    auto row_src = [&](int row) {
-        return static_cast<const unsigned char*>(a.logits) + ((row0 + row) * V + v0) * ES;
-    };
-    // Moves rows g0 .. g0+ng-1 of this sequence's slice into shared memory.
-    auto load_group = [&](int g0, int ng) {
-        if (L == 0)
-            return;
-        if (a.bulk) {
-            if (tid == 0) {
-                fence_proxy_async();
-                const uint32_t bytes = (uint32_t)(L * ES);
-                mbar_arrive_expect_tx(&sh.mbar, bytes * (uint32_t)ng);
-                for (int r = 0; r < ng; ++r)
-                    bulk_copy_g2s(bufs + (size_t)r * a.rowbuf_bytes, row_src(g0 + r), bytes,
-                                  &sh.mbar);
-                if (a.prefetch_next)
-                    for (int r = g0 + ng; r < g0 + 2 * ng && r <= K; ++r)
-                        bulk_prefetch_l2(row_src(r), bytes);
-            }
-        } else {
-            const int64_t lpad = (int64_t)nvec * E;
-            for (int r = 0; r < ng; ++r) {
-                unsigned char* dst = bufs + (size_t)r * a.rowbuf_bytes;
-                const int64_t gbase = (row0 + g0 + r) * V + v0;
-                for (int64_t k = tid; k < lpad; k += NT)
-                    Elem<ES>::store_raw(dst, k,
-                                        k < L ? Elem<ES>::load_raw(a.logits, gbase + k)
-                                              : Elem<ES>::kNegInf);
-            }
-        }
-    };
-    auto wait_group = [&]() {
-        if (L == 0)
-            return;
-        if (a.bulk) {
-            if (!mbar_wait_bounded(&sh.mbar, phase, a.wait_ns))
-                timed_out = true;
-            phase ^= 1u;
-        } else {
-            __syncthreads();
-        }
-    };
-
-    // first group's copy goes out before anything else
-    load_group(0, G < K + 1 ? G : K + 1);
-
-    // per-sequence inputs: drafts, uniforms, and the gathered p/q inputs at the drafts
+    __syncwarp();
     if (tid < K)
         sh.x[tid] = a.tokens[(int64_t)b * K + tid];
     if (tid <= K)
         sh.u[tid] = a.u[(int64_t)b * (K + 1) + tid];
     __syncthreads();
-    if (tid == 0) {
-        int code = SV_OK;
-        for (int i = 0; i < K && code == SV_OK; ++i)
-            if (sh.x[i] < 0 || (int64_t)sh.x[i] >= V)
-                code = SV_ERR_TOKEN_RANGE;
-        for (int i = 0; i <= K && code == SV_OK; ++i)
-            if (!(sh.u[i] >= 0.f && sh.u[i] < 1.f))
-                code = SV_ERR_UNIFORM_RANGE;
-        sh.code = code;
-        sh.state = code == SV_OK ? kStateRun : kStateError;
-        sh.ndec = 0;
-        sh.j = -1;
+
+    // ---- per-warp stream through the private ring ----
+    uint32_t gi = 0, gq = 0;  // chunks issued / consumed by this warp (same in all lanes)
+    bool timed_out = false;
+    auto issue = [&](const void* src, uint32_t bytes) {
+        if (lane == 0) {
+            const uint32_t st = gi % kStages;
+            fence_proxy_async();
+            mbar_arrive_expect_tx(&wbar[st], bytes);
+            bulk_copy_g2s(ring + st * kChunkBytes, src, bytes, &wbar[st]);
+        }
+        ++gi;
+    };
+    auto wait_next = [&]() -> const unsigned char* {
+        const uint32_t st = gq % kStages;
+        if (!mbar_wait_bounded(&wbar[st], (gq / kStages) & 1u, a.wait_ns))
+            timed_out = true;
+        return ring + st * kChunkBytes;
+    };
+    auto release = [&]() {
+        __syncwarp();
+        ++gq;
+    };
+    auto row_chunk_src = [&](int row, int c) {
+        return static_cast<const unsigned char*>(a.logits) + ((row0 + row) * V + v0) * ES +
+               (size_t)(wv0 + c * kChunkVecs) * 16;
+    };
+    auto row_chunk_bytes = [&](int c) {
+        return (uint32_t)(min(kChunkVecs, wn - c * kChunkVecs) * 16);
+    };
+
+    // the first chunks of row 0 go out before the inputs are checked
+    int issued = 0;  // chunks of the current group already issued
+    if (a.bulk) {
+        const int t0 = (G < K + 1 ? G : K + 1) * nch;
+        while (issued < t0 && issued < kStages) {
+            issue(row_chunk_src(issued / nch, issued % nch), row_chunk_bytes(issued % nch));
+            ++issued;
+        }
     }
-    __syncthreads();
-    if (sh.state == kStateRun && tid < K) {
+
+    // ---- validation (every warp takes the same decision) ----
+    int state = kStateRun, code = SV_OK;
+    {
+        const bool bad_x = __any_sync(kFull, lane < K && (sh.x[lane] < 0 || (int64_t)sh.x[lane] >= V));
+        const float ul = lane <= K ? sh.u[lane] : 0.5f;
+        const float uh = (lane == 0 && K == kMaxK) ? sh.u[kMaxK] : 0.5f;
+        const bool bad_u = __any_sync(kFull, !(ul >= 0.f && ul < 1.f) || !(uh >= 0.f && uh < 1.f));
+        if (bad_x) {
+            state = kStateError;
+            code = SV_ERR_TOKEN_RANGE;
+        } else if (bad_u) {
+            state = kStateError;
+            code = SV_ERR_UNIFORM_RANGE;
+        }
+    }
+    if (state == kStateRun && tid < K) {
         const int x = sh.x[tid];
         sh.lx[tid] = Elem<ES>::load(a.logits, (row0 + tid) * V + x);
         sh.qx[tid] = __ldg(a.q + ((int64_t)b * K + tid) * V + x);
     }
-    // (made visible to warp 0 by the cluster barrier below)
+    // (visible to every warp after the first cluster barrier)
 
-    // ---- test loop over groups of rows, in order ([P1]) ----
-    int par = 0;
-    int g0 = 0;
-    int gcur = 0;  // first row of the group currently staged
-    for (;;) {
+    // ---- the test loop: groups of rows, in order ([P1]) ----
+    int j = -1, ndec = 0, mode = kModeBonus;
+    float rowM = 0.f;
+    FF rowS = {0.f, 0.f};
+    int par = 0, g0 = 0;
+    while (state == kStateRun) {
         const int ng = G < K + 1 - g0 ? G : K + 1 - g0;
-        wait_group();
-        gcur = g0;
-        if (sh.state != kStateRun)
-            break;
+        const int total = ng * nch;
+        int qi = 0;
         for (int r = 0; r < ng; ++r) {
-            const float2 ms = L ? warp_slice_stats<ES, NT>(bufs + (size_t)r * a.rowbuf_bytes, nvec,
-                                                           a.c_hi, a.c_lo)
-                                : make_float2(-INFINITY, 0.f);
+            float m = -INFINITY, s = 0.f, mchk = -INFINITY;
+            if (a.bulk) {
+                for (int c = 0; c < nch; ++c, ++qi) {
+                    while (issued < total && issued < qi + kStages) {
+                        issue(row_chunk_src(g0 + issued / nch, issued % nch),
+                              row_chunk_bytes(issued % nch));
+                        ++issued;
+                    }
+                    const uint4* buf = reinterpret_cast<const uint4*>(wait_next());
+                    const int nv = min(kChunkVecs, wn - c * kChunkVecs);
+                    lane_fold<ES>([&](int v) { return buf[v]; }, nv, m, s, mchk, a.c_hi, a.c_lo);
+                    release();
+                }
+            } else {
+                const int64_t gbase = (row0 + g0 + r) * V + v0;
+                for (int c = 0; c < nch; ++c) {
+                    const int nv = min(kChunkVecs, wn - c * kChunkVecs);
+                    const int64_t cv = (int64_t)wv0 + (int64_t)c * kChunkVecs;
+                    lane_fold<ES>([&](int v) { return load_vec_elems<ES>(a.logits, gbase, (cv + v) * E, L); },
+                                  nv, m, s, mchk, a.c_hi, a.c_lo);
+                }
+            }
+            // this warp's partial for row g0 + r
+            const float Mw = warp_max_nan(m);
+            const float chk = warp_max_nan(mchk);
+            FF sw = {0.f, 0.f};
+            if (s > 0.f && Mw > -INFINITY && Mw < INFINITY)
+                sw = two_prod(s, exp2_diff_accurate(m, Mw, a.c_hi, a.c_lo));
+            const FF Sw = warp_sum_bcast(sw);
+            const bool any_to = __any_sync(kFull, timed_out);
             if (lane == 0)
-                part[(par * G + r) * NW + warp] = ms;
+                part[(par * G + r) * NW + warp] =
+                    make_float2(chk > -INFINITY && chk < INFINITY ? Mw : chk,
+                                any_to ? -1.f : Sw.hi);
         }
-        {
-            const int anyto = __any_sync(kFull, timed_out);
-            if (lane == 0)
-                part_flag[par * NW + warp] = anyto;
+        // the first chunks of the next group go out before the decision
+        issued = 0;
+        const int g1 = g0 + ng;
+        const int ng1 = G < K + 1 - g1 ? G : K + 1 - g1;
+        if (a.bulk && a.speculate && g1 <= K) {
+            const int t1 = ng1 * nch;
+            while (issued < t1 && issued < kStages) {
+                issue(row_chunk_src(g1 + issued / nch, issued % nch), row_chunk_bytes(issued % nch));
+                ++issued;
+            }
         }
         cluster.sync();
 
-        // combine the C * NW partial pairs of each row in a fixed order, then decide
-        if (warp == 0) {
-            constexpr int kPer = sv::kMaxCluster * NW / 32;  // partials per lane, at most
-            const int P = C * NW;
-            int anyflag = 0;
-            for (int p = lane; p < P; p += 32)
-                anyflag |= cluster.map_shared_rank(part_flag, p / NW)[par * NW + (p % NW)];
-            anyflag = __any_sync(kFull, anyflag != 0);
-            for (int r = 0; r < ng; ++r) {
-                float2 pv[kPer];
-                float mloc = -INFINITY;
+        // every warp combines the C * NW partials of each row in a fixed order and decides
+        const int P = C * NW;
+        for (int r = 0; r < ng && state == kStateRun; ++r) {
+            const int i = g0 + r;
+            float2 pv[kPer];
+            float mloc = -INFINITY;
+            bool to = false;
 #pragma unroll
-                for (int t = 0; t < kPer; ++t) {
-                    const int p = lane + 32 * t;
-                    pv[t] = make_float2(-INFINITY, 0.f);
-                    if (p < P) {
-                        pv[t] = cluster.map_shared_rank(part, p / NW)[(par * G + r) * NW + (p % NW)];
-                        mloc = fmax_nan(mloc, pv[t].x);
-                    }
+            for (int t = 0; t < kPer; ++t) {
+                const int p = lane + 32 * t;
+                pv[t] = make_float2(-INFINITY, 0.f);
+                if (p < P) {
+                    pv[t] = cluster.map_shared_rank(part, p / NW)[(par * G + r) * NW + (p % NW)];
+                    mloc = fmax_nan(mloc, pv[t].x);
+                    to |= pv[t].y < 0.f;
                 }
-                const float M = warp_max_nan(mloc);
-                const bool finite = M > -INFINITY && M < INFINITY;
-                FF acc = {0.f, 0.f};
-                if (finite) {
+            }
+            const float M = warp_max_nan(mloc);
+            const bool finite = M > -INFINITY && M < INFINITY;
+            FF acc = {0.f, 0.f};
+            if (finite) {
 #pragma unroll
-                    for (int t = 0; t < kPer; ++t)
-                        if (pv[t].y > 0.f)
-                            acc = ff_add(acc, two_prod(pv[t].y, exp2_diff_accurate(
-                                                                    pv[t].x, M, a.c_hi, a.c_lo)));
+                for (int t = 0; t < kPer; ++t)
+                    if (pv[t].y > 0.f)
+                        acc = ff_add(acc, two_prod(pv[t].y, exp2_diff_accurate(pv[t].x, M, a.c_hi,
+                                                                                a.c_lo)));
+            }
+            const FF S = warp_sum_bcast(acc);
+            float num = 0.f;
+            if (lane == 1 && finite && i < K)
+                num = exp2_diff_accurate(sh.lx[i], M, a.c_hi, a.c_lo);
+            num = __shfl_sync(kFull, num, 1);
+            if (__any_sync(kFull, to)) {
+                state = kStateError;
+                code = SV_ERR_TIMEOUT;
+            } else if (!finite) {
+                state = kStateError;
+                code = SV_ERR_NONFINITE;
+            } else {
+                if (warp == 0 && lane == 0) {
+                    sh.rs_m[i] = __fdiv_rn(M, a.T);
+                    sh.rs_s[i] = S.hi;
                 }
-                const FF S = warp_sum_bcast(acc);
-                // p(x) numerator 2^((l_x - M) log2e/T), on a lane of its own
-                float num = 0.f;
-                if (lane == 1 && finite && g0 + r < K)
-                    num = exp2_diff_accurate(sh.lx[g0 + r], M, a.c_hi, a.c_lo);
-                num = __shfl_sync(kFull, num, 1);
-                if (lane == 0 && sh.state == kStateRun) {
-                    const int i = g0 + r;
-                    if (anyflag) {
-                        sh.state = kStateError;
-                        sh.code = SV_ERR_TIMEOUT;
-                    } else if (!finite) {
-                        sh.state = kStateError;
-                        sh.code = SV_ERR_NONFINITE;
+                ndec = i + 1;
+                if (i < K) {
+                    const float qxf = sh.qx[i];
+                    if (!(qxf >= 0.f && qxf < INFINITY)) {
+                        state = kStateError;
+                        code = SV_ERR_NONFINITE;
                     } else {
-                        const float Sf = S.hi;
-                        sh.rs_m[i] = __fdiv_rn(M, a.T);
-                        sh.rs_s[i] = Sf;
-                        sh.ndec = i + 1;
-                        if (i < K) {
-                            const float qxf = sh.qx[i];
-                            if (!(qxf >= 0.f && qxf < INFINITY)) {
-                                sh.state = kStateError;
-                                sh.code = SV_ERR_NONFINITE;
-                            } else {
-                                sh.pd[i] = __fdiv_rn(num, Sf);
-                                // u < p(x)/q(x) as u * q(x) * S < 2^((l_x - M) log2e/T):
-                                // products only, in double-float
-                                const FF lhs = ff_mul(two_prod(sh.u[i], qxf), S);
-                                if (!ff_gt(FF{num, 0.f}, lhs)) {
-                                    sh.state = kStateSample;
-                                    sh.j = i;
-                                    sh.mode = kModeResidual;
-                                    sh.rowM = M;
-                                    sh.rowS = S;
-                                    // the draft row is needed now: start pulling it into L2
-                                    if (a.qvec && L > 0)
-                                        bulk_prefetch_l2(a.q + ((int64_t)b * K + i) * V + v0,
-                                                         (uint32_t)(L * 4));
-                                }
-                            }
-                        } else {
-                            sh.state = kStateSample;
-                            sh.j = K;
-                            sh.mode = kModeBonus;
-                            sh.rowM = M;
-                            sh.rowS = S;
+                        if (warp == 0 && lane == 0)
+                            sh.pd[i] = __fdiv_rn(num, S.hi);
+                        // u < p(x)/q(x) as u * q(x) * S < 2^((l_x - M) log2e/T)
+                        const FF lhs = ff_mul(two_prod(sh.u[i], qxf), S);
+                        if (!ff_gt(FF{num, 0.f}, lhs)) {
+                            state = kStateSample;
+                            j = i;
+                            mode = kModeResidual;
+                            rowM = M;
+                            rowS = S;
                         }
                     }
+                } else {
+                    state = kStateSample;
+                    j = K;
+                    mode = kModeBonus;
+                    rowM = M;
+                    rowS = S;
                 }
-                __syncwarp();
             }
         }
-        __syncthreads();
         par ^= 1;
-        if (sh.state != kStateRun)
-            break;
-        g0 += ng;
-        load_group(g0, G < K + 1 - g0 ? G : K + 1 - g0);
+        g0 = g1;
+    }
+    // speculative chunks that will not be used: let them land before the ring is reused
+    while (gq < gi) {
+        (void)wait_next();
+        release();
     }
 
     // ---- corrected or bonus draw over row j ([P1]) ----
-    if (sh.state == kStateSample) {
-        const int j = sh.j;
-        const unsigned char* buf = bufs + (size_t)(j - gcur) * a.rowbuf_bytes;
-        const float* qrow = j < K ? a.q + ((int64_t)b * K + j) * V + v0 : nullptr;
-        const float M = sh.rowM;
-        const float inv_s = __frcp_rn(sh.rowS.hi);
-        const float uK = sh.u[K];
-        const int ntiles = (nvec + NT - 1) / NT;
-        int mode = sh.mode;
+    const int64_t e0 = (int64_t)wv0 * E;
+    const int64_t nq = max((int64_t)0, min((int64_t)wv1 * E, L) - e0);  // entries in this stretch
+    constexpr int kTile = 32 * E;
+    const int ntile = (int)((nq + kTile - 1) / kTile);
+    const unsigned char* lrow = nullptr;
+    const float* qrow = nullptr;
+    int owner = -1, take_last = 0;
+    FF rem = {0.f, 0.f};
+    if (state == kStateSample) {
+        lrow = static_cast<const unsigned char*>(a.logits) + ((row0 + j) * V + v0) * ES;
+        qrow = j < K ? a.q + ((int64_t)b * K + j) * V + v0 : nullptr;
+        const float inv_s = __frcp_rn(rowS.hi);
         int sp = 0;
         for (int round = 0; round < 2; ++round) {
-            bool bad = false;
-            FF wacc = {0.f, 0.f};  // this warp's total over all tiles (meaningful in lane 31)
-            for (int k = 0; k < ntiles; k += 2) {
-                // two tiles in flight: both q loads go out before either is used
-                const int vi0 = k * NT + tid, vi1 = vi0 + NT;
-                float q0[E], q1[E], w[E];
-#pragma unroll
-                for (int e = 0; e < E; ++e)
-                    q0[e] = q1[e] = 0.f;
-                if (mode == kModeResidual) {
-                    if (vi0 < nvec)
-                        load_q_vec<ES>(qrow, vi0, L, a.qvec, q0);
-                    if (vi1 < nvec)
-                        load_q_vec<ES>(qrow, vi1, L, a.qvec, q1);
+            const bool ring_q = mode == kModeResidual && a.qvec;
+            const int nqc = ring_q ? (int)((nq + kQChunk - 1) / kQChunk) : 0;
+            int qissued = 0, qdone = 0;
+            const float* qbuf = nullptr;
+            FF wacc = {0.f, 0.f};
+            float qmin = 0.f, qmax = 0.f;
+            for (int t = 0; t < ntile; ++t) {
+                const int64_t tb = (int64_t)t * kTile;  // first entry of the tile in the stretch
+                if (ring_q && tb % kQChunk == 0) {
+                    while (qissued < nqc && qissued < qdone + kStages) {
+                        const int64_t cb = (int64_t)qissued * kQChunk;
+                        issue(qrow + e0 + cb, (uint32_t)(min((int64_t)kQChunk, nq - cb) * 4));
+                        ++qissued;
+                    }
+                    qbuf = reinterpret_cast<const float*>(wait_next());
                 }
-                const float ts0 = vi0 < nvec ? vec_weights<ES>(buf, vi0, L, q0, mode, M, a.c_hi,
-                                                               a.c_lo, inv_s, w, bad)
-                                             : 0.f;
-                const float ts1 = vi1 < nvec ? vec_weights<ES>(buf, vi1, L, q1, mode, M, a.c_hi,
-                                                               a.c_lo, inv_s, w, bad)
-                                             : 0.f;
-                const float in0 = warp_incl_scan(ts0);
-                const float in1 = warp_incl_scan(ts1);
-                if (lane == 31) {
-                    wt[k * NW + warp] = in0;
-                    wacc = ff_add(wacc, in0);
-                    if (k + 1 < ntiles) {
-                        wt[(k + 1) * NW + warp] = in1;
-                        wacc = ff_add(wacc, in1);
+                const int64_t te = tb + lane * E;
+                const int n = (int)max((int64_t)0, min((int64_t)E, nq - te));
+                float2 f[E / 2];
+                if (a.bulk) {
+                    uint4 raw = make_uint4(0, 0, 0, 0);
+                    if (n > 0)
+                        raw = __ldg(reinterpret_cast<const uint4*>(lrow + (e0 + te) * ES));
+                    Elem<ES>::unpack(raw, f);
+                } else {
+                    Elem<ES>::unpack(load_vec_elems<ES>(a.logits, (row0 + j) * V + v0, e0 + te, e0 + nq), f);
+                }
+                float qq[E];
+#pragma unroll
+                for (int k = 0; k < E; ++k)
+                    qq[k] = 0.f;
+                if (mode == kModeResidual) {
+                    if (ring_q) {
+                        const float* qs = qbuf + (tb % kQChunk) + lane * E;
+#pragma unroll
+                        for (int k = 0; k < E; k += 4) {
+                            const float4 v4 = *reinterpret_cast<const float4*>(qs + k);
+                            qq[k] = v4.x;
+                            qq[k + 1] = v4.y;
+                            qq[k + 2] = v4.z;
+                            qq[k + 3] = v4.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < E; ++k)
+                            qq[k] = k < n ? __ldg(qrow + e0 + te + k) : 0.f;
                     }
                 }
+                float w[E];
+                const float ts = entry_weights<ES>(f, qq, n, mode, rowM, a.c_hi, a.c_lo, inv_s, w,
+                                                   qmin, qmax);
+                const float tot = warp_sum_bcast(ts);
+                if (lane == 0)
+                    tt[warp * a.ntw + t] = tot;
+                wacc = ff_add(wacc, tot);
+                if (ring_q && ((tb + kTile) % kQChunk == 0 || t == ntile - 1)) {
+                    release();
+                    ++qdone;
+                }
             }
-            if (lane == 31)
+            const bool badq = __any_sync(kFull, !(qmin >= 0.f) || !(qmax < INFINITY));
+            const bool to = __any_sync(kFull, timed_out);
+            if (lane == 0) {
                 sh.wtot[warp] = wacc;
-            const int anybad = __syncthreads_or(bad);
+                sh.wbad[warp] = to ? 2 : (badq ? 1 : 0);
+            }
+            __syncthreads();
             if (tid == 0) {
                 FF tot = {0.f, 0.f};
-                for (int w2 = 0; w2 < NW; ++w2)
+                int bad = 0;
+                for (int w2 = 0; w2 < NW; ++w2) {
                     tot = ff_add(tot, sh.wtot[w2]);
+                    bad = max(bad, sh.wbad[w2]);
+                }
                 sh.samp_tot[sp] = tot;
-                sh.samp_bad[sp] = anybad;
+                sh.samp_bad[sp] = bad;
             }
             cluster.sync();
-            if (warp == 0) {
-                FF tot = {0.f, 0.f};
-                int cbad = 0;
-                if (lane < C) {
-                    const SvShared* rs = cluster.map_shared_rank(&sh, lane);
-                    tot = rs->samp_tot[sp];
-                    cbad = rs->samp_bad[sp];
-                }
-                cbad = __any_sync(kFull, cbad != 0);
-                const FF incl = warp_incl_scan(tot);
-                const FF S = shfl_ff(incl, C - 1);
-                const FF t = ff_mul(FF{uK, 0.f}, S);
-                int take_last = 0;
-                const int owner = pick_lane(tot.hi, incl, t, C, take_last);
-                const FF excl = shfl_ff(warp_excl_from_incl(incl, FF{0.f, 0.f}), owner < 0 ? 0 : owner);
-                if (lane == 0) {
-                    if (cbad) {
-                        sh.state = kStateError;
-                        sh.code = SV_ERR_NONFINITE;
-                        sh.mode = -1;
-                    } else if (S.hi == 0.f && mode == kModeResidual) {
-                        // max(0, p - q) vanished (rounding or an unnormalised q):
-                        // draw from p_j itself with the same uniform
-                        sh.mode = kModeTargetRow;
-                    } else if (owner < 0) {
-                        // no positive weight anywhere: unreachable when the row max is finite
-                        sh.state = kStateError;
-                        sh.code = SV_ERR_NONFINITE;
-                        sh.mode = -1;
-                    } else {
-                        sh.mode = -1;  // done
-                        sh.owner = owner;
-                        sh.take_last = take_last;
-                        sh.loc_rem = ff_add(t, ff_neg(excl));
-                    }
-                }
+            FF ctot = {0.f, 0.f};
+            int cbad = 0;
+            if (lane < C) {
+                const SvShared* rs = cluster.map_shared_rank(&sh, lane);
+                ctot = rs->samp_tot[sp];
+                cbad = rs->samp_bad[sp];
             }
-            __syncthreads();
-            if (sh.mode != kModeTargetRow)
+#pragma unroll
+            for (int o = 16; o; o >>= 1)
+                cbad = max(cbad, __shfl_xor_sync(kFull, cbad, o));
+            const FF incl = warp_incl_scan(ctot);
+            const FF S = shfl_ff(incl, C - 1);
+            const FF thr = ff_mul(FF{sh.u[K], 0.f}, S);
+            take_last = 0;
+            owner = pick_lane(ctot.hi, incl, thr, C, take_last);
+            const FF excl = shfl_ff(warp_excl_from_incl(incl, FF{0.f, 0.f}), owner < 0 ? 0 : owner);
+            if (cbad) {
+                state = kStateError;
+                code = cbad == 2 ? SV_ERR_TIMEOUT : SV_ERR_NONFINITE;
                 break;
-            mode = kModeTargetRow;
-            sp ^= 1;
+            }
+            if (S.hi == 0.f && mode == kModeResidual) {
+                // max(0, p - q) vanished (rounding or an unnormalised q):
+                // draw from p_j itself with the same uniform
+                mode = kModeTargetRow;
+                sp ^= 1;
+                continue;
+            }
+            if (owner < 0) {  // no positive weight anywhere: unreachable for a finite row max
+                state = kStateError;
+                code = SV_ERR_NONFINITE;
+            }
+            rem = ff_add(thr, ff_neg(excl));
+            break;
         }
 
-        if (sh.state == kStateSample && rank == sh.owner) {
-            // tile, then warp, by warp-parallel scans over the stored totals
-            if (warp == 0) {
-                int take_last = sh.take_last;
-                const FF rem = sh.loc_rem;
-                int kk = -1, klast = -1;
-                FF carry = {0.f, 0.f}, carry_last = {0.f, 0.f}, acc_at = {0.f, 0.f};
-                for (int c0 = 0; c0 < ntiles && kk < 0; c0 += 32) {
-                    const int k = c0 + lane;
-                    FF tk = {0.f, 0.f};
-                    if (k < ntiles)
-                        for (int w2 = 0; w2 < NW; ++w2)
-                            tk = ff_add(tk, wt[k * NW + w2]);
-                    const FF incl = ff_add(warp_incl_scan(tk), carry);
-                    const FF excl = warp_excl_from_incl(incl, carry);
-                    int tl = take_last;
-                    const int pick = pick_lane(tk.hi, incl, rem, ntiles - c0, tl);
-                    if (!tl && pick >= 0) {
-                        kk = c0 + pick;
-                        acc_at = shfl_ff(excl, pick);
-                    } else if (pick >= 0) {
-                        klast = c0 + pick;
-                        carry_last = shfl_ff(excl, pick);
-                    }
-                    carry = shfl_ff(incl, 31);
+        if (state == kStateSample && rank == owner && warp == 0) {
+            // warp stretch, then tile, then lane and entry: warp-parallel scans
+            FF wtw = lane < NW ? sh.wtot[lane] : FF{0.f, 0.f};
+            const FF inw = warp_incl_scan(wtw);
+            const int ws = max(0, pick_lane(wtw.hi, inw, rem, NW, take_last));
+            rem = ff_add(rem, ff_neg(shfl_ff(warp_excl_from_incl(inw, FF{0.f, 0.f}), ws)));
+            const int wv0s = min(nvec, ws * a.wvec);
+            const int64_t e0s = (int64_t)wv0s * E;
+            const int64_t nqs = max((int64_t)0, min((int64_t)min(nvec, wv0s + a.wvec) * E, L) - e0s);
+            const int ntiles = (int)((nqs + kTile - 1) / kTile);
+            int tsel = -1, tlast = -1;
+            FF carry = {0.f, 0.f}, at_sel = {0.f, 0.f}, at_last = {0.f, 0.f};
+            for (int c0 = 0; c0 < ntiles && tsel < 0; c0 += 32) {
+                const float tv = c0 + lane < ntiles ? tt[ws * a.ntw + c0 + lane] : 0.f;
+                const FF in = ff_add(warp_incl_scan(FF{tv, 0.f}), carry);
+                const FF ex = warp_excl_from_incl(in, carry);
+                int tl = take_last;
+                const int pk = pick_lane(tv, in, rem, ntiles - c0, tl);
+                if (!tl && pk >= 0) {
+                    tsel = c0 + pk;
+                    at_sel = shfl_ff(ex, pk);
+                } else if (pk >= 0) {
+                    tlast = c0 + pk;
+                    at_last = shfl_ff(ex, pk);
                 }
-                if (kk < 0) {
-                    take_last = 1;
-                    kk = klast;
-                    acc_at = carry_last;
-                }
-                float tw = 0.f;
-                if (kk >= 0 && lane < NW)
-                    tw = wt[kk * NW + lane];
-                const FF inclw = ff_add(warp_incl_scan(FF{tw, 0.f}), acc_at);
-                const FF exclw = warp_excl_from_incl(inclw, acc_at);
-                const int ww = pick_lane(tw, inclw, rem, NW, take_last);
-                const FF accw = shfl_ff(exclw, ww < 0 ? 0 : ww);
-                if (lane == 0) {
-                    sh.loc_tile = kk;
-                    sh.loc_warp = ww;
-                    sh.take_last = take_last;
-                    sh.loc_rem = ff_add(rem, ff_neg(accw));
-                }
+                carry = shfl_ff(in, 31);
             }
-            __syncthreads();
-            if (warp == sh.loc_warp && sh.loc_tile >= 0) {
-                // this warp re-derives the same weights and scan, then finds the
-                // lane and the entry where the running sum passes the remainder
-                int take_last = sh.take_last;
-                const FF rem = sh.loc_rem;
-                const int vi = sh.loc_tile * NT + tid;
-                float qq[E], w[E];
+            if (tsel < 0) {
+                take_last = 1;
+                tsel = max(tlast, 0);
+                at_sel = at_last;
+            }
+            rem = ff_add(rem, ff_neg(at_sel));
+            // re-derive the tile's weights (the same arithmetic as the pass)
+            const int64_t te = (int64_t)tsel * kTile + lane * E;
+            const int n = (int)max((int64_t)0, min((int64_t)E, nqs - te));
+            float2 f[E / 2];
+            if (a.bulk) {
+                uint4 raw = make_uint4(0, 0, 0, 0);
+                if (n > 0)
+                    raw = __ldg(reinterpret_cast<const uint4*>(lrow + (e0s + te) * ES));
+                Elem<ES>::unpack(raw, f);
+            } else {
+                Elem<ES>::unpack(load_vec_elems<ES>(a.logits, (row0 + j) * V + v0, e0s + te, e0s + nqs), f);
+            }
+            float qq[E];
+#pragma unroll
+            for (int k = 0; k < E; ++k)
+                qq[k] = (mode == kModeResidual && k < n) ? __ldg(qrow + e0s + te + k) : 0.f;
+            float w[E], qmn = 0.f, qmx = 0.f;
+            const float ts = entry_weights<ES>(f, qq, n, mode, rowM, a.c_hi, a.c_lo,
+                                               __frcp_rn(rowS.hi), w, qmn, qmx);
+            const float inc = warp_incl_scan(ts);
+            const int pk = pick_lane(ts, FF{inc, 0.f}, rem, 32, take_last);
+            float prev = __shfl_up_sync(kFull, inc, 1);
+            if (lane == 0)
+                prev = 0.f;
+            const float ex = __shfl_sync(kFull, prev, pk < 0 ? 0 : pk);
+            int tok = -1;
+            if (lane == pk) {
+                int e_hit = -1, e_last = -1;
+                FF acc = {ex, 0.f};
 #pragma unroll
                 for (int e = 0; e < E; ++e) {
-                    qq[e] = 0.f;
-                    w[e] = 0.f;
+                    if (w[e] > 0.f)
+                        e_last = e;
+                    acc = ff_add(acc, w[e]);
+                    if (e_hit < 0 && !take_last && ff_gt(acc, rem))
+                        e_hit = e;
                 }
-                bool dummy = false;
-                float ts = 0.f;
-                if (vi < nvec) {
-                    if (mode == kModeResidual)
-                        load_q_vec<ES>(qrow, vi, L, a.qvec, qq);
-                    ts = vec_weights<ES>(buf, vi, L, qq, mode, M, a.c_hi, a.c_lo, inv_s, w, dummy);
-                }
-                const float incl = warp_incl_scan(ts);
-                const int pick = pick_lane(ts, FF{incl, 0.f}, rem, 32, take_last);
-                float prev = __shfl_up_sync(kFull, incl, 1);
-                if (lane == 0)
-                    prev = 0.f;
-                const float excl = __shfl_sync(kFull, prev, pick < 0 ? 0 : pick);
-                if (lane == pick) {
-                    int e_hit = -1, e_last = -1;
-                    FF acc = {excl, 0.f};
-#pragma unroll
-                    for (int e = 0; e < E; ++e) {
-                        if (w[e] > 0.f)
-                            e_last = e;
-                        acc = ff_add(acc, w[e]);
-                        if (e_hit < 0 && !take_last && ff_gt(acc, rem))
-                            e_hit = e;
-                    }
-                    const int e = e_hit >= 0 ? e_hit : e_last;
-                    sh.tok = (int)(v0 + (int64_t)vi * E + (e >= 0 ? e : 0));
-                }
+                const int e = e_hit >= 0 ? e_hit : e_last;
+                tok = (int)(v0 + e0s + te + (e >= 0 ? e : 0));
             }
-            __syncthreads();
+            tok = __shfl_sync(kFull, tok, pk < 0 ? 0 : pk);
             // outputs of a finished sequence
-            const int tok = sh.tok;
-            for (int i = tid; i <= K; i += NT) {
+            for (int i = lane; i <= K; i += 32) {
                 a.out_tokens[(int64_t)b * (K + 1) + i] = i < j ? sh.x[i] : (i == j ? tok : -1);
                 if (i < K)
                     a.accept_mask[(int64_t)b * K + i] = i < j ? 1 : 0;
             }
-            if (tid == 0) {
+            if (lane == 0) {
                 a.accept_len[b] = j + 1;
                 if (a.status)
                     a.status[b] = SV_OK;
@@ -958,33 +998,35 @@ __global__ void __launch_bounds__(NT, 1536 / NT) sv_verify_kernel(const __grid_c
     }
 
     // ---- rank 0 reports the per-row statistics, or the sequence error ----
-    if (rank == 0) {
-        const bool err = sh.state == kStateError;
-        const int ndec = err ? 0 : sh.ndec;
-        for (int i = tid; i <= K; i += NT) {
+    if (rank == 0 && warp == 0) {
+        const bool err = state == kStateError;
+        const int nd = err ? 0 : ndec;
+        for (int i = lane; i <= K; i += 32) {
             if (a.row_stats) {
-                a.row_stats[((int64_t)b * (K + 1) + i) * 2] = i < ndec ? sh.rs_m[i] : NAN;
-                a.row_stats[((int64_t)b * (K + 1) + i) * 2 + 1] = i < ndec ? sh.rs_s[i] : NAN;
+                a.row_stats[((int64_t)b * (K + 1) + i) * 2] = i < nd ? sh.rs_m[i] : NAN;
+                a.row_stats[((int64_t)b * (K + 1) + i) * 2 + 1] = i < nd ? sh.rs_s[i] : NAN;
             }
             if (i < K && a.p_draft)
-                a.p_draft[(int64_t)b * K + i] = i < ndec ? sh.pd[i] : NAN;
+                a.p_draft[(int64_t)b * K + i] = i < nd ? sh.pd[i] : NAN;
             if (err) {
                 a.out_tokens[(int64_t)b * (K + 1) + i] = -1;
                 if (i < K)
                     a.accept_mask[(int64_t)b * K + i] = 0;
             }
         }
-        if (err && tid == 0) {
+        if (err && lane == 0) {
             a.accept_len[b] = 0;
             if (a.status)
-                a.status[b] = sh.code;
-            atomicOr(a.err_word, 1u << sh.code);
+                a.status[b] = code;
+            atomicOr(a.err_word, 1u << code);
         }
     }
 
-    // a copy that timed out may still land: give it one more bounded wait
-    if (timed_out)
-        (void)mbar_wait_bounded(&sh.mbar, phase ^ 1u, a.wait_ns);
+    // copies still in flight (only after an error) land before the exit
+    while (gq < gi) {
+        (void)wait_next();
+        release();
+    }
     // nobody leaves while a peer may still read its shared memory
     cluster.sync();
 }
@@ -1093,6 +1135,7 @@ int launch(sv_ctx* ctx, const void* logits, int dtype, const float* q, const int
     if (!fn)
         return SV_ERR_UNSUPPORTED;
 
+    const sv::Layout lay = sv::layout_for(plan.slice, es, plan.group, plan.threads);
     SvArgs args;
     std::memset(&args, 0, sizeof args);
     args.logits = logits;
@@ -1112,12 +1155,15 @@ int launch(sv_ctx* ctx, const void* logits, int dtype, const float* q, const int
     args.K = K;
     args.C = plan.cluster;
     args.G = plan.group;
-    args.rowbuf_bytes = (int)sv::round_up(plan.slice * es, sv::kRowBufAlign);
-    args.part_offset = (int)sv::round_up(sizeof(SvShared), 16);
-    args.wt_offset = args.part_offset + (int)sv::partial_bytes(plan.group, plan.threads);
+    args.wvec = (int)lay.wvec;
+    args.ntw = (int)lay.ntw;
+    args.off_fixed = (int)lay.off_fixed;
+    args.off_bar = (int)lay.off_bar;
+    args.off_part = (int)lay.off_part;
+    args.off_tt = (int)lay.off_tt;
     args.bulk = plan.bulk_copy && aligned(logits, 16) ? 1 : 0;
-    args.prefetch_next = plan.prefetch_next && args.bulk ? 1 : 0;
     args.qvec = (V % 4 == 0) && q && aligned(q, 16) ? 1 : 0;
+    args.speculate = plan.prefetch_next && args.bulk ? 1 : 0;
     args.T = T;
     const double c_d = 1.4426950408889634074 / (double)T;  // log2(e) / T
     // c_hi just below c_d so that c_lo = c_d - c_hi is strictly positive: a

@@ -1,5 +1,6 @@
-// sv_internal.h -- constants shared by the launch planner (planner.cpp) and the
-// verify kernel (spec_verify.cu).  Not part of the public ABI.
+// sv_internal.h -- constants and shared-memory layout shared by the launch
+// planner (planner.cpp) and the verify kernel (spec_verify.cu).  Not part of
+// the public ABI.
 #pragma once
 
 #include <stdint.h>
@@ -9,29 +10,37 @@ namespace sv {
 constexpr int kMaxK = 32;               // drafts per sequence
 constexpr int kMaxRows = kMaxK + 1;     // target rows per sequence
 constexpr int kMaxCluster = 16;         // CTAs per thread-block cluster (non-portable limit)
-constexpr int kMinSlice = 1024;         // vocabulary entries per CTA before the planner shrinks the cluster
 constexpr int kSliceAlign = 8;          // slices start on 8-entry boundaries (16 bytes of bf16)
-constexpr int kRowBufAlign = 128;       // bytes; each staged row slice starts on this boundary
+constexpr int kStages = 3;              // ring stages per warp
+constexpr int kChunkBytes = 2048;       // bytes per ring stage (one bulk copy)
 constexpr int kFixedSmem = 3072;        // bytes reserved for the kernel's fixed shared state
+constexpr int kSmemPerSM = 233472;      // shared memory of one SM (228 KB)
+constexpr int kSmemPerCtaReserved = 1024;  // the runtime's per-CTA reservation
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 
-// Per-warp (max, sum) partials: [2 parities][group rows][warps] float pairs,
-// then [2][warps] timeout flags.
-inline int64_t partial_bytes(int group, int threads) {
-    const int64_t nw = threads / 32;
-    return 2 * group * nw * 8 + round_up(2 * nw * 4, 16);
-}
+// Shared memory of one CTA: per-warp rings, the fixed state, per-warp ring
+// barriers, per-warp (max, sum) partials [2 parities][group rows][warps], and
+// the draw's per-warp tile totals.
+struct Layout {
+    int64_t wvec;       // 16-byte vectors per warp stretch
+    int64_t ntw;        // draw tiles (32 vectors) per warp stretch
+    int64_t off_fixed, off_bar, off_part, off_tt, total;
+};
 
-// Shared-memory bytes a CTA needs for a plan: staged row slices, the fixed
-// state, the partials, and one float per (tile, warp) for the draw.
-inline int64_t smem_bytes_for(int64_t slice, int elem_bytes, int group, int threads) {
-    const int E = 16 / elem_bytes;
-    const int64_t rowbuf = round_up(slice * elem_bytes, kRowBufAlign);
-    const int64_t tiles = ceil_div(ceil_div(slice, E), threads);
-    return group * rowbuf + kFixedSmem + partial_bytes(group, threads) +
-           tiles * (threads / 32) * 4 + kRowBufAlign;
+inline Layout layout_for(int64_t slice, int elem_bytes, int group, int threads) {
+    const int64_t nw = threads / 32;
+    const int64_t E = 16 / elem_bytes;
+    Layout l;
+    l.wvec = ceil_div(ceil_div(slice, E), nw);
+    l.ntw = ceil_div(l.wvec, 32);
+    l.off_fixed = nw * kStages * kChunkBytes;
+    l.off_bar = l.off_fixed + kFixedSmem;
+    l.off_part = l.off_bar + round_up(nw * kStages * 8, 16);
+    l.off_tt = l.off_part + round_up(2 * (int64_t)group * nw * 8, 16);
+    l.total = l.off_tt + round_up(nw * l.ntw * 4, 16);
+    return l;
 }
 
 }  // namespace sv

@@ -26,30 +26,32 @@ def plan(sv, B, K, V, dtype, oc=0, og=0, ot=0, dev=GB300):
     [0, 1])))
 def test_plan_invariants(sv, B, K, V, dtype):
     rc, p = plan(sv, B, K, V, dtype)
-    es = 2 if dtype == 1 else 4
-    if -(-V // 16) * es > GB300["smem"] - 4096:
-        # one CTA holds its whole slice of a row in shared memory: past 16
-        # slices of ~223 KB the shape has no plan
-        assert rc == sv.SV_ERR_UNSUPPORTED
-        return
     assert rc == sv.SV_OK
+    es = 2 if dtype == 1 else 4
     C, slice_ = p["cluster"], p["slice"]
-    assert 1 <= C <= 16
+    assert C in (1, 2, 4, 8, 16)
     assert slice_ % 8 == 0 and slice_ * C >= V and slice_ * (C - 1) < V + 8 * C
     assert p["grid"] == B * C
     assert 1 <= p["group"] <= K + 1
     assert p["smem_bytes"] <= GB300["smem"]
     assert p["bulk_copy"] == int((V * es) % 16 == 0)
-    assert p["threads"] in (128, 256, 512)
+    assert p["threads"] == 128
+    assert p["prefetch_next"] == int(p["group"] == 1)
+    # the batch is resident at once whenever a cluster of one CTA per sequence fits
+    per_sm = min(8, 233472 // (p["smem_bytes"] + 1024))
+    if B <= 152 * per_sm:
+        assert B * C <= 152 * per_sm or C == 1
 
 
 def test_workload_plans(sv):
-    # big batches read rows one at a time; small ones load every row at once
-    assert plan(sv, 256, 7, 128256, 1)[1]["group"] == 1
-    assert plan(sv, 256, 7, 128256, 1)[1]["cluster"] == 8
-    assert plan(sv, 1, 4, 32000, 0)[1]["group"] == 5
-    assert plan(sv, 1, 4, 32000, 0)[1]["cluster"] == 16
-    assert plan(sv, 64, 3, 151936, 1)[1]["group"] == 1
+    # 256 sequences: four CTAs each keep the whole batch resident, one row per step
+    p = plan(sv, 256, 7, 128256, 1)[1]
+    assert (p["cluster"], p["group"]) == (4, 1)
+    # one sequence: the largest cluster, every row at once
+    p = plan(sv, 1, 4, 32000, 0)[1]
+    assert (p["cluster"], p["group"]) == (16, 5)
+    p = plan(sv, 64, 3, 151936, 1)[1]
+    assert (p["cluster"], p["group"]) == (16, 1)
 
 
 def test_overrides(sv):
@@ -63,13 +65,12 @@ def test_overrides(sv):
     assert plan(sv, 4, 2, 1000, 1, oc=16, dev=small)[0] == sv.SV_ERR_UNSUPPORTED
 
 
-def test_shared_memory_limit(sv):
-    # a slice that cannot fit even one row: unsupported
-    tiny = dict(GB300, smem=48 * 1024)
-    assert plan(sv, 1, 1, 1 << 22, 0, dev=tiny)[0] == sv.SV_ERR_UNSUPPORTED
-    # groups shrink before the cluster grows
-    rc, p = plan(sv, 1, 32, 1 << 20, 1)
-    assert rc == 0 and p["smem_bytes"] <= GB300["smem"] and p["group"] < 33
+def test_shared_memory_does_not_grow_with_the_vocabulary(sv):
+    small = plan(sv, 1, 1, 32000, 1)[1]["smem_bytes"]
+    huge = plan(sv, 1, 1, 1 << 24, 1)[1]["smem_bytes"]
+    assert huge - small < 16 * 1024
+    tiny = dict(GB300, smem=8 * 1024)
+    assert plan(sv, 1, 1, 32000, 0, dev=tiny)[0] == sv.SV_ERR_UNSUPPORTED
 
 
 def test_bad_arguments(sv):
@@ -77,3 +78,4 @@ def test_bad_arguments(sv):
     assert plan(sv, 1, 33, 100, 0)[0] == sv.SV_ERR_INVALID_ARG
     assert plan(sv, 1, 1, 0, 0)[0] == sv.SV_ERR_INVALID_ARG
     assert plan(sv, 1, 1, 100, 2)[0] == sv.SV_ERR_INVALID_ARG
+    assert plan(sv, 1, 1, (1 << 31) + 1, 0)[0] == sv.SV_ERR_INVALID_ARG
