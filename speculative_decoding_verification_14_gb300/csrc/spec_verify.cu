@@ -144,6 +144,11 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
         : "memory");
 }
 
+// Bulk prefetch of a global range into L2 (no destination, no completion).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // One bounded poll: the waiting thread may be suspended (up to about 50 us)
 // until the phase completes, so waiting warps do not spin on issue slots.
 __device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t parity) {
@@ -793,6 +798,8 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sv_verify_kernel(const __grid_c
         lrow = static_cast<const unsigned char*>(a.logits) + ((row0 + j) * V + v0) * ES;
         qrow = j < K ? a.q + ((int64_t)b * K + j) * V + v0 : nullptr;
         const float inv_s = __frcp_rn(rowS.hi);
+        if (lane == 0 && a.bulk && nq > 0)
+            bulk_prefetch_l2(lrow + e0 * ES, (uint32_t)(nq * ES));
         int sp = 0;
         for (int round = 0; round < 2; ++round) {
             const bool ring_q = mode == kModeResidual && a.qvec;
@@ -801,8 +808,23 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sv_verify_kernel(const __grid_c
             const float* qbuf = nullptr;
             FF wacc = {0.f, 0.f};
             float qmin = 0.f, qmax = 0.f;
+            // this lane's logits vector of tile t (zero past the stretch); the
+            // loads run two tiles ahead of the arithmetic
+            auto load_lvec = [&](int t) -> uint4 {
+                const int64_t te = (int64_t)t * kTile + lane * E;
+                if (te >= nq)
+                    return make_uint4(0, 0, 0, 0);
+                if (a.bulk)
+                    return __ldg(reinterpret_cast<const uint4*>(lrow + (e0 + te) * ES));
+                return load_vec_elems<ES>(a.logits, (row0 + j) * V + v0, e0 + te, e0 + nq);
+            };
+            uint4 lv0 = ntile > 0 ? load_lvec(0) : make_uint4(0, 0, 0, 0);
+            uint4 lv1 = ntile > 1 ? load_lvec(1) : make_uint4(0, 0, 0, 0);
             for (int t = 0; t < ntile; ++t) {
                 const int64_t tb = (int64_t)t * kTile;  // first entry of the tile in the stretch
+                const uint4 lcur = lv0;
+                lv0 = lv1;
+                lv1 = t + 2 < ntile ? load_lvec(t + 2) : make_uint4(0, 0, 0, 0);
                 if (ring_q && tb % kQChunk == 0) {
                     while (qissued < nqc && qissued < qdone + kStages) {
                         const int64_t cb = (int64_t)qissued * kQChunk;
@@ -814,14 +836,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sv_verify_kernel(const __grid_c
                 const int64_t te = tb + lane * E;
                 const int n = (int)max((int64_t)0, min((int64_t)E, nq - te));
                 float2 f[E / 2];
-                if (a.bulk) {
-                    uint4 raw = make_uint4(0, 0, 0, 0);
-                    if (n > 0)
-                        raw = __ldg(reinterpret_cast<const uint4*>(lrow + (e0 + te) * ES));
-                    Elem<ES>::unpack(raw, f);
-                } else {
-                    Elem<ES>::unpack(load_vec_elems<ES>(a.logits, (row0 + j) * V + v0, e0 + te, e0 + nq), f);
-                }
+                Elem<ES>::unpack(lcur, f);
                 float qq[E];
 #pragma unroll
                 for (int k = 0; k < E; ++k)
