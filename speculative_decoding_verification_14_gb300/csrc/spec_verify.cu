@@ -124,10 +124,6 @@ __device__ __forceinline__ void fence_mbar_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
-__device__ __forceinline__ void fence_proxy_async() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 __device__ __forceinline__ void mbar_arrive_expect_tx(unsigned long long* bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
                  "r"(bytes)
@@ -149,16 +145,14 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
-// One bounded poll: the waiting thread may be suspended (up to about 50 us)
-// until the phase completes, so waiting warps do not spin on issue slots.
 __device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity), "r"(50000u)
+        : "r"(smem_addr(bar)), "r"(parity)
         : "memory");
     return ok != 0;
 }
@@ -171,15 +165,21 @@ __device__ __forceinline__ unsigned long long global_ns() {
 
 // Wait for phase `parity` of `bar`, giving up after `limit_ns` (and after a
 // fixed number of polls, whichever comes first).  Returns false on give-up.
+// Between polls the warp sleeps with exponential backoff (32 ns up to 256
+// ns): a waiting warp must not take issue slots from the warps that compute.
 __device__ bool mbar_wait_bounded(unsigned long long* bar, uint32_t parity,
                                   unsigned long long limit_ns) {
     if (mbar_try_wait(bar, parity))
         return true;
     const unsigned long long t0 = global_ns();
+    unsigned sleep = 32;
     for (uint32_t it = 0; it < (1u << 26); ++it) {
+        __nanosleep(sleep);
         if (mbar_try_wait(bar, parity))
             return true;
-        if (global_ns() - t0 > limit_ns)
+        if (sleep < 256)
+            sleep <<= 1;
+        if ((it & 15u) == 15u && global_ns() - t0 > limit_ns)
             return false;
     }
     return false;
@@ -591,7 +591,6 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sv_verify_kernel(const __grid_c
     auto issue = [&](const void* src, uint32_t bytes) {
         if (lane == 0) {
             const uint32_t st = gi % kStages;
-            fence_proxy_async();
             mbar_arrive_expect_tx(&wbar[st], bytes);
             bulk_copy_g2s(ring + st * kChunkBytes, src, bytes, &wbar[st]);
         }
