@@ -41,6 +41,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <type_traits>
 
 #include "../../include/spec_verify.h"
 #include "sv_internal.h"
@@ -501,37 +502,54 @@ __device__ __forceinline__ void lane_fold(const Src& src, int nv, float& m, floa
     }
 }
 
-// Draw weights of E entries: residual max(0, p - q) (mode 0) or the
-// unnormalised target weights exp(z - max) (modes 1 and 2).  Entries at or
-// past `n` weigh 0.  q range checks fold into qmin (NaN-propagating) / qmax.
-template <int ES>
+// Draw weights of E entries: the residual max(0, p - q) when RESID, else the
+// unnormalised target weights 2^((l - M) log2e/T).  Entries at or past `n`
+// weigh 0.  With RESID, q values fold into qmin (NaN-propagating) and qmax
+// for the range check.  Returns the sum of the E weights.
+template <int ES, bool RESID>
 __device__ __forceinline__ float entry_weights(const float2 (&f)[Elem<ES>::E / 2],
-                                               const float (&qq)[Elem<ES>::E], int n, int mode,
-                                               float M, float c_hi, float c_lo, float inv_s,
+                                               const float (&qq)[Elem<ES>::E], int n, float M,
+                                               float c_hi, float c_lo, float inv_s,
                                                float (&w)[Elem<ES>::E], float& qmin,
                                                float& qmax) {
     constexpr int E = Elem<ES>::E;
     const float2 neg_m = make_float2(-M, -M), chi = make_float2(c_hi, c_hi),
                  clo = make_float2(c_lo, c_lo);
-    float ts = 0.f;
 #pragma unroll
     for (int h = 0; h < E / 2; ++h) {
         const float2 e = exp2_pair(f[h], neg_m, chi, clo);
+        w[2 * h] = e.x;
+        w[2 * h + 1] = e.y;
+    }
+    if constexpr (RESID) {
 #pragma unroll
-        for (int g = 0; g < 2; ++g) {
-            const int idx = 2 * h + g;
-            const float ev = g ? e.y : e.x;
-            float wk = ev;
-            if (mode == kModeResidual) {
-                const float qv = qq[idx];
-                if (idx < n) {
-                    qmin = fmin_nan(qmin, qv);
-                    qmax = fmaxf(qmax, qv);
-                }
-                wk = fmaxf(__fmaf_rn(ev, inv_s, -qv), 0.f);
+        for (int k = 0; k < E; ++k)
+            w[k] = fmaxf(__fmaf_rn(w[k], inv_s, -qq[k]), 0.f);
+    }
+    float ts = 0.f;
+    if (n >= E) {
+        if constexpr (RESID) {
+#pragma unroll
+            for (int k = 0; k < E; ++k) {
+                qmin = fmin_nan(qmin, qq[k]);
+                qmax = fmaxf(qmax, qq[k]);
             }
-            w[idx] = idx < n ? wk : 0.f;
-            ts += w[idx];
+        }
+#pragma unroll
+        for (int k = 0; k < E; ++k)
+            ts += w[k];
+    } else {
+#pragma unroll
+        for (int k = 0; k < E; ++k) {
+            if (k < n) {
+                if constexpr (RESID) {
+                    qmin = fmin_nan(qmin, qq[k]);
+                    qmax = fmaxf(qmax, qq[k]);
+                }
+            } else {
+                w[k] = 0.f;
+            }
+            ts += w[k];
         }
     }
     return ts;
@@ -800,75 +818,88 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sv_verify_kernel(const __grid_c
         if (lane == 0 && a.bulk && nq > 0)
             bulk_prefetch_l2(lrow + e0 * ES, (uint32_t)(nq * ES));
         int sp = 0;
-        for (int round = 0; round < 2; ++round) {
-            const bool ring_q = mode == kModeResidual && a.qvec;
-            const int nqc = ring_q ? (int)((nq + kQChunk - 1) / kQChunk) : 0;
-            int qissued = 0, qdone = 0;
-            const float* qbuf = nullptr;
+        // one pass over this warp's stretch of row j: every tile's weight total
+        // goes to `tt` for the locate step; returns the stretch total.  Logits
+        // vectors load one q-chunk ahead; the draft row streams through the
+        // warp's ring when it is 16-byte aligned.
+        constexpr int kTPC = kQChunk / kTile;  // tiles per q chunk
+        const int nq32 = (int)nq;
+        const int nchunk = (nq32 + kQChunk - 1) / kQChunk;
+        const unsigned char* lbase = lrow + e0 * ES;
+        const float* qbase = qrow ? qrow + e0 : nullptr;
+        float* tt_w = tt + warp * a.ntw;
+        float qmin = 0.f, qmax = 0.f;
+        auto load_tile_logits = [&](int t) -> uint4 {
+            const int te = t * kTile + lane * E;
+            if (t >= ntile || te >= nq32)
+                return make_uint4(0, 0, 0, 0);
+            if (a.bulk)
+                return __ldg(reinterpret_cast<const uint4*>(lbase + (size_t)te * ES));
+            return load_vec_elems<ES>(a.logits, (row0 + j) * V + v0 + e0, te, nq32);
+        };
+        auto pass = [&](auto resid_tag) -> FF {
+            constexpr bool RESID = decltype(resid_tag)::value;
+            const bool ring = RESID && a.qvec;
             FF wacc = {0.f, 0.f};
-            float qmin = 0.f, qmax = 0.f;
-            // this lane's logits vector of tile t (zero past the stretch); the
-            // loads run two tiles ahead of the arithmetic
-            auto load_lvec = [&](int t) -> uint4 {
-                const int64_t te = (int64_t)t * kTile + lane * E;
-                if (te >= nq)
-                    return make_uint4(0, 0, 0, 0);
-                if (a.bulk)
-                    return __ldg(reinterpret_cast<const uint4*>(lrow + (e0 + te) * ES));
-                return load_vec_elems<ES>(a.logits, (row0 + j) * V + v0, e0 + te, e0 + nq);
-            };
-            uint4 lv0 = ntile > 0 ? load_lvec(0) : make_uint4(0, 0, 0, 0);
-            uint4 lv1 = ntile > 1 ? load_lvec(1) : make_uint4(0, 0, 0, 0);
-            for (int t = 0; t < ntile; ++t) {
-                const int64_t tb = (int64_t)t * kTile;  // first entry of the tile in the stretch
-                const uint4 lcur = lv0;
-                lv0 = lv1;
-                lv1 = t + 2 < ntile ? load_lvec(t + 2) : make_uint4(0, 0, 0, 0);
-                if (ring_q && tb % kQChunk == 0) {
-                    while (qissued < nqc && qissued < qdone + kStages) {
-                        const int64_t cb = (int64_t)qissued * kQChunk;
-                        issue(qrow + e0 + cb, (uint32_t)(min((int64_t)kQChunk, nq - cb) * 4));
+            // logits run two tiles ahead of the arithmetic
+            uint4 lv0 = load_tile_logits(0), lv1 = load_tile_logits(1);
+            int qissued = 0;
+            for (int c = 0; c < nchunk; ++c) {
+                const float* qs = nullptr;
+                if (ring) {
+                    while (qissued < nchunk && qissued < c + kStages) {
+                        issue(qbase + qissued * kQChunk,
+                              (uint32_t)(min(kQChunk, nq32 - qissued * kQChunk) * 4));
                         ++qissued;
                     }
-                    qbuf = reinterpret_cast<const float*>(wait_next());
+                    qs = reinterpret_cast<const float*>(wait_next());
                 }
-                const int64_t te = tb + lane * E;
-                const int n = (int)max((int64_t)0, min((int64_t)E, nq - te));
-                float2 f[E / 2];
-                Elem<ES>::unpack(lcur, f);
-                float qq[E];
 #pragma unroll
-                for (int k = 0; k < E; ++k)
-                    qq[k] = 0.f;
-                if (mode == kModeResidual) {
-                    if (ring_q) {
-                        const float* qs = qbuf + (tb % kQChunk) + lane * E;
+                for (int k = 0; k < kTPC; ++k) {
+                    const int t = c * kTPC + k;
+                    if (t < ntile) {
+                        const int te = t * kTile + lane * E;
+                        const int n = min(E, max(0, nq32 - te));
+                        const uint4 lcur = lv0;
+                        lv0 = lv1;
+                        lv1 = load_tile_logits(t + 2);
+                        float2 f[E / 2];
+                        Elem<ES>::unpack(lcur, f);
+                        float qq[E];
+                        if constexpr (RESID) {
+                            if (ring) {
+                                const float4* q4 =
+                                    reinterpret_cast<const float4*>(qs + k * kTile + lane * E);
 #pragma unroll
-                        for (int k = 0; k < E; k += 4) {
-                            const float4 v4 = *reinterpret_cast<const float4*>(qs + k);
-                            qq[k] = v4.x;
-                            qq[k + 1] = v4.y;
-                            qq[k + 2] = v4.z;
-                            qq[k + 3] = v4.w;
+                                for (int h = 0; h < E / 4; ++h) {
+                                    const float4 v4 = q4[h];
+                                    qq[4 * h] = v4.x;
+                                    qq[4 * h + 1] = v4.y;
+                                    qq[4 * h + 2] = v4.z;
+                                    qq[4 * h + 3] = v4.w;
+                                }
+                            } else {
+#pragma unroll
+                                for (int h = 0; h < E; ++h)
+                                    qq[h] = h < n ? __ldg(qbase + te + h) : 0.f;
+                            }
                         }
-                    } else {
-#pragma unroll
-                        for (int k = 0; k < E; ++k)
-                            qq[k] = k < n ? __ldg(qrow + e0 + te + k) : 0.f;
+                        float w[E];
+                        const float ts = entry_weights<ES, RESID>(f, qq, n, rowM, a.c_hi, a.c_lo,
+                                                                  inv_s, w, qmin, qmax);
+                        const float tot = warp_sum_bcast(ts);
+                        if (lane == 0)
+                            tt_w[t] = tot;
+                        wacc = ff_add(wacc, tot);
                     }
                 }
-                float w[E];
-                const float ts = entry_weights<ES>(f, qq, n, mode, rowM, a.c_hi, a.c_lo, inv_s, w,
-                                                   qmin, qmax);
-                const float tot = warp_sum_bcast(ts);
-                if (lane == 0)
-                    tt[warp * a.ntw + t] = tot;
-                wacc = ff_add(wacc, tot);
-                if (ring_q && ((tb + kTile) % kQChunk == 0 || t == ntile - 1)) {
+                if (ring)
                     release();
-                    ++qdone;
-                }
             }
+            return wacc;
+        };
+        for (int round = 0; round < 2; ++round) {
+            const FF wacc = mode == kModeResidual ? pass(std::true_type{}) : pass(std::false_type{});
             const bool badq = __any_sync(kFull, !(qmin >= 0.f) || !(qmax < INFINITY));
             const bool to = __any_sync(kFull, timed_out);
             if (lane == 0) {
@@ -973,8 +1004,12 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sv_verify_kernel(const __grid_c
             for (int k = 0; k < E; ++k)
                 qq[k] = (mode == kModeResidual && k < n) ? __ldg(qrow + e0s + te + k) : 0.f;
             float w[E], qmn = 0.f, qmx = 0.f;
-            const float ts = entry_weights<ES>(f, qq, n, mode, rowM, a.c_hi, a.c_lo,
-                                               __frcp_rn(rowS.hi), w, qmn, qmx);
+            const float ts =
+                mode == kModeResidual
+                    ? entry_weights<ES, true>(f, qq, n, rowM, a.c_hi, a.c_lo, __frcp_rn(rowS.hi), w,
+                                              qmn, qmx)
+                    : entry_weights<ES, false>(f, qq, n, rowM, a.c_hi, a.c_lo, __frcp_rn(rowS.hi), w,
+                                               qmn, qmx);
             const float inc = warp_incl_scan(ts);
             const int pk = pick_lane(ts, FF{inc, 0.f}, rem, 32, take_last);
             float prev = __shfl_up_sync(kFull, inc, 1);
