@@ -20,6 +20,7 @@ from __future__ import annotations
 
 import argparse
 import ctypes
+import hashlib
 import json
 import os
 import statistics
@@ -77,13 +78,28 @@ def measured_peak():
         return 6800.0, "fallback"
 
 
+KERNEL_SOURCES = ("speculative_decoding_verification_14_gb300/csrc/spec_verify.cu",
+                  "speculative_decoding_verification_14_gb300/csrc/sv_internal.h",
+                  "speculative_decoding_verification_14_gb300/csrc/planner.cpp")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def profile_traffic(workload):
     """DRAM bytes per launch from the committed ncu summary, if it covers this
-    workload and the current kernel (else None)."""
+    workload and was taken on the current kernel sources (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
+        if d.get("kernel_source_sha256") != kernel_source_hash():
+            return None
         e = d.get(workload)
         return float(e["dram_bytes_per_launch"]) if e else None
     except Exception:
