@@ -150,6 +150,46 @@ int spec_verify_plan_for(int num_sms, int smem_per_cta, int max_cluster,
                          int B, int K, int64_t V, int logits_dtype,
                          int ovr_cluster, int ovr_group, int ovr_threads, sv_plan* out);
 
+/* The verify of spec_verify_run with no context and no allocation of any
+ * kind (no cudaMalloc/cudaFree, no host heap, no allocating library call).
+ * The pages have no counterpart: this is a deployment convenience, not part of
+ * the method.
+ *
+ * For callers that cannot allocate where they verify: an engine that handed
+ * nearly all device memory to its own pool at start-up, a decode loop that
+ * must not take the device-wide synchronisation cudaFree implies (so it cannot
+ * own a context it later destroys), a plugin behind a fixed function table
+ * with nowhere to create or release a context.
+ *
+ * Arguments, layouts, outputs and per-sequence errors are those of
+ * spec_verify_run, with `device` (the CUDA device the pointers and `stream`
+ * belong to) in place of the context.  Limits: 0 <= device < 64,
+ * 1 <= B <= 2^20, 0 <= K <= 32, 1 <= V <= 2^31 (and B*(K+1)*V < 2^40); larger
+ * sizes return SV_ERR_INVALID_ARG before anything is launched.  The launch plan
+ * is the planner's automatic choice.
+ *
+ * Setup: the first call for a device queries it, sets the kernels' attributes
+ * and looks up the device address of the library's static scratch, with that
+ * device current.  Make that first call before any stream capture begins.  A
+ * failed setup returns SV_ERR_CUDA / SV_ERR_UNSUPPORTED and is retried by the
+ * next call.
+ *
+ * Scratch: a 256-byte array in the library's device code, one per device, of
+ * which a call uses 4 bytes (the word the kernel ORs error bits into).
+ * Nothing in it has to start at zero: the kernel never reads it.  This entry
+ * offers no way to read it either, so errors are seen through `status` (pass
+ * it) and accept_len == 0.  Every call on a device shares that scratch: calls
+ * that can overlap on the GPU (streams not ordered with each other) race on
+ * it, so order them on one stream or with events.  Host threads may call
+ * concurrently once a device is set up. */
+int spec_verify_run_noalloc(int device,
+                            const void* target_logits, int logits_dtype,
+                            const float* q, const int32_t* draft_tokens, const float* uniforms,
+                            int B, int K, int64_t V, float temperature,
+                            int32_t* accept_len, int32_t* out_tokens, uint8_t* accept_mask,
+                            float* row_stats, float* p_draft, int32_t* status,
+                            void* stream);
+
 /* Release the context and everything it owns. */
 int spec_verify_destroy(sv_ctx* ctx);
 

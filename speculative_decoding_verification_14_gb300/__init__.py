@@ -56,6 +56,7 @@ def library() -> ctypes.CDLL:
                                                 ctypes.c_int, ctypes.c_int64]),
             "spec_verify_run": (ctypes.c_int, run_args),
             "spec_verify_run_host": (ctypes.c_int, run_args),
+            "spec_verify_run_noalloc": (ctypes.c_int, [ctypes.c_int] + run_args[1:]),
             "spec_verify_get_error": (ctypes.c_int, [P, P, ctypes.POINTER(ctypes.c_uint32)]),
             "spec_verify_get_plan": (ctypes.c_int, [P, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
                                                     ctypes.c_int, ctypes.POINTER(sv_plan)]),
@@ -114,6 +115,15 @@ def spec_verify_run_host(ctx, logits_ptr, dtype, q_ptr, tokens_ptr, uniforms_ptr
                                           B, K, V, float(T), accept_len_ptr, out_tokens_ptr,
                                           accept_mask_ptr, row_stats_ptr, p_draft_ptr, status_ptr,
                                           stream)
+
+
+def spec_verify_run_noalloc(device, logits_ptr, dtype, q_ptr, tokens_ptr, uniforms_ptr, B, K, V, T,
+                            accept_len_ptr, out_tokens_ptr, accept_mask_ptr, row_stats_ptr=None,
+                            p_draft_ptr=None, status_ptr=None, stream=None) -> int:
+    return library().spec_verify_run_noalloc(int(device), logits_ptr, dtype, q_ptr, tokens_ptr,
+                                             uniforms_ptr, B, K, V, float(T), accept_len_ptr,
+                                             out_tokens_ptr, accept_mask_ptr, row_stats_ptr,
+                                             p_draft_ptr, status_ptr, stream)
 
 
 def spec_verify_get_error(ctx, stream=None):

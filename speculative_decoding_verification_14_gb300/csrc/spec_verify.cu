@@ -40,7 +40,9 @@
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
+#include <atomic>
 #include <cstring>
+#include <mutex>
 #include <type_traits>
 
 #include "../../include/spec_verify.h"
@@ -1507,3 +1509,155 @@ int spec_verify_run_host(sv_ctx* ctx, const void* target_logits, int logits_dtyp
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// spec_verify_run_noalloc: the verify of spec_verify_run without a context and
+// without allocating anything.
+//
+// Who needs it: callers that cannot allocate device memory where they verify.
+// A serving engine that reserved nearly all of HBM for its own pool (KV cache,
+// activations) at start-up has nothing left for a library to cudaMalloc; a
+// decode loop that must not pay the device-wide synchronisation cudaFree
+// implies cannot own a context it later destroys; a plugin called through a
+// fixed function table has no place to create or release one.
+//
+// What replaces the context: the kernel's only scratch is the word its
+// sequence-error bits are ORed into.  Here that word is the first element of a
+// file-scope device array (one copy per device, zero when the module is
+// loaded), whose address is looked up once per device.  The device properties
+// and kernel attributes that spec_verify_init queries are set up once per
+// device, on the first call for it, in static host storage.
+namespace {
+
+constexpr int kNoAllocScratchWords = 64;  // 256 bytes of scratch per device
+constexpr int kNoAllocScratchNeed = 1;    // words one call uses: the error word
+constexpr int kNoAllocMaxDevices = 64;
+constexpr int kNoAllocMaxB = 1 << 20;
+constexpr int64_t kNoAllocMaxV = (int64_t)1 << 31;
+static_assert(kNoAllocScratchNeed <= kNoAllocScratchWords, "scratch array too small");
+
+static __device__ __align__(256) uint32_t sv_noalloc_scratch[kNoAllocScratchWords];
+
+struct NoAllocDevice {
+    std::atomic<int> ready{0};
+    sv_ctx ctx;  // static storage: limits, planner inputs, scratch address
+};
+NoAllocDevice g_noalloc[kNoAllocMaxDevices];
+std::mutex g_noalloc_setup_mutex;
+
+// Everything spec_verify_init does except allocating: device checks, kernel
+// attributes, the largest usable cluster, and the scratch address, all with
+// `device` current.
+int noalloc_setup(int device, sv_ctx* c) {
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || device >= ndev) {
+        (void)cudaGetLastError();
+        return SV_ERR_CUDA;
+    }
+    DeviceGuard guard(device);
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess || cur != device) {
+        (void)cudaGetLastError();
+        return SV_ERR_CUDA;
+    }
+    int major = 0, minor = 0, sms = 0, optin = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) !=
+            cudaSuccess) {
+        (void)cudaGetLastError();
+        return SV_ERR_CUDA;
+    }
+    if (major != 10 || minor != 3)
+        return SV_ERR_UNSUPPORTED;
+    int max_cluster = 16;
+    const int es_list[2] = {2, 4};
+    const int nt_list[3] = {128, 256, 512};
+    for (int es : es_list)
+        for (int nt : nt_list) {
+            KernelFn fn = pick_kernel(es, nt);
+            if (cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     optin) != cudaSuccess) {
+                (void)cudaGetLastError();
+                return SV_ERR_CUDA;
+            }
+            if (cudaFuncSetAttribute((const void*)fn,
+                                     cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+                cudaSuccess) {
+                (void)cudaGetLastError();
+                max_cluster = 8;
+            }
+        }
+    if (max_cluster == 16) {
+        cudaLaunchConfig_t cfg;
+        std::memset(&cfg, 0, sizeof cfg);
+        cfg.gridDim = dim3(16, 1, 1);
+        cfg.blockDim = dim3(512, 1, 1);
+        cfg.dynamicSmemBytes = 64 * 1024;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 16;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int nclusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&nclusters, (const void*)pick_kernel(2, 512), &cfg) !=
+                cudaSuccess ||
+            nclusters < 1) {
+            (void)cudaGetLastError();
+            max_cluster = 8;
+        }
+    }
+    uint32_t* scratch = nullptr;
+    if (cudaGetSymbolAddress((void**)&scratch, sv_noalloc_scratch) != cudaSuccess || !scratch) {
+        (void)cudaGetLastError();
+        return SV_ERR_CUDA;
+    }
+    c->device = device;
+    c->max_B = kNoAllocMaxB;
+    c->max_K = kMaxK;
+    c->max_V = kNoAllocMaxV;
+    c->num_sms = sms;
+    c->smem_optin = optin;
+    c->max_cluster = max_cluster;
+    const int ms = env_int("SV_WAIT_MS", 0);
+    if (ms > 0)
+        c->wait_ns = (unsigned long long)ms * 1000000ull;
+    c->d_err = scratch;
+    return SV_OK;
+}
+
+}  // namespace
+
+extern "C" int spec_verify_run_noalloc(int device, const void* target_logits, int logits_dtype,
+                                       const float* q, const int32_t* draft_tokens,
+                                       const float* uniforms, int B, int K, int64_t V,
+                                       float temperature, int32_t* accept_len,
+                                       int32_t* out_tokens, uint8_t* accept_mask,
+                                       float* row_stats, float* p_draft, int32_t* status,
+                                       void* stream) {
+    if (device < 0 || device >= kNoAllocMaxDevices)
+        return SV_ERR_INVALID_ARG;
+    NoAllocDevice& d = g_noalloc[device];
+    if (!d.ready.load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lock(g_noalloc_setup_mutex);
+        if (!d.ready.load(std::memory_order_relaxed)) {
+            const int rc = noalloc_setup(device, &d.ctx);
+            if (rc != SV_OK)
+                return rc;  // nothing cached: the next call tries again
+            d.ready.store(1, std::memory_order_release);
+        }
+    }
+    // sizes beyond this entry's limits (B <= 2^20, K <= 32, V <= 2^31) are
+    // rejected here, before anything is launched
+    const int rc = validate(&d.ctx, target_logits, logits_dtype, q, draft_tokens, uniforms, B, K,
+                            V, temperature, accept_len, out_tokens, accept_mask, row_stats,
+                            p_draft, status);
+    if (rc != SV_OK)
+        return rc;
+    return launch(&d.ctx, target_logits, logits_dtype, q, draft_tokens, uniforms, B, K, V,
+                  temperature, accept_len, out_tokens, accept_mask, row_stats, p_draft, status,
+                  static_cast<cudaStream_t>(stream));
+}
