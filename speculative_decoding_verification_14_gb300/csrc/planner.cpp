@@ -46,11 +46,15 @@ int plan_impl(int num_sms, int smem_per_cta, int max_cluster, int B, int K, int6
     const int nw = threads / 32;
     const int cmax = max_cluster < kMaxCluster ? max_cluster : kMaxCluster;
     const int64_t min_slice = (int64_t)nw * (kChunkBytes / 16) * E / 2;  // half a stage per warp
+    // when the batch fills the GPU, each warp keeps at least 4 ring stages of
+    // work per row: below that the per-row partial, barrier and merge cost more
+    // than the streaming they serve
+    const int64_t min_slice_full = (int64_t)nw * 4 * (kChunkBytes / 16) * E;
 
     // resident CTAs per SM with a single-row plan (threads and shared memory)
-    const int64_t smem1 = layout_for(round_up(ceil_div(V, 4), kSliceAlign), es, 1, threads).total;
+    const int64_t smem1 = layout_for(round_up(ceil_div(V, 4), kSliceAlign), es, 1, threads, 4).total;
     int64_t per_sm = (int64_t)kSmemPerSM / (smem1 + kSmemPerCtaReserved);
-    const int64_t by_threads = 1024 / threads;  // the kernels' launch bounds
+    const int64_t by_threads = kThreadsPerSM / threads;  // the kernels' launch bounds
     if (per_sm > by_threads)
         per_sm = by_threads;
     if (per_sm < 1)
@@ -63,7 +67,9 @@ int plan_impl(int num_sms, int smem_per_cta, int max_cluster, int B, int K, int6
     } else {
         C = 1;
         for (int c = cmax >= 16 ? 16 : cmax; c >= 1; c /= 2) {
-            if ((int64_t)B * c <= capacity && (c == 1 || ceil_div(V, c) >= min_slice)) {
+            const bool fills = (int64_t)B * c >= num_sms;
+            if ((int64_t)B * c <= capacity &&
+                (c == 1 || ceil_div(V, c) >= (fills ? min_slice_full : min_slice))) {
                 C = c;
                 break;
             }
@@ -76,10 +82,10 @@ int plan_impl(int num_sms, int smem_per_cta, int max_cluster, int B, int K, int6
         G = (int64_t)B * C >= num_sms ? 1 : rows;
 
     const int64_t slice = round_up(ceil_div(V, C), kSliceAlign);
-    Layout l = layout_for(slice, es, G, threads);
+    Layout l = layout_for(slice, es, G, threads, C);
     while (l.total > smem_per_cta && G > 1 && !ovr_group) {
         G = (G + 1) / 2;
-        l = layout_for(slice, es, G, threads);
+        l = layout_for(slice, es, G, threads, C);
     }
     if (l.total > smem_per_cta)
         return SV_ERR_UNSUPPORTED;

@@ -86,7 +86,8 @@ struct SvArgs {
     int bulk;               // 1: rows move with cp.async.bulk (16-byte aligned rows)
     int qvec;               // 1: draft rows move with cp.async.bulk as well
     int speculate;          // 1: first chunks of the next row are issued before the decision
-    float c_hi, c_lo;       // log2(e)/T = c_hi + c_lo with c_lo > 0
+    float c_hi, c_lo;       // log2(e)/T = c_hi + c_lo with c_lo > 0 (accurate paths)
+    float c;                // log2(e)/T rounded to float (per-entry paths)
     float T;
     unsigned long long wait_ns;
 };
@@ -95,17 +96,14 @@ struct FF {  // hi + lo, see the double-float helpers below
     float hi, lo;
 };
 
-// Fixed shared state of one CTA.  samp_* is read by the other CTAs of the
-// cluster through distributed shared memory (so are the per-warp partials).
+// Fixed shared state of one CTA.  samp is written by every CTA of the cluster
+// (st.async pushes), like the row partials.
 struct __align__(16) SvShared {
-    FF samp_tot[2];
-    int samp_bad[2];
+    float4 samp[2][sv::kMaxCluster];  // pushed by every CTA: (total hi, total lo, bad, 0) per draw round
     FF wtot[kMaxWarps];
     int wbad[kMaxWarps];
     int x[kMaxK];
     float u[kMaxRows];
-    float lx[kMaxK];
-    float qx[kMaxK];
     float rs_m[kMaxRows];
     float rs_s[kMaxRows];
     float pd[kMaxK];
@@ -160,20 +158,56 @@ __device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t 
     return ok != 0;
 }
 
+// Address of the same shared-memory location in cluster CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+// 16 bytes into another CTA's shared memory, counted as complete_tx on that
+// CTA's mbarrier (the receiver waits on its own barrier, nobody else waits).
+__device__ __forceinline__ void st_async_v4(uint32_t dst, float4 v, uint32_t bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(dst),
+        "r"(__float_as_uint(v.x)), "r"(__float_as_uint(v.y)), "r"(__float_as_uint(v.z)),
+        "r"(__float_as_uint(v.w)), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(unsigned long long* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ unsigned long long global_ns() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
 
-// Wait for phase `parity` of `bar`, giving up after `limit_ns` (and after a
-// fixed number of polls, whichever comes first).  Returns false on give-up.
-// Between polls the warp sleeps with exponential backoff (32 ns up to 256
-// ns): a waiting warp must not take issue slots from the warps that compute.
-__device__ bool mbar_wait_bounded(unsigned long long* bar, uint32_t parity,
-                                  unsigned long long limit_ns) {
-    if (mbar_try_wait(bar, parity))
-        return true;
+// Slow path of a bounded wait: poll phase `parity` of `bar` until it
+// completes or `limit_ns` passes (also after a fixed number of polls).  Between
+// polls the warp sleeps with exponential backoff (32 ns up to 256 ns), so a
+// waiting warp takes no issue slots from the warps that compute.  Returns
+// false on give-up.
+__device__ __noinline__ bool mbar_wait_slow(unsigned long long* bar, uint32_t parity,
+                                            unsigned long long limit_ns) {
     const unsigned long long t0 = global_ns();
     unsigned sleep = 32;
     for (uint32_t it = 0; it < (1u << 26); ++it) {
@@ -186,6 +220,16 @@ __device__ bool mbar_wait_bounded(unsigned long long* bar, uint32_t parity,
             return false;
     }
     return false;
+}
+
+// Wait for phase `parity` of `bar`, giving up after `limit_ns`.  The first
+// try_wait (which itself suspends the warp for a while) nearly always
+// succeeds, so only that test is inline.
+__device__ __forceinline__ bool mbar_wait_bounded(unsigned long long* bar, uint32_t parity,
+                                                  unsigned long long limit_ns) {
+    if (mbar_try_wait(bar, parity))
+        return true;
+    return mbar_wait_slow(bar, parity, limit_ns);
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -201,13 +245,6 @@ __device__ __forceinline__ float fmax_nan(float a, float b) {
     return d;
 }
 
-// min that returns NaN when either input is NaN
-__device__ __forceinline__ float fmin_nan(float a, float b) {
-    float d;
-    asm("min.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
-    return d;
-}
-
 __device__ __forceinline__ uint32_t bf16x2_max_nan(uint32_t a, uint32_t b) {
     uint32_t d;
     asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
@@ -216,16 +253,6 @@ __device__ __forceinline__ uint32_t bf16x2_max_nan(uint32_t a, uint32_t b) {
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
-// 2^((l - m) * log2(e)/T) for a pair of entries.  The exponent is formed as
-// d*c_hi + d*c_lo with d = l - m (exact for bf16 inputs), so the only
-// roundings are the final one and the ex2 approximation.  c_lo > 0 keeps a
-// -inf entry at -inf (-inf*c_lo = -inf), so it weighs exactly 0.
-__device__ __forceinline__ float2 exp2_pair(float2 l, float2 neg_m, float2 chi, float2 clo) {
-    const float2 d = __fadd2_rn(l, neg_m);
-    const float2 y = __ffma2_rn(d, chi, __fmul2_rn(d, clo));
-    return make_float2(ex2_approx(y.x), ex2_approx(y.y));
-}
 
 // ------------------------------------------ double-float (fp32 pairs) -----
 // A value hi + lo with |lo| <= ulp(hi)/2, built from exact fp32
@@ -296,13 +323,15 @@ __device__ __forceinline__ FF exp2_arg_ff(float l, float m, float c_hi, float c_
     return fast_two_sum(p.hi, p.lo);
 }
 
-// 2^y for y = hi + lo <= 0 to about one ulp, on the FMA pipe (used for the
+// 2^y for y = hi + lo (y <= 8 here) to about one ulp, on the FMA pipe (used for the
 // few values that must be accurate: merge weights and p(x)).  y = n + f with
 // n = rint(hi) and |f| <= 1/2 (lo folded into f); 2^f = e^(f ln 2) by its
 // Taylor series to degree 7 in (f ln 2), whose truncation error on that
-// interval is below 1e-8 relative; 2^n is applied with ldexpf.
+// interval is below 1e-8 relative; 2^n is added to the exponent field (the
+// result stays normal for n >= -125; below that the weight is 0, negligible
+// next to the offset's own term of 1).
 __device__ __forceinline__ float exp2_accurate(FF y) {
-    if (!(y.hi > -160.f))
+    if (!(y.hi > -125.f))
         return 0.f;
     const float n = rintf(y.hi);
     const float f = (y.hi - n) + y.lo;
@@ -315,7 +344,7 @@ __device__ __forceinline__ float exp2_accurate(FF y) {
     p = fmaf(p, f, 2.4022650695910071e-01f);
     p = fmaf(p, f, 6.9314718055994531e-01f);
     p = fmaf(p, f, 1.0f);
-    return ldexpf(p, (int)n);
+    return __int_as_float(__float_as_int(p) + ((int)n << 23));
 }
 
 // 2^((l - m) log2e/T) accurately; 0 for l = -inf.
@@ -326,6 +355,25 @@ __device__ __forceinline__ float exp2_diff_accurate(float l, float m, float c_hi
 }
 
 // ------------------------------------------------------------ elements -----
+// Per-entry arithmetic.  An entry's weight is 2^y with y = (l - a) * c, where
+// c = log2(e)/T rounded to float and `a` is a reference logit (an offset).
+// Any offset gives the same softmax as long as every term of a sum, and the
+// merge of the sums, agree on the offset each sum is taken against.  For bf16
+// logits l - a is one mixed-precision subtraction (the bf16 operand is widened
+// exactly inside the instruction), for fp32 logits one packed subtraction per
+// pair; the product is one packed multiply per pair.
+
+// l - a for the two bf16 entries of a 32-bit word (na = -a)
+__device__ __forceinline__ float2 bf16x2_minus(uint32_t w, float na) {
+    float lo, hi;
+    asm("{\n\t.reg .b16 l, h;\n\t"
+        "mov.b32 {l, h}, %2;\n\t"
+        "add.rn.f32.bf16 %0, l, %3;\n\t"
+        "add.rn.f32.bf16 %1, h, %3;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(w), "f"(na));
+    return make_float2(lo, hi);
+}
 
 template <int ES>
 struct Elem;
@@ -333,47 +381,49 @@ template <>
 struct Elem<4> {
     static constexpr int E = 4;  // entries per 16-byte vector
     static constexpr uint32_t kNegInf = 0xff800000u;
-    __device__ static __forceinline__ void unpack(const uint4 w, float2 (&f)[2]) {
-        f[0] = make_float2(__uint_as_float(w.x), __uint_as_float(w.y));
-        f[1] = make_float2(__uint_as_float(w.z), __uint_as_float(w.w));
+    using Max = float;  // running max of raw values (NaN-propagating)
+    __device__ static __forceinline__ Max max_init() { return -INFINITY; }
+    __device__ static __forceinline__ Max vmax(const uint4 w, Max m) {
+        return fmax_nan(fmax_nan(m, fmax_nan(__uint_as_float(w.x), __uint_as_float(w.y))),
+                        fmax_nan(__uint_as_float(w.z), __uint_as_float(w.w)));
+    }
+    __device__ static __forceinline__ Max mmax(Max a, Max b) { return fmax_nan(a, b); }
+    __device__ static __forceinline__ float value(Max m) { return m; }
+    __device__ static __forceinline__ void diff(const uint4 w, float na, float2 (&d)[2]) {
+        const float2 n2 = make_float2(na, na);
+        d[0] = __fadd2_rn(make_float2(__uint_as_float(w.x), __uint_as_float(w.y)), n2);
+        d[1] = __fadd2_rn(make_float2(__uint_as_float(w.z), __uint_as_float(w.w)), n2);
     }
     __device__ static __forceinline__ float load(const void* base, int64_t idx) {
         return __ldg(static_cast<const float*>(base) + idx);
     }
-    __device__ static __forceinline__ void store_raw(unsigned char* buf, int64_t k, uint32_t bits) {
-        reinterpret_cast<uint32_t*>(buf)[k] = bits;
-    }
     __device__ static __forceinline__ uint32_t load_raw(const void* base, int64_t idx) {
         return __ldg(static_cast<const uint32_t*>(base) + idx);
-    }
-    __device__ static __forceinline__ float vec_max(const uint4 w, float m) {
-        return fmax_nan(m, fmax_nan(fmax_nan(__uint_as_float(w.x), __uint_as_float(w.y)),
-                                    fmax_nan(__uint_as_float(w.z), __uint_as_float(w.w))));
     }
 };
 template <>
 struct Elem<2> {
     static constexpr int E = 8;
     static constexpr uint32_t kNegInf = 0xff80u;
-    __device__ static __forceinline__ void unpack(const uint4 w, float2 (&f)[4]) {
-        f[0] = make_float2(bf16_lo(w.x), bf16_hi(w.x));
-        f[1] = make_float2(bf16_lo(w.y), bf16_hi(w.y));
-        f[2] = make_float2(bf16_lo(w.z), bf16_hi(w.z));
-        f[3] = make_float2(bf16_lo(w.w), bf16_hi(w.w));
+    using Max = uint32_t;  // running max of raw values as bf16x2 (NaN-propagating)
+    __device__ static __forceinline__ Max max_init() { return 0xff80ff80u; }
+    __device__ static __forceinline__ Max vmax(const uint4 w, Max m) {
+        return bf16x2_max_nan(m, bf16x2_max_nan(bf16x2_max_nan(w.x, w.y), bf16x2_max_nan(w.z, w.w)));
+    }
+    __device__ static __forceinline__ Max mmax(Max a, Max b) { return bf16x2_max_nan(a, b); }
+    __device__ static __forceinline__ float value(Max m) { return fmax_nan(bf16_lo(m), bf16_hi(m)); }
+    __device__ static __forceinline__ void diff(const uint4 w, float na, float2 (&d)[4]) {
+        d[0] = bf16x2_minus(w.x, na);
+        d[1] = bf16x2_minus(w.y, na);
+        d[2] = bf16x2_minus(w.z, na);
+        d[3] = bf16x2_minus(w.w, na);
     }
     __device__ static __forceinline__ float load(const void* base, int64_t idx) {
         const unsigned short h = __ldg(static_cast<const unsigned short*>(base) + idx);
         return __uint_as_float(static_cast<uint32_t>(h) << 16);
     }
-    __device__ static __forceinline__ void store_raw(unsigned char* buf, int64_t k, uint32_t bits) {
-        reinterpret_cast<unsigned short*>(buf)[k] = static_cast<unsigned short>(bits);
-    }
     __device__ static __forceinline__ uint32_t load_raw(const void* base, int64_t idx) {
         return __ldg(static_cast<const unsigned short*>(base) + idx);
-    }
-    __device__ static __forceinline__ float vec_max(const uint4 w, float m) {
-        const uint32_t p = bf16x2_max_nan(bf16x2_max_nan(w.x, w.y), bf16x2_max_nan(w.z, w.w));
-        return fmax_nan(m, fmax_nan(bf16_lo(p), bf16_hi(p)));
     }
 };
 
@@ -443,9 +493,8 @@ __device__ __forceinline__ int pick_lane(float part, FF incl, FF rem, int n, int
     return pos ? 31 - __clz(pos) : -1;
 }
 
-// One 16-byte vector of the slice from global memory with element loads,
-// entries at or past `lim` reading as -inf (used when rows are not 16-byte
-// aligned).
+// One 16-byte vector of a row stretch from global memory with element loads,
+// entries at or past `lim` reading as -inf (rows that are not 16-byte aligned).
 template <int ES>
 __device__ __forceinline__ uint4 load_vec_elems(const void* logits, int64_t gbase, int64_t e,
                                                 int64_t lim) {
@@ -461,107 +510,148 @@ __device__ __forceinline__ uint4 load_vec_elems(const void* logits, int64_t gbas
                           r[6] | (r[7] << 16));
 }
 
-// Folds this lane's vectors of one chunk (vector k*32 + lane of `buf`, for
-// k*32 + lane < nv) into the lane's running (max, sum of 2^((l - max)
-// log2e/T)): a max pass, one rescale if the max moved, then a sum pass, with
-// one vector live at a time.  mchk collects the NaN-propagating max so that a
-// NaN or +inf anywhere poisons the row.
-template <int ES, typename Src>
-__device__ __forceinline__ void lane_fold(const Src& src, int nv, float& m, float& s, float& mchk,
-                                          float c_hi, float c_lo) {
+// ------------------------------------------------------- row statistics -----
+
+// Sum over this lane's vectors of one chunk (vector k*32 + lane of `buf`, for
+// k*32 + lane < nv) of 2^((l - a) c), folding the raw values into the
+// NaN-propagating max `mx` on the way.  Two packed accumulators keep the
+// dependency chains short.
+template <int ES, bool FULL>
+__device__ __forceinline__ float fold_chunk(const uint4* buf, int nv, float a, float c,
+                                            typename Elem<ES>::Max& mx) {
     constexpr int E = Elem<ES>::E;
     const int lane = threadIdx.x & 31;
-    float cm = -INFINITY;
+    const float2 c2 = make_float2(c, c);
+    const float na = -a;
+    float2 s0 = make_float2(0.f, 0.f), s1 = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int k = 0; k < kVecPerLane; ++k)
-        if (k * 32 + lane < nv)
-            cm = Elem<ES>::vec_max(src(k * 32 + lane), cm);
-    mchk = fmax_nan(mchk, cm);
-    if (cm > m) {  // a new running max: rescale what was summed so far
-        if (s > 0.f) {
-            const float d = m - cm;
-            s *= ex2_approx(fmaf(d, c_hi, d * c_lo));
-        }
-        m = cm;
-    }
-    if (m > -INFINITY && m < INFINITY) {
-        const float2 neg_m = make_float2(-m, -m), chi = make_float2(c_hi, c_hi),
-                     clo = make_float2(c_lo, c_lo);
-        float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
-#pragma unroll 1
-        for (int k = 0; k < kVecPerLane; ++k) {
-            if (k * 32 + lane < nv) {
-                float2 f[E / 2];
-                Elem<ES>::unpack(src(k * 32 + lane), f);
+    for (int k = 0; k < kVecPerLane; ++k) {
+        if (FULL || k * 32 + lane < nv) {
+            const uint4 w = buf[k * 32 + lane];
+            mx = Elem<ES>::vmax(w, mx);
+            float2 d[E / 2];
+            Elem<ES>::diff(w, na, d);
 #pragma unroll
-                for (int h = 0; h < E / 2; h += 2) {
-                    a0 = __fadd2_rn(a0, exp2_pair(f[h], neg_m, chi, clo));
-                    a1 = __fadd2_rn(a1, exp2_pair(f[h + 1], neg_m, chi, clo));
-                }
+            for (int h = 0; h < E / 2; ++h) {
+                const float2 y = __fmul2_rn(d[h], c2);
+                const float2 e = make_float2(ex2_approx(y.x), ex2_approx(y.y));
+                if (h & 1)
+                    s1 = __fadd2_rn(s1, e);
+                else
+                    s0 = __fadd2_rn(s0, e);
             }
         }
-        s += (a0.x + a0.y) + (a1.x + a1.y);
     }
+    const float2 t = __fadd2_rn(s0, s1);
+    return t.x + t.y;
 }
 
-// Draw weights of E entries: the residual max(0, p - q) when RESID, else the
-// unnormalised target weights 2^((l - M) log2e/T).  Entries at or past `n`
-// weigh 0.  With RESID, q values fold into qmin (NaN-propagating) and qmax
-// for the range check.  Returns the sum of the E weights.
-template <int ES, bool RESID>
-__device__ __forceinline__ float entry_weights(const float2 (&f)[Elem<ES>::E / 2],
-                                               const float (&qq)[Elem<ES>::E], int n, float M,
-                                               float c_hi, float c_lo, float inv_s,
-                                               float (&w)[Elem<ES>::E], float& qmin,
-                                               float& qmax) {
+// One lane's running partial of a row: offset a, sum s of 2^((l - a) c) over
+// the entries seen so far, NaN-propagating max mx of the raw values.
+//
+// The offset starts at the max of the lane's entries in the row's first chunk
+// and moves only when a later chunk holds an entry more than 8 binades above
+// it (or a NaN / inf): the offset then moves up to that chunk's max, the sum
+// so far is rescaled and the chunk is summed again.  Accepted terms are
+// therefore at most 2^8 (no overflow, and y's rounding stays small for the
+// terms that dominate), and the offset is always the value of an entry the
+// lane has seen, so its own term keeps s >= 1 and terms that underflow are
+// negligible.  The per-chunk max pass of a textbook online softmax is gone;
+// the max is still tracked exactly because the reported row statistics are
+// taken against the row max.
+template <int ES>
+struct LaneSum {
+    float a, s;
+    typename Elem<ES>::Max mx;
+
+    __device__ __forceinline__ void start(const uint4* buf, int nv) {
+        const int lane = threadIdx.x & 31;
+        s = 0.f;
+        mx = Elem<ES>::max_init();
+        typename Elem<ES>::Max m0 = Elem<ES>::max_init();
+#pragma unroll
+        for (int k = 0; k < kVecPerLane; ++k)
+            if (k * 32 + lane < nv)
+                m0 = Elem<ES>::vmax(buf[k * 32 + lane], m0);
+        a = Elem<ES>::value(m0);
+    }
+
+    __device__ __forceinline__ void chunk(const uint4* buf, int nv, float c) {
+        typename Elem<ES>::Max cm = Elem<ES>::max_init();
+        const float cs = nv == kChunkVecs ? fold_chunk<ES, true>(buf, nv, a, c, cm)
+                                          : fold_chunk<ES, false>(buf, nv, a, c, cm);
+        mx = Elem<ES>::mmax(mx, cm);
+        const float m = Elem<ES>::value(cm);
+        if ((m - a) * c <= 8.f) {  // false for NaN, +inf, or no offset yet
+            s += cs;
+            return;
+        }
+        if (!(m < INFINITY)) {  // NaN or +inf: the row is poisoned through mx; stop summing
+            a = INFINITY;
+            s = 0.f;
+            return;
+        }
+        if (!(m > -INFINITY))  // an all -inf chunk seen with no offset yet adds nothing
+            return;
+        s = s > 0.f ? s * ex2_approx((a - m) * c) : 0.f;
+        a = m;
+        typename Elem<ES>::Max unused = Elem<ES>::max_init();
+        s += fold_chunk<ES, false>(buf, nv, a, c, unused);
+    }
+};
+
+// ----------------------------------------------------------------- draw -----
+
+// Draw weights of the E entries of one vector against the row offset a and
+// normaliser S (double-float in the caller, its high part here):
+//   RESID: S * max(0, p - q) = max(0, 2^((l - a) c) - q S)  (residual draw)
+//   else : S * p             = 2^((l - a) c)                (bonus / target row)
+// Entries at or past n weigh 0.  With RESID the bit patterns of q fold into
+// qbits (unsigned max) for the range check.  Returns the sum of the weights.
+template <int ES, bool RESID, bool MASK = true>
+__device__ __forceinline__ float entry_weights(const uint4 lv, const float (&qq)[Elem<ES>::E], int n,
+                                               float na, float c, float S,
+                                               float (&w)[Elem<ES>::E], uint32_t& qbits) {
     constexpr int E = Elem<ES>::E;
-    const float2 neg_m = make_float2(-M, -M), chi = make_float2(c_hi, c_hi),
-                 clo = make_float2(c_lo, c_lo);
+    const float2 c2 = make_float2(c, c), nS = make_float2(-S, -S);
+    float2 d[E / 2];
+    Elem<ES>::diff(lv, na, d);
+    float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
     for (int h = 0; h < E / 2; ++h) {
-        const float2 e = exp2_pair(f[h], neg_m, chi, clo);
+        const float2 y = __fmul2_rn(d[h], c2);
+        float2 e = make_float2(ex2_approx(y.x), ex2_approx(y.y));
+        if constexpr (RESID) {
+            e = __ffma2_rn(make_float2(qq[2 * h], qq[2 * h + 1]), nS, e);
+            e.x = fmaxf(e.x, 0.f);
+            e.y = fmaxf(e.y, 0.f);
+            qbits = __vimax3_u32(qbits, __float_as_uint(qq[2 * h]), __float_as_uint(qq[2 * h + 1]));
+        }
+        if (MASK && n < E) {
+            if (2 * h >= n)
+                e.x = 0.f;
+            if (2 * h + 1 >= n)
+                e.y = 0.f;
+        }
         w[2 * h] = e.x;
         w[2 * h + 1] = e.y;
+        acc = __fadd2_rn(acc, e);
     }
-    if constexpr (RESID) {
-#pragma unroll
-        for (int k = 0; k < E; ++k)
-            w[k] = fmaxf(__fmaf_rn(w[k], inv_s, -qq[k]), 0.f);
-    }
-    float ts = 0.f;
-    if (n >= E) {
-        if constexpr (RESID) {
-#pragma unroll
-            for (int k = 0; k < E; ++k) {
-                qmin = fmin_nan(qmin, qq[k]);
-                qmax = fmaxf(qmax, qq[k]);
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < E; ++k)
-            ts += w[k];
-    } else {
-#pragma unroll
-        for (int k = 0; k < E; ++k) {
-            if (k < n) {
-                if constexpr (RESID) {
-                    qmin = fmin_nan(qmin, qq[k]);
-                    qmax = fmaxf(qmax, qq[k]);
-                }
-            } else {
-                w[k] = 0.f;
-            }
-            ts += w[k];
-        }
-    }
-    return ts;
+    return acc.x + acc.y;
+}
+
+// q values of a residual draw are valid when each is in [0, +inf) (-0 counts
+// as 0): as unsigned bit patterns, below the +inf pattern, or exactly -0.
+__device__ __forceinline__ bool q_bits_valid(uint32_t qbits) {
+    return qbits < 0x7f800000u || qbits == 0x80000000u;
 }
 
 // --------------------------------------------------------------- kernel -----
 
-// Residency target: 1024 threads per SM (registers capped accordingly).
+// Residency target: sv::kThreadsPerSM threads per SM, seven CTAs of 128 (shared
+// memory allows no more), so a thread may use up to 72 registers.
 template <int ES, int NT>
-__global__ void __launch_bounds__(NT, 1024 / NT) sv_verify_kernel(const __grid_constant__ SvArgs a) {
+__global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(const __grid_constant__ SvArgs a) {
     constexpr int E = Elem<ES>::E;
     constexpr int NW = NT / 32;
     static_assert(NW <= kMaxWarps, "too many warps");
@@ -574,11 +664,13 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sv_verify_kernel(const __grid_c
     const int64_t V = a.V;
     const int C = a.C;
     const int G = a.G;
+    const float c = a.c;
 
     extern __shared__ __align__(128) unsigned char smem_raw[];
     SvShared& sh = *reinterpret_cast<SvShared*>(smem_raw + a.off_fixed);
     unsigned long long* bar = reinterpret_cast<unsigned long long*>(smem_raw + a.off_bar);
-    float2* part = reinterpret_cast<float2*>(smem_raw + a.off_part);  // [2][G][NW] (max, sum)
+    unsigned long long* xbar = bar + NW * kStages;  // [0..1] row partials by parity, [2..3] draw rounds
+    float4* part = reinterpret_cast<float4*>(smem_raw + a.off_part);  // [2][G][C*NW] (a, S.hi, S.lo, max)
     float* tt = reinterpret_cast<float*>(smem_raw + a.off_tt);          // [NW][ntw] draw tile totals
     unsigned char* ring = smem_raw + (size_t)warp * kStages * kChunkBytes;
     unsigned long long* wbar = bar + warp * kStages;
@@ -596,6 +688,9 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sv_verify_kernel(const __grid_c
     if (lane == 0) {
         for (int st = 0; st < kStages; ++st)
             mbar_init(&wbar[st], 1);
+        if (warp == 0)
+            for (int k = 0; k < sv::kExchangeBarriers; ++k)
+                mbar_init(&xbar[k], 1);
         fence_mbar_init();
     }
     __syncwarp();
@@ -604,45 +699,68 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sv_verify_kernel(const __grid_c
     if (tid <= K)
         sh.u[tid] = a.u[(int64_t)b * (K + 1) + tid];
     __syncthreads();
+    // the exchange barriers must be initialised everywhere before the first
+    // push: arrive now, wait just before pushing
+    cluster_arrive();
+    bool cluster_ready = false, cluster_left = false;
 
     // ---- per-warp stream through the private ring ----
-    uint32_t gi = 0, gq = 0;  // chunks issued / consumed by this warp (same in all lanes)
+    // stage indices and the consumer's phase bit advance incrementally; the
+    // counters below are the same in every lane of the warp
+    uint32_t st_issue = 0, st_wait = 0, ph_wait = 0;
+    int in_flight = 0;
     bool timed_out = false;
     auto issue = [&](const void* src, uint32_t bytes) {
         if (lane == 0) {
-            const uint32_t st = gi % kStages;
-            mbar_arrive_expect_tx(&wbar[st], bytes);
-            bulk_copy_g2s(ring + st * kChunkBytes, src, bytes, &wbar[st]);
+            mbar_arrive_expect_tx(&wbar[st_issue], bytes);
+            bulk_copy_g2s(ring + st_issue * kChunkBytes, src, bytes, &wbar[st_issue]);
         }
-        ++gi;
+        st_issue = st_issue == kStages - 1 ? 0 : st_issue + 1;
+        ++in_flight;
     };
-    auto wait_next = [&]() -> const unsigned char* {
-        const uint32_t st = gq % kStages;
-        if (!mbar_wait_bounded(&wbar[st], (gq / kStages) & 1u, a.wait_ns))
+    auto wait_next = [&]() -> const uint4* {
+        if (!mbar_wait_bounded(&wbar[st_wait], ph_wait, a.wait_ns))
             timed_out = true;
-        return ring + st * kChunkBytes;
+        return reinterpret_cast<const uint4*>(ring + st_wait * kChunkBytes);
     };
     auto release = [&]() {
         __syncwarp();
-        ++gq;
+        if (st_wait == kStages - 1) {
+            st_wait = 0;
+            ph_wait ^= 1u;
+        } else {
+            ++st_wait;
+        }
+        --in_flight;
     };
-    auto row_chunk_src = [&](int row, int c) {
-        return static_cast<const unsigned char*>(a.logits) + ((row0 + row) * V + v0) * ES +
-               (size_t)(wv0 + c * kChunkVecs) * 16;
+    const unsigned char* lstretch =
+        static_cast<const unsigned char*>(a.logits) + (row0 * V + v0) * ES + (size_t)wv0 * 16;
+    const size_t row_bytes = (size_t)V * ES;
+    auto row_chunk_src = [&](int row, int ch) {
+        return lstretch + (size_t)row * row_bytes + (size_t)ch * kChunkBytes;
     };
-    auto row_chunk_bytes = [&](int c) {
-        return (uint32_t)(min(kChunkVecs, wn - c * kChunkVecs) * 16);
+    auto row_chunk_bytes = [&](int ch) {
+        return (uint32_t)(min(kChunkVecs, wn - ch * kChunkVecs) * 16);
     };
 
-    // the first chunks of row 0 go out before the inputs are checked
-    int issued = 0;  // chunks of the current group already issued
-    if (a.bulk) {
-        const int t0 = (G < K + 1 ? G : K + 1) * nch;
-        while (issued < t0 && issued < kStages) {
-            issue(row_chunk_src(issued / nch, issued % nch), row_chunk_bytes(issued % nch));
-            ++issued;
+    // The row stream: (iss_row, iss_ch) is the next chunk to issue.  Chunks go
+    // out up to kStages ahead of consumption, across row boundaries, but never
+    // past row lim_row.
+    int iss_row = 0, iss_ch = 0, lim_row = (G < K + 1 ? G : K + 1) - 1;
+    auto top_up = [&]() {
+        if (nch == 0)
+            return;
+        while (in_flight < kStages && iss_row <= lim_row) {
+            issue(row_chunk_src(iss_row, iss_ch), row_chunk_bytes(iss_ch));
+            if (++iss_ch == nch) {
+                iss_ch = 0;
+                ++iss_row;
+            }
         }
-    }
+    };
+    // the first chunks of row 0 go out before the inputs are checked
+    if (a.bulk)
+        top_up();
 
     // ---- validation (every warp takes the same decision) ----
     int state = kStateRun, code = SV_OK;
@@ -659,156 +777,262 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sv_verify_kernel(const __grid_c
             code = SV_ERR_UNIFORM_RANGE;
         }
     }
-    if (state == kStateRun && tid < K) {
-        const int x = sh.x[tid];
-        sh.lx[tid] = Elem<ES>::load(a.logits, (row0 + tid) * V + x);
-        sh.qx[tid] = __ldg(a.q + ((int64_t)b * K + tid) * V + x);
+    float lx_lane = 0.f, qx_lane = 0.f;  // lane i: l(x_i), q(x_i), in every warp
+    if (state == kStateRun && lane < K) {
+        const int x = sh.x[lane];
+        lx_lane = Elem<ES>::load(a.logits, (row0 + lane) * V + x);
+        qx_lane = __ldg(a.q + ((int64_t)b * K + lane) * V + x);
     }
-    // (visible to every warp after the first cluster barrier)
+    const int P = C * NW;  // row partials per row: every warp of the cluster
+    uint32_t xph = 0;      // phase bits of the two row-partial barriers
 
-    // ---- the test loop: groups of rows, in order ([P1]) ----
+    // ---- the test loop: rows in order ([P1]) ----
     int j = -1, ndec = 0, mode = kModeBonus;
-    float rowM = 0.f;
+    float rowA = 0.f;
     FF rowS = {0.f, 0.f};
-    int par = 0, g0 = 0;
-    while (state == kStateRun) {
-        const int ng = G < K + 1 - g0 ? G : K + 1 - g0;
-        const int total = ng * nch;
-        int qi = 0;
-        for (int r = 0; r < ng; ++r) {
-            float m = -INFINITY, s = 0.f, mchk = -INFINITY;
-            if (a.bulk) {
-                for (int c = 0; c < nch; ++c, ++qi) {
-                    while (issued < total && issued < qi + kStages) {
-                        issue(row_chunk_src(g0 + issued / nch, issued % nch),
-                              row_chunk_bytes(issued % nch));
-                        ++issued;
-                    }
-                    const uint4* buf = reinterpret_cast<const uint4*>(wait_next());
-                    const int nv = min(kChunkVecs, wn - c * kChunkVecs);
-                    lane_fold<ES>([&](int v) { return buf[v]; }, nv, m, s, mchk, a.c_hi, a.c_lo);
-                    release();
-                }
-            } else {
-                const int64_t gbase = (row0 + g0 + r) * V + v0;
-                for (int c = 0; c < nch; ++c) {
-                    const int nv = min(kChunkVecs, wn - c * kChunkVecs);
-                    const int64_t cv = (int64_t)wv0 + (int64_t)c * kChunkVecs;
-                    lane_fold<ES>([&](int v) { return load_vec_elems<ES>(a.logits, gbase, (cv + v) * E, L); },
-                                  nv, m, s, mchk, a.c_hi, a.c_lo);
-                }
-            }
-            // this warp's partial for row g0 + r
-            const float Mw = warp_max_nan(m);
-            const float chk = warp_max_nan(mchk);
-            FF sw = {0.f, 0.f};
-            if (s > 0.f && Mw > -INFINITY && Mw < INFINITY)
-                sw = two_prod(s, exp2_diff_accurate(m, Mw, a.c_hi, a.c_lo));
-            const FF Sw = warp_sum_bcast(sw);
-            const bool any_to = __any_sync(kFull, timed_out);
-            if (lane == 0)
-                part[(par * G + r) * NW + warp] =
-                    make_float2(chk > -INFINITY && chk < INFINITY ? Mw : chk,
-                                any_to ? -1.f : Sw.hi);
-        }
-        // the first chunks of the next group go out before the decision
-        issued = 0;
-        const int g1 = g0 + ng;
-        const int ng1 = G < K + 1 - g1 ? G : K + 1 - g1;
-        if (a.bulk && a.speculate && g1 <= K) {
-            const int t1 = ng1 * nch;
-            while (issued < t1 && issued < kStages) {
-                issue(row_chunk_src(g1 + issued / nch, issued % nch), row_chunk_bytes(issued % nch));
-                ++issued;
-            }
-        }
-        cluster.sync();
 
-        // every warp combines the C * NW partials of each row in a fixed order and decides
-        const int P = C * NW;
-        for (int r = 0; r < ng && state == kStateRun; ++r) {
-            const int i = g0 + r;
-            float2 pv[kPer];
-            float mloc = -INFINITY;
-            bool to = false;
+    // Streams this warp's stretch of row `row` into ls.  After every chunk
+    // poll() may end the stream (returns false): a decision arrived that
+    // makes the row unnecessary.
+    auto stream_row = [&](int row, LaneSum<ES>& ls, auto&& poll) -> bool {
+        ls.a = -INFINITY;
+        ls.s = 0.f;
+        ls.mx = Elem<ES>::max_init();
+        for (int ch = 0; ch < nch; ++ch) {
+            const int nv = min(kChunkVecs, wn - ch * kChunkVecs);
+            const uint4* buf;
+            if (a.bulk) {
+                top_up();
+                buf = wait_next();
+            } else {
+                // rows that are not 16-byte aligned: element loads into the
+                // warp's current stage, then the same arithmetic
+                uint4* dst = reinterpret_cast<uint4*>(ring + st_wait * kChunkBytes);
+                const int64_t gbase = (row0 + row) * V + v0;
+                const int64_t cv = (int64_t)wv0 + (int64_t)ch * kChunkVecs;
+                for (int k = 0; k < kVecPerLane; ++k)
+                    if (k * 32 + lane < nv)
+                        dst[k * 32 + lane] = load_vec_elems<ES>(a.logits, gbase, (cv + k * 32 + lane) * E, L);
+                __syncwarp();
+                buf = dst;
+            }
+            if (ch == 0)
+                ls.start(buf, nv);
+            ls.chunk(buf, nv, c);
+            if (a.bulk)
+                release();
+            else
+                __syncwarp();
+            if (!poll())
+                return false;
+        }
+        return true;
+    };
+
+    // This warp's partial of a row -- offset = the lanes' largest, sum in
+    // double-float, NaN-propagating max -- pushed into slot (par, r) of every
+    // CTA of the cluster.
+    auto publish = [&](int par, int r, const LaneSum<ES>& ls) {
+        const float aw = warp_max_nan(ls.a);
+        const float mw = warp_max_nan(Elem<ES>::value(ls.mx));
+        FF sw = {0.f, 0.f};
+        if (ls.s > 0.f && aw < INFINITY)
+            sw = two_prod(ls.s, exp2_diff_accurate(ls.a, aw, a.c_hi, a.c_lo));
+        const FF Sw = warp_sum_bcast(sw);
+        const bool any_to = __any_sync(kFull, timed_out);
+        if (!cluster_ready) {
+            cluster_wait();
+            cluster_ready = true;
+        }
+        if (lane < C) {
+            const uint32_t slot = smem_addr(&part[(par * G + r) * P + rank * NW + warp]);
+            st_async_v4(mapa_shared(slot, lane), make_float4(aw, any_to ? -1.f : Sw.hi, Sw.lo, mw),
+                        mapa_shared(smem_addr(&xbar[par]), lane));
+        }
+    };
+
+    // Waits (bounded) for the partials of slot `par`.
+    auto wait_partials = [&](int par) {
+        // (exchange waits outlast a peer's own bounded ring waits, so a late
+        // peer's push lands before anyone gives up on it)
+        if (!mbar_wait_bounded(&xbar[par], (xph >> par) & 1u, 3 * a.wait_ns))
+            timed_out = true;
+        xph ^= 1u << par;
+    };
+
+    // Every warp combines the C * NW partials of row i (slot par, r) in a fixed
+    // order and takes the decision of [P1]'s loop for it.
+    auto decide = [&](int i, int par, int r) {
+        const bool xto = __any_sync(kFull, timed_out);
+        float4 pv[kPer];
+        float amax = -INFINITY, mloc = -INFINITY;
+        bool to = false;
 #pragma unroll
-            for (int t = 0; t < kPer; ++t) {
-                const int p = lane + 32 * t;
-                pv[t] = make_float2(-INFINITY, 0.f);
-                if (p < P) {
-                    pv[t] = cluster.map_shared_rank(part, p / NW)[(par * G + r) * NW + (p % NW)];
-                    mloc = fmax_nan(mloc, pv[t].x);
-                    to |= pv[t].y < 0.f;
+        for (int t = 0; t < kPer; ++t) {
+            const int p = lane + 32 * t;
+            pv[t] = make_float4(-INFINITY, 0.f, 0.f, -INFINITY);
+            if (p < P && !xto) {
+                pv[t] = part[(par * G + r) * P + p];
+                amax = fmaxf(amax, pv[t].x);
+                mloc = fmax_nan(mloc, pv[t].w);
+                to |= pv[t].y < 0.f;
+            }
+        }
+        const float M = warp_max_nan(mloc);
+#pragma unroll
+        for (int o = 16; o; o >>= 1)
+            amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+        const bool finite = M > -INFINITY && M < INFINITY;
+        FF acc = {0.f, 0.f};
+        if (finite) {
+#pragma unroll
+            for (int t = 0; t < kPer; ++t)
+                if (pv[t].y > 0.f) {
+                    const float wgt = exp2_diff_accurate(pv[t].x, amax, a.c_hi, a.c_lo);
+                    FF term = two_prod(pv[t].y, wgt);
+                    term.lo = fmaf(pv[t].z, wgt, term.lo);
+                    acc = ff_add(acc, term);
                 }
-            }
-            const float M = warp_max_nan(mloc);
-            const bool finite = M > -INFINITY && M < INFINITY;
-            FF acc = {0.f, 0.f};
-            if (finite) {
-#pragma unroll
-                for (int t = 0; t < kPer; ++t)
-                    if (pv[t].y > 0.f)
-                        acc = ff_add(acc, two_prod(pv[t].y, exp2_diff_accurate(pv[t].x, M, a.c_hi,
-                                                                                a.c_lo)));
-            }
-            const FF S = warp_sum_bcast(acc);
-            float num = 0.f;
-            if (lane == 1 && finite && i < K)
-                num = exp2_diff_accurate(sh.lx[i], M, a.c_hi, a.c_lo);
-            num = __shfl_sync(kFull, num, 1);
-            if (__any_sync(kFull, to)) {
-                state = kStateError;
-                code = SV_ERR_TIMEOUT;
-            } else if (!finite) {
+        }
+        const FF S = warp_sum_bcast(acc);
+        const float lxi = __shfl_sync(kFull, lx_lane, i & 31);
+        const float qxf = __shfl_sync(kFull, qx_lane, i & 31);
+        float num = 0.f;
+        if (lane == 1 && finite && i < K)
+            num = exp2_diff_accurate(lxi, amax, a.c_hi, a.c_lo);
+        num = __shfl_sync(kFull, num, 1);
+        if (xto || __any_sync(kFull, to)) {
+            state = kStateError;
+            code = SV_ERR_TIMEOUT;
+            return;
+        }
+        if (!finite) {
+            state = kStateError;
+            code = SV_ERR_NONFINITE;
+            return;
+        }
+        if (warp == 0 && lane == 0 && a.row_stats) {
+            // reported against the row max: S * 2^((a - M) c)
+            sh.rs_m[i] = __fdiv_rn(M, a.T);
+            const float w = exp2_diff_accurate(amax, M, a.c_hi, a.c_lo);
+            sh.rs_s[i] = fmaf(S.lo, w, S.hi * w);
+        }
+        ndec = i + 1;
+        if (i < K) {
+            if (!(qxf >= 0.f && qxf < INFINITY)) {
                 state = kStateError;
                 code = SV_ERR_NONFINITE;
-            } else {
-                if (warp == 0 && lane == 0) {
-                    sh.rs_m[i] = __fdiv_rn(M, a.T);
-                    sh.rs_s[i] = S.hi;
-                }
-                ndec = i + 1;
-                if (i < K) {
-                    const float qxf = sh.qx[i];
-                    if (!(qxf >= 0.f && qxf < INFINITY)) {
-                        state = kStateError;
-                        code = SV_ERR_NONFINITE;
-                    } else {
-                        if (warp == 0 && lane == 0)
-                            sh.pd[i] = __fdiv_rn(num, S.hi);
-                        // u < p(x)/q(x) as u * q(x) * S < 2^((l_x - M) log2e/T)
-                        const FF lhs = ff_mul(two_prod(sh.u[i], qxf), S);
-                        if (!ff_gt(FF{num, 0.f}, lhs)) {
-                            state = kStateSample;
-                            j = i;
-                            mode = kModeResidual;
-                            rowM = M;
-                            rowS = S;
-                        }
-                    }
-                } else {
-                    state = kStateSample;
-                    j = K;
-                    mode = kModeBonus;
-                    rowM = M;
-                    rowS = S;
-                }
+                return;
             }
+            if (warp == 0 && lane == 0 && a.p_draft)
+                sh.pd[i] = __fdiv_rn(num, S.hi);
+            // u < p(x)/q(x) as u * q(x) * S < 2^((l_x - a) c)
+            const FF lhs = ff_mul(two_prod(sh.u[i], qxf), S);
+            if (!ff_gt(FF{num, 0.f}, lhs)) {
+                state = kStateSample;
+                j = i;
+                mode = kModeResidual;
+                rowA = amax;
+                rowS = S;
+            }
+        } else {
+            state = kStateSample;
+            j = K;
+            mode = kModeBonus;
+            rowA = amax;
+            rowS = S;
         }
-        par ^= 1;
-        g0 = g1;
+    };
+
+    if (G == 1) {
+        // Rows stream back to back: while row cur streams, the partials of row
+        // cur - 1 arrive, and the decision on it is taken between two chunks.
+        // A rejection there ends the stream, so the next row is read only as
+        // far as it got before the decision (a few chunks per warp).
+        int cur = 0, pend = -1;
+        auto poll = [&]() -> bool {
+            if (pend < 0)
+                return true;
+            const int pp = pend & 1;
+            const bool ready = __shfl_sync(kFull, (int)mbar_test(&xbar[pp], (xph >> pp) & 1u), 0) != 0;
+            if (!ready)
+                return true;
+            xph ^= 1u << pp;
+            decide(pend, pp, 0);
+            pend = -1;
+            return state == kStateRun;
+        };
+        while (state == kStateRun) {
+            const int pc = cur & 1;
+            if (tid == 0)
+                mbar_arrive_expect_tx(&xbar[pc], (uint32_t)(P * 16));
+            lim_row = cur < K ? cur + 1 : K;
+            LaneSum<ES> ls;
+            if (!stream_row(cur, ls, poll))
+                break;
+            if (pend >= 0) {  // the decision on the previous row is still open
+                wait_partials(pend & 1);
+                decide(pend, pend & 1, 0);
+                pend = -1;
+                if (state != kStateRun)
+                    break;
+            }
+            publish(pc, 0, ls);
+            pend = cur;
+            if (cur == K) {  // the bonus row: nothing left to stream
+                wait_partials(pc);
+                decide(cur, pc, 0);
+                pend = -1;
+                break;
+            }
+            ++cur;
+        }
+    } else {
+        // Groups of G rows: every row of a group streams, the partials of the
+        // whole group meet, and the rows are decided in order.
+        int par = 0, g0 = 0;
+        auto no_poll = []() { return true; };
+        while (state == kStateRun) {
+            const int ng = G < K + 1 - g0 ? G : K + 1 - g0;
+            if (tid == 0)
+                mbar_arrive_expect_tx(&xbar[par], (uint32_t)(P * ng * 16));
+            lim_row = g0 + ng - 1;
+            for (int r = 0; r < ng; ++r) {
+                LaneSum<ES> ls;
+                (void)stream_row(g0 + r, ls, no_poll);
+                publish(par, r, ls);
+            }
+            // the first chunks of the next group go out before the decision
+            const int g1 = g0 + ng;
+            if (a.bulk && a.speculate && g1 <= K) {
+                lim_row = min(K, g1 + G - 1);
+                top_up();
+            }
+            wait_partials(par);
+            for (int r = 0; r < ng && state == kStateRun; ++r)
+                decide(g0 + r, par, r);
+            par ^= 1;
+            g0 = g1;
+        }
     }
     // speculative chunks that will not be used: let them land before the ring is reused
-    while (gq < gi) {
+    while (in_flight > 0) {
         (void)wait_next();
         release();
     }
 
     // ---- corrected or bonus draw over row j ([P1]) ----
+    // This warp's stretch of row j is walked in tiles of kDrawTile entries: a
+    // tile's draft probabilities are one ring stage, and lane l takes vectors
+    // k*32 + l (k < kDV) of the tile's logits, loaded one tile ahead (the
+    // stretch is prefetched into L2 first).  Every tile's weight total goes to
+    // `tt` for the locate step.
+    constexpr int kDrawTile = sv::kDrawTile;    // entries per draw tile
+    constexpr int kDV = kDrawTile / (32 * E);   // logits vectors per lane per tile
     const int64_t e0 = (int64_t)wv0 * E;
     const int64_t nq = max((int64_t)0, min((int64_t)wv1 * E, L) - e0);  // entries in this stretch
-    constexpr int kTile = 32 * E;
-    const int ntile = (int)((nq + kTile - 1) / kTile);
+    const int nq32 = (int)nq;
+    const int ntile = (nq32 + kDrawTile - 1) / kDrawTile;
     const unsigned char* lrow = nullptr;
     const float* qrow = nullptr;
     int owner = -1, take_last = 0;
@@ -816,116 +1040,122 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sv_verify_kernel(const __grid_c
     if (state == kStateSample) {
         lrow = static_cast<const unsigned char*>(a.logits) + ((row0 + j) * V + v0) * ES;
         qrow = j < K ? a.q + ((int64_t)b * K + j) * V + v0 : nullptr;
-        const float inv_s = __frcp_rn(rowS.hi);
+        const float na = -rowA;
+        const float Sf = rowS.hi;
+        const int64_t gbase_j = (row0 + j) * V + v0;  // element index of the slice start
         if (lane == 0 && a.bulk && nq > 0)
             bulk_prefetch_l2(lrow + e0 * ES, (uint32_t)(nq * ES));
         int sp = 0;
-        // one pass over this warp's stretch of row j: every tile's weight total
-        // goes to `tt` for the locate step; returns the stretch total.  Logits
-        // vectors load one q-chunk ahead; the draft row streams through the
-        // warp's ring when it is 16-byte aligned.
-        constexpr int kTPC = kQChunk / kTile;  // tiles per q chunk
-        const int nq32 = (int)nq;
-        const int nchunk = (nq32 + kQChunk - 1) / kQChunk;
         const unsigned char* lbase = lrow + e0 * ES;
         const float* qbase = qrow ? qrow + e0 : nullptr;
         float* tt_w = tt + warp * a.ntw;
-        float qmin = 0.f, qmax = 0.f;
-        auto load_tile_logits = [&](int t) -> uint4 {
-            const int te = t * kTile + lane * E;
-            if (t >= ntile || te >= nq32)
-                return make_uint4(0, 0, 0, 0);
-            if (a.bulk)
-                return __ldg(reinterpret_cast<const uint4*>(lbase + (size_t)te * ES));
-            return load_vec_elems<ES>(a.logits, (row0 + j) * V + v0 + e0, te, nq32);
+        uint32_t qbits = 0;
+        auto load_logits = [&](int t, uint4 (&lv)[kDV]) {
+#pragma unroll
+            for (int k = 0; k < kDV; ++k) {
+                const int ve = t * kDrawTile + (k * 32 + lane) * E;
+                if (ve >= nq32)
+                    lv[k] = make_uint4(0, 0, 0, 0);
+                else if (a.bulk)
+                    lv[k] = __ldg(reinterpret_cast<const uint4*>(lbase + (size_t)ve * ES));
+                else
+                    lv[k] = load_vec_elems<ES>(a.logits, gbase_j + e0, ve, nq32);
+            }
         };
         auto pass = [&](auto resid_tag) -> FF {
             constexpr bool RESID = decltype(resid_tag)::value;
-            const bool ring = RESID && a.qvec;
+            const bool use_ring = RESID && a.qvec;
             FF wacc = {0.f, 0.f};
-            // logits run two tiles ahead of the arithmetic
-            uint4 lv0 = load_tile_logits(0), lv1 = load_tile_logits(1);
+            uint4 lv[kDV], ln[kDV];
+            load_logits(0, lv);
             int qissued = 0;
-            for (int c = 0; c < nchunk; ++c) {
+            for (int t = 0; t < ntile; ++t) {
+                if (t + 1 < ntile)
+                    load_logits(t + 1, ln);
                 const float* qs = nullptr;
-                if (ring) {
-                    while (qissued < nchunk && qissued < c + kStages) {
-                        issue(qbase + qissued * kQChunk,
-                              (uint32_t)(min(kQChunk, nq32 - qissued * kQChunk) * 4));
+                if (use_ring) {
+                    while (qissued < ntile && qissued < t + kStages) {
+                        issue(qbase + (size_t)qissued * kDrawTile,
+                              (uint32_t)(min(kDrawTile, nq32 - qissued * kDrawTile) * 4));
                         ++qissued;
                     }
                     qs = reinterpret_cast<const float*>(wait_next());
                 }
+                const bool full = (t + 1) * kDrawTile <= nq32;
+                float ts = 0.f;
 #pragma unroll
-                for (int k = 0; k < kTPC; ++k) {
-                    const int t = c * kTPC + k;
-                    if (t < ntile) {
-                        const int te = t * kTile + lane * E;
-                        const int n = min(E, max(0, nq32 - te));
-                        const uint4 lcur = lv0;
-                        lv0 = lv1;
-                        lv1 = load_tile_logits(t + 2);
-                        float2 f[E / 2];
-                        Elem<ES>::unpack(lcur, f);
-                        float qq[E];
-                        if constexpr (RESID) {
-                            if (ring) {
-                                const float4* q4 =
-                                    reinterpret_cast<const float4*>(qs + k * kTile + lane * E);
+                for (int k = 0; k < kDV; ++k) {
+                    const int vi = k * 32 + lane;  // vector within the tile
+                    const int ve = t * kDrawTile + vi * E;
+                    const int n = full ? E : min(E, max(0, nq32 - ve));
+                    float qq[E];
+                    if constexpr (RESID) {
+                        if (use_ring) {
+                            const float4* q4 = reinterpret_cast<const float4*>(qs + vi * E);
 #pragma unroll
-                                for (int h = 0; h < E / 4; ++h) {
-                                    const float4 v4 = q4[h];
-                                    qq[4 * h] = v4.x;
-                                    qq[4 * h + 1] = v4.y;
-                                    qq[4 * h + 2] = v4.z;
-                                    qq[4 * h + 3] = v4.w;
-                                }
-                            } else {
-#pragma unroll
-                                for (int h = 0; h < E; ++h)
-                                    qq[h] = h < n ? __ldg(qbase + te + h) : 0.f;
+                            for (int h = 0; h < E / 4; ++h) {
+                                const float4 v4 = 4 * h < n ? q4[h] : make_float4(0.f, 0.f, 0.f, 0.f);
+                                qq[4 * h] = v4.x;
+                                qq[4 * h + 1] = v4.y;
+                                qq[4 * h + 2] = v4.z;
+                                qq[4 * h + 3] = v4.w;
                             }
+                        } else {
+#pragma unroll
+                            for (int h = 0; h < E; ++h)
+                                qq[h] = h < n ? __ldg(qbase + ve + h) : 0.f;
                         }
-                        float w[E];
-                        const float ts = entry_weights<ES, RESID>(f, qq, n, rowM, a.c_hi, a.c_lo,
-                                                                  inv_s, w, qmin, qmax);
-                        const float tot = warp_sum_bcast(ts);
-                        if (lane == 0)
-                            tt_w[t] = tot;
-                        wacc = ff_add(wacc, tot);
+                    } else {
+#pragma unroll
+                        for (int h = 0; h < E; ++h)
+                            qq[h] = 0.f;
                     }
+                    float w[E];
+                    ts += full ? entry_weights<ES, RESID, false>(lv[k], qq, E, na, c, Sf, w, qbits)
+                               : entry_weights<ES, RESID, true>(lv[k], qq, n, na, c, Sf, w, qbits);
                 }
-                if (ring)
+                const float tot = warp_sum_bcast(ts);
+                if (lane == 0)
+                    tt_w[t] = tot;
+                wacc = ff_add(wacc, tot);
+                if (use_ring)
                     release();
+#pragma unroll
+                for (int k = 0; k < kDV; ++k)
+                    lv[k] = ln[k];
             }
             return wacc;
         };
         for (int round = 0; round < 2; ++round) {
+            if (tid == 0)
+                mbar_arrive_expect_tx(&xbar[2 + sp], (uint32_t)(C * 16));
             const FF wacc = mode == kModeResidual ? pass(std::true_type{}) : pass(std::false_type{});
-            const bool badq = __any_sync(kFull, !(qmin >= 0.f) || !(qmax < INFINITY));
+            const bool badq = __any_sync(kFull, !q_bits_valid(qbits));
             const bool to = __any_sync(kFull, timed_out);
             if (lane == 0) {
                 sh.wtot[warp] = wacc;
                 sh.wbad[warp] = to ? 2 : (badq ? 1 : 0);
             }
             __syncthreads();
-            if (tid == 0) {
+            if (warp == 0) {
                 FF tot = {0.f, 0.f};
                 int bad = 0;
                 for (int w2 = 0; w2 < NW; ++w2) {
                     tot = ff_add(tot, sh.wtot[w2]);
                     bad = max(bad, sh.wbad[w2]);
                 }
-                sh.samp_tot[sp] = tot;
-                sh.samp_bad[sp] = bad;
+                if (lane < C)
+                    st_async_v4(mapa_shared(smem_addr(&sh.samp[sp][rank]), lane),
+                                make_float4(tot.hi, tot.lo, (float)bad, 0.f),
+                                mapa_shared(smem_addr(&xbar[2 + sp]), lane));
             }
-            cluster.sync();
+            const bool dto = !mbar_wait_bounded(&xbar[2 + sp], 0u, 3 * a.wait_ns);
             FF ctot = {0.f, 0.f};
-            int cbad = 0;
-            if (lane < C) {
-                const SvShared* rs = cluster.map_shared_rank(&sh, lane);
-                ctot = rs->samp_tot[sp];
-                cbad = rs->samp_bad[sp];
+            int cbad = __any_sync(kFull, dto) ? 2 : 0;
+            if (lane < C && !cbad) {
+                const float4 v4 = sh.samp[sp][lane];
+                ctot = FF{v4.x, v4.y};
+                cbad = (int)v4.z;
             }
 #pragma unroll
             for (int o = 16; o; o >>= 1)
@@ -955,17 +1185,20 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sv_verify_kernel(const __grid_c
             rem = ff_add(thr, ff_neg(excl));
             break;
         }
+        // no CTA of the cluster touches another's shared memory after this
+        cluster_arrive();
+        cluster_left = true;
 
         if (state == kStateSample && rank == owner && warp == 0) {
-            // warp stretch, then tile, then lane and entry: warp-parallel scans
+            // warp stretch, then tile, then sub-tile, lane and entry
             FF wtw = lane < NW ? sh.wtot[lane] : FF{0.f, 0.f};
             const FF inw = warp_incl_scan(wtw);
             const int ws = max(0, pick_lane(wtw.hi, inw, rem, NW, take_last));
             rem = ff_add(rem, ff_neg(shfl_ff(warp_excl_from_incl(inw, FF{0.f, 0.f}), ws)));
             const int wv0s = min(nvec, ws * a.wvec);
             const int64_t e0s = (int64_t)wv0s * E;
-            const int64_t nqs = max((int64_t)0, min((int64_t)min(nvec, wv0s + a.wvec) * E, L) - e0s);
-            const int ntiles = (int)((nqs + kTile - 1) / kTile);
+            const int nqs = (int)max((int64_t)0, min((int64_t)min(nvec, wv0s + a.wvec) * E, L) - e0s);
+            const int ntiles = (nqs + kDrawTile - 1) / kDrawTile;
             int tsel = -1, tlast = -1;
             FF carry = {0.f, 0.f}, at_sel = {0.f, 0.f}, at_last = {0.f, 0.f};
             for (int c0 = 0; c0 < ntiles && tsel < 0; c0 += 32) {
@@ -990,30 +1223,58 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sv_verify_kernel(const __grid_c
             }
             rem = ff_add(rem, ff_neg(at_sel));
             // re-derive the tile's weights (the same arithmetic as the pass)
-            const int64_t te = (int64_t)tsel * kTile + lane * E;
-            const int n = (int)max((int64_t)0, min((int64_t)E, nqs - te));
-            float2 f[E / 2];
-            if (a.bulk) {
+            float w[kDV][E], ts[kDV];
+#pragma unroll
+            for (int k = 0; k < kDV; ++k) {
+                const int ve = tsel * kDrawTile + (k * 32 + lane) * E;
+                const int n = min(E, max(0, nqs - ve));
                 uint4 raw = make_uint4(0, 0, 0, 0);
                 if (n > 0)
-                    raw = __ldg(reinterpret_cast<const uint4*>(lrow + (e0s + te) * ES));
-                Elem<ES>::unpack(raw, f);
-            } else {
-                Elem<ES>::unpack(load_vec_elems<ES>(a.logits, (row0 + j) * V + v0, e0s + te, e0s + nqs), f);
-            }
-            float qq[E];
+                    raw = a.bulk ? __ldg(reinterpret_cast<const uint4*>(lrow + (e0s + ve) * ES))
+                                 : load_vec_elems<ES>(a.logits, gbase_j, e0s + ve, e0s + nqs);
+                float qq[E];
 #pragma unroll
-            for (int k = 0; k < E; ++k)
-                qq[k] = (mode == kModeResidual && k < n) ? __ldg(qrow + e0s + te + k) : 0.f;
-            float w[E], qmn = 0.f, qmx = 0.f;
-            const float ts =
-                mode == kModeResidual
-                    ? entry_weights<ES, true>(f, qq, n, rowM, a.c_hi, a.c_lo, __frcp_rn(rowS.hi), w,
-                                              qmn, qmx)
-                    : entry_weights<ES, false>(f, qq, n, rowM, a.c_hi, a.c_lo, __frcp_rn(rowS.hi), w,
-                                               qmn, qmx);
-            const float inc = warp_incl_scan(ts);
-            const int pk = pick_lane(ts, FF{inc, 0.f}, rem, 32, take_last);
+                for (int h = 0; h < E; ++h)
+                    qq[h] = (mode == kModeResidual && h < n) ? __ldg(qrow + e0s + ve + h) : 0.f;
+                uint32_t qb = 0;
+                ts[k] = mode == kModeResidual
+                            ? entry_weights<ES, true>(raw, qq, n, -rowA, c, rowS.hi, w[k], qb)
+                            : entry_weights<ES, false>(raw, qq, n, -rowA, c, rowS.hi, w[k], qb);
+            }
+            // sub-tile k holds tile entries [k*32*E, (k+1)*32*E)
+            int ksel = -1, klast = -1;
+            FF run = {0.f, 0.f}, at_k = {0.f, 0.f}, at_klast = {0.f, 0.f};
+#pragma unroll
+            for (int k = 0; k < kDV; ++k) {
+                const float sk = warp_sum_bcast(ts[k]);
+                const FF nxt = ff_add(run, sk);
+                if (ksel < 0 && !take_last && ff_gt(nxt, rem)) {
+                    ksel = k;
+                    at_k = run;
+                }
+                if (sk > 0.f) {
+                    klast = k;
+                    at_klast = run;
+                }
+                run = nxt;
+            }
+            if (ksel < 0) {
+                take_last = 1;
+                ksel = max(klast, 0);
+                at_k = at_klast;
+            }
+            rem = ff_add(rem, ff_neg(at_k));
+            float tk = 0.f, wk[E];
+#pragma unroll
+            for (int k = 0; k < kDV; ++k)
+                if (k == ksel) {
+                    tk = ts[k];
+#pragma unroll
+                    for (int h = 0; h < E; ++h)
+                        wk[h] = w[k][h];
+                }
+            const float inc = warp_incl_scan(tk);
+            const int pk = pick_lane(tk, FF{inc, 0.f}, rem, 32, take_last);
             float prev = __shfl_up_sync(kFull, inc, 1);
             if (lane == 0)
                 prev = 0.f;
@@ -1024,14 +1285,14 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sv_verify_kernel(const __grid_c
                 FF acc = {ex, 0.f};
 #pragma unroll
                 for (int e = 0; e < E; ++e) {
-                    if (w[e] > 0.f)
+                    if (wk[e] > 0.f)
                         e_last = e;
-                    acc = ff_add(acc, w[e]);
+                    acc = ff_add(acc, wk[e]);
                     if (e_hit < 0 && !take_last && ff_gt(acc, rem))
                         e_hit = e;
                 }
                 const int e = e_hit >= 0 ? e_hit : e_last;
-                tok = (int)(v0 + e0s + te + (e >= 0 ? e : 0));
+                tok = (int)(v0 + e0s + tsel * kDrawTile + (ksel * 32 + lane) * E + (e >= 0 ? e : 0));
             }
             tok = __shfl_sync(kFull, tok, pk < 0 ? 0 : pk);
             // outputs of a finished sequence
@@ -1074,12 +1335,16 @@ __global__ void __launch_bounds__(NT, 1024 / NT) sv_verify_kernel(const __grid_c
     }
 
     // copies still in flight (only after an error) land before the exit
-    while (gq < gi) {
+    while (in_flight > 0) {
         (void)wait_next();
         release();
     }
-    // nobody leaves while a peer may still read its shared memory
-    cluster.sync();
+    // nobody leaves before every CTA is past its last push into the others
+    if (!cluster_ready)
+        cluster_wait();
+    if (!cluster_left)
+        cluster_arrive();
+    cluster_wait();
 }
 
 // ----------------------------------------------------------------- host -----
@@ -1186,7 +1451,7 @@ int launch(sv_ctx* ctx, const void* logits, int dtype, const float* q, const int
     if (!fn)
         return SV_ERR_UNSUPPORTED;
 
-    const sv::Layout lay = sv::layout_for(plan.slice, es, plan.group, plan.threads);
+    const sv::Layout lay = sv::layout_for(plan.slice, es, plan.group, plan.threads, plan.cluster);
     SvArgs args;
     std::memset(&args, 0, sizeof args);
     args.logits = logits;
@@ -1223,6 +1488,7 @@ int launch(sv_ctx* ctx, const void* logits, int dtype, const float* q, const int
     if ((double)args.c_hi >= c_d)
         args.c_hi = std::nextafter(args.c_hi, 0.0f);
     args.c_lo = (float)(c_d - (double)args.c_hi);
+    args.c = (float)c_d;
     args.wait_ns = ctx->wait_ns;
 
     cudaLaunchConfig_t cfg;

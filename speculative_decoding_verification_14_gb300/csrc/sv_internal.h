@@ -13,32 +13,39 @@ constexpr int kMaxCluster = 16;         // CTAs per thread-block cluster (non-po
 constexpr int kSliceAlign = 8;          // slices start on 8-entry boundaries (16 bytes of bf16)
 constexpr int kStages = 3;              // ring stages per warp
 constexpr int kChunkBytes = 2048;       // bytes per ring stage (one bulk copy)
+constexpr int kDrawTile = kChunkBytes / 4;  // entries per draw tile (its draft row fills one stage)
 constexpr int kFixedSmem = 3072;        // bytes reserved for the kernel's fixed shared state
 constexpr int kSmemPerSM = 233472;      // shared memory of one SM (228 KB)
 constexpr int kSmemPerCtaReserved = 1024;  // the runtime's per-CTA reservation
+constexpr int kThreadsPerSM = 896;      // resident threads the kernels' launch bounds target (7 CTAs of 128)
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 
-// Shared memory of one CTA: per-warp rings, the fixed state, per-warp ring
-// barriers, per-warp (max, sum) partials [2 parities][group rows][warps], and
-// the draw's per-warp tile totals.
+// Shared memory of one CTA: per-warp rings, the fixed state, the barriers
+// (per-warp ring stages, then four exchange barriers: row partials of the two
+// parities, draw totals of the two draw rounds), the row partials pushed by
+// every warp of the cluster (offset, sum hi, sum lo, max: 16 bytes)
+// [2 parities][group rows][cluster CTAs x warps], and the draw's per-warp tile
+// totals.
 struct Layout {
     int64_t wvec;       // 16-byte vectors per warp stretch
-    int64_t ntw;        // draw tiles (32 vectors) per warp stretch
+    int64_t ntw;        // draw tiles (kDrawTile entries) per warp stretch
     int64_t off_fixed, off_bar, off_part, off_tt, total;
 };
 
-inline Layout layout_for(int64_t slice, int elem_bytes, int group, int threads) {
+constexpr int kExchangeBarriers = 4;
+
+inline Layout layout_for(int64_t slice, int elem_bytes, int group, int threads, int cluster) {
     const int64_t nw = threads / 32;
     const int64_t E = 16 / elem_bytes;
     Layout l;
     l.wvec = ceil_div(ceil_div(slice, E), nw);
-    l.ntw = ceil_div(l.wvec, 32);
+    l.ntw = ceil_div(l.wvec * E, kDrawTile);
     l.off_fixed = nw * kStages * kChunkBytes;
     l.off_bar = l.off_fixed + kFixedSmem;
-    l.off_part = l.off_bar + round_up(nw * kStages * 8, 16);
-    l.off_tt = l.off_part + round_up(2 * (int64_t)group * nw * 8, 16);
+    l.off_part = l.off_bar + round_up((nw * kStages + kExchangeBarriers) * 8, 16);
+    l.off_tt = l.off_part + round_up(2 * (int64_t)group * cluster * nw * 16, 16);
     l.total = l.off_tt + round_up(nw * l.ntw * 4, 16);
     return l;
 }
