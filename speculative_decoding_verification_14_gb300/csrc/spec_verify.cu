@@ -747,14 +747,19 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
     // out up to kStages ahead of consumption, across row boundaries, but never
     // past row lim_row.
     int iss_row = 0, iss_ch = 0, lim_row = (G < K + 1 ? G : K + 1) - 1;
+    const unsigned char* iss_src = lstretch;
+    const uint32_t last_bytes = nch > 0 ? row_chunk_bytes(nch - 1) : 0u;
     auto top_up = [&]() {
         if (nch == 0)
             return;
         while (in_flight < kStages && iss_row <= lim_row) {
-            issue(row_chunk_src(iss_row, iss_ch), row_chunk_bytes(iss_ch));
+            issue(iss_src, iss_ch == nch - 1 ? last_bytes : (uint32_t)kChunkBytes);
             if (++iss_ch == nch) {
                 iss_ch = 0;
                 ++iss_row;
+                iss_src = row_chunk_src(iss_row, 0);
+            } else {
+                iss_src += kChunkBytes;
             }
         }
     };
@@ -1066,28 +1071,97 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
             constexpr bool RESID = decltype(resid_tag)::value;
             const bool use_ring = RESID && a.qvec;
             FF wacc = {0.f, 0.f};
-            uint4 lv[kDV], ln[kDV];
-            load_logits(0, lv);
             int qissued = 0;
-            for (int t = 0; t < ntile; ++t) {
-                if (t + 1 < ntile)
-                    load_logits(t + 1, ln);
+            // the draft row's stages go out up to kStages tiles ahead
+            auto q_top_up = [&](int t) {
+                while (qissued < ntile && qissued < t + kStages) {
+                    issue(qbase + (size_t)qissued * kDrawTile,
+                          (uint32_t)(min(kDrawTile, nq32 - qissued * kDrawTile) * 4));
+                    ++qissued;
+                }
+            };
+            if (use_ring)
+                q_top_up(0);
+            auto tile_done = [&](int t, float ts) {
+                const float tot = warp_sum_bcast(ts);
+                if (lane == 0)
+                    tt_w[t] = tot;
+                wacc = ff_add(wacc, tot);
+            };
+            // Full tiles of 16-byte aligned rows: no masks, a pointer that
+            // advances a tile at a time, the next tile's logits in flight.
+            const int nfull = (a.bulk && (use_ring || !RESID)) ? nq32 / kDrawTile : 0;
+            if (nfull > 0) {
+                const float2 c2 = make_float2(c, c), nS = make_float2(-Sf, -Sf);
+                const uint4* lp = reinterpret_cast<const uint4*>(lbase) + lane;
+                uint4 lv[kDV];
+#pragma unroll
+                for (int k = 0; k < kDV; ++k)
+                    lv[k] = __ldg(lp + k * 32);
+                for (int t = 0; t < nfull; ++t) {
+                    uint4 cur[kDV];
+#pragma unroll
+                    for (int k = 0; k < kDV; ++k)
+                        cur[k] = lv[k];
+                    if (t + 1 < nfull) {
+                        lp += kDrawTile * ES / 16;
+#pragma unroll
+                        for (int k = 0; k < kDV; ++k)
+                            lv[k] = __ldg(lp + k * 32);
+                    }
+                    const float4* q4 = nullptr;
+                    if constexpr (RESID)
+                        q4 = reinterpret_cast<const float4*>(wait_next());
+                    float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int k = 0; k < kDV; ++k) {
+                        float2 d[E / 2];
+                        Elem<ES>::diff(cur[k], na, d);
+                        float2 qp[E / 2];
+                        if constexpr (RESID) {
+#pragma unroll
+                            for (int h = 0; h < E / 4; ++h) {
+                                const float4 v4 = q4[(k * 32 + lane) * (E / 4) + h];
+                                qp[2 * h] = make_float2(v4.x, v4.y);
+                                qp[2 * h + 1] = make_float2(v4.z, v4.w);
+                            }
+                        }
+#pragma unroll
+                        for (int h = 0; h < E / 2; ++h) {
+                            const float2 y = __fmul2_rn(d[h], c2);
+                            float2 e = make_float2(ex2_approx(y.x), ex2_approx(y.y));
+                            if constexpr (RESID) {
+                                e = __ffma2_rn(qp[h], nS, e);
+                                e.x = fmaxf(e.x, 0.f);
+                                e.y = fmaxf(e.y, 0.f);
+                                qbits = __vimax3_u32(qbits, __float_as_uint(qp[h].x),
+                                                     __float_as_uint(qp[h].y));
+                            }
+                            acc = __fadd2_rn(acc, e);
+                        }
+                    }
+                    if (use_ring) {
+                        release();
+                        q_top_up(t + 1);
+                    }
+                    tile_done(t, acc.x + acc.y);
+                }
+            }
+            // the rest: a partial last tile, or rows that need element loads
+            for (int t = nfull; t < ntile; ++t) {
+                uint4 lv[kDV];
+                load_logits(t, lv);
                 const float* qs = nullptr;
                 if (use_ring) {
-                    while (qissued < ntile && qissued < t + kStages) {
-                        issue(qbase + (size_t)qissued * kDrawTile,
-                              (uint32_t)(min(kDrawTile, nq32 - qissued * kDrawTile) * 4));
-                        ++qissued;
-                    }
+                    q_top_up(t);
                     qs = reinterpret_cast<const float*>(wait_next());
                 }
-                const bool full = (t + 1) * kDrawTile <= nq32;
                 float ts = 0.f;
 #pragma unroll
                 for (int k = 0; k < kDV; ++k) {
                     const int vi = k * 32 + lane;  // vector within the tile
                     const int ve = t * kDrawTile + vi * E;
-                    const int n = full ? E : min(E, max(0, nq32 - ve));
+                    const int n = min(E, max(0, nq32 - ve));
                     float qq[E];
                     if constexpr (RESID) {
                         if (use_ring) {
@@ -1111,18 +1185,11 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
                             qq[h] = 0.f;
                     }
                     float w[E];
-                    ts += full ? entry_weights<ES, RESID, false>(lv[k], qq, E, na, c, Sf, w, qbits)
-                               : entry_weights<ES, RESID, true>(lv[k], qq, n, na, c, Sf, w, qbits);
+                    ts += entry_weights<ES, RESID, true>(lv[k], qq, n, na, c, Sf, w, qbits);
                 }
-                const float tot = warp_sum_bcast(ts);
-                if (lane == 0)
-                    tt_w[t] = tot;
-                wacc = ff_add(wacc, tot);
                 if (use_ring)
                     release();
-#pragma unroll
-                for (int k = 0; k < kDV; ++k)
-                    lv[k] = ln[k];
+                tile_done(t, ts);
             }
             return wacc;
         };
