@@ -179,6 +179,12 @@ __device__ __forceinline__ void cluster_arrive() {
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
 
+// Arrive with no memory ordering: used where the barrier only bounds CTA
+// lifetimes and carries no data.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -470,6 +476,18 @@ __device__ __forceinline__ FF warp_incl_scan(FF v) {
         const FF n = shfl_up_ff(v, o);
         if (lane >= o)
             v = ff_add(v, n);
+    }
+    return v;
+}
+
+// Inclusive double-float scan over the first n lanes (lanes >= n hold
+// whatever arrives; callers ignore them).  log2(n) steps instead of five.
+__device__ __forceinline__ FF warp_incl_scan_n(FF v, int n) {
+    const int lane = threadIdx.x & 31;
+    for (int o = 1; o < n; o <<= 1) {
+        const FF u = shfl_up_ff(v, o);
+        if (lane >= o)
+            v = ff_add(v, u);
     }
     return v;
 }
@@ -1227,7 +1245,7 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
 #pragma unroll
             for (int o = 16; o; o >>= 1)
                 cbad = max(cbad, __shfl_xor_sync(kFull, cbad, o));
-            const FF incl = warp_incl_scan(ctot);
+            const FF incl = warp_incl_scan_n(ctot, C);
             const FF S = shfl_ff(incl, C - 1);
             const FF thr = ff_mul(FF{sh.u[K], 0.f}, S);
             take_last = 0;
@@ -1253,42 +1271,80 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
             break;
         }
         // no CTA of the cluster touches another's shared memory after this
-        cluster_arrive();
+        // (every push into a CTA has landed before it passed the exchange)
+        cluster_arrive_relaxed();
         cluster_left = true;
 
         if (state == kStateSample && rank == owner && warp == 0) {
-            // warp stretch, then tile, then sub-tile, lane and entry
-            FF wtw = lane < NW ? sh.wtot[lane] : FF{0.f, 0.f};
-            const FF inw = warp_incl_scan(wtw);
-            const int ws = max(0, pick_lane(wtw.hi, inw, rem, NW, take_last));
-            rem = ff_add(rem, ff_neg(shfl_ff(warp_excl_from_incl(inw, FF{0.f, 0.f}), ws)));
-            const int wv0s = min(nvec, ws * a.wvec);
-            const int64_t e0s = (int64_t)wv0s * E;
-            const int nqs = (int)max((int64_t)0, min((int64_t)min(nvec, wv0s + a.wvec) * E, L) - e0s);
-            const int ntiles = (nqs + kDrawTile - 1) / kDrawTile;
-            int tsel = -1, tlast = -1;
+            // Tile, then sub-tile, lane and entry.  The CTA's tiles in
+            // vocabulary order are warp-major: flat index f = w * ntw + t, and
+            // tiles past a warp's stretch weigh 0.  Lane l takes kTL
+            // consecutive flat tiles per round, so one scan across lanes
+            // covers 32 * kTL tiles.
+            constexpr int kTL = 4;
+            const int ntw = a.ntw;
+            const int nflat = NW * ntw;
+            auto tile_total = [&](int f) -> float {
+                if (f >= nflat)
+                    return 0.f;
+                const int w = f / ntw, t = f - (f / ntw) * ntw;
+                const int wv0w = min(nvec, w * a.wvec);
+                const int nqw = (int)max((int64_t)0, min((int64_t)min(nvec, wv0w + a.wvec) * E, L) - (int64_t)wv0w * E);
+                return t * kDrawTile < nqw ? tt[f] : 0.f;
+            };
+            int fsel = -1, flast = -1;
             FF carry = {0.f, 0.f}, at_sel = {0.f, 0.f}, at_last = {0.f, 0.f};
-            for (int c0 = 0; c0 < ntiles && tsel < 0; c0 += 32) {
-                const float tv = c0 + lane < ntiles ? tt[ws * a.ntw + c0 + lane] : 0.f;
-                const FF in = ff_add(warp_incl_scan(FF{tv, 0.f}), carry);
+            for (int c0 = 0; c0 < nflat && fsel < 0; c0 += 32 * kTL) {
+                float tv[kTL];
+                FF ls_ = {0.f, 0.f};
+#pragma unroll
+                for (int k = 0; k < kTL; ++k) {
+                    tv[k] = tile_total(c0 + lane * kTL + k);
+                    ls_ = ff_add(ls_, tv[k]);
+                }
+                const FF in = ff_add(warp_incl_scan(ls_), carry);
                 const FF ex = warp_excl_from_incl(in, carry);
                 int tl = take_last;
-                const int pk = pick_lane(tv, in, rem, ntiles - c0, tl);
-                if (!tl && pk >= 0) {
-                    tsel = c0 + pk;
-                    at_sel = shfl_ff(ex, pk);
-                } else if (pk >= 0) {
-                    tlast = c0 + pk;
-                    at_last = shfl_ff(ex, pk);
+                const int pk = pick_lane(ls_.hi, in, rem, 32, tl);
+                if (pk >= 0) {
+                    // within lane pk's kTL tiles, in order
+                    FF run = shfl_ff(ex, pk);
+                    int hit = -1, last = -1;
+                    FF at_hit = {0.f, 0.f}, at_l = {0.f, 0.f};
+#pragma unroll
+                    for (int k = 0; k < kTL; ++k) {
+                        const float v = __shfl_sync(kFull, tv[k], pk);
+                        const FF nxt = ff_add(run, v);
+                        if (hit < 0 && !tl && ff_gt(nxt, rem)) {
+                            hit = k;
+                            at_hit = run;
+                        }
+                        if (v > 0.f) {
+                            last = k;
+                            at_l = run;
+                        }
+                        run = nxt;
+                    }
+                    if (hit >= 0) {
+                        fsel = c0 + pk * kTL + hit;
+                        at_sel = at_hit;
+                    } else if (last >= 0) {
+                        flast = c0 + pk * kTL + last;
+                        at_last = at_l;
+                    }
                 }
                 carry = shfl_ff(in, 31);
             }
-            if (tsel < 0) {
+            if (fsel < 0) {
                 take_last = 1;
-                tsel = max(tlast, 0);
+                fsel = max(flast, 0);
                 at_sel = at_last;
             }
             rem = ff_add(rem, ff_neg(at_sel));
+            const int ws = fsel / ntw, tsel = fsel - ws * ntw;
+            const int wv0s = min(nvec, ws * a.wvec);
+            const int64_t e0s = (int64_t)wv0s * E;
+            const int nqs = (int)max((int64_t)0, min((int64_t)min(nvec, wv0s + a.wvec) * E, L) - e0s);
             // re-derive the tile's weights (the same arithmetic as the pass)
             float w[kDV][E], ts[kDV];
 #pragma unroll
@@ -1300,9 +1356,20 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
                     raw = a.bulk ? __ldg(reinterpret_cast<const uint4*>(lrow + (e0s + ve) * ES))
                                  : load_vec_elems<ES>(a.logits, gbase_j, e0s + ve, e0s + nqs);
                 float qq[E];
+                if (mode == kModeResidual && a.qvec && n == E) {
 #pragma unroll
-                for (int h = 0; h < E; ++h)
-                    qq[h] = (mode == kModeResidual && h < n) ? __ldg(qrow + e0s + ve + h) : 0.f;
+                    for (int h = 0; h < E / 4; ++h) {
+                        const float4 v4 = __ldg(reinterpret_cast<const float4*>(qrow + e0s + ve) + h);
+                        qq[4 * h] = v4.x;
+                        qq[4 * h + 1] = v4.y;
+                        qq[4 * h + 2] = v4.z;
+                        qq[4 * h + 3] = v4.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int h = 0; h < E; ++h)
+                        qq[h] = (mode == kModeResidual && h < n) ? __ldg(qrow + e0s + ve + h) : 0.f;
+                }
                 uint32_t qb = 0;
                 ts[k] = mode == kModeResidual
                             ? entry_weights<ES, true>(raw, qq, n, -rowA, c, rowS.hi, w[k], qb)
@@ -1345,23 +1412,22 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
             float prev = __shfl_up_sync(kFull, inc, 1);
             if (lane == 0)
                 prev = 0.f;
-            const float ex = __shfl_sync(kFull, prev, pk < 0 ? 0 : pk);
-            int tok = -1;
-            if (lane == pk) {
-                int e_hit = -1, e_last = -1;
-                FF acc = {ex, 0.f};
+            const int src = pk < 0 ? 0 : pk;
+            const float ex = __shfl_sync(kFull, prev, src);
+            // the entry: lane pk's E weights spread over lanes 0..E-1, one scan
+            float we = 0.f;
 #pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    if (wk[e] > 0.f)
-                        e_last = e;
-                    acc = ff_add(acc, wk[e]);
-                    if (e_hit < 0 && !take_last && ff_gt(acc, rem))
-                        e_hit = e;
-                }
-                const int e = e_hit >= 0 ? e_hit : e_last;
-                tok = (int)(v0 + e0s + tsel * kDrawTile + (ksel * 32 + lane) * E + (e >= 0 ? e : 0));
+            for (int e = 0; e < E; ++e) {
+                const float v = __shfl_sync(kFull, wk[e], src);
+                if (lane == e)
+                    we = v;
             }
-            tok = __shfl_sync(kFull, tok, pk < 0 ? 0 : pk);
+            const FF ine = ff_add(warp_incl_scan_n(FF{we, 0.f}, E), FF{ex, 0.f});
+            int tle = take_last;
+            int e = pick_lane(we, ine, rem, E, tle);
+            if (e < 0)
+                e = 0;
+            const int tok = (int)(v0 + e0s + tsel * kDrawTile + (ksel * 32 + src) * E + e);
             // outputs of a finished sequence
             for (int i = lane; i <= K; i += 32) {
                 a.out_tokens[(int64_t)b * (K + 1) + i] = i < j ? sh.x[i] : (i == j ? tok : -1);
