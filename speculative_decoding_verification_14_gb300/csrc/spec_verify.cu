@@ -107,6 +107,8 @@ struct __align__(16) SvShared {
     float rs_m[kMaxRows];
     float rs_s[kMaxRows];
     float pd[kMaxK];
+    float4 grp[kMaxRows];   // a group's row outcomes (amax, M, num, kind)
+    float2 grpS[kMaxRows];  // ... and their normalisers (hi, lo)
 };
 static_assert(sizeof(SvShared) + 64 <= sv::kFixedSmem, "fixed shared state outgrew its reservation");
 
@@ -883,9 +885,15 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
         xph ^= 1u << par;
     };
 
-    // Every warp combines the C * NW partials of row i (slot par, r) in a fixed
-    // order and takes the decision of [P1]'s loop for it.
-    auto decide = [&](int i, int par, int r) {
+    // The combined statistics of row i and what its test concluded.
+    struct RowOutcome {
+        float amax, M, num;
+        FF S;
+        int kind;  // 0 accept, 1 reject (or bonus row), 2 timeout, 3 non-finite
+    };
+    // A warp combines the C * NW partials of row i (slot par, r) in a fixed
+    // order and evaluates [P1]'s test for it.
+    auto merge_row = [&](int i, int par, int r) -> RowOutcome {
         const bool xto = __any_sync(kFull, timed_out);
         float4 pv[kPer];
         float amax = -INFINITY, mloc = -INFINITY;
@@ -901,11 +909,13 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
                 to |= pv[t].y < 0.f;
             }
         }
-        const float M = warp_max_nan(mloc);
+        RowOutcome o;
+        o.M = warp_max_nan(mloc);
 #pragma unroll
-        for (int o = 16; o; o >>= 1)
-            amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
-        const bool finite = M > -INFINITY && M < INFINITY;
+        for (int sft = 16; sft; sft >>= 1)
+            amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, sft));
+        o.amax = amax;
+        const bool finite = o.M > -INFINITY && o.M < INFINITY;
         FF acc = {0.f, 0.f};
         if (finite) {
 #pragma unroll
@@ -917,55 +927,58 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
                     acc = ff_add(acc, term);
                 }
         }
-        const FF S = warp_sum_bcast(acc);
+        o.S = warp_sum_bcast(acc);
         const float lxi = __shfl_sync(kFull, lx_lane, i & 31);
         const float qxf = __shfl_sync(kFull, qx_lane, i & 31);
         float num = 0.f;
         if (lane == 1 && finite && i < K)
             num = exp2_diff_accurate(lxi, amax, a.c_hi, a.c_lo);
-        num = __shfl_sync(kFull, num, 1);
-        if (xto || __any_sync(kFull, to)) {
+        o.num = __shfl_sync(kFull, num, 1);
+        if (xto || __any_sync(kFull, to))
+            o.kind = 2;
+        else if (!finite || (i < K && !(qxf >= 0.f && qxf < INFINITY)))
+            o.kind = 3;
+        else if (i == K)
+            o.kind = 1;
+        else  // u < p(x)/q(x) as u * q(x) * S < 2^((l_x - a) c)
+            o.kind = ff_gt(FF{o.num, 0.f}, ff_mul(two_prod(sh.u[i], qxf), o.S)) ? 0 : 1;
+        return o;
+    };
+    // The loop of [P1] acting on row i's outcome.
+    auto apply_row = [&](int i, const RowOutcome& o) {
+        if (o.kind == 2) {
             state = kStateError;
             code = SV_ERR_TIMEOUT;
             return;
         }
-        if (!finite) {
+        if (o.kind == 3 && !(o.M > -INFINITY && o.M < INFINITY)) {
             state = kStateError;
             code = SV_ERR_NONFINITE;
             return;
         }
         if (warp == 0 && lane == 0 && a.row_stats) {
             // reported against the row max: S * 2^((a - M) c)
-            sh.rs_m[i] = __fdiv_rn(M, a.T);
-            const float w = exp2_diff_accurate(amax, M, a.c_hi, a.c_lo);
-            sh.rs_s[i] = fmaf(S.lo, w, S.hi * w);
+            sh.rs_m[i] = __fdiv_rn(o.M, a.T);
+            const float w = exp2_diff_accurate(o.amax, o.M, a.c_hi, a.c_lo);
+            sh.rs_s[i] = fmaf(o.S.lo, w, o.S.hi * w);
         }
         ndec = i + 1;
-        if (i < K) {
-            if (!(qxf >= 0.f && qxf < INFINITY)) {
-                state = kStateError;
-                code = SV_ERR_NONFINITE;
-                return;
-            }
-            if (warp == 0 && lane == 0 && a.p_draft)
-                sh.pd[i] = __fdiv_rn(num, S.hi);
-            // u < p(x)/q(x) as u * q(x) * S < 2^((l_x - a) c)
-            const FF lhs = ff_mul(two_prod(sh.u[i], qxf), S);
-            if (!ff_gt(FF{num, 0.f}, lhs)) {
-                state = kStateSample;
-                j = i;
-                mode = kModeResidual;
-                rowA = amax;
-                rowS = S;
-            }
-        } else {
+        if (o.kind == 3) {  // the draft probability of x_i is not a probability
+            state = kStateError;
+            code = SV_ERR_NONFINITE;
+            return;
+        }
+        if (i < K && warp == 0 && lane == 0 && a.p_draft)
+            sh.pd[i] = __fdiv_rn(o.num, o.S.hi);
+        if (o.kind == 1) {
             state = kStateSample;
-            j = K;
-            mode = kModeBonus;
-            rowA = amax;
-            rowS = S;
+            j = i;
+            mode = i < K ? kModeResidual : kModeBonus;
+            rowA = o.amax;
+            rowS = o.S;
         }
     };
+    auto decide = [&](int i, int par, int r) { apply_row(i, merge_row(i, par, r)); };
 
     if (G == 1) {
         // Rows stream back to back: while row cur streams, the partials of row
@@ -1032,8 +1045,28 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
                 top_up();
             }
             wait_partials(par);
-            for (int r = 0; r < ng && state == kStateRun; ++r)
-                decide(g0 + r, par, r);
+            // the group's rows are combined in parallel, one warp per row,
+            // then every warp walks the outcomes in order
+            for (int r = warp; r < ng; r += NW) {
+                const RowOutcome o = merge_row(g0 + r, par, r);
+                if (lane == 0) {
+                    sh.grp[r] = make_float4(o.amax, o.M, o.num, __int_as_float(o.kind));
+                    sh.grpS[r] = make_float2(o.S.hi, o.S.lo);
+                }
+            }
+            __syncthreads();
+            for (int r = 0; r < ng && state == kStateRun; ++r) {
+                const float4 g4 = sh.grp[r];
+                const float2 g2 = sh.grpS[r];
+                RowOutcome o;
+                o.amax = g4.x;
+                o.M = g4.y;
+                o.num = g4.z;
+                o.kind = __float_as_int(g4.w);
+                o.S = FF{g2.x, g2.y};
+                apply_row(g0 + r, o);
+            }
+            __syncthreads();  // the outcome slots are reused by the next group
             par ^= 1;
             g0 = g1;
         }
