@@ -143,6 +143,24 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
         : "memory");
 }
 
+// L2 eviction policy "evict first": for data read once (the draft row of a
+// draw), so that it does not push out logits that a draw may read again.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// The bulk copy above with an L2 eviction policy.
+__device__ __forceinline__ void bulk_copy_g2s_hint(void* dst, const void* src, uint32_t bytes,
+                                                   unsigned long long* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
 // Bulk prefetch of a global range into L2 (no destination, no completion).
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
@@ -730,10 +748,14 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
     uint32_t st_issue = 0, st_wait = 0, ph_wait = 0;
     int in_flight = 0;
     bool timed_out = false;
-    auto issue = [&](const void* src, uint32_t bytes) {
+    auto issue = [&](const void* src, uint32_t bytes, bool read_once = false) {
         if (lane == 0) {
             mbar_arrive_expect_tx(&wbar[st_issue], bytes);
-            bulk_copy_g2s(ring + st_issue * kChunkBytes, src, bytes, &wbar[st_issue]);
+            if (read_once)
+                bulk_copy_g2s_hint(ring + st_issue * kChunkBytes, src, bytes, &wbar[st_issue],
+                                   l2_policy_evict_first());
+            else
+                bulk_copy_g2s(ring + st_issue * kChunkBytes, src, bytes, &wbar[st_issue]);
         }
         st_issue = st_issue == kStages - 1 ? 0 : st_issue + 1;
         ++in_flight;
@@ -1127,7 +1149,7 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
             auto q_top_up = [&](int t) {
                 while (qissued < ntile && qissued < t + kStages) {
                     issue(qbase + (size_t)qissued * kDrawTile,
-                          (uint32_t)(min(kDrawTile, nq32 - qissued * kDrawTile) * 4));
+                          (uint32_t)(min(kDrawTile, nq32 - qissued * kDrawTile) * 4), true);
                     ++qissued;
                 }
             };

@@ -137,7 +137,7 @@ def stat_errors(g: dict, o: dict) -> dict:
     """Largest relative errors of the GPU's softmax normaliser and p(x)."""
     both = ~np.isnan(o["row_s"]) & ~np.isnan(g["row_s"])
     res = {"row_s_rel": float(np.max(_rel(g["row_s"][both], o["row_s"][both]))) if both.any() else 0.0}
-    if o["p_draft"].size:
+    if o["p_draft"].size and "p_draft" in g:
         bp = ~np.isnan(o["p_draft"]) & ~np.isnan(g["p_draft"])
         res["p_draft_rel"] = float(np.max(_rel(g["p_draft"][bp], o["p_draft"][bp]))) if bp.any() else 0.0
     return res

@@ -189,6 +189,37 @@ def test_device_errors_mark_only_their_sequence_and_clear():
     assert v.error() == (sv.SV_OK, 0)
 
 
+@pytest.mark.parametrize("name", workloads.CONFIG_ORDER)
+def test_without_row_stats_nothing_changes(name):
+    """Without row_stats the kernel drops the exact running max from its fold;
+    the offsets move at the same chunks, so lengths, tokens, masks and statuses
+    must be the same bits as with row_stats, and still match the oracle."""
+    inp = workloads.make_config(name)
+    on = gh.gpu_verify_inputs(inp, stats=True)
+    off = gh.gpu_verify_inputs(inp, stats=False)
+    for k in ("accept_len", "out_tokens", "accept_mask", "status"):
+        np.testing.assert_array_equal(off[k], on[k], err_msg=k)
+    info = gh.compare(off, oracle.verify_inputs(inp), inp.K, check_stats=False, label=name + "/no_stats")
+    assert info["exact"] + info["accept_ties"] + info["draw_ties"] == inp.B
+
+
+def test_special_values_without_row_stats():
+    """NaN, +inf and all -inf rows are still caught when the running max is not kept."""
+    import speculative_decoding_verification_14_gb300 as sv
+    inp = workloads.make_random(6, 3, 3000, dtype="bf16", seed=15)
+    lg = inp.logits.copy()
+    lg[0, 1, 2900] = 0x7FC0                      # NaN late in row 1
+    lg[1, 0, 5] = 0x7F80                         # +inf early in row 0
+    lg[2, 0, :] = 0xFF80                         # row 0 entirely -inf
+    lg[3, :, ::2] = 0xFF80                       # -inf in half the vocabulary: still valid
+    inp.logits = lg
+    o = oracle.verify_inputs(inp)
+    g = gh.gpu_verify_inputs(inp, stats=False)
+    gh.compare(g, o, 3, check_stats=False, label="special_no_stats")
+    assert g["status"][1] == sv.SV_ERR_NONFINITE and g["status"][2] == sv.SV_ERR_NONFINITE
+    gh.verifier().error()  # clear the sticky word for the tests after this one
+
+
 def test_host_side_validation_launches_nothing():
     import speculative_decoding_verification_14_gb300 as sv
     import torch
