@@ -107,6 +107,12 @@ struct __align__(16) SvShared {
     float rs_m[kMaxRows];
     float rs_s[kMaxRows];
     float pd[kMaxK];
+    // one-row steps: the warp that first finds a row's partials complete
+    // decides it and posts the outcome here for the CTA's other warps
+    int claim;     // rows claimed so far (row i is claimed by moving it from i to i + 1)
+    int rec_row;   // the row whose outcome the record holds
+    int rec_state, rec_code, rec_j, rec_mode, rec_ndec;
+    float rec_A, rec_Shi, rec_Slo;
     float4 grp[kMaxRows];   // a group's row outcomes (amax, M, num, kind)
     float2 grpS[kMaxRows];  // ... and their normalisers (hi, lo)
 };
@@ -219,6 +225,16 @@ __device__ __forceinline__ bool mbar_test(unsigned long long* bar, uint32_t pari
         : "r"(smem_addr(bar)), "r"(parity)
         : "memory");
     return ok != 0;
+}
+
+__device__ __forceinline__ int ld_acquire_cta(const int* p) {
+    int v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_cta(int* p, int v) {
+    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ unsigned long long global_ns() {
@@ -736,6 +752,10 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
         sh.x[tid] = a.tokens[(int64_t)b * K + tid];
     if (tid <= K)
         sh.u[tid] = a.u[(int64_t)b * (K + 1) + tid];
+    if (tid == 0) {
+        sh.claim = 0;
+        sh.rec_row = -1;
+    }
     __syncthreads();
     // the exchange barriers must be initialised everywhere before the first
     // push: arrive now, wait just before pushing
@@ -966,8 +986,9 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
             o.kind = ff_gt(FF{o.num, 0.f}, ff_mul(two_prod(sh.u[i], qxf), o.S)) ? 0 : 1;
         return o;
     };
-    // The loop of [P1] acting on row i's outcome.
-    auto apply_row = [&](int i, const RowOutcome& o) {
+    // The loop of [P1] acting on row i's outcome; `writer` warps also record
+    // the optional per-row outputs.
+    auto apply_row = [&](int i, const RowOutcome& o, bool writer) {
         if (o.kind == 2) {
             state = kStateError;
             code = SV_ERR_TIMEOUT;
@@ -978,7 +999,7 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
             code = SV_ERR_NONFINITE;
             return;
         }
-        if (warp == 0 && lane == 0 && a.row_stats) {
+        if (writer && lane == 0 && a.row_stats) {
             // reported against the row max: S * 2^((a - M) c)
             sh.rs_m[i] = __fdiv_rn(o.M, a.T);
             const float w = exp2_diff_accurate(o.amax, o.M, a.c_hi, a.c_lo);
@@ -990,7 +1011,7 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
             code = SV_ERR_NONFINITE;
             return;
         }
-        if (i < K && warp == 0 && lane == 0 && a.p_draft)
+        if (i < K && writer && lane == 0 && a.p_draft)
             sh.pd[i] = __fdiv_rn(o.num, o.S.hi);
         if (o.kind == 1) {
             state = kStateSample;
@@ -1000,7 +1021,7 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
             rowS = o.S;
         }
     };
-    auto decide = [&](int i, int par, int r) { apply_row(i, merge_row(i, par, r)); };
+    auto decide = [&](int i, int par, int r) { apply_row(i, merge_row(i, par, r), true); };
 
     if (G == 1) {
         // Rows stream back to back: while row cur streams, the partials of row
@@ -1008,17 +1029,79 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
         // A rejection there ends the stream, so the next row is read only as
         // far as it got before the decision (a few chunks per warp).
         int cur = 0, pend = -1;
+        // One warp per CTA decides a row -- the first to find its partials
+        // complete -- and posts the outcome; the others pick it up.
+        auto take_record = [&]() {
+            state = sh.rec_state;
+            code = sh.rec_code;
+            j = sh.rec_j;
+            mode = sh.rec_mode;
+            ndec = sh.rec_ndec;
+            rowA = sh.rec_A;
+            rowS = FF{sh.rec_Shi, sh.rec_Slo};
+        };
+        auto record_posted = [&](int i) {
+            // every lane acquires, so each lane's reads of the record follow it
+            return __all_sync(kFull, ld_acquire_cta(&sh.rec_row) >= i);
+        };
+        auto decide_claimed = [&](int i) -> bool {  // true if this warp decided row i
+            int won = 0;
+            if (lane == 0)
+                won = atomicCAS(&sh.claim, i, i + 1) == i;
+            if (!__shfl_sync(kFull, won, 0))
+                return false;
+            decide(i, i & 1, 0);
+            if (lane == 0) {
+                sh.rec_state = state;
+                sh.rec_code = code;
+                sh.rec_j = j;
+                sh.rec_mode = mode;
+                sh.rec_ndec = ndec;
+                sh.rec_A = rowA;
+                sh.rec_Shi = rowS.hi;
+                sh.rec_Slo = rowS.lo;
+                st_release_cta(&sh.rec_row, i);
+            }
+            __syncwarp();
+            return true;
+        };
+        // non-blocking: the decision on row `pend` if it can be had now
         auto poll = [&]() -> bool {
             if (pend < 0)
                 return true;
             const int pp = pend & 1;
-            const bool ready = __shfl_sync(kFull, (int)mbar_test(&xbar[pp], (xph >> pp) & 1u), 0) != 0;
-            if (!ready)
-                return true;
+            if (record_posted(pend)) {
+                take_record();
+            } else {
+                const bool ready = __shfl_sync(kFull, (int)mbar_test(&xbar[pp], (xph >> pp) & 1u), 0) != 0;
+                if (!ready || !decide_claimed(pend))
+                    return true;
+            }
             xph ^= 1u << pp;
-            decide(pend, pp, 0);
             pend = -1;
             return state == kStateRun;
+        };
+        // blocking (bounded): the decision on row i
+        auto settle_row = [&](int i) {
+            const int pp = i & 1;
+            if (!record_posted(i)) {
+                wait_partials(pp);  // flips xph
+                if (!decide_claimed(i)) {
+                    const unsigned long long t0 = global_ns();
+                    while (!record_posted(i)) {
+                        __nanosleep(64);
+                        if (global_ns() - t0 > 4 * a.wait_ns) {
+                            state = kStateError;
+                            code = SV_ERR_TIMEOUT;
+                            return;
+                        }
+                    }
+                    take_record();
+                }
+                return;
+            }
+            take_record();
+            xph ^= 1u << pp;
         };
         while (state == kStateRun) {
             const int pc = cur & 1;
@@ -1029,8 +1112,7 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
             if (!stream_row(cur, ls, poll))
                 break;
             if (pend >= 0) {  // the decision on the previous row is still open
-                wait_partials(pend & 1);
-                decide(pend, pend & 1, 0);
+                settle_row(pend);
                 pend = -1;
                 if (state != kStateRun)
                     break;
@@ -1038,8 +1120,7 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
             publish(pc, 0, ls);
             pend = cur;
             if (cur == K) {  // the bonus row: nothing left to stream
-                wait_partials(pc);
-                decide(cur, pc, 0);
+                settle_row(cur);
                 pend = -1;
                 break;
             }
@@ -1086,7 +1167,7 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
                 o.num = g4.z;
                 o.kind = __float_as_int(g4.w);
                 o.S = FF{g2.x, g2.y};
-                apply_row(g0 + r, o);
+                apply_row(g0 + r, o, warp == 0);
             }
             __syncthreads();  // the outcome slots are reused by the next group
             par ^= 1;
