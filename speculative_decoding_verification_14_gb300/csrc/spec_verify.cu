@@ -567,10 +567,10 @@ __device__ __forceinline__ uint4 load_vec_elems(const void* logits, int64_t gbas
 // ------------------------------------------------------- row statistics -----
 
 // Sum over this lane's vectors of one chunk (vector k*32 + lane of `buf`, for
-// k*32 + lane < nv) of 2^((l - a) c), folding the raw values into the
-// NaN-propagating max `mx` on the way.  Two packed accumulators keep the
+// k*32 + lane < nv) of 2^((l - a) c), with TRACK folding the raw values into
+// the NaN-propagating max `mx` on the way.  Two packed accumulators keep the
 // dependency chains short.
-template <int ES, bool FULL>
+template <int ES, bool FULL, bool TRACK>
 __device__ __forceinline__ float fold_chunk(const uint4* buf, int nv, float a, float c,
                                             typename Elem<ES>::Max& mx) {
     constexpr int E = Elem<ES>::E;
@@ -582,7 +582,8 @@ __device__ __forceinline__ float fold_chunk(const uint4* buf, int nv, float a, f
     for (int k = 0; k < kVecPerLane; ++k) {
         if (FULL || k * 32 + lane < nv) {
             const uint4 w = buf[k * 32 + lane];
-            mx = Elem<ES>::vmax(w, mx);
+            if constexpr (TRACK)
+                mx = Elem<ES>::vmax(w, mx);
             float2 d[E / 2];
             Elem<ES>::diff(w, na, d);
 #pragma unroll
@@ -610,11 +611,15 @@ __device__ __forceinline__ float fold_chunk(const uint4* buf, int nv, float a, f
 // therefore at most 2^8 (no overflow, and y's rounding stays small for the
 // terms that dominate), and the offset is always the value of an entry the
 // lane has seen, so its own term keeps s >= 1 and terms that underflow are
-// negligible.  The per-chunk max pass of a textbook online softmax is gone;
-// the max is still tracked exactly because the reported row statistics are
-// taken against the row max.
+// negligible.  The per-chunk max pass of a textbook online softmax is gone.
+// With `track` the max is kept exactly (the reported row statistics are taken
+// against the row max); without it a chunk is accepted on its sum alone: a
+// sum of at most kFoldBound = (entries per lane per chunk) x 2^8 means every
+// term is at most kFoldBound, and a larger (or NaN / inf) sum sends the chunk
+// through the max and the rules above.
 template <int ES>
 struct LaneSum {
+    static constexpr float kFoldBound = (float)(kVecPerLane * Elem<ES>::E * 256);
     float a, s;
     typename Elem<ES>::Max mx;
 
@@ -630,12 +635,28 @@ struct LaneSum {
         a = Elem<ES>::value(m0);
     }
 
-    __device__ __forceinline__ void chunk(const uint4* buf, int nv, float c) {
+    __device__ __forceinline__ void chunk(const uint4* buf, int nv, float c, bool track) {
         typename Elem<ES>::Max cm = Elem<ES>::max_init();
-        const float cs = nv == kChunkVecs ? fold_chunk<ES, true>(buf, nv, a, c, cm)
-                                          : fold_chunk<ES, false>(buf, nv, a, c, cm);
-        mx = Elem<ES>::mmax(mx, cm);
-        const float m = Elem<ES>::value(cm);
+        float cs, m;
+        if (track) {
+            cs = nv == kChunkVecs ? fold_chunk<ES, true, true>(buf, nv, a, c, cm)
+                                  : fold_chunk<ES, false, true>(buf, nv, a, c, cm);
+            mx = Elem<ES>::mmax(mx, cm);
+            m = Elem<ES>::value(cm);
+        } else {
+            cs = nv == kChunkVecs ? fold_chunk<ES, true, false>(buf, nv, a, c, cm)
+                                  : fold_chunk<ES, false, false>(buf, nv, a, c, cm);
+            if (cs <= kFoldBound) {  // false for NaN
+                s += cs;
+                return;
+            }
+            const int lane = threadIdx.x & 31;
+#pragma unroll
+            for (int k = 0; k < kVecPerLane; ++k)
+                if (k * 32 + lane < nv)
+                    cm = Elem<ES>::vmax(buf[k * 32 + lane], cm);
+            m = Elem<ES>::value(cm);
+        }
         if ((m - a) * c <= 8.f) {  // false for NaN, +inf, or no offset yet
             s += cs;
             return;
@@ -650,7 +671,7 @@ struct LaneSum {
         s = s > 0.f ? s * ex2_approx((a - m) * c) : 0.f;
         a = m;
         typename Elem<ES>::Max unused = Elem<ES>::max_init();
-        s += fold_chunk<ES, false>(buf, nv, a, c, unused);
+        s += fold_chunk<ES, false, false>(buf, nv, a, c, unused);
     }
 };
 
@@ -851,6 +872,7 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
         qx_lane = __ldg(a.q + ((int64_t)b * K + lane) * V + x);
     }
     const int P = C * NW;  // row partials per row: every warp of the cluster
+    const bool track = a.row_stats != nullptr;  // the row max is reported
     uint32_t xph = 0;      // phase bits of the two row-partial barriers
 
     // ---- the test loop: rows in order ([P1]) ----
@@ -885,7 +907,7 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
             }
             if (ch == 0)
                 ls.start(buf, nv);
-            ls.chunk(buf, nv, c);
+            ls.chunk(buf, nv, c, track);
             if (a.bulk)
                 release();
             else
@@ -901,7 +923,7 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
     // CTA of the cluster.
     auto publish = [&](int par, int r, const LaneSum<ES>& ls) {
         const float aw = warp_max_nan(ls.a);
-        const float mw = warp_max_nan(Elem<ES>::value(ls.mx));
+        const float mw = track ? warp_max_nan(Elem<ES>::value(ls.mx)) : aw;
         FF sw = {0.f, 0.f};
         if (ls.s > 0.f && aw < INFINITY)
             sw = two_prod(ls.s, exp2_diff_accurate(ls.a, aw, a.c_hi, a.c_lo));
@@ -957,7 +979,9 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
         for (int sft = 16; sft; sft >>= 1)
             amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, sft));
         o.amax = amax;
-        const bool finite = o.M > -INFINITY && o.M < INFINITY;
+        // (a NaN or inf entry poisons its lane's offset to +inf, an all -inf
+        // row leaves every offset at -inf: both show in the merged offset)
+        const bool finite = amax > -INFINITY && amax < INFINITY;
         FF acc = {0.f, 0.f};
         if (finite) {
 #pragma unroll
@@ -994,7 +1018,7 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
             code = SV_ERR_TIMEOUT;
             return;
         }
-        if (o.kind == 3 && !(o.M > -INFINITY && o.M < INFINITY)) {
+        if (o.kind == 3 && !(o.amax > -INFINITY && o.amax < INFINITY)) {
             state = kStateError;
             code = SV_ERR_NONFINITE;
             return;
