@@ -1207,9 +1207,10 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
     // ---- corrected or bonus draw over row j ([P1]) ----
     // This warp's stretch of row j is walked in tiles of kDrawTile entries: a
     // tile's draft probabilities are one ring stage, and lane l takes vectors
-    // k*32 + l (k < kDV) of the tile's logits, loaded one tile ahead (the
-    // stretch is prefetched into L2 first).  Every tile's weight total goes to
-    // `tt` for the locate step.
+    // k*32 + l (k < kDV) of the tile's logits, loaded one tile ahead (an L2
+    // prefetch of the whole stretch measured slower: in a full batch it only
+    // adds to the DRAM queues).  Every tile's weight total goes to `tt` for
+    // the locate step.
     constexpr int kDrawTile = sv::kDrawTile;    // entries per draw tile
     constexpr int kDV = kDrawTile / (32 * E);   // logits vectors per lane per tile
     const int64_t e0 = (int64_t)wv0 * E;
@@ -1226,8 +1227,6 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
         const float na = -rowA;
         const float Sf = rowS.hi;
         const int64_t gbase_j = (row0 + j) * V + v0;  // element index of the slice start
-        if (lane == 0 && a.bulk && nq > 0)
-            bulk_prefetch_l2(lrow + e0 * ES, (uint32_t)(nq * ES));
         int sp = 0;
         const unsigned char* lbase = lrow + e0 * ES;
         const float* qbase = qrow ? qrow + e0 : nullptr;

@@ -191,15 +191,32 @@ def test_device_errors_mark_only_their_sequence_and_clear():
 
 @pytest.mark.parametrize("name", workloads.CONFIG_ORDER)
 def test_without_row_stats_nothing_changes(name):
-    """Without row_stats the kernel drops the exact running max from its fold;
-    the offsets move at the same chunks, so lengths, tokens, masks and statuses
-    must be the same bits as with row_stats, and still match the oracle."""
+    """Without row_stats the kernel drops the exact running max from its fold
+    and moves an offset on a chunk-sum bound instead; that changes rounding
+    only, so on these workloads lengths, tokens, masks and statuses are the
+    same bits as with row_stats, and still match the oracle."""
     inp = workloads.make_config(name)
     on = gh.gpu_verify_inputs(inp, stats=True)
     off = gh.gpu_verify_inputs(inp, stats=False)
     for k in ("accept_len", "out_tokens", "accept_mask", "status"):
         np.testing.assert_array_equal(off[k], on[k], err_msg=k)
     info = gh.compare(off, oracle.verify_inputs(inp), inp.K, check_stats=False, label=name + "/no_stats")
+    assert info["exact"] + info["accept_ties"] + info["draw_ties"] == inp.B
+
+
+def test_rebase_without_row_stats():
+    """Spikes far above the bulk of a row sit in later chunks of many lanes, so
+    offsets move mid-row -- without row_stats through the chunk-sum bound --
+    and the outputs still match the oracle and the run with row_stats."""
+    inp = workloads.make_random(2, 3, 300000, dtype="bf16", seed=16)
+    lg = inp.logits.copy()
+    lg[:, :, 4095::4096] = 0x41C8                # bf16 25.0 every 4096 entries
+    inp.logits = lg
+    on = gh.gpu_verify_inputs(inp, stats=True)
+    off = gh.gpu_verify_inputs(inp, stats=False)
+    for k in ("accept_len", "out_tokens", "accept_mask", "status"):
+        np.testing.assert_array_equal(off[k], on[k], err_msg=k)
+    info = gh.compare(off, oracle.verify_inputs(inp), inp.K, check_stats=False, label="rebase_no_stats")
     assert info["exact"] + info["accept_ties"] + info["draw_ties"] == inp.B
 
 
