@@ -150,6 +150,44 @@ int spec_verify_plan_for(int num_sms, int smem_per_cta, int max_cluster,
                          int B, int K, int64_t V, int logits_dtype,
                          int ovr_cluster, int ovr_group, int ovr_threads, sv_plan* out);
 
+/* Acceptance telemetry ([P1] "Production perspective": ship the acceptance
+ * rate and the mean accepted length; its operational checklist: record
+ * acceptance histograms).  With `accept_hist` set, every later verify on this
+ * context adds 1, per sequence, to accept_hist[AL] (AL = accepted length,
+ * 1..K+1; bin 0 counts sequences that reported an error).  `accept_hist` is a
+ * DEVICE array of `bins` uint32 counters owned by the caller, who zeroes it and
+ * keeps it alive while set; counts accumulate across calls (atomic adds on the
+ * launch stream).  A run whose K + 2 exceeds `bins` returns SV_ERR_INVALID_ARG.
+ * NULL (bins ignored) turns the counting off.  Keep one histogram per draft
+ * depth K: spec_adapt reads it for one K.
+ * Returns SV_OK or SV_ERR_INVALID_ARG (no context, bins < 2, misaligned). */
+int spec_verify_set_telemetry(sv_ctx* ctx, uint32_t* accept_hist, int bins);
+
+/* What a histogram of accepted lengths for one draft depth K says. */
+typedef struct {
+    uint64_t sequences;          /* sequences counted (bins 1..K+1)                       */
+    uint64_t errors;             /* bin 0                                                  */
+    uint64_t tested;             /* draft tokens tested: sum of min(AL, K)                 */
+    uint64_t accepted;           /* draft tokens accepted: sum of AL - 1                   */
+    double acceptance;           /* accepted / tested (NaN if nothing was tested)          */
+    double mean_accept_len;      /* tokens emitted per pass (NaN if no sequence)           */
+    uint64_t pos_tested[32];     /* position i tested by sequences with AL >= i + 1        */
+    double pos_acceptance[32];   /* accepted at i / tested at i (NaN if untested or i >= K) */
+    int next_K;                  /* the draft depth for the next passes                    */
+} sv_adapt;
+
+/* Adaptive draft depth ([P2] "Two things that follow from the math": cap the
+ * depth when the measured acceptance falls below 35 %; "Rules I follow": pick
+ * the depth from measured acceptance and keep measuring).  Host function, no
+ * CUDA call.  `hist` is a HOST copy of a telemetry histogram collected at
+ * depth K (bins >= K + 2).  next_K = K (bounded by K_max) while fewer than
+ * `min_tested` drafts were tested; K_floor when acceptance < threshold (the
+ * pages use 0.35); K_max otherwise.
+ * Returns SV_OK or SV_ERR_INVALID_ARG (null pointers, K or K_max outside
+ * [0, 32], K_floor outside [0, K_max], bins < K + 2, threshold outside [0, 1]). */
+int spec_adapt(const uint32_t* hist, int bins, int K, int K_max, int K_floor,
+               double threshold, uint64_t min_tested, sv_adapt* out);
+
 /* The verify of spec_verify_run with no context and no allocation of any
  * kind (no cudaMalloc/cudaFree, no host heap, no allocating library call).
  * The pages have no counterpart: this is a deployment convenience, not part of

@@ -43,6 +43,11 @@ def _bind(path: str) -> ctypes.CDLL:
     lib.oracle_verify.restype = ctypes.c_int
     lib.oracle_verify.argtypes = [P, ctypes.c_int, P, P, P, ctypes.c_int64, ctypes.c_int,
                                   ctypes.c_int64, ctypes.c_float] + [P] * 10
+    lib.oracle_accept_hist.restype = ctypes.c_int
+    lib.oracle_accept_hist.argtypes = [P, ctypes.c_int64, ctypes.c_int, P]
+    lib.oracle_adapt.restype = ctypes.c_int
+    lib.oracle_adapt.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                                 ctypes.c_uint64, P, P, P, P]
     lib.oracle_softmax_row.restype = ctypes.c_int
     lib.oracle_softmax_row.argtypes = [P, ctypes.c_int, ctypes.c_int64, ctypes.c_double,
                                        P, P, P]
@@ -116,6 +121,33 @@ def verify(logits: np.ndarray, dtype: str, q: np.ndarray, tokens: np.ndarray,
     if rc != 0:
         raise ValueError(f"oracle_verify rejected its arguments (rc={rc})")
     return out
+
+
+def accept_hist(accept_len: np.ndarray, K: int) -> np.ndarray:
+    """Counts of accepted lengths 0..K+1 (uint64)."""
+    lib = _load()
+    al = np.ascontiguousarray(accept_len, dtype=np.int32)
+    hist = np.zeros(K + 2, np.uint64)
+    if lib.oracle_accept_hist(_ptr(al), al.size, K, _ptr(hist)) != 0:
+        raise ValueError("accepted length outside [0, K+1]")
+    return hist
+
+
+def adapt(hist, K: int, K_max: int, K_floor: int = 1, threshold: float = 0.35,
+          min_tested: int = 0) -> dict:
+    """Acceptance rate, mean accepted length, per-position acceptance and the
+    next draft depth of a histogram taken at depth K."""
+    lib = _load()
+    h = np.zeros(max(K + 2, len(hist)), np.uint64)
+    h[:len(hist)] = np.asarray(hist, dtype=np.uint64)
+    acc, mlen = ctypes.c_double(), ctypes.c_double()
+    pos = np.full(max(K, 1), np.nan)
+    nk = ctypes.c_int()
+    if lib.oracle_adapt(_ptr(h), K, K_max, K_floor, float(threshold), int(min_tested),
+                        ctypes.byref(acc), ctypes.byref(mlen), _ptr(pos), ctypes.byref(nk)) != 0:
+        raise ValueError("oracle_adapt rejected its arguments")
+    return {"acceptance": acc.value, "mean_accept_len": mlen.value, "pos_acceptance": pos[:K],
+            "next_K": nk.value}
 
 
 def verify_inputs(inp, lib: Optional[ctypes.CDLL] = None) -> dict:

@@ -299,3 +299,56 @@ int oracle_verify(const void* logits, int dtype, const float* q, const int32_t* 
     free(p); free(w); free(rm); free(rs); free(pd);
     return 0;
 }
+
+/* Acceptance telemetry ([P1] "Production perspective" and its operational
+ * checklist: acceptance rate, mean accepted length, acceptance histograms),
+ * from the definitions, one sequence at a time. */
+int oracle_accept_hist(const int32_t* accept_len, int64_t B, int K, uint64_t* hist) {
+    if (K < 0 || B < 0)
+        return 1;
+    for (int n = 0; n <= K + 1; ++n)
+        hist[n] = 0;
+    for (int64_t b = 0; b < B; ++b) {
+        const int32_t n = accept_len[b];
+        if (n < 0 || n > K + 1)
+            return 1;
+        hist[n] += 1;
+    }
+    return 0;
+}
+
+/* What a histogram at depth K says, and the depth rule of [P2] ("Two things
+ * that follow from the math": cap the depth when the measured acceptance is
+ * below the threshold, 35 % on the page).  A sequence with accepted length n
+ * (1 <= n <= K+1) tested min(n, K) drafts and accepted n - 1 of them; it
+ * tested position i when n >= i + 1 and accepted it when n >= i + 2. */
+int oracle_adapt(const uint64_t* hist, int K, int K_max, int K_floor, double threshold,
+                 uint64_t min_tested, double* acceptance, double* mean_len,
+                 double* pos_acceptance, int* next_K) {
+    if (K < 0 || K_floor < 0 || K_floor > K_max)
+        return 1;
+    uint64_t seqs = 0, tested = 0, accepted = 0, len_sum = 0;
+    for (int n = 1; n <= K + 1; ++n) {
+        seqs += hist[n];
+        tested += hist[n] * (uint64_t)(n < K ? n : K);
+        accepted += hist[n] * (uint64_t)(n - 1);
+        len_sum += hist[n] * (uint64_t)n;
+    }
+    for (int i = 0; i < K; ++i) {
+        uint64_t t = 0, a = 0;
+        for (int n = i + 1; n <= K + 1; ++n)
+            t += hist[n];
+        for (int n = i + 2; n <= K + 1; ++n)
+            a += hist[n];
+        pos_acceptance[i] = t ? (double)a / (double)t : NAN;
+    }
+    *acceptance = tested ? (double)accepted / (double)tested : NAN;
+    *mean_len = seqs ? (double)len_sum / (double)seqs : NAN;
+    if (tested == 0 || tested < min_tested)
+        *next_K = K < K_max ? K : K_max;
+    else if (*acceptance < threshold)
+        *next_K = K_floor;
+    else
+        *next_K = K_max;
+    return 0;
+}

@@ -78,6 +78,18 @@ int oracle_verify(const void* logits, int dtype, const float* q, const int32_t* 
                   int32_t* status, double* row_m, double* row_s, double* p_draft,
                   double* accept_margin, double* sample_margin, int32_t* sample_alt);
 
+/* Histogram of accepted lengths: hist[n] = sequences with accept_len n,
+ * n = 0..K+1 (0 = sequence error).  Returns 1 if a length is outside that range. */
+int oracle_accept_hist(const int32_t* accept_len, int64_t B, int K, uint64_t* hist);
+
+/* Acceptance rate (accepted / tested drafts), mean accepted length, per-position
+ * acceptance (K values) of a histogram taken at depth K, and the next depth:
+ * K (bounded by K_max) while fewer than min_tested drafts were tested, K_floor
+ * when the acceptance is below `threshold`, K_max otherwise. */
+int oracle_adapt(const uint64_t* hist, int K, int K_max, int K_floor, double threshold,
+                 uint64_t min_tested, double* acceptance, double* mean_len,
+                 double* pos_acceptance, int* next_K);
+
 #ifdef __cplusplus
 }
 #endif

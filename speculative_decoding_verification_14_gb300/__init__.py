@@ -37,6 +37,20 @@ class sv_plan(ctypes.Structure):
         return {f: getattr(self, f) for f, _ in self._fields_}
 
 
+class sv_adapt(ctypes.Structure):
+    _fields_ = [("sequences", ctypes.c_uint64), ("errors", ctypes.c_uint64),
+                ("tested", ctypes.c_uint64), ("accepted", ctypes.c_uint64),
+                ("acceptance", ctypes.c_double), ("mean_accept_len", ctypes.c_double),
+                ("pos_tested", ctypes.c_uint64 * 32), ("pos_acceptance", ctypes.c_double * 32),
+                ("next_K", ctypes.c_int)]
+
+    def as_dict(self) -> dict:
+        d = {f: getattr(self, f) for f, _ in self._fields_}
+        d["pos_tested"] = list(self.pos_tested)
+        d["pos_acceptance"] = list(self.pos_acceptance)
+        return d
+
+
 _lib: Optional[ctypes.CDLL] = None
 P = ctypes.c_void_p
 
@@ -66,6 +80,10 @@ def library() -> ctypes.CDLL:
                                                     ctypes.c_int, ctypes.c_int, ctypes.c_int64,
                                                     ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                     ctypes.c_int, ctypes.POINTER(sv_plan)]),
+            "spec_verify_set_telemetry": (ctypes.c_int, [P, P, ctypes.c_int]),
+            "spec_adapt": (ctypes.c_int, [P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                          ctypes.c_int, ctypes.c_double, ctypes.c_uint64,
+                                          ctypes.POINTER(sv_adapt)]),
             "spec_verify_destroy": (ctypes.c_int, [P]),
             "spec_verify_strerror": (ctypes.c_char_p, [ctypes.c_int]),
             "spec_verify_version": (ctypes.c_int, []),
@@ -124,6 +142,23 @@ def spec_verify_run_noalloc(device, logits_ptr, dtype, q_ptr, tokens_ptr, unifor
                                              uniforms_ptr, B, K, V, float(T), accept_len_ptr,
                                              out_tokens_ptr, accept_mask_ptr, row_stats_ptr,
                                              p_draft_ptr, status_ptr, stream)
+
+
+def spec_verify_set_telemetry(ctx, hist_ptr, bins) -> int:
+    return library().spec_verify_set_telemetry(ctx, hist_ptr, int(bins))
+
+
+def spec_adapt(hist, K: int, K_max: int, K_floor: int = 1, threshold: float = 0.35,
+               min_tested: int = 0) -> dict:
+    """`hist`: host sequence of accepted-length counts (bin 0 = errors) taken
+    at draft depth K.  Returns the sv_adapt fields as a dict."""
+    arr = (ctypes.c_uint32 * len(hist))(*[int(h) for h in hist])
+    out = sv_adapt()
+    rc = library().spec_adapt(arr, len(hist), K, K_max, K_floor, float(threshold),
+                              int(min_tested), ctypes.byref(out))
+    if rc != SV_OK:
+        raise SpecVerifyError(rc, "spec_adapt")
+    return out.as_dict()
 
 
 def spec_verify_get_error(ctx, stream=None):
@@ -206,6 +241,23 @@ class Verifier:
 
     def error(self, stream=None):
         return spec_verify_get_error(self.ctx, stream)
+
+    def set_telemetry(self, hist) -> None:
+        """Count accepted lengths of every later run into `hist`, a uint32
+        CUDA tensor of at least K + 2 counters (zeroed by the caller); None
+        stops counting.  The tensor must stay alive while it is set."""
+        if hist is None:
+            rc = spec_verify_set_telemetry(self.ctx, None, 0)
+        else:
+            import torch
+            if hist.dtype != torch.int32 and hist.dtype != getattr(torch, "uint32", None):
+                raise TypeError("telemetry counters must be a 32-bit integer tensor")
+            if not hist.is_cuda or not hist.is_contiguous():
+                raise ValueError("telemetry counters must be a contiguous CUDA tensor")
+            rc = spec_verify_set_telemetry(self.ctx, hist.data_ptr(), hist.numel())
+        if rc != SV_OK:
+            raise SpecVerifyError(rc, "spec_verify_set_telemetry")
+        self._telemetry = hist
 
     def run(self, logits, q, tokens, uniforms, temperature: float, out: Optional[dict] = None,
             stats: bool = False, status: bool = True, stream=None) -> dict:

@@ -1,4 +1,4 @@
-"""Builds libspecverify.so in-tree for sm_103a (nvcc + g++, two translation
+"""Builds libspecverify.so in-tree for sm_103a (nvcc + g++, three translation
 units compiled in parallel, no cmake).  Run as ``python -m
 speculative_decoding_verification_14_gb300.build`` or through ``build()``."""
 from __future__ import annotations
@@ -15,7 +15,8 @@ OUT = os.path.join(PKG, "libspecverify.so")
 BUILD_DIR = os.path.join(PKG, "_build")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = [os.path.join(CSRC, f) for f in ("spec_verify.cu", "planner.cpp", "sv_internal.h")] + [
+HOST_SOURCES = ("planner.cpp", "adapt.cpp")
+SOURCES = [os.path.join(CSRC, f) for f in ("spec_verify.cu", "sv_internal.h", *HOST_SOURCES)] + [
     os.path.join(INCLUDE, "spec_verify.h")]
 
 
@@ -38,13 +39,12 @@ def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(BUILD_DIR, exist_ok=True)
     nvcc = _nvcc()
     obj_cu = os.path.join(BUILD_DIR, "spec_verify.o")
-    obj_cpp = os.path.join(BUILD_DIR, "planner.o")
+    obj_cpp = [os.path.join(BUILD_DIR, f.replace(".cpp", ".o")) for f in HOST_SOURCES]
     cmds = [
         [nvcc, *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,
          "-c", os.path.join(CSRC, "spec_verify.cu"), "-o", obj_cu],
-        ["g++", "-O2", "-std=c++17", "-fPIC", "-Wall", "-I", INCLUDE, "-c",
-         os.path.join(CSRC, "planner.cpp"), "-o", obj_cpp],
-    ]
+    ] + [["g++", "-O2", "-std=c++17", "-fPIC", "-Wall", "-I", INCLUDE, "-c",
+          os.path.join(CSRC, f), "-o", o] for f, o in zip(HOST_SOURCES, obj_cpp)]
     procs = [subprocess.Popen(c, stdout=subprocess.PIPE, stderr=subprocess.STDOUT) for c in cmds]
     for c, p in zip(cmds, procs):
         out, _ = p.communicate()
@@ -53,7 +53,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         if verbose and out:
             sys.stdout.write(out.decode(errors="replace"))
     tmp = OUT + f".tmp{os.getpid()}"
-    link = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, obj_cu, obj_cpp]
+    link = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, obj_cu, *obj_cpp]
     r = subprocess.run(link, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)
     if r.returncode != 0:
         raise RuntimeError("link failed: " + " ".join(link) + "\n" + r.stdout.decode(errors="replace"))

@@ -61,7 +61,6 @@ constexpr unsigned kFull = 0xffffffffu;
 constexpr int kMaxWarps = 16;
 constexpr int kChunkVecs = kChunkBytes / 16;  // 16-byte vectors per ring stage
 constexpr int kVecPerLane = kChunkVecs / 32;
-constexpr int kQChunk = kChunkBytes / 4;      // draft probabilities per ring stage
 constexpr int kStateRun = 0, kStateSample = 1, kStateError = 2;
 constexpr int kModeResidual = 0, kModeBonus = 1, kModeTargetRow = 2;
 
@@ -77,6 +76,7 @@ struct SvArgs {
     float* p_draft;
     int32_t* status;
     uint32_t* err_word;
+    uint32_t* al_hist;      // optional: one count per accepted length (0 = sequence error)
     int64_t V;
     int64_t slice;          // vocabulary entries per CTA (multiple of 8)
     int B, K, C, G;
@@ -165,11 +165,6 @@ __device__ __forceinline__ void bulk_copy_g2s_hint(void* dst, const void* src, u
             smem_addr(dst)),
         "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
         : "memory");
-}
-
-// Bulk prefetch of a global range into L2 (no destination, no completion).
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t parity) {
@@ -1597,6 +1592,8 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
                 a.accept_len[b] = j + 1;
                 if (a.status)
                     a.status[b] = SV_OK;
+                if (a.al_hist)
+                    atomicAdd(a.al_hist + j + 1, 1u);
             }
         }
     }
@@ -1623,6 +1620,8 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
             if (a.status)
                 a.status[b] = code;
             atomicOr(a.err_word, 1u << code);
+            if (a.al_hist)
+                atomicAdd(a.al_hist, 1u);
         }
     }
 
@@ -1680,6 +1679,8 @@ struct sv_ctx {
     uint32_t* d_err = nullptr;
     int ovr_cluster = 0, ovr_group = 0, ovr_threads = 0;
     int ovr_prefetch = -1;  // -1: the planner decides
+    uint32_t* al_hist = nullptr;  // caller's accepted-length counters (device), or none
+    int al_bins = 0;
     unsigned long long wait_ns = 2000000000ull;
     // staging for the host-buffer entry point
     unsigned char* d_stage = nullptr;
@@ -1734,6 +1735,8 @@ int launch(sv_ctx* ctx, const void* logits, int dtype, const float* q, const int
            const float* uniforms, int B, int K, int64_t V, float T, int32_t* accept_len,
            int32_t* out_tokens, uint8_t* accept_mask, float* row_stats, float* p_draft,
            int32_t* status, cudaStream_t stream) {
+    if (ctx->al_hist && K + 2 > ctx->al_bins)
+        return SV_ERR_INVALID_ARG;
     sv_plan plan;
     int rc = make_plan(ctx, B, K, V, dtype, &plan);
     if (rc != SV_OK)
@@ -1757,6 +1760,7 @@ int launch(sv_ctx* ctx, const void* logits, int dtype, const float* q, const int
     args.p_draft = p_draft;
     args.status = status;
     args.err_word = ctx->d_err;
+    args.al_hist = ctx->al_hist;
     args.V = V;
     args.slice = plan.slice;
     args.B = B;
@@ -1932,6 +1936,21 @@ int spec_verify_set_plan_override(sv_ctx* ctx, int cluster, int group, int threa
     ctx->ovr_cluster = cluster;
     ctx->ovr_group = group;
     ctx->ovr_threads = threads;
+    return SV_OK;
+}
+
+int spec_verify_set_telemetry(sv_ctx* ctx, uint32_t* accept_hist, int bins) {
+    if (!ctx)
+        return SV_ERR_INVALID_ARG;
+    if (!accept_hist) {
+        ctx->al_hist = nullptr;
+        ctx->al_bins = 0;
+        return SV_OK;
+    }
+    if (bins < 2 || !aligned(accept_hist, 4))
+        return SV_ERR_INVALID_ARG;
+    ctx->al_hist = accept_hist;
+    ctx->al_bins = bins;
     return SV_OK;
 }
 
