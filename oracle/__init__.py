@@ -43,6 +43,9 @@ def _bind(path: str) -> ctypes.CDLL:
     lib.oracle_verify.restype = ctypes.c_int
     lib.oracle_verify.argtypes = [P, ctypes.c_int, P, P, P, ctypes.c_int64, ctypes.c_int,
                                   ctypes.c_int64, ctypes.c_float] + [P] * 10
+    lib.oracle_verify_greedy.restype = ctypes.c_int
+    lib.oracle_verify_greedy.argtypes = [P, ctypes.c_int, P, ctypes.c_int64, ctypes.c_int,
+                                         ctypes.c_int64, P, P, P, P, P]
     lib.oracle_accept_hist.restype = ctypes.c_int
     lib.oracle_accept_hist.argtypes = [P, ctypes.c_int64, ctypes.c_int, P]
     lib.oracle_adapt.restype = ctypes.c_int
@@ -120,6 +123,32 @@ def verify(logits: np.ndarray, dtype: str, q: np.ndarray, tokens: np.ndarray,
                            _ptr(out["sample_margin"]), _ptr(out["sample_alt"]))
     if rc != 0:
         raise ValueError(f"oracle_verify rejected its arguments (rc={rc})")
+    return out
+
+
+def verify_greedy(logits: np.ndarray, dtype: str, tokens: np.ndarray,
+                  lib: Optional[ctypes.CDLL] = None) -> dict:
+    """Greedy (T -> 0) verification.  logits [B, K+1, V] (float32, or uint16
+    bf16 bits), tokens [B, K] int32.  Returns accept_len, out_tokens,
+    accept_mask, status, row_argmax."""
+    lib = lib or _load()
+    logits = np.ascontiguousarray(logits, dtype=np.float32 if dtype == "f32" else np.uint16)
+    B, K1, V = logits.shape
+    K = K1 - 1
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32).reshape(B, K)
+    out = {
+        "accept_len": np.empty(B, np.int32),
+        "out_tokens": np.empty((B, K + 1), np.int32),
+        "accept_mask": np.empty((B, K), np.uint8),
+        "status": np.empty(B, np.int32),
+        "row_argmax": np.empty((B, K + 1), np.int32),
+    }
+    rc = lib.oracle_verify_greedy(_ptr(logits), _dtype_code(dtype), _ptr(tokens), B, K, V,
+                                  _ptr(out["accept_len"]), _ptr(out["out_tokens"]),
+                                  _ptr(out["accept_mask"]), _ptr(out["status"]),
+                                  _ptr(out["row_argmax"]))
+    if rc != 0:
+        raise ValueError(f"oracle_verify_greedy rejected its arguments (rc={rc})")
     return out
 
 

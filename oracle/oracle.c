@@ -352,3 +352,84 @@ int oracle_adapt(const uint64_t* hist, int K, int K_max, int K_floor, double thr
         *next_K = K_max;
     return 0;
 }
+
+/* Greedy verification: the verify step in the limit T -> 0.  As T falls, the
+ * softmax of l/T ([P1] "Speculative decoding: draft first, then verify")
+ * puts all of its mass on the largest logit, so p_i becomes one-hot at
+ * a_i = argmax_v l[b,i,v].  Then [P1]'s test u*q(x) < p(x) accepts exactly
+ * when x_i = a_i (p(x) = 1 > u*q(x) for u < 1, q <= 1; p(x) = 0 otherwise),
+ * the residual max(0, p_j - q_j) is positive only at a_j, and the bonus row
+ * draws a_K, so neither q nor u is needed.  Readings where the limit is not
+ * unique: among equal largest logits the lowest token id is a_i (the
+ * first-occurrence rule of argmax); a row the loop reaches that holds a NaN or
+ * +inf, or only -inf, is a sequence error, as for the sampled verify.
+ *
+ * Outputs as oracle_verify; row_argmax [B, K+1] (optional) holds a_i for the
+ * rows the loop reached and -1 for the others. */
+int oracle_verify_greedy(const void* logits, int dtype, const int32_t* tokens, int64_t B, int K,
+                         int64_t V, int32_t* accept_len, int32_t* out_tokens,
+                         uint8_t* accept_mask, int32_t* status, int32_t* row_argmax)
+{
+    if (B < 0 || K < 0 || V < 1)
+        return 1;
+    const size_t es = dtype == 0 ? 4 : 2;
+    for (int64_t b = 0; b < B; ++b) {
+        int st = ORACLE_OK, len = 0;
+        int32_t* ot = out_tokens + (size_t)b * (size_t)(K + 1);
+        for (int i = 0; i <= K; ++i)
+            ot[i] = -1;
+        for (int i = 0; i < K; ++i)
+            accept_mask[(size_t)b * (size_t)K + (size_t)i] = 0;
+        if (row_argmax)
+            for (int i = 0; i <= K; ++i)
+                row_argmax[(size_t)b * (size_t)(K + 1) + (size_t)i] = -1;
+        for (int i = 0; i < K; ++i) {
+            const int32_t x = tokens[(size_t)b * (size_t)K + (size_t)i];
+            if (x < 0 || (int64_t)x >= V)
+                st = ORACLE_TOKEN_RANGE;
+        }
+        for (int i = 0; st == ORACLE_OK && i <= K; ++i) {
+            const char* row = (const char*)logits + ((size_t)b * (size_t)(K + 1) + (size_t)i) *
+                                                        (size_t)V * es;
+            /* a_i: the first token holding the largest logit */
+            double best = -INFINITY;
+            int64_t a = -1;
+            for (int64_t v = 0; v < V; ++v) {
+                const double l = logit_at(row, dtype, v);
+                if (isnan(l) || l == INFINITY) {
+                    st = ORACLE_NONFINITE;
+                    break;
+                }
+                if (l > best) {
+                    best = l;
+                    a = v;
+                }
+            }
+            if (st == ORACLE_OK && a < 0)
+                st = ORACLE_NONFINITE; /* every logit is -inf */
+            if (st != ORACLE_OK)
+                break;
+            if (row_argmax)
+                row_argmax[(size_t)b * (size_t)(K + 1) + (size_t)i] = (int32_t)a;
+            if (i < K && tokens[(size_t)b * (size_t)K + (size_t)i] == (int32_t)a) {
+                ot[i] = (int32_t)a; /* accepted: the draft token stays */
+                accept_mask[(size_t)b * (size_t)K + (size_t)i] = 1;
+                continue;
+            }
+            ot[i] = (int32_t)a; /* the corrected token (i < K) or the bonus token (i = K) */
+            len = i + 1;
+            break;
+        }
+        if (st != ORACLE_OK) {
+            len = 0;
+            for (int i = 0; i <= K; ++i)
+                ot[i] = -1;
+            for (int i = 0; i < K; ++i)
+                accept_mask[(size_t)b * (size_t)K + (size_t)i] = 0;
+        }
+        accept_len[b] = len;
+        if (status)
+            status[b] = st;
+    }
+    return 0;
+}

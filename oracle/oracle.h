@@ -78,6 +78,16 @@ int oracle_verify(const void* logits, int dtype, const float* q, const int32_t* 
                   int32_t* status, double* row_m, double* row_s, double* p_draft,
                   double* accept_margin, double* sample_margin, int32_t* sample_alt);
 
+/* Greedy verification, the limit T -> 0 of oracle_verify: a_i = the first
+ * token holding the largest logit of row i; draft x_i is accepted iff
+ * x_i = a_i; the first rejected position j emits a_j, and a fully accepted
+ * sequence emits the bonus a_K.  No q and no uniforms.  Outputs as
+ * oracle_verify (accept_len 0 and tokens -1 on a sequence error); row_argmax
+ * [B, K+1] (optional) holds a_i for the rows reached, -1 for the others. */
+int oracle_verify_greedy(const void* logits, int dtype, const int32_t* tokens, int64_t B, int K,
+                         int64_t V, int32_t* accept_len, int32_t* out_tokens,
+                         uint8_t* accept_mask, int32_t* status, int32_t* row_argmax);
+
 /* Histogram of accepted lengths: hist[n] = sequences with accept_len n,
  * n = 0..K+1 (0 = sequence error).  Returns 1 if a length is outside that range. */
 int oracle_accept_hist(const int32_t* accept_len, int64_t B, int K, uint64_t* hist);
