@@ -51,6 +51,9 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=workloads.CONFIG_ORDER)
+    ap.add_argument("--mode", choices=["sampled", "greedy"], default="sampled",
+                    help="sampled: spec_verify_run at the workload's temperature; greedy: "
+                         "spec_verify_run_greedy (T -> 0) with a greedy drafter")
     ap.add_argument("--sets", type=int, default=3, help="input copies rotated between steps")
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--no-e2e", action="store_true")
@@ -79,6 +82,7 @@ def measured_peak():
 
 
 KERNEL_SOURCES = ("speculative_decoding_verification_14_gb300/csrc/spec_verify.cu",
+                  "speculative_decoding_verification_14_gb300/csrc/greedy.cu",
                   "speculative_decoding_verification_14_gb300/csrc/sv_internal.h",
                   "speculative_decoding_verification_14_gb300/csrc/planner.cpp")
 
@@ -129,6 +133,14 @@ def algorithmic_bytes(inp, accept_len: np.ndarray) -> int:
     tests = int(np.minimum(n, K).sum())
     return (rows * V * es + rejected * V * 4 + tests * 4 + B * K * 4 + B * (K + 1) * 4
             + B * (4 + (K + 1) * 4 + K))
+
+
+def algorithmic_bytes_greedy(inp, accept_len: np.ndarray) -> int:
+    """Greedy verification: n rows of logits per sequence (rows 0..n-1, read in
+    order up to the first rejection), the K draft tokens, and the outputs."""
+    B, K, V, es = inp.B, inp.K, inp.V, inp.logit_bytes
+    rows = int(accept_len.astype(np.int64).sum())
+    return rows * V * es + B * K * 4 + B * (4 + (K + 1) * 4 + K)
 
 
 # ---------------------------------------------------------------- clocks -----
@@ -200,9 +212,12 @@ def run_ours(args):
 
     cfg = workloads.CONFIGS[args.workload]
     inp = workloads.make_config(args.workload, seed=cfg.seed + rank)
+    greedy = args.mode == "greedy"
+    if greedy:
+        inp = workloads.greedy_drafts(inp)
     B, K, V, T = inp.B, inp.K, inp.V, inp.T
     dcode = sv.SV_BF16 if inp.dtype == "bf16" else sv.SV_F32
-    per_set = inp.nominal_bytes()
+    per_set = inp.nominal_bytes() if not greedy else inp.logits.nbytes + inp.tokens.nbytes
     nsets = max(1, args.sets)
 
     def dev_logits():
@@ -212,8 +227,11 @@ def run_ours(args):
 
     sets = []
     for s in range(nsets):
-        sets.append((dev_logits(), torch.from_numpy(inp.q).cuda(), torch.from_numpy(inp.tokens).cuda(),
-                     torch.from_numpy(inp.uniforms).cuda()))
+        if greedy:  # the greedy step reads no draft probabilities and no uniforms
+            sets.append((dev_logits(), None, torch.from_numpy(inp.tokens).cuda(), None))
+        else:
+            sets.append((dev_logits(), torch.from_numpy(inp.q).cuda(),
+                         torch.from_numpy(inp.tokens).cuda(), torch.from_numpy(inp.uniforms).cuda()))
     outs = {"accept_len": torch.empty(B, dtype=torch.int32, device="cuda"),
             "out_tokens": torch.empty(B, K + 1, dtype=torch.int32, device="cuda"),
             "accept_mask": torch.empty(B, K, dtype=torch.uint8, device="cuda")}
@@ -222,16 +240,21 @@ def run_ours(args):
     lib = sv.library()
     calls = []
     for (lg, q, x, u) in sets:
-        calls.append((verifier.ctx, lg.data_ptr(), dcode, q.data_ptr(), x.data_ptr(), u.data_ptr(),
-                      B, K, V, ctypes.c_float(T), outs["accept_len"].data_ptr(),
-                      outs["out_tokens"].data_ptr(), outs["accept_mask"].data_ptr(), None, None,
-                      None, stream.cuda_stream))
-    run = lib.spec_verify_run
+        if greedy:
+            calls.append((verifier.ctx, lg.data_ptr(), dcode, x.data_ptr(), B, K, V,
+                          outs["accept_len"].data_ptr(), outs["out_tokens"].data_ptr(),
+                          outs["accept_mask"].data_ptr(), None, None, stream.cuda_stream))
+        else:
+            calls.append((verifier.ctx, lg.data_ptr(), dcode, q.data_ptr(), x.data_ptr(),
+                          u.data_ptr(), B, K, V, ctypes.c_float(T), outs["accept_len"].data_ptr(),
+                          outs["out_tokens"].data_ptr(), outs["accept_mask"].data_ptr(), None,
+                          None, None, stream.cuda_stream))
+    run = lib.spec_verify_run_greedy if greedy else lib.spec_verify_run
 
     def step(k):
         rc = run(*calls[k % nsets])
         if rc != 0:
-            raise sv.SpecVerifyError(rc, "spec_verify_run")
+            raise sv.SpecVerifyError(rc, "spec_verify_run_greedy" if greedy else "spec_verify_run")
 
     def barrier():
         if dist is not None:
@@ -278,18 +301,20 @@ def run_ours(args):
     if err != sv.SV_OK:
         raise sv.SpecVerifyError(err, "device error during the benchmark")
     acc = outs["accept_len"].cpu().numpy()
-    alg = algorithmic_bytes(inp, acc)
+    alg = algorithmic_bytes_greedy(inp, acc) if greedy else algorithmic_bytes(inp, acc)
     avg_launch_s = statistics.mean(launch_ms) / 1e3
     rows_per_step = B * (K + 1)
     value = world * rows_per_step * args.steps / (total_ms / 1e3)
     tokens_per_step = int(acc.sum())
     peak, peak_kind = measured_peak()
     achieved = alg / avg_launch_s / 1e9
-    plan = verifier.plan(B, K, V, dcode)
+    plan = verifier.plan_greedy(B, K, V, dcode) if greedy else verifier.plan(B, K, V, dcode)
 
     # end to end through the host-buffer entry point, copies inside the region
     e2e = None
-    if not args.no_e2e and args.e2e_steps > 0:
+    if greedy and not args.no_e2e and args.e2e_steps > 0:
+        e2e = e2e_greedy(args, inp, verifier, acc, dist, world, rows_per_step)
+    elif not args.no_e2e and args.e2e_steps > 0:
         def pinned(a):
             t = torch.empty(a.shape, dtype={np.float32: torch.float32, np.uint16: torch.int16,
                                             np.int32: torch.int32, np.uint8: torch.uint8}[a.dtype.type],
@@ -333,7 +358,7 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(inp, args.cpu_seconds)
+        cpu = cpu_baseline(inp, args.cpu_seconds, greedy=greedy)
 
     if rank != 0:
         return None
@@ -341,8 +366,10 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": args.workload, "B": B, "K": K, "V": V, "logits_dtype": inp.dtype,
-                   "T": T, "l2": f"{nsets} input copies of {per_set / 1e9:.2f} GB rotated "
+        "config": {"workload": args.workload + (" with a greedy drafter, greedy verify (T -> 0)"
+                                                if greedy else ""),
+                   "B": B, "K": K, "V": V, "logits_dtype": inp.dtype,
+                   "T": 0.0 if greedy else T, "l2": f"{nsets} input copies of {per_set / 1e9:.2f} GB rotated "
                                  f"(each larger than the {L2_BYTES >> 20} MB L2)",
                    "plan": plan},
         "tokens_per_s": world * tokens_per_step * args.steps / (total_ms / 1e3),
@@ -350,7 +377,8 @@ def run_ours(args):
         "hbm_gbs_algorithmic": achieved,
         "hbm_gbs_nominal": inp.nominal_bytes() / avg_launch_s / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": profile_traffic(args.workload),
+                     "frac": achieved / peak,
+                     "traffic": profile_traffic(args.workload + ("_greedy" if greedy else "")),
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind ==
                      "measured" else "fallback 6.8 TB/s",
                      "algorithmic_bytes_per_launch": alg, "avg_launch_us": avg_launch_s * 1e6},
@@ -362,23 +390,72 @@ def run_ours(args):
     return line
 
 
-def cpu_baseline(inp, seconds: float) -> dict:
-    """The fp64 oracle as it stands, single thread, on whole passes over the
+def cpu_baseline(inp, seconds: float, greedy: bool = False) -> dict:
+    """The oracle as it stands, single thread, on whole passes over the
     workload's sequences until `seconds` of CPU work have accumulated."""
     import oracle
     oracle.build()
+
+    def one(n):
+        if greedy:
+            oracle.verify_greedy(inp.logits[:n], inp.dtype, inp.tokens[:n])
+        else:
+            oracle.verify(inp.logits[:n], inp.dtype, inp.q[:n], inp.tokens[:n], inp.uniforms[:n],
+                          inp.T)
     # one sequence first, to size the sample
     t = time.perf_counter()
-    oracle.verify(inp.logits[:1], inp.dtype, inp.q[:1], inp.tokens[:1], inp.uniforms[:1], inp.T)
+    one(1)
     per_seq = max(time.perf_counter() - t, 1e-6)
     n = int(min(inp.B, max(1, seconds / per_seq)))
     reps = max(1, int(seconds / (per_seq * n)))
     t = time.perf_counter()
     for _ in range(reps):
-        oracle.verify(inp.logits[:n], inp.dtype, inp.q[:n], inp.tokens[:n], inp.uniforms[:n], inp.T)
+        one(n)
     el = time.perf_counter() - t
     return {"value": reps * n * (inp.K + 1) / el, "unit": "rows/s", "cores": 1, "kind": "oracle",
             "sample": f"{reps} pass(es) over the first {n} of {inp.B} sequences ({el:.1f} s)"}
+
+
+def e2e_greedy(args, inp, verifier, acc, dist, world, rows_per_step) -> dict:
+    """Greedy verification end to end through the public API: pinned host
+    logits and tokens copied to the device, spec_verify_run_greedy, outputs
+    copied back, all inside the timed region."""
+    import torch
+    B, K = inp.B, inp.K
+    h_lg = torch.from_numpy(inp.logits.view(np.int16) if inp.dtype == "bf16" else inp.logits)
+    h_lg = h_lg.pin_memory()
+    h_x = torch.from_numpy(inp.tokens).pin_memory()
+    d_lg = torch.empty(h_lg.shape, dtype=h_lg.dtype, device="cuda")
+    d_x = torch.empty(h_x.shape, dtype=h_x.dtype, device="cuda")
+    h_out = {k: torch.empty(shape, dtype=dt).pin_memory() for k, shape, dt in
+             (("accept_len", (B,), torch.int32), ("out_tokens", (B, K + 1), torch.int32),
+              ("accept_mask", (B, K), torch.uint8))}
+
+    def once():
+        d_lg.copy_(h_lg, non_blocking=True)
+        d_x.copy_(h_x, non_blocking=True)
+        lg = d_lg.view(torch.bfloat16) if inp.dtype == "bf16" else d_lg
+        out = verifier.run_greedy(lg, d_x, status=False)
+        for k, t in h_out.items():
+            t.copy_(out[k], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    once()
+    if dist is not None:
+        dist.barrier()
+    ts = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        once()
+    el = time.perf_counter() - ts
+    if dist is not None:
+        tt = torch.tensor([el], device="cuda", dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        el = float(tt.item())
+    assert np.array_equal(h_out["accept_len"].numpy(), acc)
+    return {"value": world * rows_per_step * args.e2e_steps / el, "unit": "rows/s",
+            "h2d_bytes_per_step": int(inp.logits.nbytes + inp.tokens.nbytes),
+            "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in h_out.values())),
+            "steps": args.e2e_steps,
+            "api": "Verifier.run_greedy (spec_verify_run_greedy) with pinned host copies"}
 
 
 # -------------------------------------------------------- reference arm -----

@@ -150,6 +150,48 @@ int spec_verify_plan_for(int num_sms, int smem_per_cta, int max_cluster,
                          int B, int K, int64_t V, int logits_dtype,
                          int ovr_cluster, int ovr_group, int ovr_threads, sv_plan* out);
 
+/* Greedy verification: the verify of spec_verify_run in the limit T -> 0
+ * ([P1] "Speculative decoding: draft first, then verify": as T falls, the
+ * softmax of logits/T puts all its mass on the largest logit).  Row i becomes
+ * one-hot at a_i = argmax_v target_logits[b, i, v], the LOWEST token id among
+ * equal maxima; draft x_i is accepted iff x_i == a_i (the test u*q(x) < p(x)
+ * with a one-hot p); the first rejected position j emits a_j (the only token
+ * with max(0, p_j - q_j) > 0), and a fully accepted sequence emits the bonus
+ * a_K.  So neither draft probabilities nor uniforms are taken.
+ *
+ *   target_logits [B, K+1, V]  float32 or bfloat16 (SV_F32 / SV_BF16), device
+ *   draft_tokens  [B, K]       int32, device (may be NULL when K == 0)
+ *   accept_len    [B]          out, accepted drafts + 1 in [1, K+1]; 0 = sequence error
+ *   out_tokens    [B, K+1]     out, accepted drafts, then a_j, then -1
+ *   accept_mask   [B, K]       out, 1 for accepted positions (may be NULL when K == 0)
+ *   row_argmax    [B, K+1]     optional out: a_i for the rows read, -1 for the others
+ *                              (and for every row of an erroneous sequence)
+ *   status        [B]          optional out: per-sequence status
+ *
+ * Rows are read in order and not past the first rejection.  Device-detected
+ * errors (a draft token outside [0, V); a row the loop reaches holding a NaN
+ * or +inf, or only -inf) mark the sequence as for spec_verify_run, set the
+ * context's error word, and count in bin 0 of the telemetry histogram if one
+ * is set.  Asynchronous, no allocation, one launch on `stream`.
+ * Returns SV_OK, SV_ERR_INVALID_ARG (null or misaligned pointers, shapes outside
+ * the context's limits, telemetry bins < K + 2) or SV_ERR_CUDA (launch failed). */
+int spec_verify_run_greedy(sv_ctx* ctx,
+                           const void* target_logits, int logits_dtype,
+                           const int32_t* draft_tokens, int B, int K, int64_t V,
+                           int32_t* accept_len, int32_t* out_tokens, uint8_t* accept_mask,
+                           int32_t* row_argmax, int32_t* status, void* stream);
+
+/* The greedy kernel's launch plan for a shape on the context's device. */
+int spec_verify_get_plan_greedy(sv_ctx* ctx, int B, int K, int64_t V, int logits_dtype,
+                                sv_plan* out);
+
+/* The greedy planner as a pure host function (no CUDA call), for tests:
+ * one cluster per sequence, the largest that keeps the batch resident (eight
+ * 128-thread CTAs per SM) and gives every warp enough work; ovr_cluster > 0
+ * forces the cluster size. */
+int spec_verify_plan_greedy_for(int num_sms, int max_cluster, int B, int K, int64_t V,
+                                int logits_dtype, int ovr_cluster, sv_plan* out);
+
 /* Acceptance telemetry ([P1] "Production perspective": ship the acceptance
  * rate and the mean accepted length; its operational checklist: record
  * acceptance histograms).  With `accept_hist` set, every later verify on this

@@ -420,12 +420,15 @@ int oracle_verify_greedy(const void* logits, int dtype, const int32_t* tokens, i
             len = i + 1;
             break;
         }
-        if (st != ORACLE_OK) {
+        if (st != ORACLE_OK) { /* an erroneous sequence reports no per-row outputs */
             len = 0;
             for (int i = 0; i <= K; ++i)
                 ot[i] = -1;
             for (int i = 0; i < K; ++i)
                 accept_mask[(size_t)b * (size_t)K + (size_t)i] = 0;
+            if (row_argmax)
+                for (int i = 0; i <= K; ++i)
+                    row_argmax[(size_t)b * (size_t)(K + 1) + (size_t)i] = -1;
         }
         accept_len[b] = len;
         if (status)

@@ -83,7 +83,8 @@ int oracle_verify(const void* logits, int dtype, const float* q, const int32_t* 
  * x_i = a_i; the first rejected position j emits a_j, and a fully accepted
  * sequence emits the bonus a_K.  No q and no uniforms.  Outputs as
  * oracle_verify (accept_len 0 and tokens -1 on a sequence error); row_argmax
- * [B, K+1] (optional) holds a_i for the rows reached, -1 for the others. */
+ * [B, K+1] (optional) holds a_i for the rows reached, -1 for the others and for
+ * every row of an erroneous sequence. */
 int oracle_verify_greedy(const void* logits, int dtype, const int32_t* tokens, int64_t B, int K,
                          int64_t V, int32_t* accept_len, int32_t* out_tokens,
                          uint8_t* accept_mask, int32_t* status, int32_t* row_argmax);

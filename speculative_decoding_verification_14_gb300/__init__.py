@@ -80,6 +80,16 @@ def library() -> ctypes.CDLL:
                                                     ctypes.c_int, ctypes.c_int, ctypes.c_int64,
                                                     ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                     ctypes.c_int, ctypes.POINTER(sv_plan)]),
+            "spec_verify_run_greedy": (ctypes.c_int, [P, P, ctypes.c_int, P, ctypes.c_int,
+                                                      ctypes.c_int, ctypes.c_int64, P, P, P, P,
+                                                      P, P]),
+            "spec_verify_get_plan_greedy": (ctypes.c_int, [P, ctypes.c_int, ctypes.c_int,
+                                                           ctypes.c_int64, ctypes.c_int,
+                                                           ctypes.POINTER(sv_plan)]),
+            "spec_verify_plan_greedy_for": (ctypes.c_int, [ctypes.c_int, ctypes.c_int,
+                                                           ctypes.c_int, ctypes.c_int,
+                                                           ctypes.c_int64, ctypes.c_int,
+                                                           ctypes.c_int, ctypes.POINTER(sv_plan)]),
             "spec_verify_set_telemetry": (ctypes.c_int, [P, P, ctypes.c_int]),
             "spec_adapt": (ctypes.c_int, [P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                           ctypes.c_int, ctypes.c_double, ctypes.c_uint64,
@@ -142,6 +152,29 @@ def spec_verify_run_noalloc(device, logits_ptr, dtype, q_ptr, tokens_ptr, unifor
                                              uniforms_ptr, B, K, V, float(T), accept_len_ptr,
                                              out_tokens_ptr, accept_mask_ptr, row_stats_ptr,
                                              p_draft_ptr, status_ptr, stream)
+
+
+def spec_verify_run_greedy(ctx, logits_ptr, dtype, tokens_ptr, B, K, V, accept_len_ptr,
+                           out_tokens_ptr, accept_mask_ptr, row_argmax_ptr=None, status_ptr=None,
+                           stream=None) -> int:
+    return library().spec_verify_run_greedy(ctx, logits_ptr, dtype, tokens_ptr, B, K, V,
+                                            accept_len_ptr, out_tokens_ptr, accept_mask_ptr,
+                                            row_argmax_ptr, status_ptr, stream)
+
+
+def spec_verify_get_plan_greedy(ctx, B, K, V, dtype) -> dict:
+    plan = sv_plan()
+    rc = library().spec_verify_get_plan_greedy(ctx, B, K, V, dtype, ctypes.byref(plan))
+    if rc != SV_OK:
+        raise SpecVerifyError(rc, "spec_verify_get_plan_greedy")
+    return plan.as_dict()
+
+
+def spec_verify_plan_greedy_for(num_sms, max_cluster, B, K, V, dtype, ovr_cluster=0):
+    plan = sv_plan()
+    rc = library().spec_verify_plan_greedy_for(num_sms, max_cluster, B, K, V, dtype, ovr_cluster,
+                                               ctypes.byref(plan))
+    return rc, plan.as_dict()
 
 
 def spec_verify_set_telemetry(ctx, hist_ptr, bins) -> int:
@@ -290,6 +323,42 @@ class Verifier:
         if rc != SV_OK:
             raise SpecVerifyError(rc, "spec_verify_run")
         return out
+
+    def run_greedy(self, logits, tokens, out: Optional[dict] = None, argmax: bool = False,
+                   status: bool = True, stream=None) -> dict:
+        """Greedy (T -> 0) verification: logits [B, K+1, V] (float32 or bfloat16)
+        and tokens [B, K] int32 CUDA tensors.  Returns accept_len, out_tokens,
+        accept_mask and optionally row_argmax [B, K+1] and status."""
+        import torch
+        B, K1, V = logits.shape
+        K = K1 - 1
+        dev = logits.device
+        if out is None:
+            out = {
+                "accept_len": torch.empty(B, dtype=torch.int32, device=dev),
+                "out_tokens": torch.empty(B, K + 1, dtype=torch.int32, device=dev),
+                "accept_mask": torch.empty(B, max(K, 1), dtype=torch.uint8, device=dev)[:, :K],
+            }
+            if argmax:
+                out["row_argmax"] = torch.empty(B, K + 1, dtype=torch.int32, device=dev)
+            if status:
+                out["status"] = torch.empty(B, dtype=torch.int32, device=dev)
+        s = stream if stream is not None else torch.cuda.current_stream(dev).cuda_stream
+
+        def ptr(name):
+            t = out.get(name)
+            return None if t is None else t.data_ptr()
+
+        rc = spec_verify_run_greedy(self.ctx, logits.data_ptr(), _dtype_code(logits),
+                                    tokens.data_ptr() if K else None, B, K, V, ptr("accept_len"),
+                                    ptr("out_tokens"), ptr("accept_mask") if K else None,
+                                    ptr("row_argmax"), ptr("status"), s)
+        if rc != SV_OK:
+            raise SpecVerifyError(rc, "spec_verify_run_greedy")
+        return out
+
+    def plan_greedy(self, B, K, V, dtype=SV_BF16) -> dict:
+        return spec_verify_get_plan_greedy(self.ctx, B, K, V, dtype)
 
     def run_host(self, logits, dtype: int, q, tokens, uniforms, temperature: float,
                  out: dict, stream=None) -> int:

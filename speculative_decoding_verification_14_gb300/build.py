@@ -1,4 +1,4 @@
-"""Builds libspecverify.so in-tree for sm_103a (nvcc + g++, three translation
+"""Builds libspecverify.so in-tree for sm_103a (nvcc + g++, four translation
 units compiled in parallel, no cmake).  Run as ``python -m
 speculative_decoding_verification_14_gb300.build`` or through ``build()``."""
 from __future__ import annotations
@@ -15,8 +15,9 @@ OUT = os.path.join(PKG, "libspecverify.so")
 BUILD_DIR = os.path.join(PKG, "_build")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+CUDA_SOURCES = ("spec_verify.cu", "greedy.cu")
 HOST_SOURCES = ("planner.cpp", "adapt.cpp")
-SOURCES = [os.path.join(CSRC, f) for f in ("spec_verify.cu", "sv_internal.h", *HOST_SOURCES)] + [
+SOURCES = [os.path.join(CSRC, f) for f in (*CUDA_SOURCES, "sv_internal.h", *HOST_SOURCES)] + [
     os.path.join(INCLUDE, "spec_verify.h")]
 
 
@@ -38,11 +39,11 @@ def build(force: bool = False, verbose: bool = False) -> str:
         return OUT
     os.makedirs(BUILD_DIR, exist_ok=True)
     nvcc = _nvcc()
-    obj_cu = os.path.join(BUILD_DIR, "spec_verify.o")
+    obj_cu = [os.path.join(BUILD_DIR, f.replace(".cu", ".o")) for f in CUDA_SOURCES]
     obj_cpp = [os.path.join(BUILD_DIR, f.replace(".cpp", ".o")) for f in HOST_SOURCES]
     cmds = [
         [nvcc, *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,
-         "-c", os.path.join(CSRC, "spec_verify.cu"), "-o", obj_cu],
+         "-c", os.path.join(CSRC, f), "-o", o] for f, o in zip(CUDA_SOURCES, obj_cu)
     ] + [["g++", "-O2", "-std=c++17", "-fPIC", "-Wall", "-I", INCLUDE, "-c",
           os.path.join(CSRC, f), "-o", o] for f, o in zip(HOST_SOURCES, obj_cpp)]
     procs = [subprocess.Popen(c, stdout=subprocess.PIPE, stderr=subprocess.STDOUT) for c in cmds]
@@ -53,7 +54,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         if verbose and out:
             sys.stdout.write(out.decode(errors="replace"))
     tmp = OUT + f".tmp{os.getpid()}"
-    link = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, obj_cu, *obj_cpp]
+    link = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *obj_cu, *obj_cpp]
     r = subprocess.run(link, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)
     if r.returncode != 0:
         raise RuntimeError("link failed: " + " ".join(link) + "\n" + r.stdout.decode(errors="replace"))

@@ -108,3 +108,49 @@ extern "C" int spec_verify_plan_for(int num_sms, int smem_per_cta, int max_clust
     return plan_impl(num_sms, smem_per_cta, max_cluster, B, K, V, logits_dtype, ovr_cluster,
                      ovr_group, ovr_threads, out);
 }
+
+// Greedy verification (greedy.cu): the same mapping -- one cluster of C CTAs
+// per sequence, vocabulary slices, rows in order -- with no shared-memory
+// ring, so residency is set by the kernel's launch bounds (eight 128-thread
+// CTAs per SM).  Each lane keeps eight 16-byte loads in flight; a batch that
+// fills the GPU gets at least two such rounds per warp and row, a smaller
+// batch the largest cluster that leaves every lane one vector.
+extern "C" int spec_verify_plan_greedy_for(int num_sms, int max_cluster, int B, int K, int64_t V,
+                                           int logits_dtype, int ovr_cluster, sv_plan* out) {
+    using namespace sv;
+    if (!out || num_sms < 1 || max_cluster < 1 || B < 1 || K < 0 || K > kMaxK || V < 1 ||
+        V > ((int64_t)1 << 31) || (logits_dtype != SV_F32 && logits_dtype != SV_BF16) ||
+        ovr_cluster < 0 || ovr_cluster > kMaxCluster)
+        return SV_ERR_INVALID_ARG;
+    if (ovr_cluster > max_cluster)
+        return SV_ERR_UNSUPPORTED;
+    const int es = logits_dtype == SV_BF16 ? 2 : 4;
+    const int64_t E = 16 / es;
+    const int nw = 4;
+    const int64_t capacity = (int64_t)kGreedyCtasPerSM * num_sms;
+    const int64_t min_full = (int64_t)nw * 32 * kGreedyDepth * E * 2;
+    const int64_t min_small = (int64_t)nw * 32 * E;
+    const int cmax = max_cluster < kMaxCluster ? max_cluster : kMaxCluster;
+    int C = 1;
+    if (ovr_cluster) {
+        C = ovr_cluster;
+    } else {
+        for (int c = cmax >= 16 ? 16 : cmax; c >= 1; c /= 2) {
+            const bool fills = (int64_t)B * c >= num_sms;
+            if ((int64_t)B * c <= capacity &&
+                (c == 1 || ceil_div(V, c) >= (fills ? min_full : min_small))) {
+                C = c;
+                break;
+            }
+        }
+    }
+    out->cluster = C;
+    out->group = 1;
+    out->threads = nw * 32;
+    out->smem_bytes = 0;
+    out->slice = round_up(ceil_div(V, C), kSliceAlign);
+    out->grid = (int64_t)B * C;
+    out->bulk_copy = ((V * es) % 16) == 0 ? 1 : 0;
+    out->prefetch_next = 0;
+    return SV_OK;
+}

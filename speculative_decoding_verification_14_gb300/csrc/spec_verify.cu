@@ -1676,6 +1676,7 @@ struct sv_ctx {
     int max_B = 0, max_K = 0;
     int64_t max_V = 0;
     int num_sms = 0, smem_optin = 0, max_cluster = 8;
+    int greedy_max_cluster = 8;
     uint32_t* d_err = nullptr;
     int ovr_cluster = 0, ovr_group = 0, ovr_threads = 0;
     int ovr_prefetch = -1;  // -1: the planner decides
@@ -1900,6 +1901,8 @@ int spec_verify_init(sv_ctx** out, int device, int max_B, int max_K, int64_t max
         }
     }
     ctx->max_cluster = max_cluster;
+    // the greedy kernel may use 16-CTA clusters only where the main kernel may
+    ctx->greedy_max_cluster = (max_cluster >= 16 && sv::greedy_set_attributes() == 0) ? 16 : 8;
     ctx->ovr_cluster = env_int("SV_CLUSTER", 0);
     ctx->ovr_group = env_int("SV_GROUP", 0);
     ctx->ovr_threads = env_int("SV_THREADS", 0);
@@ -1937,6 +1940,62 @@ int spec_verify_set_plan_override(sv_ctx* ctx, int cluster, int group, int threa
     ctx->ovr_group = group;
     ctx->ovr_threads = threads;
     return SV_OK;
+}
+
+int spec_verify_get_plan_greedy(sv_ctx* ctx, int B, int K, int64_t V, int logits_dtype,
+                                sv_plan* out) {
+    if (!ctx)
+        return SV_ERR_INVALID_ARG;
+    return spec_verify_plan_greedy_for(ctx->num_sms, ctx->greedy_max_cluster, B, K, V,
+                                       logits_dtype, ctx->ovr_cluster, out);
+}
+
+int spec_verify_run_greedy(sv_ctx* ctx, const void* target_logits, int logits_dtype,
+                           const int32_t* draft_tokens, int B, int K, int64_t V,
+                           int32_t* accept_len, int32_t* out_tokens, uint8_t* accept_mask,
+                           int32_t* row_argmax, int32_t* status, void* stream) {
+    if (!ctx || !target_logits || !accept_len || !out_tokens)
+        return SV_ERR_INVALID_ARG;
+    if (logits_dtype != SV_F32 && logits_dtype != SV_BF16)
+        return SV_ERR_INVALID_ARG;
+    if (B < 1 || B > ctx->max_B || K < 0 || K > ctx->max_K || K > kMaxK || V < 1 ||
+        V > ctx->max_V)
+        return SV_ERR_INVALID_ARG;
+    if ((double)B * (double)(K + 1) * (double)V >= 1099511627776.0)  // 2^40
+        return SV_ERR_INVALID_ARG;
+    if (K > 0 && (!draft_tokens || !accept_mask))
+        return SV_ERR_INVALID_ARG;
+    const int es = logits_dtype == SV_BF16 ? 2 : 4;
+    if (!aligned(target_logits, es) || (draft_tokens && !aligned(draft_tokens, 4)) ||
+        !aligned(accept_len, 4) || !aligned(out_tokens, 4) ||
+        (row_argmax && !aligned(row_argmax, 4)) || (status && !aligned(status, 4)))
+        return SV_ERR_INVALID_ARG;
+    if (ctx->al_hist && K + 2 > ctx->al_bins)
+        return SV_ERR_INVALID_ARG;
+    sv_plan plan;
+    const int rc = spec_verify_get_plan_greedy(ctx, B, K, V, logits_dtype, &plan);
+    if (rc != SV_OK)
+        return rc;
+    sv::GreedyLaunch g;
+    std::memset(&g, 0, sizeof g);
+    g.logits = target_logits;
+    g.tokens = draft_tokens;
+    g.accept_len = accept_len;
+    g.out_tokens = out_tokens;
+    g.accept_mask = accept_mask;
+    g.row_argmax = row_argmax;
+    g.status = status;
+    g.err_word = ctx->d_err;
+    g.al_hist = ctx->al_hist;
+    g.V = V;
+    g.slice = plan.slice;
+    g.B = B;
+    g.K = K;
+    g.C = plan.cluster;
+    g.es = es;
+    g.vec = plan.bulk_copy && aligned(target_logits, 16) ? 1 : 0;
+    DeviceGuard guard(ctx->device);
+    return sv::greedy_launch(g, stream) == 0 ? SV_OK : SV_ERR_CUDA;
 }
 
 int spec_verify_set_telemetry(sv_ctx* ctx, uint32_t* accept_hist, int bins) {

@@ -19,6 +19,9 @@ constexpr int kSmemPerSM = 233472;      // shared memory of one SM (228 KB)
 constexpr int kSmemPerCtaReserved = 1024;  // the runtime's per-CTA reservation
 constexpr int kThreadsPerSM = 896;      // resident threads the kernels' launch bounds target (7 CTAs of 128)
 
+constexpr int kGreedyDepth = 8;         // greedy kernel: 16-byte loads in flight per lane
+constexpr int kGreedyCtasPerSM = 8;     // greedy kernel: resident 128-thread CTAs per SM (launch bounds)
+
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 
@@ -49,5 +52,24 @@ inline Layout layout_for(int64_t slice, int elem_bytes, int group, int threads, 
     l.total = l.off_tt + round_up(nw * l.ntw * 4, 16);
     return l;
 }
+
+// Greedy verification kernel (greedy.cu): launch description and entry points.
+struct GreedyLaunch {
+    const void* logits;
+    const int32_t* tokens;
+    int32_t* accept_len;
+    int32_t* out_tokens;
+    uint8_t* accept_mask;
+    int32_t* row_argmax;
+    int32_t* status;
+    uint32_t* err_word;
+    uint32_t* al_hist;
+    int64_t V, slice;
+    int B, K, C;
+    int es;   // bytes per logit (2 or 4)
+    int vec;  // 1: 16-byte vector loads (aligned rows)
+};
+int greedy_set_attributes();                              // 0 on success
+int greedy_launch(const GreedyLaunch& g, void* stream);  // 0 on success
 
 }  // namespace sv

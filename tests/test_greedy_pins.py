@@ -114,7 +114,7 @@ def test_special_values():
         lg[0, 1, 2] = bad
         g = oracle.verify_greedy(lg, "f32", x)
         assert g["status"][0] == oracle.NONFINITE and g["accept_len"][0] == 0
-        assert np.all(g["out_tokens"][0] == -1)
+        assert np.all(g["out_tokens"][0] == -1) and np.all(g["row_argmax"][0] == -1)
     lg = base.copy()
     lg[0, 0] = -np.inf
     assert oracle.verify_greedy(lg, "f32", x)["status"][0] == oracle.NONFINITE
@@ -136,8 +136,8 @@ MUTANTS = {
                         "                if (l >= best) {\n                    best = l;\n                    a = v;"),
     "emit_draft_on_reject": ("            ot[i] = (int32_t)a; /* the corrected token",
                              "            ot[i] = i < K ? tokens[(size_t)b * (size_t)K + (size_t)i] : (int32_t)a; /* the corrected token"),
-    "no_stop_at_rejection": ("            len = i + 1;\n            break;\n        }\n        if (st != ORACLE_OK) {\n            len = 0;",
-                             "            len = i + 1;\n        }\n        if (st != ORACLE_OK) {\n            len = 0;"),
+    "no_stop_at_rejection": ("            len = i + 1;\n            break;\n        }\n        if (st != ORACLE_OK) {",
+                             "            len = i + 1;\n        }\n        if (st != ORACLE_OK) {"),
     "length_off_by_one": ("            len = i + 1;\n            break;", "            len = i;\n            break;"),
     "max_of_wrong_row": ("((size_t)b * (size_t)(K + 1) + (size_t)i) *\n                                                        (size_t)V * es;",
                          "((size_t)b * (size_t)(K + 1) + (size_t)(i ? i - 1 : 0)) *\n                                                        (size_t)V * es;"),

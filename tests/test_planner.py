@@ -81,3 +81,36 @@ def test_bad_arguments(sv):
     assert plan(sv, 1, 1, 0, 0)[0] == sv.SV_ERR_INVALID_ARG
     assert plan(sv, 1, 1, 100, 2)[0] == sv.SV_ERR_INVALID_ARG
     assert plan(sv, 1, 1, (1 << 31) + 1, 0)[0] == sv.SV_ERR_INVALID_ARG
+
+
+# ------------------------------------------------------------ greedy -----
+
+def gplan(sv, B, K, V, dtype, oc=0, dev=GB300):
+    return sv.spec_verify_plan_greedy_for(dev["num_sms"], dev["max_cluster"], B, K, V, dtype, oc)
+
+
+@pytest.mark.parametrize("B,K,V,dtype", list(itertools.product(
+    [1, 8, 64, 256, 5000], [0, 4, 32], [1, 7, 32000, 128256, 151936, 1 << 20], [0, 1])))
+def test_greedy_plan_invariants(sv, B, K, V, dtype):
+    rc, p = gplan(sv, B, K, V, dtype)
+    assert rc == sv.SV_OK
+    es = 2 if dtype == 1 else 4
+    C, slice_ = p["cluster"], p["slice"]
+    assert C in (1, 2, 4, 8, 16)
+    assert slice_ % 8 == 0 and slice_ * C >= V and slice_ * (C - 1) < V + 8 * C
+    assert p["grid"] == B * C and p["group"] == 1 and p["threads"] == 128
+    assert p["bulk_copy"] == int((V * es) % 16 == 0)
+    # the batch stays resident (eight CTAs per SM) whenever one CTA per sequence fits
+    if B <= 152 * 8:
+        assert B * C <= 152 * 8
+
+
+def test_greedy_workload_plans(sv):
+    assert gplan(sv, 256, 7, 128256, 1)[1]["cluster"] == 4
+    assert gplan(sv, 64, 3, 151936, 1)[1]["cluster"] == 8
+    assert gplan(sv, 8, 4, 32000, 1)[1]["cluster"] == 16
+    assert gplan(sv, 1, 4, 32000, 0)[1]["cluster"] == 16
+    assert gplan(sv, 4, 2, 50000, 1, oc=2)[1]["cluster"] == 2
+    assert gplan(sv, 4, 2, 50000, 1, oc=16, dev=dict(GB300, max_cluster=8))[0] == sv.SV_ERR_UNSUPPORTED
+    assert gplan(sv, 0, 2, 50000, 1)[0] == sv.SV_ERR_INVALID_ARG
+    assert gplan(sv, 1, 33, 50000, 1)[0] == sv.SV_ERR_INVALID_ARG

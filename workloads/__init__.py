@@ -277,6 +277,16 @@ def make_config(name: str, seed: Optional[int] = None, B: Optional[int] = None,
     return Inputs(name, B, K, V, cfg.dtype, T, logits, q, tokens, np.ascontiguousarray(u))
 
 
+def greedy_drafts(inp: Inputs) -> Inputs:
+    """The same workload with a greedy drafter: x_i = argmax_v q[b, i, v] (lowest
+    id among equal maxima) instead of a draw from q.  Used for greedy
+    verification, where the target side is greedy too."""
+    tokens = (np.argmax(inp.q, axis=-1).astype(np.int32) if inp.K
+              else np.zeros((inp.B, 0), np.int32))
+    return Inputs(inp.name + "_greedy", inp.B, inp.K, inp.V, inp.dtype, inp.T, inp.logits, inp.q,
+                  np.ascontiguousarray(tokens), inp.uniforms)
+
+
 def make_random(B: int, K: int, V: int, dtype: str = "f32", T: float = 1.0, sigma: float = 2.0,
                 sigma_draft: float = 1.0, seed: int = 0, name: str = "random") -> Inputs:
     """Small random instance with the value distribution of the first workload."""
