@@ -16,11 +16,12 @@
 // Design: a thread-block cluster of C CTAs per sequence, CTA r owning a
 // vocabulary slice of every row and each warp a stretch of that slice.  Lanes
 // stream 16-byte vectors (eight deep per lane) with non-allocating loads and
-// keep the largest vector maximum and the vector that first reached it; the
-// entry index is recovered at the end of the row by re-reading that one
-// vector.  Warp, CTA and cluster partials (value, lowest index, bad-value
-// flag) meet through shared memory and one cluster barrier per row; every CTA
-// takes the same decision from the same data.
+// keep the largest value and the first entry holding it (found from the
+// registers in the rare step where the maximum grows).  Each warp pushes its
+// partial (value, lowest index, bad-value flag) into a slot of every CTA of
+// the cluster with st.async, counted on that CTA's mbarrier; every warp then
+// merges all partials itself and reaches the same decision, so a row costs no
+// CTA or cluster barrier.
 #include <cuda_runtime.h>
 #include <cooperative_groups.h>
 
@@ -52,6 +53,7 @@ struct GArgs {
     uint32_t* al_hist;
     int64_t V, slice;
     int B, K, C, vec;
+    unsigned long long wait_ns;
 };
 
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
@@ -123,45 +125,109 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return (uint32_t)__cvta_generic_to_shared(p);
 }
 
-__device__ __forceinline__ float4 ld_cluster_v4(const void* local, uint32_t rank) {
-    uint32_t a;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_addr(local)), "r"(rank));
-    float4 r;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
-                 : "r"(a)
-                 : "memory");
-    return r;
+__device__ __forceinline__ void mbar_init(unsigned long long* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
 }
 
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+__device__ __forceinline__ void mbar_expect(unsigned long long* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(unsigned long long* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long now_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for phase `parity` of `bar`, sleeping between polls; false after
+// `limit_ns` (the partials never came).
+__device__ __noinline__ bool mbar_wait_limited(unsigned long long* bar, uint32_t parity,
+                                               unsigned long long limit_ns) {
+    if (mbar_try(bar, parity))
+        return true;
+    const unsigned long long t0 = now_ns();
+    unsigned sleep = 32;
+    for (uint32_t it = 0; it < (1u << 26); ++it) {
+        __nanosleep(sleep);
+        if (mbar_try(bar, parity))
+            return true;
+        if (sleep < 256)
+            sleep <<= 1;
+        if ((it & 15u) == 15u && now_ns() - t0 > limit_ns)
+            return false;
+    }
+    return false;
+}
+
+// 16 bytes into the same shared-memory slot of cluster CTA `rank`, counted on
+// that CTA's barrier `bar` (same offset) as complete_tx.
+__device__ __forceinline__ void push_v4(const void* slot, const void* bar, uint32_t rank, float4 v) {
+    uint32_t d, m;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(smem_addr(slot)), "r"(rank));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(m) : "r"(smem_addr(bar)), "r"(rank));
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(d),
+        "r"(__float_as_uint(v.x)), "r"(__float_as_uint(v.y)), "r"(__float_as_uint(v.z)),
+        "r"(__float_as_uint(v.w)), "r"(m)
+        : "memory");
+}
+
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 template <int ES>
 __global__ void __launch_bounds__(kNT, 8) sv_greedy_kernel(const __grid_constant__ GArgs a) {
     constexpr int E = 16 / ES;  // entries per 16-byte vector
     constexpr uint32_t kPad = ES == 2 ? 0xff80ff80u : 0xff800000u;  // -inf entries past the stretch
+    constexpr int kPer = (sv::kMaxCluster * kNW + 31) / 32;           // partials per lane, at most
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = (int)cluster.block_rank();
     const int b = (int)(blockIdx.x / (unsigned)a.C);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int K = a.K, C = a.C;
+    const int P = C * kNW;  // partials per row: every warp of the cluster
     const int64_t V = a.V;
 
-    __shared__ float4 wpart[kNW];          // per warp: (value, index bits, bad, 0)
-    __shared__ __align__(16) float4 cpart[2];  // this CTA's partial, by row parity
-    __shared__ int dec[2];                 // (a_i, state) of the row just decided
+    // part[parity][rank * kNW + warp] is pushed by that warp of every CTA;
+    // xbar[parity] counts the bytes (one phase per row of that parity)
+    __shared__ __align__(16) float4 part[2][sv::kMaxCluster * kNW];
+    __shared__ __align__(8) unsigned long long xbar[2];
     __shared__ int xs[sv::kMaxK];
 
     const int64_t v0 = (int64_t)rank * a.slice;
     const int64_t L = v0 < V ? (V - v0 < a.slice ? V - v0 : a.slice) : 0;
     const int64_t row0 = (int64_t)b * (K + 1);
 
+    if (tid == 0) {
+        mbar_init(&xbar[0], 1);
+        mbar_init(&xbar[1], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
     if (tid < K)
         xs[tid] = a.tokens[(int64_t)b * K + tid];
     __syncthreads();
+    // every CTA's barriers are initialised before anyone pushes into them
+    cluster_arrive();
+    bool ready = false;
     int state = SV_OK;
     if (__any_sync(kFull, lane < K && (xs[lane] < 0 || (int64_t)xs[lane] >= V)))
         state = SV_ERR_TOKEN_RANGE;
@@ -175,6 +241,10 @@ __global__ void __launch_bounds__(kNT, 8) sv_greedy_kernel(const __grid_constant
 
     int j = -1, tok = -1;
     for (int i = 0; i <= K && state == SV_OK; ++i) {
+        const int par = i & 1;
+        const uint32_t phase = (uint32_t)(i >> 1) & 1u;
+        if (tid == 0)  // this row's partials, from every warp of the cluster
+            mbar_expect(&xbar[par], (uint32_t)(P * 16));
         const unsigned char* row =
             static_cast<const unsigned char*>(a.logits) + ((row0 + i) * V + v0) * ES;
         float best = -INFINITY;
@@ -182,7 +252,6 @@ __global__ void __launch_bounds__(kNT, 8) sv_greedy_kernel(const __grid_constant
         bool bad = false;
         if (a.vec) {
             const uint4* rp = reinterpret_cast<const uint4*>(row);
-            int64_t bvec = -1;
             for (int64_t base = w0; base < w1; base += 32 * kDepth) {
                 uint4 r[kDepth];
 #pragma unroll
@@ -193,24 +262,20 @@ __global__ void __launch_bounds__(kNT, 8) sv_greedy_kernel(const __grid_constant
 #pragma unroll
                 for (int k = 0; k < kDepth; ++k) {
                     const float m = vec_max<ES>(r[k]);
-                    if (!(m <= best)) {  // larger, or NaN
+                    if (!(m <= best)) {  // larger, or NaN (rare after the first vectors)
                         if (m != m) {
                             bad = true;
-                        } else {
+                        } else {  // the first entry of this vector holding m
+                            int e = E - 1;
+#pragma unroll
+                            for (int t = E - 1; t >= 0; --t)
+                                if (vec_entry<ES>(r[k], t) == m)
+                                    e = t;
                             best = m;
-                            bvec = base + k * 32 + lane;
+                            bidx = (int)(v0 + (base + k * 32 + lane) * E + e);
                         }
                     }
                 }
-            }
-            if (bvec >= 0 && best > -INFINITY) {  // the first entry of that vector holding best
-                const uint4 r = ld_stream(rp + bvec);
-                int e = E - 1;
-#pragma unroll
-                for (int t = E - 1; t >= 0; --t)
-                    if (vec_entry<ES>(r, t) == best)
-                        e = t;
-                bidx = (int)(v0 + bvec * E + e);
             }
         } else {
             for (int64_t e = w0 + lane; e < w1; e += 32) {
@@ -227,55 +292,42 @@ __global__ void __launch_bounds__(kNT, 8) sv_greedy_kernel(const __grid_constant
             bad = true;
         warp_best(best, bidx);
         bad = __any_sync(kFull, bad);
-        const int par = i & 1;
-        if (lane == 0)
-            wpart[warp] = make_float4(best, __int_as_float(bidx), bad ? 1.f : 0.f, 0.f);
-        __syncthreads();
-        if (warp == 0) {
-            float v = -INFINITY;
-            int ix = kNoIndex;
-            float bd = 0.f;
-            if (lane < kNW) {
-                const float4 p = wpart[lane];
-                v = p.x;
-                ix = __float_as_int(p.y);
-                bd = p.z;
-            }
-            warp_best(v, ix);
-            const bool any_bad = __any_sync(kFull, bd != 0.f);
-            if (lane == 0)
-                cpart[par] = make_float4(v, __int_as_float(ix), any_bad ? 1.f : 0.f, 0.f);
+        if (!ready) {
+            cluster_wait();
+            ready = true;
         }
-        cluster_sync_all();  // every CTA's partial of row i is in place
-        if (warp == 0) {
-            float v = -INFINITY;
-            int ix = kNoIndex;
-            float bd = 0.f;
-            if (lane < C) {
-                const float4 p = ld_cluster_v4(&cpart[par], (uint32_t)lane);
-                v = p.x;
-                ix = __float_as_int(p.y);
-                bd = p.z;
-            }
-            warp_best(v, ix);
-            const bool any_bad = __any_sync(kFull, bd != 0.f);
-            if (lane == 0) {
-                dec[0] = ix;
-                dec[1] = (any_bad || !(v > -INFINITY)) ? SV_ERR_NONFINITE : SV_OK;
-            }
-        }
-        __syncthreads();
-        const int ai = dec[0];
-        state = dec[1];
-        __syncthreads();  // dec is rewritten by the next row
-        if (state != SV_OK)
+        if (lane < C)
+            push_v4(&part[par][rank * kNW + warp], &xbar[par], (uint32_t)lane,
+                    make_float4(best, __int_as_float(bidx), bad ? 1.f : 0.f, 0.f));
+        // every warp merges the P partials itself and reaches the same decision
+        if (!mbar_wait_limited(&xbar[par], phase, a.wait_ns)) {
+            state = SV_ERR_TIMEOUT;
             break;
+        }
+        float v = -INFINITY;
+        int ix = kNoIndex;
+        bool any_bad = false;
+#pragma unroll
+        for (int t = 0; t < kPer; ++t) {
+            const int p = lane + 32 * t;
+            if (p < P) {
+                const float4 q = part[par][p];
+                better(v, ix, q.x, __float_as_int(q.y));
+                any_bad |= q.z != 0.f;
+            }
+        }
+        warp_best(v, ix);
+        any_bad = __any_sync(kFull, any_bad);
+        if (any_bad || !(v > -INFINITY)) {
+            state = SV_ERR_NONFINITE;
+            break;
+        }
         if (a.row_argmax && rank == 0 && tid == 0)
-            a.row_argmax[row0 + i] = ai;
-        if (i < K && xs[i] == ai)
+            a.row_argmax[row0 + i] = ix;
+        if (i < K && xs[i] == ix)
             continue;
         j = i;
-        tok = ai;
+        tok = ix;
         break;
     }
 
@@ -301,8 +353,11 @@ __global__ void __launch_bounds__(kNT, 8) sv_greedy_kernel(const __grid_constant
                 atomicAdd(a.al_hist + (err ? 0 : j + 1), 1u);
         }
     }
-    // no CTA leaves while another may still read its partials
-    cluster_sync_all();
+    // no CTA leaves while a push into it may still be on its way
+    if (!ready)
+        cluster_wait();
+    cluster_arrive();
+    cluster_wait();
 }
 
 }  // namespace
@@ -338,6 +393,7 @@ int greedy_launch(const GreedyLaunch& g, void* stream) {
     a.K = g.K;
     a.C = g.C;
     a.vec = g.vec;
+    a.wait_ns = g.wait_ns;
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
     cfg.gridDim = dim3((unsigned)((int64_t)g.B * g.C), 1, 1);

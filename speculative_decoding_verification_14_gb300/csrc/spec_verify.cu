@@ -1994,6 +1994,7 @@ int spec_verify_run_greedy(sv_ctx* ctx, const void* target_logits, int logits_dt
     g.C = plan.cluster;
     g.es = es;
     g.vec = plan.bulk_copy && aligned(target_logits, 16) ? 1 : 0;
+    g.wait_ns = ctx->wait_ns;
     DeviceGuard guard(ctx->device);
     return sv::greedy_launch(g, stream) == 0 ? SV_OK : SV_ERR_CUDA;
 }

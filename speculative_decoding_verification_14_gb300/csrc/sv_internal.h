@@ -68,6 +68,7 @@ struct GreedyLaunch {
     int B, K, C;
     int es;   // bytes per logit (2 or 4)
     int vec;  // 1: 16-byte vector loads (aligned rows)
+    unsigned long long wait_ns;  // give up on a row's partials after this long
 };
 int greedy_set_attributes();                              // 0 on success
 int greedy_launch(const GreedyLaunch& g, void* stream);  // 0 on success
