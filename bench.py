@@ -58,6 +58,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph-launches", type=int, default=30,
+                    help="steps captured in one CUDA graph for the graph-replay timing (0 = skip)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--clock-window", type=float, default=2.0,
                     help="seconds of untimed load, sampled for clocks, before the timed steps")
@@ -243,16 +245,16 @@ def run_ours(args):
         if greedy:
             calls.append((verifier.ctx, lg.data_ptr(), dcode, x.data_ptr(), B, K, V,
                           outs["accept_len"].data_ptr(), outs["out_tokens"].data_ptr(),
-                          outs["accept_mask"].data_ptr(), None, None, stream.cuda_stream))
+                          outs["accept_mask"].data_ptr(), None, None))
         else:
             calls.append((verifier.ctx, lg.data_ptr(), dcode, q.data_ptr(), x.data_ptr(),
                           u.data_ptr(), B, K, V, ctypes.c_float(T), outs["accept_len"].data_ptr(),
                           outs["out_tokens"].data_ptr(), outs["accept_mask"].data_ptr(), None,
-                          None, None, stream.cuda_stream))
+                          None, None))
     run = lib.spec_verify_run_greedy if greedy else lib.spec_verify_run
 
-    def step(k):
-        rc = run(*calls[k % nsets])
+    def step(k, s=None):
+        rc = run(*calls[k % nsets], stream.cuda_stream if s is None else s)
         if rc != 0:
             raise sv.SpecVerifyError(rc, "spec_verify_run_greedy" if greedy else "spec_verify_run")
 
@@ -274,35 +276,61 @@ def run_ours(args):
             k += 1
         torch.cuda.synchronize()
 
-    # timed region: K steps, an event pair around every launch on its stream
+    # timed region: K back-to-back steps between two events on the launch
+    # stream (events between the launches would add their own gaps)
     barrier()
     torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for k in range(args.steps):
-        ev[k][0].record(stream)
         step(k)
-        ev[k][1].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
     total_ms = t0.elapsed_time(t1)
-    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    local_ms = total_ms
     if dist is not None:
         tt = torch.tensor([total_ms], device="cuda")
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         total_ms = float(tt.item())
+
+    # the same steps replayed from a CUDA graph: no host launch cost between
+    # kernels, so small workloads show their device time
+    graph = None
+    if args.graph_launches > 0:
+        n_in = args.graph_launches
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step(0, side.cuda_stream)  # outside the capture: the library is set up
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=side):
+                for k in range(n_in):
+                    step(k, side.cuda_stream)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        reps = max(3, min(50, int(2e5 / max(1.0, local_ms * 1e3 / args.steps * n_in))))
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        g1.record(stream)
+        torch.cuda.synchronize()
+        graph = {"us_per_launch": g0.elapsed_time(g1) * 1e3 / (reps * n_in),
+                 "launches_per_graph": n_in, "replays": reps}
+        del g
 
     err, _ = verifier.error()
     if err != sv.SV_OK:
         raise sv.SpecVerifyError(err, "device error during the benchmark")
     acc = outs["accept_len"].cpu().numpy()
     alg = algorithmic_bytes_greedy(inp, acc) if greedy else algorithmic_bytes(inp, acc)
-    avg_launch_s = statistics.mean(launch_ms) / 1e3
+    avg_launch_s = local_ms / args.steps / 1e3  # this rank's average launch duration
     rows_per_step = B * (K + 1)
     value = world * rows_per_step * args.steps / (total_ms / 1e3)
     tokens_per_step = int(acc.sum())
@@ -385,6 +413,7 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": args.steps,
+        "graph_replay": graph,
         "clocks": clk,
     }
     return line
