@@ -21,7 +21,7 @@ _SRC = os.path.join(_HERE, "oracle.c")
 _HDR = os.path.join(_HERE, "oracle.h")
 _LIB = os.path.join(_HERE, "liboracle.so")
 
-OK, TOKEN_RANGE, NONFINITE, UNIFORM_RANGE = 0, 4, 5, 7
+OK, TOKEN_RANGE, NONFINITE, UNIFORM_RANGE, BAD_OFFSETS = 0, 4, 5, 7, 8
 
 _lib: Optional[ctypes.CDLL] = None
 
@@ -43,6 +43,9 @@ def _bind(path: str) -> ctypes.CDLL:
     lib.oracle_verify.restype = ctypes.c_int
     lib.oracle_verify.argtypes = [P, ctypes.c_int, P, P, P, ctypes.c_int64, ctypes.c_int,
                                   ctypes.c_int64, ctypes.c_float] + [P] * 10
+    lib.oracle_verify_ragged.restype = ctypes.c_int
+    lib.oracle_verify_ragged.argtypes = [P, ctypes.c_int, P, P, P, P, ctypes.c_int64, ctypes.c_int,
+                                         ctypes.c_int64, ctypes.c_int64, ctypes.c_float] + [P] * 10
     lib.oracle_verify_greedy.restype = ctypes.c_int
     lib.oracle_verify_greedy.argtypes = [P, ctypes.c_int, P, ctypes.c_int64, ctypes.c_int,
                                          ctypes.c_int64, P, P, P, P, P]
@@ -123,6 +126,42 @@ def verify(logits: np.ndarray, dtype: str, q: np.ndarray, tokens: np.ndarray,
                            _ptr(out["sample_margin"]), _ptr(out["sample_alt"]))
     if rc != 0:
         raise ValueError(f"oracle_verify rejected its arguments (rc={rc})")
+    return out
+
+
+def verify_ragged(logits: np.ndarray, dtype: str, q: np.ndarray, tokens: np.ndarray,
+                  uniforms: np.ndarray, offsets: np.ndarray, K_max: int, T: float,
+                  lib: Optional[ctypes.CDLL] = None) -> dict:
+    """Ragged batch.  logits [R, V] packed target rows (sequence b owns rows
+    offsets[b]..offsets[b+1]-1), q [R-B, V], tokens [R-B], uniforms [R],
+    offsets [B+1] int32.  Returns packed accept_len [B], out_tokens [R],
+    accept_mask [R-B], status [B], row_m/row_s [R], p_draft [R-B] and the
+    margins [B]."""
+    lib = lib or _load()
+    logits = np.ascontiguousarray(logits, dtype=np.float32 if dtype == "f32" else np.uint16)
+    R, V = logits.shape
+    offsets = np.ascontiguousarray(offsets, dtype=np.int32)
+    B = offsets.size - 1
+    nd = max(R - B, 0)
+    q = np.ascontiguousarray(q, dtype=np.float32).reshape(nd, V)
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32).reshape(nd)
+    uniforms = np.ascontiguousarray(uniforms, dtype=np.float32).reshape(R)
+    out = {
+        "accept_len": np.empty(B, np.int32), "out_tokens": np.full(R, -1, np.int32),
+        "accept_mask": np.zeros(max(nd, 1), np.uint8)[:nd], "status": np.empty(B, np.int32),
+        "row_m": np.full(R, np.nan), "row_s": np.full(R, np.nan), "p_draft": np.full(nd, np.nan),
+        "accept_margin": np.empty(B), "sample_margin": np.empty(B),
+        "sample_alt": np.empty(B, np.int32),
+    }
+    rc = lib.oracle_verify_ragged(_ptr(logits), _dtype_code(dtype), _ptr(q), _ptr(tokens),
+                                  _ptr(uniforms), _ptr(offsets), B, K_max, R, V, float(T),
+                                  _ptr(out["accept_len"]), _ptr(out["out_tokens"]),
+                                  _ptr(out["accept_mask"]), _ptr(out["status"]),
+                                  _ptr(out["row_m"]), _ptr(out["row_s"]), _ptr(out["p_draft"]),
+                                  _ptr(out["accept_margin"]), _ptr(out["sample_margin"]),
+                                  _ptr(out["sample_alt"]))
+    if rc != 0:
+        raise ValueError(f"oracle_verify_ragged rejected its arguments (rc={rc})")
     return out
 
 

@@ -436,3 +436,53 @@ int oracle_verify_greedy(const void* logits, int dtype, const int32_t* tokens, i
     }
     return 0;
 }
+
+/* Ragged batches: sequence b owns target rows [off[b], off[b+1]) of a packed
+ * [R, V] logits array, so its draft depth is K_b = off[b+1] - off[b] - 1.  The
+ * pages verify one sequence at a time ([P1]'s loop); batching is a scheduling
+ * matter ([P1] "Scheduling interaction"), so each sequence is verified on its
+ * own by oracle_verify with its own K_b.  Its draft rows, tokens, mask and
+ * draft probabilities start at off[b] - b (K_b of them); uniforms, output
+ * tokens and row statistics at off[b] (K_b + 1).  Offsets that do not describe
+ * such a packing (off[b] < b, off[b+1] <= off[b], K_b > K_max, or too few rows
+ * left for the sequences after b) make that sequence an error
+ * (ORACLE_BAD_OFFSETS, accept_len 0) and nothing of it is read or written
+ * except accept_len and status. */
+int oracle_verify_ragged(const void* logits, int dtype, const float* q, const int32_t* tokens,
+                         const float* uniforms, const int32_t* off, int64_t B, int K_max,
+                         int64_t R, int64_t V, float temperature, int32_t* accept_len,
+                         int32_t* out_tokens, uint8_t* accept_mask, int32_t* status,
+                         double* row_m, double* row_s, double* p_draft, double* accept_margin,
+                         double* sample_margin, int32_t* sample_alt)
+{
+    if (!off || B < 0 || K_max < 0 || R < B)
+        return -1;
+    const size_t esz = dtype == 0 ? 4 : 2;
+    for (int64_t b = 0; b < B; ++b) {
+        const int64_t o0 = off[b], o1 = off[b + 1];
+        const int64_t Kb = o1 - o0 - 1;
+        if (o0 < b || Kb < 0 || Kb > K_max || o1 + (B - b - 1) > R) {
+            accept_len[b] = 0;
+            if (status)
+                status[b] = ORACLE_BAD_OFFSETS;
+            if (accept_margin)
+                accept_margin[b] = INFINITY;
+            if (sample_margin)
+                sample_margin[b] = INFINITY;
+            if (sample_alt)
+                sample_alt[b] = -1;
+            continue;
+        }
+        const int64_t d0 = o0 - b; /* first draft row of sequence b */
+        const int rc = oracle_verify(
+            (const char*)logits + (size_t)o0 * (size_t)V * esz, dtype,
+            Kb ? q + (size_t)d0 * (size_t)V : 0, Kb ? tokens + d0 : 0, uniforms + o0, 1, (int)Kb, V,
+            temperature, accept_len + b, out_tokens + o0, Kb ? accept_mask + d0 : 0,
+            status ? status + b : 0, row_m ? row_m + o0 : 0, row_s ? row_s + o0 : 0,
+            p_draft && Kb ? p_draft + d0 : 0, accept_margin ? accept_margin + b : 0,
+            sample_margin ? sample_margin + b : 0, sample_alt ? sample_alt + b : 0);
+        if (rc != 0)
+            return rc;
+    }
+    return 0;
+}

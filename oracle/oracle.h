@@ -36,6 +36,7 @@ extern "C" {
 #define ORACLE_TOKEN_RANGE 4   /* a draft token outside [0, V)                       */
 #define ORACLE_NONFINITE 5     /* NaN / +inf / all -inf target row, or bad q value    */
 #define ORACLE_UNIFORM_RANGE 7 /* a uniform outside [0, 1) or NaN                     */
+#define ORACLE_BAD_OFFSETS 8   /* ragged batch: offsets that describe no packing      */
 
 /* Softmax of one target row at temperature T, in double precision.
  *   row: V stored logits (dtype 0 = float32, 1 = bfloat16 bit patterns).
@@ -77,6 +78,18 @@ int oracle_verify(const void* logits, int dtype, const float* q, const int32_t* 
                   int32_t* accept_len, int32_t* out_tokens, uint8_t* accept_mask,
                   int32_t* status, double* row_m, double* row_s, double* p_draft,
                   double* accept_margin, double* sample_margin, int32_t* sample_alt);
+
+/* Ragged batch: sequence b owns packed target rows [off[b], off[b+1]) of R,
+ * K_b = off[b+1] - off[b] - 1 <= K_max; its draft rows, tokens, mask and
+ * p_draft start at off[b] - b, its uniforms, out_tokens and row stats at
+ * off[b].  Each sequence is verified by oracle_verify with its own K_b;
+ * offsets that describe no packing give ORACLE_BAD_OFFSETS for that sequence. */
+int oracle_verify_ragged(const void* logits, int dtype, const float* q, const int32_t* tokens,
+                         const float* uniforms, const int32_t* off, int64_t B, int K_max,
+                         int64_t R, int64_t V, float temperature, int32_t* accept_len,
+                         int32_t* out_tokens, uint8_t* accept_mask, int32_t* status,
+                         double* row_m, double* row_s, double* p_draft, double* accept_margin,
+                         double* sample_margin, int32_t* sample_alt);
 
 /* Greedy verification, the limit T -> 0 of oracle_verify: a_i = the first
  * token holding the largest logit of row i; draft x_i is accepted iff

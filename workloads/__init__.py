@@ -277,6 +277,53 @@ def make_config(name: str, seed: Optional[int] = None, B: Optional[int] = None,
     return Inputs(name, B, K, V, cfg.dtype, T, logits, q, tokens, np.ascontiguousarray(u))
 
 
+@dataclasses.dataclass
+class RaggedInputs:
+    """A ragged batch: sequence b owns packed target rows offsets[b] ..
+    offsets[b+1]-1, i.e. K_b + 1 rows with its own draft depth K_b.
+
+    logits [R, V], q [R-B, V], tokens [R-B], uniforms [R], offsets [B+1] int32.
+    """
+    name: str
+    B: int
+    K_max: int
+    V: int
+    dtype: str
+    T: float
+    logits: np.ndarray
+    q: np.ndarray
+    tokens: np.ndarray
+    uniforms: np.ndarray
+    offsets: np.ndarray
+
+    @property
+    def R(self) -> int:
+        return int(self.offsets[-1])
+
+    @property
+    def logit_bytes(self) -> int:
+        return 2 if self.dtype == "bf16" else 4
+
+
+def ragged_from(inp: Inputs, Ks) -> RaggedInputs:
+    """Pack the first K_b + 1 target rows, K_b draft rows, K_b tokens and
+    K_b + 1 uniforms of every sequence of a uniform batch (K_b <= K)."""
+    Ks = np.asarray(Ks, dtype=np.int64)
+    assert Ks.shape == (inp.B,) and Ks.min() >= 0 and Ks.max() <= inp.K
+    offsets = np.zeros(inp.B + 1, np.int32)
+    offsets[1:] = np.cumsum(Ks + 1)
+    lg = np.concatenate([inp.logits[b, :k + 1] for b, k in enumerate(Ks)])
+    q = (np.concatenate([inp.q[b, :k] for b, k in enumerate(Ks)]) if Ks.sum()
+         else np.zeros((0, inp.V), np.float32))
+    x = (np.concatenate([inp.tokens[b, :k] for b, k in enumerate(Ks)]) if Ks.sum()
+         else np.zeros(0, np.int32))
+    u = np.concatenate([inp.uniforms[b, :k + 1] for b, k in enumerate(Ks)])
+    return RaggedInputs(inp.name + "_ragged", inp.B, inp.K, inp.V, inp.dtype, inp.T,
+                        np.ascontiguousarray(lg), np.ascontiguousarray(q, dtype=np.float32),
+                        np.ascontiguousarray(x, dtype=np.int32),
+                        np.ascontiguousarray(u, dtype=np.float32), offsets)
+
+
 def greedy_drafts(inp: Inputs) -> Inputs:
     """The same workload with a greedy drafter: x_i = argmax_v q[b, i, v] (lowest
     id among equal maxima) instead of a draw from q.  Used for greedy
