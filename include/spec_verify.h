@@ -80,7 +80,8 @@ typedef enum {
     SV_ERR_TOKEN_RANGE = 4,   /* device: a draft token outside [0, V)                         */
     SV_ERR_NONFINITE = 5,     /* device: NaN/+inf/all -inf logits row, or NaN/inf/negative q  */
     SV_ERR_TIMEOUT = 6,       /* device: a bounded wait for a bulk copy ran out               */
-    SV_ERR_UNIFORM_RANGE = 7  /* device: a uniform outside [0, 1)                             */
+    SV_ERR_UNIFORM_RANGE = 7, /* device: a uniform outside [0, 1)                             */
+    SV_ERR_BAD_OFFSETS = 8    /* device: ragged-batch row offsets that describe no packing    */
 } sv_status;
 
 /* Opaque context: device id, limits, launch-plan cache, error word. */
@@ -149,6 +150,37 @@ int spec_verify_set_plan_override(sv_ctx* ctx, int cluster, int group, int threa
 int spec_verify_plan_for(int num_sms, int smem_per_cta, int max_cluster,
                          int B, int K, int64_t V, int logits_dtype,
                          int ovr_cluster, int ovr_group, int ovr_threads, sv_plan* out);
+
+/* Ragged batch ([P1] "Scheduling interaction": continuous batching mixes
+ * sequences at different points): every sequence b has its own draft depth
+ * K_b <= K_max and its rows are packed.  `row_offsets` [B+1] (int32, device)
+ * gives sequence b the target rows row_offsets[b] .. row_offsets[b+1]-1, so
+ * K_b = row_offsets[b+1] - row_offsets[b] - 1, with row_offsets[0] = 0 and
+ * row_offsets[B] = total_rows.  Packed layouts (device, V innermost):
+ *   target_logits [total_rows, V]   rows of b from row_offsets[b]
+ *   q             [total_rows-B, V] draft rows of b from row_offsets[b] - b
+ *   draft_tokens  [total_rows-B]    from row_offsets[b] - b
+ *   uniforms      [total_rows]      from row_offsets[b]: K_b tests, then the draw
+ *   accept_len    [B]               in [1, K_b+1]; 0 = sequence error
+ *   out_tokens    [total_rows]      from row_offsets[b], -1 padded
+ *   accept_mask   [total_rows-B]    from row_offsets[b] - b
+ *   row_stats     [total_rows, 2]   optional, from row_offsets[b]
+ *   p_draft       [total_rows-B]    optional, from row_offsets[b] - b
+ *   status        [B]               optional
+ * Each sequence is verified exactly as spec_verify_run verifies it alone.
+ * Offsets are read on the device: a sequence whose pair describes no packing
+ * (row_offsets[b] < b, K_b < 0 or > K_max, or fewer than B-1-b rows left after
+ * it within total_rows) gets SV_ERR_BAD_OFFSETS (status, error word,
+ * accept_len 0) and nothing else of it is read or written.
+ * Returns SV_OK, SV_ERR_INVALID_ARG (as spec_verify_run, with B <= total_rows
+ * <= B*(K_max+1)), SV_ERR_UNSUPPORTED or SV_ERR_CUDA. */
+int spec_verify_run_ragged(sv_ctx* ctx,
+                           const void* target_logits, int logits_dtype,
+                           const float* q, const int32_t* draft_tokens, const float* uniforms,
+                           const int32_t* row_offsets, int64_t total_rows,
+                           int B, int K_max, int64_t V, float temperature,
+                           int32_t* accept_len, int32_t* out_tokens, uint8_t* accept_mask,
+                           float* row_stats, float* p_draft, int32_t* status, void* stream);
 
 /* Greedy verification: the verify of spec_verify_run in the limit T -> 0
  * ([P1] "Speculative decoding: draft first, then verify": as T falls, the

@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(PKG, "libspecverify.so")
 
 SV_F32, SV_BF16 = 0, 1
 (SV_OK, SV_ERR_INVALID_ARG, SV_ERR_UNSUPPORTED, SV_ERR_CUDA, SV_ERR_TOKEN_RANGE, SV_ERR_NONFINITE,
- SV_ERR_TIMEOUT, SV_ERR_UNIFORM_RANGE) = range(8)
+ SV_ERR_TIMEOUT, SV_ERR_UNIFORM_RANGE, SV_ERR_BAD_OFFSETS) = range(9)
 
 
 class SpecVerifyError(RuntimeError):
@@ -80,6 +80,10 @@ def library() -> ctypes.CDLL:
                                                     ctypes.c_int, ctypes.c_int, ctypes.c_int64,
                                                     ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                     ctypes.c_int, ctypes.POINTER(sv_plan)]),
+            "spec_verify_run_ragged": (ctypes.c_int, [P, P, ctypes.c_int, P, P, P, P,
+                                                      ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                                      ctypes.c_int64, ctypes.c_float, P, P, P, P,
+                                                      P, P, P]),
             "spec_verify_run_greedy": (ctypes.c_int, [P, P, ctypes.c_int, P, ctypes.c_int,
                                                       ctypes.c_int, ctypes.c_int64, P, P, P, P,
                                                       P, P]),
@@ -152,6 +156,17 @@ def spec_verify_run_noalloc(device, logits_ptr, dtype, q_ptr, tokens_ptr, unifor
                                              uniforms_ptr, B, K, V, float(T), accept_len_ptr,
                                              out_tokens_ptr, accept_mask_ptr, row_stats_ptr,
                                              p_draft_ptr, status_ptr, stream)
+
+
+def spec_verify_run_ragged(ctx, logits_ptr, dtype, q_ptr, tokens_ptr, uniforms_ptr, offsets_ptr,
+                           total_rows, B, K_max, V, T, accept_len_ptr, out_tokens_ptr,
+                           accept_mask_ptr, row_stats_ptr=None, p_draft_ptr=None, status_ptr=None,
+                           stream=None) -> int:
+    return library().spec_verify_run_ragged(ctx, logits_ptr, dtype, q_ptr, tokens_ptr,
+                                            uniforms_ptr, offsets_ptr, total_rows, B, K_max, V,
+                                            float(T), accept_len_ptr, out_tokens_ptr,
+                                            accept_mask_ptr, row_stats_ptr, p_draft_ptr,
+                                            status_ptr, stream)
 
 
 def spec_verify_run_greedy(ctx, logits_ptr, dtype, tokens_ptr, B, K, V, accept_len_ptr,
@@ -355,6 +370,44 @@ class Verifier:
                                     ptr("row_argmax"), ptr("status"), s)
         if rc != SV_OK:
             raise SpecVerifyError(rc, "spec_verify_run_greedy")
+        return out
+
+    def run_ragged(self, logits, q, tokens, uniforms, offsets, K_max: int, temperature: float,
+                   out: Optional[dict] = None, stats: bool = False, status: bool = True,
+                   stream=None) -> dict:
+        """Ragged batch: logits [R, V], q [R-B, V], tokens [R-B], uniforms [R],
+        offsets [B+1] int32 CUDA tensors (sequence b owns rows offsets[b] ..
+        offsets[b+1]-1).  Returns packed accept_len [B], out_tokens [R],
+        accept_mask [R-B], optionally row_stats [R, 2], p_draft [R-B], status [B]."""
+        import torch
+        R, V = logits.shape
+        B = offsets.numel() - 1
+        nd = R - B
+        dev = logits.device
+        if out is None:
+            out = {"accept_len": torch.empty(B, dtype=torch.int32, device=dev),
+                   "out_tokens": torch.empty(R, dtype=torch.int32, device=dev),
+                   "accept_mask": torch.empty(max(nd, 1), dtype=torch.uint8, device=dev)[:nd]}
+            if stats:
+                out["row_stats"] = torch.empty(R, 2, dtype=torch.float32, device=dev)
+                out["p_draft"] = torch.empty(max(nd, 1), dtype=torch.float32, device=dev)[:nd]
+            if status:
+                out["status"] = torch.empty(B, dtype=torch.int32, device=dev)
+        s = stream if stream is not None else torch.cuda.current_stream(dev).cuda_stream
+
+        def ptr(name):
+            t = out.get(name)
+            return None if t is None else t.data_ptr()
+
+        rc = spec_verify_run_ragged(self.ctx, logits.data_ptr(), _dtype_code(logits),
+                                    q.data_ptr() if nd else None,
+                                    tokens.data_ptr() if nd else None, uniforms.data_ptr(),
+                                    offsets.data_ptr(), R, B, K_max, V, temperature,
+                                    ptr("accept_len"), ptr("out_tokens"),
+                                    ptr("accept_mask") if nd else None, ptr("row_stats"),
+                                    ptr("p_draft") if nd else None, ptr("status"), s)
+        if rc != SV_OK:
+            raise SpecVerifyError(rc, "spec_verify_run_ragged")
         return out
 
     def plan_greedy(self, B, K, V, dtype=SV_BF16) -> dict:

@@ -77,6 +77,8 @@ struct SvArgs {
     int32_t* status;
     uint32_t* err_word;
     uint32_t* al_hist;      // optional: one count per accepted length (0 = sequence error)
+    const int32_t* offsets; // ragged batch: [B+1] packed row offsets (NULL: K rows for all)
+    int64_t total_rows;     // ragged batch: rows in the packed arrays
     int64_t V;
     int64_t slice;          // vocabulary entries per CTA (multiple of 8)
     int B, K, C, G;
@@ -730,7 +732,24 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
     const int rank = (int)cluster.block_rank();
     const int b = (int)(blockIdx.x / (unsigned)a.C);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int K = a.K;
+    // Sequence b's rows: b*(K+1) .. for a uniform batch; for a ragged one the
+    // packed rows offsets[b] .. offsets[b+1]-1 (its own depth K_b), draft rows
+    // from offsets[b] - b.  Offsets that describe no packing leave K = 0 and
+    // nothing of the sequence is read or written but accept_len and status.
+    int k_seq = a.K;
+    int64_t r_seq = (int64_t)b * (a.K + 1), d_seq = (int64_t)b * a.K;
+    bool bad_off = false;
+    if (a.offsets) {
+        const int o0 = __ldg(a.offsets + b), o1 = __ldg(a.offsets + b + 1);
+        bad_off = !(o0 >= b && o1 > o0 && o1 - o0 - 1 <= a.K &&
+                    (int64_t)o1 + (a.B - 1 - b) <= a.total_rows);
+        k_seq = bad_off ? 0 : o1 - o0 - 1;
+        r_seq = bad_off ? 0 : o0;
+        d_seq = bad_off ? 0 : (int64_t)o0 - b;
+    }
+    const int K = k_seq;
+    const int64_t row0 = r_seq;   // first target row of sequence b
+    const int64_t drow0 = d_seq;  // first draft row (and token, mask, p_draft entry)
     const int64_t V = a.V;
     const int C = a.C;
     const int G = a.G;
@@ -753,7 +772,6 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
     const int wv1 = min(nvec, wv0 + a.wvec);
     const int wn = wv1 - wv0;
     const int nch = (wn + kChunkVecs - 1) / kChunkVecs;  // ring chunks per row
-    const int64_t row0 = (int64_t)b * (K + 1);
 
     if (lane == 0) {
         for (int st = 0; st < kStages; ++st)
@@ -765,9 +783,9 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
     }
     __syncwarp();
     if (tid < K)
-        sh.x[tid] = a.tokens[(int64_t)b * K + tid];
+        sh.x[tid] = a.tokens[drow0 + tid];
     if (tid <= K)
-        sh.u[tid] = a.u[(int64_t)b * (K + 1) + tid];
+        sh.u[tid] = a.u[row0 + tid];
     if (tid == 0) {
         sh.claim = 0;
         sh.rec_row = -1;
@@ -842,7 +860,7 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
         }
     };
     // the first chunks of row 0 go out before the inputs are checked
-    if (a.bulk)
+    if (a.bulk && !bad_off)
         top_up();
 
     // ---- validation (every warp takes the same decision) ----
@@ -852,7 +870,10 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
         const float ul = lane <= K ? sh.u[lane] : 0.5f;
         const float uh = (lane == 0 && K == kMaxK) ? sh.u[kMaxK] : 0.5f;
         const bool bad_u = __any_sync(kFull, !(ul >= 0.f && ul < 1.f) || !(uh >= 0.f && uh < 1.f));
-        if (bad_x) {
+        if (bad_off) {
+            state = kStateError;
+            code = SV_ERR_BAD_OFFSETS;
+        } else if (bad_x) {
             state = kStateError;
             code = SV_ERR_TOKEN_RANGE;
         } else if (bad_u) {
@@ -864,7 +885,7 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
     if (state == kStateRun && lane < K) {
         const int x = sh.x[lane];
         lx_lane = Elem<ES>::load(a.logits, (row0 + lane) * V + x);
-        qx_lane = __ldg(a.q + ((int64_t)b * K + lane) * V + x);
+        qx_lane = __ldg(a.q + (drow0 + lane) * V + x);
     }
     const int P = C * NW;  // row partials per row: every warp of the cluster
     const bool track = a.row_stats != nullptr;  // the row max is reported
@@ -1218,7 +1239,7 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
     FF rem = {0.f, 0.f};
     if (state == kStateSample) {
         lrow = static_cast<const unsigned char*>(a.logits) + ((row0 + j) * V + v0) * ES;
-        qrow = j < K ? a.q + ((int64_t)b * K + j) * V + v0 : nullptr;
+        qrow = j < K ? a.q + (drow0 + j) * V + v0 : nullptr;
         const float na = -rowA;
         const float Sf = rowS.hi;
         const int64_t gbase_j = (row0 + j) * V + v0;  // element index of the slice start
@@ -1584,9 +1605,9 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
             const int tok = (int)(v0 + e0s + tsel * kDrawTile + (ksel * 32 + src) * E + e);
             // outputs of a finished sequence
             for (int i = lane; i <= K; i += 32) {
-                a.out_tokens[(int64_t)b * (K + 1) + i] = i < j ? sh.x[i] : (i == j ? tok : -1);
+                a.out_tokens[row0 + i] = i < j ? sh.x[i] : (i == j ? tok : -1);
                 if (i < K)
-                    a.accept_mask[(int64_t)b * K + i] = i < j ? 1 : 0;
+                    a.accept_mask[drow0 + i] = i < j ? 1 : 0;
             }
             if (lane == 0) {
                 a.accept_len[b] = j + 1;
@@ -1602,17 +1623,17 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
     if (rank == 0 && warp == 0) {
         const bool err = state == kStateError;
         const int nd = err ? 0 : ndec;
-        for (int i = lane; i <= K; i += 32) {
+        for (int i = lane; i <= K && !bad_off; i += 32) {
             if (a.row_stats) {
-                a.row_stats[((int64_t)b * (K + 1) + i) * 2] = i < nd ? sh.rs_m[i] : NAN;
-                a.row_stats[((int64_t)b * (K + 1) + i) * 2 + 1] = i < nd ? sh.rs_s[i] : NAN;
+                a.row_stats[(row0 + i) * 2] = i < nd ? sh.rs_m[i] : NAN;
+                a.row_stats[(row0 + i) * 2 + 1] = i < nd ? sh.rs_s[i] : NAN;
             }
             if (i < K && a.p_draft)
-                a.p_draft[(int64_t)b * K + i] = i < nd ? sh.pd[i] : NAN;
+                a.p_draft[drow0 + i] = i < nd ? sh.pd[i] : NAN;
             if (err) {
-                a.out_tokens[(int64_t)b * (K + 1) + i] = -1;
+                a.out_tokens[row0 + i] = -1;
                 if (i < K)
-                    a.accept_mask[(int64_t)b * K + i] = 0;
+                    a.accept_mask[drow0 + i] = 0;
             }
         }
         if (err && lane == 0) {
@@ -1735,7 +1756,8 @@ int make_plan(const sv_ctx* ctx, int B, int K, int64_t V, int dtype, sv_plan* pl
 int launch(sv_ctx* ctx, const void* logits, int dtype, const float* q, const int32_t* tokens,
            const float* uniforms, int B, int K, int64_t V, float T, int32_t* accept_len,
            int32_t* out_tokens, uint8_t* accept_mask, float* row_stats, float* p_draft,
-           int32_t* status, cudaStream_t stream) {
+           int32_t* status, cudaStream_t stream, const int32_t* offsets = nullptr,
+           int64_t total_rows = 0) {
     if (ctx->al_hist && K + 2 > ctx->al_bins)
         return SV_ERR_INVALID_ARG;
     sv_plan plan;
@@ -1762,6 +1784,8 @@ int launch(sv_ctx* ctx, const void* logits, int dtype, const float* q, const int
     args.status = status;
     args.err_word = ctx->d_err;
     args.al_hist = ctx->al_hist;
+    args.offsets = offsets;
+    args.total_rows = total_rows;
     args.V = V;
     args.slice = plan.slice;
     args.B = B;
@@ -1825,6 +1849,7 @@ const char* spec_verify_strerror(int code) {
         case SV_ERR_NONFINITE: return "non-finite target row or invalid draft probability";
         case SV_ERR_TIMEOUT: return "bounded wait for a bulk copy ran out";
         case SV_ERR_UNIFORM_RANGE: return "uniform outside [0, 1)";
+        case SV_ERR_BAD_OFFSETS: return "ragged-batch row offsets describe no packing";
         default: return "unknown status";
     }
 }
@@ -1940,6 +1965,30 @@ int spec_verify_set_plan_override(sv_ctx* ctx, int cluster, int group, int threa
     ctx->ovr_group = group;
     ctx->ovr_threads = threads;
     return SV_OK;
+}
+
+int spec_verify_run_ragged(sv_ctx* ctx, const void* target_logits, int logits_dtype,
+                           const float* q, const int32_t* draft_tokens, const float* uniforms,
+                           const int32_t* row_offsets, int64_t total_rows, int B, int K_max,
+                           int64_t V, float temperature, int32_t* accept_len,
+                           int32_t* out_tokens, uint8_t* accept_mask, float* row_stats,
+                           float* p_draft, int32_t* status, void* stream) {
+    if (!ctx || !row_offsets || !aligned(row_offsets, 4))
+        return SV_ERR_INVALID_ARG;
+    if (B < 1 || K_max < 0 || total_rows < B || total_rows > (int64_t)B * (K_max + 1))
+        return SV_ERR_INVALID_ARG;
+    // the packed arrays are checked like a uniform batch of depth K_max; the
+    // draft-side arrays are needed only if some sequence can have drafts
+    const int rc = validate(ctx, target_logits, logits_dtype, q, draft_tokens, uniforms, B,
+                            total_rows > B ? K_max : 0, V, temperature, accept_len, out_tokens,
+                            accept_mask, row_stats, p_draft, status);
+    if (rc != SV_OK)
+        return rc;
+    if ((double)total_rows * (double)V >= 1099511627776.0)  // 2^40
+        return SV_ERR_INVALID_ARG;
+    return launch(ctx, target_logits, logits_dtype, q, draft_tokens, uniforms, B, K_max, V,
+                  temperature, accept_len, out_tokens, accept_mask, row_stats, p_draft, status,
+                  static_cast<cudaStream_t>(stream), row_offsets, total_rows);
 }
 
 int spec_verify_get_plan_greedy(sv_ctx* ctx, int B, int K, int64_t V, int logits_dtype,

@@ -39,7 +39,7 @@ def test_binding_has_the_abi_names(sv):
 
 
 def test_status_strings(sv):
-    for code in range(8):
+    for code in range(9):
         assert sv.spec_verify_strerror(code) not in ("", "unknown status")
     assert sv.spec_verify_strerror(99) == "unknown status"
     assert sv.spec_verify_version() >= 100
