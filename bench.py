@@ -51,9 +51,10 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=workloads.CONFIG_ORDER)
-    ap.add_argument("--mode", choices=["sampled", "greedy"], default="sampled",
+    ap.add_argument("--mode", choices=["sampled", "greedy", "ragged"], default="sampled",
                     help="sampled: spec_verify_run at the workload's temperature; greedy: "
-                         "spec_verify_run_greedy (T -> 0) with a greedy drafter")
+                         "spec_verify_run_greedy (T -> 0) with a greedy drafter; ragged: "
+                         "spec_verify_run_ragged with per-sequence depths K_b ~ U{0..K}")
     ap.add_argument("--sets", type=int, default=3, help="input copies rotated between steps")
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--no-e2e", action="store_true")
@@ -137,6 +138,17 @@ def algorithmic_bytes(inp, accept_len: np.ndarray) -> int:
             + B * (4 + (K + 1) * 4 + K))
 
 
+def algorithmic_bytes_ragged(rg, accept_len: np.ndarray) -> int:
+    """Ragged batch: the per-sequence count of algorithmic_bytes with each
+    sequence's own depth K_b, plus the row offsets."""
+    V, es = rg.V, rg.logit_bytes
+    Ks = np.diff(rg.offsets.astype(np.int64)) - 1
+    n = accept_len.astype(np.int64)
+    per = (n * V * es + (n <= Ks) * V * 4 + np.minimum(n, Ks) * 4 + Ks * 4 + (Ks + 1) * 4
+           + 4 + (Ks + 1) * 4 + Ks)
+    return int(per.sum()) + (rg.B + 1) * 4
+
+
 def algorithmic_bytes_greedy(inp, accept_len: np.ndarray) -> int:
     """Greedy verification: n rows of logits per sequence (rows 0..n-1, read in
     order up to the first rejection), the K draft tokens, and the outputs."""
@@ -215,34 +227,52 @@ def run_ours(args):
     cfg = workloads.CONFIGS[args.workload]
     inp = workloads.make_config(args.workload, seed=cfg.seed + rank)
     greedy = args.mode == "greedy"
+    ragged = args.mode == "ragged"
     if greedy:
         inp = workloads.greedy_drafts(inp)
+    rg = None
+    if ragged:  # each sequence keeps its first K_b + 1 rows, K_b ~ U{0..K}
+        Ks = np.random.default_rng(1000 + cfg.seed + rank).integers(0, inp.K + 1, inp.B)
+        rg = workloads.ragged_from(inp, Ks)
     B, K, V, T = inp.B, inp.K, inp.V, inp.T
     dcode = sv.SV_BF16 if inp.dtype == "bf16" else sv.SV_F32
-    per_set = inp.nominal_bytes() if not greedy else inp.logits.nbytes + inp.tokens.nbytes
+    per_set = (inp.logits.nbytes + inp.tokens.nbytes if greedy else
+               rg.logits.nbytes + rg.q.nbytes if ragged else inp.nominal_bytes())
     nsets = max(1, args.sets)
 
-    def dev_logits():
+    def dev_logits(src=None):
+        src = inp.logits if src is None else src
         if inp.dtype == "bf16":
-            return torch.from_numpy(inp.logits.view(np.int16)).cuda().view(torch.bfloat16)
-        return torch.from_numpy(inp.logits).cuda()
+            return torch.from_numpy(src.view(np.int16)).cuda().view(torch.bfloat16)
+        return torch.from_numpy(src).cuda()
 
     sets = []
     for s in range(nsets):
         if greedy:  # the greedy step reads no draft probabilities and no uniforms
             sets.append((dev_logits(), None, torch.from_numpy(inp.tokens).cuda(), None))
+        elif ragged:
+            sets.append((dev_logits(rg.logits), torch.from_numpy(rg.q).cuda(),
+                         torch.from_numpy(rg.tokens).cuda(), torch.from_numpy(rg.uniforms).cuda(),
+                         torch.from_numpy(rg.offsets).cuda()))
         else:
             sets.append((dev_logits(), torch.from_numpy(inp.q).cuda(),
                          torch.from_numpy(inp.tokens).cuda(), torch.from_numpy(inp.uniforms).cuda()))
+    rows_per_step = rg.R if ragged else B * (K + 1)
     outs = {"accept_len": torch.empty(B, dtype=torch.int32, device="cuda"),
-            "out_tokens": torch.empty(B, K + 1, dtype=torch.int32, device="cuda"),
-            "accept_mask": torch.empty(B, K, dtype=torch.uint8, device="cuda")}
+            "out_tokens": torch.empty(rows_per_step, dtype=torch.int32, device="cuda"),
+            "accept_mask": torch.empty(rows_per_step - B, dtype=torch.uint8, device="cuda")}
     verifier = sv.Verifier(B, K, V)
     stream = torch.cuda.current_stream()
     lib = sv.library()
     calls = []
-    for (lg, q, x, u) in sets:
-        if greedy:
+    for st in sets:
+        lg, q, x, u = st[:4]
+        if ragged:
+            calls.append((verifier.ctx, lg.data_ptr(), dcode, q.data_ptr(), x.data_ptr(),
+                          u.data_ptr(), st[4].data_ptr(), rg.R, B, K, V, ctypes.c_float(T),
+                          outs["accept_len"].data_ptr(), outs["out_tokens"].data_ptr(),
+                          outs["accept_mask"].data_ptr(), None, None, None))
+        elif greedy:
             calls.append((verifier.ctx, lg.data_ptr(), dcode, x.data_ptr(), B, K, V,
                           outs["accept_len"].data_ptr(), outs["out_tokens"].data_ptr(),
                           outs["accept_mask"].data_ptr(), None, None))
@@ -251,12 +281,13 @@ def run_ours(args):
                           u.data_ptr(), B, K, V, ctypes.c_float(T), outs["accept_len"].data_ptr(),
                           outs["out_tokens"].data_ptr(), outs["accept_mask"].data_ptr(), None,
                           None, None))
-    run = lib.spec_verify_run_greedy if greedy else lib.spec_verify_run
+    run = (lib.spec_verify_run_greedy if greedy else lib.spec_verify_run_ragged if ragged
+           else lib.spec_verify_run)
 
     def step(k, s=None):
         rc = run(*calls[k % nsets], stream.cuda_stream if s is None else s)
         if rc != 0:
-            raise sv.SpecVerifyError(rc, "spec_verify_run_greedy" if greedy else "spec_verify_run")
+            raise sv.SpecVerifyError(rc, f"verify ({args.mode})")
 
     def barrier():
         if dist is not None:
@@ -329,9 +360,9 @@ def run_ours(args):
     if err != sv.SV_OK:
         raise sv.SpecVerifyError(err, "device error during the benchmark")
     acc = outs["accept_len"].cpu().numpy()
-    alg = algorithmic_bytes_greedy(inp, acc) if greedy else algorithmic_bytes(inp, acc)
+    alg = (algorithmic_bytes_greedy(inp, acc) if greedy else
+           algorithmic_bytes_ragged(rg, acc) if ragged else algorithmic_bytes(inp, acc))
     avg_launch_s = local_ms / args.steps / 1e3  # this rank's average launch duration
-    rows_per_step = B * (K + 1)
     value = world * rows_per_step * args.steps / (total_ms / 1e3)
     tokens_per_step = int(acc.sum())
     peak, peak_kind = measured_peak()
@@ -342,6 +373,8 @@ def run_ours(args):
     e2e = None
     if greedy and not args.no_e2e and args.e2e_steps > 0:
         e2e = e2e_greedy(args, inp, verifier, acc, dist, world, rows_per_step)
+    elif ragged and not args.no_e2e and args.e2e_steps > 0:
+        e2e = e2e_ragged(args, rg, verifier, acc, dist, world)
     elif not args.no_e2e and args.e2e_steps > 0:
         def pinned(a):
             t = torch.empty(a.shape, dtype={np.float32: torch.float32, np.uint16: torch.int16,
@@ -386,7 +419,8 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(inp, args.cpu_seconds, greedy=greedy)
+        cpu = (cpu_baseline_ragged(rg, args.cpu_seconds) if ragged
+               else cpu_baseline(inp, args.cpu_seconds, greedy=greedy))
 
     if rank != 0:
         return None
@@ -395,7 +429,10 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": args.workload + (" with a greedy drafter, greedy verify (T -> 0)"
-                                                if greedy else ""),
+                                                if greedy else
+                                                " as a ragged batch, K_b ~ U{0..K}, packed rows"
+                                                if ragged else ""),
+                   "rows": rows_per_step,
                    "B": B, "K": K, "V": V, "logits_dtype": inp.dtype,
                    "T": 0.0 if greedy else T, "l2": f"{nsets} input copies of {per_set / 1e9:.2f} GB rotated "
                                  f"(each larger than the {L2_BYTES >> 20} MB L2)",
@@ -406,7 +443,8 @@ def run_ours(args):
         "hbm_gbs_nominal": inp.nominal_bytes() / avg_launch_s / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
-                     "traffic": profile_traffic(args.workload + ("_greedy" if greedy else "")),
+                     "traffic": profile_traffic(args.workload + ("" if args.mode == "sampled"
+                                                                 else "_" + args.mode)),
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind ==
                      "measured" else "fallback 6.8 TB/s",
                      "algorithmic_bytes_per_launch": alg, "avg_launch_us": avg_launch_s * 1e6},
@@ -443,6 +481,67 @@ def cpu_baseline(inp, seconds: float, greedy: bool = False) -> dict:
     el = time.perf_counter() - t
     return {"value": reps * n * (inp.K + 1) / el, "unit": "rows/s", "cores": 1, "kind": "oracle",
             "sample": f"{reps} pass(es) over the first {n} of {inp.B} sequences ({el:.1f} s)"}
+
+
+def cpu_baseline_ragged(rg, seconds: float) -> dict:
+    """The ragged oracle as it stands, single thread, whole passes over the batch."""
+    import oracle
+    oracle.build()
+    t = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.verify_ragged(rg.logits, rg.dtype, rg.q, rg.tokens, rg.uniforms, rg.offsets,
+                             rg.K_max, rg.T)
+        reps += 1
+        el = time.perf_counter() - t
+        if el >= seconds:
+            break
+    return {"value": reps * rg.R / el, "unit": "rows/s", "cores": 1, "kind": "oracle",
+            "sample": f"{reps} pass(es) over all {rg.B} sequences ({rg.R} rows, {el:.1f} s)"}
+
+
+def e2e_ragged(args, rg, verifier, acc, dist, world) -> dict:
+    """Ragged batch end to end through the public API: pinned host copies of
+    the packed inputs to the device, spec_verify_run_ragged, outputs back, all
+    inside the timed region."""
+    import torch
+    h = {"logits": torch.from_numpy(rg.logits.view(np.int16) if rg.dtype == "bf16"
+                                    else rg.logits).pin_memory(),
+         "q": torch.from_numpy(rg.q).pin_memory(), "tokens": torch.from_numpy(rg.tokens).pin_memory(),
+         "uniforms": torch.from_numpy(rg.uniforms).pin_memory(),
+         "offsets": torch.from_numpy(rg.offsets).pin_memory()}
+    d = {k: torch.empty(t.shape, dtype=t.dtype, device="cuda") for k, t in h.items()}
+    R, B = rg.R, rg.B
+    h_out = {k: torch.empty(n, dtype=dt).pin_memory() for k, n, dt in
+             (("accept_len", B, torch.int32), ("out_tokens", R, torch.int32),
+              ("accept_mask", R - B, torch.uint8))}
+
+    def once():
+        for k in h:
+            d[k].copy_(h[k], non_blocking=True)
+        lg = d["logits"].view(torch.bfloat16) if rg.dtype == "bf16" else d["logits"]
+        out = verifier.run_ragged(lg, d["q"], d["tokens"], d["uniforms"], d["offsets"], rg.K_max,
+                                  rg.T, status=False)
+        for k, t in h_out.items():
+            t.copy_(out[k], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    once()
+    if dist is not None:
+        dist.barrier()
+    ts = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        once()
+    el = time.perf_counter() - ts
+    if dist is not None:
+        tt = torch.tensor([el], device="cuda", dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        el = float(tt.item())
+    assert np.array_equal(h_out["accept_len"].numpy(), acc)
+    return {"value": world * R * args.e2e_steps / el, "unit": "rows/s",
+            "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in h.values())),
+            "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in h_out.values())),
+            "steps": args.e2e_steps,
+            "api": "Verifier.run_ragged (spec_verify_run_ragged) with pinned host copies"}
 
 
 def e2e_greedy(args, inp, verifier, acc, dist, world, rows_per_step) -> dict:
