@@ -74,6 +74,24 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(x: float, dist, device: str = "cuda") -> float:
+    """The largest of every rank's x (the job takes as long as its slowest rank)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_inputs(workload: str, rank: int):
+    """Weak scaling: every rank verifies a batch of its own, the workload's
+    recipe with the seed moved by the rank (sequences are independent, so the
+    ranks exchange nothing)."""
+    cfg = workloads.CONFIGS[workload]
+    return workloads.make_config(workload, seed=cfg.seed + rank)
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -225,7 +243,7 @@ def run_ours(args):
     dev = torch.cuda.current_device()
 
     cfg = workloads.CONFIGS[args.workload]
-    inp = workloads.make_config(args.workload, seed=cfg.seed + rank)
+    inp = rank_inputs(args.workload, rank)
     greedy = args.mode == "greedy"
     ragged = args.mode == "ragged"
     if greedy:
@@ -322,10 +340,7 @@ def run_ours(args):
     clk = clocks.stop()
     total_ms = t0.elapsed_time(t1)
     local_ms = total_ms
-    if dist is not None:
-        tt = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(total_ms, dist)
 
     # the same steps replayed from a CUDA graph: no host launch cost between
     # kernels, so small workloads show their device time
@@ -406,10 +421,7 @@ def run_ours(args):
                                    stream=stream.cuda_stream)
             assert rc == sv.SV_OK
         el = time.perf_counter() - ts
-        if dist is not None:
-            tt = torch.tensor([el], device="cuda", dtype=torch.float64)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            el = float(tt.item())
+        el = max_over_ranks(el, dist)
         assert np.array_equal(hout["accept_len"], acc)
         h2d = inp.logits.nbytes + inp.q.nbytes + inp.tokens.nbytes + inp.uniforms.nbytes
         d2h = hout["accept_len"].nbytes + hout["out_tokens"].nbytes + hout["accept_mask"].nbytes + 4
@@ -532,10 +544,7 @@ def e2e_ragged(args, rg, verifier, acc, dist, world) -> dict:
     for _ in range(args.e2e_steps):
         once()
     el = time.perf_counter() - ts
-    if dist is not None:
-        tt = torch.tensor([el], device="cuda", dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        el = float(tt.item())
+    el = max_over_ranks(el, dist)
     assert np.array_equal(h_out["accept_len"].numpy(), acc)
     return {"value": world * R * args.e2e_steps / el, "unit": "rows/s",
             "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in h.values())),
@@ -574,10 +583,7 @@ def e2e_greedy(args, inp, verifier, acc, dist, world, rows_per_step) -> dict:
     for _ in range(args.e2e_steps):
         once()
     el = time.perf_counter() - ts
-    if dist is not None:
-        tt = torch.tensor([el], device="cuda", dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        el = float(tt.item())
+    el = max_over_ranks(el, dist)
     assert np.array_equal(h_out["accept_len"].numpy(), acc)
     return {"value": world * rows_per_step * args.e2e_steps / el, "unit": "rows/s",
             "h2d_bytes_per_step": int(inp.logits.nbytes + inp.tokens.nbytes),
