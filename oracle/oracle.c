@@ -120,11 +120,102 @@ static int64_t draw_inverse_cdf(const double* w, int64_t V, double S, double u,
     return tok;
 }
 
-/* One sequence.  p and w are scratch rows of V doubles. */
+/* Truncation of a target row (the production sampler settings of [P2] "Two
+ * things that follow from the math": temperature 0.6, top-p 0.95, min-p 0.05).
+ * The pages name the settings, not the definitions or their order; the
+ * readings taken, both on the untruncated p and therefore order-free:
+ *   min-p keeps v when p_v >= min_p * max_u p_u;
+ *   top-p keeps v when the mass of the tokens strictly more probable than v
+ *         is below top_p (the smallest set of most probable tokens whose mass
+ *         reaches top_p, with every token tied at its boundary kept);
+ * a token is kept when both keep it, and p~ = p on the kept tokens, divided by
+ * their sum.  top_p >= 1 and min_p <= 0 switch a filter off. */
+typedef struct {
+    double top_p, min_p;
+} trunc_opts;
+
+static const double* g_sort_p; /* the row qsort orders (single-threaded test code) */
+
+static int by_p_desc(const void* a, const void* b)
+{
+    const int64_t i = *(const int64_t*)a, j = *(const int64_t*)b;
+    if (g_sort_p[i] != g_sort_p[j])
+        return g_sort_p[i] > g_sort_p[j] ? -1 : 1;
+    return i < j ? -1 : (i > j);
+}
+
+/* p (a softmax row) becomes p~ in place.  *margin is lowered to the distance
+ * of the row from a filter boundary: |log(p_v / p_max) - log(min_p)| over
+ * tokens, and |mass above v - top_p| over tokens, for the filters in use. */
+static int truncate_row(double* p, int64_t V, const trunc_opts* tr, double* margin)
+{
+    double pmax = 0.0;
+    for (int64_t v = 0; v < V; ++v)
+        if (p[v] > pmax)
+            pmax = p[v];
+    unsigned char* keep = (unsigned char*)malloc((size_t)V);
+    int64_t* order = (int64_t*)malloc((size_t)V * sizeof(int64_t));
+    if (!keep || !order) {
+        free(keep);
+        free(order);
+        return -2;
+    }
+    for (int64_t v = 0; v < V; ++v) {
+        keep[v] = 1;
+        if (tr->min_p > 0.0) {
+            if (!(p[v] >= tr->min_p * pmax))
+                keep[v] = 0;
+            const double d = fabs(log(p[v] / pmax) - log(tr->min_p));
+            if (d < *margin)
+                *margin = d;
+        }
+    }
+    if (tr->top_p < 1.0) {
+        for (int64_t v = 0; v < V; ++v)
+            order[v] = v;
+        g_sort_p = p;
+        qsort(order, (size_t)V, sizeof(int64_t), by_p_desc);
+        double above = 0.0; /* mass of the tokens strictly more probable */
+        int64_t g0 = 0;
+        while (g0 < V) {
+            int64_t g1 = g0;
+            double gm = 0.0;
+            while (g1 < V && p[order[g1]] == p[order[g0]]) {
+                gm += p[order[g1]];
+                ++g1;
+            }
+            const double d = fabs(above - tr->top_p);
+            if (d < *margin)
+                *margin = d;
+            if (!(above < tr->top_p))
+                for (int64_t k = g0; k < g1; ++k)
+                    keep[order[k]] = 0;
+            above += gm;
+            g0 = g1;
+        }
+    }
+    /* nothing dropped: p~ is p itself (no second normalisation) */
+    int64_t dropped = 0;
+    for (int64_t v = 0; v < V; ++v)
+        dropped += !keep[v];
+    double kept = 0.0;
+    for (int64_t v = 0; v < V; ++v)
+        if (keep[v])
+            kept += p[v];
+    for (int64_t v = 0; v < V && dropped; ++v)
+        p[v] = keep[v] ? p[v] / kept : 0.0;
+    free(keep);
+    free(order);
+    return ORACLE_OK;
+}
+
+/* One sequence.  p and w are scratch rows of V doubles.  With `tr`, every
+ * target row is truncated (truncate_row) before it is used. */
 static int verify_one(const void* logits, int dtype, const float* q, const int32_t* x,
                       const float* u, int K, int64_t V, double T, double* p, double* w,
                       int32_t* out_tok, uint8_t* mask, double* rm, double* rs, double* pd,
-                      double* a_margin, double* s_margin, int32_t* s_alt, int32_t* len)
+                      double* a_margin, double* s_margin, int32_t* s_alt, int32_t* len,
+                      const trunc_opts* tr, double* t_margin)
 {
     const size_t esz = dtype == 0 ? 4 : 2;
     const char* lbase = (const char*)logits;
@@ -149,6 +240,8 @@ static int verify_one(const void* logits, int dtype, const float* q, const int32
     for (int i = 0; i < K; ++i) {
         int st = oracle_softmax_row(lbase + (size_t)i * (size_t)V * esz, dtype, V, T, p, &m, &s);
         if (st != ORACLE_OK)
+            return st;
+        if (tr && (st = truncate_row(p, V, tr, t_margin)) != ORACLE_OK)
             return st;
         rm[i] = m;
         rs[i] = s;
@@ -196,6 +289,8 @@ static int verify_one(const void* logits, int dtype, const float* q, const int32
         int st = oracle_softmax_row(lbase + (size_t)K * (size_t)V * esz, dtype, V, T, p, &m, &s);
         if (st != ORACLE_OK)
             return st;
+        if (tr && (st = truncate_row(p, V, tr, t_margin)) != ORACLE_OK)
+            return st;
         rm[K] = m;
         rs[K] = s;
         for (int64_t v = 0; v < V; ++v) {
@@ -218,11 +313,12 @@ static int verify_one(const void* logits, int dtype, const float* q, const int32
     return ORACLE_OK;
 }
 
-int oracle_verify(const void* logits, int dtype, const float* q, const int32_t* tokens,
-                  const float* uniforms, int64_t B, int K, int64_t V, float temperature,
-                  int32_t* accept_len, int32_t* out_tokens, uint8_t* accept_mask,
-                  int32_t* status, double* row_m, double* row_s, double* p_draft,
-                  double* accept_margin, double* sample_margin, int32_t* sample_alt)
+static int verify_batch(const void* logits, int dtype, const float* q, const int32_t* tokens,
+                        const float* uniforms, int64_t B, int K, int64_t V, float temperature,
+                        int32_t* accept_len, int32_t* out_tokens, uint8_t* accept_mask,
+                        int32_t* status, double* row_m, double* row_s, double* p_draft,
+                        double* accept_margin, double* sample_margin, int32_t* sample_alt,
+                        const trunc_opts* tr, double* trunc_margin)
 {
     if (!logits || !uniforms || !accept_len || !out_tokens || B < 0 || K < 0 || V < 1 ||
         (K > 0 && (!q || !tokens || !accept_mask)) || (dtype != 0 && dtype != 1) ||
@@ -254,13 +350,14 @@ int oracle_verify(const void* logits, int dtype, const float* q, const int32_t* 
                 pd[i] = NAN;
             }
         }
-        double a_mg = INFINITY, s_mg = INFINITY;
+        double a_mg = INFINITY, s_mg = INFINITY, t_mg = INFINITY;
         int32_t s_alt = -1, len = 0;
         int st = verify_one((const char*)logits + (size_t)b * (size_t)(K + 1) * (size_t)V * esz,
                             dtype, K > 0 ? q + (size_t)b * (size_t)K * (size_t)V : 0,
                             K > 0 ? tokens + (size_t)b * (size_t)K : 0,
                             uniforms + (size_t)b * (size_t)(K + 1), K, V, T, p, w, ot,
-                            mk ? mk : mk_dummy, rm, rs, pd, &a_mg, &s_mg, &s_alt, &len);
+                            mk ? mk : mk_dummy, rm, rs, pd, &a_mg, &s_mg, &s_alt, &len, tr,
+                            &t_mg);
         if (st != ORACLE_OK) {
             /* an erroneous sequence reports nothing but its status */
             len = 0;
@@ -280,6 +377,8 @@ int oracle_verify(const void* logits, int dtype, const float* q, const int32_t* 
         accept_len[b] = len;
         if (status)
             status[b] = st;
+        if (trunc_margin)
+            trunc_margin[b] = st == ORACLE_OK ? t_mg : INFINITY;
         if (row_m)
             for (int i = 0; i <= K; ++i)
                 row_m[(size_t)b * (size_t)(K + 1) + (size_t)i] = rm[i];
@@ -298,6 +397,38 @@ int oracle_verify(const void* logits, int dtype, const float* q, const int32_t* 
     }
     free(p); free(w); free(rm); free(rs); free(pd);
     return 0;
+}
+
+int oracle_verify(const void* logits, int dtype, const float* q, const int32_t* tokens,
+                  const float* uniforms, int64_t B, int K, int64_t V, float temperature,
+                  int32_t* accept_len, int32_t* out_tokens, uint8_t* accept_mask,
+                  int32_t* status, double* row_m, double* row_s, double* p_draft,
+                  double* accept_margin, double* sample_margin, int32_t* sample_alt)
+{
+    return verify_batch(logits, dtype, q, tokens, uniforms, B, K, V, temperature, accept_len,
+                        out_tokens, accept_mask, status, row_m, row_s, p_draft, accept_margin,
+                        sample_margin, sample_alt, 0, 0);
+}
+
+/* The verify with the truncated target p~ (truncate_row) in place of p in
+ * every step: the test u*q(x) < p~(x), the residual max(0, p~_j - q_j), the
+ * bonus row p~_K.  Row statistics stay those of the untruncated softmax;
+ * p_draft reports p~(x).  trunc_margin [B] (optional): the smallest distance of
+ * a reached row from a filter boundary (see truncate_row). */
+int oracle_verify_truncated(const void* logits, int dtype, const float* q, const int32_t* tokens,
+                            const float* uniforms, int64_t B, int K, int64_t V,
+                            float temperature, double top_p, double min_p, int32_t* accept_len,
+                            int32_t* out_tokens, uint8_t* accept_mask, int32_t* status,
+                            double* row_m, double* row_s, double* p_draft,
+                            double* accept_margin, double* sample_margin, int32_t* sample_alt,
+                            double* trunc_margin)
+{
+    if (!(top_p > 0.0) || !(min_p < 1.0) || isnan(top_p) || isnan(min_p))
+        return -1;
+    trunc_opts tr = {top_p, min_p};
+    return verify_batch(logits, dtype, q, tokens, uniforms, B, K, V, temperature, accept_len,
+                        out_tokens, accept_mask, status, row_m, row_s, p_draft, accept_margin,
+                        sample_margin, sample_alt, &tr, trunc_margin);
 }
 
 /* Acceptance telemetry ([P1] "Production perspective" and its operational

@@ -79,6 +79,24 @@ int oracle_verify(const void* logits, int dtype, const float* q, const int32_t* 
                   int32_t* status, double* row_m, double* row_s, double* p_draft,
                   double* accept_margin, double* sample_margin, int32_t* sample_alt);
 
+/* Verification against the truncated target ([P2] "Two things that follow
+ * from the math": production settings temperature 0.6, top-p 0.95, min-p
+ * 0.05).  p~ keeps token v when p_v >= min_p * max p (min-p) and the mass of
+ * the tokens strictly more probable than v is below top_p (top-p, ties at the
+ * boundary kept), both on the untruncated p; p~ is p on the kept tokens over
+ * their sum and replaces p in the test, the residual and the bonus draw.
+ * top_p >= 1 / min_p <= 0 switch a filter off; top_p must be > 0, min_p < 1.
+ * Outputs as oracle_verify (p_draft = p~(x)); trunc_margin [B] (optional) is
+ * the smallest distance of a reached row from a filter boundary:
+ * |log(p_v/p_max) - log(min_p)| and |mass above v - top_p| over its tokens. */
+int oracle_verify_truncated(const void* logits, int dtype, const float* q, const int32_t* tokens,
+                            const float* uniforms, int64_t B, int K, int64_t V,
+                            float temperature, double top_p, double min_p, int32_t* accept_len,
+                            int32_t* out_tokens, uint8_t* accept_mask, int32_t* status,
+                            double* row_m, double* row_s, double* p_draft,
+                            double* accept_margin, double* sample_margin, int32_t* sample_alt,
+                            double* trunc_margin);
+
 /* Ragged batch: sequence b owns packed target rows [off[b], off[b+1]) of R,
  * K_b = off[b+1] - off[b] - 1 <= K_max; its draft rows, tokens, mask and
  * p_draft start at off[b] - b, its uniforms, out_tokens and row stats at
