@@ -182,6 +182,38 @@ int spec_verify_run_ragged(sv_ctx* ctx,
                            int32_t* accept_len, int32_t* out_tokens, uint8_t* accept_mask,
                            float* row_stats, float* p_draft, int32_t* status, void* stream);
 
+/* Verification against a truncated target ([P2] "Two things that follow from
+ * the math" names the production settings temperature 0.6, top-p 0.95, min-p
+ * 0.05).  The target distribution of every row becomes p~: token v is kept
+ * when p_v >= min_p * max p (min-p) and when the mass of the tokens strictly
+ * more probable than v is below top_p (top-p; every token tied at the
+ * boundary is kept); both filters look at the untruncated p = softmax(l/T),
+ * and p~ is p on the kept tokens divided by their sum.  p~ replaces p in the
+ * test (u*q(x) < p~(x)), the residual max(0, p~_j - q_j) and the bonus draw.
+ * top_p >= 1 turns top-p off, min_p <= 0 turns min-p off (both off: the same
+ * outputs as spec_verify_run up to rounding).
+ *
+ * Arguments, layouts and errors as spec_verify_run; row_stats are those of the
+ * untruncated softmax of the rows read, p_draft = p~(x_i).  Requires
+ * 0 < top_p and min_p < 1 (SV_ERR_INVALID_ARG otherwise).  The kernel reads
+ * each row it reaches two (bf16) to four (f32) more times from L2 for the
+ * top-p cut; clusters have at most 8 CTAs. */
+int spec_verify_run_truncated(sv_ctx* ctx,
+                              const void* target_logits, int logits_dtype,
+                              const float* q, const int32_t* draft_tokens, const float* uniforms,
+                              int B, int K, int64_t V, float temperature,
+                              double top_p, double min_p,
+                              int32_t* accept_len, int32_t* out_tokens, uint8_t* accept_mask,
+                              float* row_stats, float* p_draft, int32_t* status, void* stream);
+
+/* The truncated-target kernel's launch plan on the context's device. */
+int spec_verify_get_plan_truncated(sv_ctx* ctx, int B, int K, int64_t V, int logits_dtype,
+                                   sv_plan* out);
+
+/* Its planner as a pure host function (no CUDA call), for tests. */
+int spec_verify_plan_truncated_for(int num_sms, int max_cluster, int B, int K, int64_t V,
+                                   int logits_dtype, int ovr_cluster, sv_plan* out);
+
 /* Greedy verification: the verify of spec_verify_run in the limit T -> 0
  * ([P1] "Speculative decoding: draft first, then verify": as T falls, the
  * softmax of logits/T puts all its mass on the largest logit).  Row i becomes

@@ -80,6 +80,19 @@ def library() -> ctypes.CDLL:
                                                     ctypes.c_int, ctypes.c_int, ctypes.c_int64,
                                                     ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                     ctypes.c_int, ctypes.POINTER(sv_plan)]),
+            "spec_verify_run_truncated": (ctypes.c_int, [P, P, ctypes.c_int, P, P, P,
+                                                         ctypes.c_int, ctypes.c_int,
+                                                         ctypes.c_int64, ctypes.c_float,
+                                                         ctypes.c_double, ctypes.c_double, P, P, P,
+                                                         P, P, P, P]),
+            "spec_verify_get_plan_truncated": (ctypes.c_int, [P, ctypes.c_int, ctypes.c_int,
+                                                              ctypes.c_int64, ctypes.c_int,
+                                                              ctypes.POINTER(sv_plan)]),
+            "spec_verify_plan_truncated_for": (ctypes.c_int, [ctypes.c_int, ctypes.c_int,
+                                                              ctypes.c_int, ctypes.c_int,
+                                                              ctypes.c_int64, ctypes.c_int,
+                                                              ctypes.c_int,
+                                                              ctypes.POINTER(sv_plan)]),
             "spec_verify_run_ragged": (ctypes.c_int, [P, P, ctypes.c_int, P, P, P, P,
                                                       ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                                       ctypes.c_int64, ctypes.c_float, P, P, P, P,
@@ -156,6 +169,32 @@ def spec_verify_run_noalloc(device, logits_ptr, dtype, q_ptr, tokens_ptr, unifor
                                              uniforms_ptr, B, K, V, float(T), accept_len_ptr,
                                              out_tokens_ptr, accept_mask_ptr, row_stats_ptr,
                                              p_draft_ptr, status_ptr, stream)
+
+
+def spec_verify_run_truncated(ctx, logits_ptr, dtype, q_ptr, tokens_ptr, uniforms_ptr, B, K, V,
+                              T, top_p, min_p, accept_len_ptr, out_tokens_ptr, accept_mask_ptr,
+                              row_stats_ptr=None, p_draft_ptr=None, status_ptr=None,
+                              stream=None) -> int:
+    return library().spec_verify_run_truncated(ctx, logits_ptr, dtype, q_ptr, tokens_ptr,
+                                               uniforms_ptr, B, K, V, float(T), float(top_p),
+                                               float(min_p), accept_len_ptr, out_tokens_ptr,
+                                               accept_mask_ptr, row_stats_ptr, p_draft_ptr,
+                                               status_ptr, stream)
+
+
+def spec_verify_get_plan_truncated(ctx, B, K, V, dtype) -> dict:
+    plan = sv_plan()
+    rc = library().spec_verify_get_plan_truncated(ctx, B, K, V, dtype, ctypes.byref(plan))
+    if rc != SV_OK:
+        raise SpecVerifyError(rc, "spec_verify_get_plan_truncated")
+    return plan.as_dict()
+
+
+def spec_verify_plan_truncated_for(num_sms, max_cluster, B, K, V, dtype, ovr_cluster=0):
+    plan = sv_plan()
+    rc = library().spec_verify_plan_truncated_for(num_sms, max_cluster, B, K, V, dtype,
+                                                  ovr_cluster, ctypes.byref(plan))
+    return rc, plan.as_dict()
 
 
 def spec_verify_run_ragged(ctx, logits_ptr, dtype, q_ptr, tokens_ptr, uniforms_ptr, offsets_ptr,
@@ -409,6 +448,45 @@ class Verifier:
         if rc != SV_OK:
             raise SpecVerifyError(rc, "spec_verify_run_ragged")
         return out
+
+    def run_truncated(self, logits, q, tokens, uniforms, temperature: float, top_p: float,
+                      min_p: float, out: Optional[dict] = None, stats: bool = False,
+                      status: bool = True, stream=None) -> dict:
+        """run() against the truncated target (top-p, min-p)."""
+        import torch
+        B, K1, V = logits.shape
+        K = K1 - 1
+        dev = logits.device
+        if out is None:
+            out = {
+                "accept_len": torch.empty(B, dtype=torch.int32, device=dev),
+                "out_tokens": torch.empty(B, K + 1, dtype=torch.int32, device=dev),
+                "accept_mask": torch.empty(B, max(K, 1), dtype=torch.uint8, device=dev)[:, :K],
+            }
+            if stats:
+                out["row_stats"] = torch.empty(B, K + 1, 2, dtype=torch.float32, device=dev)
+                out["p_draft"] = torch.empty(B, max(K, 1), dtype=torch.float32, device=dev)[:, :K]
+            if status:
+                out["status"] = torch.empty(B, dtype=torch.int32, device=dev)
+        s = stream if stream is not None else torch.cuda.current_stream(dev).cuda_stream
+
+        def ptr(name):
+            t = out.get(name)
+            return None if t is None else t.data_ptr()
+
+        rc = spec_verify_run_truncated(self.ctx, logits.data_ptr(), _dtype_code(logits),
+                                       q.data_ptr() if K else None,
+                                       tokens.data_ptr() if K else None, uniforms.data_ptr(), B,
+                                       K, V, temperature, top_p, min_p, ptr("accept_len"),
+                                       ptr("out_tokens"), ptr("accept_mask") if K else None,
+                                       ptr("row_stats"), ptr("p_draft") if K else None,
+                                       ptr("status"), s)
+        if rc != SV_OK:
+            raise SpecVerifyError(rc, "spec_verify_run_truncated")
+        return out
+
+    def plan_truncated(self, B, K, V, dtype=SV_BF16) -> dict:
+        return spec_verify_get_plan_truncated(self.ctx, B, K, V, dtype)
 
     def plan_greedy(self, B, K, V, dtype=SV_BF16) -> dict:
         return spec_verify_get_plan_greedy(self.ctx, B, K, V, dtype)

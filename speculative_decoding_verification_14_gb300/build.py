@@ -1,4 +1,4 @@
-"""Builds libspecverify.so in-tree for sm_103a (nvcc + g++, four translation
+"""Builds libspecverify.so in-tree for sm_103a (nvcc + g++, five translation
 units compiled in parallel, no cmake).  Run as ``python -m
 speculative_decoding_verification_14_gb300.build`` or through ``build()``."""
 from __future__ import annotations
@@ -15,7 +15,7 @@ OUT = os.path.join(PKG, "libspecverify.so")
 BUILD_DIR = os.path.join(PKG, "_build")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-CUDA_SOURCES = ("spec_verify.cu", "greedy.cu")
+CUDA_SOURCES = ("spec_verify.cu", "greedy.cu", "truncated.cu")
 HOST_SOURCES = ("planner.cpp", "adapt.cpp")
 SOURCES = [os.path.join(CSRC, f) for f in (*CUDA_SOURCES, "sv_internal.h", *HOST_SOURCES)] + [
     os.path.join(INCLUDE, "spec_verify.h")]

@@ -300,7 +300,8 @@ __global__ void __launch_bounds__(kNT, 8) sv_greedy_kernel(const __grid_constant
             push_v4(&part[par][rank * kNW + warp], &xbar[par], (uint32_t)lane,
                     make_float4(best, __int_as_float(bidx), bad ? 1.f : 0.f, 0.f));
         // every warp merges the P partials itself and reaches the same decision
-        if (!mbar_wait_limited(&xbar[par], phase, a.wait_ns)) {
+        // (one outcome for the whole warp, even when the wait runs out)
+        if (!__all_sync(kFull, mbar_wait_limited(&xbar[par], phase, a.wait_ns))) {
             state = SV_ERR_TIMEOUT;
             break;
         }

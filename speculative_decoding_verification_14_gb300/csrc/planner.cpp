@@ -115,22 +115,27 @@ extern "C" int spec_verify_plan_for(int num_sms, int smem_per_cta, int max_clust
 // CTAs per SM).  Each lane keeps eight 16-byte loads in flight; a batch that
 // fills the GPU gets at least two such rounds per warp and row, a smaller
 // batch the largest cluster that leaves every lane one vector.
-extern "C" int spec_verify_plan_greedy_for(int num_sms, int max_cluster, int B, int K, int64_t V,
-                                           int logits_dtype, int ovr_cluster, sv_plan* out) {
+namespace {
+
+// Cluster-per-sequence plan for the kernels without a shared-memory ring
+// (greedy and truncated-target verification): ctas_per_sm resident 128-thread
+// CTAs per SM, `depth` 16-byte loads in flight per lane, clusters up to cap.
+int plan_rows(int num_sms, int max_cluster, int B, int K, int64_t V, int logits_dtype,
+              int ovr_cluster, int ctas_per_sm, int depth, int cap, sv_plan* out) {
     using namespace sv;
     if (!out || num_sms < 1 || max_cluster < 1 || B < 1 || K < 0 || K > kMaxK || V < 1 ||
         V > ((int64_t)1 << 31) || (logits_dtype != SV_F32 && logits_dtype != SV_BF16) ||
-        ovr_cluster < 0 || ovr_cluster > kMaxCluster)
+        ovr_cluster < 0 || ovr_cluster > cap)
         return SV_ERR_INVALID_ARG;
     if (ovr_cluster > max_cluster)
         return SV_ERR_UNSUPPORTED;
     const int es = logits_dtype == SV_BF16 ? 2 : 4;
     const int64_t E = 16 / es;
     const int nw = 4;
-    const int64_t capacity = (int64_t)kGreedyCtasPerSM * num_sms;
-    const int64_t min_full = (int64_t)nw * 32 * kGreedyDepth * E * 2;
+    const int64_t capacity = (int64_t)ctas_per_sm * num_sms;
+    const int64_t min_full = (int64_t)nw * 32 * depth * E * 2;
     const int64_t min_small = (int64_t)nw * 32 * E;
-    const int cmax = max_cluster < kMaxCluster ? max_cluster : kMaxCluster;
+    const int cmax = max_cluster < cap ? max_cluster : cap;
     int C = 1;
     if (ovr_cluster) {
         C = ovr_cluster;
@@ -153,4 +158,22 @@ extern "C" int spec_verify_plan_greedy_for(int num_sms, int max_cluster, int B, 
     out->bulk_copy = ((V * es) % 16) == 0 ? 1 : 0;
     out->prefetch_next = 0;
     return SV_OK;
+}
+
+}  // namespace
+
+extern "C" int spec_verify_plan_greedy_for(int num_sms, int max_cluster, int B, int K, int64_t V,
+                                           int logits_dtype, int ovr_cluster, sv_plan* out) {
+    return plan_rows(num_sms, max_cluster, B, K, V, logits_dtype, ovr_cluster,
+                     sv::kGreedyCtasPerSM, sv::kGreedyDepth, sv::kMaxCluster, out);
+}
+
+// Truncated-target verification: the same mapping with four resident CTAs
+// per SM (its shared histograms), four loads in flight per lane, and
+// clusters of at most eight CTAs.
+extern "C" int spec_verify_plan_truncated_for(int num_sms, int max_cluster, int B, int K,
+                                              int64_t V, int logits_dtype, int ovr_cluster,
+                                              sv_plan* out) {
+    return plan_rows(num_sms, max_cluster, B, K, V, logits_dtype, ovr_cluster,
+                     sv::kTruncCtasPerSM, 4, sv::kTruncMaxCluster, out);
 }

@@ -1928,6 +1928,7 @@ int spec_verify_init(sv_ctx** out, int device, int max_B, int max_K, int64_t max
     ctx->max_cluster = max_cluster;
     // the greedy kernel may use 16-CTA clusters only where the main kernel may
     ctx->greedy_max_cluster = (max_cluster >= 16 && sv::greedy_set_attributes() == 0) ? 16 : 8;
+    (void)sv::trunc_set_attributes();  // clusters of at most 8 CTAs: portable either way
     ctx->ovr_cluster = env_int("SV_CLUSTER", 0);
     ctx->ovr_group = env_int("SV_GROUP", 0);
     ctx->ovr_threads = env_int("SV_THREADS", 0);
@@ -1989,6 +1990,67 @@ int spec_verify_run_ragged(sv_ctx* ctx, const void* target_logits, int logits_dt
     return launch(ctx, target_logits, logits_dtype, q, draft_tokens, uniforms, B, K_max, V,
                   temperature, accept_len, out_tokens, accept_mask, row_stats, p_draft, status,
                   static_cast<cudaStream_t>(stream), row_offsets, total_rows);
+}
+
+int spec_verify_get_plan_truncated(sv_ctx* ctx, int B, int K, int64_t V, int logits_dtype,
+                                   sv_plan* out) {
+    if (!ctx)
+        return SV_ERR_INVALID_ARG;
+    const int ovr = ctx->ovr_cluster > sv::kTruncMaxCluster ? sv::kTruncMaxCluster
+                                                            : ctx->ovr_cluster;
+    return spec_verify_plan_truncated_for(ctx->num_sms, ctx->max_cluster, B, K, V, logits_dtype,
+                                          ovr, out);
+}
+
+int spec_verify_run_truncated(sv_ctx* ctx, const void* target_logits, int logits_dtype,
+                              const float* q, const int32_t* draft_tokens, const float* uniforms,
+                              int B, int K, int64_t V, float temperature, double top_p,
+                              double min_p, int32_t* accept_len, int32_t* out_tokens,
+                              uint8_t* accept_mask, float* row_stats, float* p_draft,
+                              int32_t* status, void* stream) {
+    const int rc = validate(ctx, target_logits, logits_dtype, q, draft_tokens, uniforms, B, K, V,
+                            temperature, accept_len, out_tokens, accept_mask, row_stats, p_draft,
+                            status);
+    if (rc != SV_OK)
+        return rc;
+    if (!(top_p > 0.0) || !(min_p < 1.0) || std::isnan(top_p) || std::isnan(min_p))
+        return SV_ERR_INVALID_ARG;
+    if (ctx->al_hist && K + 2 > ctx->al_bins)
+        return SV_ERR_INVALID_ARG;
+    sv_plan plan;
+    const int prc = spec_verify_get_plan_truncated(ctx, B, K, V, logits_dtype, &plan);
+    if (prc != SV_OK)
+        return prc;
+    const int es = logits_dtype == SV_BF16 ? 2 : 4;
+    sv::TruncLaunch g;
+    std::memset(&g, 0, sizeof g);
+    g.logits = target_logits;
+    g.q = q;
+    g.tokens = draft_tokens;
+    g.u = uniforms;
+    g.accept_len = accept_len;
+    g.out_tokens = out_tokens;
+    g.accept_mask = accept_mask;
+    g.row_stats = row_stats;
+    g.p_draft = p_draft;
+    g.status = status;
+    g.err_word = ctx->d_err;
+    g.al_hist = ctx->al_hist;
+    g.V = V;
+    g.slice = plan.slice;
+    g.B = B;
+    g.K = K;
+    g.C = plan.cluster;
+    g.es = es;
+    g.vec = plan.bulk_copy && aligned(target_logits, 16) ? 1 : 0;
+    g.c = (float)(1.4426950408889634074 / (double)temperature);
+    g.T = temperature;
+    // min-p keeps l - l_max >= T ln(min_p); ln(min_p) = -inf for min_p <= 0 (off)
+    g.dmin = min_p > 0.0 ? (float)((double)temperature * std::log(min_p)) : -INFINITY;
+    g.top_p = top_p;
+    g.wait_ns = ctx->wait_ns;
+    DeviceGuard guard(ctx->device);
+    return sv::trunc_launch(g, stream) == 0 ? SV_OK : SV_ERR_CUDA;
 }
 
 int spec_verify_get_plan_greedy(sv_ctx* ctx, int B, int K, int64_t V, int logits_dtype,

@@ -21,6 +21,8 @@ constexpr int kThreadsPerSM = 896;      // resident threads the kernels' launch 
 
 constexpr int kGreedyDepth = 8;         // greedy kernel: 16-byte loads in flight per lane
 constexpr int kGreedyCtasPerSM = 8;     // greedy kernel: resident 128-thread CTAs per SM (launch bounds)
+constexpr int kTruncCtasPerSM = 4;      // truncated-target kernel: resident CTAs per SM (launch bounds)
+constexpr int kTruncMaxCluster = 8;     // truncated-target kernel: largest cluster (shared histograms)
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
@@ -72,5 +74,29 @@ struct GreedyLaunch {
 };
 int greedy_set_attributes();                              // 0 on success
 int greedy_launch(const GreedyLaunch& g, void* stream);  // 0 on success
+
+// Truncated-target verification kernel (truncated.cu).
+struct TruncLaunch {
+    const void* logits;
+    const float* q;
+    const int32_t* tokens;
+    const float* u;
+    int32_t* accept_len;
+    int32_t* out_tokens;
+    uint8_t* accept_mask;
+    float* row_stats;
+    float* p_draft;
+    int32_t* status;
+    uint32_t* err_word;
+    uint32_t* al_hist;
+    int64_t V, slice;
+    int B, K, C;
+    int es, vec;
+    float c, T, dmin;
+    double top_p;
+    unsigned long long wait_ns;
+};
+int trunc_set_attributes();                               // 0 on success
+int trunc_launch(const TruncLaunch& g, void* stream);    // 0 on success
 
 }  // namespace sv

@@ -1,0 +1,790 @@
+// truncated.cu -- verification against a truncated target distribution
+// (top-p and min-p) for sm_103a.
+//
+// [P2] names the production sampler settings of its engine: temperature 0.6,
+// top-p 0.95, min-p 0.05.  With such a sampler the target distribution of the
+// verify step is p~ instead of p = softmax(l/T):
+//   min-p keeps token v when p_v >= min_p * max p;
+//   top-p keeps v when the mass of the tokens strictly more probable than v is
+//         below top_p (every token tied at the boundary is kept);
+//   p~ = p on the kept tokens, divided by their sum.
+// Both filters look at the untruncated p, so their order does not matter.
+// p~ then replaces p in every step of [P1]'s loop: the test u*q(x) < p~(x),
+// the residual max(0, p~_j - q_j) and the bonus draw from p~_K.
+//
+// [P1] reactapp.top, "Speculative decoding and early exit: speeding up
+//      autoregressive decode", section "Speculative decoding: draft first,
+//      then verify".
+// [P2] trefon.com, "Decode is memory-bound: a ~59 tok/s ceiling on an RTX
+//      4090 and how speculative decoding breaks it", section "Two things that
+//      follow from the math".
+//
+// Design: one cluster of C CTAs per sequence, vocabulary slices per CTA and
+// stretches per warp, rows in order with the early stop.  Per row:
+//  A. one pass for the row maximum l_max and S = sum 2^((l - l_max) c)
+//     (c = log2(e)/T), pushed as warp partials to every CTA (st.async on an
+//     mbarrier) and merged by every warp;
+//  B. the top-p cut by radix selection over an order-preserving key of the
+//     stored logits (two 8-bit levels for bf16, four for f32): each level is
+//     one pass that bins the weights of the candidate tokens (min-p survivors
+//     whose key matches the prefix chosen so far) into 256 shared-memory
+//     bins, the CTA histograms are pushed to every CTA, and every warp finds
+//     the digit where the mass above crosses top_p * S;
+//  C. the test on x_i with p~(x_i) * E = 2^((l_x - l_max) c) for a kept x_i,
+//     E the kept mass;
+//  D. for the corrected or bonus token: a pass for per-warp weight totals,
+//     pushed to every CTA; the warp that holds the crossing point walks its
+//     stretch again to find the token and writes the outputs.
+// Threshold decisions are taken on the stored logits: min-p as
+// l - l_max >= T ln(min_p), top-p on the key, so the kept set depends on the
+// weights only through the top-p masses.
+#include <cuda_runtime.h>
+#include <cooperative_groups.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/spec_verify.h"
+#include "sv_internal.h"
+
+namespace cg = cooperative_groups;
+
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kNT = 128;
+constexpr int kNW = kNT / 32;
+constexpr int kMaxC = sv::kTruncMaxCluster;
+constexpr int kBins = 256;
+
+struct TArgs {
+    const void* logits;
+    const float* q;
+    const int32_t* tokens;
+    const float* u;
+    int32_t* accept_len;
+    int32_t* out_tokens;
+    uint8_t* accept_mask;
+    float* row_stats;
+    float* p_draft;
+    int32_t* status;
+    uint32_t* err_word;
+    uint32_t* al_hist;
+    int64_t V, slice;
+    int B, K, C, vec;
+    float c;         // log2(e) / T, rounded to float
+    float T;
+    float dmin;      // T * ln(min_p): min-p keeps l - l_max >= dmin (-inf: off)
+    double top_p;    // >= 1: top-p off
+    unsigned long long wait_ns;
+};
+
+// ------------------------------------------------------------------ PTX -----
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(unsigned long long* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect(unsigned long long* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(unsigned long long* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long now_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Phase `parity` of `bar`, polled with a growing sleep; false after limit_ns.
+__device__ __noinline__ bool mbar_wait_limited(unsigned long long* bar, uint32_t parity,
+                                               unsigned long long limit_ns) {
+    if (mbar_try(bar, parity))
+        return true;
+    const unsigned long long t0 = now_ns();
+    unsigned sleep = 32;
+    for (uint32_t it = 0; it < (1u << 26); ++it) {
+        __nanosleep(sleep);
+        if (mbar_try(bar, parity))
+            return true;
+        if (sleep < 256)
+            sleep <<= 1;
+        if ((it & 15u) == 15u && now_ns() - t0 > limit_ns)
+            return false;
+    }
+    return false;
+}
+
+// 16 bytes into the same slot of cluster CTA `rank`, counted on its `bar`.
+__device__ __forceinline__ void push_v4(const void* slot, const void* bar, uint32_t rank, float4 v) {
+    uint32_t d, m;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(smem_addr(slot)), "r"(rank));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(m) : "r"(smem_addr(bar)), "r"(rank));
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(d),
+        "r"(__float_as_uint(v.x)), "r"(__float_as_uint(v.y)), "r"(__float_as_uint(v.z)),
+        "r"(__float_as_uint(v.w)), "r"(m)
+        : "memory");
+}
+
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// ------------------------------------------------------------- elements -----
+
+// Entry e of a 16-byte vector of ES-byte logits, widened exactly to float.
+template <int ES>
+__device__ __forceinline__ float vec_entry(const uint4& v, int e) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    if constexpr (ES == 4) {
+        return __uint_as_float(w[e]);
+    } else {
+        const uint32_t x = w[e >> 1];
+        return __uint_as_float((e & 1) ? (x & 0xffff0000u) : (x << 16));
+    }
+}
+
+// Order-preserving key of a stored logit (larger logit, larger key).
+template <int ES>
+__device__ __forceinline__ uint32_t key_of(float l) {
+    uint32_t b = __float_as_uint(l);
+    if constexpr (ES == 2)
+        b >>= 16;
+    constexpr uint32_t sign = ES == 2 ? 0x8000u : 0x80000000u;
+    constexpr uint32_t all = ES == 2 ? 0xffffu : 0xffffffffu;
+    return (b & sign) ? (b ^ all) : (b | sign);
+}
+
+__device__ __forceinline__ float load_entry(const void* base, int es, int64_t idx) {
+    if (es == 4)
+        return __ldg(static_cast<const float*>(base) + idx);
+    const uint16_t h = __ldg(static_cast<const unsigned short*>(base) + idx);
+    return __uint_as_float((uint32_t)h << 16);
+}
+
+// Kahan-style compensated accumulation (sum, compensation).
+__device__ __forceinline__ void acc_add(float& s, float& comp, float x) {
+    const float y = x - comp;
+    const float t = s + y;
+    comp = (t - s) - y;
+    s = t;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1)
+        v += __shfl_xor_sync(kFull, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1)
+        v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
+    return v;
+}
+
+}  // namespace
+
+namespace {
+
+constexpr int kDepth = 4;  // 16-byte loads in flight per lane
+
+// Calls fn(l, e) for every entry of this warp's stretch of one row (e = entry
+// index within the CTA's slice), lane by lane; entries of one lane come in
+// increasing order, the lanes interleave by vector.
+template <int ES, typename F>
+__device__ __forceinline__ void visit(const TArgs& a, int64_t row_elem, int64_t w0, int64_t w1,
+                                      int lane, F&& fn) {
+    constexpr int E = 16 / ES;
+    if (a.vec) {
+        const uint4* rp = reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(a.logits) +
+                                                         row_elem * ES);
+        for (int64_t base = w0; base < w1; base += 32 * kDepth) {
+            uint4 r[kDepth];
+#pragma unroll
+            for (int k = 0; k < kDepth; ++k) {
+                const int64_t idx = base + k * 32 + lane;
+                if (idx < w1)
+                    r[k] = ld_stream(rp + idx);
+            }
+#pragma unroll
+            for (int k = 0; k < kDepth; ++k) {
+                const int64_t idx = base + k * 32 + lane;
+                if (idx < w1) {
+#pragma unroll
+                    for (int t = 0; t < E; ++t)
+                        fn(vec_entry<ES>(r[k], t), idx * E + t);
+                }
+            }
+        }
+    } else {
+        for (int64_t e = w0 + lane; e < w1; e += 32)
+            fn(load_entry(a.logits, ES, row_elem + e), e);
+    }
+}
+
+template <int ES>
+__global__ void __launch_bounds__(kNT, sv::kTruncCtasPerSM) sv_trunc_kernel(const __grid_constant__ TArgs a) {
+    constexpr int E = 16 / ES;
+    constexpr int KEYBITS = 8 * ES;
+    constexpr int LEVELS = KEYBITS / 8;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = (int)cluster.block_rank();
+    const int b = (int)(blockIdx.x / (unsigned)a.C);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int K = a.K, C = a.C;
+    const int P = C * kNW;
+    const int64_t V = a.V;
+    const float c = a.c;
+    const bool use_min = a.dmin > -INFINITY;
+    const bool use_top = a.top_p < 1.0;
+
+    __shared__ __align__(16) float4 part[2][kMaxC * kNW];       // warp partials, by use parity
+    __shared__ __align__(16) double hrecv[2][kMaxC][kBins];     // CTA histograms, by use parity
+    __shared__ __align__(16) double hloc[kBins];                // this CTA's histogram
+    __shared__ __align__(8) unsigned long long xbar[2], hbar[2];
+    __shared__ int xs[sv::kMaxK];
+    __shared__ float us[sv::kMaxRows];
+    __shared__ float rsm[sv::kMaxRows], rss[sv::kMaxRows], pdr[sv::kMaxK];
+
+    const int64_t v0 = (int64_t)rank * a.slice;
+    const int64_t L = v0 < V ? (V - v0 < a.slice ? V - v0 : a.slice) : 0;
+    const int64_t row0 = (int64_t)b * (K + 1);
+    const int64_t units = a.vec ? L / E : L;
+    const int64_t per_w = (units + kNW - 1) / kNW;
+    const int64_t w0 = per_w * warp < units ? per_w * warp : units;
+    const int64_t w1 = w0 + per_w < units ? w0 + per_w : units;
+
+    if (tid == 0) {
+        mbar_init(&xbar[0], 1);
+        mbar_init(&xbar[1], 1);
+        mbar_init(&hbar[0], 1);
+        mbar_init(&hbar[1], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (tid < K)
+        xs[tid] = a.tokens[(int64_t)b * K + tid];
+    if (tid <= K)
+        us[tid] = a.u[row0 + tid];
+    __syncthreads();
+    cluster_arrive();
+    bool ready = false;
+    int state = SV_OK;
+    {
+        const bool bad_x = __any_sync(kFull, lane < K && (xs[lane] < 0 || (int64_t)xs[lane] >= V));
+        const float ul = lane <= K ? us[lane] : 0.5f;
+        const float uh = (lane == 0 && K == sv::kMaxK) ? us[sv::kMaxK] : 0.5f;
+        const bool bad_u = __any_sync(kFull, !(ul >= 0.f && ul < 1.f) || !(uh >= 0.f && uh < 1.f));
+        if (bad_x)
+            state = SV_ERR_TOKEN_RANGE;
+        else if (bad_u)
+            state = SV_ERR_UNIFORM_RANGE;
+    }
+
+    uint32_t xcnt = 0, hcnt = 0;  // exchanges so far (slot = cnt & 1, phase = (cnt >> 1) & 1)
+    // Every warp pushes one float4 to slot (rank, warp) of every CTA and gets
+    // back all P of them in part[slot]; false if they did not come in time.
+    auto exchange = [&](float4 v) -> int {
+        const int s = (int)(xcnt & 1u);
+        const uint32_t ph = (xcnt >> 1) & 1u;
+        ++xcnt;
+        if (!ready) {
+            cluster_wait();
+            ready = true;
+        }
+        if (tid == 0)
+            mbar_expect(&xbar[s], (uint32_t)(P * 16));
+        if (lane < C)
+            push_v4(&part[s][rank * kNW + warp], &xbar[s], (uint32_t)lane, v);
+        // (every thread of the CTA takes the same outcome, so control flow
+        // stays uniform even when a wait runs out)
+        const int ok = __syncthreads_and(mbar_wait_limited(&xbar[s], ph, a.wait_ns) ? 1 : 0);
+        return ok ? s : -1;
+    };
+    // The CTA histogram hloc goes to slot (rank) of every CTA; every warp then
+    // sees all C of them in hrecv[slot].
+    auto exchange_hist = [&]() -> int {
+        const int s = (int)(hcnt & 1u);
+        const uint32_t ph = (hcnt >> 1) & 1u;
+        ++hcnt;
+        if (!ready) {
+            cluster_wait();
+            ready = true;
+        }
+        __syncthreads();  // hloc complete
+        if (tid == 0)
+            mbar_expect(&hbar[s], (uint32_t)(C * kBins * 8));
+        for (int idx = tid; idx < C * (kBins / 2); idx += kNT) {
+            const int d = idx / (kBins / 2), k = idx % (kBins / 2);
+            push_v4(&hrecv[s][rank][k * 2], &hbar[s], (uint32_t)d,
+                    reinterpret_cast<const float4*>(hloc)[k]);
+        }
+        // (one outcome for the whole CTA; also: hloc is read by everyone
+        // before it is cleared again)
+        const int ok = __syncthreads_and(mbar_wait_limited(&hbar[s], ph, a.wait_ns) ? 1 : 0);
+        return ok ? s : -1;
+    };
+
+    int j = -1;
+    float lmax = 0.f, E_kept = 0.f;       // the decided row's statistics
+    uint32_t key_t = 0;                   // top-p: kept keys are >= key_t
+    for (int i = 0; i <= K && state == SV_OK; ++i) {
+        const int64_t re = (row0 + i) * V + v0;  // first element of this CTA's slice of row i
+        // ---- A: row maximum and S = sum 2^((l - l_max) c) ----
+        float mx = -INFINITY, sm = 0.f, sc = 0.f;
+        bool bad = false;
+        visit<ES>(a, re, w0, w1, lane, [&](float l, int64_t) {
+            if (l != l || l == INFINITY) {
+                bad = true;
+                return;
+            }
+            if (l == -INFINITY)  // weight 0
+                return;
+            if (l > mx) {
+                sm = sm * ex2((mx - l) * c);
+                sc = sc * ex2((mx - l) * c);
+                mx = l;
+            }
+            acc_add(sm, sc, ex2((l - mx) * c));
+        });
+        const float wmx = warp_max(mx);
+        float wsm = (mx > -INFINITY) ? (sm - sc) * ex2((mx - wmx) * c) : 0.f;
+        wsm = warp_sum(wsm);
+        const int s1 = exchange(make_float4(wmx, wsm, __any_sync(kFull, bad) ? 1.f : 0.f, 0.f));
+        if (s1 < 0) {
+            state = SV_ERR_TIMEOUT;
+            break;
+        }
+        {
+            float m = -INFINITY, bd = 0.f;
+            for (int p = lane; p < P; p += 32) {
+                m = fmaxf(m, part[s1][p].x);
+                bd = fmaxf(bd, part[s1][p].z);
+            }
+            m = warp_max(m);
+            float S = 0.f, Sc = 0.f;
+            for (int p = 0; p < P; ++p) {  // fixed order: the same S in every warp
+                const float4 q4 = part[s1][p];
+                if (q4.x > -INFINITY)
+                    acc_add(S, Sc, q4.y * ex2((q4.x - m) * c));
+            }
+            S -= Sc;
+            if (__any_sync(kFull, bd != 0.f) || !(m > -INFINITY)) {
+                state = SV_ERR_NONFINITE;
+                break;
+            }
+            lmax = m;
+            E_kept = S;
+            if (lane == 0 && warp == 0) {
+                rsm[i] = __fdiv_rn(m, a.T);
+                rss[i] = S;
+            }
+        }
+        const float S_all = E_kept;
+        key_t = 0;
+        // ---- B: the kept set ----
+        if (use_min || use_top) {
+            const double thr = a.top_p * (double)S_all;
+            uint32_t prefix = 0;
+            double above = 0.0;  // mass of candidates with keys above the prefix group
+            for (int lev = 0; lev < LEVELS; ++lev) {
+                for (int k = tid; k < kBins; k += kNT)
+                    hloc[k] = 0.0;
+                __syncthreads();
+                const int sh_hi = KEYBITS - 8 * lev;   // prefix = key >> sh_hi
+                const int sh_lo = KEYBITS - 8 * (lev + 1);
+                visit<ES>(a, re, w0, w1, lane, [&](float l, int64_t) {
+                    if (use_min && !(l - lmax >= a.dmin))
+                        return;
+                    const uint32_t key = key_of<ES>(l);
+                    if (lev > 0 && (key >> sh_hi) != prefix)
+                        return;
+                    atomicAdd(&hloc[(key >> sh_lo) & 0xffu], (double)ex2((l - lmax) * c));
+                });
+                const int s2 = exchange_hist();
+                if (s2 < 0) {
+                    state = SV_ERR_TIMEOUT;
+                    break;
+                }
+                // lane l holds bins 8l .. 8l+7, summed over the CTAs in a fixed order
+                double bin[8];
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    double acc = 0.0;
+                    for (int r = 0; r < C; ++r)
+                        acc += hrecv[s2][r][lane * 8 + t];
+                    bin[t] = acc;
+                }
+                double lt = 0.0;
+#pragma unroll
+                for (int t = 0; t < 8; ++t)
+                    lt += bin[t];
+                // mass of the bins of this and higher lanes (suffix sum over lanes)
+                double incl = lt;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const double v = __shfl_down_sync(kFull, incl, o);
+                    if (lane + o < 32)
+                        incl += v;
+                }
+                const double above_lane = incl - lt;
+                const double total = __shfl_sync(kFull, incl, 0);
+                if (lev == 0 && (!use_top || total < thr)) {
+                    // min-p alone, or candidates holding less than top_p: all kept
+                    E_kept = (float)total;
+                    break;
+                }
+                // the lowest non-empty digit whose mass above is below thr
+                int hc = -1;
+                double hab = 0.0, hb = 0.0;
+                double run = above + above_lane;
+#pragma unroll
+                for (int t = 7; t >= 0; --t) {
+                    if (bin[t] > 0.0 && run < thr) {
+                        hc = lane * 8 + t;
+                        hab = run;
+                        hb = bin[t];
+                    }
+                    run += bin[t];
+                }
+                int best = hc < 0 ? 0x7fffffff : hc;
+#pragma unroll
+                for (int o = 16; o; o >>= 1)
+                    best = min(best, __shfl_xor_sync(kFull, best, o));
+                if (best == 0x7fffffff) {  // no digit below the cut: cannot happen for S > 0
+                    state = SV_ERR_NONFINITE;
+                    break;
+                }
+                const int src = best >> 3;
+                hab = __shfl_sync(kFull, hab, src);
+                hb = __shfl_sync(kFull, hb, src);
+                prefix = (prefix << 8) | (uint32_t)best;
+                above = hab;
+                E_kept = (float)(hab + hb);
+                if (lev == LEVELS - 1)
+                    key_t = prefix;
+            }
+            if (state != SV_OK)
+                break;
+            if (!use_top)
+                key_t = 0;
+        }
+        // ---- C: the test at position i ([P1]) ----
+        if (i < K) {
+            const int x = xs[i];
+            const float lx = load_entry(a.logits, ES, (row0 + i) * V + x);
+            const bool kept = (!use_min || lx - lmax >= a.dmin) && key_of<ES>(lx) >= key_t;
+            const float ex = kept ? ex2((lx - lmax) * c) : 0.f;
+            const float qx = __ldg(a.q + ((int64_t)b * K + i) * V + x);
+            if (!(qx >= 0.f && qx < INFINITY)) {
+                state = SV_ERR_NONFINITE;
+                break;
+            }
+            if (lane == 0 && warp == 0)
+                pdr[i] = __fdiv_rn(ex, E_kept);
+            if (us[i] * qx * E_kept < ex)
+                continue;  // accepted
+        }
+        j = i;
+        break;
+    }
+
+    // ---- D: the corrected (j < K) or bonus (j = K) token, from p~ ([P1]) ----
+    if (state == SV_OK) {
+        const bool resid = j < K;
+        const int64_t re = (row0 + j) * V + v0;
+        const float* qrow = resid ? a.q + ((int64_t)b * K + j) * V + v0 : nullptr;
+        const float Ek = E_kept;
+        bool fallback = false;
+        // weight of an entry, scaled by E: max(0, e - q E) (residual) or e
+        // (bonus, or the fallback to p~_j when the residual is all zero), 0
+        // for a dropped token; e = 2^((l - l_max) c)
+        auto weight = [&](float l, int64_t e) -> float {
+            const bool kept = l > -INFINITY && (!use_min || l - lmax >= a.dmin) &&
+                              key_of<ES>(l) >= key_t;
+            if (!kept)
+                return 0.f;
+            const float ev = ex2((l - lmax) * c);
+            if (!resid || fallback)
+                return ev;
+            return fmaxf(ev - __ldg(qrow + e) * Ek, 0.f);
+        };
+        float cum_before = 0.f, Sw = 0.f, t = 0.f;
+        int owner = -1;
+        for (int round = 0; round < 2; ++round) {
+            float tot = 0.f, tc = 0.f;
+            bool badq = false;
+            visit<ES>(a, re, w0, w1, lane, [&](float l, int64_t e) {
+                if (resid && !fallback) {
+                    const float qv = __ldg(qrow + e);
+                    if (!(qv >= 0.f && qv < INFINITY))
+                        badq = true;
+                }
+                acc_add(tot, tc, weight(l, e));
+            });
+            const float wt = warp_sum(tot - tc);
+            const int s3 = exchange(make_float4(wt, __any_sync(kFull, badq) ? 1.f : 0.f, 0.f, 0.f));
+            if (s3 < 0) {
+                state = SV_ERR_TIMEOUT;
+                break;
+            }
+            // totals in vocabulary order: CTA rank, then warp
+            float bq = 0.f;
+            for (int p = lane; p < P; p += 32)
+                bq = fmaxf(bq, part[s3][p].y);
+            if (__any_sync(kFull, bq != 0.f)) {
+                state = SV_ERR_NONFINITE;
+                break;
+            }
+            Sw = 0.f;
+            for (int p = 0; p < P; ++p)
+                Sw += part[s3][p].x;
+            if (Sw > 0.f || fallback)
+                break;
+            fallback = true;  // residual all zero: draw from p~_j itself
+        }
+        if (state == SV_OK) {
+            t = us[K] * Sw;
+            float cum = 0.f;
+            int last_pos = -1;
+            for (int p = 0; p < P; ++p) {
+                const float w = part[(xcnt - 1) & 1u][p].x;
+                if (w > 0.f)
+                    last_pos = p;
+                if (owner < 0 && cum + w > t) {
+                    owner = p;
+                    cum_before = cum;
+                }
+                cum += w;
+            }
+            if (owner < 0) {  // rounding left the point past the last positive total
+                owner = last_pos;
+                cum_before = 0.f;
+                for (int p = 0; p < last_pos; ++p)
+                    cum_before += part[(xcnt - 1) & 1u][p].x;
+            }
+        }
+        // ---- the owner warp locates the token and writes the outputs ----
+        if (state == SV_OK && owner == rank * kNW + warp) {
+            const float tl = t - cum_before;
+            float run = 0.f;
+            int64_t tok = -1, last = -1;
+            for (int64_t cb = w0; cb < w1 && tok < 0; cb += 32) {  // one unit per lane
+                const int64_t ui = cb + lane;  // this lane's unit
+                float wl[16 / ES];
+                float lt = 0.f;
+#pragma unroll
+                for (int k = 0; k < 16 / ES; ++k)
+                    wl[k] = 0.f;
+                if (ui < w1) {
+                    if (a.vec) {
+                        const uint4 r = ld_stream(reinterpret_cast<const uint4*>(
+                                                      static_cast<const unsigned char*>(a.logits) +
+                                                      re * ES) + ui);
+#pragma unroll
+                        for (int k = 0; k < E; ++k) {
+                            wl[k] = weight(vec_entry<ES>(r, k), ui * E + k);
+                            lt += wl[k];
+                        }
+                    } else {
+                        wl[0] = weight(load_entry(a.logits, ES, re + ui), ui);
+                        lt = wl[0];
+                    }
+                }
+                // the last positive entry so far (rounding guard)
+                int lpos = -1;
+                const int ne = a.vec ? E : 1;
+                for (int k = 0; k < ne; ++k)
+                    if (wl[k] > 0.f)
+                        lpos = k;
+                const int64_t mylast = lpos >= 0 ? (a.vec ? ui * E + lpos : ui) : -1;
+                int64_t wl_last = mylast;
+#pragma unroll
+                for (int o = 16; o; o >>= 1) {
+                    const long long ov = __shfl_xor_sync(kFull, (long long)wl_last, o);
+                    wl_last = wl_last > ov ? wl_last : ov;
+                }
+                if (wl_last > last)
+                    last = wl_last;
+                // inclusive scan of the lane totals
+                float inc = lt;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float v = __shfl_up_sync(kFull, inc, o);
+                    if (lane >= o)
+                        inc += v;
+                }
+                const unsigned hit = __ballot_sync(kFull, run + inc > tl);
+                if (hit) {
+                    const int src = __ffs(hit) - 1;
+                    if (lane == src) {
+                        float acc = run + inc - lt;
+                        int64_t pick = -1;
+                        for (int k = 0; k < ne; ++k) {
+                            acc += wl[k];
+                            if (acc > tl && wl[k] > 0.f) {
+                                pick = a.vec ? ui * E + k : ui;
+                                break;
+                            }
+                        }
+                        if (pick < 0)  // the crossing fell on this lane's last weight
+                            pick = mylast;
+                        tok = pick;
+                    }
+                    tok = __shfl_sync(kFull, (long long)tok, src);
+                }
+                run += __shfl_sync(kFull, inc, 31);
+            }
+            if (tok < 0)
+                tok = last;
+            const int32_t token = (int32_t)(v0 + tok);
+            for (int i = lane; i <= K; i += 32) {
+                a.out_tokens[row0 + i] = i < j ? xs[i] : (i == j ? token : -1);
+                if (i < K)
+                    a.accept_mask[(int64_t)b * K + i] = i < j ? 1 : 0;
+                if (a.row_stats) {
+                    a.row_stats[(row0 + i) * 2] = i <= j ? rsm[i] : NAN;
+                    a.row_stats[(row0 + i) * 2 + 1] = i <= j ? rss[i] : NAN;
+                }
+                if (i < K && a.p_draft)
+                    a.p_draft[(int64_t)b * K + i] = i <= j ? pdr[i] : NAN;
+            }
+            if (lane == 0) {
+                a.accept_len[b] = j + 1;
+                if (a.status)
+                    a.status[b] = SV_OK;
+                if (a.al_hist)
+                    atomicAdd(a.al_hist + j + 1, 1u);
+            }
+        }
+    }
+
+    // ---- a sequence error: rank 0 reports it ----
+    if (state != SV_OK && rank == 0 && warp == 0) {
+        for (int i = lane; i <= K; i += 32) {
+            a.out_tokens[row0 + i] = -1;
+            if (i < K)
+                a.accept_mask[(int64_t)b * K + i] = 0;
+            if (a.row_stats) {
+                a.row_stats[(row0 + i) * 2] = NAN;
+                a.row_stats[(row0 + i) * 2 + 1] = NAN;
+            }
+            if (i < K && a.p_draft)
+                a.p_draft[(int64_t)b * K + i] = NAN;
+        }
+        if (lane == 0) {
+            a.accept_len[b] = 0;
+            if (a.status)
+                a.status[b] = state;
+            atomicOr(a.err_word, 1u << state);
+            if (a.al_hist)
+                atomicAdd(a.al_hist, 1u);
+        }
+    }
+    // no CTA leaves while a push into it may still be on its way
+    if (!ready)
+        cluster_wait();
+    cluster_arrive();
+    cluster_wait();
+}
+
+}  // namespace
+
+namespace sv {
+
+int trunc_set_attributes() {
+    const void* fns[2] = {(const void*)sv_trunc_kernel<2>, (const void*)sv_trunc_kernel<4>};
+    for (const void* f : fns)
+        if (cudaFuncSetAttribute(f, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+            cudaSuccess) {
+            (void)cudaGetLastError();
+            return 1;
+        }
+    return 0;
+}
+
+int trunc_launch(const TruncLaunch& g, void* stream) {
+    TArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.logits = g.logits;
+    a.q = g.q;
+    a.tokens = g.tokens;
+    a.u = g.u;
+    a.accept_len = g.accept_len;
+    a.out_tokens = g.out_tokens;
+    a.accept_mask = g.accept_mask;
+    a.row_stats = g.row_stats;
+    a.p_draft = g.p_draft;
+    a.status = g.status;
+    a.err_word = g.err_word;
+    a.al_hist = g.al_hist;
+    a.V = g.V;
+    a.slice = g.slice;
+    a.B = g.B;
+    a.K = g.K;
+    a.C = g.C;
+    a.vec = g.vec;
+    a.c = g.c;
+    a.T = g.T;
+    a.dmin = g.dmin;
+    a.top_p = g.top_p;
+    a.wait_ns = g.wait_ns;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)((int64_t)g.B * g.C), 1, 1);
+    cfg.blockDim = dim3(kNT, 1, 1);
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)g.C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = g.es == 2 ? cudaLaunchKernelEx(&cfg, sv_trunc_kernel<2>, a)
+                                    : cudaLaunchKernelEx(&cfg, sv_trunc_kernel<4>, a);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 1;
+    }
+    return 0;
+}
+
+}  // namespace sv
