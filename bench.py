@@ -51,10 +51,14 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=workloads.CONFIG_ORDER)
-    ap.add_argument("--mode", choices=["sampled", "greedy", "ragged"], default="sampled",
+    ap.add_argument("--mode", choices=["sampled", "greedy", "ragged", "truncated"],
+                    default="sampled",
                     help="sampled: spec_verify_run at the workload's temperature; greedy: "
                          "spec_verify_run_greedy (T -> 0) with a greedy drafter; ragged: "
-                         "spec_verify_run_ragged with per-sequence depths K_b ~ U{0..K}")
+                         "spec_verify_run_ragged with per-sequence depths K_b ~ U{0..K}; "
+                         "truncated: spec_verify_run_truncated with --top-p / --min-p")
+    ap.add_argument("--top-p", type=float, default=0.95)
+    ap.add_argument("--min-p", type=float, default=0.05)
     ap.add_argument("--sets", type=int, default=3, help="input copies rotated between steps")
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--no-e2e", action="store_true")
@@ -104,6 +108,7 @@ def measured_peak():
 
 KERNEL_SOURCES = ("speculative_decoding_verification_14_gb300/csrc/spec_verify.cu",
                   "speculative_decoding_verification_14_gb300/csrc/greedy.cu",
+                  "speculative_decoding_verification_14_gb300/csrc/truncated.cu",
                   "speculative_decoding_verification_14_gb300/csrc/sv_internal.h",
                   "speculative_decoding_verification_14_gb300/csrc/planner.cpp")
 
@@ -246,6 +251,7 @@ def run_ours(args):
     inp = rank_inputs(args.workload, rank)
     greedy = args.mode == "greedy"
     ragged = args.mode == "ragged"
+    trunc = args.mode == "truncated"
     if greedy:
         inp = workloads.greedy_drafts(inp)
     rg = None
@@ -290,6 +296,12 @@ def run_ours(args):
                           u.data_ptr(), st[4].data_ptr(), rg.R, B, K, V, ctypes.c_float(T),
                           outs["accept_len"].data_ptr(), outs["out_tokens"].data_ptr(),
                           outs["accept_mask"].data_ptr(), None, None, None))
+        elif trunc:
+            calls.append((verifier.ctx, lg.data_ptr(), dcode, q.data_ptr(), x.data_ptr(),
+                          u.data_ptr(), B, K, V, ctypes.c_float(T), ctypes.c_double(args.top_p),
+                          ctypes.c_double(args.min_p), outs["accept_len"].data_ptr(),
+                          outs["out_tokens"].data_ptr(), outs["accept_mask"].data_ptr(), None,
+                          None, None))
         elif greedy:
             calls.append((verifier.ctx, lg.data_ptr(), dcode, x.data_ptr(), B, K, V,
                           outs["accept_len"].data_ptr(), outs["out_tokens"].data_ptr(),
@@ -300,7 +312,7 @@ def run_ours(args):
                           outs["out_tokens"].data_ptr(), outs["accept_mask"].data_ptr(), None,
                           None, None))
     run = (lib.spec_verify_run_greedy if greedy else lib.spec_verify_run_ragged if ragged
-           else lib.spec_verify_run)
+           else lib.spec_verify_run_truncated if trunc else lib.spec_verify_run)
 
     def step(k, s=None):
         rc = run(*calls[k % nsets], stream.cuda_stream if s is None else s)
@@ -382,7 +394,8 @@ def run_ours(args):
     tokens_per_step = int(acc.sum())
     peak, peak_kind = measured_peak()
     achieved = alg / avg_launch_s / 1e9
-    plan = verifier.plan_greedy(B, K, V, dcode) if greedy else verifier.plan(B, K, V, dcode)
+    plan = (verifier.plan_greedy(B, K, V, dcode) if greedy else
+            verifier.plan_truncated(B, K, V, dcode) if trunc else verifier.plan(B, K, V, dcode))
 
     # end to end through the host-buffer entry point, copies inside the region
     e2e = None
@@ -390,6 +403,8 @@ def run_ours(args):
         e2e = e2e_greedy(args, inp, verifier, acc, dist, world, rows_per_step)
     elif ragged and not args.no_e2e and args.e2e_steps > 0:
         e2e = e2e_ragged(args, rg, verifier, acc, dist, world)
+    elif trunc and not args.no_e2e and args.e2e_steps > 0:
+        e2e = e2e_truncated(args, inp, verifier, acc, dist, world, rows_per_step)
     elif not args.no_e2e and args.e2e_steps > 0:
         def pinned(a):
             t = torch.empty(a.shape, dtype={np.float32: torch.float32, np.uint16: torch.int16,
@@ -432,7 +447,8 @@ def run_ours(args):
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = (cpu_baseline_ragged(rg, args.cpu_seconds) if ragged
-               else cpu_baseline(inp, args.cpu_seconds, greedy=greedy))
+               else cpu_baseline(inp, args.cpu_seconds, greedy=greedy,
+                                 trunc=(args.top_p, args.min_p) if trunc else None))
 
     if rank != 0:
         return None
@@ -443,7 +459,10 @@ def run_ours(args):
         "config": {"workload": args.workload + (" with a greedy drafter, greedy verify (T -> 0)"
                                                 if greedy else
                                                 " as a ragged batch, K_b ~ U{0..K}, packed rows"
-                                                if ragged else ""),
+                                                if ragged else
+                                                f" against the truncated target (top-p "
+                                                f"{args.top_p}, min-p {args.min_p})"
+                                                if trunc else ""),
                    "rows": rows_per_step,
                    "B": B, "K": K, "V": V, "logits_dtype": inp.dtype,
                    "T": 0.0 if greedy else T, "l2": f"{nsets} input copies of {per_set / 1e9:.2f} GB rotated "
@@ -469,7 +488,7 @@ def run_ours(args):
     return line
 
 
-def cpu_baseline(inp, seconds: float, greedy: bool = False) -> dict:
+def cpu_baseline(inp, seconds: float, greedy: bool = False, trunc=None) -> dict:
     """The oracle as it stands, single thread, on whole passes over the
     workload's sequences until `seconds` of CPU work have accumulated."""
     import oracle
@@ -478,6 +497,9 @@ def cpu_baseline(inp, seconds: float, greedy: bool = False) -> dict:
     def one(n):
         if greedy:
             oracle.verify_greedy(inp.logits[:n], inp.dtype, inp.tokens[:n])
+        elif trunc is not None:
+            oracle.verify_truncated(inp.logits[:n], inp.dtype, inp.q[:n], inp.tokens[:n],
+                                    inp.uniforms[:n], inp.T, trunc[0], trunc[1])
         else:
             oracle.verify(inp.logits[:n], inp.dtype, inp.q[:n], inp.tokens[:n], inp.uniforms[:n],
                           inp.T)
@@ -551,6 +573,45 @@ def e2e_ragged(args, rg, verifier, acc, dist, world) -> dict:
             "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in h_out.values())),
             "steps": args.e2e_steps,
             "api": "Verifier.run_ragged (spec_verify_run_ragged) with pinned host copies"}
+
+
+def e2e_truncated(args, inp, verifier, acc, dist, world, rows_per_step) -> dict:
+    """Truncated-target verify end to end through the public API: pinned host
+    inputs copied to the device, spec_verify_run_truncated, outputs copied
+    back, all inside the timed region."""
+    import torch
+    B, K = inp.B, inp.K
+    h = {"logits": torch.from_numpy(inp.logits.view(np.int16) if inp.dtype == "bf16"
+                                    else inp.logits).pin_memory(),
+         "q": torch.from_numpy(inp.q).pin_memory(), "tokens": torch.from_numpy(inp.tokens).pin_memory(),
+         "uniforms": torch.from_numpy(inp.uniforms).pin_memory()}
+    d = {k: torch.empty(t.shape, dtype=t.dtype, device="cuda") for k, t in h.items()}
+    h_out = {k: torch.empty(shape, dtype=dt).pin_memory() for k, shape, dt in
+             (("accept_len", (B,), torch.int32), ("out_tokens", (B, K + 1), torch.int32),
+              ("accept_mask", (B, K), torch.uint8))}
+
+    def once():
+        for k in h:
+            d[k].copy_(h[k], non_blocking=True)
+        lg = d["logits"].view(torch.bfloat16) if inp.dtype == "bf16" else d["logits"]
+        out = verifier.run_truncated(lg, d["q"], d["tokens"], d["uniforms"], inp.T, args.top_p,
+                                     args.min_p, status=False)
+        for k, t in h_out.items():
+            t.copy_(out[k], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    once()
+    if dist is not None:
+        dist.barrier()
+    ts = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        once()
+    el = max_over_ranks(time.perf_counter() - ts, dist)
+    assert np.array_equal(h_out["accept_len"].numpy(), acc)
+    return {"value": world * rows_per_step * args.e2e_steps / el, "unit": "rows/s",
+            "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in h.values())),
+            "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in h_out.values())),
+            "steps": args.e2e_steps,
+            "api": "Verifier.run_truncated (spec_verify_run_truncated) with pinned host copies"}
 
 
 def e2e_greedy(args, inp, verifier, acc, dist, world, rows_per_step) -> dict:
