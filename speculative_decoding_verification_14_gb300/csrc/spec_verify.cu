@@ -2043,6 +2043,7 @@ int spec_verify_run_truncated(sv_ctx* ctx, const void* target_logits, int logits
     g.C = plan.cluster;
     g.es = es;
     g.vec = plan.bulk_copy && aligned(target_logits, 16) ? 1 : 0;
+    g.qvec = (V % 4 == 0) && q && aligned(q, 16) ? 1 : 0;
     g.c = (float)(1.4426950408889634074 / (double)temperature);
     g.T = temperature;
     // min-p keeps l - l_max >= T ln(min_p); ln(min_p) = -inf for min_p <= 0 (off)

@@ -91,7 +91,7 @@ struct TruncLaunch {
     uint32_t* al_hist;
     int64_t V, slice;
     int B, K, C;
-    int es, vec;
+    int es, vec, qvec;
     float c, T, dmin;
     double top_p;
     unsigned long long wait_ns;

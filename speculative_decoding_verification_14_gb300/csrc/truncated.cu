@@ -72,6 +72,7 @@ struct TArgs {
     uint32_t* al_hist;
     int64_t V, slice;
     int B, K, C, vec;
+    int qvec;        // 1: draft rows may be read as float4 (16-byte aligned rows)
     float c;         // log2(e) / T, rounded to float
     float T;
     float dmin;      // T * ln(min_p): min-p keeps l - l_max >= dmin (-inf: off)
@@ -224,7 +225,8 @@ __device__ __forceinline__ float warp_max(float v) {
 
 namespace {
 
-constexpr int kDepth = 4;  // 16-byte loads in flight per lane
+constexpr int kDepth = 4;     // 16-byte loads in flight per lane
+constexpr int kChunks = 128;  // draw: chunk totals kept per warp
 
 // Calls fn(l, e) for every entry of this warp's stretch of one row (e = entry
 // index within the CTA's slice), lane by lane; entries of one lane come in
@@ -260,6 +262,49 @@ __device__ __forceinline__ void visit(const TArgs& a, int64_t row_elem, int64_t 
     }
 }
 
+// Calls fn(l, n) for every unit of this warp's stretch: a 16-byte vector of
+// E = 16/ES entries (vector path) or one entry (n = 1, element path).
+template <int ES, typename F>
+__device__ __forceinline__ void visit_units(const TArgs& a, int64_t row_elem, int64_t w0, int64_t w1,
+                                            int lane, F&& fn) {
+    constexpr int E = 16 / ES;
+    if (a.vec) {
+        const uint4* rp = reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(a.logits) +
+                                                         row_elem * ES);
+        for (int64_t base = w0; base < w1; base += 32 * kDepth) {
+            uint4 r[kDepth];
+#pragma unroll
+            for (int k = 0; k < kDepth; ++k) {
+                const int64_t idx = base + k * 32 + lane;
+                if (idx < w1)
+                    r[k] = ld_stream(rp + idx);
+            }
+#pragma unroll
+            for (int k = 0; k < kDepth; ++k) {
+                if (base + k * 32 + lane < w1) {
+                    float l[E];
+#pragma unroll
+                    for (int t = 0; t < E; ++t)
+                        l[t] = vec_entry<ES>(r[k], t);
+                    fn(l, E);
+                }
+            }
+        }
+    } else {
+        for (int64_t e = w0 + lane; e < w1; e += 32) {
+            float l[E];
+            l[0] = load_entry(a.logits, ES, row_elem + e);
+            fn(l, 1);
+        }
+    }
+}
+
+__device__ __forceinline__ float fmax_nan(float x, float y) {
+    float d;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(x), "f"(y));
+    return d;
+}
+
 template <int ES>
 __global__ void __launch_bounds__(kNT, sv::kTruncCtasPerSM) sv_trunc_kernel(const __grid_constant__ TArgs a) {
     constexpr int E = 16 / ES;
@@ -283,6 +328,7 @@ __global__ void __launch_bounds__(kNT, sv::kTruncCtasPerSM) sv_trunc_kernel(cons
     __shared__ int xs[sv::kMaxK];
     __shared__ float us[sv::kMaxRows];
     __shared__ float rsm[sv::kMaxRows], rss[sv::kMaxRows], pdr[sv::kMaxK];
+    __shared__ float ctot[kNW][kChunks];                         // draw: chunk totals per warp
 
     const int64_t v0 = (int64_t)rank * a.slice;
     const int64_t L = v0 < V ? (V - v0 < a.slice ? V - v0 : a.slice) : 0;
@@ -370,19 +416,28 @@ __global__ void __launch_bounds__(kNT, sv::kTruncCtasPerSM) sv_trunc_kernel(cons
         // ---- A: row maximum and S = sum 2^((l - l_max) c) ----
         float mx = -INFINITY, sm = 0.f, sc = 0.f;
         bool bad = false;
-        visit<ES>(a, re, w0, w1, lane, [&](float l, int64_t) {
-            if (l != l || l == INFINITY) {
+        // per unit: its maximum (NaN-propagating), a rescale when the lane's
+        // maximum grows, then the unit's terms against the lane maximum
+        visit_units<ES>(a, re, w0, w1, lane, [&](const float* l, int n) {
+            float vm = l[0];
+            for (int t = 1; t < n; ++t)
+                vm = fmax_nan(vm, l[t]);
+            if (vm != vm || vm == INFINITY) {
                 bad = true;
                 return;
             }
-            if (l == -INFINITY)  // weight 0
+            if (vm == -INFINITY)  // weights 0
                 return;
-            if (l > mx) {
-                sm = sm * ex2((mx - l) * c);
-                sc = sc * ex2((mx - l) * c);
-                mx = l;
+            if (vm > mx) {
+                const float r = ex2((mx - vm) * c);
+                sm *= r;
+                sc *= r;
+                mx = vm;
             }
-            acc_add(sm, sc, ex2((l - mx) * c));
+            float vs = 0.f;
+            for (int t = 0; t < n; ++t)
+                vs += ex2((l[t] - mx) * c);
+            acc_add(sm, sc, vs);
         });
         const float wmx = warp_max(mx);
         float wsm = (mx > -INFINITY) ? (sm - sc) * ex2((mx - wmx) * c) : 0.f;
@@ -531,35 +586,100 @@ __global__ void __launch_bounds__(kNT, sv::kTruncCtasPerSM) sv_trunc_kernel(cons
         const bool resid = j < K;
         const int64_t re = (row0 + j) * V + v0;
         const float* qrow = resid ? a.q + ((int64_t)b * K + j) * V + v0 : nullptr;
+        const uint4* rp = reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(a.logits) +
+                                                         re * ES);
         const float Ek = E_kept;
         bool fallback = false;
-        // weight of an entry, scaled by E: max(0, e - q E) (residual) or e
-        // (bonus, or the fallback to p~_j when the residual is all zero), 0
-        // for a dropped token; e = 2^((l - l_max) c)
-        auto weight = [&](float l, int64_t e) -> float {
+        // 2^((l - l_max) c) for a kept token, 0 for a dropped one
+        auto kept_w = [&](float l) -> float {
             const bool kept = l > -INFINITY && (!use_min || l - lmax >= a.dmin) &&
                               key_of<ES>(l) >= key_t;
-            if (!kept)
-                return 0.f;
-            const float ev = ex2((l - lmax) * c);
-            if (!resid || fallback)
-                return ev;
-            return fmaxf(ev - __ldg(qrow + e) * Ek, 0.f);
+            return kept ? ex2((l - lmax) * c) : 0.f;
+        };
+        // The stretch is walked in steps of 32 units (one per lane); g steps
+        // make a chunk, whose total is kept in shared memory for the locate.
+        const int64_t nsub = (w1 - w0 + 31) / 32;
+        const int64_t g = nsub > 0 ? (nsub + kChunks - 1) / kChunks : 1;
+        const int nch = (int)((nsub + g - 1) / g);
+        const int U = a.vec ? E : 1;  // entries per unit
+        // the lane's unit of step st: logits and (residual) draft probabilities
+        auto load_unit = [&](int64_t st, float (&l)[E], float (&qv)[E]) -> bool {
+            const int64_t ui = w0 + st * 32 + lane;
+            if (ui >= w1)
+                return false;
+            if (a.vec) {
+                const uint4 r = ld_stream(rp + ui);
+#pragma unroll
+                for (int t = 0; t < E; ++t)
+                    l[t] = vec_entry<ES>(r, t);
+            } else {
+                l[0] = load_entry(a.logits, ES, re + ui);
+            }
+            if (resid && !fallback) {
+                if (a.vec && a.qvec) {
+                    const float4* q4 = reinterpret_cast<const float4*>(qrow + ui * E);
+#pragma unroll
+                    for (int h = 0; h < E / 4; ++h) {
+                        const float4 v4 = __ldg(q4 + h);
+                        qv[4 * h] = v4.x;
+                        qv[4 * h + 1] = v4.y;
+                        qv[4 * h + 2] = v4.z;
+                        qv[4 * h + 3] = v4.w;
+                    }
+                } else {
+                    for (int t = 0; t < U; ++t)
+                        qv[t] = __ldg(qrow + ui * U + t);
+                }
+            }
+            return true;
+        };
+        // weights (scaled by E): max(0, e - q E) for the residual, e for the
+        // bonus row or the fallback to p~_j; returns their sum
+        auto unit_weights = [&](const float (&l)[E], const float (&qv)[E], float (&w)[E],
+                                bool& badq) -> float {
+            float sum = 0.f;
+            for (int t = 0; t < U; ++t) {
+                const float ev = kept_w(l[t]);
+                if (resid && !fallback) {
+                    if (!(qv[t] >= 0.f && qv[t] < INFINITY))
+                        badq = true;
+                    w[t] = fmaxf(ev - qv[t] * Ek, 0.f);
+                } else {
+                    w[t] = ev;
+                }
+                sum += w[t];
+            }
+            return sum;
         };
         float cum_before = 0.f, Sw = 0.f, t = 0.f;
         int owner = -1;
         for (int round = 0; round < 2; ++round) {
-            float tot = 0.f, tc = 0.f;
+            float wt = 0.f, wtc = 0.f, cpart = 0.f;
             bool badq = false;
-            visit<ES>(a, re, w0, w1, lane, [&](float l, int64_t e) {
-                if (resid && !fallback) {
-                    const float qv = __ldg(qrow + e);
-                    if (!(qv >= 0.f && qv < INFINITY))
-                        badq = true;
+            for (int64_t st0 = 0; st0 < nsub; st0 += kDepth) {
+                float l[kDepth][E], qv[kDepth][E];
+                bool have[kDepth];
+#pragma unroll
+                for (int k = 0; k < kDepth; ++k)
+                    have[k] = st0 + k < nsub && load_unit(st0 + k, l[k], qv[k]);
+#pragma unroll
+                for (int k = 0; k < kDepth; ++k) {
+                    const int64_t st = st0 + k;
+                    if (st >= nsub)
+                        break;
+                    float w[E];
+                    if (have[k])
+                        cpart += unit_weights(l[k], qv[k], w, badq);
+                    if ((st + 1) % g == 0 || st + 1 == nsub) {  // a chunk ends here
+                        const float ct = warp_sum(cpart);
+                        cpart = 0.f;
+                        if (lane == 0)
+                            ctot[warp][st / g] = ct;
+                        acc_add(wt, wtc, ct);
+                    }
                 }
-                acc_add(tot, tc, weight(l, e));
-            });
-            const float wt = warp_sum(tot - tc);
+            }
+            wt -= wtc;
             const int s3 = exchange(make_float4(wt, __any_sync(kFull, badq) ? 1.f : 0.f, 0.f, 0.f));
             if (s3 < 0) {
                 state = SV_ERR_TIMEOUT;
@@ -581,11 +701,12 @@ __global__ void __launch_bounds__(kNT, sv::kTruncCtasPerSM) sv_trunc_kernel(cons
             fallback = true;  // residual all zero: draw from p~_j itself
         }
         if (state == SV_OK) {
+            const int s3 = (int)((xcnt - 1) & 1u);
             t = us[K] * Sw;
             float cum = 0.f;
             int last_pos = -1;
             for (int p = 0; p < P; ++p) {
-                const float w = part[(xcnt - 1) & 1u][p].x;
+                const float w = part[s3][p].x;
                 if (w > 0.f)
                     last_pos = p;
                 if (owner < 0 && cum + w > t) {
@@ -598,53 +719,63 @@ __global__ void __launch_bounds__(kNT, sv::kTruncCtasPerSM) sv_trunc_kernel(cons
                 owner = last_pos;
                 cum_before = 0.f;
                 for (int p = 0; p < last_pos; ++p)
-                    cum_before += part[(xcnt - 1) & 1u][p].x;
+                    cum_before += part[s3][p].x;
             }
         }
         // ---- the owner warp locates the token and writes the outputs ----
         if (state == SV_OK && owner == rank * kNW + warp) {
             const float tl = t - cum_before;
-            float run = 0.f;
+            // the chunk holding the crossing point (same sums as the total)
+            int fc = -1, lastc = -1;
+            float before = 0.f, lastc_before = 0.f;
+            {
+                float run = 0.f, rc = 0.f;
+                for (int ch = 0; ch < nch; ++ch) {
+                    const float x = ctot[warp][ch];
+                    const float cur = run - rc;
+                    if (x > 0.f) {
+                        lastc = ch;
+                        lastc_before = cur;
+                    }
+                    if (cur + x > tl) {
+                        fc = ch;
+                        before = cur;
+                        break;
+                    }
+                    acc_add(run, rc, x);
+                }
+            }
+            if (fc < 0) {  // rounding: the last chunk with weight
+                fc = lastc;
+                before = lastc_before;
+            }
+            float run = before;
             int64_t tok = -1, last = -1;
-            for (int64_t cb = w0; cb < w1 && tok < 0; cb += 32) {  // one unit per lane
-                const int64_t ui = cb + lane;  // this lane's unit
-                float wl[16 / ES];
+            const int64_t s_end = min(nsub, (int64_t)(fc + 1) * g);
+            for (int64_t st = (int64_t)fc * g; st < s_end && tok < 0; ++st) {
+                float l[E], qv[E], w[E];
+                bool dummy = false;
                 float lt = 0.f;
 #pragma unroll
-                for (int k = 0; k < 16 / ES; ++k)
-                    wl[k] = 0.f;
-                if (ui < w1) {
-                    if (a.vec) {
-                        const uint4 r = ld_stream(reinterpret_cast<const uint4*>(
-                                                      static_cast<const unsigned char*>(a.logits) +
-                                                      re * ES) + ui);
-#pragma unroll
-                        for (int k = 0; k < E; ++k) {
-                            wl[k] = weight(vec_entry<ES>(r, k), ui * E + k);
-                            lt += wl[k];
-                        }
-                    } else {
-                        wl[0] = weight(load_entry(a.logits, ES, re + ui), ui);
-                        lt = wl[0];
-                    }
-                }
-                // the last positive entry so far (rounding guard)
+                for (int k = 0; k < E; ++k)
+                    w[k] = 0.f;
+                const int64_t ui = w0 + st * 32 + lane;
+                if (load_unit(st, l, qv))
+                    lt = unit_weights(l, qv, w, dummy);
                 int lpos = -1;
-                const int ne = a.vec ? E : 1;
-                for (int k = 0; k < ne; ++k)
-                    if (wl[k] > 0.f)
+                for (int k = 0; k < U; ++k)
+                    if (w[k] > 0.f)
                         lpos = k;
-                const int64_t mylast = lpos >= 0 ? (a.vec ? ui * E + lpos : ui) : -1;
-                int64_t wl_last = mylast;
+                const long long mylast = lpos >= 0 ? (long long)(ui * U + lpos) : -1ll;
+                long long wl_last = mylast;
 #pragma unroll
                 for (int o = 16; o; o >>= 1) {
-                    const long long ov = __shfl_xor_sync(kFull, (long long)wl_last, o);
+                    const long long ov = __shfl_xor_sync(kFull, wl_last, o);
                     wl_last = wl_last > ov ? wl_last : ov;
                 }
                 if (wl_last > last)
                     last = wl_last;
-                // inclusive scan of the lane totals
-                float inc = lt;
+                float inc = lt;  // inclusive scan of the lane sums
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
                     const float v = __shfl_up_sync(kFull, inc, o);
@@ -654,21 +785,20 @@ __global__ void __launch_bounds__(kNT, sv::kTruncCtasPerSM) sv_trunc_kernel(cons
                 const unsigned hit = __ballot_sync(kFull, run + inc > tl);
                 if (hit) {
                     const int src = __ffs(hit) - 1;
+                    long long pick = -1;
                     if (lane == src) {
                         float acc = run + inc - lt;
-                        int64_t pick = -1;
-                        for (int k = 0; k < ne; ++k) {
-                            acc += wl[k];
-                            if (acc > tl && wl[k] > 0.f) {
-                                pick = a.vec ? ui * E + k : ui;
+                        for (int k = 0; k < U; ++k) {
+                            acc += w[k];
+                            if (acc > tl && w[k] > 0.f) {
+                                pick = ui * U + k;
                                 break;
                             }
                         }
                         if (pick < 0)  // the crossing fell on this lane's last weight
                             pick = mylast;
-                        tok = pick;
                     }
-                    tok = __shfl_sync(kFull, (long long)tok, src);
+                    tok = __shfl_sync(kFull, pick, src);
                 }
                 run += __shfl_sync(kFull, inc, 31);
             }
@@ -761,6 +891,7 @@ int trunc_launch(const TruncLaunch& g, void* stream) {
     a.K = g.K;
     a.C = g.C;
     a.vec = g.vec;
+    a.qvec = g.qvec;
     a.c = g.c;
     a.T = g.T;
     a.dmin = g.dmin;
