@@ -47,6 +47,10 @@ def _bind(path: str) -> ctypes.CDLL:
     lib.oracle_verify_truncated.argtypes = [P, ctypes.c_int, P, P, P, ctypes.c_int64, ctypes.c_int,
                                             ctypes.c_int64, ctypes.c_float, ctypes.c_double,
                                             ctypes.c_double] + [P] * 11
+    lib.oracle_verify_draft_logits.restype = ctypes.c_int
+    lib.oracle_verify_draft_logits.argtypes = [P, ctypes.c_int, P, P, P, ctypes.c_int64,
+                                               ctypes.c_int, ctypes.c_int64, ctypes.c_float,
+                                               ctypes.c_float, ctypes.c_double, ctypes.c_double] + [P] * 11
     lib.oracle_verify_ragged.restype = ctypes.c_int
     lib.oracle_verify_ragged.argtypes = [P, ctypes.c_int, P, P, P, P, ctypes.c_int64, ctypes.c_int,
                                          ctypes.c_int64, ctypes.c_int64, ctypes.c_float] + [P] * 10
@@ -251,6 +255,40 @@ def verify_truncated(logits: np.ndarray, dtype: str, q: np.ndarray, tokens: np.n
                                      _ptr(out["sample_alt"]), _ptr(out["trunc_margin"]))
     if rc != 0:
         raise ValueError(f"oracle_verify_truncated rejected its arguments (rc={rc})")
+    return out
+
+
+def verify_draft_logits(logits: np.ndarray, dtype: str, dlogits: np.ndarray, tokens: np.ndarray,
+                        uniforms: np.ndarray, T: float, T_draft: float, top_p: float = 1.0,
+                        min_p: float = 0.0, lib: Optional[ctypes.CDLL] = None) -> dict:
+    """verify_truncated() with draft logits dlogits [B, K, V] (same dtype as the
+    target) instead of q: q_i = softmax(d_i / T_draft) in float64."""
+    lib = lib or _load()
+    st = np.float32 if dtype == "f32" else np.uint16
+    logits = np.ascontiguousarray(logits, dtype=st)
+    B, K1, V = logits.shape
+    K = K1 - 1
+    dlogits = np.ascontiguousarray(dlogits, dtype=st).reshape(B, K, V)
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32).reshape(B, K)
+    uniforms = np.ascontiguousarray(uniforms, dtype=np.float32).reshape(B, K + 1)
+    out = {
+        "accept_len": np.empty(B, np.int32), "out_tokens": np.empty((B, K + 1), np.int32),
+        "accept_mask": np.empty((B, K), np.uint8), "status": np.empty(B, np.int32),
+        "row_m": np.empty((B, K + 1)), "row_s": np.empty((B, K + 1)), "p_draft": np.empty((B, K)),
+        "accept_margin": np.empty(B), "sample_margin": np.empty(B),
+        "sample_alt": np.empty(B, np.int32), "trunc_margin": np.empty(B),
+    }
+    rc = lib.oracle_verify_draft_logits(_ptr(logits), _dtype_code(dtype), _ptr(dlogits),
+                                        _ptr(tokens), _ptr(uniforms), B, K, V, float(T),
+                                        float(T_draft), float(top_p), float(min_p),
+                                        _ptr(out["accept_len"]), _ptr(out["out_tokens"]),
+                                        _ptr(out["accept_mask"]), _ptr(out["status"]),
+                                        _ptr(out["row_m"]), _ptr(out["row_s"]),
+                                        _ptr(out["p_draft"]), _ptr(out["accept_margin"]),
+                                        _ptr(out["sample_margin"]), _ptr(out["sample_alt"]),
+                                        _ptr(out["trunc_margin"]))
+    if rc != 0:
+        raise ValueError(f"oracle_verify_draft_logits rejected its arguments (rc={rc})")
     return out
 
 

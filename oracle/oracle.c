@@ -215,7 +215,8 @@ static int verify_one(const void* logits, int dtype, const float* q, const int32
                       const float* u, int K, int64_t V, double T, double* p, double* w,
                       int32_t* out_tok, uint8_t* mask, double* rm, double* rs, double* pd,
                       double* a_margin, double* s_margin, int32_t* s_alt, int32_t* len,
-                      const trunc_opts* tr, double* t_margin)
+                      const trunc_opts* tr, double* t_margin, const void* dlog, double Td,
+                      double* qrow)
 {
     const size_t esz = dtype == 0 ? 4 : 2;
     const char* lbase = (const char*)logits;
@@ -246,10 +247,22 @@ static int verify_one(const void* logits, int dtype, const float* q, const int32
         rm[i] = m;
         rs[i] = s;
         const double px = p[x[i]];
-        const float qf = q[(size_t)i * (size_t)V + (size_t)x[i]];
-        if (!q_value_ok(qf))
-            return ORACLE_NONFINITE;
-        const double qx = (double)qf;
+        double qx;
+        if (dlog) {
+            /* draft logits given: q_i = softmax(d_i / T_d), the row the drafter
+             * sampled x_i from, computed when its test runs */
+            double dm, ds;
+            st = oracle_softmax_row((const char*)dlog + (size_t)i * (size_t)V * esz, dtype, V, Td,
+                                    qrow, &dm, &ds);
+            if (st != ORACLE_OK)
+                return st;
+            qx = qrow[x[i]];
+        } else {
+            const float qf = q[(size_t)i * (size_t)V + (size_t)x[i]];
+            if (!q_value_ok(qf))
+                return ORACLE_NONFINITE;
+            qx = (double)qf;
+        }
         pd[i] = px;
         if (qx > 0.0) {
             double mg = fabs((double)u[i] - px / qx);
@@ -266,11 +279,17 @@ static int verify_one(const void* logits, int dtype, const float* q, const int32
     if (j < K) {
         /* [P1] rejection at position j: the corrected token comes from
          * relu(p_j - q_j) normalised by its sum. */
-        const float* qj = q + (size_t)j * (size_t)V;
+        const float* qj = dlog ? 0 : q + (size_t)j * (size_t)V;
         for (int64_t v = 0; v < V; ++v) {
-            if (!q_value_ok(qj[v]))
-                return ORACLE_NONFINITE;
-            const double d = p[v] - (double)qj[v];
+            double qv;
+            if (dlog) {
+                qv = qrow[v]; /* row j: the last row tested */
+            } else {
+                if (!q_value_ok(qj[v]))
+                    return ORACLE_NONFINITE;
+                qv = (double)qj[v];
+            }
+            const double d = p[v] - qv;
             w[v] = d > 0.0 ? d : 0.0;
             S += w[v];
         }
@@ -318,10 +337,11 @@ static int verify_batch(const void* logits, int dtype, const float* q, const int
                         int32_t* accept_len, int32_t* out_tokens, uint8_t* accept_mask,
                         int32_t* status, double* row_m, double* row_s, double* p_draft,
                         double* accept_margin, double* sample_margin, int32_t* sample_alt,
-                        const trunc_opts* tr, double* trunc_margin)
+                        const trunc_opts* tr, double* trunc_margin, const void* dlogits,
+                        double Td)
 {
     if (!logits || !uniforms || !accept_len || !out_tokens || B < 0 || K < 0 || V < 1 ||
-        (K > 0 && (!q || !tokens || !accept_mask)) || (dtype != 0 && dtype != 1) ||
+        (K > 0 && ((!q && !dlogits) || !tokens || !accept_mask)) || (dtype != 0 && dtype != 1) ||
         !(temperature > 0.0f) || !isfinite(temperature))
         return -1;
     /* scratch: two rows of V doubles, plus the per-row results of one sequence */
@@ -330,8 +350,9 @@ static int verify_batch(const void* logits, int dtype, const float* q, const int
     double* rm = (double*)malloc((size_t)(K + 1) * sizeof(double));
     double* rs = (double*)malloc((size_t)(K + 1) * sizeof(double));
     double* pd = (double*)malloc((size_t)(K + 1) * sizeof(double));
-    if (!p || !w || !rm || !rs || !pd) {
-        free(p); free(w); free(rm); free(rs); free(pd);
+    double* qrow = dlogits ? (double*)malloc((size_t)V * sizeof(double)) : 0;
+    if (!p || !w || !rm || !rs || !pd || (dlogits && !qrow)) {
+        free(p); free(w); free(rm); free(rs); free(pd); free(qrow);
         return -2;
     }
     const size_t esz = dtype == 0 ? 4 : 2;
@@ -353,11 +374,14 @@ static int verify_batch(const void* logits, int dtype, const float* q, const int
         double a_mg = INFINITY, s_mg = INFINITY, t_mg = INFINITY;
         int32_t s_alt = -1, len = 0;
         int st = verify_one((const char*)logits + (size_t)b * (size_t)(K + 1) * (size_t)V * esz,
-                            dtype, K > 0 ? q + (size_t)b * (size_t)K * (size_t)V : 0,
+                            dtype, K > 0 && q ? q + (size_t)b * (size_t)K * (size_t)V : 0,
                             K > 0 ? tokens + (size_t)b * (size_t)K : 0,
                             uniforms + (size_t)b * (size_t)(K + 1), K, V, T, p, w, ot,
                             mk ? mk : mk_dummy, rm, rs, pd, &a_mg, &s_mg, &s_alt, &len, tr,
-                            &t_mg);
+                            &t_mg,
+                            dlogits ? (const char*)dlogits +
+                                          (size_t)b * (size_t)K * (size_t)V * esz : 0,
+                            Td, qrow);
         if (st != ORACLE_OK) {
             /* an erroneous sequence reports nothing but its status */
             len = 0;
@@ -395,7 +419,7 @@ static int verify_batch(const void* logits, int dtype, const float* q, const int
         if (sample_alt)
             sample_alt[b] = s_alt;
     }
-    free(p); free(w); free(rm); free(rs); free(pd);
+    free(p); free(w); free(rm); free(rs); free(pd); free(qrow);
     return 0;
 }
 
@@ -407,7 +431,7 @@ int oracle_verify(const void* logits, int dtype, const float* q, const int32_t* 
 {
     return verify_batch(logits, dtype, q, tokens, uniforms, B, K, V, temperature, accept_len,
                         out_tokens, accept_mask, status, row_m, row_s, p_draft, accept_margin,
-                        sample_margin, sample_alt, 0, 0);
+                        sample_margin, sample_alt, 0, 0, 0, 1.0);
 }
 
 /* The verify with the truncated target p~ (truncate_row) in place of p in
@@ -428,7 +452,34 @@ int oracle_verify_truncated(const void* logits, int dtype, const float* q, const
     trunc_opts tr = {top_p, min_p};
     return verify_batch(logits, dtype, q, tokens, uniforms, B, K, V, temperature, accept_len,
                         out_tokens, accept_mask, status, row_m, row_s, p_draft, accept_margin,
-                        sample_margin, sample_alt, &tr, trunc_margin);
+                        sample_margin, sample_alt, &tr, trunc_margin, 0, 1.0);
+}
+
+/* The verify with draft LOGITS in place of draft probabilities: the drafter's
+ * distribution at position i is q_i = softmax(d_i / T_d) ([P1]'s loop forms it
+ * the same way from the draft model's logits), computed in double precision
+ * when the loop needs it (the test at i; the residual at the rejected row).
+ * A draft row that holds a NaN or +inf, or only -inf, is a sequence error when
+ * the loop reaches it.  dlogits [B, K, V] has the target's dtype.  top_p >= 1
+ * and min_p <= 0 leave the target untruncated. */
+int oracle_verify_draft_logits(const void* logits, int dtype, const void* dlogits,
+                               const int32_t* tokens, const float* uniforms, int64_t B, int K,
+                               int64_t V, float temperature, float draft_temperature,
+                               double top_p, double min_p, int32_t* accept_len,
+                               int32_t* out_tokens, uint8_t* accept_mask, int32_t* status,
+                               double* row_m, double* row_s, double* p_draft,
+                               double* accept_margin, double* sample_margin,
+                               int32_t* sample_alt, double* trunc_margin)
+{
+    if (!dlogits || !(top_p > 0.0) || !(min_p < 1.0) || isnan(top_p) || isnan(min_p) ||
+        !(draft_temperature > 0.0f) || !isfinite(draft_temperature))
+        return -1;
+    trunc_opts tr = {top_p, min_p};
+    const int off = top_p >= 1.0 && min_p <= 0.0;
+    return verify_batch(logits, dtype, 0, tokens, uniforms, B, K, V, temperature, accept_len,
+                        out_tokens, accept_mask, status, row_m, row_s, p_draft, accept_margin,
+                        sample_margin, sample_alt, off ? 0 : &tr, trunc_margin, dlogits,
+                        (double)draft_temperature);
 }
 
 /* Acceptance telemetry ([P1] "Production perspective" and its operational

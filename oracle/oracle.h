@@ -97,6 +97,21 @@ int oracle_verify_truncated(const void* logits, int dtype, const float* q, const
                             double* accept_margin, double* sample_margin, int32_t* sample_alt,
                             double* trunc_margin);
 
+/* The verify (optionally against the truncated target) with draft LOGITS
+ * dlogits [B, K, V] (the target's dtype) instead of draft probabilities: q_i =
+ * softmax(d_i / T_d), in double precision, computed when the loop reaches row
+ * i.  A reached draft row with a NaN or +inf, or only -inf, is a sequence error.
+ * top_p >= 1 and min_p <= 0 leave the target untruncated.  Outputs as
+ * oracle_verify_truncated. */
+int oracle_verify_draft_logits(const void* logits, int dtype, const void* dlogits,
+                               const int32_t* tokens, const float* uniforms, int64_t B, int K,
+                               int64_t V, float temperature, float draft_temperature,
+                               double top_p, double min_p, int32_t* accept_len,
+                               int32_t* out_tokens, uint8_t* accept_mask, int32_t* status,
+                               double* row_m, double* row_s, double* p_draft,
+                               double* accept_margin, double* sample_margin,
+                               int32_t* sample_alt, double* trunc_margin);
+
 /* Ragged batch: sequence b owns packed target rows [off[b], off[b+1]) of R,
  * K_b = off[b+1] - off[b] - 1 <= K_max; its draft rows, tokens, mask and
  * p_draft start at off[b] - b, its uniforms, out_tokens and row stats at

@@ -12,8 +12,8 @@ from tests import oracle_pins as pins
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 
 MUTANTS = {
-    "residual_sign": ("const double d = p[v] - (double)qj[v];",
-                      "const double d = (double)qj[v] - p[v];"),
+    "residual_sign": ("const double d = p[v] - qv;",
+                      "const double d = qv - p[v];"),
     "test_uses_sample_uniform": ("if ((double)u[i] * qx < px)", "if ((double)u[K] * qx < px)"),
     "ratio_transposed": ("if ((double)u[i] * qx < px)", "if ((double)u[i] * px < qx)"),
     "accept_inverted": ("if ((double)u[i] * qx < px)", "if ((double)u[i] * qx > px)"),
@@ -25,8 +25,8 @@ MUTANTS = {
     "unnormalised_p": ("        p[v] /= s;", "        p[v] /= 1.0;"),
     "sample_uses_test_uniform": ("draw_inverse_cdf(w, V, S, (double)u[K]",
                                  "draw_inverse_cdf(w, V, S, (double)u[0]"),
-    "residual_from_wrong_q_row": ("const float* qj = q + (size_t)j * (size_t)V;",
-                                  "const float* qj = q + (size_t)(j ? j - 1 : 0) * (size_t)V;"),
+    "residual_from_wrong_q_row": ("const float* qj = dlog ? 0 : q + (size_t)j * (size_t)V;",
+                                  "const float* qj = dlog ? 0 : q + (size_t)(j ? j - 1 : 0) * (size_t)V;"),
     "accept_len_off_by_one": ("*len = j + 1;", "*len = j;"),
     "cdf_non_strict": ("if (run > t) {", "if (run >= t && w[v] >= 0.0 && v > 0) {"),
 }

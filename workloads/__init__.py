@@ -324,6 +324,51 @@ def ragged_from(inp: Inputs, Ks) -> RaggedInputs:
                         np.ascontiguousarray(u, dtype=np.float32), offsets)
 
 
+@dataclasses.dataclass
+class DraftLogitInputs:
+    """A workload whose drafter hands over its logits: dlogits [B, K, V] in the
+    target's dtype, draft tokens sampled from softmax(dlogits / T_draft), and q
+    [B, K, V] = that softmax rounded to float32 (for reference)."""
+    name: str
+    B: int
+    K: int
+    V: int
+    dtype: str
+    T: float
+    T_draft: float
+    logits: np.ndarray
+    dlogits: np.ndarray
+    q: np.ndarray
+    tokens: np.ndarray
+    uniforms: np.ndarray
+
+
+def with_draft_logits(name: str, seed: Optional[int] = None, B: Optional[int] = None) -> DraftLogitInputs:
+    """One of the named workloads with the draft logits themselves: the same
+    target rows and the same draft noise stream as make_config (d = target +
+    N(0, sigma_draft^2)), d stored in the target's dtype, and draft tokens drawn
+    from softmax(d_stored / T) with the same token stream."""
+    cfg = CONFIGS[name]
+    seed = cfg.seed if seed is None else seed
+    inp = make_config(name, seed=seed, B=B)
+    Bn, K, V, T = inp.B, cfg.K, cfg.V, cfg.T
+    d_st = np.empty((Bn, K, V), dtype=inp.logits.dtype)
+    q = np.empty((Bn, K, V), dtype=np.float32)
+    tokens = np.empty((Bn, K), dtype=np.int32)
+    for b in range(Bn):
+        rn, rx = _rng3(seed, 1, b), _rng3(seed, 3, b)
+        if not K:
+            continue
+        up = logits_as_f64(inp.logits[b, :K], cfg.dtype)
+        d = up + cfg.sigma_draft * rn.standard_normal(up.shape)
+        d_st[b] = _cast(d, cfg.dtype)
+        qd = softmax64(logits_as_f64(d_st[b], cfg.dtype) / T)
+        q[b] = qd.astype(np.float32)
+        tokens[b] = sample_tokens(qd, rx.random((K, 1)))[:, 0]
+    return DraftLogitInputs(name + "_dlogits", Bn, K, V, cfg.dtype, T, T, inp.logits, d_st, q,
+                            tokens, inp.uniforms)
+
+
 def greedy_drafts(inp: Inputs) -> Inputs:
     """The same workload with a greedy drafter: x_i = argmax_v q[b, i, v] (lowest
     id among equal maxima) instead of a draw from q.  Used for greedy
