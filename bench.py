@@ -51,12 +51,15 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=workloads.CONFIG_ORDER)
-    ap.add_argument("--mode", choices=["sampled", "greedy", "ragged", "truncated"],
+    ap.add_argument("--mode", choices=["sampled", "greedy", "ragged", "truncated",
+                                       "draft_logits"],
                     default="sampled",
                     help="sampled: spec_verify_run at the workload's temperature; greedy: "
                          "spec_verify_run_greedy (T -> 0) with a greedy drafter; ragged: "
                          "spec_verify_run_ragged with per-sequence depths K_b ~ U{0..K}; "
-                         "truncated: spec_verify_run_truncated with --top-p / --min-p")
+                         "truncated: spec_verify_run_truncated with --top-p / --min-p; "
+                         "draft_logits: spec_verify_run_draft_logits with the drafter's "
+                         "logits (T_d = T, untruncated target)")
     ap.add_argument("--top-p", type=float, default=0.95)
     ap.add_argument("--min-p", type=float, default=0.05)
     ap.add_argument("--sets", type=int, default=3, help="input copies rotated between steps")
@@ -172,6 +175,18 @@ def algorithmic_bytes_ragged(rg, accept_len: np.ndarray) -> int:
     return int(per.sum()) + (rg.B + 1) * 4
 
 
+def algorithmic_bytes_draft_logits(inp, accept_len: np.ndarray) -> int:
+    """Verify with draft logits: per sequence with accepted length n, the n
+    target rows reached and the min(n, K) draft rows tested (each row's
+    normaliser needs all of it; the residual re-uses the rejected draft row),
+    plus tokens, uniforms and outputs as algorithmic_bytes."""
+    B, K, V = inp.B, inp.K, inp.V
+    es = 2 if inp.dtype == "bf16" else 4
+    n = accept_len.astype(np.int64)
+    rows = int(n.sum()) + int(np.minimum(n, K).sum())
+    return rows * V * es + B * K * 4 + B * (K + 1) * 4 + B * (4 + (K + 1) * 4 + K)
+
+
 def algorithmic_bytes_greedy(inp, accept_len: np.ndarray) -> int:
     """Greedy verification: n rows of logits per sequence (rows 0..n-1, read in
     order up to the first rejection), the K draft tokens, and the outputs."""
@@ -252,8 +267,11 @@ def run_ours(args):
     greedy = args.mode == "greedy"
     ragged = args.mode == "ragged"
     trunc = args.mode == "truncated"
+    dlog = args.mode == "draft_logits"
     if greedy:
         inp = workloads.greedy_drafts(inp)
+    if dlog:
+        inp = workloads.with_draft_logits(args.workload, seed=cfg.seed + rank)
     rg = None
     if ragged:  # each sequence keeps its first K_b + 1 rows, K_b ~ U{0..K}
         Ks = np.random.default_rng(1000 + cfg.seed + rank).integers(0, inp.K + 1, inp.B)
@@ -261,7 +279,9 @@ def run_ours(args):
     B, K, V, T = inp.B, inp.K, inp.V, inp.T
     dcode = sv.SV_BF16 if inp.dtype == "bf16" else sv.SV_F32
     per_set = (inp.logits.nbytes + inp.tokens.nbytes if greedy else
-               rg.logits.nbytes + rg.q.nbytes if ragged else inp.nominal_bytes())
+               rg.logits.nbytes + rg.q.nbytes if ragged else
+               inp.logits.nbytes + inp.dlogits.nbytes + inp.tokens.nbytes + inp.uniforms.nbytes
+               if dlog else inp.nominal_bytes())
     nsets = max(1, args.sets)
 
     def dev_logits(src=None):
@@ -274,6 +294,9 @@ def run_ours(args):
     for s in range(nsets):
         if greedy:  # the greedy step reads no draft probabilities and no uniforms
             sets.append((dev_logits(), None, torch.from_numpy(inp.tokens).cuda(), None))
+        elif dlog:  # the drafter's logits take q's place
+            sets.append((dev_logits(), dev_logits(inp.dlogits), torch.from_numpy(inp.tokens).cuda(),
+                         torch.from_numpy(inp.uniforms).cuda()))
         elif ragged:
             sets.append((dev_logits(rg.logits), torch.from_numpy(rg.q).cuda(),
                          torch.from_numpy(rg.tokens).cuda(), torch.from_numpy(rg.uniforms).cuda(),
@@ -296,6 +319,12 @@ def run_ours(args):
                           u.data_ptr(), st[4].data_ptr(), rg.R, B, K, V, ctypes.c_float(T),
                           outs["accept_len"].data_ptr(), outs["out_tokens"].data_ptr(),
                           outs["accept_mask"].data_ptr(), None, None, None))
+        elif dlog:
+            calls.append((verifier.ctx, lg.data_ptr(), dcode, q.data_ptr(), x.data_ptr(),
+                          u.data_ptr(), B, K, V, ctypes.c_float(T), ctypes.c_float(inp.T_draft),
+                          ctypes.c_double(1.0), ctypes.c_double(0.0),
+                          outs["accept_len"].data_ptr(), outs["out_tokens"].data_ptr(),
+                          outs["accept_mask"].data_ptr(), None, None, None))
         elif trunc:
             calls.append((verifier.ctx, lg.data_ptr(), dcode, q.data_ptr(), x.data_ptr(),
                           u.data_ptr(), B, K, V, ctypes.c_float(T), ctypes.c_double(args.top_p),
@@ -312,7 +341,8 @@ def run_ours(args):
                           outs["out_tokens"].data_ptr(), outs["accept_mask"].data_ptr(), None,
                           None, None))
     run = (lib.spec_verify_run_greedy if greedy else lib.spec_verify_run_ragged if ragged
-           else lib.spec_verify_run_truncated if trunc else lib.spec_verify_run)
+           else lib.spec_verify_run_truncated if trunc
+           else lib.spec_verify_run_draft_logits if dlog else lib.spec_verify_run)
 
     def step(k, s=None):
         rc = run(*calls[k % nsets], stream.cuda_stream if s is None else s)
@@ -388,14 +418,16 @@ def run_ours(args):
         raise sv.SpecVerifyError(err, "device error during the benchmark")
     acc = outs["accept_len"].cpu().numpy()
     alg = (algorithmic_bytes_greedy(inp, acc) if greedy else
-           algorithmic_bytes_ragged(rg, acc) if ragged else algorithmic_bytes(inp, acc))
+           algorithmic_bytes_ragged(rg, acc) if ragged else
+           algorithmic_bytes_draft_logits(inp, acc) if dlog else algorithmic_bytes(inp, acc))
     avg_launch_s = local_ms / args.steps / 1e3  # this rank's average launch duration
     value = world * rows_per_step * args.steps / (total_ms / 1e3)
     tokens_per_step = int(acc.sum())
     peak, peak_kind = measured_peak()
     achieved = alg / avg_launch_s / 1e9
     plan = (verifier.plan_greedy(B, K, V, dcode) if greedy else
-            verifier.plan_truncated(B, K, V, dcode) if trunc else verifier.plan(B, K, V, dcode))
+            verifier.plan_truncated(B, K, V, dcode) if trunc else
+            verifier.plan_draft_logits(B, K, V, dcode, 0) if dlog else verifier.plan(B, K, V, dcode))
 
     # end to end through the host-buffer entry point, copies inside the region
     e2e = None
@@ -405,6 +437,8 @@ def run_ours(args):
         e2e = e2e_ragged(args, rg, verifier, acc, dist, world)
     elif trunc and not args.no_e2e and args.e2e_steps > 0:
         e2e = e2e_truncated(args, inp, verifier, acc, dist, world, rows_per_step)
+    elif dlog and not args.no_e2e and args.e2e_steps > 0:
+        e2e = e2e_draft_logits(args, inp, verifier, acc, dist, world, rows_per_step)
     elif not args.no_e2e and args.e2e_steps > 0:
         def pinned(a):
             t = torch.empty(a.shape, dtype={np.float32: torch.float32, np.uint16: torch.int16,
@@ -448,7 +482,7 @@ def run_ours(args):
     if rank == 0 and not args.no_cpu_baseline:
         cpu = (cpu_baseline_ragged(rg, args.cpu_seconds) if ragged
                else cpu_baseline(inp, args.cpu_seconds, greedy=greedy,
-                                 trunc=(args.top_p, args.min_p) if trunc else None))
+                                 trunc=(args.top_p, args.min_p) if trunc else None, dlog=dlog))
 
     if rank != 0:
         return None
@@ -462,7 +496,10 @@ def run_ours(args):
                                                 if ragged else
                                                 f" against the truncated target (top-p "
                                                 f"{args.top_p}, min-p {args.min_p})"
-                                                if trunc else ""),
+                                                if trunc else
+                                                " with the drafter's logits (bf16/f32 like the "
+                                                "target, T_d = T), untruncated target"
+                                                if dlog else ""),
                    "rows": rows_per_step,
                    "B": B, "K": K, "V": V, "logits_dtype": inp.dtype,
                    "T": 0.0 if greedy else T, "l2": f"{nsets} input copies of {per_set / 1e9:.2f} GB rotated "
@@ -471,7 +508,7 @@ def run_ours(args):
         "tokens_per_s": world * tokens_per_step * args.steps / (total_ms / 1e3),
         "mean_accept_len": float(acc.mean()),
         "hbm_gbs_algorithmic": achieved,
-        "hbm_gbs_nominal": inp.nominal_bytes() / avg_launch_s / 1e9,
+        "hbm_gbs_nominal": (per_set if dlog else inp.nominal_bytes()) / avg_launch_s / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
                      "traffic": profile_traffic(args.workload + ("" if args.mode == "sampled"
@@ -488,7 +525,7 @@ def run_ours(args):
     return line
 
 
-def cpu_baseline(inp, seconds: float, greedy: bool = False, trunc=None) -> dict:
+def cpu_baseline(inp, seconds: float, greedy: bool = False, trunc=None, dlog=False) -> dict:
     """The oracle as it stands, single thread, on whole passes over the
     workload's sequences until `seconds` of CPU work have accumulated."""
     import oracle
@@ -497,6 +534,9 @@ def cpu_baseline(inp, seconds: float, greedy: bool = False, trunc=None) -> dict:
     def one(n):
         if greedy:
             oracle.verify_greedy(inp.logits[:n], inp.dtype, inp.tokens[:n])
+        elif dlog:
+            oracle.verify_draft_logits(inp.logits[:n], inp.dtype, inp.dlogits[:n], inp.tokens[:n],
+                                       inp.uniforms[:n], inp.T, inp.T_draft)
         elif trunc is not None:
             oracle.verify_truncated(inp.logits[:n], inp.dtype, inp.q[:n], inp.tokens[:n],
                                     inp.uniforms[:n], inp.T, trunc[0], trunc[1])
@@ -612,6 +652,49 @@ def e2e_truncated(args, inp, verifier, acc, dist, world, rows_per_step) -> dict:
             "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in h_out.values())),
             "steps": args.e2e_steps,
             "api": "Verifier.run_truncated (spec_verify_run_truncated) with pinned host copies"}
+
+
+def e2e_draft_logits(args, inp, verifier, acc, dist, world, rows_per_step) -> dict:
+    """Draft-logit verify end to end through the public API: pinned host target
+    and draft logits, tokens and uniforms copied to the device,
+    spec_verify_run_draft_logits, outputs copied back, all inside the timed
+    region."""
+    import torch
+    B, K = inp.B, inp.K
+
+    def host(a):
+        return torch.from_numpy(a.view(np.int16) if inp.dtype == "bf16" else a).pin_memory()
+    h = {"logits": host(inp.logits), "dlogits": host(inp.dlogits),
+         "tokens": torch.from_numpy(inp.tokens).pin_memory(),
+         "uniforms": torch.from_numpy(inp.uniforms).pin_memory()}
+    d = {k: torch.empty(t.shape, dtype=t.dtype, device="cuda") for k, t in h.items()}
+    h_out = {k: torch.empty(shape, dtype=dt).pin_memory() for k, shape, dt in
+             (("accept_len", (B,), torch.int32), ("out_tokens", (B, K + 1), torch.int32),
+              ("accept_mask", (B, K), torch.uint8))}
+
+    def once():
+        for k in h:
+            d[k].copy_(h[k], non_blocking=True)
+        lg, dl = ((d["logits"].view(torch.bfloat16), d["dlogits"].view(torch.bfloat16))
+                  if inp.dtype == "bf16" else (d["logits"], d["dlogits"]))
+        out = verifier.run_draft_logits(lg, dl, d["tokens"], d["uniforms"], inp.T, inp.T_draft,
+                                        status=False)
+        for k, t in h_out.items():
+            t.copy_(out[k], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    once()
+    if dist is not None:
+        dist.barrier()
+    ts = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        once()
+    el = max_over_ranks(time.perf_counter() - ts, dist)
+    assert np.array_equal(h_out["accept_len"].numpy(), acc)
+    return {"value": world * rows_per_step * args.e2e_steps / el, "unit": "rows/s",
+            "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in h.values())),
+            "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in h_out.values())),
+            "steps": args.e2e_steps,
+            "api": "Verifier.run_draft_logits (spec_verify_run_draft_logits) with pinned host copies"}
 
 
 def e2e_greedy(args, inp, verifier, acc, dist, world, rows_per_step) -> dict:

@@ -214,6 +214,55 @@ int spec_verify_get_plan_truncated(sv_ctx* ctx, int B, int K, int64_t V, int log
 int spec_verify_plan_truncated_for(int num_sms, int max_cluster, int B, int K, int64_t V,
                                    int logits_dtype, int ovr_cluster, sv_plan* out);
 
+/* Verification with draft LOGITS instead of draft probabilities ([P1]
+ * "Speculative decoding: draft first, then verify": the drafter's distribution
+ * is q = softmax(draft_logits / T), formed from its logits at its temperature).
+ * Position i uses q_i = softmax(draft_logits[b, i] / draft_temperature): the
+ * test u*q(x) < p(x), and after a rejection at j the residual max(0, p_j - q_j).
+ * The kernel forms q from the draft row's own maximum and normaliser, taken in
+ * the same pass as the target row's, so no q array exists anywhere.  top_p < 1
+ * or min_p > 0 verify against the truncated target exactly as
+ * spec_verify_run_truncated does (q itself is never truncated); top_p >= 1
+ * with min_p <= 0 is the plain verify.
+ *
+ *   draft_logits [B, K, V]  the target's dtype (logits_dtype), device; row i is
+ *                           the drafter's scores at position i (may be NULL
+ *                           when K == 0)
+ *   draft_temperature       > 0 and finite
+ * Every other argument, layout and output as spec_verify_run_truncated
+ * (row_stats: the target rows' untruncated statistics; p_draft: p~(x_i)).
+ *
+ * Bytes: each row the pass reaches is read with its draft row (rows after the
+ * first rejection are never read), plus the rejected pair again for the draw.
+ * Device-detected errors as spec_verify_run, plus: a draft row the pass
+ * reaches holding a NaN or +inf, or only -inf, is SV_ERR_NONFINITE for that
+ * sequence.  16-byte aligned target and draft rows (V * element size a
+ * multiple of 16) take the vector path; other layouts the element path.
+ * Asynchronous, no allocation, one launch on `stream`.  Returns SV_OK,
+ * SV_ERR_INVALID_ARG (as spec_verify_run_truncated, plus a null or misaligned
+ * draft_logits with K > 0, or a draft temperature that is not positive and
+ * finite) or SV_ERR_CUDA. */
+int spec_verify_run_draft_logits(sv_ctx* ctx,
+                                 const void* target_logits, int logits_dtype,
+                                 const void* draft_logits, const int32_t* draft_tokens,
+                                 const float* uniforms, int B, int K, int64_t V,
+                                 float temperature, float draft_temperature,
+                                 double top_p, double min_p,
+                                 int32_t* accept_len, int32_t* out_tokens, uint8_t* accept_mask,
+                                 float* row_stats, float* p_draft, int32_t* status, void* stream);
+
+/* The draft-logit kernel's launch plan on the context's device (filters: 1
+ * when top-p or min-p is on). */
+int spec_verify_get_plan_draft_logits(sv_ctx* ctx, int B, int K, int64_t V, int logits_dtype,
+                                      int filters, sv_plan* out);
+
+/* Its planner as a pure host function (no CUDA call), for tests: the
+ * truncated planner when filters is 1; without filters clusters of up to 16
+ * CTAs (capped by max_cluster), four resident 128-thread CTAs per SM. */
+int spec_verify_plan_draft_logits_for(int num_sms, int max_cluster, int B, int K, int64_t V,
+                                      int logits_dtype, int filters, int ovr_cluster,
+                                      sv_plan* out);
+
 /* Greedy verification: the verify of spec_verify_run in the limit T -> 0
  * ([P1] "Speculative decoding: draft first, then verify": as T falls, the
  * softmax of logits/T puts all its mass on the largest logit).  Row i becomes

@@ -93,6 +93,21 @@ def library() -> ctypes.CDLL:
                                                               ctypes.c_int64, ctypes.c_int,
                                                               ctypes.c_int,
                                                               ctypes.POINTER(sv_plan)]),
+            "spec_verify_run_draft_logits": (ctypes.c_int, [P, P, ctypes.c_int, P, P, P,
+                                                            ctypes.c_int, ctypes.c_int,
+                                                            ctypes.c_int64, ctypes.c_float,
+                                                            ctypes.c_float, ctypes.c_double,
+                                                            ctypes.c_double, P, P, P, P, P, P,
+                                                            P]),
+            "spec_verify_get_plan_draft_logits": (ctypes.c_int, [P, ctypes.c_int, ctypes.c_int,
+                                                                 ctypes.c_int64, ctypes.c_int,
+                                                                 ctypes.c_int,
+                                                                 ctypes.POINTER(sv_plan)]),
+            "spec_verify_plan_draft_logits_for": (ctypes.c_int, [ctypes.c_int, ctypes.c_int,
+                                                                 ctypes.c_int, ctypes.c_int,
+                                                                 ctypes.c_int64, ctypes.c_int,
+                                                                 ctypes.c_int, ctypes.c_int,
+                                                                 ctypes.POINTER(sv_plan)]),
             "spec_verify_run_ragged": (ctypes.c_int, [P, P, ctypes.c_int, P, P, P, P,
                                                       ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                                       ctypes.c_int64, ctypes.c_float, P, P, P, P,
@@ -194,6 +209,35 @@ def spec_verify_plan_truncated_for(num_sms, max_cluster, B, K, V, dtype, ovr_clu
     plan = sv_plan()
     rc = library().spec_verify_plan_truncated_for(num_sms, max_cluster, B, K, V, dtype,
                                                   ovr_cluster, ctypes.byref(plan))
+    return rc, plan.as_dict()
+
+
+def spec_verify_run_draft_logits(ctx, logits_ptr, dtype, dlogits_ptr, tokens_ptr, uniforms_ptr, B,
+                                 K, V, T, T_draft, top_p, min_p, accept_len_ptr, out_tokens_ptr,
+                                 accept_mask_ptr, row_stats_ptr=None, p_draft_ptr=None,
+                                 status_ptr=None, stream=None) -> int:
+    return library().spec_verify_run_draft_logits(ctx, logits_ptr, dtype, dlogits_ptr, tokens_ptr,
+                                                  uniforms_ptr, B, K, V, float(T), float(T_draft),
+                                                  float(top_p), float(min_p), accept_len_ptr,
+                                                  out_tokens_ptr, accept_mask_ptr, row_stats_ptr,
+                                                  p_draft_ptr, status_ptr, stream)
+
+
+def spec_verify_get_plan_draft_logits(ctx, B, K, V, dtype, filters) -> dict:
+    plan = sv_plan()
+    rc = library().spec_verify_get_plan_draft_logits(ctx, B, K, V, dtype, int(filters),
+                                                     ctypes.byref(plan))
+    if rc != SV_OK:
+        raise SpecVerifyError(rc, "spec_verify_get_plan_draft_logits")
+    return plan.as_dict()
+
+
+def spec_verify_plan_draft_logits_for(num_sms, max_cluster, B, K, V, dtype, filters,
+                                      ovr_cluster=0):
+    plan = sv_plan()
+    rc = library().spec_verify_plan_draft_logits_for(num_sms, max_cluster, B, K, V, dtype,
+                                                     int(filters), ovr_cluster,
+                                                     ctypes.byref(plan))
     return rc, plan.as_dict()
 
 
@@ -484,6 +528,49 @@ class Verifier:
         if rc != SV_OK:
             raise SpecVerifyError(rc, "spec_verify_run_truncated")
         return out
+
+    def run_draft_logits(self, logits, dlogits, tokens, uniforms, temperature: float,
+                         draft_temperature: float, top_p: float = 1.0, min_p: float = 0.0,
+                         out: Optional[dict] = None, stats: bool = False, status: bool = True,
+                         stream=None) -> dict:
+        """run() with the drafter's logits dlogits [B, K, V] (the target's dtype)
+        in place of q; top_p < 1 / min_p > 0 truncate the target."""
+        import torch
+        B, K1, V = logits.shape
+        K = K1 - 1
+        if K and (dlogits.dtype != logits.dtype or tuple(dlogits.shape) != (B, K, V)):
+            raise ValueError("dlogits must be [B, K, V] in the target's dtype")
+        dev = logits.device
+        if out is None:
+            out = {
+                "accept_len": torch.empty(B, dtype=torch.int32, device=dev),
+                "out_tokens": torch.empty(B, K + 1, dtype=torch.int32, device=dev),
+                "accept_mask": torch.empty(B, max(K, 1), dtype=torch.uint8, device=dev)[:, :K],
+            }
+            if stats:
+                out["row_stats"] = torch.empty(B, K + 1, 2, dtype=torch.float32, device=dev)
+                out["p_draft"] = torch.empty(B, max(K, 1), dtype=torch.float32, device=dev)[:, :K]
+            if status:
+                out["status"] = torch.empty(B, dtype=torch.int32, device=dev)
+        s = stream if stream is not None else torch.cuda.current_stream(dev).cuda_stream
+
+        def ptr(name):
+            t = out.get(name)
+            return None if t is None else t.data_ptr()
+
+        rc = spec_verify_run_draft_logits(self.ctx, logits.data_ptr(), _dtype_code(logits),
+                                          dlogits.data_ptr() if K else None,
+                                          tokens.data_ptr() if K else None, uniforms.data_ptr(),
+                                          B, K, V, temperature, draft_temperature, top_p, min_p,
+                                          ptr("accept_len"), ptr("out_tokens"),
+                                          ptr("accept_mask") if K else None, ptr("row_stats"),
+                                          ptr("p_draft") if K else None, ptr("status"), s)
+        if rc != SV_OK:
+            raise SpecVerifyError(rc, "spec_verify_run_draft_logits")
+        return out
+
+    def plan_draft_logits(self, B, K, V, dtype=SV_BF16, filters=0) -> dict:
+        return spec_verify_get_plan_draft_logits(self.ctx, B, K, V, dtype, filters)
 
     def plan_truncated(self, B, K, V, dtype=SV_BF16) -> dict:
         return spec_verify_get_plan_truncated(self.ctx, B, K, V, dtype)

@@ -177,3 +177,15 @@ extern "C" int spec_verify_plan_truncated_for(int num_sms, int max_cluster, int 
     return plan_rows(num_sms, max_cluster, B, K, V, logits_dtype, ovr_cluster,
                      sv::kTruncCtasPerSM, 4, sv::kTruncMaxCluster, out);
 }
+
+// Verification with draft logits: the truncated kernel's mapping when a
+// filter is on; without filters the kernel holds no histograms, so clusters
+// may grow to 16 CTAs (four resident CTAs per SM either way).
+extern "C" int spec_verify_plan_draft_logits_for(int num_sms, int max_cluster, int B, int K,
+                                                 int64_t V, int logits_dtype, int filters,
+                                                 int ovr_cluster, sv_plan* out) {
+    return filters ? plan_rows(num_sms, max_cluster, B, K, V, logits_dtype, ovr_cluster,
+                               sv::kTruncCtasPerSM, 4, sv::kTruncMaxCluster, out)
+                   : plan_rows(num_sms, max_cluster, B, K, V, logits_dtype, ovr_cluster,
+                               sv::kDraftCtasPerSM, 4, sv::kMaxCluster, out);
+}

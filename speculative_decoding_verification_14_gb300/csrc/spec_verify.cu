@@ -1698,6 +1698,7 @@ struct sv_ctx {
     int64_t max_V = 0;
     int num_sms = 0, smem_optin = 0, max_cluster = 8;
     int greedy_max_cluster = 8;
+    int draft_max_cluster = 8;  // draft-logit kernel without filters
     uint32_t* d_err = nullptr;
     int ovr_cluster = 0, ovr_group = 0, ovr_threads = 0;
     int ovr_prefetch = -1;  // -1: the planner decides
@@ -1928,7 +1929,9 @@ int spec_verify_init(sv_ctx** out, int device, int max_B, int max_K, int64_t max
     ctx->max_cluster = max_cluster;
     // the greedy kernel may use 16-CTA clusters only where the main kernel may
     ctx->greedy_max_cluster = (max_cluster >= 16 && sv::greedy_set_attributes() == 0) ? 16 : 8;
-    (void)sv::trunc_set_attributes();  // clusters of at most 8 CTAs: portable either way
+    // the truncated kernel's clusters stay at 8 CTAs (portable either way); the
+    // draft-logit kernel without filters may use 16 where the main kernel may
+    ctx->draft_max_cluster = (sv::trunc_set_attributes() == 0 && max_cluster >= 16) ? 16 : 8;
     ctx->ovr_cluster = env_int("SV_CLUSTER", 0);
     ctx->ovr_group = env_int("SV_GROUP", 0);
     ctx->ovr_threads = env_int("SV_THREADS", 0);
@@ -2049,6 +2052,82 @@ int spec_verify_run_truncated(sv_ctx* ctx, const void* target_logits, int logits
     // min-p keeps l - l_max >= T ln(min_p); ln(min_p) = -inf for min_p <= 0 (off)
     g.dmin = min_p > 0.0 ? (float)((double)temperature * std::log(min_p)) : -INFINITY;
     g.top_p = top_p;
+    g.wait_ns = ctx->wait_ns;
+    DeviceGuard guard(ctx->device);
+    return sv::trunc_launch(g, stream) == 0 ? SV_OK : SV_ERR_CUDA;
+}
+
+int spec_verify_get_plan_draft_logits(sv_ctx* ctx, int B, int K, int64_t V, int logits_dtype,
+                                      int filters, sv_plan* out) {
+    if (!ctx)
+        return SV_ERR_INVALID_ARG;
+    const int cap = filters ? sv::kTruncMaxCluster : ctx->draft_max_cluster;
+    const int ovr = ctx->ovr_cluster > cap ? cap : ctx->ovr_cluster;
+    return spec_verify_plan_draft_logits_for(ctx->num_sms, cap, B, K, V, logits_dtype, filters,
+                                             ovr, out);
+}
+
+int spec_verify_run_draft_logits(sv_ctx* ctx, const void* target_logits, int logits_dtype,
+                                 const void* draft_logits, const int32_t* draft_tokens,
+                                 const float* uniforms, int B, int K, int64_t V,
+                                 float temperature, float draft_temperature, double top_p,
+                                 double min_p, int32_t* accept_len, int32_t* out_tokens,
+                                 uint8_t* accept_mask, float* row_stats, float* p_draft,
+                                 int32_t* status, void* stream) {
+    const size_t es = logits_dtype == SV_BF16 ? 2 : 4;
+    if (K > 0 && (!draft_logits || !aligned(draft_logits, es)))
+        return SV_ERR_INVALID_ARG;
+    // the shared checks want a float q for K > 0; the draft logits were
+    // checked above, so a stand-in that passes those checks takes q's place
+    static const float no_q = 0.f;
+    const int rc = validate(ctx, target_logits, logits_dtype, K > 0 ? &no_q : nullptr,
+                            draft_tokens, uniforms, B, K, V, temperature, accept_len, out_tokens,
+                            accept_mask, row_stats, p_draft, status);
+    if (rc != SV_OK)
+        return rc;
+    if (!(draft_temperature > 0.f) || !std::isfinite(draft_temperature))
+        return SV_ERR_INVALID_ARG;
+    if (!(top_p > 0.0) || !(min_p < 1.0) || std::isnan(top_p) || std::isnan(min_p))
+        return SV_ERR_INVALID_ARG;
+    if (ctx->al_hist && K + 2 > ctx->al_bins)
+        return SV_ERR_INVALID_ARG;
+    const int filters = (top_p < 1.0 || min_p > 0.0) ? 1 : 0;
+    sv_plan plan;
+    const int prc = spec_verify_get_plan_draft_logits(ctx, B, K, V, logits_dtype, filters, &plan);
+    if (prc != SV_OK)
+        return prc;
+    sv::TruncLaunch g;
+    std::memset(&g, 0, sizeof g);
+    g.logits = target_logits;
+    g.q = nullptr;
+    g.dlogits = K > 0 ? draft_logits : target_logits;  // K = 0: never read
+    g.tokens = draft_tokens;
+    g.u = uniforms;
+    g.accept_len = accept_len;
+    g.out_tokens = out_tokens;
+    g.accept_mask = accept_mask;
+    g.row_stats = row_stats;
+    g.p_draft = p_draft;
+    g.status = status;
+    g.err_word = ctx->d_err;
+    g.al_hist = ctx->al_hist;
+    g.V = V;
+    g.slice = plan.slice;
+    g.B = B;
+    g.K = K;
+    g.C = plan.cluster;
+    g.es = (int)es;
+    // target and draft rows share one unit layout: vectors only when both are aligned
+    g.vec = plan.bulk_copy && aligned(target_logits, 16) && (K == 0 || aligned(draft_logits, 16))
+                ? 1
+                : 0;
+    g.qvec = 0;
+    g.c = (float)(1.4426950408889634074 / (double)temperature);
+    g.cd = (float)(1.4426950408889634074 / (double)draft_temperature);
+    g.T = temperature;
+    g.dmin = min_p > 0.0 ? (float)((double)temperature * std::log(min_p)) : -INFINITY;
+    g.top_p = top_p;
+    g.filters = filters;
     g.wait_ns = ctx->wait_ns;
     DeviceGuard guard(ctx->device);
     return sv::trunc_launch(g, stream) == 0 ? SV_OK : SV_ERR_CUDA;

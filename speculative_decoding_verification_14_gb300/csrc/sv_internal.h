@@ -23,6 +23,7 @@ constexpr int kGreedyDepth = 8;         // greedy kernel: 16-byte loads in fligh
 constexpr int kGreedyCtasPerSM = 8;     // greedy kernel: resident 128-thread CTAs per SM (launch bounds)
 constexpr int kTruncCtasPerSM = 4;      // truncated-target kernel: resident CTAs per SM (launch bounds)
 constexpr int kTruncMaxCluster = 8;     // truncated-target kernel: largest cluster (shared histograms)
+constexpr int kDraftCtasPerSM = 4;      // draft-logit kernel without filters: resident CTAs per SM (launch bounds)
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
@@ -95,6 +96,9 @@ struct TruncLaunch {
     float c, T, dmin;
     double top_p;
     unsigned long long wait_ns;
+    const void* dlogits;  // draft logits [B, K, V] in the target's dtype (q unused), or NULL
+    float cd;             // log2(e) / T_draft rounded to float (draft logits)
+    int filters;          // draft logits: 1 when top-p or min-p is on
 };
 int trunc_set_attributes();                               // 0 on success
 int trunc_launch(const TruncLaunch& g, void* stream);    // 0 on success

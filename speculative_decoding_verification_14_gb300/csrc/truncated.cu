@@ -73,7 +73,9 @@ struct TArgs {
     int64_t V, slice;
     int B, K, C, vec;
     int qvec;        // 1: draft rows may be read as float4 (16-byte aligned rows)
+    const void* dlogits;  // draft logits [B, K, V] (target dtype), or NULL: q given
     float c;         // log2(e) / T, rounded to float
+    float cd;        // log2(e) / T_draft, rounded to float (draft logits)
     float T;
     float dmin;      // T * ln(min_p): min-p keeps l - l_max >= dmin (-inf: off)
     double top_p;    // >= 1: top-p off
@@ -262,14 +264,15 @@ __device__ __forceinline__ void visit(const TArgs& a, int64_t row_elem, int64_t 
     }
 }
 
-// Calls fn(l, n) for every unit of this warp's stretch: a 16-byte vector of
-// E = 16/ES entries (vector path) or one entry (n = 1, element path).
+// Calls fn(l, n) for every unit of this warp's stretch of a row of `base`
+// (the target or the draft logits): a 16-byte vector of E = 16/ES entries
+// (vector path) or one entry (n = 1, element path).
 template <int ES, typename F>
-__device__ __forceinline__ void visit_units(const TArgs& a, int64_t row_elem, int64_t w0, int64_t w1,
-                                            int lane, F&& fn) {
+__device__ __forceinline__ void visit_units(const TArgs& a, const void* base, int64_t row_elem,
+                                            int64_t w0, int64_t w1, int lane, F&& fn) {
     constexpr int E = 16 / ES;
     if (a.vec) {
-        const uint4* rp = reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(a.logits) +
+        const uint4* rp = reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(base) +
                                                          row_elem * ES);
         for (int64_t base = w0; base < w1; base += 32 * kDepth) {
             uint4 r[kDepth];
@@ -293,7 +296,7 @@ __device__ __forceinline__ void visit_units(const TArgs& a, int64_t row_elem, in
     } else {
         for (int64_t e = w0 + lane; e < w1; e += 32) {
             float l[E];
-            l[0] = load_entry(a.logits, ES, row_elem + e);
+            l[0] = load_entry(base, ES, row_elem + e);
             fn(l, 1);
         }
     }
@@ -305,11 +308,56 @@ __device__ __forceinline__ float fmax_nan(float x, float y) {
     return d;
 }
 
+// One row's statistics over this warp's stretch of `base`: the warp's
+// maximum and S = sum 2^((l - max) c) against it; bad when the stretch holds
+// a NaN or +inf.  Per unit: its maximum (NaN-propagating), a rescale when the
+// lane's maximum grows, then the unit's terms against the lane maximum.
 template <int ES>
-__global__ void __launch_bounds__(kNT, sv::kTruncCtasPerSM) sv_trunc_kernel(const __grid_constant__ TArgs a) {
+__device__ __forceinline__ void warp_row_stats(const TArgs& a, const void* base, int64_t re,
+                                               int64_t w0, int64_t w1, int lane, float c,
+                                               float& wmx, float& wsm, bool& wbad) {
+    float mx = -INFINITY, sm = 0.f, sc = 0.f;
+    bool bad = false;
+    visit_units<ES>(a, base, re, w0, w1, lane, [&](const float* l, int n) {
+        float vm = l[0];
+        for (int t = 1; t < n; ++t)
+            vm = fmax_nan(vm, l[t]);
+        if (vm != vm || vm == INFINITY) {
+            bad = true;
+            return;
+        }
+        if (vm == -INFINITY)  // weights 0
+            return;
+        if (vm > mx) {
+            const float r = ex2((mx - vm) * c);
+            sm *= r;
+            sc *= r;
+            mx = vm;
+        }
+        float vs = 0.f;
+        for (int t = 0; t < n; ++t)
+            vs += ex2((l[t] - mx) * c);
+        acc_add(sm, sc, vs);
+    });
+    wmx = warp_max(mx);
+    const float s = (mx > -INFINITY) ? (sm - sc) * ex2((mx - wmx) * c) : 0.f;
+    wsm = warp_sum(s);
+    wbad = __any_sync(kFull, bad);
+}
+
+// DL: draft logits instead of draft probabilities (q_i = softmax(d_i / T_d),
+// formed here from the draft row's own statistics).  TR: the top-p / min-p
+// machinery is compiled in (the untruncated draft-logit verify leaves it out,
+// which keeps shared memory small and the cluster up to 16 CTAs).
+template <int ES, bool DL, bool TR>
+__global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtasPerSM)
+    sv_trunc_kernel(const __grid_constant__ TArgs a) {
     constexpr int E = 16 / ES;
     constexpr int KEYBITS = 8 * ES;
     constexpr int LEVELS = KEYBITS / 8;
+    constexpr int MC = TR ? kMaxC : sv::kMaxCluster;  // largest cluster
+    constexpr int HB = TR ? kBins : 1;                // histogram bins held
+    constexpr int HC = TR ? kMaxC : 1;
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = (int)cluster.block_rank();
     const int b = (int)(blockIdx.x / (unsigned)a.C);
@@ -318,12 +366,12 @@ __global__ void __launch_bounds__(kNT, sv::kTruncCtasPerSM) sv_trunc_kernel(cons
     const int P = C * kNW;
     const int64_t V = a.V;
     const float c = a.c;
-    const bool use_min = a.dmin > -INFINITY;
-    const bool use_top = a.top_p < 1.0;
+    const bool use_min = TR && a.dmin > -INFINITY;
+    const bool use_top = TR && a.top_p < 1.0;
 
-    __shared__ __align__(16) float4 part[2][kMaxC * kNW];       // warp partials, by use parity
-    __shared__ __align__(16) double hrecv[2][kMaxC][kBins];     // CTA histograms, by use parity
-    __shared__ __align__(16) double hloc[kBins];                // this CTA's histogram
+    __shared__ __align__(16) float4 part[2][MC * kNW];          // warp partials, by use parity
+    __shared__ __align__(16) double hrecv[2][HC][HB];            // CTA histograms, by use parity
+    __shared__ __align__(16) double hloc[HB];                    // this CTA's histogram
     __shared__ __align__(8) unsigned long long xbar[2], hbar[2];
     __shared__ int xs[sv::kMaxK];
     __shared__ float us[sv::kMaxRows];
@@ -410,63 +458,55 @@ __global__ void __launch_bounds__(kNT, sv::kTruncCtasPerSM) sv_trunc_kernel(cons
 
     int j = -1;
     float lmax = 0.f, E_kept = 0.f;       // the decided row's statistics
+    float dmax = 0.f, dS = 0.f;           // ... and its draft row's (draft logits)
     uint32_t key_t = 0;                   // top-p: kept keys are >= key_t
     for (int i = 0; i <= K && state == SV_OK; ++i) {
         const int64_t re = (row0 + i) * V + v0;  // first element of this CTA's slice of row i
-        // ---- A: row maximum and S = sum 2^((l - l_max) c) ----
-        float mx = -INFINITY, sm = 0.f, sc = 0.f;
-        bool bad = false;
-        // per unit: its maximum (NaN-propagating), a rescale when the lane's
-        // maximum grows, then the unit's terms against the lane maximum
-        visit_units<ES>(a, re, w0, w1, lane, [&](const float* l, int n) {
-            float vm = l[0];
-            for (int t = 1; t < n; ++t)
-                vm = fmax_nan(vm, l[t]);
-            if (vm != vm || vm == INFINITY) {
-                bad = true;
-                return;
-            }
-            if (vm == -INFINITY)  // weights 0
-                return;
-            if (vm > mx) {
-                const float r = ex2((mx - vm) * c);
-                sm *= r;
-                sc *= r;
-                mx = vm;
-            }
-            float vs = 0.f;
-            for (int t = 0; t < n; ++t)
-                vs += ex2((l[t] - mx) * c);
-            acc_add(sm, sc, vs);
-        });
-        const float wmx = warp_max(mx);
-        float wsm = (mx > -INFINITY) ? (sm - sc) * ex2((mx - wmx) * c) : 0.f;
-        wsm = warp_sum(wsm);
-        const int s1 = exchange(make_float4(wmx, wsm, __any_sync(kFull, bad) ? 1.f : 0.f, 0.f));
+        // ---- A: row maximum and S = sum 2^((l - l_max) c); with draft
+        // logits, the same for the draft row d_i at c_d (i < K) ----
+        // (partial: (max, S or -1 when bad, draft max, draft S or -1))
+        float wmx, wsm, dmx = -INFINITY, dsm = 0.f;
+        bool bad, dbad = false;
+        warp_row_stats<ES>(a, a.logits, re, w0, w1, lane, c, wmx, wsm, bad);
+        if constexpr (DL) {
+            if (i < K)
+                warp_row_stats<ES>(a, a.dlogits, ((int64_t)b * K + i) * V + v0, w0, w1, lane, a.cd,
+                                   dmx, dsm, dbad);
+        }
+        const int s1 = exchange(make_float4(wmx, bad ? -1.f : wsm, dmx, dbad ? -1.f : dsm));
         if (s1 < 0) {
             state = SV_ERR_TIMEOUT;
             break;
         }
         {
-            float m = -INFINITY, bd = 0.f;
+            // merged in a fixed order, so every warp holds the same statistics
+            float m = -INFINITY, md = -INFINITY;
+            bool bd = false;
             for (int p = lane; p < P; p += 32) {
-                m = fmaxf(m, part[s1][p].x);
-                bd = fmaxf(bd, part[s1][p].z);
+                const float4 q4 = part[s1][p];
+                m = fmaxf(m, q4.x);
+                md = fmaxf(md, q4.z);
+                bd = bd || q4.y < 0.f || q4.w < 0.f;
             }
             m = warp_max(m);
-            float S = 0.f, Sc = 0.f;
-            for (int p = 0; p < P; ++p) {  // fixed order: the same S in every warp
+            md = warp_max(md);
+            float S = 0.f, Sc = 0.f, Sd = 0.f, Sdc = 0.f;
+            for (int p = 0; p < P; ++p) {
                 const float4 q4 = part[s1][p];
                 if (q4.x > -INFINITY)
                     acc_add(S, Sc, q4.y * ex2((q4.x - m) * c));
+                if (DL && q4.z > -INFINITY)
+                    acc_add(Sd, Sdc, q4.w * ex2((q4.z - md) * a.cd));
             }
             S -= Sc;
-            if (__any_sync(kFull, bd != 0.f) || !(m > -INFINITY)) {
+            if (__any_sync(kFull, bd) || !(m > -INFINITY) || (DL && i < K && !(md > -INFINITY))) {
                 state = SV_ERR_NONFINITE;
                 break;
             }
             lmax = m;
             E_kept = S;
+            dmax = md;
+            dS = Sd - Sdc;
             if (lane == 0 && warp == 0) {
                 rsm[i] = __fdiv_rn(m, a.T);
                 rss[i] = S;
@@ -475,7 +515,7 @@ __global__ void __launch_bounds__(kNT, sv::kTruncCtasPerSM) sv_trunc_kernel(cons
         const float S_all = E_kept;
         key_t = 0;
         // ---- B: the kept set ----
-        if (use_min || use_top) {
+        if constexpr (TR) if (use_min || use_top) {
             const double thr = a.top_p * (double)S_all;
             uint32_t prefix = 0;
             double above = 0.0;  // mass of candidates with keys above the prefix group
@@ -566,16 +606,29 @@ __global__ void __launch_bounds__(kNT, sv::kTruncCtasPerSM) sv_trunc_kernel(cons
             const int x = xs[i];
             const float lx = load_entry(a.logits, ES, (row0 + i) * V + x);
             const bool kept = (!use_min || lx - lmax >= a.dmin) && key_of<ES>(lx) >= key_t;
-            const float ex = kept ? ex2((lx - lmax) * c) : 0.f;
-            const float qx = __ldg(a.q + ((int64_t)b * K + i) * V + x);
-            if (!(qx >= 0.f && qx < INFINITY)) {
-                state = SV_ERR_NONFINITE;
-                break;
+            if constexpr (DL) {
+                // p~(x) E = 2^((l_x - l_max) c) and q(x) S_d = 2^((d_x - d_max) c_d),
+                // in double (one test per row): u q(x) < p~(x) <=>
+                // u 2^((d_x - d_max) c_d) E < 2^((l_x - l_max) c) S_d
+                const float dx = load_entry(a.dlogits, ES, ((int64_t)b * K + i) * V + x);
+                const double ex = kept ? exp2((double)(lx - lmax) * (double)c) : 0.0;
+                const double qn = exp2((double)(dx - dmax) * (double)a.cd);
+                if (lane == 0 && warp == 0)
+                    pdr[i] = (float)(ex / (double)E_kept);
+                if ((double)us[i] * qn * (double)E_kept < ex * (double)dS)
+                    continue;  // accepted
+            } else {
+                const float ex = kept ? ex2((lx - lmax) * c) : 0.f;
+                const float qx = __ldg(a.q + ((int64_t)b * K + i) * V + x);
+                if (!(qx >= 0.f && qx < INFINITY)) {
+                    state = SV_ERR_NONFINITE;
+                    break;
+                }
+                if (lane == 0 && warp == 0)
+                    pdr[i] = __fdiv_rn(ex, E_kept);
+                if (us[i] * qx * E_kept < ex)
+                    continue;  // accepted
             }
-            if (lane == 0 && warp == 0)
-                pdr[i] = __fdiv_rn(ex, E_kept);
-            if (us[i] * qx * E_kept < ex)
-                continue;  // accepted
         }
         j = i;
         break;
@@ -585,7 +638,13 @@ __global__ void __launch_bounds__(kNT, sv::kTruncCtasPerSM) sv_trunc_kernel(cons
     if (state == SV_OK) {
         const bool resid = j < K;
         const int64_t re = (row0 + j) * V + v0;
-        const float* qrow = resid ? a.q + ((int64_t)b * K + j) * V + v0 : nullptr;
+        const float* qrow = (resid && !DL) ? a.q + ((int64_t)b * K + j) * V + v0 : nullptr;
+        const int64_t dre = ((int64_t)b * K + j) * V + v0;  // draft logits: row j's slice
+        const uint4* dp = DL && resid ? reinterpret_cast<const uint4*>(
+                                            static_cast<const unsigned char*>(a.dlogits) + dre * ES)
+                                      : nullptr;
+        // draft logits: q_v E = 2^((d_v - d_max) c_d) * (E / S_d)
+        const float rq = DL && resid ? __fdiv_rn(E_kept, dS) : 0.f;
         const uint4* rp = reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(a.logits) +
                                                          re * ES);
         const float Ek = E_kept;
@@ -615,7 +674,16 @@ __global__ void __launch_bounds__(kNT, sv::kTruncCtasPerSM) sv_trunc_kernel(cons
             } else {
                 l[0] = load_entry(a.logits, ES, re + ui);
             }
-            if (resid && !fallback) {
+            if (DL && resid && !fallback) {
+                if (a.vec) {
+                    const uint4 r = ld_stream(dp + ui);
+#pragma unroll
+                    for (int t = 0; t < E; ++t)
+                        qv[t] = vec_entry<ES>(r, t);
+                } else {
+                    qv[0] = load_entry(a.dlogits, ES, dre + ui);
+                }
+            } else if (resid && !fallback) {
                 if (a.vec && a.qvec) {
                     const float4* q4 = reinterpret_cast<const float4*>(qrow + ui * E);
 #pragma unroll
@@ -640,7 +708,10 @@ __global__ void __launch_bounds__(kNT, sv::kTruncCtasPerSM) sv_trunc_kernel(cons
             float sum = 0.f;
             for (int t = 0; t < U; ++t) {
                 const float ev = kept_w(l[t]);
-                if (resid && !fallback) {
+                if (DL && resid && !fallback) {
+                    // qv holds the draft logits (checked when the row was read)
+                    w[t] = fmaxf(ev - ex2((qv[t] - dmax) * a.cd) * rq, 0.f);
+                } else if (resid && !fallback) {
                     if (!(qv[t] >= 0.f && qv[t] < INFINITY))
                         badq = true;
                     w[t] = fmaxf(ev - qv[t] * Ek, 0.f);
@@ -860,7 +931,12 @@ __global__ void __launch_bounds__(kNT, sv::kTruncCtasPerSM) sv_trunc_kernel(cons
 namespace sv {
 
 int trunc_set_attributes() {
-    const void* fns[2] = {(const void*)sv_trunc_kernel<2>, (const void*)sv_trunc_kernel<4>};
+    const void* fns[6] = {(const void*)sv_trunc_kernel<2, false, true>,
+                          (const void*)sv_trunc_kernel<4, false, true>,
+                          (const void*)sv_trunc_kernel<2, true, true>,
+                          (const void*)sv_trunc_kernel<4, true, true>,
+                          (const void*)sv_trunc_kernel<2, true, false>,
+                          (const void*)sv_trunc_kernel<4, true, false>};
     for (const void* f : fns)
         if (cudaFuncSetAttribute(f, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
             cudaSuccess) {
@@ -892,7 +968,9 @@ int trunc_launch(const TruncLaunch& g, void* stream) {
     a.C = g.C;
     a.vec = g.vec;
     a.qvec = g.qvec;
+    a.dlogits = g.dlogits;
     a.c = g.c;
+    a.cd = g.cd;
     a.T = g.T;
     a.dmin = g.dmin;
     a.top_p = g.top_p;
@@ -909,8 +987,17 @@ int trunc_launch(const TruncLaunch& g, void* stream) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = g.es == 2 ? cudaLaunchKernelEx(&cfg, sv_trunc_kernel<2>, a)
-                                    : cudaLaunchKernelEx(&cfg, sv_trunc_kernel<4>, a);
+    // q given: the truncated kernel; draft logits: with or without the filters
+    cudaError_t e;
+    if (!g.dlogits)
+        e = g.es == 2 ? cudaLaunchKernelEx(&cfg, sv_trunc_kernel<2, false, true>, a)
+                      : cudaLaunchKernelEx(&cfg, sv_trunc_kernel<4, false, true>, a);
+    else if (g.filters)
+        e = g.es == 2 ? cudaLaunchKernelEx(&cfg, sv_trunc_kernel<2, true, true>, a)
+                      : cudaLaunchKernelEx(&cfg, sv_trunc_kernel<4, true, true>, a);
+    else
+        e = g.es == 2 ? cudaLaunchKernelEx(&cfg, sv_trunc_kernel<2, true, false>, a)
+                      : cudaLaunchKernelEx(&cfg, sv_trunc_kernel<4, true, false>, a);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return 1;

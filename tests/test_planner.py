@@ -114,3 +114,40 @@ def test_greedy_workload_plans(sv):
     assert gplan(sv, 4, 2, 50000, 1, oc=16, dev=dict(GB300, max_cluster=8))[0] == sv.SV_ERR_UNSUPPORTED
     assert gplan(sv, 0, 2, 50000, 1)[0] == sv.SV_ERR_INVALID_ARG
     assert gplan(sv, 1, 33, 50000, 1)[0] == sv.SV_ERR_INVALID_ARG
+
+
+# ------------------------------------------------------- draft logits -----
+
+def dplan(sv, B, K, V, dtype, filters, oc=0, dev=GB300):
+    return sv.spec_verify_plan_draft_logits_for(dev["num_sms"], dev["max_cluster"], B, K, V, dtype,
+                                                filters, oc)
+
+
+@pytest.mark.parametrize("B,K,V,dtype,filters", list(itertools.product(
+    [1, 8, 64, 256, 5000], [0, 7], [1, 7, 32000, 128256], [0, 1], [0, 1])))
+def test_draft_logits_plan_invariants(sv, B, K, V, dtype, filters):
+    rc, p = dplan(sv, B, K, V, dtype, filters)
+    assert rc == sv.SV_OK
+    es = 2 if dtype == 1 else 4
+    C, slice_ = p["cluster"], p["slice"]
+    assert C in ((1, 2, 4, 8) if filters else (1, 2, 4, 8, 16))
+    assert slice_ % 8 == 0 and slice_ * C >= V and slice_ * (C - 1) < V + 8 * C
+    assert p["grid"] == B * C and p["threads"] == 128
+    assert p["bulk_copy"] == int((V * es) % 16 == 0)
+    if B <= 152 * 4:  # four resident CTAs per SM
+        assert B * C <= 152 * 4
+    # with a filter on, the plan is the truncated kernel's
+    if filters:
+        assert p == sv.spec_verify_plan_truncated_for(152, 16, B, K, V, dtype, 0)[1]
+
+
+def test_draft_logits_workload_plans(sv):
+    assert dplan(sv, 256, 7, 128256, 1, 0)[1]["cluster"] == 2
+    assert dplan(sv, 64, 3, 151936, 1, 0)[1]["cluster"] == 8
+    assert dplan(sv, 8, 4, 32000, 1, 0)[1]["cluster"] == 16
+    assert dplan(sv, 8, 4, 32000, 1, 1)[1]["cluster"] == 8
+    assert dplan(sv, 8, 4, 32000, 1, 0, dev=dict(GB300, max_cluster=8))[1]["cluster"] == 8
+    assert dplan(sv, 4, 2, 50000, 1, 0, oc=16, dev=dict(GB300, max_cluster=8))[0] == \
+        sv.SV_ERR_UNSUPPORTED
+    assert dplan(sv, 4, 2, 50000, 1, 1, oc=16)[0] == sv.SV_ERR_INVALID_ARG
+    assert dplan(sv, 0, 2, 50000, 1, 0)[0] == sv.SV_ERR_INVALID_ARG

@@ -369,6 +369,25 @@ def with_draft_logits(name: str, seed: Optional[int] = None, B: Optional[int] = 
                             tokens, inp.uniforms)
 
 
+def make_random_draft_logits(B: int, K: int, V: int, dtype: str = "f32", T: float = 1.0,
+                             T_draft: float = 1.0, sigma: float = 2.0, sigma_draft: float = 1.0,
+                             seed: int = 0) -> DraftLogitInputs:
+    """Small random instance whose drafter hands over its logits: target rows as
+    make_random, d = target + N(0, sigma_draft^2) stored in the target's dtype,
+    draft tokens drawn from softmax(d_stored / T_draft)."""
+    inp = make_random(B, K, V, dtype, T=T, sigma=sigma, sigma_draft=sigma_draft, seed=seed)
+    rn, rx = _rng(seed, 11), _rng(seed, 13)
+    up = logits_as_f64(inp.logits[:, :K], dtype)
+    d_st = _cast(up + sigma_draft * rn.standard_normal(up.shape), dtype)
+    q64 = softmax64(logits_as_f64(d_st, dtype) / float(np.float32(T_draft))) if K else \
+        np.zeros((B, 0, V))
+    tokens = (sample_tokens(q64, rx.random((B, K, 1)))[..., 0] if K
+              else np.zeros((B, 0), np.int32))
+    return DraftLogitInputs(f"random_dlogits_{B}x{K}x{V}", B, K, V, dtype, T, T_draft, inp.logits,
+                            np.ascontiguousarray(d_st), q64.astype(np.float32),
+                            np.ascontiguousarray(tokens.astype(np.int32)), inp.uniforms)
+
+
 def greedy_drafts(inp: Inputs) -> Inputs:
     """The same workload with a greedy drafter: x_i = argmax_v q[b, i, v] (lowest
     id among equal maxima) instead of a draw from q.  Used for greedy
