@@ -109,32 +109,38 @@ def measured_peak():
         return 6800.0, "fallback"
 
 
-KERNEL_SOURCES = ("speculative_decoding_verification_14_gb300/csrc/spec_verify.cu",
-                  "speculative_decoding_verification_14_gb300/csrc/greedy.cu",
-                  "speculative_decoding_verification_14_gb300/csrc/truncated.cu",
-                  "speculative_decoding_verification_14_gb300/csrc/sv_internal.h",
-                  "speculative_decoding_verification_14_gb300/csrc/planner.cpp")
+_CSRC = "speculative_decoding_verification_14_gb300/csrc/"
+# the sources each mode's kernel and launch path are built from (every entry
+# point's host side lives in spec_verify.cu)
+KERNEL_SOURCES = {
+    "sampled": ("spec_verify.cu", "sv_internal.h", "planner.cpp"),
+    "ragged": ("spec_verify.cu", "sv_internal.h", "planner.cpp"),
+    "greedy": ("greedy.cu", "spec_verify.cu", "sv_internal.h", "planner.cpp"),
+    "truncated": ("truncated.cu", "spec_verify.cu", "sv_internal.h", "planner.cpp"),
+    "draft_logits": ("truncated.cu", "spec_verify.cu", "sv_internal.h", "planner.cpp"),
+}
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(mode: str = "sampled") -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
+    for rel in KERNEL_SOURCES[mode]:
+        with open(os.path.join(ROOT, _CSRC + rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
 
 
-def profile_traffic(workload):
+def profile_traffic(workload: str, mode: str):
     """DRAM bytes per launch from the committed ncu summary, if it covers this
-    workload and was taken on the current kernel sources (else None)."""
+    workload and mode and was taken on the current sources of that mode's
+    kernel (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
+    key = workload + ("" if mode == "sampled" else "_" + mode)
     try:
         with open(path) as f:
-            d = json.load(f)
-        if d.get("kernel_source_sha256") != kernel_source_hash():
+            e = json.load(f).get(key)
+        if not e or e.get("kernel_source_sha256") != kernel_source_hash(mode):
             return None
-        e = d.get(workload)
-        return float(e["dram_bytes_per_launch"]) if e else None
+        return float(e["dram_bytes_per_launch"])
     except Exception:
         return None
 
@@ -511,8 +517,7 @@ def run_ours(args):
         "hbm_gbs_nominal": (per_set if dlog else inp.nominal_bytes()) / avg_launch_s / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
-                     "traffic": profile_traffic(args.workload + ("" if args.mode == "sampled"
-                                                                 else "_" + args.mode)),
+                     "traffic": profile_traffic(args.workload, args.mode),
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind ==
                      "measured" else "fallback 6.8 TB/s",
                      "algorithmic_bytes_per_launch": alg, "avg_launch_us": avg_launch_s * 1e6},

@@ -267,23 +267,23 @@ __device__ __forceinline__ void visit(const TArgs& a, int64_t row_elem, int64_t 
 // Calls fn(l, n) for every unit of this warp's stretch of a row of `base`
 // (the target or the draft logits): a 16-byte vector of E = 16/ES entries
 // (vector path) or one entry (n = 1, element path).
-template <int ES, typename F>
+template <int ES, int D, typename F>
 __device__ __forceinline__ void visit_units(const TArgs& a, const void* base, int64_t row_elem,
                                             int64_t w0, int64_t w1, int lane, F&& fn) {
     constexpr int E = 16 / ES;
     if (a.vec) {
         const uint4* rp = reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(base) +
                                                          row_elem * ES);
-        for (int64_t base = w0; base < w1; base += 32 * kDepth) {
-            uint4 r[kDepth];
+        for (int64_t base = w0; base < w1; base += 32 * D) {
+            uint4 r[D];
 #pragma unroll
-            for (int k = 0; k < kDepth; ++k) {
+            for (int k = 0; k < D; ++k) {
                 const int64_t idx = base + k * 32 + lane;
                 if (idx < w1)
                     r[k] = ld_stream(rp + idx);
             }
 #pragma unroll
-            for (int k = 0; k < kDepth; ++k) {
+            for (int k = 0; k < D; ++k) {
                 if (base + k * 32 + lane < w1) {
                     float l[E];
 #pragma unroll
@@ -308,41 +308,101 @@ __device__ __forceinline__ float fmax_nan(float x, float y) {
     return d;
 }
 
-// One row's statistics over this warp's stretch of `base`: the warp's
-// maximum and S = sum 2^((l - max) c) against it; bad when the stretch holds
-// a NaN or +inf.  Per unit: its maximum (NaN-propagating), a rescale when the
+// A lane's running row statistics: its maximum mx and the compensated sum
+// (sm, sc) of 2^((l - mx) c); bad once a NaN or +inf was seen.
+struct LaneStats {
+    float mx = -INFINITY, sm = 0.f, sc = 0.f;
+    bool bad = false;
+};
+
+// One unit of n entries: its maximum (NaN-propagating), a rescale when the
 // lane's maximum grows, then the unit's terms against the lane maximum.
-template <int ES>
+__device__ __forceinline__ void lane_update(LaneStats& st, const float* l, int n, float c) {
+    float vm = l[0];
+    for (int t = 1; t < n; ++t)
+        vm = fmax_nan(vm, l[t]);
+    if (vm != vm || vm == INFINITY) {
+        st.bad = true;
+        return;
+    }
+    if (vm == -INFINITY)  // weights 0
+        return;
+    if (vm > st.mx) {
+        const float r = ex2((st.mx - vm) * c);
+        st.sm *= r;
+        st.sc *= r;
+        st.mx = vm;
+    }
+    float vs = 0.f;
+    for (int t = 0; t < n; ++t)
+        vs += ex2((l[t] - st.mx) * c);
+    acc_add(st.sm, st.sc, vs);
+}
+
+// The warp's maximum and S = sum 2^((l - max) c) against it, from its lanes.
+__device__ __forceinline__ void warp_finish(const LaneStats& st, float c, float& wmx, float& wsm,
+                                            bool& wbad) {
+    wmx = warp_max(st.mx);
+    const float s = (st.mx > -INFINITY) ? (st.sm - st.sc) * ex2((st.mx - wmx) * c) : 0.f;
+    wsm = warp_sum(s);
+    wbad = __any_sync(kFull, st.bad);
+}
+
+// One row's statistics over this warp's stretch of `base`, D loads in flight
+// per lane.
+template <int ES, int D>
 __device__ __forceinline__ void warp_row_stats(const TArgs& a, const void* base, int64_t re,
                                                int64_t w0, int64_t w1, int lane, float c,
                                                float& wmx, float& wsm, bool& wbad) {
-    float mx = -INFINITY, sm = 0.f, sc = 0.f;
-    bool bad = false;
-    visit_units<ES>(a, base, re, w0, w1, lane, [&](const float* l, int n) {
-        float vm = l[0];
-        for (int t = 1; t < n; ++t)
-            vm = fmax_nan(vm, l[t]);
-        if (vm != vm || vm == INFINITY) {
-            bad = true;
-            return;
+    LaneStats st;
+    visit_units<ES, D>(a, base, re, w0, w1, lane,
+                       [&](const float* l, int n) { lane_update(st, l, n, c); });
+    warp_finish(st, c, wmx, wsm, wbad);
+}
+
+// The target row and the draft row together (vector path): both rows' units
+// come in one loop, D deep each, so a lane has 2 D loads in flight.  A lane
+// visits its units in the same order as warp_row_stats, so the statistics are
+// the same bits as two separate passes.
+template <int ES, int D>
+__device__ __forceinline__ void warp_row_stats_pair(const void* tbase, int64_t tre,
+                                                    const void* dbase, int64_t dre, int64_t w0,
+                                                    int64_t w1, int lane, float c, float cd,
+                                                    float& wmx, float& wsm, bool& wbad,
+                                                    float& dmx, float& dsm, bool& dbad) {
+    constexpr int E = 16 / ES;
+    const uint4* tp = reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(tbase) +
+                                                     tre * ES);
+    const uint4* dp = reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(dbase) +
+                                                     dre * ES);
+    LaneStats st, sd;
+    for (int64_t base = w0; base < w1; base += 32 * D) {
+        uint4 rt[D], rd[D];
+#pragma unroll
+        for (int k = 0; k < D; ++k) {
+            const int64_t idx = base + k * 32 + lane;
+            if (idx < w1) {
+                rt[k] = ld_stream(tp + idx);
+                rd[k] = ld_stream(dp + idx);
+            }
         }
-        if (vm == -INFINITY)  // weights 0
-            return;
-        if (vm > mx) {
-            const float r = ex2((mx - vm) * c);
-            sm *= r;
-            sc *= r;
-            mx = vm;
+#pragma unroll
+        for (int k = 0; k < D; ++k) {
+            if (base + k * 32 + lane < w1) {
+                float l[E];
+#pragma unroll
+                for (int t = 0; t < E; ++t)
+                    l[t] = vec_entry<ES>(rt[k], t);
+                lane_update(st, l, E, c);
+#pragma unroll
+                for (int t = 0; t < E; ++t)
+                    l[t] = vec_entry<ES>(rd[k], t);
+                lane_update(sd, l, E, cd);
+            }
         }
-        float vs = 0.f;
-        for (int t = 0; t < n; ++t)
-            vs += ex2((l[t] - mx) * c);
-        acc_add(sm, sc, vs);
-    });
-    wmx = warp_max(mx);
-    const float s = (mx > -INFINITY) ? (sm - sc) * ex2((mx - wmx) * c) : 0.f;
-    wsm = warp_sum(s);
-    wbad = __any_sync(kFull, bad);
+    }
+    warp_finish(st, c, wmx, wsm, wbad);
+    warp_finish(sd, cd, dmx, dsm, dbad);
 }
 
 // DL: draft logits instead of draft probabilities (q_i = softmax(d_i / T_d),
@@ -358,6 +418,10 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
     constexpr int MC = TR ? kMaxC : sv::kMaxCluster;  // largest cluster
     constexpr int HB = TR ? kBins : 1;                // histogram bins held
     constexpr int HC = TR ? kMaxC : 1;
+    // row pass: loads in flight per lane and row (a target row alone, or the
+    // target and draft rows together: deeper pairs spill registers)
+    constexpr int DA = (DL && !TR) ? 8 : kDepth;
+    constexpr int DP = 4;
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = (int)cluster.block_rank();
     const int b = (int)(blockIdx.x / (unsigned)a.C);
@@ -467,11 +531,14 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
         // (partial: (max, S or -1 when bad, draft max, draft S or -1))
         float wmx, wsm, dmx = -INFINITY, dsm = 0.f;
         bool bad, dbad = false;
-        warp_row_stats<ES>(a, a.logits, re, w0, w1, lane, c, wmx, wsm, bad);
-        if constexpr (DL) {
-            if (i < K)
-                warp_row_stats<ES>(a, a.dlogits, ((int64_t)b * K + i) * V + v0, w0, w1, lane, a.cd,
-                                   dmx, dsm, dbad);
+        if (DL && i < K && a.vec) {
+            warp_row_stats_pair<ES, DP>(a.logits, re, a.dlogits, ((int64_t)b * K + i) * V + v0, w0,
+                                        w1, lane, c, a.cd, wmx, wsm, bad, dmx, dsm, dbad);
+        } else {
+            warp_row_stats<ES, DA>(a, a.logits, re, w0, w1, lane, c, wmx, wsm, bad);
+            if (DL && i < K)
+                warp_row_stats<ES, DA>(a, a.dlogits, ((int64_t)b * K + i) * V + v0, w0, w1, lane,
+                                       a.cd, dmx, dsm, dbad);
         }
         const int s1 = exchange(make_float4(wmx, bad ? -1.f : wsm, dmx, dbad ? -1.f : dsm));
         if (s1 < 0) {
@@ -607,15 +674,29 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
             const float lx = load_entry(a.logits, ES, (row0 + i) * V + x);
             const bool kept = (!use_min || lx - lmax >= a.dmin) && key_of<ES>(lx) >= key_t;
             if constexpr (DL) {
-                // p~(x) E = 2^((l_x - l_max) c) and q(x) S_d = 2^((d_x - d_max) c_d),
-                // in double (one test per row): u q(x) < p~(x) <=>
-                // u 2^((d_x - d_max) c_d) E < 2^((l_x - l_max) c) S_d
+                // p~(x) E = 2^((l_x - l_max) c) and q(x) S_d = 2^((d_x - d_max) c_d), so
+                // u q(x) < p~(x) <=> u E < 2^y S_d with y = (l_x - l_max) c - (d_x - d_max) c_d.
+                // y is exact in double (products of two floats); 2^y = 2^n 2^f with one
+                // float exp2 of the fraction, so the test has one rounded exponential
+                // and no double transcendental.  Lane 0 decides, the warp follows.
                 const float dx = load_entry(a.dlogits, ES, ((int64_t)b * K + i) * V + x);
-                const double ex = kept ? exp2((double)(lx - lmax) * (double)c) : 0.0;
-                const double qn = exp2((double)(dx - dmax) * (double)a.cd);
-                if (lane == 0 && warp == 0)
-                    pdr[i] = (float)(ex / (double)E_kept);
-                if ((double)us[i] * qn * (double)E_kept < ex * (double)dS)
+                int acc = 0;
+                if (lane == 0) {
+                    if (!kept || lx == -INFINITY) {
+                        acc = 0;  // p~(x) = 0
+                    } else if (dx == -INFINITY) {
+                        acc = 1;  // q(x) = 0 < p~(x)
+                    } else {
+                        double y = (double)(lx - lmax) * (double)c - (double)(dx - dmax) * (double)a.cd;
+                        y = fmin(fmax(y, -4000.0), 4000.0);  // beyond: 2^y is 0 or inf in double
+                        const double n = floor(y);
+                        const float m = exp2f((float)(y - n));
+                        acc = (double)us[i] * (double)E_kept < ldexp((double)m * (double)dS, (int)n);
+                    }
+                    if (warp == 0)
+                        pdr[i] = kept ? __fdiv_rn(ex2((lx - lmax) * c), E_kept) : 0.f;
+                }
+                if (__shfl_sync(kFull, acc, 0))
                     continue;  // accepted
             } else {
                 const float ex = kept ? ex2((lx - lmax) * c) : 0.f;
@@ -724,10 +805,53 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
         };
         float cum_before = 0.f, Sw = 0.f, t = 0.f;
         int owner = -1;
+        // draft logits, vector path: the draw's row pair (or the target row
+        // alone for the bonus row and the fallback) stays packed in registers,
+        // eight units deep; the weights are the bits unit_weights gives
+        const auto unit_weights_raw = [&](const uint4& lr, const uint4& dr, bool two) -> float {
+            float sum = 0.f;
+#pragma unroll
+            for (int t = 0; t < E; ++t) {
+                const float ev = kept_w(vec_entry<ES>(lr, t));
+                sum += two ? fmaxf(ev - ex2((vec_entry<ES>(dr, t) - dmax) * a.cd) * rq, 0.f) : ev;
+            }
+            return sum;
+        };
         for (int round = 0; round < 2; ++round) {
             float wt = 0.f, wtc = 0.f, cpart = 0.f;
             bool badq = false;
-            for (int64_t st0 = 0; st0 < nsub; st0 += kDepth) {
+            if constexpr (DL) if (a.vec) {
+                constexpr int DD = 8;
+                const bool two = resid && !fallback;
+                for (int64_t st0 = 0; st0 < nsub; st0 += DD) {
+                    uint4 lr[DD], dr[DD];
+#pragma unroll
+                    for (int k = 0; k < DD; ++k) {
+                        const int64_t ui = w0 + (st0 + k) * 32 + lane;
+                        if (st0 + k < nsub && ui < w1) {
+                            lr[k] = ld_stream(rp + ui);
+                            if (two)
+                                dr[k] = ld_stream(dp + ui);
+                        }
+                    }
+#pragma unroll
+                    for (int k = 0; k < DD; ++k) {
+                        const int64_t st = st0 + k;
+                        if (st >= nsub)
+                            break;
+                        if (w0 + st * 32 + lane < w1)
+                            cpart += unit_weights_raw(lr[k], dr[k], two);
+                        if ((st + 1) % g == 0 || st + 1 == nsub) {  // a chunk ends here
+                            const float ct = warp_sum(cpart);
+                            cpart = 0.f;
+                            if (lane == 0)
+                                ctot[warp][st / g] = ct;
+                            acc_add(wt, wtc, ct);
+                        }
+                    }
+                }
+            }
+            for (int64_t st0 = 0; st0 < ((DL && a.vec) ? 0 : nsub); st0 += kDepth) {
                 float l[kDepth][E], qv[kDepth][E];
                 bool have[kDepth];
 #pragma unroll
