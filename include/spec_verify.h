@@ -258,7 +258,8 @@ int spec_verify_get_plan_draft_logits(sv_ctx* ctx, int B, int K, int64_t V, int 
 
 /* Its planner as a pure host function (no CUDA call), for tests: the
  * truncated planner when filters is 1; without filters clusters of up to 16
- * CTAs (capped by max_cluster), four resident 128-thread CTAs per SM. */
+ * CTAs (capped by max_cluster), seven resident 128-thread CTAs per SM (four
+ * with a filter on). */
 int spec_verify_plan_draft_logits_for(int num_sms, int max_cluster, int B, int K, int64_t V,
                                       int logits_dtype, int filters, int ovr_cluster,
                                       sv_plan* out);

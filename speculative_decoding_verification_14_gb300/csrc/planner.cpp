@@ -180,7 +180,7 @@ extern "C" int spec_verify_plan_truncated_for(int num_sms, int max_cluster, int 
 
 // Verification with draft logits: the truncated kernel's mapping when a
 // filter is on; without filters the kernel holds no histograms, so clusters
-// may grow to 16 CTAs (four resident CTAs per SM either way).
+// may grow to 16 CTAs and seven CTAs fit on an SM (72 registers a thread).
 extern "C" int spec_verify_plan_draft_logits_for(int num_sms, int max_cluster, int B, int K,
                                                  int64_t V, int logits_dtype, int filters,
                                                  int ovr_cluster, sv_plan* out) {

@@ -23,7 +23,7 @@ constexpr int kGreedyDepth = 8;         // greedy kernel: 16-byte loads in fligh
 constexpr int kGreedyCtasPerSM = 8;     // greedy kernel: resident 128-thread CTAs per SM (launch bounds)
 constexpr int kTruncCtasPerSM = 4;      // truncated-target kernel: resident CTAs per SM (launch bounds)
 constexpr int kTruncMaxCluster = 8;     // truncated-target kernel: largest cluster (shared histograms)
-constexpr int kDraftCtasPerSM = 4;      // draft-logit kernel without filters: resident CTAs per SM (launch bounds)
+constexpr int kDraftCtasPerSM = 7;      // draft-logit kernel without filters: resident CTAs per SM (launch bounds)
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }

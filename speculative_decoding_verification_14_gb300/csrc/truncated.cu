@@ -264,48 +264,61 @@ __device__ __forceinline__ void visit(const TArgs& a, int64_t row_elem, int64_t 
     }
 }
 
-// Calls fn(l, n) for every unit of this warp's stretch of a row of `base`
-// (the target or the draft logits): a 16-byte vector of E = 16/ES entries
-// (vector path) or one entry (n = 1, element path).
-template <int ES, int D, typename F>
-__device__ __forceinline__ void visit_units(const TArgs& a, const void* base, int64_t row_elem,
-                                            int64_t w0, int64_t w1, int lane, F&& fn) {
-    constexpr int E = 16 / ES;
-    if (a.vec) {
-        const uint4* rp = reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(base) +
-                                                         row_elem * ES);
-        for (int64_t base = w0; base < w1; base += 32 * D) {
-            uint4 r[D];
-#pragma unroll
-            for (int k = 0; k < D; ++k) {
-                const int64_t idx = base + k * 32 + lane;
-                if (idx < w1)
-                    r[k] = ld_stream(rp + idx);
-            }
-#pragma unroll
-            for (int k = 0; k < D; ++k) {
-                if (base + k * 32 + lane < w1) {
-                    float l[E];
-#pragma unroll
-                    for (int t = 0; t < E; ++t)
-                        l[t] = vec_entry<ES>(r[k], t);
-                    fn(l, E);
-                }
-            }
-        }
-    } else {
-        for (int64_t e = w0 + lane; e < w1; e += 32) {
-            float l[E];
-            l[0] = load_entry(base, ES, row_elem + e);
-            fn(l, 1);
-        }
-    }
-}
-
 __device__ __forceinline__ float fmax_nan(float x, float y) {
     float d;
     asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(x), "f"(y));
     return d;
+}
+
+// ------------------------------------------------------ packed vectors -----
+// A 16-byte vector of E = 16/ES logits taken with packed instructions: the
+// NaN-propagating maximum (max.NaN.bf16x2 for bf16), l - m with a bf16
+// operand widened exactly inside the subtraction (add.rn.f32.bf16), and f32x2
+// multiplies and adds.  Entry 2h and 2h + 1 form pair h (the low and high
+// halves of word h for bf16), the order vec_entry uses.
+
+__device__ __forceinline__ uint32_t bf16x2_max_nan(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// l - m for the two bf16 entries of a 32-bit word (nm = -m), each rounded once
+__device__ __forceinline__ float2 bf16x2_minus(uint32_t w, float nm) {
+    float lo, hi;
+    asm("{\n\t.reg .b16 l, h;\n\t"
+        "mov.b32 {l, h}, %2;\n\t"
+        "add.rn.f32.bf16 %0, l, %3;\n\t"
+        "add.rn.f32.bf16 %1, h, %3;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(w), "f"(nm));
+    return make_float2(lo, hi);
+}
+
+template <int ES>
+__device__ __forceinline__ float vec_max(const uint4& w) {
+    if constexpr (ES == 2) {
+        const uint32_t m = bf16x2_max_nan(bf16x2_max_nan(w.x, w.y), bf16x2_max_nan(w.z, w.w));
+        return fmax_nan(__uint_as_float(m << 16), __uint_as_float(m & 0xffff0000u));
+    } else {
+        return fmax_nan(fmax_nan(__uint_as_float(w.x), __uint_as_float(w.y)),
+                        fmax_nan(__uint_as_float(w.z), __uint_as_float(w.w)));
+    }
+}
+
+// d[h] = (entry 2h - m, entry 2h + 1 - m), nm = -m
+template <int ES>
+__device__ __forceinline__ void vec_minus(const uint4& w, float nm, float2 (&d)[8 / ES]) {
+    if constexpr (ES == 2) {
+        d[0] = bf16x2_minus(w.x, nm);
+        d[1] = bf16x2_minus(w.y, nm);
+        d[2] = bf16x2_minus(w.z, nm);
+        d[3] = bf16x2_minus(w.w, nm);
+    } else {
+        const float2 n2 = make_float2(nm, nm);
+        d[0] = __fadd2_rn(make_float2(__uint_as_float(w.x), __uint_as_float(w.y)), n2);
+        d[1] = __fadd2_rn(make_float2(__uint_as_float(w.z), __uint_as_float(w.w)), n2);
+    }
 }
 
 // A lane's running row statistics: its maximum mx and the compensated sum
@@ -315,28 +328,22 @@ struct LaneStats {
     bool bad = false;
 };
 
-// One unit of n entries: its maximum (NaN-propagating), a rescale when the
-// lane's maximum grows, then the unit's terms against the lane maximum.
-__device__ __forceinline__ void lane_update(LaneStats& st, const float* l, int n, float c) {
-    float vm = l[0];
-    for (int t = 1; t < n; ++t)
-        vm = fmax_nan(vm, l[t]);
-    if (vm != vm || vm == INFINITY) {
+// One entry (element path): a rescale when it lies above the lane's maximum,
+// then its term against the lane maximum.
+__device__ __forceinline__ void lane_update_one(LaneStats& st, float l, float c) {
+    if (l != l || l == INFINITY) {
         st.bad = true;
         return;
     }
-    if (vm == -INFINITY)  // weights 0
+    if (l == -INFINITY)  // weight 0
         return;
-    if (vm > st.mx) {
-        const float r = ex2((st.mx - vm) * c);
-        st.sm *= r;
-        st.sc *= r;
-        st.mx = vm;
+    if (l > st.mx) {
+        const float f = ex2((st.mx - l) * c);
+        st.sm *= f;
+        st.sc *= f;
+        st.mx = l;
     }
-    float vs = 0.f;
-    for (int t = 0; t < n; ++t)
-        vs += ex2((l[t] - st.mx) * c);
-    acc_add(st.sm, st.sc, vs);
+    acc_add(st.sm, st.sc, ex2((l - st.mx) * c));
 }
 
 // The warp's maximum and S = sum 2^((l - max) c) against it, from its lanes.
@@ -348,58 +355,144 @@ __device__ __forceinline__ void warp_finish(const LaneStats& st, float c, float&
     wbad = __any_sync(kFull, st.bad);
 }
 
-// One row's statistics over this warp's stretch of `base`, D loads in flight
-// per lane.
+// A batch of loaded units (ok[k]: unit k was loaded): the batch maximum, a
+// rescale when it lies above the lane's maximum, then every term against the
+// lane maximum with packed arithmetic and two packed accumulators.  Terms stay
+// at most 1, as with one unit at a time, but the maximum is compared once per
+// batch.
+template <int ES, int D>
+__device__ __forceinline__ void lane_update_batch(LaneStats& st, const uint4 (&r)[D],
+                                                  const bool (&ok)[D], float c) {
+    float bm = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < D; ++k)
+        if (ok[k])
+            bm = fmax_nan(bm, vec_max<ES>(r[k]));
+    if (bm != bm || bm == INFINITY) {
+        st.bad = true;
+        return;
+    }
+    if (bm == -INFINITY)  // weights 0
+        return;
+    if (bm > st.mx) {
+        const float f = ex2((st.mx - bm) * c);
+        st.sm *= f;
+        st.sc *= f;
+        st.mx = bm;
+    }
+    const float2 c2 = make_float2(c, c);
+    const float nm = -st.mx;
+    float2 s0 = make_float2(0.f, 0.f), s1 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < D; ++k) {
+        if (ok[k]) {
+            float2 d[8 / ES];
+            vec_minus<ES>(r[k], nm, d);
+#pragma unroll
+            for (int h = 0; h < 8 / ES; ++h) {
+                const float2 y = __fmul2_rn(d[h], c2);
+                const float2 e = make_float2(ex2(y.x), ex2(y.y));
+                if (h & 1)
+                    s1 = __fadd2_rn(s1, e);
+                else
+                    s0 = __fadd2_rn(s0, e);
+            }
+        }
+    }
+    const float2 t = __fadd2_rn(s0, s1);
+    acc_add(st.sm, st.sc, t.x + t.y);
+}
+
+// Loads of one batch: units b0 + k*32 + lane (k < D) of the stretch ending at
+// w1; ok[k] tells which exist.
+template <int D>
+__device__ __forceinline__ void load_batch(const uint4* rp, int64_t b0, int64_t w1, int lane,
+                                           uint4 (&r)[D], bool (&ok)[D]) {
+#pragma unroll
+    for (int k = 0; k < D; ++k) {
+        const int64_t idx = b0 + k * 32 + lane;
+        ok[k] = idx < w1;
+        if (ok[k])
+            r[k] = ld_stream(rp + idx);
+    }
+}
+
+// L2 lookahead for the batch loops: lane 0 asks L2 for the batch `kAhead`
+// batches past b0 (one bulk prefetch of its contiguous units), so the loads
+// of a batch find their lines in L2 instead of waiting a full DRAM latency.
+// No registers are held for it, and nothing past the stretch is touched.
+constexpr int kAhead = 3;
+
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+template <int D>
+__device__ __forceinline__ void prefetch_batch(const uint4* rp, int64_t b, int64_t w1, int lane) {
+    if (lane == 0 && b < w1) {
+        const int64_t n = w1 - b < 32 * D ? w1 - b : 32 * D;
+        prefetch_l2(rp + b, (uint32_t)(n * 16));
+    }
+}
+
+// The prologue: batches 1 .. kAhead - 1 of the stretch.
+template <int D>
+__device__ __forceinline__ void prefetch_start(const uint4* rp, int64_t w0, int64_t w1, int lane) {
+#pragma unroll
+    for (int n = 1; n < kAhead; ++n)
+        prefetch_batch<D>(rp, w0 + (int64_t)n * 32 * D, w1, lane);
+}
+
+// One row's statistics over this warp's stretch of `base` (vector path; the
+// element path takes one entry at a time), D loads in flight per lane.
 template <int ES, int D>
 __device__ __forceinline__ void warp_row_stats(const TArgs& a, const void* base, int64_t re,
                                                int64_t w0, int64_t w1, int lane, float c,
                                                float& wmx, float& wsm, bool& wbad) {
     LaneStats st;
-    visit_units<ES, D>(a, base, re, w0, w1, lane,
-                       [&](const float* l, int n) { lane_update(st, l, n, c); });
+    if (a.vec) {
+        const uint4* rp = reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(base) +
+                                                         re * ES);
+        prefetch_start<D>(rp, w0, w1, lane);
+        for (int64_t b0 = w0; b0 < w1; b0 += 32 * D) {
+            prefetch_batch<D>(rp, b0 + kAhead * 32 * D, w1, lane);
+            uint4 r[D];
+            bool ok[D];
+            load_batch<D>(rp, b0, w1, lane, r, ok);
+            lane_update_batch<ES, D>(st, r, ok, c);
+        }
+    } else {
+        for (int64_t e = w0 + lane; e < w1; e += 32) {
+            lane_update_one(st, load_entry(base, ES, re + e), c);
+        }
+    }
     warp_finish(st, c, wmx, wsm, wbad);
 }
 
 // The target row and the draft row together (vector path): both rows' units
-// come in one loop, D deep each, so a lane has 2 D loads in flight.  A lane
-// visits its units in the same order as warp_row_stats, so the statistics are
-// the same bits as two separate passes.
+// come in one loop, D deep each, so a lane has 2 D loads in flight.
 template <int ES, int D>
 __device__ __forceinline__ void warp_row_stats_pair(const void* tbase, int64_t tre,
                                                     const void* dbase, int64_t dre, int64_t w0,
                                                     int64_t w1, int lane, float c, float cd,
                                                     float& wmx, float& wsm, bool& wbad,
                                                     float& dmx, float& dsm, bool& dbad) {
-    constexpr int E = 16 / ES;
     const uint4* tp = reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(tbase) +
                                                      tre * ES);
     const uint4* dp = reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(dbase) +
                                                      dre * ES);
     LaneStats st, sd;
-    for (int64_t base = w0; base < w1; base += 32 * D) {
+    prefetch_start<D>(tp, w0, w1, lane);
+    prefetch_start<D>(dp, w0, w1, lane);
+    for (int64_t b0 = w0; b0 < w1; b0 += 32 * D) {
+        prefetch_batch<D>(tp, b0 + kAhead * 32 * D, w1, lane);
+        prefetch_batch<D>(dp, b0 + kAhead * 32 * D, w1, lane);
         uint4 rt[D], rd[D];
-#pragma unroll
-        for (int k = 0; k < D; ++k) {
-            const int64_t idx = base + k * 32 + lane;
-            if (idx < w1) {
-                rt[k] = ld_stream(tp + idx);
-                rd[k] = ld_stream(dp + idx);
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < D; ++k) {
-            if (base + k * 32 + lane < w1) {
-                float l[E];
-#pragma unroll
-                for (int t = 0; t < E; ++t)
-                    l[t] = vec_entry<ES>(rt[k], t);
-                lane_update(st, l, E, c);
-#pragma unroll
-                for (int t = 0; t < E; ++t)
-                    l[t] = vec_entry<ES>(rd[k], t);
-                lane_update(sd, l, E, cd);
-            }
-        }
+        bool ok[D];
+        load_batch<D>(tp, b0, w1, lane, rt, ok);
+        load_batch<D>(dp, b0, w1, lane, rd, ok);
+        lane_update_batch<ES, D>(st, rt, ok, c);
+        lane_update_batch<ES, D>(sd, rd, ok, cd);
     }
     warp_finish(st, c, wmx, wsm, wbad);
     warp_finish(sd, cd, dmx, dsm, dbad);
@@ -420,8 +513,8 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
     constexpr int HC = TR ? kMaxC : 1;
     // row pass: loads in flight per lane and row (a target row alone, or the
     // target and draft rows together: deeper pairs spill registers)
-    constexpr int DA = (DL && !TR) ? 8 : kDepth;
-    constexpr int DP = 4;
+    constexpr int DA = (DL && !TR) ? 4 : kDepth;
+    constexpr int DP = (DL && !TR) ? 2 : 4;
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = (int)cluster.block_rank();
     const int b = (int)(blockIdx.x / (unsigned)a.C);
@@ -807,7 +900,39 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
         int owner = -1;
         // draft logits, vector path: the draw's row pair (or the target row
         // alone for the bonus row and the fallback) stays packed in registers,
-        // eight units deep; the weights are the bits unit_weights gives
+        // DD units deep.  With filters the weights are the bits unit_weights
+        // gives (the locate re-derives them that way); without filters every
+        // entry is kept, and both the totals pass and the locate take the
+        // packed vec_weights below.
+        const float2 c2 = make_float2(c, c), cd2 = make_float2(a.cd, a.cd);
+        const float2 nrq2 = make_float2(-rq, -rq);
+        const float nl = -lmax, nd = -dmax;
+        // w[t] = max(0, 2^((l - l_max) c) - 2^((d - d_max) c_d) E / S_d) (two), or
+        // 2^((l - l_max) c); returns their sum in entry order
+        const auto vec_weights = [&](const uint4& lr, const uint4& dr, bool two,
+                                     float (&w)[E]) -> float {
+            float2 dl[E / 2], dd[E / 2];
+            vec_minus<ES>(lr, nl, dl);
+            if (two)
+                vec_minus<ES>(dr, nd, dd);
+            float sum = 0.f;
+#pragma unroll
+            for (int h = 0; h < E / 2; ++h) {
+                const float2 y = __fmul2_rn(dl[h], c2);
+                float2 ev = make_float2(ex2(y.x), ex2(y.y));
+                if (two) {
+                    const float2 yd = __fmul2_rn(dd[h], cd2);
+                    ev = __ffma2_rn(make_float2(ex2(yd.x), ex2(yd.y)), nrq2, ev);
+                    ev.x = fmaxf(ev.x, 0.f);
+                    ev.y = fmaxf(ev.y, 0.f);
+                }
+                w[2 * h] = ev.x;
+                w[2 * h + 1] = ev.y;
+                sum += ev.x;
+                sum += ev.y;
+            }
+            return sum;
+        };
         const auto unit_weights_raw = [&](const uint4& lr, const uint4& dr, bool two) -> float {
             float sum = 0.f;
 #pragma unroll
@@ -821,9 +946,17 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
             float wt = 0.f, wtc = 0.f, cpart = 0.f;
             bool badq = false;
             if constexpr (DL) if (a.vec) {
-                constexpr int DD = 8;
+                constexpr int DD = TR ? 8 : 4;
                 const bool two = resid && !fallback;
+                // the steps st0 .. st0 + DD - 1 are units w0 + st * 32 + lane: one
+                // contiguous batch of DD * 32 units, as in the row loops
+                prefetch_start<DD>(rp, w0, w1, lane);
+                if (two)
+                    prefetch_start<DD>(dp, w0, w1, lane);
                 for (int64_t st0 = 0; st0 < nsub; st0 += DD) {
+                    prefetch_batch<DD>(rp, w0 + (st0 + kAhead * DD) * 32, w1, lane);
+                    if (two)
+                        prefetch_batch<DD>(dp, w0 + (st0 + kAhead * DD) * 32, w1, lane);
                     uint4 lr[DD], dr[DD];
 #pragma unroll
                     for (int k = 0; k < DD; ++k) {
@@ -839,8 +972,14 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
                         const int64_t st = st0 + k;
                         if (st >= nsub)
                             break;
-                        if (w0 + st * 32 + lane < w1)
-                            cpart += unit_weights_raw(lr[k], dr[k], two);
+                        if (w0 + st * 32 + lane < w1) {
+                            if constexpr (TR) {
+                                cpart += unit_weights_raw(lr[k], dr[k], two);
+                            } else {
+                                float w[E];
+                                cpart += vec_weights(lr[k], dr[k], two, w);
+                            }
+                        }
                         if ((st + 1) % g == 0 || st + 1 == nsub) {  // a chunk ends here
                             const float ct = warp_sum(cpart);
                             cpart = 0.f;
@@ -955,8 +1094,19 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
                 for (int k = 0; k < E; ++k)
                     w[k] = 0.f;
                 const int64_t ui = w0 + st * 32 + lane;
-                if (load_unit(st, l, qv))
+                bool packed = false;  // the totals pass took vec_weights
+                if constexpr (DL && !TR)
+                    packed = a.vec != 0;
+                if (packed) {
+                    if (ui < w1) {
+                        const bool two = resid && !fallback;
+                        const uint4 lr = ld_stream(rp + ui);
+                        const uint4 dr = two ? ld_stream(dp + ui) : lr;
+                        lt = vec_weights(lr, dr, two, w);
+                    }
+                } else if (load_unit(st, l, qv)) {
                     lt = unit_weights(l, qv, w, dummy);
+                }
                 int lpos = -1;
                 for (int k = 0; k < U; ++k)
                     if (w[k] > 0.f)

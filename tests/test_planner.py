@@ -134,16 +134,18 @@ def test_draft_logits_plan_invariants(sv, B, K, V, dtype, filters):
     assert slice_ % 8 == 0 and slice_ * C >= V and slice_ * (C - 1) < V + 8 * C
     assert p["grid"] == B * C and p["threads"] == 128
     assert p["bulk_copy"] == int((V * es) % 16 == 0)
-    if B <= 152 * 4:  # four resident CTAs per SM
-        assert B * C <= 152 * 4
+    per_sm = 4 if filters else 7  # resident CTAs per SM (launch bounds)
+    if B <= 152 * per_sm:
+        assert B * C <= 152 * per_sm
     # with a filter on, the plan is the truncated kernel's
     if filters:
         assert p == sv.spec_verify_plan_truncated_for(152, 16, B, K, V, dtype, 0)[1]
 
 
 def test_draft_logits_workload_plans(sv):
-    assert dplan(sv, 256, 7, 128256, 1, 0)[1]["cluster"] == 2
-    assert dplan(sv, 64, 3, 151936, 1, 0)[1]["cluster"] == 8
+    assert dplan(sv, 256, 7, 128256, 1, 0)[1]["cluster"] == 4
+    assert dplan(sv, 256, 7, 128256, 1, 1)[1]["cluster"] == 2
+    assert dplan(sv, 64, 3, 151936, 1, 0)[1]["cluster"] == 16
     assert dplan(sv, 8, 4, 32000, 1, 0)[1]["cluster"] == 16
     assert dplan(sv, 8, 4, 32000, 1, 1)[1]["cluster"] == 8
     assert dplan(sv, 8, 4, 32000, 1, 0, dev=dict(GB300, max_cluster=8))[1]["cluster"] == 8
