@@ -408,12 +408,15 @@ __device__ __forceinline__ void lane_update_batch(LaneStats& st, const uint4 (&r
 template <int D>
 __device__ __forceinline__ void load_batch(const uint4* rp, int64_t b0, int64_t w1, int lane,
                                            uint4 (&r)[D], bool (&ok)[D]) {
+    // 32-bit offsets inside the batch (a stretch holds far fewer than 2^31 units)
+    const uint4* bp = rp + b0;
+    const int64_t rem64 = w1 - b0;
+    const int rem = rem64 < 32 * D ? (int)rem64 : 32 * D;
 #pragma unroll
     for (int k = 0; k < D; ++k) {
-        const int64_t idx = b0 + k * 32 + lane;
-        ok[k] = idx < w1;
+        ok[k] = k * 32 + lane < rem;
         if (ok[k])
-            r[k] = ld_stream(rp + idx);
+            r[k] = ld_stream(bp + (k * 32 + lane));
     }
 }
 
@@ -422,6 +425,10 @@ __device__ __forceinline__ void load_batch(const uint4* rp, int64_t b0, int64_t 
 // of a batch find their lines in L2 instead of waiting a full DRAM latency.
 // No registers are held for it, and nothing past the stretch is touched.
 constexpr int kAhead = 3;
+
+__device__ __forceinline__ void prefetch_line_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
 
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
@@ -619,6 +626,18 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
     uint32_t key_t = 0;                   // top-p: kept keys are >= key_t
     for (int i = 0; i <= K && state == SV_OK; ++i) {
         const int64_t re = (row0 + i) * V + v0;  // first element of this CTA's slice of row i
+        // the test's two values (l_x and the draft's d_x or q(x)) sit at random
+        // positions: ask L2 for them now, so the test after the exchange does
+        // not wait a DRAM latency
+        if (i < K && lane == 0) {
+            const int64_t xi = (int64_t)xs[i];
+            prefetch_line_l2(static_cast<const unsigned char*>(a.logits) + ((row0 + i) * V + xi) * ES);
+            if constexpr (DL)
+                prefetch_line_l2(static_cast<const unsigned char*>(a.dlogits) +
+                                 (((int64_t)b * K + i) * V + xi) * ES);
+            else
+                prefetch_line_l2(a.q + ((int64_t)b * K + i) * V + xi);
+        }
         // ---- A: row maximum and S = sum 2^((l - l_max) c); with draft
         // logits, the same for the draft row d_i at c_d (i < K) ----
         // (partial: (max, S or -1 when bad, draft max, draft S or -1))
@@ -650,15 +669,19 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
             }
             m = warp_max(m);
             md = warp_max(md);
-            float S = 0.f, Sc = 0.f, Sd = 0.f, Sdc = 0.f;
-            for (int p = 0; p < P; ++p) {
+            // each lane rescales its partials, one butterfly sums them (the
+            // same order in every warp)
+            float S = 0.f, Sd = 0.f;
+            for (int p = lane; p < P; p += 32) {
                 const float4 q4 = part[s1][p];
                 if (q4.x > -INFINITY)
-                    acc_add(S, Sc, q4.y * ex2((q4.x - m) * c));
+                    S += q4.y * ex2((q4.x - m) * c);
                 if (DL && q4.z > -INFINITY)
-                    acc_add(Sd, Sdc, q4.w * ex2((q4.z - md) * a.cd));
+                    Sd += q4.w * ex2((q4.z - md) * a.cd);
             }
-            S -= Sc;
+            S = warp_sum(S);
+            if constexpr (DL)
+                Sd = warp_sum(Sd);
             if (__any_sync(kFull, bd) || !(m > -INFINITY) || (DL && i < K && !(md > -INFINITY))) {
                 state = SV_ERR_NONFINITE;
                 break;
@@ -666,7 +689,7 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
             lmax = m;
             E_kept = S;
             dmax = md;
-            dS = Sd - Sdc;
+            dS = Sd;
             if (lane == 0 && warp == 0) {
                 rsm[i] = __fdiv_rn(m, a.T);
                 rss[i] = S;
@@ -942,9 +965,11 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
             }
             return sum;
         };
+        const int g32 = (int)g;  // steps per chunk (chunk ends counted, not divided)
         for (int round = 0; round < 2; ++round) {
             float wt = 0.f, wtc = 0.f, cpart = 0.f;
             bool badq = false;
+            int gcnt = 0, chunk = 0;
             if constexpr (DL) if (a.vec) {
                 constexpr int DD = TR ? 8 : 4;
                 const bool two = resid && !fallback;
@@ -980,11 +1005,13 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
                                 cpart += vec_weights(lr[k], dr[k], two, w);
                             }
                         }
-                        if ((st + 1) % g == 0 || st + 1 == nsub) {  // a chunk ends here
+                        if (++gcnt == g32 || st + 1 == nsub) {  // chunk `chunk` ends here
                             const float ct = warp_sum(cpart);
                             cpart = 0.f;
                             if (lane == 0)
-                                ctot[warp][st / g] = ct;
+                                ctot[warp][chunk] = ct;
+                            ++chunk;
+                            gcnt = 0;
                             acc_add(wt, wtc, ct);
                         }
                     }
@@ -1004,11 +1031,13 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
                     float w[E];
                     if (have[k])
                         cpart += unit_weights(l[k], qv[k], w, badq);
-                    if ((st + 1) % g == 0 || st + 1 == nsub) {  // a chunk ends here
+                    if (++gcnt == g32 || st + 1 == nsub) {  // chunk `chunk` ends here
                         const float ct = warp_sum(cpart);
                         cpart = 0.f;
                         if (lane == 0)
-                            ctot[warp][st / g] = ct;
+                            ctot[warp][chunk] = ct;
+                        ++chunk;
+                        gcnt = 0;
                         acc_add(wt, wtc, ct);
                     }
                 }
