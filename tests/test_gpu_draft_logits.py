@@ -159,3 +159,31 @@ def test_agrees_with_the_q_kernel_fed_the_softmax():
            (r["accept_margin"] < 1e-5) | (r["sample_margin"] < 1e-5))
     assert np.array_equal(g["accept_len"][~tie], s["accept_len"][~tie])
     assert np.array_equal(g["out_tokens"][~tie], s["out_tokens"][~tie])
+
+
+@pytest.mark.parametrize("top_p,min_p", [(1.0, 0.0), (0.95, 0.05)])
+def test_telemetry_counts(top_p, min_p):
+    """The accepted-length counters of the draft-logit kernel: twice the
+    histogram of its own accepted lengths after two calls, errors in bin 0."""
+    import torch
+    v = gh.verifier()
+    inp = workloads.make_random_draft_logits(40, 5, 3000, "bf16", T=0.7, T_draft=0.9, seed=17)
+    x = inp.tokens.copy()
+    x[3, 2] = -1                                   # sequence 3 errors
+    hist = torch.zeros(inp.K + 2, dtype=torch.int32, device="cuda")
+    lg, dl = _to_dev(inp.logits, "bf16"), _to_dev(inp.dlogits, "bf16")
+    xd = torch.from_numpy(x).cuda()
+    ud = torch.from_numpy(inp.uniforms).cuda()
+    v.set_telemetry(hist)
+    try:
+        o1 = v.run_draft_logits(lg, dl, xd, ud, inp.T, inp.T_draft, top_p, min_p)
+        o2 = v.run_draft_logits(lg, dl, xd, ud, inp.T, inp.T_draft, top_p, min_p)
+        torch.cuda.synchronize()
+    finally:
+        v.set_telemetry(None)
+    v.error()
+    al1, al2 = o1["accept_len"].cpu().numpy(), o2["accept_len"].cpu().numpy()
+    assert np.array_equal(al1, al2) and al1[3] == 0
+    h = hist.cpu().numpy().astype(np.int64)
+    expect = np.bincount(al1, minlength=inp.K + 2)
+    assert np.array_equal(h, 2 * expect)
