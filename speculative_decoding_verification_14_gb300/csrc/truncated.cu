@@ -38,6 +38,17 @@
 // Threshold decisions are taken on the stored logits: min-p as
 // l - l_max >= T ln(min_p), top-p on the key, so the kept set depends on the
 // weights only through the top-p masses.
+//
+// The same kernel verifies from the drafter's LOGITS d [B, K, V] instead of q
+// (DL): [P1]'s loop forms q = softmax(d / T_d) itself.  Pass A then streams the
+// target row and the draft row together and keeps both rows' statistics; the
+// test uses q(x) S_d = 2^((d_x - d_max) c_d), and the draw's residual forms q
+// from the draft row the same way.  Without filters (TR off) B is compiled out
+// and the kernel fits seven CTAs per SM.
+//
+// Row passes load batches of 16-byte units per lane, sum them with packed
+// arithmetic (one maximum test per batch), and ask L2 for the batch three
+// ahead; the test's two values are asked into L2 when a row starts.
 #include <cuda_runtime.h>
 #include <cooperative_groups.h>
 
@@ -233,9 +244,14 @@ constexpr int kChunks = 128;  // draw: chunk totals kept per warp
 // Calls fn(l, e) for every entry of this warp's stretch of one row (e = entry
 // index within the CTA's slice), lane by lane; entries of one lane come in
 // increasing order, the lanes interleave by vector.
-template <int ES, typename F>
+template <int ES>
+__device__ __forceinline__ float vec_max(const uint4& w);  // below, with the packed helpers
+
+// (vector path) unit_may(m) tells from a unit's largest entry m whether any
+// of its entries can matter to fn; units it rules out are skipped whole.
+template <int ES, typename U, typename F>
 __device__ __forceinline__ void visit(const TArgs& a, int64_t row_elem, int64_t w0, int64_t w1,
-                                      int lane, F&& fn) {
+                                      int lane, U&& unit_may, F&& fn) {
     constexpr int E = 16 / ES;
     if (a.vec) {
         const uint4* rp = reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(a.logits) +
@@ -251,7 +267,7 @@ __device__ __forceinline__ void visit(const TArgs& a, int64_t row_elem, int64_t 
 #pragma unroll
             for (int k = 0; k < kDepth; ++k) {
                 const int64_t idx = base + k * 32 + lane;
-                if (idx < w1) {
+                if (idx < w1 && unit_may(vec_max<ES>(r[k]))) {
 #pragma unroll
                     for (int t = 0; t < E; ++t)
                         fn(vec_entry<ES>(r[k], t), idx * E + t);
@@ -708,7 +724,15 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
                 __syncthreads();
                 const int sh_hi = KEYBITS - 8 * lev;   // prefix = key >> sh_hi
                 const int sh_lo = KEYBITS - 8 * (lev + 1);
-                visit<ES>(a, re, w0, w1, lane, [&](float l, int64_t) {
+                // a unit can hold a candidate only if its largest entry passes
+                // min-p and, past the first level, its key prefix is not below
+                // the chosen one (keys order like the logits)
+                const auto unit_may = [&](float um) -> bool {
+                    if (use_min && !(um - lmax >= a.dmin))
+                        return false;
+                    return lev == 0 || (key_of<ES>(um) >> sh_hi) >= prefix;
+                };
+                visit<ES>(a, re, w0, w1, lane, unit_may, [&](float l, int64_t) {
                     if (use_min && !(l - lmax >= a.dmin))
                         return;
                     const uint32_t key = key_of<ES>(l);
