@@ -384,6 +384,18 @@ int spec_verify_run_noalloc(int device,
                             float* row_stats, float* p_draft, int32_t* status,
                             void* stream);
 
+/* Self-test of the bounded wait the kernels use for every mbarrier wait (the
+ * pages have no counterpart: a diagnostic of this library).  One thread on
+ * `device` waits on a barrier of its own through the same routine as the
+ * greedy kernel's waits; with arrive = 1 the barrier's phase is completed
+ * first and the wait succeeds at once, with arrive = 0 nothing ever completes
+ * it and the wait gives up after limit_ns.  Outputs: *completed (1 = the wait
+ * succeeded, 0 = it ran out) and *elapsed_ns (device global timer).
+ * Synchronises the device's legacy default stream.  Returns SV_OK,
+ * SV_ERR_INVALID_ARG (null outputs, limit_ns > 2e9) or SV_ERR_CUDA. */
+int spec_verify_selftest_wait(int device, unsigned long long limit_ns, int arrive,
+                              int* completed, unsigned long long* elapsed_ns);
+
 /* Release the context and everything it owns. */
 int spec_verify_destroy(sv_ctx* ctx);
 

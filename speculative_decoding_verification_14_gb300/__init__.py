@@ -123,6 +123,10 @@ def library() -> ctypes.CDLL:
                                                            ctypes.c_int64, ctypes.c_int,
                                                            ctypes.c_int, ctypes.POINTER(sv_plan)]),
             "spec_verify_set_telemetry": (ctypes.c_int, [P, P, ctypes.c_int]),
+            "spec_verify_selftest_wait": (ctypes.c_int, [ctypes.c_int, ctypes.c_ulonglong,
+                                                         ctypes.c_int,
+                                                         ctypes.POINTER(ctypes.c_int),
+                                                         ctypes.POINTER(ctypes.c_ulonglong)]),
             "spec_adapt": (ctypes.c_int, [P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                           ctypes.c_int, ctypes.c_double, ctypes.c_uint64,
                                           ctypes.POINTER(sv_adapt)]),
@@ -273,6 +277,15 @@ def spec_verify_plan_greedy_for(num_sms, max_cluster, B, K, V, dtype, ovr_cluste
     rc = library().spec_verify_plan_greedy_for(num_sms, max_cluster, B, K, V, dtype, ovr_cluster,
                                                ctypes.byref(plan))
     return rc, plan.as_dict()
+
+
+def spec_verify_selftest_wait(device: int, limit_ns: int, arrive: bool):
+    """Returns (status, completed, elapsed_ns) of the bounded-wait self-test."""
+    done = ctypes.c_int(-1)
+    el = ctypes.c_ulonglong(0)
+    rc = library().spec_verify_selftest_wait(int(device), int(limit_ns), 1 if arrive else 0,
+                                             ctypes.byref(done), ctypes.byref(el))
+    return rc, done.value, el.value
 
 
 def spec_verify_set_telemetry(ctx, hist_ptr, bins) -> int:

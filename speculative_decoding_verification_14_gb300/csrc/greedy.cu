@@ -361,7 +361,51 @@ __global__ void __launch_bounds__(kNT, 8) sv_greedy_kernel(const __grid_constant
     cluster_wait();
 }
 
+// Self-test of the bounded wait above (the routine every wait of this
+// kernel goes through): one thread waits on a barrier of its own.  With
+// `arrive` the thread first completes the barrier's phase 0, so the wait must
+// succeed at once; without it nothing ever arrives, so the wait must give up
+// once limit_ns have passed.  Nothing is in flight when it returns.
+__device__ unsigned long long sv_wait_selftest_out[2];  // completed, elapsed ns
+
+__global__ void sv_wait_selftest_kernel(unsigned long long limit_ns, int arrive) {
+    __shared__ __align__(8) unsigned long long bar;
+    mbar_init(&bar, 1);
+    if (arrive)
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&bar)) : "memory");
+    const unsigned long long t0 = now_ns();
+    const bool ok = mbar_wait_limited(&bar, 0, limit_ns);
+    sv_wait_selftest_out[0] = ok ? 1ull : 0ull;
+    sv_wait_selftest_out[1] = now_ns() - t0;
+}
+
 }  // namespace
+
+extern "C" int spec_verify_selftest_wait(int device, unsigned long long limit_ns, int arrive,
+                                         int* completed, unsigned long long* elapsed_ns) {
+    if (!completed || !elapsed_ns || limit_ns > 2000000000ull)
+        return SV_ERR_INVALID_ARG;
+    int prev = 0;
+    if (cudaGetDevice(&prev) != cudaSuccess || cudaSetDevice(device) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SV_ERR_CUDA;
+    }
+    sv_wait_selftest_kernel<<<1, 1>>>(limit_ns, arrive ? 1 : 0);
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(0);
+    unsigned long long h[2] = {0, 0};
+    if (e == cudaSuccess)
+        e = cudaMemcpyFromSymbol(h, sv_wait_selftest_out, sizeof h);
+    (void)cudaSetDevice(prev);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SV_ERR_CUDA;
+    }
+    *completed = (int)h[0];
+    *elapsed_ns = h[1];
+    return SV_OK;
+}
 
 namespace sv {
 

@@ -69,3 +69,7 @@ def test_no_cpu_fallback(sv):
         pytest.skip("a GPU is present")
     with pytest.raises(RuntimeError):
         sv.Verifier(8, 4, 1000)
+
+
+def test_wait_selftest_checks_its_arguments_before_cuda(sv):
+    assert sv.spec_verify_selftest_wait(0, 3_000_000_000, False)[0] == sv.SV_ERR_INVALID_ARG

@@ -68,3 +68,4 @@ def test_draft_logit_entry_rejects_a_null_context_without_cuda():
         sv.SV_ERR_INVALID_ARG
     assert sv.spec_verify_plan_draft_logits_for(152, 16, 1, 3, 1000, 7, 0)[0] == \
         sv.SV_ERR_INVALID_ARG
+
