@@ -187,3 +187,37 @@ def test_telemetry_counts(top_p, min_p):
     h = hist.cpu().numpy().astype(np.int64)
     expect = np.bincount(al1, minlength=inp.K + 2)
     assert np.array_equal(h, 2 * expect)
+
+
+def test_repeated_runs_are_bit_identical_and_outputs_stay_in_bounds():
+    """Two runs give the same bits; guard regions around every output keep
+    their fill (no write outside [B], [B, K+1], [B, K], [B, K+1, 2])."""
+    import torch
+    v = gh.verifier()
+    inp = workloads.make_random_draft_logits(9, 4, 3000, "bf16", T=0.8, T_draft=0.8, seed=23)
+    B, K = inp.B, inp.K
+    lg, dl = _to_dev(inp.logits, "bf16"), _to_dev(inp.dlogits, "bf16")
+    xd = torch.from_numpy(inp.tokens).cuda()
+    ud = torch.from_numpy(inp.uniforms).cuda()
+    guard = 64
+    runs = []
+    for _ in range(2):
+        fences, out = [], {}
+        for name, shape, dtype, fill in (("accept_len", (B,), torch.int32, 0x5A5A5A5A),
+                                         ("out_tokens", (B, K + 1), torch.int32, 0x5A5A5A5A),
+                                         ("accept_mask", (B, K), torch.uint8, 0xA5),
+                                         ("row_stats", (B, K + 1, 2), torch.float32, 12345.0),
+                                         ("p_draft", (B, K), torch.float32, 12345.0),
+                                         ("status", (B,), torch.int32, 0x5A5A5A5A)):
+            n = int(np.prod(shape))
+            full = torch.full((n + 2 * guard,), fill, dtype=dtype, device="cuda")
+            fences.append((name, full, n, fill))
+            out[name] = full[guard:guard + n].view(shape)
+        v.run_draft_logits(lg, dl, xd, ud, inp.T, inp.T_draft, out=out)
+        torch.cuda.synchronize()
+        for name, full, n, fill in fences:
+            assert torch.all(full[:guard] == fill) and torch.all(full[guard + n:] == fill), name
+        runs.append({k: t.cpu().numpy().copy() for k, t in out.items()})
+    for k in runs[0]:
+        np.testing.assert_array_equal(runs[0][k], runs[1][k], err_msg=k)
+    assert np.all(runs[0]["status"] == 0)
