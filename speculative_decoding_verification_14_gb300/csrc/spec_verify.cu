@@ -23,13 +23,16 @@
 //    a row, and shared memory does not grow with the vocabulary;
 //  * lanes keep a running (max, sum of exponentials) with packed f32x2
 //    arithmetic; each warp publishes one partial per row;
-//  * after one cluster barrier, every warp reads the C x warps partials through
-//    distributed shared memory, merges them in a fixed order (double-float
-//    accumulation, accurate exp2) and takes the accept/reject decision itself,
-//    so no broadcast is needed;
+//  * each warp pushes its 16-byte partial into a slot of every CTA of the
+//    cluster with st.async, completing on that CTA's exchange mbarrier (armed
+//    for the C x warps partials of the row), so no cluster barrier sits on
+//    the per-row path; the first warp of a CTA to find a row's partials
+//    complete merges them in a fixed order (double-float accumulation,
+//    accurate exp2), takes the accept/reject decision and posts it in shared
+//    memory for the CTA's other warps;
 //  * rows are consumed in order and the loop stops at the first rejection,
-//    like the pages' loop; the first chunks of the next row are already in
-//    flight while a row is decided;
+//    like the pages' loop; a warp streams the next row while the decision on
+//    the previous one is taken, and a rejection ends that stream;
 //  * the residual (or bonus) draw streams the rejected draft row through the
 //    same rings, records per-tile totals, meets the other CTAs' totals in
 //    distributed shared memory, and one warp of the owning CTA locates the
@@ -91,7 +94,6 @@ struct SvArgs {
     float c_hi, c_lo;       // log2(e)/T = c_hi + c_lo with c_lo > 0 (accurate paths)
     float c;                // log2(e)/T rounded to float (per-entry paths)
     float T;
-    unsigned long long wait_ns;
 };
 
 struct FF {  // hi + lo, see the double-float helpers below
@@ -799,6 +801,11 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
     // ---- per-warp stream through the private ring ----
     // stage indices and the consumer's phase bit advance incrementally; the
     // counters below are the same in every lane of the warp
+    //
+    // A copy into the warp's own stage depends on no other CTA and always
+    // lands, so its wait has a long fixed limit of its own (sv::kCopyWaitNs,
+    // five times the limit on waits for other CTAs); nothing at run time
+    // shortens it.
     uint32_t st_issue = 0, st_wait = 0, ph_wait = 0;
     int in_flight = 0;
     bool timed_out = false;
@@ -815,7 +822,7 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
         ++in_flight;
     };
     auto wait_next = [&]() -> const uint4* {
-        if (!mbar_wait_bounded(&wbar[st_wait], ph_wait, a.wait_ns))
+        if (!mbar_wait_bounded(&wbar[st_wait], ph_wait, sv::kCopyWaitNs))
             timed_out = true;
         return reinterpret_cast<const uint4*>(ring + st_wait * kChunkBytes);
     };
@@ -960,7 +967,7 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
     auto wait_partials = [&](int par) {
         // (exchange waits outlast a peer's own bounded ring waits, so a late
         // peer's push lands before anyone gives up on it)
-        if (!mbar_wait_bounded(&xbar[par], (xph >> par) & 1u, 3 * a.wait_ns))
+        if (!mbar_wait_bounded(&xbar[par], (xph >> par) & 1u, 3 * sv::kWaitNs))
             timed_out = true;
         xph ^= 1u << par;
     };
@@ -1130,7 +1137,7 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
                     const unsigned long long t0 = global_ns();
                     while (!record_posted(i)) {
                         __nanosleep(64);
-                        if (global_ns() - t0 > 4 * a.wait_ns) {
+                        if (global_ns() - t0 > 4 * sv::kWaitNs) {
                             state = kStateError;
                             code = SV_ERR_TIMEOUT;
                             return;
@@ -1409,7 +1416,7 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
                                 make_float4(tot.hi, tot.lo, (float)bad, 0.f),
                                 mapa_shared(smem_addr(&xbar[2 + sp]), lane));
             }
-            const bool dto = !mbar_wait_bounded(&xbar[2 + sp], 0u, 3 * a.wait_ns);
+            const bool dto = !mbar_wait_bounded(&xbar[2 + sp], 0u, 3 * sv::kWaitNs);
             FF ctot = {0.f, 0.f};
             int cbad = __any_sync(kFull, dto) ? 2 : 0;
             if (lane < C && !cbad) {
@@ -1700,22 +1707,15 @@ struct sv_ctx {
     int greedy_max_cluster = 8;
     int draft_max_cluster = 8;  // draft-logit kernel without filters
     uint32_t* d_err = nullptr;
-    int ovr_cluster = 0, ovr_group = 0, ovr_threads = 0;
-    int ovr_prefetch = -1;  // -1: the planner decides
+    int ovr_cluster = 0, ovr_group = 0, ovr_threads = 0;  // spec_verify_set_plan_override
     uint32_t* al_hist = nullptr;  // caller's accepted-length counters (device), or none
     int al_bins = 0;
-    unsigned long long wait_ns = 2000000000ull;
     // staging for the host-buffer entry point
     unsigned char* d_stage = nullptr;
     size_t stage_bytes = 0;
 };
 
 namespace {
-
-int env_int(const char* name, int dflt) {
-    const char* s = std::getenv(name);
-    return s && *s ? std::atoi(s) : dflt;
-}
 
 bool aligned(const void* p, size_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
 
@@ -1746,12 +1746,8 @@ int validate(const sv_ctx* ctx, const void* logits, int dtype, const float* q, c
 }
 
 int make_plan(const sv_ctx* ctx, int B, int K, int64_t V, int dtype, sv_plan* plan) {
-    const int rc = spec_verify_plan_for(ctx->num_sms, ctx->smem_optin, ctx->max_cluster, B, K, V,
-                                        dtype, ctx->ovr_cluster, ctx->ovr_group, ctx->ovr_threads,
-                                        plan);
-    if (rc == SV_OK && ctx->ovr_prefetch >= 0)
-        plan->prefetch_next = ctx->ovr_prefetch ? 1 : 0;
-    return rc;
+    return spec_verify_plan_for(ctx->num_sms, ctx->smem_optin, ctx->max_cluster, B, K, V, dtype,
+                                ctx->ovr_cluster, ctx->ovr_group, ctx->ovr_threads, plan);
 }
 
 int launch(sv_ctx* ctx, const void* logits, int dtype, const float* q, const int32_t* tokens,
@@ -1811,7 +1807,6 @@ int launch(sv_ctx* ctx, const void* logits, int dtype, const float* q, const int
         args.c_hi = std::nextafter(args.c_hi, 0.0f);
     args.c_lo = (float)(c_d - (double)args.c_hi);
     args.c = (float)c_d;
-    args.wait_ns = ctx->wait_ns;
 
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
@@ -1832,6 +1827,89 @@ int launch(sv_ctx* ctx, const void* logits, int dtype, const float* q, const int
         return SV_ERR_CUDA;
     }
     return SV_OK;
+}
+
+// What spec_verify_init and the no-allocation entry both need to know about a
+// device before the first launch on it.
+struct DeviceInfo {
+    int num_sms = 0, smem_optin = 0;
+    int max_cluster = 8;         // sampled verify kernel: largest usable cluster
+    int greedy_max_cluster = 8;  // greedy kernel
+    int draft_max_cluster = 8;   // draft-logit kernel without filters
+};
+
+// Device checks, kernel attributes and the largest usable clusters, with
+// `device` current.  Shared by both entries so that their plans agree.
+int device_setup(int device, DeviceInfo* info) {
+    int major = 0, minor = 0, sms = 0, optin = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) !=
+            cudaSuccess) {
+        (void)cudaGetLastError();
+        return SV_ERR_CUDA;
+    }
+    if (major != 10 || minor != 3)  // the kernels are built for sm_103a only
+        return SV_ERR_UNSUPPORTED;
+    int max_cluster = 16;
+    const int es_list[2] = {2, 4};
+    const int nt_list[3] = {128, 256, 512};
+    for (int es : es_list)
+        for (int nt : nt_list) {
+            KernelFn fn = pick_kernel(es, nt);
+            if (cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     optin) != cudaSuccess) {
+                (void)cudaGetLastError();
+                return SV_ERR_CUDA;
+            }
+            if (cudaFuncSetAttribute((const void*)fn,
+                                     cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+                cudaSuccess) {
+                (void)cudaGetLastError();
+                max_cluster = 8;
+            }
+        }
+    if (max_cluster == 16) {
+        // confirm that a 16-CTA cluster of the widest plan can be resident
+        cudaLaunchConfig_t cfg;
+        std::memset(&cfg, 0, sizeof cfg);
+        cfg.gridDim = dim3(16, 1, 1);
+        cfg.blockDim = dim3(512, 1, 1);
+        cfg.dynamicSmemBytes = 64 * 1024;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 16;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int nclusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&nclusters, (const void*)pick_kernel(2, 512), &cfg) !=
+                cudaSuccess ||
+            nclusters < 1) {
+            (void)cudaGetLastError();
+            max_cluster = 8;
+        }
+    }
+    info->num_sms = sms;
+    info->smem_optin = optin;
+    info->max_cluster = max_cluster;
+    // the greedy kernel may use 16-CTA clusters only where the main kernel may
+    info->greedy_max_cluster =
+        (max_cluster >= 16 && sv::greedy_set_attributes() == 0) ? 16 : 8;
+    // the truncated kernel's clusters stay at 8 CTAs (portable either way); the
+    // draft-logit kernel without filters may use 16 where the main kernel may
+    info->draft_max_cluster = (sv::trunc_set_attributes() == 0 && max_cluster >= 16) ? 16 : 8;
+    return SV_OK;
+}
+
+void apply_device_info(sv_ctx* c, const DeviceInfo& info) {
+    c->num_sms = info.num_sms;
+    c->smem_optin = info.smem_optin;
+    c->max_cluster = info.max_cluster;
+    c->greedy_max_cluster = info.greedy_max_cluster;
+    c->draft_max_cluster = info.draft_max_cluster;
 }
 
 }  // namespace
@@ -1864,78 +1942,16 @@ int spec_verify_init(sv_ctx** out, int device, int max_B, int max_K, int64_t max
         return SV_ERR_CUDA;
     }
     DeviceGuard guard(device);
-    int major = 0, minor = 0, sms = 0, optin = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
-        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) !=
-            cudaSuccess) {
-        (void)cudaGetLastError();
-        return SV_ERR_CUDA;
-    }
-    if (major != 10 || minor != 3)  // the kernels are built for sm_103a only
-        return SV_ERR_UNSUPPORTED;
+    DeviceInfo info;
+    const int rc = device_setup(device, &info);
+    if (rc != SV_OK)
+        return rc;
     sv_ctx* ctx = new sv_ctx();
     ctx->device = device;
     ctx->max_B = max_B;
     ctx->max_K = max_K;
     ctx->max_V = max_V;
-    ctx->num_sms = sms;
-    ctx->smem_optin = optin;
-    const int ns = env_int("SV_WAIT_MS", 0);
-    if (ns > 0)
-        ctx->wait_ns = (unsigned long long)ns * 1000000ull;
-    int max_cluster = 16;
-    const int es_list[2] = {2, 4};
-    const int nt_list[3] = {128, 256, 512};
-    for (int es : es_list)
-        for (int nt : nt_list) {
-            KernelFn fn = pick_kernel(es, nt);
-            if (cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     optin) != cudaSuccess) {
-                (void)cudaGetLastError();
-                delete ctx;
-                return SV_ERR_CUDA;
-            }
-            if (cudaFuncSetAttribute((const void*)fn,
-                                     cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
-                cudaSuccess) {
-                (void)cudaGetLastError();
-                max_cluster = 8;
-            }
-        }
-    if (max_cluster == 16) {
-        // confirm that a 16-CTA cluster of the widest plan can be resident
-        cudaLaunchConfig_t cfg;
-        std::memset(&cfg, 0, sizeof cfg);
-        cfg.gridDim = dim3(16, 1, 1);
-        cfg.blockDim = dim3(512, 1, 1);
-        cfg.dynamicSmemBytes = 64 * 1024;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 16;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        int nclusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&nclusters, (const void*)pick_kernel(2, 512), &cfg) !=
-                cudaSuccess ||
-            nclusters < 1) {
-            (void)cudaGetLastError();
-            max_cluster = 8;
-        }
-    }
-    ctx->max_cluster = max_cluster;
-    // the greedy kernel may use 16-CTA clusters only where the main kernel may
-    ctx->greedy_max_cluster = (max_cluster >= 16 && sv::greedy_set_attributes() == 0) ? 16 : 8;
-    // the truncated kernel's clusters stay at 8 CTAs (portable either way); the
-    // draft-logit kernel without filters may use 16 where the main kernel may
-    ctx->draft_max_cluster = (sv::trunc_set_attributes() == 0 && max_cluster >= 16) ? 16 : 8;
-    ctx->ovr_cluster = env_int("SV_CLUSTER", 0);
-    ctx->ovr_group = env_int("SV_GROUP", 0);
-    ctx->ovr_threads = env_int("SV_THREADS", 0);
-    ctx->ovr_prefetch = env_int("SV_PREFETCH", -1);
+    apply_device_info(ctx, info);
     if (cudaMalloc(&ctx->d_err, sizeof(uint32_t)) != cudaSuccess ||
         cudaMemset(ctx->d_err, 0, sizeof(uint32_t)) != cudaSuccess) {
         (void)cudaGetLastError();
@@ -2052,7 +2068,7 @@ int spec_verify_run_truncated(sv_ctx* ctx, const void* target_logits, int logits
     // min-p keeps l - l_max >= T ln(min_p); ln(min_p) = -inf for min_p <= 0 (off)
     g.dmin = min_p > 0.0 ? (float)((double)temperature * std::log(min_p)) : -INFINITY;
     g.top_p = top_p;
-    g.wait_ns = ctx->wait_ns;
+    g.wait_ns = sv::kWaitNs;
     DeviceGuard guard(ctx->device);
     return sv::trunc_launch(g, stream) == 0 ? SV_OK : SV_ERR_CUDA;
 }
@@ -2128,7 +2144,7 @@ int spec_verify_run_draft_logits(sv_ctx* ctx, const void* target_logits, int log
     g.dmin = min_p > 0.0 ? (float)((double)temperature * std::log(min_p)) : -INFINITY;
     g.top_p = top_p;
     g.filters = filters;
-    g.wait_ns = ctx->wait_ns;
+    g.wait_ns = sv::kWaitNs;
     DeviceGuard guard(ctx->device);
     return sv::trunc_launch(g, stream) == 0 ? SV_OK : SV_ERR_CUDA;
 }
@@ -2185,7 +2201,7 @@ int spec_verify_run_greedy(sv_ctx* ctx, const void* target_logits, int logits_dt
     g.C = plan.cluster;
     g.es = es;
     g.vec = plan.bulk_copy && aligned(target_logits, 16) ? 1 : 0;
-    g.wait_ns = ctx->wait_ns;
+    g.wait_ns = sv::kWaitNs;
     DeviceGuard guard(ctx->device);
     return sv::greedy_launch(g, stream) == 0 ? SV_OK : SV_ERR_CUDA;
 }
@@ -2388,56 +2404,10 @@ int noalloc_setup(int device, sv_ctx* c) {
         (void)cudaGetLastError();
         return SV_ERR_CUDA;
     }
-    int major = 0, minor = 0, sms = 0, optin = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
-        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) !=
-            cudaSuccess) {
-        (void)cudaGetLastError();
-        return SV_ERR_CUDA;
-    }
-    if (major != 10 || minor != 3)
-        return SV_ERR_UNSUPPORTED;
-    int max_cluster = 16;
-    const int es_list[2] = {2, 4};
-    const int nt_list[3] = {128, 256, 512};
-    for (int es : es_list)
-        for (int nt : nt_list) {
-            KernelFn fn = pick_kernel(es, nt);
-            if (cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     optin) != cudaSuccess) {
-                (void)cudaGetLastError();
-                return SV_ERR_CUDA;
-            }
-            if (cudaFuncSetAttribute((const void*)fn,
-                                     cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
-                cudaSuccess) {
-                (void)cudaGetLastError();
-                max_cluster = 8;
-            }
-        }
-    if (max_cluster == 16) {
-        cudaLaunchConfig_t cfg;
-        std::memset(&cfg, 0, sizeof cfg);
-        cfg.gridDim = dim3(16, 1, 1);
-        cfg.blockDim = dim3(512, 1, 1);
-        cfg.dynamicSmemBytes = 64 * 1024;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 16;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        int nclusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&nclusters, (const void*)pick_kernel(2, 512), &cfg) !=
-                cudaSuccess ||
-            nclusters < 1) {
-            (void)cudaGetLastError();
-            max_cluster = 8;
-        }
-    }
+    DeviceInfo info;
+    const int rc = device_setup(device, &info);
+    if (rc != SV_OK)
+        return rc;
     uint32_t* scratch = nullptr;
     if (cudaGetSymbolAddress((void**)&scratch, sv_noalloc_scratch) != cudaSuccess || !scratch) {
         (void)cudaGetLastError();
@@ -2447,12 +2417,7 @@ int noalloc_setup(int device, sv_ctx* c) {
     c->max_B = kNoAllocMaxB;
     c->max_K = kMaxK;
     c->max_V = kNoAllocMaxV;
-    c->num_sms = sms;
-    c->smem_optin = optin;
-    c->max_cluster = max_cluster;
-    const int ms = env_int("SV_WAIT_MS", 0);
-    if (ms > 0)
-        c->wait_ns = (unsigned long long)ms * 1000000ull;
+    apply_device_info(c, info);
     c->d_err = scratch;
     return SV_OK;
 }

@@ -12,6 +12,13 @@ constexpr int kMaxRows = kMaxK + 1;     // target rows per sequence
 constexpr int kMaxCluster = 16;         // CTAs per thread-block cluster (non-portable limit)
 constexpr int kSliceAlign = 8;          // slices start on 8-entry boundaries (16 bytes of bf16)
 constexpr int kStages = 3;              // ring stages per warp
+// Wait limits (fixed; nothing at run time shortens them).  A wait on another
+// CTA's or warp's progress (pushed partials, a posted decision) gives up after
+// kWaitNs and the sequence reports SV_ERR_TIMEOUT.  A wait on one of the
+// warp's own global-to-shared bulk copies depends on no other CTA and always
+// ends; it has a limit of its own, kCopyWaitNs.
+constexpr unsigned long long kWaitNs = 2000000000ull;       // 2 s
+constexpr unsigned long long kCopyWaitNs = 10000000000ull;  // 10 s
 constexpr int kChunkBytes = 2048;       // bytes per ring stage (one bulk copy)
 constexpr int kDrawTile = kChunkBytes / 4;  // entries per draw tile (its draft row fills one stage)
 constexpr int kFixedSmem = 3072;        // bytes reserved for the kernel's fixed shared state
