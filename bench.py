@@ -69,6 +69,8 @@ def parse_args():
     ap.add_argument("--graph-launches", type=int, default=30,
                     help="steps captured in one CUDA graph for the graph-replay timing (0 = skip)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--stat-launches", type=int, default=100,
+                    help="launches timed one by one for the median / p95 per launch")
     ap.add_argument("--clock-window", type=float, default=2.0,
                     help="seconds of untimed load, sampled for clocks, before the timed steps")
     return ap.parse_args()
@@ -373,22 +375,69 @@ def run_ours(args):
             k += 1
         torch.cuda.synchronize()
 
-    # timed region: K back-to-back steps between two events on the launch
-    # stream (events between the launches would add their own gaps)
+    # Inputs larger than L2 (several copies rotated): K back-to-back steps
+    # between two events on the launch stream (events between the launches
+    # would add their own gaps).  Inputs that fit in L2: every step is preceded
+    # by a write of twice the L2 size, and the step alone is timed between two
+    # events, so each step starts with its inputs in HBM only.
+    flush = per_set <= L2_BYTES
+    flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda") if flush else None
     barrier()
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for k in range(args.steps):
-        step(k)
-    t1.record(stream)
-    torch.cuda.synchronize()
+    if flush:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        t0.record(stream)
+        for k in range(args.steps):
+            flush_buf.zero_()
+            evs[k][0].record(stream)
+            step(k)
+            evs[k][1].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        total_ms = sum(a.elapsed_time(b) for a, b in evs)
+    else:
+        t0.record(stream)
+        for k in range(args.steps):
+            step(k)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        total_ms = t0.elapsed_time(t1)
     barrier()
     clk = clocks.stop()
-    total_ms = t0.elapsed_time(t1)
     local_ms = total_ms
     total_ms = max_over_ranks(total_ms, dist)
+
+    # per-launch statistics: an event after every launch (flushed inputs: an
+    # event pair around every launch); the event adds its own small gap
+    stats = None
+    if args.stat_launches > 0:
+        n_st = args.stat_launches
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_st + 1)]
+        per = []
+        if flush:
+            for k in range(n_st):
+                flush_buf.zero_()
+                ev[0].record(stream)
+                step(k)
+                ev[1].record(stream)
+                torch.cuda.synchronize()
+                per.append(ev[0].elapsed_time(ev[1]) * 1e3)
+        else:
+            ev[0].record(stream)
+            for k in range(n_st):
+                step(k)
+                ev[k + 1].record(stream)
+            torch.cuda.synchronize()
+            per = [ev[k].elapsed_time(ev[k + 1]) * 1e3 for k in range(n_st)]
+        per = np.sort(np.asarray(per))
+        stats = {"median_us": float(np.median(per)), "p95_us": float(np.percentile(per, 95)),
+                 "mean_us": float(per.mean()), "min_us": float(per[0]), "n": n_st,
+                 "method": ("an event pair around each launch, L2 flushed before it" if flush else
+                            "an event recorded after each of n back-to-back launches (the events "
+                            "add their own gaps)")}
 
     # the same steps replayed from a CUDA graph: no host launch cost between
     # kernels, so small workloads show their device time
@@ -508,13 +557,17 @@ def run_ours(args):
                                                 if dlog else ""),
                    "rows": rows_per_step,
                    "B": B, "K": K, "V": V, "logits_dtype": inp.dtype,
-                   "T": 0.0 if greedy else T, "l2": f"{nsets} input copies of {per_set / 1e9:.2f} GB rotated "
-                                 f"(each larger than the {L2_BYTES >> 20} MB L2)",
+                   "T": 0.0 if greedy else T,
+                   "l2": (f"L2 flushed before every step ({2 * L2_BYTES >> 20} MB written; inputs "
+                          f"{per_set / 1e6:.1f} MB), each step timed alone between two events"
+                          if flush else
+                          f"{nsets} input copies of {per_set / 1e9:.2f} GB rotated "
+                          f"(each larger than the {L2_BYTES >> 20} MB L2)"),
                    "plan": plan},
         "tokens_per_s": world * tokens_per_step * args.steps / (total_ms / 1e3),
         "mean_accept_len": float(acc.mean()),
         "hbm_gbs_algorithmic": achieved,
-        "hbm_gbs_nominal": (per_set if dlog else inp.nominal_bytes()) / avg_launch_s / 1e9,
+        "per_launch": stats,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
                      "traffic": profile_traffic(args.workload, args.mode),
@@ -530,53 +583,117 @@ def run_ours(args):
     return line
 
 
-def cpu_baseline(inp, seconds: float, greedy: bool = False, trunc=None, dlog=False) -> dict:
-    """The oracle as it stands, single thread, on whole passes over the
-    workload's sequences until `seconds` of CPU work have accumulated."""
-    import oracle
-    oracle.build()
-
-    def one(n):
-        if greedy:
-            oracle.verify_greedy(inp.logits[:n], inp.dtype, inp.tokens[:n])
-        elif dlog:
-            oracle.verify_draft_logits(inp.logits[:n], inp.dtype, inp.dlogits[:n], inp.tokens[:n],
-                                       inp.uniforms[:n], inp.T, inp.T_draft)
-        elif trunc is not None:
-            oracle.verify_truncated(inp.logits[:n], inp.dtype, inp.q[:n], inp.tokens[:n],
-                                    inp.uniforms[:n], inp.T, trunc[0], trunc[1])
-        else:
-            oracle.verify(inp.logits[:n], inp.dtype, inp.q[:n], inp.tokens[:n], inp.uniforms[:n],
-                          inp.T)
-    # one sequence first, to size the sample
-    t = time.perf_counter()
-    one(1)
-    per_seq = max(time.perf_counter() - t, 1e-6)
-    n = int(min(inp.B, max(1, seconds / per_seq)))
-    reps = max(1, int(seconds / (per_seq * n)))
-    t = time.perf_counter()
-    for _ in range(reps):
-        one(n)
-    el = time.perf_counter() - t
-    return {"value": reps * n * (inp.K + 1) / el, "unit": "rows/s", "cores": 1, "kind": "oracle",
-            "sample": f"{reps} pass(es) over the first {n} of {inp.B} sequences ({el:.1f} s)"}
+def host_cores() -> dict:
+    """The host threads this process may run on, and lscpu's CPU count."""
+    info = {"affinity": len(os.sched_getaffinity(0))}
+    try:
+        out = subprocess.run(["lscpu"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                             text=True, timeout=10).stdout
+        for line in out.splitlines():
+            k, _, v = line.partition(":")
+            if k.strip() in ("CPU(s)", "Model name", "Thread(s) per core"):
+                info["lscpu " + k.strip()] = v.strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return info
 
 
-def cpu_baseline_ragged(rg, seconds: float) -> dict:
-    """The ragged oracle as it stands, single thread, whole passes over the batch."""
-    import oracle
-    oracle.build()
+def _time_oracle(one, B: int, seconds: float, rows_per_seq: float, par: int = 1):
+    """Whole passes of one(n) over the first n sequences until `seconds` of
+    wall time have passed; n is sized from a first call on min(B, par)
+    sequences so that a pass takes about a quarter of `seconds`."""
+    m = min(B, par)
     t = time.perf_counter()
+    one(m)
+    rate = m / max(time.perf_counter() - t, 1e-6)  # sequences per second
+    n = int(min(B, max(m, rate * seconds / 4)))
     reps = 0
+    t = time.perf_counter()
     while True:
-        oracle.verify_ragged(rg.logits, rg.dtype, rg.q, rg.tokens, rg.uniforms, rg.offsets,
-                             rg.K_max, rg.T)
+        one(n)
         reps += 1
         el = time.perf_counter() - t
         if el >= seconds:
             break
-    return {"value": reps * rg.R / el, "unit": "rows/s", "cores": 1, "kind": "oracle",
-            "sample": f"{reps} pass(es) over all {rg.B} sequences ({rg.R} rows, {el:.1f} s)"}
+    return (reps * n * rows_per_seq / el,
+            f"{reps} pass(es) over the first {n} of {B} sequences ({el:.1f} s)")
+
+
+def _oracle_call(inp, lib, greedy=False, trunc=None, dlog=False):
+    import oracle
+
+    def one(n):
+        if greedy:
+            oracle.verify_greedy(inp.logits[:n], inp.dtype, inp.tokens[:n], lib=lib)
+        elif dlog:
+            oracle.verify_draft_logits(inp.logits[:n], inp.dtype, inp.dlogits[:n], inp.tokens[:n],
+                                       inp.uniforms[:n], inp.T, inp.T_draft, lib=lib)
+        elif trunc is not None:
+            oracle.verify_truncated(inp.logits[:n], inp.dtype, inp.q[:n], inp.tokens[:n],
+                                    inp.uniforms[:n], inp.T, trunc[0], trunc[1], lib=lib)
+        else:
+            oracle.verify(inp.logits[:n], inp.dtype, inp.q[:n], inp.tokens[:n], inp.uniforms[:n],
+                          inp.T, lib=lib)
+    return one
+
+
+def cpu_baseline(inp, seconds: float, greedy: bool = False, trunc=None, dlog=False) -> dict:
+    """The oracle as it stands on the host cores: the OpenMP build of oracle.c
+    (sequences spread over every core this process may use) and, beside it, the
+    plain build on one thread, each on whole passes over the first sequences of
+    the workload until `seconds` have passed."""
+    import oracle
+    oracle.build()
+    cores = host_cores()
+    v1, s1 = _time_oracle(_oracle_call(inp, None, greedy, trunc, dlog), inp.B, seconds, inp.K + 1)
+    single = {"value": v1, "unit": "rows/s", "cores": 1, "kind": "oracle", "sample": s1,
+              "build": "oracle.c, plain"}
+    try:
+        omp = oracle.load_openmp(cores["affinity"])
+        nth = omp.oracle_threads()
+    except Exception as e:  # no OpenMP runtime: the single-thread figure alone
+        single["host"] = cores
+        single["openmp"] = f"unavailable: {e}"
+        return single
+    vn, sn = _time_oracle(_oracle_call(inp, omp, greedy, trunc, dlog), inp.B, seconds, inp.K + 1,
+                          par=nth)
+    return {"value": vn, "unit": "rows/s", "cores": nth, "kind": "oracle", "sample": sn,
+            "build": f"oracle.c with -fopenmp, sequences over {nth} threads",
+            "host": cores, "single_thread": single}
+
+
+def cpu_baseline_ragged(rg, seconds: float) -> dict:
+    """The ragged oracle as it stands: OpenMP build on every core, and the
+    plain build on one thread beside it, whole passes over the batch."""
+    import oracle
+    oracle.build()
+    cores = host_cores()
+
+    def timed(lib):
+        t = time.perf_counter()
+        reps = 0
+        while True:
+            oracle.verify_ragged(rg.logits, rg.dtype, rg.q, rg.tokens, rg.uniforms, rg.offsets,
+                                 rg.K_max, rg.T, lib=lib)
+            reps += 1
+            el = time.perf_counter() - t
+            if el >= seconds:
+                break
+        return reps * rg.R / el, f"{reps} pass(es) over all {rg.B} sequences ({rg.R} rows, {el:.1f} s)"
+    v1, s1 = timed(None)
+    single = {"value": v1, "unit": "rows/s", "cores": 1, "kind": "oracle", "sample": s1,
+              "build": "oracle.c, plain"}
+    try:
+        omp = oracle.load_openmp(cores["affinity"])
+        nth = omp.oracle_threads()
+    except Exception as e:
+        single["host"] = cores
+        single["openmp"] = f"unavailable: {e}"
+        return single
+    vn, sn = timed(omp)
+    return {"value": vn, "unit": "rows/s", "cores": nth, "kind": "oracle", "sample": sn,
+            "build": f"oracle.c with -fopenmp, sequences over {nth} threads",
+            "host": cores, "single_thread": single}
 
 
 def e2e_ragged(args, rg, verifier, acc, dist, world) -> dict:
@@ -745,24 +862,37 @@ def e2e_greedy(args, inp, verifier, acc, dist, world, rows_per_step) -> dict:
 
 def run_reference(args):
     """The oracle (fp64 CPU) timed as the reference arm on a bounded sample of
-    the same workload per step."""
+    the same workload per step: the OpenMP build of oracle.c on every core
+    this process may use (the plain build on one thread if OpenMP is
+    unavailable)."""
     world, rank, local = dist_env()
     if rank != 0:
         return None
     import oracle
     oracle.build()
+    cores = host_cores()
+    try:
+        lib = oracle.load_openmp(cores["affinity"])
+        nth = lib.oracle_threads()
+        build = f"oracle.c with -fopenmp, sequences over {nth} threads"
+    except Exception as e:
+        lib, nth, build = None, 1, f"oracle.c, plain (OpenMP unavailable: {e})"
     inp = workloads.make_config(args.workload)
+
+    def one(n):
+        oracle.verify(inp.logits[:n], inp.dtype, inp.q[:n], inp.tokens[:n], inp.uniforms[:n],
+                      inp.T, lib=lib)
+    m = min(inp.B, nth)
     t = time.perf_counter()
-    oracle.verify(inp.logits[:1], inp.dtype, inp.q[:1], inp.tokens[:1], inp.uniforms[:1], inp.T)
-    per_seq = max(time.perf_counter() - t, 1e-6)
+    one(m)
+    rate = m / max(time.perf_counter() - t, 1e-6)
     budget = 120.0 / max(1, args.steps + args.warmup)   # whole run within ~2 minutes
-    n = int(min(inp.B, max(1, budget / per_seq)))
-    sl = slice(0, n)
+    n = int(min(inp.B, max(m, rate * budget)))
     for _ in range(args.warmup):
-        oracle.verify(inp.logits[sl], inp.dtype, inp.q[sl], inp.tokens[sl], inp.uniforms[sl], inp.T)
+        one(n)
     t = time.perf_counter()
     for _ in range(args.steps):
-        oracle.verify(inp.logits[sl], inp.dtype, inp.q[sl], inp.tokens[sl], inp.uniforms[sl], inp.T)
+        one(n)
     el = time.perf_counter() - t
     value = args.steps * n * (inp.K + 1) / el
     sample = f"first {n} of {inp.B} sequences per step"
@@ -771,8 +901,8 @@ def run_reference(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": args.workload, "B": inp.B, "K": inp.K,
                                             "V": inp.V, "logits_dtype": inp.dtype, "T": inp.T},
-            "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
-                             "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "rows/s", "cores": nth, "kind": "oracle",
+                             "sample": sample, "build": build, "host": cores},
             "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
             "gpu_launches": 0}

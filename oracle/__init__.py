@@ -20,21 +20,37 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
 _HDR = os.path.join(_HERE, "oracle.h")
 _LIB = os.path.join(_HERE, "liboracle.so")
+_LIB_OMP = os.path.join(_HERE, "liboracle_omp.so")
 
 OK, TOKEN_RANGE, NONFINITE, UNIFORM_RANGE, BAD_OFFSETS = 0, 4, 5, 7, 8
 
 _lib: Optional[ctypes.CDLL] = None
 
 
-def build(force: bool = False, src: str = _SRC, out: str = _LIB) -> str:
-    """Compile an oracle source into a shared library (skipped when up to date)."""
+def build(force: bool = False, src: str = _SRC, out: str = _LIB, openmp: bool = False) -> str:
+    """Compile an oracle source into a shared library (skipped when up to date).
+    ``openmp``: the same source with -fopenmp, so that a batch's sequences are
+    verified on several host threads."""
     newest = max(os.path.getmtime(src), os.path.getmtime(_HDR))
     if force or not os.path.exists(out) or os.path.getmtime(out) < newest:
         tmp = out + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-O2", "-ffp-contract=off", "-std=c99", "-Wall",
-                               "-I", _HERE, "-shared", "-fPIC", "-o", tmp, src, "-lm"])
+        subprocess.check_call(["gcc", "-O2", "-ffp-contract=off", "-std=gnu99", "-Wall"] +
+                              (["-fopenmp"] if openmp else []) +
+                              ["-I", _HERE, "-shared", "-fPIC", "-o", tmp, src, "-lm"])
         os.replace(tmp, out)
     return out
+
+
+def load_openmp(threads: Optional[int] = None) -> ctypes.CDLL:
+    """The OpenMP build of oracle.c, bound like the plain one, set to
+    ``threads`` host threads (default: the cores this process may run on)."""
+    lib = _bind(build(src=_SRC, out=_LIB_OMP, openmp=True))
+    lib.oracle_threads.restype = ctypes.c_int
+    lib.oracle_threads.argtypes = []
+    lib.oracle_set_threads.restype = ctypes.c_int
+    lib.oracle_set_threads.argtypes = [ctypes.c_int]
+    lib.oracle_set_threads(int(threads or len(os.sched_getaffinity(0))))
+    return lib
 
 
 def _bind(path: str) -> ctypes.CDLL:

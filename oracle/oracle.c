@@ -8,12 +8,41 @@
  * taken is stated next to the step.
  *
  * Build: gcc -O2 -ffp-contract=off -shared -fPIC oracle.c -lm
+ * The same source built with -fopenmp verifies the sequences of a batch on
+ * several host threads (each sequence on one thread, with its own scratch
+ * rows); every sequence's arithmetic is the same either way.
  */
 #include "oracle.h"
 
 #include <math.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Host threads the batch loops use: 1 unless built with OpenMP. */
+int oracle_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* Sets the thread count of later batch loops (OpenMP build; n >= 1) and
+ * returns the count now in force. */
+int oracle_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n >= 1)
+        omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+    return oracle_threads();
+}
 
 /* One stored logit as an exact double.  bf16 widens to fp32 by placing its 16
  * bits in the high half of the word; both widen exactly to double. */
@@ -134,7 +163,12 @@ typedef struct {
     double top_p, min_p;
 } trunc_opts;
 
-static const double* g_sort_p; /* the row qsort orders (single-threaded test code) */
+/* the row qsort orders: one per thread in the OpenMP build */
+#ifdef _OPENMP
+static __thread const double* g_sort_p;
+#else
+static const double* g_sort_p;
+#endif
 
 static int by_p_desc(const void* a, const void* b)
 {
@@ -344,21 +378,38 @@ static int verify_batch(const void* logits, int dtype, const float* q, const int
         (K > 0 && ((!q && !dlogits) || !tokens || !accept_mask)) || (dtype != 0 && dtype != 1) ||
         !(temperature > 0.0f) || !isfinite(temperature))
         return -1;
-    /* scratch: two rows of V doubles, plus the per-row results of one sequence */
-    double* p = (double*)malloc((size_t)V * sizeof(double));
-    double* w = (double*)malloc((size_t)V * sizeof(double));
-    double* rm = (double*)malloc((size_t)(K + 1) * sizeof(double));
-    double* rs = (double*)malloc((size_t)(K + 1) * sizeof(double));
-    double* pd = (double*)malloc((size_t)(K + 1) * sizeof(double));
-    double* qrow = dlogits ? (double*)malloc((size_t)V * sizeof(double)) : 0;
-    if (!p || !w || !rm || !rs || !pd || (dlogits && !qrow)) {
-        free(p); free(w); free(rm); free(rs); free(pd); free(qrow);
+    /* scratch per thread: two rows of V doubles (three with draft logits),
+     * plus the per-row results of one sequence */
+    const int nth = oracle_threads();
+    const size_t nr = (size_t)(K + 1);
+    double* p_all = (double*)malloc((size_t)nth * (size_t)V * sizeof(double));
+    double* w_all = (double*)malloc((size_t)nth * (size_t)V * sizeof(double));
+    double* rm_all = (double*)malloc((size_t)nth * nr * sizeof(double));
+    double* rs_all = (double*)malloc((size_t)nth * nr * sizeof(double));
+    double* pd_all = (double*)malloc((size_t)nth * nr * sizeof(double));
+    double* q_all = dlogits ? (double*)malloc((size_t)nth * (size_t)V * sizeof(double)) : 0;
+    if (!p_all || !w_all || !rm_all || !rs_all || !pd_all || (dlogits && !q_all)) {
+        free(p_all); free(w_all); free(rm_all); free(rs_all); free(pd_all); free(q_all);
         return -2;
     }
     const size_t esz = dtype == 0 ? 4 : 2;
     const double T = (double)temperature;
 
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nth)
+#endif
     for (int64_t b = 0; b < B; ++b) {
+#ifdef _OPENMP
+        const size_t th = (size_t)omp_get_thread_num();
+#else
+        const size_t th = 0;
+#endif
+        double* p = p_all + th * (size_t)V;
+        double* w = w_all + th * (size_t)V;
+        double* rm = rm_all + th * nr;
+        double* rs = rs_all + th * nr;
+        double* pd = pd_all + th * nr;
+        double* qrow = q_all ? q_all + th * (size_t)V : 0;
         int32_t* ot = out_tokens + (size_t)b * (size_t)(K + 1);
         uint8_t* mk = K > 0 ? accept_mask + (size_t)b * (size_t)K : 0;
         uint8_t mk_dummy[1];
@@ -419,7 +470,7 @@ static int verify_batch(const void* logits, int dtype, const float* q, const int
         if (sample_alt)
             sample_alt[b] = s_alt;
     }
-    free(p); free(w); free(rm); free(rs); free(pd); free(qrow);
+    free(p_all); free(w_all); free(rm_all); free(rs_all); free(pd_all); free(q_all);
     return 0;
 }
 
@@ -555,6 +606,9 @@ int oracle_verify_greedy(const void* logits, int dtype, const int32_t* tokens, i
     if (B < 0 || K < 0 || V < 1)
         return 1;
     const size_t es = dtype == 0 ? 4 : 2;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
     for (int64_t b = 0; b < B; ++b) {
         int st = ORACLE_OK, len = 0;
         int32_t* ot = out_tokens + (size_t)b * (size_t)(K + 1);
@@ -640,6 +694,10 @@ int oracle_verify_ragged(const void* logits, int dtype, const float* q, const in
     if (!off || B < 0 || K_max < 0 || R < B)
         return -1;
     const size_t esz = dtype == 0 ? 4 : 2;
+    int rc_any = 0;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
     for (int64_t b = 0; b < B; ++b) {
         const int64_t o0 = off[b], o1 = off[b + 1];
         const int64_t Kb = o1 - o0 - 1;
@@ -663,8 +721,12 @@ int oracle_verify_ragged(const void* logits, int dtype, const float* q, const in
             status ? status + b : 0, row_m ? row_m + o0 : 0, row_s ? row_s + o0 : 0,
             p_draft && Kb ? p_draft + d0 : 0, accept_margin ? accept_margin + b : 0,
             sample_margin ? sample_margin + b : 0, sample_alt ? sample_alt + b : 0);
-        if (rc != 0)
-            return rc;
+        if (rc != 0) {
+#ifdef _OPENMP
+#pragma omp critical
+#endif
+            rc_any = rc;
+        }
     }
-    return 0;
+    return rc_any;
 }

@@ -73,6 +73,12 @@ int oracle_softmax_row(const void* row, int dtype, int64_t V, double T,
  *   sample_alt [B]        the positive-weight token across that nearer
  *                         boundary, or -1 (optional)
  */
+/* Host threads oracle_verify and its variants use for a batch: 1 in the plain
+ * build, OpenMP's thread count in a build with -fopenmp. */
+int oracle_threads(void);
+/* Sets that count (OpenMP build, n >= 1); returns the count now in force. */
+int oracle_set_threads(int n);
+
 int oracle_verify(const void* logits, int dtype, const float* q, const int32_t* tokens,
                   const float* uniforms, int64_t B, int K, int64_t V, float temperature,
                   int32_t* accept_len, int32_t* out_tokens, uint8_t* accept_mask,

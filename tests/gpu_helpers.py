@@ -20,6 +20,20 @@ TIE = 1e-6
 RTOL = 1e-5
 
 _verifiers = {}
+_oracle_lib = []
+
+
+def oracle_lib():
+    """The OpenMP build of the oracle on every core this process may use
+    (results identical to the plain build: tests/test_oracle_openmp.py), or
+    None -- the plain build -- where no OpenMP runtime is available."""
+    if not _oracle_lib:
+        import oracle
+        try:
+            _oracle_lib.append(oracle.load_openmp())
+        except Exception:
+            _oracle_lib.append(None)
+    return _oracle_lib[0]
 
 
 def verifier(max_B=1 << 20, max_K=32, max_V=1 << 21):
