@@ -6,6 +6,8 @@ Bar: as for the sampled verify (tests/gpu_helpers.py) -- bit-exact outside the
 1e-6 tie band, statuses exact, row statistics and p(x) within 1e-5 relative --
 and, with a truncated target, the truncated test's extra tie class (a reached
 row within 1e-6 of a filter boundary: validity only)."""
+import json
+
 import numpy as np
 import pytest
 
@@ -51,7 +53,7 @@ def _check(inp, top_p=1.0, min_p=0.0, label="", cluster=0, dl_dev=None, tokens=N
     o = oracle.verify_draft_logits(inp.logits, inp.dtype,
                                    inp.dlogits if dlogits is None else dlogits,
                                    inp.tokens if tokens is None else tokens, inp.uniforms, inp.T,
-                                   inp.T_draft, top_p, min_p)
+                                   inp.T_draft, top_p, min_p, lib=gh.oracle_lib())
     g = _gpu(inp, top_p, min_p, cluster, dl_dev, tokens)
     tt = o["trunc_margin"] < gh.TIE
     o = dict(o)
@@ -74,12 +76,17 @@ def test_workloads_full_size(name):
     assert info["exact"] >= 0.8 * inp.B
 
 
-@pytest.mark.parametrize("name,B", [("b64_k3_v151936_bf16", None), ("b256_k7_v128256_bf16_zipf", 64)])
-def test_workloads_truncated_target(name, B):
-    """Draft logits with the production sampler settings on the target side."""
-    inp = workloads.with_draft_logits(name, B=B)
+@pytest.mark.parametrize("name", ["b64_k3_v151936_bf16", "b256_k7_v128256_bf16_zipf"])
+def test_workloads_truncated_target(name):
+    """Draft logits with [P2]'s production sampler settings (top-p 0.95, min-p
+    0.05) on the target side, every sequence of the workload, under the
+    planner's own plan.  Every sequence is exact or a counted tie; the ties stay
+    below 8 % of the batch."""
+    inp = workloads.with_draft_logits(name)
     info, _, _ = _check(inp, 0.95, 0.05, label=name + " top-p/min-p")
-    assert info["exact"] >= 0.8 * inp.B
+    print("draft logits, truncated target: " + json.dumps({"case": name, **info}))
+    assert info["exact"] + info["accept_ties"] + info["draw_ties"] == inp.B
+    assert info["accept_ties"] + info["draw_ties"] + info["trunc_ties"] <= 0.08 * inp.B
 
 
 @pytest.mark.parametrize("cluster", [0, 1, 2, 4, 8, 16])

@@ -2,7 +2,6 @@
 the same seeded inputs and the same uniforms.  Bar and tie band: see
 tests/gpu_helpers.py."""
 import json
-import os
 
 import numpy as np
 import pytest
@@ -14,17 +13,10 @@ from tests import oracle_pins as pins
 
 pytestmark = pytest.mark.gpu
 
-OUT_DIR = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "gpurun_out")
-
-
 def _record(name, info):
-    """Keep a line per parity case (tie counts, stat errors) for the record."""
-    try:
-        os.makedirs(OUT_DIR, exist_ok=True)
-        with open(os.path.join(OUT_DIR, "parity_cases.jsonl"), "a") as f:
-            f.write(json.dumps({"case": name, **info}) + "\n")
-    except OSError:
-        pass
+    """Print a line per parity case (tie counts, stat errors): pytest shows it
+    with -rP or -s."""
+    print("parity case " + json.dumps({"case": name, **info}))
 
 
 # ----------------------------------------------------------- workloads -----

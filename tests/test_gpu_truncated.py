@@ -9,6 +9,8 @@ that lies within 1e-6 of a filter boundary (a token's log(p/p_max) within 1e-6
 of log(min_p), or a mass-above value within 1e-6 of top_p), where float32 and
 float64 may keep different sets; such sequences are counted and checked for
 validity only."""
+import json
+
 import numpy as np
 import pytest
 
@@ -40,7 +42,7 @@ def _gpu(inp, top_p, min_p, cluster=0):
 
 def _check(inp, top_p, min_p, label, cluster=0):
     o = oracle.verify_truncated(inp.logits, inp.dtype, inp.q, inp.tokens, inp.uniforms, inp.T,
-                                top_p, min_p)
+                                top_p, min_p, lib=gh.oracle_lib())
     g = _gpu(inp, top_p, min_p, cluster)
     tt = o["trunc_margin"] < gh.TIE
     # truncation ties: validity only (folded into the acceptance-tie class),
@@ -63,10 +65,17 @@ def test_workloads_at_the_production_settings(name):
     assert info["exact"] + info["accept_ties"] + info["draw_ties"] == inp.B
 
 
-def test_b256_prefix_at_the_production_settings():
-    inp = workloads.make_config("b256_k7_v128256_bf16_zipf", B=64)
-    info, _ = _check(inp, 0.95, 0.05, "b256 prefix")
-    assert info["exact"] >= 0.8 * inp.B
+def test_b256_full_at_the_production_settings():
+    """All 256 sequences of the 256 x 8 x 128256 bf16 workload, at [P2]'s
+    production sampler settings (top-p 0.95, min-p 0.05), under the plan the
+    planner picks for that size (the one the benchmark times).  Every sequence
+    is exact or a counted tie; the ties stay below 8 % of the batch."""
+    inp = workloads.make_config("b256_k7_v128256_bf16_zipf")
+    info, _ = _check(inp, 0.95, 0.05, "b256 full")
+    ties = info["accept_ties"] + info["draw_ties"] + info["trunc_ties"]
+    print("truncated b256 full: " + json.dumps(info))
+    assert info["exact"] + info["accept_ties"] + info["draw_ties"] == inp.B
+    assert ties <= 0.08 * inp.B
 
 
 @pytest.mark.parametrize("cluster", [0, 1, 2, 4, 8])

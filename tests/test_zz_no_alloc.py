@@ -101,3 +101,51 @@ def test_noalloc_rejects_a_bad_device_without_cuda():
     for dev in (-1, 64):
         assert sv.spec_verify_run_noalloc(dev, None, 0, None, None, None, 1, 0, 1, 1.0, None, None,
                                           None) == sv.SV_ERR_INVALID_ARG
+
+
+@pytest.mark.gpu
+def test_noalloc_error_paths_mark_only_their_sequence():
+    """Planted faults -- a draft token outside [0, V), a NaN in a row the loop
+    reaches, a uniform of 1.0 -- mark only their own sequence: its status
+    carries the error, accept_len is 0 and its tokens are -1, as with
+    spec_verify_run and the oracle.  A clean call right after still matches
+    spec_verify_run."""
+    torch = pytest.importorskip("torch")
+    import oracle
+    import speculative_decoding_verification_14_gb300 as sv
+    inp = workloads.make_random(6, 4, 3001, "f32", T=0.8, seed=21)
+    lg, x, u = inp.logits.copy(), inp.tokens.copy(), inp.uniforms.copy()
+    x[1, 2] = inp.V                 # token out of range
+    lg[3, 0, 1234] = np.nan         # row 0 is always reached
+    u[4, 1] = np.float32(1.0)       # uniform outside [0, 1)
+    inp.logits, inp.tokens, inp.uniforms = lg, x, u
+    want = oracle.verify_inputs(inp)
+    assert list(want["status"]) == [0, sv.SV_ERR_TOKEN_RANGE, 0, sv.SV_ERR_NONFINITE,
+                                    sv.SV_ERR_UNIFORM_RANGE, 0]
+    d = to_device(inp.logits, inp.dtype, inp.q, inp.tokens, inp.uniforms)
+    ref = verifier().run(*d, inp.T, stats=True, status=True)
+    torch.cuda.synchronize()
+    ref = {k: t.cpu().numpy() for k, t in ref.items()}
+    stream = torch.cuda.current_stream().cuda_stream
+    rc, out = _run_noalloc(sv, torch, inp, *d, stream)
+    assert rc == sv.SV_OK, sv.spec_verify_strerror(rc)
+    torch.cuda.synchronize()
+    got = {k: t.cpu().numpy() for k, t in out.items()}
+    _same(ref, got, inp.K)
+    np.testing.assert_array_equal(got["status"], want["status"])
+    bad = want["status"] != 0
+    assert (got["accept_len"][bad] == 0).all()
+    assert (got["out_tokens"][bad] == -1).all()
+    assert (got["accept_mask"][bad] == 0).all()
+    np.testing.assert_array_equal(got["accept_len"][~bad], want["accept_len"][~bad])
+    # a clean call after the faulty one: the same outputs as the context entry
+    clean = workloads.make_random(6, 4, 3001, "f32", T=0.8, seed=22)
+    dc = to_device(clean.logits, clean.dtype, clean.q, clean.tokens, clean.uniforms)
+    ref = verifier().run(*dc, clean.T, stats=True, status=True)
+    torch.cuda.synchronize()
+    ref = {k: t.cpu().numpy() for k, t in ref.items()}
+    rc, out = _run_noalloc(sv, torch, clean, *dc, stream)
+    assert rc == sv.SV_OK
+    torch.cuda.synchronize()
+    _same(ref, {k: t.cpu().numpy() for k, t in out.items()}, clean.K)
+    assert (ref["status"] == 0).all()
