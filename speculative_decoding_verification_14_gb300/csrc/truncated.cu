@@ -550,8 +550,11 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
     const bool use_top = TR && a.top_p < 1.0;
 
     __shared__ __align__(16) float4 part[2][MC * kNW];          // warp partials, by use parity
-    __shared__ __align__(16) double hrecv[2][HC][HB];            // CTA histograms, by use parity
-    __shared__ __align__(16) double hloc[HB];                    // this CTA's histogram
+    // top-p histograms hold fixed-point masses: weights 2^((l - l_max) c) <= 1
+    // scaled by 2^fix and rounded to integers, so the adds are exact and their
+    // order does not matter
+    __shared__ __align__(16) unsigned long long hrecv[2][HC][HB];  // CTA histograms, by use parity
+    __shared__ __align__(16) unsigned long long hloc[HB];          // this CTA's histogram
     __shared__ __align__(8) unsigned long long xbar[2], hbar[2];
     __shared__ int xs[sv::kMaxK];
     __shared__ float us[sv::kMaxRows];
@@ -715,12 +718,20 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
         key_t = 0;
         // ---- B: the kept set ----
         if constexpr (TR) if (use_min || use_top) {
-            const double thr = a.top_p * (double)S_all;
+            // fixed point: 2^fix per unit weight, with fix chosen so that V
+            // weights of at most 1 sum below 2^63 (44 bits for V <= 2^18);
+            // each weight is off by at most 2^-(fix+1) after rounding
+            const int vbits = 64 - __clzll((unsigned long long)(V > 1 ? V - 1 : 1));
+            const int fix = min(44, 62 - vbits);
+            const float fscale = __int_as_float((127 + fix) << 23);      // 2^fix
+            const float funscale = __int_as_float((127 - fix) << 23);    // 2^-fix
+            const unsigned long long thr =
+                (unsigned long long)(a.top_p * (double)S_all * (double)fscale);
             uint32_t prefix = 0;
-            double above = 0.0;  // mass of candidates with keys above the prefix group
+            unsigned long long above = 0;  // mass of candidates with keys above the prefix group
             for (int lev = 0; lev < LEVELS; ++lev) {
                 for (int k = tid; k < kBins; k += kNT)
-                    hloc[k] = 0.0;
+                    hloc[k] = 0ull;
                 __syncthreads();
                 const int sh_hi = KEYBITS - 8 * lev;   // prefix = key >> sh_hi
                 const int sh_lo = KEYBITS - 8 * (lev + 1);
@@ -738,7 +749,8 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
                     const uint32_t key = key_of<ES>(l);
                     if (lev > 0 && (key >> sh_hi) != prefix)
                         return;
-                    atomicAdd(&hloc[(key >> sh_lo) & 0xffu], (double)ex2((l - lmax) * c));
+                    atomicAdd(&hloc[(key >> sh_lo) & 0xffu],
+                              __float2ull_rn(ex2((l - lmax) * c) * fscale));
                 });
                 const int s2 = exchange_hist();
                 if (s2 < 0) {
@@ -746,40 +758,40 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
                     break;
                 }
                 // lane l holds bins 8l .. 8l+7, summed over the CTAs in a fixed order
-                double bin[8];
+                unsigned long long bin[8];
 #pragma unroll
                 for (int t = 0; t < 8; ++t) {
-                    double acc = 0.0;
+                    unsigned long long acc = 0;
                     for (int r = 0; r < C; ++r)
                         acc += hrecv[s2][r][lane * 8 + t];
                     bin[t] = acc;
                 }
-                double lt = 0.0;
+                unsigned long long lt = 0;
 #pragma unroll
                 for (int t = 0; t < 8; ++t)
                     lt += bin[t];
                 // mass of the bins of this and higher lanes (suffix sum over lanes)
-                double incl = lt;
+                unsigned long long incl = lt;
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
-                    const double v = __shfl_down_sync(kFull, incl, o);
+                    const unsigned long long v = __shfl_down_sync(kFull, incl, o);
                     if (lane + o < 32)
                         incl += v;
                 }
-                const double above_lane = incl - lt;
-                const double total = __shfl_sync(kFull, incl, 0);
+                const unsigned long long above_lane = incl - lt;
+                const unsigned long long total = __shfl_sync(kFull, incl, 0);
                 if (lev == 0 && (!use_top || total < thr)) {
                     // min-p alone, or candidates holding less than top_p: all kept
-                    E_kept = (float)total;
+                    E_kept = __ull2float_rn(total) * funscale;
                     break;
                 }
                 // the lowest non-empty digit whose mass above is below thr
                 int hc = -1;
-                double hab = 0.0, hb = 0.0;
-                double run = above + above_lane;
+                unsigned long long hab = 0, hb = 0;
+                unsigned long long run = above + above_lane;
 #pragma unroll
                 for (int t = 7; t >= 0; --t) {
-                    if (bin[t] > 0.0 && run < thr) {
+                    if (bin[t] > 0 && run < thr) {
                         hc = lane * 8 + t;
                         hab = run;
                         hb = bin[t];
@@ -799,7 +811,7 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
                 hb = __shfl_sync(kFull, hb, src);
                 prefix = (prefix << 8) | (uint32_t)best;
                 above = hab;
-                E_kept = (float)(hab + hb);
+                E_kept = __ull2float_rn(hab + hb) * funscale;
                 if (lev == LEVELS - 1)
                     key_t = prefix;
             }

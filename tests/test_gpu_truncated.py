@@ -118,3 +118,37 @@ def test_errors_and_special_values():
         lgd, qd, td, ud = gh.to_device(inp.logits, inp.dtype, inp.q, inp.tokens, inp.uniforms)
         v.run_truncated(lgd, qd, td, ud, inp.T, 0.0, 0.05)
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("entry", ["truncated", "draft_logits"])
+def test_repeated_runs_with_filters_are_bit_identical(entry):
+    """With top-p < 1 and min-p > 0 two runs give the same bits: the top-p
+    histograms add fixed-point integers, so the order in which warps add their
+    weights cannot move a cut.  The rows hold many equal logits, so that
+    top-p masses land on bin boundaries."""
+    import torch
+    v = gh.verifier()
+    if entry == "truncated":
+        inp = workloads.make_random(12, 4, 5000, "bf16", T=0.7, sigma=1.0, seed=41)
+    else:
+        inp = workloads.make_random_draft_logits(12, 4, 5000, "bf16", T=0.7, T_draft=0.9,
+                                                 sigma=1.0, seed=41)
+    lg = inp.logits.copy()
+    lg[:, :, ::3] = lg[:, :, :1]                 # a third of every row ties the first entry
+    inp.logits = lg
+    runs = []
+    for _ in range(3):
+        if entry == "truncated":
+            lgd, qd, td, ud = gh.to_device(inp.logits, inp.dtype, inp.q, inp.tokens, inp.uniforms)
+            out = v.run_truncated(lgd, qd, td, ud, inp.T, 0.9, 0.05, stats=True)
+        else:
+            lgd, _, td, ud = gh.to_device(inp.logits, inp.dtype, np.zeros(1, np.float32),
+                                          inp.tokens, inp.uniforms)
+            dld = torch.from_numpy(np.ascontiguousarray(inp.dlogits).view(np.int16)).cuda().view(
+                torch.bfloat16)
+            out = v.run_draft_logits(lgd, dld, td, ud, inp.T, inp.T_draft, 0.9, 0.05, stats=True)
+        torch.cuda.synchronize()
+        runs.append({k: t.cpu().numpy().copy() for k, t in out.items()})
+    for r in runs[1:]:
+        for k in runs[0]:
+            np.testing.assert_array_equal(runs[0][k], r[k], err_msg=k)
