@@ -375,9 +375,9 @@ __device__ __forceinline__ void warp_finish(const LaneStats& st, float c, float&
 // rescale when it lies above the lane's maximum, then every term against the
 // lane maximum with packed arithmetic and two packed accumulators.  Terms stay
 // at most 1, as with one unit at a time, but the maximum is compared once per
-// batch.
+// batch.  Returns the batch maximum.
 template <int ES, int D>
-__device__ __forceinline__ void lane_update_batch(LaneStats& st, const uint4 (&r)[D],
+__device__ __forceinline__ float lane_update_batch(LaneStats& st, const uint4 (&r)[D],
                                                   const bool (&ok)[D], float c) {
     float bm = -INFINITY;
 #pragma unroll
@@ -386,10 +386,10 @@ __device__ __forceinline__ void lane_update_batch(LaneStats& st, const uint4 (&r
             bm = fmax_nan(bm, vec_max<ES>(r[k]));
     if (bm != bm || bm == INFINITY) {
         st.bad = true;
-        return;
+        return bm;
     }
     if (bm == -INFINITY)  // weights 0
-        return;
+        return bm;
     if (bm > st.mx) {
         const float f = ex2((st.mx - bm) * c);
         st.sm *= f;
@@ -417,6 +417,7 @@ __device__ __forceinline__ void lane_update_batch(LaneStats& st, const uint4 (&r
     }
     const float2 t = __fadd2_rn(s0, s1);
     acc_add(st.sm, st.sc, t.x + t.y);
+    return bm;
 }
 
 // Loads of one batch: units b0 + k*32 + lane (k < D) of the stretch ending at
@@ -466,12 +467,78 @@ __device__ __forceinline__ void prefetch_start(const uint4* rp, int64_t w0, int6
         prefetch_batch<D>(rp, w0 + (int64_t)n * 32 * D, w1, lane);
 }
 
+// min-p survivor lists (truncated target with min-p on): per warp and row,
+// and per CTA (the CTA's list travels with its count in one histogram slot).
+constexpr int kCandW = 128;
+constexpr int kCandC = 511;
+
+// The largest entry of each group of batches of a warp's row pass, kept in
+// shared memory (slots of `per` consecutive batches, at most kSlots of them),
+// so that a later pass over the row can skip every group that cannot hold a
+// min-p survivor.
+constexpr int kSlots = 32;
+
+struct SlotMax {
+    float* slot;   // [kSlots], or null: not recorded
+    int per;       // batches per slot
+    int cnt = 0, s = 0;
+    float run = -INFINITY;
+    __device__ __forceinline__ void add(float lane_bm, bool last, int lane) {
+        if (!slot)
+            return;
+        run = fmaxf(run, warp_max(lane_bm));
+        if (++cnt == per || last) {
+            if (lane == 0)
+                slot[s] = run;
+            ++s;
+            cnt = 0;
+            run = -INFINITY;
+        }
+    }
+};
+
+// Whether entries [e0, e1) of a sampled draft row hold a value that is not a
+// probability (negative, inf or NaN); `vec4`: 16-byte aligned, four at a time.
+__device__ __forceinline__ bool q_stretch_bad(const float* qrow, int64_t e0, int64_t e1, int lane,
+                                              bool vec4) {
+    bool bad = false;
+    const auto check = [&](uint32_t bits) {
+        const float x = __uint_as_float(bits);
+        bad = bad || !(x >= 0.f && x < INFINITY);
+    };
+    if (vec4) {
+        constexpr int D = 4;
+        const uint4* qp = reinterpret_cast<const uint4*>(qrow);
+        const int64_t u0 = e0 / 4, u1 = e1 / 4;
+        prefetch_start<D>(qp, u0, u1, lane);
+        for (int64_t b0 = u0; b0 < u1; b0 += 32 * D) {
+            prefetch_batch<D>(qp, b0 + kAhead * 32 * D, u1, lane);
+            uint4 r[D];
+            bool ok[D];
+            load_batch<D>(qp, b0, u1, lane, r, ok);
+#pragma unroll
+            for (int k = 0; k < D; ++k)
+                if (ok[k]) {
+                    check(r[k].x);
+                    check(r[k].y);
+                    check(r[k].z);
+                    check(r[k].w);
+                }
+        }
+    } else {
+        for (int64_t e = e0 + lane; e < e1; e += 32)
+            check(__float_as_uint(__ldg(qrow + e)));
+    }
+    return __any_sync(kFull, bad);
+}
+
 // One row's statistics over this warp's stretch of `base` (vector path; the
 // element path takes one entry at a time), D loads in flight per lane.
 template <int ES, int D>
 __device__ __forceinline__ void warp_row_stats(const TArgs& a, const void* base, int64_t re,
                                                int64_t w0, int64_t w1, int lane, float c,
-                                               float& wmx, float& wsm, bool& wbad) {
+                                               float& wmx, float& wsm, bool& wbad,
+                                               SlotMax* sm = nullptr) {
     LaneStats st;
     if (a.vec) {
         const uint4* rp = reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(base) +
@@ -482,7 +549,9 @@ __device__ __forceinline__ void warp_row_stats(const TArgs& a, const void* base,
             uint4 r[D];
             bool ok[D];
             load_batch<D>(rp, b0, w1, lane, r, ok);
-            lane_update_batch<ES, D>(st, r, ok, c);
+            const float bm = lane_update_batch<ES, D>(st, r, ok, c);
+            if (sm)
+                sm->add(bm, b0 + 32 * D >= w1, lane);
         }
     } else {
         for (int64_t e = w0 + lane; e < w1; e += 32) {
@@ -499,7 +568,8 @@ __device__ __forceinline__ void warp_row_stats_pair(const void* tbase, int64_t t
                                                     const void* dbase, int64_t dre, int64_t w0,
                                                     int64_t w1, int lane, float c, float cd,
                                                     float& wmx, float& wsm, bool& wbad,
-                                                    float& dmx, float& dsm, bool& dbad) {
+                                                    float& dmx, float& dsm, bool& dbad,
+                                                    SlotMax* sm = nullptr) {
     const uint4* tp = reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(tbase) +
                                                      tre * ES);
     const uint4* dp = reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(dbase) +
@@ -514,8 +584,10 @@ __device__ __forceinline__ void warp_row_stats_pair(const void* tbase, int64_t t
         bool ok[D];
         load_batch<D>(tp, b0, w1, lane, rt, ok);
         load_batch<D>(dp, b0, w1, lane, rd, ok);
-        lane_update_batch<ES, D>(st, rt, ok, c);
+        const float bm = lane_update_batch<ES, D>(st, rt, ok, c);
         lane_update_batch<ES, D>(sd, rd, ok, cd);
+        if (sm)
+            sm->add(bm, b0 + 32 * D >= w1, lane);
     }
     warp_finish(st, c, wmx, wsm, wbad);
     warp_finish(sd, cd, dmx, dsm, dbad);
@@ -548,6 +620,9 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
     const float c = a.c;
     const bool use_min = TR && a.dmin > -INFINITY;
     const bool use_top = TR && a.top_p < 1.0;
+    // min-p bounds the kept set: one pass lists the survivors of a row and
+    // the top-p cut is taken over those lists (aligned rows)
+    const bool list_ok = use_min && a.vec;
 
     __shared__ __align__(16) float4 part[2][MC * kNW];          // warp partials, by use parity
     // top-p histograms hold fixed-point masses: weights 2^((l - l_max) c) <= 1
@@ -560,6 +635,16 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
     __shared__ float us[sv::kMaxRows];
     __shared__ float rsm[sv::kMaxRows], rss[sv::kMaxRows], pdr[sv::kMaxK];
     __shared__ float ctot[kNW][kChunks];                         // draw: chunk totals per warp
+    // min-p survivors: each warp's, then the CTA's (values and entry
+    // indices); the draw over a listed row reuses them
+    constexpr int CW = TR ? kCandW : 1, CC = TR ? kCandC : 1;
+    __shared__ float cw_v[kNW][CW];
+    __shared__ int cw_i[kNW][CW];
+    __shared__ int cw_n[kNW];
+    __shared__ float cl_v[CC];
+    __shared__ int cl_i[CC];
+    __shared__ int cl_cnt[kNW];
+    __shared__ float smax[kNW][TR ? kSlots : 1];                // row pass: group maxima
 
     const int64_t v0 = (int64_t)rank * a.slice;
     const int64_t L = v0 < V ? (V - v0 < a.slice ? V - v0 : a.slice) : 0;
@@ -580,6 +665,8 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
         xs[tid] = a.tokens[(int64_t)b * K + tid];
     if (tid <= K)
         us[tid] = a.u[row0 + tid];
+    if (tid < kNW)
+        cw_n[tid] = 0;
     __syncthreads();
     cluster_arrive();
     bool ready = false;
@@ -640,6 +727,8 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
     };
 
     int j = -1;
+    bool listed = false;                  // the decided row's kept set came from its survivor list
+    int ncl = 0;                          // ... this CTA's survivors in cl_v / cl_i
     float lmax = 0.f, E_kept = 0.f;       // the decided row's statistics
     float dmax = 0.f, dS = 0.f;           // ... and its draft row's (draft logits)
     uint32_t key_t = 0;                   // top-p: kept keys are >= key_t
@@ -662,11 +751,16 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
         // (partial: (max, S or -1 when bad, draft max, draft S or -1))
         float wmx, wsm, dmx = -INFINITY, dsm = 0.f;
         bool bad, dbad = false;
+        // (with min-p lists: the largest entry of every slot of batches)
+        const int batch_u = 32 * ((DL && i < K && a.vec) ? DP : DA);
+        const int nbat = (int)((w1 - w0 + batch_u - 1) / batch_u);
+        const int per = (nbat + kSlots - 1) / kSlots > 0 ? (nbat + kSlots - 1) / kSlots : 1;
+        SlotMax slm{TR && list_ok ? smax[warp] : nullptr, per};
         if (DL && i < K && a.vec) {
             warp_row_stats_pair<ES, DP>(a.logits, re, a.dlogits, ((int64_t)b * K + i) * V + v0, w0,
-                                        w1, lane, c, a.cd, wmx, wsm, bad, dmx, dsm, dbad);
+                                        w1, lane, c, a.cd, wmx, wsm, bad, dmx, dsm, dbad, &slm);
         } else {
-            warp_row_stats<ES, DA>(a, a.logits, re, w0, w1, lane, c, wmx, wsm, bad);
+            warp_row_stats<ES, DA>(a, a.logits, re, w0, w1, lane, c, wmx, wsm, bad, &slm);
             if (DL && i < K)
                 warp_row_stats<ES, DA>(a, a.dlogits, ((int64_t)b * K + i) * V + v0, w0, w1, lane,
                                        a.cd, dmx, dsm, dbad);
@@ -716,6 +810,7 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
         }
         const float S_all = E_kept;
         key_t = 0;
+        listed = false;
         // ---- B: the kept set ----
         if constexpr (TR) if (use_min || use_top) {
             // fixed point: 2^fix per unit weight, with fix chosen so that V
@@ -727,6 +822,68 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
             const float funscale = __int_as_float((127 - fix) << 23);    // 2^-fix
             const unsigned long long thr =
                 (unsigned long long)(a.top_p * (double)S_all * (double)fscale);
+            // With min-p on, one pass over the row lists its survivors
+            // (l - l_max >= T ln(min_p)); they are compacted per CTA (warp
+            // order, then the order found) and exchanged as values, and the cut
+            // is taken over the union of the lists in every CTA alike, with the
+            // same histograms as over the whole row.  A list past its capacity
+            // anywhere sends every CTA through the histogram passes instead.
+            int sL = -1;
+            if (list_ok) {
+                // only the slots of batches whose largest entry passes min-p
+                const int64_t su = (int64_t)slm.per * batch_u;  // units per slot
+                for (int sl = 0; sl < slm.s; ++sl) {
+                    if (!(smax[warp][sl] - lmax >= a.dmin))
+                        continue;
+                    const int64_t u0 = w0 + sl * su;
+                    visit<ES>(a, re, u0, u0 + su < w1 ? u0 + su : w1, lane,
+                              [&](float um) -> bool { return um - lmax >= a.dmin; },
+                              [&](float l, int64_t e) {
+                                  if (l - lmax >= a.dmin) {
+                                      const int pos = atomicAdd(&cw_n[warp], 1);
+                                      if (pos < kCandW) {
+                                          cw_v[warp][pos] = l;
+                                          cw_i[warp][pos] = (int)e;
+                                      }
+                                  }
+                              });
+                }
+                __syncwarp();
+                const int nw = cw_n[warp];
+                if (lane == 0)
+                    cl_cnt[warp] = nw <= kCandW ? nw : -1;
+                __syncthreads();
+                int off = 0, tot = 0;
+                bool ovf = false;
+                for (int w2 = 0; w2 < kNW; ++w2) {
+                    const int c2 = cl_cnt[w2];
+                    ovf = ovf || c2 < 0;
+                    off += (w2 < warp && c2 > 0) ? c2 : 0;
+                    tot += c2 > 0 ? c2 : 0;
+                }
+                ovf = ovf || tot > kCandC;
+                if (!ovf)
+                    for (int k = lane; k < nw; k += 32) {
+                        cl_v[off + k] = cw_v[warp][k];
+                        cl_i[off + k] = cw_i[warp][k];
+                    }
+                if (lane == 0)
+                    cw_n[warp] = 0;  // the next row lists afresh
+                ncl = ovf ? 0 : tot;
+                __syncthreads();     // the CTA's list is complete
+                float* stg = reinterpret_cast<float*>(hloc);  // [count or -1, values]
+                for (int k = tid; k <= ncl; k += kNT)
+                    stg[k] = k == 0 ? (ovf ? -1.f : (float)tot) : cl_v[k - 1];
+                sL = exchange_hist();
+                if (sL < 0) {
+                    state = SV_ERR_TIMEOUT;
+                    break;
+                }
+                bool any_ovf = false;
+                for (int r = 0; r < C; ++r)
+                    any_ovf = any_ovf || reinterpret_cast<const float*>(hrecv[sL][r])[0] < 0.f;
+                listed = !any_ovf;
+            }
             uint32_t prefix = 0;
             unsigned long long above = 0;  // mass of candidates with keys above the prefix group
             for (int lev = 0; lev < LEVELS; ++lev) {
@@ -743,27 +900,48 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
                         return false;
                     return lev == 0 || (key_of<ES>(um) >> sh_hi) >= prefix;
                 };
-                visit<ES>(a, re, w0, w1, lane, unit_may, [&](float l, int64_t) {
-                    if (use_min && !(l - lmax >= a.dmin))
-                        return;
-                    const uint32_t key = key_of<ES>(l);
-                    if (lev > 0 && (key >> sh_hi) != prefix)
-                        return;
-                    atomicAdd(&hloc[(key >> sh_lo) & 0xffu],
-                              __float2ull_rn(ex2((l - lmax) * c) * fscale));
-                });
-                const int s2 = exchange_hist();
-                if (s2 < 0) {
-                    state = SV_ERR_TIMEOUT;
-                    break;
+                int s2 = -1;
+                if (listed) {
+                    // the union of the survivor lists, every CTA the same
+                    for (int r = 0; r < C; ++r) {
+                        const float* lv = reinterpret_cast<const float*>(hrecv[sL][r]);
+                        const int nr = (int)lv[0];
+                        for (int k = tid; k < nr; k += kNT) {
+                            const float l = lv[1 + k];
+                            const uint32_t key = key_of<ES>(l);
+                            if (lev > 0 && (key >> sh_hi) != prefix)
+                                continue;
+                            atomicAdd(&hloc[(key >> sh_lo) & 0xffu],
+                                      __float2ull_rn(ex2((l - lmax) * c) * fscale));
+                        }
+                    }
+                    __syncthreads();
+                } else {
+                    visit<ES>(a, re, w0, w1, lane, unit_may, [&](float l, int64_t) {
+                        if (use_min && !(l - lmax >= a.dmin))
+                            return;
+                        const uint32_t key = key_of<ES>(l);
+                        if (lev > 0 && (key >> sh_hi) != prefix)
+                            return;
+                        atomicAdd(&hloc[(key >> sh_lo) & 0xffu],
+                                  __float2ull_rn(ex2((l - lmax) * c) * fscale));
+                    });
+                    s2 = exchange_hist();
+                    if (s2 < 0) {
+                        state = SV_ERR_TIMEOUT;
+                        break;
+                    }
                 }
                 // lane l holds bins 8l .. 8l+7, summed over the CTAs in a fixed order
                 unsigned long long bin[8];
 #pragma unroll
                 for (int t = 0; t < 8; ++t) {
                     unsigned long long acc = 0;
-                    for (int r = 0; r < C; ++r)
-                        acc += hrecv[s2][r][lane * 8 + t];
+                    if (listed)
+                        acc = hloc[lane * 8 + t];
+                    else
+                        for (int r = 0; r < C; ++r)
+                            acc += hrecv[s2][r][lane * 8 + t];
                     bin[t] = acc;
                 }
                 unsigned long long lt = 0;
@@ -814,6 +992,8 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
                 E_kept = __ull2float_rn(hab + hb) * funscale;
                 if (lev == LEVELS - 1)
                     key_t = prefix;
+                if (listed)
+                    __syncthreads();  // every warp has read the bins before they are cleared
             }
             if (state != SV_OK)
                 break;
@@ -1002,11 +1182,54 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
             return sum;
         };
         const int g32 = (int)g;  // steps per chunk (chunk ends counted, not divided)
+        // A listed row: p~_j is zero outside the survivors with keys >= key_t,
+        // so max(0, p~_j - q_j) and p~_j are too, and the draw's weights are
+        // those of the survivors alone, sorted into vocabulary order here
+        // (into cw_v / cw_i); q or the draft logit is read at those entries
+        // only.  The sampled draft row is still checked whole (a value that is
+        // not a probability anywhere in it is an error, as when it streams).
+        float* sv_v = &cw_v[0][0];
+        int* sv_i = &cw_i[0][0];
+        if (TR && listed) {
+            for (int k = tid; k < ncl; k += kNT) {
+                const int ik = cl_i[k];
+                int r = 0;
+                for (int m = 0; m < ncl; ++m)
+                    r += cl_i[m] < ik ? 1 : 0;
+                sv_v[r] = cl_v[k];
+                sv_i[r] = ik;
+            }
+            __syncthreads();
+        }
         for (int round = 0; round < 2; ++round) {
             float wt = 0.f, wtc = 0.f, cpart = 0.f;
             bool badq = false;
             int gcnt = 0, chunk = 0;
-            if constexpr (DL) if (a.vec) {
+            if (TR && listed) {
+                if (round == 0 && resid && !DL)
+                    badq = q_stretch_bad(qrow, w0 * E, w1 * E, lane, a.qvec != 0);
+                if (warp == 0) {
+                    // weights (scaled by E) in vocabulary order, kept in cl_v
+                    for (int k0 = 0; k0 < ncl; k0 += 32) {
+                        const int k = k0 + lane;
+                        float w = 0.f;
+                        if (k < ncl) {
+                            const float l = sv_v[k];
+                            const float ev = key_of<ES>(l) >= key_t ? ex2((l - lmax) * c) : 0.f;
+                            if (DL && resid && !fallback)
+                                w = fmaxf(ev - ex2((load_entry(a.dlogits, ES, dre + sv_i[k]) - dmax) *
+                                                   a.cd) * rq, 0.f);
+                            else if (resid && !fallback)
+                                w = fmaxf(ev - __ldg(qrow + sv_i[k]) * Ek, 0.f);
+                            else
+                                w = ev;
+                            cl_v[k] = w;
+                        }
+                        acc_add(wt, wtc, warp_sum(w));
+                    }
+                }
+            }
+            if constexpr (DL) if (a.vec && !(TR && listed)) {
                 constexpr int DD = TR ? 8 : 4;
                 const bool two = resid && !fallback;
                 // the steps st0 .. st0 + DD - 1 are units w0 + st * 32 + lane: one
@@ -1053,7 +1276,8 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
                     }
                 }
             }
-            for (int64_t st0 = 0; st0 < ((DL && a.vec) ? 0 : nsub); st0 += kDepth) {
+            for (int64_t st0 = 0; st0 < (((DL && a.vec) || (TR && listed)) ? 0 : nsub);
+                 st0 += kDepth) {
                 float l[kDepth][E], qv[kDepth][E];
                 bool have[kDepth];
 #pragma unroll
@@ -1124,96 +1348,125 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
         // ---- the owner warp locates the token and writes the outputs ----
         if (state == SV_OK && owner == rank * kNW + warp) {
             const float tl = t - cum_before;
-            // the chunk holding the crossing point (same sums as the total)
-            int fc = -1, lastc = -1;
-            float before = 0.f, lastc_before = 0.f;
-            {
-                float run = 0.f, rc = 0.f;
-                for (int ch = 0; ch < nch; ++ch) {
-                    const float x = ctot[warp][ch];
-                    const float cur = run - rc;
-                    if (x > 0.f) {
-                        lastc = ch;
-                        lastc_before = cur;
-                    }
-                    if (cur + x > tl) {
-                        fc = ch;
-                        before = cur;
-                        break;
-                    }
-                    acc_add(run, rc, x);
-                }
-            }
-            if (fc < 0) {  // rounding: the last chunk with weight
-                fc = lastc;
-                before = lastc_before;
-            }
-            float run = before;
-            int64_t tok = -1, last = -1;
-            const int64_t s_end = min(nsub, (int64_t)(fc + 1) * g);
-            for (int64_t st = (int64_t)fc * g; st < s_end && tok < 0; ++st) {
-                float l[E], qv[E], w[E];
-                bool dummy = false;
-                float lt = 0.f;
+            int64_t tok = -1;
+            if (TR && listed) {
+                // first survivor whose running weight passes the point, or
+                // (rounding) the last one with weight
+                float run = 0.f;
+                int pick = -1, lastk = -1;
+                for (int k0 = 0; k0 < ncl && pick < 0; k0 += 32) {
+                    const int k = k0 + lane;
+                    const float w = k < ncl ? cl_v[k] : 0.f;
+                    float inc = w;
 #pragma unroll
-                for (int k = 0; k < E; ++k)
-                    w[k] = 0.f;
-                const int64_t ui = w0 + st * 32 + lane;
-                bool packed = false;  // the totals pass took vec_weights
-                if constexpr (DL && !TR)
-                    packed = a.vec != 0;
-                if (packed) {
-                    if (ui < w1) {
-                        const bool two = resid && !fallback;
-                        const uint4 lr = ld_stream(rp + ui);
-                        const uint4 dr = two ? ld_stream(dp + ui) : lr;
-                        lt = vec_weights(lr, dr, two, w);
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const float v = __shfl_up_sync(kFull, inc, o);
+                        if (lane >= o)
+                            inc += v;
                     }
-                } else if (load_unit(st, l, qv)) {
-                    lt = unit_weights(l, qv, w, dummy);
+                    const unsigned pos = __ballot_sync(kFull, w > 0.f);
+                    if (pos)
+                        lastk = k0 + 31 - __clz(pos);
+                    const unsigned hit = __ballot_sync(kFull, w > 0.f && run + inc > tl);
+                    if (hit)
+                        pick = k0 + __ffs(hit) - 1;
+                    run += __shfl_sync(kFull, inc, 31);
                 }
-                int lpos = -1;
-                for (int k = 0; k < U; ++k)
-                    if (w[k] > 0.f)
-                        lpos = k;
-                const long long mylast = lpos >= 0 ? (long long)(ui * U + lpos) : -1ll;
-                long long wl_last = mylast;
-#pragma unroll
-                for (int o = 16; o; o >>= 1) {
-                    const long long ov = __shfl_xor_sync(kFull, wl_last, o);
-                    wl_last = wl_last > ov ? wl_last : ov;
-                }
-                if (wl_last > last)
-                    last = wl_last;
-                float inc = lt;  // inclusive scan of the lane sums
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const float v = __shfl_up_sync(kFull, inc, o);
-                    if (lane >= o)
-                        inc += v;
-                }
-                const unsigned hit = __ballot_sync(kFull, run + inc > tl);
-                if (hit) {
-                    const int src = __ffs(hit) - 1;
-                    long long pick = -1;
-                    if (lane == src) {
-                        float acc = run + inc - lt;
-                        for (int k = 0; k < U; ++k) {
-                            acc += w[k];
-                            if (acc > tl && w[k] > 0.f) {
-                                pick = ui * U + k;
-                                break;
-                            }
+                if (pick < 0)
+                    pick = lastk;
+                tok = pick >= 0 ? sv_i[pick] : 0;
+            } else {
+                // the chunk holding the crossing point (same sums as the total)
+                int fc = -1, lastc = -1;
+                float before = 0.f, lastc_before = 0.f;
+                {
+                    float run = 0.f, rc = 0.f;
+                    for (int ch = 0; ch < nch; ++ch) {
+                        const float x = ctot[warp][ch];
+                        const float cur = run - rc;
+                        if (x > 0.f) {
+                            lastc = ch;
+                            lastc_before = cur;
                         }
-                        if (pick < 0)  // the crossing fell on this lane's last weight
-                            pick = mylast;
+                        if (cur + x > tl) {
+                            fc = ch;
+                            before = cur;
+                            break;
+                        }
+                        acc_add(run, rc, x);
                     }
-                    tok = __shfl_sync(kFull, pick, src);
                 }
-                run += __shfl_sync(kFull, inc, 31);
+                if (fc < 0) {  // rounding: the last chunk with weight
+                    fc = lastc;
+                    before = lastc_before;
+                }
+                float run = before;
+                int64_t last = -1;
+                const int64_t s_end = min(nsub, (int64_t)(fc + 1) * g);
+                for (int64_t st = (int64_t)fc * g; st < s_end && tok < 0; ++st) {
+                    float l[E], qv[E], w[E];
+                    bool dummy = false;
+                    float lt = 0.f;
+    #pragma unroll
+                    for (int k = 0; k < E; ++k)
+                        w[k] = 0.f;
+                    const int64_t ui = w0 + st * 32 + lane;
+                    bool packed = false;  // the totals pass took vec_weights
+                    if constexpr (DL && !TR)
+                        packed = a.vec != 0;
+                    if (packed) {
+                        if (ui < w1) {
+                            const bool two = resid && !fallback;
+                            const uint4 lr = ld_stream(rp + ui);
+                            const uint4 dr = two ? ld_stream(dp + ui) : lr;
+                            lt = vec_weights(lr, dr, two, w);
+                        }
+                    } else if (load_unit(st, l, qv)) {
+                        lt = unit_weights(l, qv, w, dummy);
+                    }
+                    int lpos = -1;
+                    for (int k = 0; k < U; ++k)
+                        if (w[k] > 0.f)
+                            lpos = k;
+                    const long long mylast = lpos >= 0 ? (long long)(ui * U + lpos) : -1ll;
+                    long long wl_last = mylast;
+    #pragma unroll
+                    for (int o = 16; o; o >>= 1) {
+                        const long long ov = __shfl_xor_sync(kFull, wl_last, o);
+                        wl_last = wl_last > ov ? wl_last : ov;
+                    }
+                    if (wl_last > last)
+                        last = wl_last;
+                    float inc = lt;  // inclusive scan of the lane sums
+    #pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const float v = __shfl_up_sync(kFull, inc, o);
+                        if (lane >= o)
+                            inc += v;
+                    }
+                    const unsigned hit = __ballot_sync(kFull, run + inc > tl);
+                    if (hit) {
+                        const int src = __ffs(hit) - 1;
+                        long long pick = -1;
+                        if (lane == src) {
+                            float acc = run + inc - lt;
+                            for (int k = 0; k < U; ++k) {
+                                acc += w[k];
+                                if (acc > tl && w[k] > 0.f) {
+                                    pick = ui * U + k;
+                                    break;
+                                }
+                            }
+                            if (pick < 0)  // the crossing fell on this lane's last weight
+                                pick = mylast;
+                        }
+                        tok = __shfl_sync(kFull, pick, src);
+                    }
+                    run += __shfl_sync(kFull, inc, 31);
+                }
+                if (tok < 0)
+                    tok = last;
             }
-            if (tok < 0)
-                tok = last;
             const int32_t token = (int32_t)(v0 + tok);
             for (int i = lane; i <= K; i += 32) {
                 a.out_tokens[row0 + i] = i < j ? xs[i] : (i == j ? token : -1);
