@@ -316,6 +316,14 @@ static int verify_one(const void* logits, int dtype, const float* q, const int32
         const float* qj = dlog ? 0 : q + (size_t)j * (size_t)V;
         for (int64_t v = 0; v < V; ++v) {
             double qv;
+            if (tr && (tr->top_p < 1.0 || tr->min_p > 0.0) && p[v] == 0.0) {
+                /* Against a truncated target the residual max(0, p~ - q) is
+                 * zero wherever p~ is: q_j enters only at the kept tokens,
+                 * and is read (and checked) there alone, as q(x_i) is in the
+                 * test. */
+                w[v] = 0.0;
+                continue;
+            }
             if (dlog) {
                 qv = qrow[v]; /* row j: the last row tested */
             } else {

@@ -497,41 +497,6 @@ struct SlotMax {
     }
 };
 
-// Whether entries [e0, e1) of a sampled draft row hold a value that is not a
-// probability (negative, inf or NaN); `vec4`: 16-byte aligned, four at a time.
-__device__ __forceinline__ bool q_stretch_bad(const float* qrow, int64_t e0, int64_t e1, int lane,
-                                              bool vec4) {
-    bool bad = false;
-    const auto check = [&](uint32_t bits) {
-        const float x = __uint_as_float(bits);
-        bad = bad || !(x >= 0.f && x < INFINITY);
-    };
-    if (vec4) {
-        constexpr int D = 4;
-        const uint4* qp = reinterpret_cast<const uint4*>(qrow);
-        const int64_t u0 = e0 / 4, u1 = e1 / 4;
-        prefetch_start<D>(qp, u0, u1, lane);
-        for (int64_t b0 = u0; b0 < u1; b0 += 32 * D) {
-            prefetch_batch<D>(qp, b0 + kAhead * 32 * D, u1, lane);
-            uint4 r[D];
-            bool ok[D];
-            load_batch<D>(qp, b0, u1, lane, r, ok);
-#pragma unroll
-            for (int k = 0; k < D; ++k)
-                if (ok[k]) {
-                    check(r[k].x);
-                    check(r[k].y);
-                    check(r[k].z);
-                    check(r[k].w);
-                }
-        }
-    } else {
-        for (int64_t e = e0 + lane; e < e1; e += 32)
-            check(__float_as_uint(__ldg(qrow + e)));
-    }
-    return __any_sync(kFull, bad);
-}
-
 // One row's statistics over this warp's stretch of `base` (vector path; the
 // element path takes one entry at a time), D loads in flight per lane.
 template <int ES, int D>
@@ -608,7 +573,7 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
     constexpr int HC = TR ? kMaxC : 1;
     // row pass: loads in flight per lane and row (a target row alone, or the
     // target and draft rows together: deeper pairs spill registers)
-    constexpr int DA = (DL && !TR) ? 4 : kDepth;
+    constexpr int DA = (DL && !TR) ? 4 : ((TR && !DL) ? 8 : kDepth);
     constexpr int DP = (DL && !TR) ? 2 : 4;
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = (int)cluster.block_rank();
@@ -880,10 +845,65 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
                     break;
                 }
                 bool any_ovf = false;
-                for (int r = 0; r < C; ++r)
-                    any_ovf = any_ovf || reinterpret_cast<const float*>(hrecv[sL][r])[0] < 0.f;
+                int nall = 0;
+                for (int r = 0; r < C; ++r) {
+                    const float cr = reinterpret_cast<const float*>(hrecv[sL][r])[0];
+                    any_ovf = any_ovf || cr < 0.f;
+                    nall += cr > 0.f ? (int)cr : 0;
+                }
                 listed = !any_ovf;
+                if (listed && nall <= 64) {
+                    // A short union: every warp takes the cut itself.  Lane l
+                    // holds survivors l and l + 32 (in CTA order); a survivor is
+                    // kept when the fixed-point mass of the survivors with a
+                    // larger key is below top_p * S -- the same integers, and
+                    // so the same kept set and E, as the histogram levels give.
+                    float vv[2];
+                    uint32_t kk[2];
+                    unsigned long long ww[2], ab[2] = {0ull, 0ull};
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int f = lane + 32 * h;
+                        vv[h] = -INFINITY;
+                        for (int r = 0, base = 0; r < C; ++r) {
+                            const float* lv = reinterpret_cast<const float*>(hrecv[sL][r]);
+                            const int nr = (int)lv[0];
+                            if (f >= base && f < base + nr)
+                                vv[h] = lv[1 + f - base];
+                            base += nr;
+                        }
+                        kk[h] = f < nall ? key_of<ES>(vv[h]) : 0u;
+                        ww[h] = f < nall ? __float2ull_rn(ex2((vv[h] - lmax) * c) * fscale) : 0ull;
+                    }
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+                        for (int src = 0; src < 32; ++src) {
+                            const uint32_t ks = __shfl_sync(kFull, kk[h], src);
+                            const unsigned long long ws = __shfl_sync(kFull, ww[h], src);
+                            ab[0] += ks > kk[0] ? ws : 0ull;
+                            ab[1] += ks > kk[1] ? ws : 0ull;
+                        }
+                    unsigned long long ek = 0;
+                    uint32_t kmin = 0xffffffffu;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+                        if (lane + 32 * h < nall && (!use_top || ab[h] < thr)) {
+                            ek += ww[h];
+                            kmin = min(kmin, kk[h]);
+                        }
+#pragma unroll
+                    for (int o = 16; o; o >>= 1) {
+                        ek += __shfl_xor_sync(kFull, ek, o);
+                        kmin = min(kmin, __shfl_xor_sync(kFull, kmin, o));
+                    }
+                    E_kept = __ull2float_rn(ek) * funscale;
+                    key_t = use_top && nall > 0 ? kmin : 0u;
+                    if (lane == 0)
+                        cw_n[warp] = 0;  // (already clear; keeps the lists' state uniform)
+                    goto cut_done;
+                }
             }
+            {
             uint32_t prefix = 0;
             unsigned long long above = 0;  // mass of candidates with keys above the prefix group
             for (int lev = 0; lev < LEVELS; ++lev) {
@@ -999,6 +1019,8 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
                 break;
             if (!use_top)
                 key_t = 0;
+            }
+        cut_done:;
         }
         // ---- C: the test at position i ([P1]) ----
         if (i < K) {
@@ -1062,12 +1084,15 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
                                                          re * ES);
         const float Ek = E_kept;
         bool fallback = false;
-        // 2^((l - l_max) c) for a kept token, 0 for a dropped one
-        auto kept_w = [&](float l) -> float {
-            const bool kept = l > -INFINITY && (!use_min || l - lmax >= a.dmin) &&
-                              key_of<ES>(l) >= key_t;
-            return kept ? ex2((l - lmax) * c) : 0.f;
+        // whether a token is kept, and 2^((l - l_max) c) for a kept token, 0
+        // for a dropped one
+        auto is_kept = [&](float l) -> bool {
+            return l > -INFINITY && (!use_min || l - lmax >= a.dmin) && key_of<ES>(l) >= key_t;
         };
+        auto kept_w = [&](float l) -> float { return is_kept(l) ? ex2((l - lmax) * c) : 0.f; };
+        // with a filter on, q_j is read only at kept tokens (the residual is
+        // zero elsewhere) and checked there alone
+        const bool filt = use_min || use_top;
         // The stretch is walked in steps of 32 units (one per lane); g steps
         // make a chunk, whose total is kept in shared memory for the locate.
         const int64_t nsub = (w1 - w0 + 31) / 32;
@@ -1125,7 +1150,7 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
                     // qv holds the draft logits (checked when the row was read)
                     w[t] = fmaxf(ev - ex2((qv[t] - dmax) * a.cd) * rq, 0.f);
                 } else if (resid && !fallback) {
-                    if (!(qv[t] >= 0.f && qv[t] < INFINITY))
+                    if (!(qv[t] >= 0.f && qv[t] < INFINITY) && (!filt || is_kept(l[t])))
                         badq = true;
                     w[t] = fmaxf(ev - qv[t] * Ek, 0.f);
                 } else {
@@ -1185,9 +1210,8 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
         // A listed row: p~_j is zero outside the survivors with keys >= key_t,
         // so max(0, p~_j - q_j) and p~_j are too, and the draw's weights are
         // those of the survivors alone, sorted into vocabulary order here
-        // (into cw_v / cw_i); q or the draft logit is read at those entries
-        // only.  The sampled draft row is still checked whole (a value that is
-        // not a probability anywhere in it is an error, as when it streams).
+        // (into cw_v / cw_i); q or the draft logit is read, and q checked, at
+        // the kept entries only.
         float* sv_v = &cw_v[0][0];
         int* sv_i = &cw_i[0][0];
         if (TR && listed) {
@@ -1206,8 +1230,6 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
             bool badq = false;
             int gcnt = 0, chunk = 0;
             if (TR && listed) {
-                if (round == 0 && resid && !DL)
-                    badq = q_stretch_bad(qrow, w0 * E, w1 * E, lane, a.qvec != 0);
                 if (warp == 0) {
                     // weights (scaled by E) in vocabulary order, kept in cl_v
                     for (int k0 = 0; k0 < ncl; k0 += 32) {
@@ -1215,14 +1237,18 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
                         float w = 0.f;
                         if (k < ncl) {
                             const float l = sv_v[k];
-                            const float ev = key_of<ES>(l) >= key_t ? ex2((l - lmax) * c) : 0.f;
-                            if (DL && resid && !fallback)
+                            const bool kept = key_of<ES>(l) >= key_t;
+                            const float ev = kept ? ex2((l - lmax) * c) : 0.f;
+                            if (DL && resid && !fallback) {
                                 w = fmaxf(ev - ex2((load_entry(a.dlogits, ES, dre + sv_i[k]) - dmax) *
                                                    a.cd) * rq, 0.f);
-                            else if (resid && !fallback)
-                                w = fmaxf(ev - __ldg(qrow + sv_i[k]) * Ek, 0.f);
-                            else
+                            } else if (resid && !fallback && kept) {
+                                const float qv = __ldg(qrow + sv_i[k]);
+                                badq = badq || !(qv >= 0.f && qv < INFINITY);
+                                w = fmaxf(ev - qv * Ek, 0.f);
+                            } else if (!resid || fallback) {
                                 w = ev;
+                            }
                             cl_v[k] = w;
                         }
                         acc_add(wt, wtc, warp_sum(w));

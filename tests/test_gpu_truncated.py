@@ -152,3 +152,29 @@ def test_repeated_runs_with_filters_are_bit_identical(entry):
     for r in runs[1:]:
         for k in runs[0]:
             np.testing.assert_array_equal(runs[0][k], r[k], err_msg=k)
+
+
+def test_draft_values_checked_at_kept_tokens_only():
+    """Against the truncated target q_j is read, and checked, where p~_j > 0:
+    a NaN at a dropped token of the rejected row leaves the sequence as it
+    was, a NaN at a kept token makes it an error -- on the survivor-list path
+    (min-p on) and on the row path (top-p alone)."""
+    import torch
+    inp = workloads.make_random(8, 3, 4000, "bf16", T=0.7, sigma=3.0, seed=52)
+    for top_p, min_p in ((0.95, 0.05), (0.9, 0.0)):
+        base = oracle.verify_truncated(inp.logits, inp.dtype, inp.q, inp.tokens, inp.uniforms,
+                                       inp.T, top_p, min_p)
+        rej = [b for b in range(inp.B) if base["status"][b] == 0 and base["accept_len"][b] <= inp.K]
+        assert len(rej) >= 2
+        lgf = (inp.logits.astype(np.uint32) << 16).view(np.float32)
+        q = inp.q.copy()
+        b0, b1 = rej[0], rej[1]
+        j0, j1 = base["accept_len"][b0] - 1, base["accept_len"][b1] - 1
+        q[b0, j0, int(np.argmin(lgf[b0, j0]))] = np.nan   # dropped by either filter
+        q[b1, j1, int(np.argmax(lgf[b1, j1]))] = np.nan   # always kept
+        bad = workloads.Inputs(inp.name, inp.B, inp.K, inp.V, inp.dtype, inp.T, inp.logits, q,
+                               inp.tokens, inp.uniforms)
+        info, o = _check(bad, top_p, min_p, f"q NaN p={top_p} m={min_p}")
+        assert o["status"][b0] == 0 and o["status"][b1] == oracle.NONFINITE
+        np.testing.assert_array_equal(o["out_tokens"][b0], base["out_tokens"][b0])
+    torch.cuda.synchronize()

@@ -152,6 +152,34 @@ def test_output_law_is_the_truncated_target(seed):
     check_output_law(oracle.verify_truncated, seed=seed)
 
 
+def test_draft_values_are_checked_where_the_residual_reads_them():
+    """Against a truncated target the residual max(0, p~_j - q_j) is zero
+    wherever p~_j is, so q_j is read, and checked, at the kept tokens only: a
+    NaN at a dropped token changes nothing, a NaN at a kept one is an error
+    (as for q(x_i) in the test).  With both filters off every entry is read."""
+    V = 6
+    logits = np.log(np.array([0.5, 0.3, 0.1, 0.05, 0.03, 0.02])).astype(np.float32)
+    lg = np.broadcast_to(logits, (1, 2, V)).copy()
+    q = np.full((1, 1, V), 1.0 / V, np.float32)
+    x = np.array([[5]], np.int32)               # p(5) < q(5) u at u = 0.99: rejected
+    u = np.array([[0.99, 0.5]], np.float32)
+    base = oracle.verify_truncated(lg, "f32", q, x, u, 1.0, 0.95, 0.15)
+    assert base["status"][0] == 0 and base["accept_len"][0] == 1
+    kept = {0, 1, 2}                            # min-p 0.15: p >= 0.075
+    for v in range(V):
+        qq = q.copy()
+        qq[0, 0, v] = np.nan
+        out = oracle.verify_truncated(lg, "f32", qq, x, u, 1.0, 0.95, 0.15)
+        if v in kept:
+            assert out["status"][0] == oracle.NONFINITE, v
+        elif v == 5:                            # q(x_0) itself, read by the test
+            assert out["status"][0] == oracle.NONFINITE
+        else:
+            assert out["status"][0] == 0 and out["out_tokens"][0, 0] == base["out_tokens"][0, 0], v
+        off = oracle.verify_truncated(lg, "f32", qq, x, u, 1.0, 1.0, 0.0)
+        assert off["status"][0] == oracle.NONFINITE, v
+
+
 def test_argument_checks():
     inp = workloads.make_random(2, 1, 50, "f32", seed=1)
     for top_p, min_p in ((0.0, 0.0), (0.5, 1.0), (np.nan, 0.0)):
