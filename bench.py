@@ -161,7 +161,8 @@ def algorithmic_bytes(inp, accept_len: np.ndarray) -> int:
       + 4 per test that ran (q(x_i) gathered), min(n, K) tests
       + K * 4 (draft tokens) + (K + 1) * 4 (uniforms)
       + outputs: 4 + (K + 1) * 4 + K
-    The logits of row j are re-used for the draw from shared memory, not re-read.
+    The method needs row j once: the draw's second read of it (and rows read
+    before a rejection was known) are traffic, not algorithmic bytes.
     """
     B, K, V, es = inp.B, inp.K, inp.V, inp.logit_bytes
     n = accept_len.astype(np.int64)
@@ -170,6 +171,18 @@ def algorithmic_bytes(inp, accept_len: np.ndarray) -> int:
     tests = int(np.minimum(n, K).sum())
     return (rows * V * es + rejected * V * 4 + tests * 4 + B * K * 4 + B * (K + 1) * 4
             + B * (4 + (K + 1) * 4 + K))
+
+
+def algorithmic_bytes_truncated(inp, accept_len: np.ndarray, min_p: float) -> int:
+    """As algorithmic_bytes, except that with min-p on the residual reads q_j
+    only at the kept tokens (max(0, p~ - q) is zero elsewhere): the rejected
+    draft row's V * 4 bytes drop out (its few kept entries, 4-byte gathers,
+    are not counted).  With min-p off the draw streams q_j whole."""
+    full = algorithmic_bytes(inp, accept_len)
+    if min_p <= 0.0:
+        return full
+    rejected = int((accept_len.astype(np.int64) <= inp.K).sum())
+    return full - rejected * inp.V * 4
 
 
 def algorithmic_bytes_ragged(rg, accept_len: np.ndarray) -> int:
@@ -474,7 +487,8 @@ def run_ours(args):
     acc = outs["accept_len"].cpu().numpy()
     alg = (algorithmic_bytes_greedy(inp, acc) if greedy else
            algorithmic_bytes_ragged(rg, acc) if ragged else
-           algorithmic_bytes_draft_logits(inp, acc) if dlog else algorithmic_bytes(inp, acc))
+           algorithmic_bytes_draft_logits(inp, acc) if dlog else
+           algorithmic_bytes_truncated(inp, acc, args.min_p) if trunc else algorithmic_bytes(inp, acc))
     avg_launch_s = local_ms / args.steps / 1e3  # this rank's average launch duration
     value = world * rows_per_step * args.steps / (total_ms / 1e3)
     tokens_per_step = int(acc.sum())

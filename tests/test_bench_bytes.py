@@ -25,11 +25,14 @@ def _per_sequence(K, V, es, n, kind):
     if kind == "draft_logits":                    # every tested draft row, whole
         return rows + min(n, K) * V * es + tokens + uniforms + outputs
     rejected = V * 4 if n <= K else 0             # the rejected row of q
+    if kind == "truncated_min_p":                 # q_j read at kept tokens only
+        rejected = 0
     gathered = min(n, K) * 4                      # q(x) of each test
     return rows + rejected + gathered + tokens + uniforms + outputs
 
 
-@pytest.mark.parametrize("kind", ["sampled", "greedy", "draft_logits"])
+@pytest.mark.parametrize("kind", ["sampled", "greedy", "draft_logits", "truncated_min_p",
+                                  "truncated_top_p"])
 @pytest.mark.parametrize("B,K,V,dtype", [(256, 7, 128256, "bf16"), (1, 4, 32000, "f32"),
                                          (5, 0, 1000, "bf16"), (3, 32, 7, "f32")])
 def test_uniform_batches(kind, B, K, V, dtype):
@@ -37,9 +40,12 @@ def test_uniform_batches(kind, B, K, V, dtype):
     rng = np.random.default_rng(B + K + V)
     for al in (rng.integers(1, K + 2, B), np.ones(B, np.int64), np.full(B, K + 1)):
         al = al.astype(np.int32)
-        want = sum(_per_sequence(K, V, inp.logit_bytes, int(n), kind) for n in al)
+        want = sum(_per_sequence(K, V, inp.logit_bytes, int(n),
+                                 "sampled" if kind == "truncated_top_p" else kind) for n in al)
         fn = {"sampled": bench.algorithmic_bytes, "greedy": bench.algorithmic_bytes_greedy,
-              "draft_logits": bench.algorithmic_bytes_draft_logits}[kind]
+              "draft_logits": bench.algorithmic_bytes_draft_logits,
+              "truncated_min_p": lambda i, a: bench.algorithmic_bytes_truncated(i, a, 0.05),
+              "truncated_top_p": lambda i, a: bench.algorithmic_bytes_truncated(i, a, 0.0)}[kind]
         assert fn(inp, al) == want
 
 
