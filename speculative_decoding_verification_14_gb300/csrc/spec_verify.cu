@@ -1272,9 +1272,13 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
             const bool use_ring = RESID && a.qvec;
             FF wacc = {0.f, 0.f};
             int qissued = 0;
-            // the draft row's stages go out up to kStages tiles ahead
+            // the draft row's stages go out up to kStages tiles ahead -- one
+            // for a rejection in the first half of the drafts: such a draw
+            // has the most time before the batch's last sequences finish,
+            // and its copies in flight would lengthen the memory queues the
+            // rows of the sequences still testing wait in
             auto q_top_up = [&](int t) {
-                while (qissued < ntile && qissued < t + kStages) {
+                while (qissued < ntile && qissued < t + (2 * j < K ? 1 : kStages)) {
                     issue(qbase + (size_t)qissued * kDrawTile,
                           (uint32_t)(min(kDrawTile, nq32 - qissued * kDrawTile) * 4), true);
                     ++qissued;
