@@ -193,11 +193,17 @@ int spec_verify_run_ragged(sv_ctx* ctx,
  * top_p >= 1 turns top-p off, min_p <= 0 turns min-p off (both off: the same
  * outputs as spec_verify_run up to rounding).
  *
- * Arguments, layouts and errors as spec_verify_run; row_stats are those of the
+ * Arguments, layouts and errors as spec_verify_run, except that with a filter
+ * on the rejected draft row q_j is read -- and checked for values that are
+ * not probabilities (SV_ERR_NONFINITE) -- only at the kept tokens, since
+ * max(0, p~_j - q_j) is zero wherever p~_j is; row_stats are those of the
  * untruncated softmax of the rows read, p_draft = p~(x_i).  Requires
- * 0 < top_p and min_p < 1 (SV_ERR_INVALID_ARG otherwise).  The kernel reads
- * each row it reaches two (bf16) to four (f32) more times from L2 for the
- * top-p cut; clusters have at most 8 CTAs. */
+ * 0 < top_p and min_p < 1 (SV_ERR_INVALID_ARG otherwise).  With min-p on, the
+ * kernel reads each row it reaches once in full and then only the stretches
+ * that can hold min-p survivors, and takes the top-p cut and the draw over
+ * the survivors; without min-p (or with more survivors than its lists hold)
+ * it takes the cut by histogram passes over the row, two (bf16) to four (f32)
+ * more reads from L2.  Clusters have at most 8 CTAs. */
 int spec_verify_run_truncated(sv_ctx* ctx,
                               const void* target_logits, int logits_dtype,
                               const float* q, const int32_t* draft_tokens, const float* uniforms,
@@ -233,7 +239,8 @@ int spec_verify_plan_truncated_for(int num_sms, int max_cluster, int B, int K, i
  * (row_stats: the target rows' untruncated statistics; p_draft: p~(x_i)).
  *
  * Bytes: each row the pass reaches is read with its draft row (rows after the
- * first rejection are never read), plus the rejected pair again for the draw.
+ * first rejection are never read), plus the rejected pair again for the draw
+ * (with min-p on, only the kept tokens of the pair).
  * Device-detected errors as spec_verify_run, plus: a draft row the pass
  * reaches holding a NaN or +inf, or only -inf, is SV_ERR_NONFINITE for that
  * sequence.  16-byte aligned target and draft rows (V * element size a
