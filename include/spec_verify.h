@@ -97,6 +97,8 @@ typedef struct {
     int64_t grid;      /* CTAs in the launch = B * cluster                             */
     int bulk_copy;     /* 1: row slices move with cp.async.bulk; 0: element-wise loads */
     int prefetch_next; /* 1: the next row slice is prefetched into L2 while one is reduced */
+    int stages;        /* 2 KB ring stages per warp (3, or 6 for batches that leave SMs
+                          room; 0 for the kernels without a ring)                     */
 } sv_plan;
 
 /* Create a context on `device` for calls with B <= max_B, K <= max_K (<= 32)

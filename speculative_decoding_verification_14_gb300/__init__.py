@@ -31,7 +31,7 @@ class SpecVerifyError(RuntimeError):
 class sv_plan(ctypes.Structure):
     _fields_ = [("cluster", ctypes.c_int), ("group", ctypes.c_int), ("threads", ctypes.c_int),
                 ("smem_bytes", ctypes.c_int), ("slice", ctypes.c_int64), ("grid", ctypes.c_int64),
-                ("bulk_copy", ctypes.c_int), ("prefetch_next", ctypes.c_int)]
+                ("bulk_copy", ctypes.c_int), ("prefetch_next", ctypes.c_int), ("stages", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         return {f: getattr(self, f) for f, _ in self._fields_}

@@ -20,6 +20,9 @@
 // row is decided); all K+1 for batches too small to fill it, where latency
 // rules and one barrier decides every row.
 //
+// Ring depth: three 2 KB stages per warp, or six when the plan's CTAs fit at
+// four per SM with the deeper rings (batches that leave SMs room).
+//
 // [P1] = reactapp.top, "Speculative decoding and early exit: speeding up
 // autoregressive decode", section "Speculative decoding: draft first, then
 // verify".
@@ -89,6 +92,20 @@ int plan_impl(int num_sms, int smem_per_cta, int max_cluster, int B, int K, int6
     }
     if (l.total > smem_per_cta)
         return SV_ERR_UNSUPPORTED;
+    // Deeper rings when the plan's CTAs are few enough to be resident at the
+    // deep kernels' occupancy: a warp then keeps more of its stretch in flight,
+    // which shortens every step of a latency-bound chain.
+    int stages = kStages;
+    if (threads == 128) {
+        const Layout ld = layout_for(slice, es, G, threads, C, kStagesDeep);
+        int64_t per_sm_deep = (int64_t)kSmemPerSM / (ld.total + kSmemPerCtaReserved);
+        if (per_sm_deep > kDeepCtasPerSM)
+            per_sm_deep = kDeepCtasPerSM;
+        if (ld.total <= smem_per_cta && (int64_t)B * C <= per_sm_deep * num_sms) {
+            stages = kStagesDeep;
+            l = ld;
+        }
+    }
     out->cluster = C;
     out->group = G;
     out->threads = threads;
@@ -97,6 +114,7 @@ int plan_impl(int num_sms, int smem_per_cta, int max_cluster, int B, int K, int6
     out->grid = (int64_t)B * C;
     out->bulk_copy = ((V * es) % 16) == 0 ? 1 : 0;
     out->prefetch_next = G == 1 ? 1 : 0;
+    out->stages = stages;
     return SV_OK;
 }
 
@@ -157,6 +175,7 @@ int plan_rows(int num_sms, int max_cluster, int B, int K, int64_t V, int logits_
     out->grid = (int64_t)B * C;
     out->bulk_copy = ((V * es) % 16) == 0 ? 1 : 0;
     out->prefetch_next = 0;
+    out->stages = 0;  // no shared-memory ring
     return SV_OK;
 }
 

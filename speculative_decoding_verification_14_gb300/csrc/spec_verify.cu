@@ -57,7 +57,6 @@ namespace {
 
 using sv::kMaxK;
 using sv::kMaxRows;
-using sv::kStages;
 using sv::kChunkBytes;
 
 constexpr unsigned kFull = 0xffffffffu;
@@ -724,8 +723,10 @@ __device__ __forceinline__ bool q_bits_valid(uint32_t qbits) {
 
 // Residency target: sv::kThreadsPerSM threads per SM, seven CTAs of 128 (shared
 // memory allows no more), so a thread may use up to 72 registers.
-template <int ES, int NT>
-__global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(const __grid_constant__ SvArgs a) {
+template <int ES, int NT, int S>
+__global__ void __launch_bounds__(NT, S == sv::kStages ? sv::kThreadsPerSM / NT : sv::kDeepCtasPerSM)
+    sv_verify_kernel(const __grid_constant__ SvArgs a) {
+    constexpr int kStages = S;  // ring stages per warp
     constexpr int E = Elem<ES>::E;
     constexpr int NW = NT / 32;
     static_assert(NW <= kMaxWarps, "too many warps");
@@ -1674,15 +1675,20 @@ __global__ void __launch_bounds__(NT, sv::kThreadsPerSM / NT) sv_verify_kernel(c
 
 using KernelFn = void (*)(SvArgs);
 
-KernelFn pick_kernel(int es, int threads) {
+KernelFn pick_kernel(int es, int threads, int stages = sv::kStages) {
+    if (stages == sv::kStagesDeep) {
+        if (threads != 128)
+            return nullptr;
+        return es == 2 ? sv_verify_kernel<2, 128, sv::kStagesDeep> : sv_verify_kernel<4, 128, sv::kStagesDeep>;
+    }
     if (es == 2) {
-        if (threads == 128) return sv_verify_kernel<2, 128>;
-        if (threads == 256) return sv_verify_kernel<2, 256>;
-        if (threads == 512) return sv_verify_kernel<2, 512>;
+        if (threads == 128) return sv_verify_kernel<2, 128, sv::kStages>;
+        if (threads == 256) return sv_verify_kernel<2, 256, sv::kStages>;
+        if (threads == 512) return sv_verify_kernel<2, 512, sv::kStages>;
     } else {
-        if (threads == 128) return sv_verify_kernel<4, 128>;
-        if (threads == 256) return sv_verify_kernel<4, 256>;
-        if (threads == 512) return sv_verify_kernel<4, 512>;
+        if (threads == 128) return sv_verify_kernel<4, 128, sv::kStages>;
+        if (threads == 256) return sv_verify_kernel<4, 256, sv::kStages>;
+        if (threads == 512) return sv_verify_kernel<4, 512, sv::kStages>;
     }
     return nullptr;
 }
@@ -1766,11 +1772,12 @@ int launch(sv_ctx* ctx, const void* logits, int dtype, const float* q, const int
     if (rc != SV_OK)
         return rc;
     const int es = dtype == SV_BF16 ? 2 : 4;
-    KernelFn fn = pick_kernel(es, plan.threads);
+    KernelFn fn = pick_kernel(es, plan.threads, plan.stages);
     if (!fn)
         return SV_ERR_UNSUPPORTED;
 
-    const sv::Layout lay = sv::layout_for(plan.slice, es, plan.group, plan.threads, plan.cluster);
+    const sv::Layout lay =
+        sv::layout_for(plan.slice, es, plan.group, plan.threads, plan.cluster, plan.stages);
     SvArgs args;
     std::memset(&args, 0, sizeof args);
     args.logits = logits;
@@ -1858,10 +1865,10 @@ int device_setup(int device, DeviceInfo* info) {
         return SV_ERR_UNSUPPORTED;
     int max_cluster = 16;
     const int es_list[2] = {2, 4};
-    const int nt_list[3] = {128, 256, 512};
+    const int nt_list[4] = {128, 256, 512, 0};  // 0: the deep-ring kernel (128 threads)
     for (int es : es_list)
         for (int nt : nt_list) {
-            KernelFn fn = pick_kernel(es, nt);
+            KernelFn fn = nt ? pick_kernel(es, nt) : pick_kernel(es, 128, sv::kStagesDeep);
             if (cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      optin) != cudaSuccess) {
                 (void)cudaGetLastError();

@@ -11,7 +11,12 @@ constexpr int kMaxK = 32;               // drafts per sequence
 constexpr int kMaxRows = kMaxK + 1;     // target rows per sequence
 constexpr int kMaxCluster = 16;         // CTAs per thread-block cluster (non-portable limit)
 constexpr int kSliceAlign = 8;          // slices start on 8-entry boundaries (16 bytes of bf16)
-constexpr int kStages = 3;              // ring stages per warp
+constexpr int kStages = 3;              // ring stages per warp (batches that fill the GPU)
+// Batches whose clusters leave SMs room take deeper rings: kStagesDeep
+// stages per warp, kDeepCtasPerSM 128-thread CTAs per SM (the launch bounds
+// of those kernels), so a warp keeps more of its stretch in flight.
+constexpr int kStagesDeep = 6;
+constexpr int kDeepCtasPerSM = 4;
 // Wait limits (fixed; nothing at run time shortens them).  A wait on another
 // CTA's or warp's progress (pushed partials, a posted decision) gives up after
 // kWaitNs and the sequence reports SV_ERR_TIMEOUT.  A wait on one of the
@@ -49,15 +54,16 @@ struct Layout {
 
 constexpr int kExchangeBarriers = 4;
 
-inline Layout layout_for(int64_t slice, int elem_bytes, int group, int threads, int cluster) {
+inline Layout layout_for(int64_t slice, int elem_bytes, int group, int threads, int cluster,
+                         int stages = kStages) {
     const int64_t nw = threads / 32;
     const int64_t E = 16 / elem_bytes;
     Layout l;
     l.wvec = ceil_div(ceil_div(slice, E), nw);
     l.ntw = ceil_div(l.wvec * E, kDrawTile);
-    l.off_fixed = nw * kStages * kChunkBytes;
+    l.off_fixed = nw * stages * kChunkBytes;
     l.off_bar = l.off_fixed + kFixedSmem;
-    l.off_part = l.off_bar + round_up((nw * kStages + kExchangeBarriers) * 8, 16);
+    l.off_part = l.off_bar + round_up((nw * stages + kExchangeBarriers) * 8, 16);
     l.off_tt = l.off_part + round_up(2 * (int64_t)group * cluster * nw * 16, 16);
     l.total = l.off_tt + round_up(nw * l.ntw * 4, 16);
     return l;

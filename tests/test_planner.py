@@ -56,6 +56,32 @@ def test_workload_plans(sv):
     assert (p["cluster"], p["group"]) == (8, 1)
 
 
+@pytest.mark.parametrize("B,K,V,dtype", list(itertools.product(
+    [1, 8, 64, 128, 152, 256, 1024], [0, 3, 7], [32000, 128256, 151936], [0, 1])))
+def test_ring_depth(sv, B, K, V, dtype):
+    """Six ring stages exactly when the plan has 128 threads and its CTAs are
+    all resident at the deep kernels' occupancy (at most four per SM, as the
+    deeper rings' shared memory allows); three otherwise."""
+    rc, p = plan(sv, B, K, V, dtype)
+    assert rc == sv.SV_OK
+    assert p["stages"] in (3, 6)
+    if p["stages"] == 6:
+        per_sm = min(4, 233472 // (p["smem_bytes"] + 1024))
+        assert p["threads"] == 128 and p["grid"] <= per_sm * 152
+    else:
+        # with three more stages per warp the plan's CTAs would not all be
+        # resident at the deep kernels' occupancy (or the plan is wider)
+        per_sm = min(4, 233472 // (p["smem_bytes"] + 3 * 4 * 2048 + 1024))
+        assert p["threads"] != 128 or p["grid"] > per_sm * 152
+
+
+def test_workload_ring_depths(sv):
+    assert plan(sv, 256, 7, 128256, 1)[1]["stages"] == 3     # 1024 CTAs: seven per SM
+    assert plan(sv, 64, 3, 151936, 1)[1]["stages"] == 6      # 512 CTAs
+    assert plan(sv, 8, 4, 32000, 1)[1]["stages"] == 6
+    assert plan(sv, 1, 4, 32000, 0)[1]["stages"] == 6
+
+
 def test_overrides(sv):
     rc, p = plan(sv, 4, 5, 50000, 1, oc=4, og=3, ot=512)
     assert rc == 0 and (p["cluster"], p["group"], p["threads"]) == (4, 3, 512)
