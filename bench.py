@@ -119,7 +119,7 @@ KERNEL_SOURCES = {
     "ragged": ("spec_verify.cu", "sv_internal.h", "planner.cpp"),
     "greedy": ("greedy.cu", "spec_verify.cu", "sv_internal.h", "planner.cpp"),
     "truncated": ("truncated.cu", "spec_verify.cu", "sv_internal.h", "planner.cpp"),
-    "draft_logits": ("truncated.cu", "spec_verify.cu", "sv_internal.h", "planner.cpp"),
+    "draft_logits": ("spec_verify.cu", "sv_internal.h", "planner.cpp"),
 }
 
 

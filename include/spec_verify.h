@@ -231,7 +231,9 @@ int spec_verify_plan_truncated_for(int num_sms, int max_cluster, int B, int K, i
  * the same pass as the target row's, so no q array exists anywhere.  top_p < 1
  * or min_p > 0 verify against the truncated target exactly as
  * spec_verify_run_truncated does (q itself is never truncated); top_p >= 1
- * with min_p <= 0 is the plain verify.
+ * with min_p <= 0 is the plain verify, run by spec_verify_run's kernel in its
+ * draft-logit form: each test row's draft row streams through the same
+ * shared-memory ring right after it.
  *
  *   draft_logits [B, K, V]  the target's dtype (logits_dtype), device; row i is
  *                           the drafter's scores at position i (may be NULL
@@ -241,8 +243,9 @@ int spec_verify_plan_truncated_for(int num_sms, int max_cluster, int B, int K, i
  * (row_stats: the target rows' untruncated statistics; p_draft: p~(x_i)).
  *
  * Bytes: each row the pass reaches is read with its draft row (rows after the
- * first rejection are never read), plus the rejected pair again for the draw
- * (with min-p on, only the kept tokens of the pair).
+ * first rejection are never read; without filters the row after it is read
+ * only as far as it got before the decision), plus the rejected pair again
+ * for the draw (with min-p on, only the kept tokens of the pair).
  * Device-detected errors as spec_verify_run, plus: a draft row the pass
  * reaches holding a NaN or +inf, or only -inf, is SV_ERR_NONFINITE for that
  * sequence.  16-byte aligned target and draft rows (V * element size a
@@ -266,9 +269,10 @@ int spec_verify_get_plan_draft_logits(sv_ctx* ctx, int B, int K, int64_t V, int 
                                       int filters, sv_plan* out);
 
 /* Its planner as a pure host function (no CUDA call), for tests: the
- * truncated planner when filters is 1; without filters clusters of up to 16
- * CTAs (capped by max_cluster), seven resident 128-thread CTAs per SM (four
- * with a filter on). */
+ * truncated planner when filters is 1; without filters spec_verify_plan_for's
+ * mapping for 128-thread CTAs with the 227 KB of shared memory a GB300 CTA
+ * may opt into, and room for two rows of partials (target and draft) per
+ * group row. */
 int spec_verify_plan_draft_logits_for(int num_sms, int max_cluster, int B, int K, int64_t V,
                                       int logits_dtype, int filters, int ovr_cluster,
                                       sv_plan* out);

@@ -31,8 +31,10 @@
 
 namespace {
 
+// dl: verification with draft logits -- every test row's draft row streams
+// with it, so each group row holds two rows of partials; 128 threads only.
 int plan_impl(int num_sms, int smem_per_cta, int max_cluster, int B, int K, int64_t V, int dtype,
-              int ovr_cluster, int ovr_group, int ovr_threads, sv_plan* out) {
+              int ovr_cluster, int ovr_group, int ovr_threads, sv_plan* out, bool dl = false) {
     using namespace sv;
     if (!out || num_sms < 1 || smem_per_cta < 1 || max_cluster < 1 || B < 1 || K < 0 ||
         K > kMaxK || V < 1 || V > ((int64_t)1 << 31) || (dtype != SV_F32 && dtype != SV_BF16))
@@ -45,7 +47,10 @@ int plan_impl(int num_sms, int smem_per_cta, int max_cluster, int B, int K, int6
     const int es = dtype == SV_BF16 ? 2 : 4;
     const int E = 16 / es;
     const int rows = K + 1;
+    if (dl && ovr_threads != 0 && ovr_threads != 128)
+        return SV_ERR_INVALID_ARG;
     const int threads = ovr_threads ? ovr_threads : 128;
+    const int pr = dl ? 2 : 1;  // partial rows per group row
     const int nw = threads / 32;
     const int cmax = max_cluster < kMaxCluster ? max_cluster : kMaxCluster;
     const int64_t min_slice = (int64_t)nw * (kChunkBytes / 16) * E / 2;  // half a stage per warp
@@ -55,7 +60,7 @@ int plan_impl(int num_sms, int smem_per_cta, int max_cluster, int B, int K, int6
     const int64_t min_slice_full = (int64_t)nw * 4 * (kChunkBytes / 16) * E;
 
     // resident CTAs per SM with a single-row plan (threads and shared memory)
-    const int64_t smem1 = layout_for(round_up(ceil_div(V, 4), kSliceAlign), es, 1, threads, 4).total;
+    const int64_t smem1 = layout_for(round_up(ceil_div(V, 4), kSliceAlign), es, pr, threads, 4).total;
     int64_t per_sm = (int64_t)kSmemPerSM / (smem1 + kSmemPerCtaReserved);
     const int64_t by_threads = kThreadsPerSM / threads;  // the kernels' launch bounds
     if (per_sm > by_threads)
@@ -85,10 +90,10 @@ int plan_impl(int num_sms, int smem_per_cta, int max_cluster, int B, int K, int6
         G = (int64_t)B * C >= num_sms ? 1 : rows;
 
     const int64_t slice = round_up(ceil_div(V, C), kSliceAlign);
-    Layout l = layout_for(slice, es, G, threads, C);
+    Layout l = layout_for(slice, es, pr * G, threads, C);
     while (l.total > smem_per_cta && G > 1 && !ovr_group) {
         G = (G + 1) / 2;
-        l = layout_for(slice, es, G, threads, C);
+        l = layout_for(slice, es, pr * G, threads, C);
     }
     if (l.total > smem_per_cta)
         return SV_ERR_UNSUPPORTED;
@@ -97,7 +102,7 @@ int plan_impl(int num_sms, int smem_per_cta, int max_cluster, int B, int K, int6
     // which shortens every step of a latency-bound chain.
     int stages = kStages;
     if (threads == 128) {
-        const Layout ld = layout_for(slice, es, G, threads, C, kStagesDeep);
+        const Layout ld = layout_for(slice, es, pr * G, threads, C, kStagesDeep);
         int64_t per_sm_deep = (int64_t)kSmemPerSM / (ld.total + kSmemPerCtaReserved);
         if (per_sm_deep > kDeepCtasPerSM)
             per_sm_deep = kDeepCtasPerSM;
@@ -198,13 +203,14 @@ extern "C" int spec_verify_plan_truncated_for(int num_sms, int max_cluster, int 
 }
 
 // Verification with draft logits: the truncated kernel's mapping when a
-// filter is on; without filters the kernel holds no histograms, so clusters
-// may grow to 16 CTAs and seven CTAs fit on an SM (72 registers a thread).
+// filter is on; without filters the sampled verify's mapping (its kernel in
+// the draft-logit form, 128 threads), with two rows of partials per group row
+// and the per-CTA shared memory a GB300 CTA may opt into.
 extern "C" int spec_verify_plan_draft_logits_for(int num_sms, int max_cluster, int B, int K,
                                                  int64_t V, int logits_dtype, int filters,
                                                  int ovr_cluster, sv_plan* out) {
     return filters ? plan_rows(num_sms, max_cluster, B, K, V, logits_dtype, ovr_cluster,
                                sv::kTruncCtasPerSM, 4, sv::kTruncMaxCluster, out)
-                   : plan_rows(num_sms, max_cluster, B, K, V, logits_dtype, ovr_cluster,
-                               sv::kDraftCtasPerSM, 4, sv::kMaxCluster, out);
+                   : plan_impl(num_sms, sv::kSmemOptinPerCta, max_cluster, B, K, V, logits_dtype,
+                               ovr_cluster, 0, 0, out, true);
 }

@@ -36,7 +36,12 @@
 //  * the residual (or bonus) draw streams the rejected draft row through the
 //    same rings, records per-tile totals, meets the other CTAs' totals in
 //    distributed shared memory, and one warp of the owning CTA locates the
-//    token by warp-parallel scans.
+//    token by warp-parallel scans;
+//  * with the drafter's logits in place of q (the DL form), each test row's
+//    draft row streams through the ring right after it, once the decision on
+//    the previous row is settled, and yields a second partial per warp; the
+//    test and the residual draw form q from the draft row's merged offset
+//    and normaliser.
 #include <cuda_runtime.h>
 #include <cooperative_groups.h>
 
@@ -93,6 +98,10 @@ struct SvArgs {
     float c_hi, c_lo;       // log2(e)/T = c_hi + c_lo with c_lo > 0 (accurate paths)
     float c;                // log2(e)/T rounded to float (per-entry paths)
     float T;
+    // draft logits in place of q (the DL kernels): q_i = softmax(d_i / T_d)
+    const void* dlogits;    // [B, K, V] in the target's dtype
+    float cd_hi, cd_lo;     // log2(e)/T_d split as c_hi, c_lo
+    float cd;               // log2(e)/T_d rounded to float
 };
 
 struct FF {  // hi + lo, see the double-float helpers below
@@ -116,8 +125,10 @@ struct __align__(16) SvShared {
     int rec_row;   // the row whose outcome the record holds
     int rec_state, rec_code, rec_j, rec_mode, rec_ndec;
     float rec_A, rec_Shi, rec_Slo;
+    float rec_Ad, rec_Sd;   // draft logits: the draft row's offset and normaliser
     float4 grp[kMaxRows];   // a group's row outcomes (amax, M, num, kind)
     float2 grpS[kMaxRows];  // ... and their normalisers (hi, lo)
+    float2 grpD[kMaxRows];  // draft logits: the draft rows' (offset, normaliser)
 };
 static_assert(sizeof(SvShared) + 64 <= sv::kFixedSmem, "fixed shared state outgrew its reservation");
 
@@ -713,6 +724,24 @@ __device__ __forceinline__ float entry_weights(const uint4 lv, const float (&qq)
     return acc.x + acc.y;
 }
 
+// Draft logits: the E entries of one vector of draft row j as q_v S_d scaled
+// to the target side, 2^((d_v - a_d) c_d) (nad = -a_d); the caller multiplies
+// by S / S_d.  The pass and the locate step of the residual draw both call
+// this, so both see the same weights.
+template <int ES>
+__device__ __forceinline__ void draft_q(const uint4 dv, float nad, float cd, float (&qq)[Elem<ES>::E]) {
+    constexpr int E = Elem<ES>::E;
+    float2 d[E / 2];
+    Elem<ES>::diff(dv, nad, d);
+    const float2 c2 = make_float2(cd, cd);
+#pragma unroll
+    for (int h = 0; h < E / 2; ++h) {
+        const float2 y = __fmul2_rn(d[h], c2);
+        qq[2 * h] = ex2_approx(y.x);
+        qq[2 * h + 1] = ex2_approx(y.y);
+    }
+}
+
 // q values of a residual draw are valid when each is in [0, +inf) (-0 counts
 // as 0): as unsigned bit patterns, below the +inf pattern, or exactly -0.
 __device__ __forceinline__ bool q_bits_valid(uint32_t qbits) {
@@ -723,10 +752,15 @@ __device__ __forceinline__ bool q_bits_valid(uint32_t qbits) {
 
 // Residency target: sv::kThreadsPerSM threads per SM, seven CTAs of 128 (shared
 // memory allows no more), so a thread may use up to 72 registers.
-template <int ES, int NT, int S>
-__global__ void __launch_bounds__(NT, S == sv::kStages ? sv::kThreadsPerSM / NT : sv::kDeepCtasPerSM)
+// DL: the drafter's logits in place of q.  Every test row's draft row then
+// streams right after its target row through the same ring (q_i needs the draft
+// row's own maximum and normaliser), each warp publishes a second partial for
+// it, the test is u * q(x) < p(x) with q(x) = 2^((d_x - a_d) c_d) / S_d, and
+// the residual draw reads the draft row's logits where it would read q.
+template <int ES, int NT, int NS, bool DL>
+__global__ void __launch_bounds__(NT, NS == sv::kStages ? sv::kThreadsPerSM / NT : sv::kDeepCtasPerSM)
     sv_verify_kernel(const __grid_constant__ SvArgs a) {
-    constexpr int kStages = S;  // ring stages per warp
+    constexpr int kStages = NS;  // ring stages per warp
     constexpr int E = Elem<ES>::E;
     constexpr int NW = NT / 32;
     static_assert(NW <= kMaxWarps, "too many warps");
@@ -756,13 +790,14 @@ __global__ void __launch_bounds__(NT, S == sv::kStages ? sv::kThreadsPerSM / NT 
     const int64_t V = a.V;
     const int C = a.C;
     const int G = a.G;
+    const int GG = DL ? 2 * G : G;  // partial rows per parity: a draft partial per target row (DL)
     const float c = a.c;
 
     extern __shared__ __align__(128) unsigned char smem_raw[];
     SvShared& sh = *reinterpret_cast<SvShared*>(smem_raw + a.off_fixed);
     unsigned long long* bar = reinterpret_cast<unsigned long long*>(smem_raw + a.off_bar);
     unsigned long long* xbar = bar + NW * kStages;  // [0..1] row partials by parity, [2..3] draw rounds
-    float4* part = reinterpret_cast<float4*>(smem_raw + a.off_part);  // [2][G][C*NW] (a, S.hi, S.lo, max)
+    float4* part = reinterpret_cast<float4*>(smem_raw + a.off_part);  // [2][GG][C*NW] (a, S.hi, S.lo, max)
     float* tt = reinterpret_cast<float*>(smem_raw + a.off_tt);          // [NW][ntw] draw tile totals
     unsigned char* ring = smem_raw + (size_t)warp * kStages * kChunkBytes;
     unsigned long long* wbar = bar + warp * kStages;
@@ -846,11 +881,15 @@ __global__ void __launch_bounds__(NT, S == sv::kStages ? sv::kThreadsPerSM / NT 
     auto row_chunk_bytes = [&](int ch) {
         return (uint32_t)(min(kChunkVecs, wn - ch * kChunkVecs) * 16);
     };
+    // DL: this warp's stretch of draft row 0 (draft rows share the target's geometry)
+    const unsigned char* dstretch =
+        DL ? static_cast<const unsigned char*>(a.dlogits) + (drow0 * V + v0) * ES + (size_t)wv0 * 16
+           : nullptr;
 
     // The row stream: (iss_row, iss_ch) is the next chunk to issue.  Chunks go
     // out up to kStages ahead of consumption, across row boundaries, but never
-    // past row lim_row.
-    int iss_row = 0, iss_ch = 0, lim_row = (G < K + 1 ? G : K + 1) - 1;
+    // past row lim_row.  DL: a test row's draft row (iss_half 1) follows it.
+    int iss_row = 0, iss_ch = 0, iss_half = 0, lim_row = (G < K + 1 ? G : K + 1) - 1;
     const unsigned char* iss_src = lstretch;
     const uint32_t last_bytes = nch > 0 ? row_chunk_bytes(nch - 1) : 0u;
     auto top_up = [&]() {
@@ -860,8 +899,14 @@ __global__ void __launch_bounds__(NT, S == sv::kStages ? sv::kThreadsPerSM / NT 
             issue(iss_src, iss_ch == nch - 1 ? last_bytes : (uint32_t)kChunkBytes);
             if (++iss_ch == nch) {
                 iss_ch = 0;
-                ++iss_row;
-                iss_src = row_chunk_src(iss_row, 0);
+                if (DL && iss_half == 0 && iss_row < K) {
+                    iss_half = 1;
+                    iss_src = dstretch + (size_t)iss_row * row_bytes;
+                } else {
+                    iss_half = 0;
+                    ++iss_row;
+                    iss_src = row_chunk_src(iss_row, 0);
+                }
             } else {
                 iss_src += kChunkBytes;
             }
@@ -889,11 +934,13 @@ __global__ void __launch_bounds__(NT, S == sv::kStages ? sv::kThreadsPerSM / NT 
             code = SV_ERR_UNIFORM_RANGE;
         }
     }
-    float lx_lane = 0.f, qx_lane = 0.f;  // lane i: l(x_i), q(x_i), in every warp
+    // lane i: l(x_i), and q(x_i) -- or, from draft logits, d_x_i -- in every warp
+    float lx_lane = 0.f, qx_lane = 0.f;
     if (state == kStateRun && lane < K) {
         const int x = sh.x[lane];
         lx_lane = Elem<ES>::load(a.logits, (row0 + lane) * V + x);
-        qx_lane = __ldg(a.q + (drow0 + lane) * V + x);
+        qx_lane = DL ? Elem<ES>::load(a.dlogits, (drow0 + lane) * V + x)
+                     : __ldg(a.q + (drow0 + lane) * V + x);
     }
     const int P = C * NW;  // row partials per row: every warp of the cluster
     const bool track = a.row_stats != nullptr;  // the row max is reported
@@ -903,11 +950,15 @@ __global__ void __launch_bounds__(NT, S == sv::kStages ? sv::kThreadsPerSM / NT 
     int j = -1, ndec = 0, mode = kModeBonus;
     float rowA = 0.f;
     FF rowS = {0.f, 0.f};
+    float rowAd = 0.f, rowSd = 1.f;  // DL: the rejected row's draft offset and normaliser
 
     // Streams this warp's stretch of row `row` into ls.  After every chunk
     // poll() may end the stream (returns false): a decision arrived that
     // makes the row unnecessary.
-    auto stream_row = [&](int row, LaneSum<ES>& ls, auto&& poll) -> bool {
+    // (DL: half 1 streams the draft row of `row` at c_d, without the exact max)
+    auto stream_row = [&](int row, LaneSum<ES>& ls, auto&& poll, int half = 0) -> bool {
+        const float cc = half ? a.cd : c;
+        const bool trk = half ? false : track;
         ls.a = -INFINITY;
         ls.s = 0.f;
         ls.mx = Elem<ES>::max_init();
@@ -921,17 +972,18 @@ __global__ void __launch_bounds__(NT, S == sv::kStages ? sv::kThreadsPerSM / NT 
                 // rows that are not 16-byte aligned: element loads into the
                 // warp's current stage, then the same arithmetic
                 uint4* dst = reinterpret_cast<uint4*>(ring + st_wait * kChunkBytes);
-                const int64_t gbase = (row0 + row) * V + v0;
+                const int64_t gbase = (half ? drow0 : row0) * V + (int64_t)row * V + v0;
+                const void* src = half ? a.dlogits : a.logits;
                 const int64_t cv = (int64_t)wv0 + (int64_t)ch * kChunkVecs;
                 for (int k = 0; k < kVecPerLane; ++k)
                     if (k * 32 + lane < nv)
-                        dst[k * 32 + lane] = load_vec_elems<ES>(a.logits, gbase, (cv + k * 32 + lane) * E, L);
+                        dst[k * 32 + lane] = load_vec_elems<ES>(src, gbase, (cv + k * 32 + lane) * E, L);
                 __syncwarp();
                 buf = dst;
             }
             if (ch == 0)
                 ls.start(buf, nv);
-            ls.chunk(buf, nv, c, track);
+            ls.chunk(buf, nv, cc, trk);
             if (a.bulk)
                 release();
             else
@@ -945,12 +997,14 @@ __global__ void __launch_bounds__(NT, S == sv::kStages ? sv::kThreadsPerSM / NT 
     // This warp's partial of a row -- offset = the lanes' largest, sum in
     // double-float, NaN-propagating max -- pushed into slot (par, r) of every
     // CTA of the cluster.
-    auto publish = [&](int par, int r, const LaneSum<ES>& ls) {
+    // (DL: half 1 publishes the draft row's partial, at c_d, into slot r + G)
+    auto publish = [&](int par, int r, const LaneSum<ES>& ls, int half = 0) {
         const float aw = warp_max_nan(ls.a);
-        const float mw = track ? warp_max_nan(Elem<ES>::value(ls.mx)) : aw;
+        const float mw = (track && !half) ? warp_max_nan(Elem<ES>::value(ls.mx)) : aw;
         FF sw = {0.f, 0.f};
+        const float2 ch = half ? make_float2(a.cd_hi, a.cd_lo) : make_float2(a.c_hi, a.c_lo);
         if (ls.s > 0.f && aw < INFINITY)
-            sw = two_prod(ls.s, exp2_diff_accurate(ls.a, aw, a.c_hi, a.c_lo));
+            sw = two_prod(ls.s, exp2_diff_accurate(ls.a, aw, ch.x, ch.y));
         const FF Sw = warp_sum_bcast(sw);
         const bool any_to = __any_sync(kFull, timed_out);
         if (!cluster_ready) {
@@ -958,7 +1012,7 @@ __global__ void __launch_bounds__(NT, S == sv::kStages ? sv::kThreadsPerSM / NT 
             cluster_ready = true;
         }
         if (lane < C) {
-            const uint32_t slot = smem_addr(&part[(par * G + r) * P + rank * NW + warp]);
+            const uint32_t slot = smem_addr(&part[(par * GG + r + (half ? G : 0)) * P + rank * NW + warp]);
             st_async_v4(mapa_shared(slot, lane), make_float4(aw, any_to ? -1.f : Sw.hi, Sw.lo, mw),
                         mapa_shared(smem_addr(&xbar[par]), lane));
         }
@@ -978,58 +1032,90 @@ __global__ void __launch_bounds__(NT, S == sv::kStages ? sv::kThreadsPerSM / NT 
         float amax, M, num;
         FF S;
         int kind;  // 0 accept, 1 reject (or bonus row), 2 timeout, 3 non-finite
+        float ad;  // DL: the draft row's offset ...
+        FF Sd;     // ... and normaliser
     };
-    // A warp combines the C * NW partials of row i (slot par, r) in a fixed
-    // order and evaluates [P1]'s test for it.
-    auto merge_row = [&](int i, int par, int r) -> RowOutcome {
-        const bool xto = __any_sync(kFull, timed_out);
+    // The C * NW partials in slot (par, r): their largest offset, NaN-
+    // propagating max and sum against that offset, merged in a fixed order
+    // (c2 = (c_hi, c_lo) of the row's temperature).  Sets `to` when a warp
+    // timed out.
+    auto merge_slot = [&](int slot, bool xto, float2 c2, float& amax, float& M, bool& to) -> FF {
         float4 pv[kPer];
-        float amax = -INFINITY, mloc = -INFINITY;
-        bool to = false;
+        float mloc = -INFINITY;
+        amax = -INFINITY;
 #pragma unroll
         for (int t = 0; t < kPer; ++t) {
             const int p = lane + 32 * t;
             pv[t] = make_float4(-INFINITY, 0.f, 0.f, -INFINITY);
             if (p < P && !xto) {
-                pv[t] = part[(par * G + r) * P + p];
+                pv[t] = part[slot * P + p];
                 amax = fmaxf(amax, pv[t].x);
                 mloc = fmax_nan(mloc, pv[t].w);
                 to |= pv[t].y < 0.f;
             }
         }
-        RowOutcome o;
-        o.M = warp_max_nan(mloc);
+        M = warp_max_nan(mloc);
 #pragma unroll
         for (int sft = 16; sft; sft >>= 1)
             amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, sft));
-        o.amax = amax;
         // (a NaN or inf entry poisons its lane's offset to +inf, an all -inf
         // row leaves every offset at -inf: both show in the merged offset)
-        const bool finite = amax > -INFINITY && amax < INFINITY;
         FF acc = {0.f, 0.f};
-        if (finite) {
+        if (amax > -INFINITY && amax < INFINITY) {
 #pragma unroll
             for (int t = 0; t < kPer; ++t)
                 if (pv[t].y > 0.f) {
-                    const float wgt = exp2_diff_accurate(pv[t].x, amax, a.c_hi, a.c_lo);
+                    const float wgt = exp2_diff_accurate(pv[t].x, amax, c2.x, c2.y);
                     FF term = two_prod(pv[t].y, wgt);
                     term.lo = fmaf(pv[t].z, wgt, term.lo);
                     acc = ff_add(acc, term);
                 }
         }
-        o.S = warp_sum_bcast(acc);
+        return warp_sum_bcast(acc);
+    };
+    // A warp combines the partials of row i (slot par, r) and evaluates
+    // [P1]'s test for it.
+    auto merge_row = [&](int i, int par, int r) -> RowOutcome {
+        const bool xto = __any_sync(kFull, timed_out);
+        bool to = false;
+        RowOutcome o;
+        o.ad = 0.f;
+        o.Sd = FF{0.f, 0.f};
+        // (DL: the draft row's slot too, through the same code)
+        for (int h = 0; h < ((DL && i < K) ? 2 : 1); ++h) {
+            float am, mm;
+            const FF Sx = merge_slot(par * GG + r + (h ? G : 0), xto,
+                                     h ? make_float2(a.cd_hi, a.cd_lo) : make_float2(a.c_hi, a.c_lo),
+                                     am, mm, to);
+            if (h == 0) {
+                o.S = Sx;
+                o.amax = am;
+                o.M = mm;
+            } else {
+                o.Sd = Sx;
+                o.ad = am;
+            }
+        }
+        const bool finite = o.amax > -INFINITY && o.amax < INFINITY;
+        const bool dfinite = !(DL && i < K) || (o.ad > -INFINITY && o.ad < INFINITY);
         const float lxi = __shfl_sync(kFull, lx_lane, i & 31);
-        const float qxf = __shfl_sync(kFull, qx_lane, i & 31);
+        const float qxf = __shfl_sync(kFull, qx_lane, i & 31);  // DL: d(x_i)
+        // lane 1: 2^((l_x - a) c); DL, lane 2: 2^((d_x - a_d) c_d)
         float num = 0.f;
-        if (lane == 1 && finite && i < K)
-            num = exp2_diff_accurate(lxi, amax, a.c_hi, a.c_lo);
+        const bool dl2 = DL && lane == 2;
+        if ((lane == 1 || dl2) && (dl2 ? dfinite : finite) && i < K)
+            num = exp2_diff_accurate(dl2 ? qxf : lxi, dl2 ? o.ad : o.amax, dl2 ? a.cd_hi : a.c_hi,
+                                     dl2 ? a.cd_lo : a.c_lo);
+        const float numd = DL ? __shfl_sync(kFull, num, 2) : 0.f;
         o.num = __shfl_sync(kFull, num, 1);
         if (xto || __any_sync(kFull, to))
             o.kind = 2;
-        else if (!finite || (i < K && !(qxf >= 0.f && qxf < INFINITY)))
+        else if (!finite || !dfinite || (!DL && i < K && !(qxf >= 0.f && qxf < INFINITY)))
             o.kind = 3;
         else if (i == K)
             o.kind = 1;
+        else if (DL)  // u < p(x)/q(x) as u * 2^((d_x - a_d) c_d) * S < 2^((l_x - a) c) * S_d
+            o.kind = ff_gt(ff_mul(FF{o.num, 0.f}, o.Sd), ff_mul(two_prod(sh.u[i], numd), o.S)) ? 0 : 1;
         else  // u < p(x)/q(x) as u * q(x) * S < 2^((l_x - a) c)
             o.kind = ff_gt(FF{o.num, 0.f}, ff_mul(two_prod(sh.u[i], qxf), o.S)) ? 0 : 1;
         return o;
@@ -1067,6 +1153,10 @@ __global__ void __launch_bounds__(NT, S == sv::kStages ? sv::kThreadsPerSM / NT 
             mode = i < K ? kModeResidual : kModeBonus;
             rowA = o.amax;
             rowS = o.S;
+            if (DL && i < K) {
+                rowAd = o.ad;
+                rowSd = o.Sd.hi;
+            }
         }
     };
     auto decide = [&](int i, int par, int r) { apply_row(i, merge_row(i, par, r), true); };
@@ -1087,6 +1177,10 @@ __global__ void __launch_bounds__(NT, S == sv::kStages ? sv::kThreadsPerSM / NT 
             ndec = sh.rec_ndec;
             rowA = sh.rec_A;
             rowS = FF{sh.rec_Shi, sh.rec_Slo};
+            if (DL) {
+                rowAd = sh.rec_Ad;
+                rowSd = sh.rec_Sd;
+            }
         };
         auto record_posted = [&](int i) {
             // every lane acquires, so each lane's reads of the record follow it
@@ -1108,6 +1202,10 @@ __global__ void __launch_bounds__(NT, S == sv::kStages ? sv::kThreadsPerSM / NT 
                 sh.rec_A = rowA;
                 sh.rec_Shi = rowS.hi;
                 sh.rec_Slo = rowS.lo;
+                if (DL) {
+                    sh.rec_Ad = rowAd;
+                    sh.rec_Sd = rowSd;
+                }
                 st_release_cta(&sh.rec_row, i);
             }
             __syncwarp();
@@ -1154,18 +1252,30 @@ __global__ void __launch_bounds__(NT, S == sv::kStages ? sv::kThreadsPerSM / NT 
         while (state == kStateRun) {
             const int pc = cur & 1;
             if (tid == 0)
-                mbar_arrive_expect_tx(&xbar[pc], (uint32_t)(P * 16));
+                mbar_arrive_expect_tx(&xbar[pc], (uint32_t)(P * 16 * ((DL && cur < K) ? 2 : 1)));
             lim_row = cur < K ? cur + 1 : K;
-            LaneSum<ES> ls;
-            if (!stream_row(cur, ls, poll))
-                break;
-            if (pend >= 0) {  // the decision on the previous row is still open
-                settle_row(pend);
-                pend = -1;
-                if (state != kStateRun)
+            // (DL: the draft row streams after the decision on the previous
+            // row is settled, so of a row the loop does not reach no more
+            // than the ring's lookahead into its draft row is read)
+            bool stopped = false;
+            for (int h = 0; h < ((DL && cur < K) ? 2 : 1); ++h) {
+                LaneSum<ES> ls;
+                if (!stream_row(cur, ls, poll, h)) {
+                    stopped = true;
                     break;
+                }
+                if (pend >= 0) {  // the decision on the previous row is still open
+                    settle_row(pend);
+                    pend = -1;
+                    if (state != kStateRun) {
+                        stopped = true;
+                        break;
+                    }
+                }
+                publish(pc, 0, ls, h);
             }
-            publish(pc, 0, ls);
+            if (stopped)
+                break;
             pend = cur;
             if (cur == K) {  // the bonus row: nothing left to stream
                 settle_row(cur);
@@ -1181,14 +1291,16 @@ __global__ void __launch_bounds__(NT, S == sv::kStages ? sv::kThreadsPerSM / NT 
         auto no_poll = []() { return true; };
         while (state == kStateRun) {
             const int ng = G < K + 1 - g0 ? G : K + 1 - g0;
+            const int nd = DL ? max(0, min(ng, K - g0)) : 0;  // rows with a draft row
             if (tid == 0)
-                mbar_arrive_expect_tx(&xbar[par], (uint32_t)(P * ng * 16));
+                mbar_arrive_expect_tx(&xbar[par], (uint32_t)(P * (ng + nd) * 16));
             lim_row = g0 + ng - 1;
-            for (int r = 0; r < ng; ++r) {
-                LaneSum<ES> ls;
-                (void)stream_row(g0 + r, ls, no_poll);
-                publish(par, r, ls);
-            }
+            for (int r = 0; r < ng; ++r)
+                for (int h = 0; h < (r < nd ? 2 : 1); ++h) {
+                    LaneSum<ES> ls;
+                    (void)stream_row(g0 + r, ls, no_poll, h);
+                    publish(par, r, ls, h);
+                }
             // the first chunks of the next group go out before the decision
             const int g1 = g0 + ng;
             if (a.bulk && a.speculate && g1 <= K) {
@@ -1203,6 +1315,8 @@ __global__ void __launch_bounds__(NT, S == sv::kStages ? sv::kThreadsPerSM / NT 
                 if (lane == 0) {
                     sh.grp[r] = make_float4(o.amax, o.M, o.num, __int_as_float(o.kind));
                     sh.grpS[r] = make_float2(o.S.hi, o.S.lo);
+                    if (DL)
+                        sh.grpD[r] = make_float2(o.ad, o.Sd.hi);
                 }
             }
             __syncthreads();
@@ -1215,6 +1329,11 @@ __global__ void __launch_bounds__(NT, S == sv::kStages ? sv::kThreadsPerSM / NT 
                 o.num = g4.z;
                 o.kind = __float_as_int(g4.w);
                 o.S = FF{g2.x, g2.y};
+                if (DL) {
+                    const float2 gd = sh.grpD[r];
+                    o.ad = gd.x;
+                    o.Sd = FF{gd.y, 0.f};
+                }
                 apply_row(g0 + r, o, warp == 0);
             }
             __syncthreads();  // the outcome slots are reused by the next group
@@ -1243,17 +1362,24 @@ __global__ void __launch_bounds__(NT, S == sv::kStages ? sv::kThreadsPerSM / NT 
     const int ntile = (nq32 + kDrawTile - 1) / kDrawTile;
     const unsigned char* lrow = nullptr;
     const float* qrow = nullptr;
+    const unsigned char* drow = nullptr;  // DL: draft row j's slice
     int owner = -1, take_last = 0;
     FF rem = {0.f, 0.f};
+    // the residual's q scale: S, or with draft logits S / S_d (see draft_q)
+    const float Sf = (DL && j < K) ? __fdiv_rn(rowS.hi, rowSd) : rowS.hi;
+    const int64_t gbase_j = (row0 + j) * V + v0;    // element index of the slice start
+    const int64_t dgbase_j = (drow0 + j) * V + v0;  // DL: the same in the draft logits
     if (state == kStateSample) {
         lrow = static_cast<const unsigned char*>(a.logits) + ((row0 + j) * V + v0) * ES;
-        qrow = j < K ? a.q + (drow0 + j) * V + v0 : nullptr;
+        if (DL)
+            drow = j < K ? static_cast<const unsigned char*>(a.dlogits) + dgbase_j * ES : nullptr;
+        else
+            qrow = j < K ? a.q + (drow0 + j) * V + v0 : nullptr;
         const float na = -rowA;
-        const float Sf = rowS.hi;
-        const int64_t gbase_j = (row0 + j) * V + v0;  // element index of the slice start
         int sp = 0;
         const unsigned char* lbase = lrow + e0 * ES;
         const float* qbase = qrow ? qrow + e0 : nullptr;
+        const unsigned char* dbase = drow ? drow + e0 * ES : nullptr;
         float* tt_w = tt + warp * a.ntw;
         uint32_t qbits = 0;
         auto load_logits = [&](int t, uint4 (&lv)[kDV]) {
@@ -1280,8 +1406,12 @@ __global__ void __launch_bounds__(NT, S == sv::kStages ? sv::kThreadsPerSM / NT 
             // rows of the sequences still testing wait in
             auto q_top_up = [&](int t) {
                 while (qissued < ntile && qissued < t + (2 * j < K ? 1 : kStages)) {
-                    issue(qbase + (size_t)qissued * kDrawTile,
-                          (uint32_t)(min(kDrawTile, nq32 - qissued * kDrawTile) * 4), true);
+                    if (DL)
+                        issue(dbase + (size_t)qissued * kDrawTile * ES,
+                              (uint32_t)(min(kDrawTile, nq32 - qissued * kDrawTile) * ES), true);
+                    else
+                        issue(qbase + (size_t)qissued * kDrawTile,
+                              (uint32_t)(min(kDrawTile, nq32 - qissued * kDrawTile) * 4), true);
                     ++qissued;
                 }
             };
@@ -1323,7 +1453,13 @@ __global__ void __launch_bounds__(NT, S == sv::kStages ? sv::kThreadsPerSM / NT 
                         float2 d[E / 2];
                         Elem<ES>::diff(cur[k], na, d);
                         float2 qp[E / 2];
-                        if constexpr (RESID) {
+                        if constexpr (RESID && DL) {
+                            float qd[E];
+                            draft_q<ES>(reinterpret_cast<const uint4*>(q4)[k * 32 + lane], -rowAd, a.cd, qd);
+#pragma unroll
+                            for (int h = 0; h < E / 2; ++h)
+                                qp[h] = make_float2(qd[2 * h], qd[2 * h + 1]);
+                        } else if constexpr (RESID) {
 #pragma unroll
                             for (int h = 0; h < E / 4; ++h) {
                                 const float4 v4 = q4[(k * 32 + lane) * (E / 4) + h];
@@ -1339,8 +1475,9 @@ __global__ void __launch_bounds__(NT, S == sv::kStages ? sv::kThreadsPerSM / NT 
                                 e = __ffma2_rn(qp[h], nS, e);
                                 e.x = fmaxf(e.x, 0.f);
                                 e.y = fmaxf(e.y, 0.f);
-                                qbits = __vimax3_u32(qbits, __float_as_uint(qp[h].x),
-                                                     __float_as_uint(qp[h].y));
+                                if (!DL)
+                                    qbits = __vimax3_u32(qbits, __float_as_uint(qp[h].x),
+                                                         __float_as_uint(qp[h].y));
                             }
                             acc = __fadd2_rn(acc, e);
                         }
@@ -1368,7 +1505,16 @@ __global__ void __launch_bounds__(NT, S == sv::kStages ? sv::kThreadsPerSM / NT 
                     const int ve = t * kDrawTile + vi * E;
                     const int n = min(E, max(0, nq32 - ve));
                     float qq[E];
-                    if constexpr (RESID) {
+                    if constexpr (RESID && DL) {
+                        // (entries at or past n weigh 0 whatever qq holds there)
+                        const uint4 dv = use_ring ? reinterpret_cast<const uint4*>(qs)[vi]
+                                                  : load_vec_elems<ES>(a.dlogits, dgbase_j + e0, ve, nq32);
+                        draft_q<ES>(dv, -rowAd, a.cd, qq);
+#pragma unroll
+                        for (int h = 0; h < E; ++h)
+                            if (h >= n)
+                                qq[h] = 0.f;
+                    } else if constexpr (RESID) {
                         if (use_ring) {
                             const float4* q4 = reinterpret_cast<const float4*>(qs + vi * E);
 #pragma unroll
@@ -1543,7 +1689,13 @@ __global__ void __launch_bounds__(NT, S == sv::kStages ? sv::kThreadsPerSM / NT 
                     raw = a.bulk ? __ldg(reinterpret_cast<const uint4*>(lrow + (e0s + ve) * ES))
                                  : load_vec_elems<ES>(a.logits, gbase_j, e0s + ve, e0s + nqs);
                 float qq[E];
-                if (mode == kModeResidual && a.qvec && n == E) {
+                if (DL && mode == kModeResidual) {
+                    uint4 dv = make_uint4(0, 0, 0, 0);
+                    if (n > 0)
+                        dv = a.qvec ? __ldg(reinterpret_cast<const uint4*>(drow + (e0s + ve) * ES))
+                                    : load_vec_elems<ES>(a.dlogits, dgbase_j, e0s + ve, e0s + nqs);
+                    draft_q<ES>(dv, -rowAd, a.cd, qq);
+                } else if (mode == kModeResidual && a.qvec && n == E) {
 #pragma unroll
                     for (int h = 0; h < E / 4; ++h) {
                         const float4 v4 = __ldg(reinterpret_cast<const float4*>(qrow + e0s + ve) + h);
@@ -1559,7 +1711,7 @@ __global__ void __launch_bounds__(NT, S == sv::kStages ? sv::kThreadsPerSM / NT 
                 }
                 uint32_t qb = 0;
                 ts[k] = mode == kModeResidual
-                            ? entry_weights<ES, true>(raw, qq, n, -rowA, c, rowS.hi, w[k], qb)
+                            ? entry_weights<ES, true>(raw, qq, n, -rowA, c, Sf, w[k], qb)
                             : entry_weights<ES, false>(raw, qq, n, -rowA, c, rowS.hi, w[k], qb);
             }
             // sub-tile k holds tile entries [k*32*E, (k+1)*32*E)
@@ -1675,20 +1827,29 @@ __global__ void __launch_bounds__(NT, S == sv::kStages ? sv::kThreadsPerSM / NT 
 
 using KernelFn = void (*)(SvArgs);
 
-KernelFn pick_kernel(int es, int threads, int stages = sv::kStages) {
-    if (stages == sv::kStagesDeep) {
+// dl: the draft-logit form (128 threads only)
+KernelFn pick_kernel(int es, int threads, int stages = sv::kStages, bool dl = false) {
+    constexpr int S3 = sv::kStages, S6 = sv::kStagesDeep;
+    if (dl) {
+        if (threads != 128 || (stages != S3 && stages != S6))
+            return nullptr;
+        if (es == 2)
+            return stages == S6 ? sv_verify_kernel<2, 128, S6, true> : sv_verify_kernel<2, 128, S3, true>;
+        return stages == S6 ? sv_verify_kernel<4, 128, S6, true> : sv_verify_kernel<4, 128, S3, true>;
+    }
+    if (stages == S6) {
         if (threads != 128)
             return nullptr;
-        return es == 2 ? sv_verify_kernel<2, 128, sv::kStagesDeep> : sv_verify_kernel<4, 128, sv::kStagesDeep>;
+        return es == 2 ? sv_verify_kernel<2, 128, S6, false> : sv_verify_kernel<4, 128, S6, false>;
     }
     if (es == 2) {
-        if (threads == 128) return sv_verify_kernel<2, 128, sv::kStages>;
-        if (threads == 256) return sv_verify_kernel<2, 256, sv::kStages>;
-        if (threads == 512) return sv_verify_kernel<2, 512, sv::kStages>;
+        if (threads == 128) return sv_verify_kernel<2, 128, S3, false>;
+        if (threads == 256) return sv_verify_kernel<2, 256, S3, false>;
+        if (threads == 512) return sv_verify_kernel<2, 512, S3, false>;
     } else {
-        if (threads == 128) return sv_verify_kernel<4, 128, sv::kStages>;
-        if (threads == 256) return sv_verify_kernel<4, 256, sv::kStages>;
-        if (threads == 512) return sv_verify_kernel<4, 512, sv::kStages>;
+        if (threads == 128) return sv_verify_kernel<4, 128, S3, false>;
+        if (threads == 256) return sv_verify_kernel<4, 256, S3, false>;
+        if (threads == 512) return sv_verify_kernel<4, 512, S3, false>;
     }
     return nullptr;
 }
@@ -1715,7 +1876,6 @@ struct sv_ctx {
     int64_t max_V = 0;
     int num_sms = 0, smem_optin = 0, max_cluster = 8;
     int greedy_max_cluster = 8;
-    int draft_max_cluster = 8;  // draft-logit kernel without filters
     uint32_t* d_err = nullptr;
     int ovr_cluster = 0, ovr_group = 0, ovr_threads = 0;  // spec_verify_set_plan_override
     uint32_t* al_hist = nullptr;  // caller's accepted-length counters (device), or none
@@ -1760,24 +1920,42 @@ int make_plan(const sv_ctx* ctx, int B, int K, int64_t V, int dtype, sv_plan* pl
                                 ctx->ovr_cluster, ctx->ovr_group, ctx->ovr_threads, plan);
 }
 
+// (log2(e) / T) as hi + lo, hi just below the exact value so that lo is
+// strictly positive: a -inf logit then gives -inf * lo = -inf, not NaN
+void split_log2e_over(float T, float* hi, float* lo, float* rounded) {
+    const double c_d = 1.4426950408889634074 / (double)T;
+    *hi = (float)c_d;
+    if ((double)*hi >= c_d)
+        *hi = std::nextafter(*hi, 0.0f);
+    *lo = (float)(c_d - (double)*hi);
+    *rounded = (float)c_d;
+}
+
+// The draft-logit form's extra inputs (see spec_verify_run_draft_logits).
+struct DraftLogits {
+    const void* dlogits;  // [B, K, V], the target's dtype
+    float T_draft;
+};
+
 int launch(sv_ctx* ctx, const void* logits, int dtype, const float* q, const int32_t* tokens,
            const float* uniforms, int B, int K, int64_t V, float T, int32_t* accept_len,
            int32_t* out_tokens, uint8_t* accept_mask, float* row_stats, float* p_draft,
            int32_t* status, cudaStream_t stream, const int32_t* offsets = nullptr,
-           int64_t total_rows = 0) {
+           int64_t total_rows = 0, const DraftLogits* dl = nullptr) {
     if (ctx->al_hist && K + 2 > ctx->al_bins)
         return SV_ERR_INVALID_ARG;
     sv_plan plan;
-    int rc = make_plan(ctx, B, K, V, dtype, &plan);
+    const int es = dtype == SV_BF16 ? 2 : 4;
+    int rc = dl ? spec_verify_get_plan_draft_logits(ctx, B, K, V, dtype, 0, &plan)
+                : make_plan(ctx, B, K, V, dtype, &plan);
     if (rc != SV_OK)
         return rc;
-    const int es = dtype == SV_BF16 ? 2 : 4;
-    KernelFn fn = pick_kernel(es, plan.threads, plan.stages);
+    KernelFn fn = pick_kernel(es, plan.threads, plan.stages, dl != nullptr);
     if (!fn)
         return SV_ERR_UNSUPPORTED;
 
-    const sv::Layout lay =
-        sv::layout_for(plan.slice, es, plan.group, plan.threads, plan.cluster, plan.stages);
+    const sv::Layout lay = sv::layout_for(plan.slice, es, dl ? 2 * plan.group : plan.group,
+                                          plan.threads, plan.cluster, plan.stages);
     SvArgs args;
     std::memset(&args, 0, sizeof args);
     args.logits = logits;
@@ -1806,18 +1984,21 @@ int launch(sv_ctx* ctx, const void* logits, int dtype, const float* q, const int
     args.off_bar = (int)lay.off_bar;
     args.off_part = (int)lay.off_part;
     args.off_tt = (int)lay.off_tt;
-    args.bulk = plan.bulk_copy && aligned(logits, 16) ? 1 : 0;
-    args.qvec = (V % 4 == 0) && q && aligned(q, 16) ? 1 : 0;
+    if (dl) {
+        // target and draft rows share one chunk layout: the bulk copies only
+        // when both are 16-byte aligned; qvec: draft row tiles through the ring
+        args.q = nullptr;
+        args.dlogits = K > 0 ? dl->dlogits : logits;  // K = 0: never read
+        args.bulk = plan.bulk_copy && aligned(logits, 16) && aligned(args.dlogits, 16) ? 1 : 0;
+        args.qvec = args.bulk;
+        split_log2e_over(dl->T_draft, &args.cd_hi, &args.cd_lo, &args.cd);
+    } else {
+        args.bulk = plan.bulk_copy && aligned(logits, 16) ? 1 : 0;
+        args.qvec = (V % 4 == 0) && q && aligned(q, 16) ? 1 : 0;
+    }
     args.speculate = plan.prefetch_next && args.bulk ? 1 : 0;
     args.T = T;
-    const double c_d = 1.4426950408889634074 / (double)T;  // log2(e) / T
-    // c_hi just below c_d so that c_lo = c_d - c_hi is strictly positive: a
-    // -inf logit then gives -inf * c_lo = -inf instead of NaN
-    args.c_hi = (float)c_d;
-    if ((double)args.c_hi >= c_d)
-        args.c_hi = std::nextafter(args.c_hi, 0.0f);
-    args.c_lo = (float)(c_d - (double)args.c_hi);
-    args.c = (float)c_d;
+    split_log2e_over(T, &args.c_hi, &args.c_lo, &args.c);
 
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
@@ -1846,7 +2027,6 @@ struct DeviceInfo {
     int num_sms = 0, smem_optin = 0;
     int max_cluster = 8;         // sampled verify kernel: largest usable cluster
     int greedy_max_cluster = 8;  // greedy kernel
-    int draft_max_cluster = 8;   // draft-logit kernel without filters
 };
 
 // Device checks, kernel attributes and the largest usable clusters, with
@@ -1865,10 +2045,13 @@ int device_setup(int device, DeviceInfo* info) {
         return SV_ERR_UNSUPPORTED;
     int max_cluster = 16;
     const int es_list[2] = {2, 4};
-    const int nt_list[4] = {128, 256, 512, 0};  // 0: the deep-ring kernel (128 threads)
+    // 0: the deep-ring kernel (128 threads); -1, -2: the draft-logit forms
+    const int nt_list[6] = {128, 256, 512, 0, -1, -2};
     for (int es : es_list)
         for (int nt : nt_list) {
-            KernelFn fn = nt ? pick_kernel(es, nt) : pick_kernel(es, 128, sv::kStagesDeep);
+            KernelFn fn = nt > 0    ? pick_kernel(es, nt)
+                          : nt == 0 ? pick_kernel(es, 128, sv::kStagesDeep)
+                                    : pick_kernel(es, 128, nt == -1 ? sv::kStages : sv::kStagesDeep, true);
             if (cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      optin) != cudaSuccess) {
                 (void)cudaGetLastError();
@@ -1909,9 +2092,6 @@ int device_setup(int device, DeviceInfo* info) {
     // the greedy kernel may use 16-CTA clusters only where the main kernel may
     info->greedy_max_cluster =
         (max_cluster >= 16 && sv::greedy_set_attributes() == 0) ? 16 : 8;
-    // the truncated kernel's clusters stay at 8 CTAs (portable either way); the
-    // draft-logit kernel without filters may use 16 where the main kernel may
-    info->draft_max_cluster = (sv::trunc_set_attributes() == 0 && max_cluster >= 16) ? 16 : 8;
     return SV_OK;
 }
 
@@ -1920,7 +2100,6 @@ void apply_device_info(sv_ctx* c, const DeviceInfo& info) {
     c->smem_optin = info.smem_optin;
     c->max_cluster = info.max_cluster;
     c->greedy_max_cluster = info.greedy_max_cluster;
-    c->draft_max_cluster = info.draft_max_cluster;
 }
 
 }  // namespace
@@ -2088,7 +2267,7 @@ int spec_verify_get_plan_draft_logits(sv_ctx* ctx, int B, int K, int64_t V, int 
                                       int filters, sv_plan* out) {
     if (!ctx)
         return SV_ERR_INVALID_ARG;
-    const int cap = filters ? sv::kTruncMaxCluster : ctx->draft_max_cluster;
+    const int cap = filters ? sv::kTruncMaxCluster : ctx->max_cluster;
     const int ovr = ctx->ovr_cluster > cap ? cap : ctx->ovr_cluster;
     return spec_verify_plan_draft_logits_for(ctx->num_sms, cap, B, K, V, logits_dtype, filters,
                                              ovr, out);
@@ -2119,6 +2298,14 @@ int spec_verify_run_draft_logits(sv_ctx* ctx, const void* target_logits, int log
     if (ctx->al_hist && K + 2 > ctx->al_bins)
         return SV_ERR_INVALID_ARG;
     const int filters = (top_p < 1.0 || min_p > 0.0) ? 1 : 0;
+    if (!filters) {
+        // the plain verify with q formed from the draft logits: the main
+        // kernel's draft-logit form
+        const DraftLogits dl = {draft_logits, draft_temperature};
+        return launch(ctx, target_logits, logits_dtype, nullptr, draft_tokens, uniforms, B, K, V,
+                      temperature, accept_len, out_tokens, accept_mask, row_stats, p_draft, status,
+                      static_cast<cudaStream_t>(stream), nullptr, 0, &dl);
+    }
     sv_plan plan;
     const int prc = spec_verify_get_plan_draft_logits(ctx, B, K, V, logits_dtype, filters, &plan);
     if (prc != SV_OK)
@@ -2154,7 +2341,6 @@ int spec_verify_run_draft_logits(sv_ctx* ctx, const void* target_logits, int log
     g.T = temperature;
     g.dmin = min_p > 0.0 ? (float)((double)temperature * std::log(min_p)) : -INFINITY;
     g.top_p = top_p;
-    g.filters = filters;
     g.wait_ns = sv::kWaitNs;
     DeviceGuard guard(ctx->device);
     return sv::trunc_launch(g, stream) == 0 ? SV_OK : SV_ERR_CUDA;

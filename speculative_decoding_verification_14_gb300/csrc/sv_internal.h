@@ -29,13 +29,13 @@ constexpr int kDrawTile = kChunkBytes / 4;  // entries per draw tile (its draft 
 constexpr int kFixedSmem = 3072;        // bytes reserved for the kernel's fixed shared state
 constexpr int kSmemPerSM = 233472;      // shared memory of one SM (228 KB)
 constexpr int kSmemPerCtaReserved = 1024;  // the runtime's per-CTA reservation
+constexpr int kSmemOptinPerCta = 232448;   // shared memory one CTA may opt into (227 KB)
 constexpr int kThreadsPerSM = 896;      // resident threads the kernels' launch bounds target (7 CTAs of 128)
 
 constexpr int kGreedyDepth = 8;         // greedy kernel: 16-byte loads in flight per lane
 constexpr int kGreedyCtasPerSM = 8;     // greedy kernel: resident 128-thread CTAs per SM (launch bounds)
 constexpr int kTruncCtasPerSM = 4;      // truncated-target kernel: resident CTAs per SM (launch bounds)
 constexpr int kTruncMaxCluster = 8;     // truncated-target kernel: largest cluster (shared histograms)
-constexpr int kDraftCtasPerSM = 7;      // draft-logit kernel without filters: resident CTAs per SM (launch bounds)
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
@@ -111,9 +111,7 @@ struct TruncLaunch {
     unsigned long long wait_ns;
     const void* dlogits;  // draft logits [B, K, V] in the target's dtype (q unused), or NULL
     float cd;             // log2(e) / T_draft rounded to float (draft logits)
-    int filters;          // draft logits: 1 when top-p or min-p is on
 };
-int trunc_set_attributes();                               // 0 on success
 int trunc_launch(const TruncLaunch& g, void* stream);    // 0 on success
 
 }  // namespace sv

@@ -43,8 +43,8 @@
 // (DL): [P1]'s loop forms q = softmax(d / T_d) itself.  Pass A then streams the
 // target row and the draft row together and keeps both rows' statistics; the
 // test uses q(x) S_d = 2^((d_x - d_max) c_d), and the draw's residual forms q
-// from the draft row the same way.  Without filters (TR off) B is compiled out
-// and the kernel fits seven CTAs per SM.
+// from the draft row the same way.  (The untruncated draft-logit verify runs
+// on the sampled verify's kernel instead.)
 //
 // Row passes load batches of 16-byte units per lane, sum them with packed
 // arithmetic (one maximum test per batch), and ask L2 for the batch three
@@ -559,22 +559,20 @@ __device__ __forceinline__ void warp_row_stats_pair(const void* tbase, int64_t t
 }
 
 // DL: draft logits instead of draft probabilities (q_i = softmax(d_i / T_d),
-// formed here from the draft row's own statistics).  TR: the top-p / min-p
-// machinery is compiled in (the untruncated draft-logit verify leaves it out,
-// which keeps shared memory small and the cluster up to 16 CTAs).
-template <int ES, bool DL, bool TR>
-__global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtasPerSM)
+// formed here from the draft row's own statistics).
+template <int ES, bool DL>
+__global__ void __launch_bounds__(kNT, sv::kTruncCtasPerSM)
     sv_trunc_kernel(const __grid_constant__ TArgs a) {
     constexpr int E = 16 / ES;
     constexpr int KEYBITS = 8 * ES;
     constexpr int LEVELS = KEYBITS / 8;
-    constexpr int MC = TR ? kMaxC : sv::kMaxCluster;  // largest cluster
-    constexpr int HB = TR ? kBins : 1;                // histogram bins held
-    constexpr int HC = TR ? kMaxC : 1;
+    constexpr int MC = kMaxC;  // largest cluster
+    constexpr int HB = kBins;  // histogram bins held
+    constexpr int HC = kMaxC;
     // row pass: loads in flight per lane and row (a target row alone, or the
     // target and draft rows together: deeper pairs spill registers)
-    constexpr int DA = (DL && !TR) ? 4 : ((TR && !DL) ? 8 : kDepth);
-    constexpr int DP = (DL && !TR) ? 2 : 4;
+    constexpr int DA = DL ? kDepth : 8;
+    constexpr int DP = 4;
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = (int)cluster.block_rank();
     const int b = (int)(blockIdx.x / (unsigned)a.C);
@@ -583,8 +581,8 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
     const int P = C * kNW;
     const int64_t V = a.V;
     const float c = a.c;
-    const bool use_min = TR && a.dmin > -INFINITY;
-    const bool use_top = TR && a.top_p < 1.0;
+    const bool use_min = a.dmin > -INFINITY;
+    const bool use_top = a.top_p < 1.0;
     // min-p bounds the kept set: one pass lists the survivors of a row and
     // the top-p cut is taken over those lists (aligned rows)
     const bool list_ok = use_min && a.vec;
@@ -602,14 +600,14 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
     __shared__ float ctot[kNW][kChunks];                         // draw: chunk totals per warp
     // min-p survivors: each warp's, then the CTA's (values and entry
     // indices); the draw over a listed row reuses them
-    constexpr int CW = TR ? kCandW : 1, CC = TR ? kCandC : 1;
+    constexpr int CW = kCandW, CC = kCandC;
     __shared__ float cw_v[kNW][CW];
     __shared__ int cw_i[kNW][CW];
     __shared__ int cw_n[kNW];
     __shared__ float cl_v[CC];
     __shared__ int cl_i[CC];
     __shared__ int cl_cnt[kNW];
-    __shared__ float smax[kNW][TR ? kSlots : 1];                // row pass: group maxima
+    __shared__ float smax[kNW][kSlots];                         // row pass: group maxima
 
     const int64_t v0 = (int64_t)rank * a.slice;
     const int64_t L = v0 < V ? (V - v0 < a.slice ? V - v0 : a.slice) : 0;
@@ -720,7 +718,7 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
         const int batch_u = 32 * ((DL && i < K && a.vec) ? DP : DA);
         const int nbat = (int)((w1 - w0 + batch_u - 1) / batch_u);
         const int per = (nbat + kSlots - 1) / kSlots > 0 ? (nbat + kSlots - 1) / kSlots : 1;
-        SlotMax slm{TR && list_ok ? smax[warp] : nullptr, per};
+        SlotMax slm{list_ok ? smax[warp] : nullptr, per};
         if (DL && i < K && a.vec) {
             warp_row_stats_pair<ES, DP>(a.logits, re, a.dlogits, ((int64_t)b * K + i) * V + v0, w0,
                                         w1, lane, c, a.cd, wmx, wsm, bad, dmx, dsm, dbad, &slm);
@@ -777,7 +775,7 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
         key_t = 0;
         listed = false;
         // ---- B: the kept set ----
-        if constexpr (TR) if (use_min || use_top) {
+        if (use_min || use_top) {
             // fixed point: 2^fix per unit weight, with fix chosen so that V
             // weights of at most 1 sum below 2^63 (44 bits for V <= 2^18);
             // each weight is off by at most 2^-(fix+1) after rounding
@@ -1163,40 +1161,9 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
         float cum_before = 0.f, Sw = 0.f, t = 0.f;
         int owner = -1;
         // draft logits, vector path: the draw's row pair (or the target row
-        // alone for the bonus row and the fallback) stays packed in registers,
-        // DD units deep.  With filters the weights are the bits unit_weights
-        // gives (the locate re-derives them that way); without filters every
-        // entry is kept, and both the totals pass and the locate take the
-        // packed vec_weights below.
-        const float2 c2 = make_float2(c, c), cd2 = make_float2(a.cd, a.cd);
-        const float2 nrq2 = make_float2(-rq, -rq);
-        const float nl = -lmax, nd = -dmax;
-        // w[t] = max(0, 2^((l - l_max) c) - 2^((d - d_max) c_d) E / S_d) (two), or
-        // 2^((l - l_max) c); returns their sum in entry order
-        const auto vec_weights = [&](const uint4& lr, const uint4& dr, bool two,
-                                     float (&w)[E]) -> float {
-            float2 dl[E / 2], dd[E / 2];
-            vec_minus<ES>(lr, nl, dl);
-            if (two)
-                vec_minus<ES>(dr, nd, dd);
-            float sum = 0.f;
-#pragma unroll
-            for (int h = 0; h < E / 2; ++h) {
-                const float2 y = __fmul2_rn(dl[h], c2);
-                float2 ev = make_float2(ex2(y.x), ex2(y.y));
-                if (two) {
-                    const float2 yd = __fmul2_rn(dd[h], cd2);
-                    ev = __ffma2_rn(make_float2(ex2(yd.x), ex2(yd.y)), nrq2, ev);
-                    ev.x = fmaxf(ev.x, 0.f);
-                    ev.y = fmaxf(ev.y, 0.f);
-                }
-                w[2 * h] = ev.x;
-                w[2 * h + 1] = ev.y;
-                sum += ev.x;
-                sum += ev.y;
-            }
-            return sum;
-        };
+        // alone for the bonus row and the fallback) stays in registers, DD
+        // units deep; the weights are the bits unit_weights gives (the locate
+        // re-derives them that way).
         const auto unit_weights_raw = [&](const uint4& lr, const uint4& dr, bool two) -> float {
             float sum = 0.f;
 #pragma unroll
@@ -1214,7 +1181,7 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
         // the kept entries only.
         float* sv_v = &cw_v[0][0];
         int* sv_i = &cw_i[0][0];
-        if (TR && listed) {
+        if (listed) {
             for (int k = tid; k < ncl; k += kNT) {
                 const int ik = cl_i[k];
                 int r = 0;
@@ -1229,7 +1196,7 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
             float wt = 0.f, wtc = 0.f, cpart = 0.f;
             bool badq = false;
             int gcnt = 0, chunk = 0;
-            if (TR && listed) {
+            if (listed) {
                 if (warp == 0) {
                     // weights (scaled by E) in vocabulary order, kept in cl_v
                     for (int k0 = 0; k0 < ncl; k0 += 32) {
@@ -1255,8 +1222,8 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
                     }
                 }
             }
-            if constexpr (DL) if (a.vec && !(TR && listed)) {
-                constexpr int DD = TR ? 8 : 4;
+            if constexpr (DL) if (a.vec && !listed) {
+                constexpr int DD = 8;
                 const bool two = resid && !fallback;
                 // the steps st0 .. st0 + DD - 1 are units w0 + st * 32 + lane: one
                 // contiguous batch of DD * 32 units, as in the row loops
@@ -1283,12 +1250,7 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
                         if (st >= nsub)
                             break;
                         if (w0 + st * 32 + lane < w1) {
-                            if constexpr (TR) {
-                                cpart += unit_weights_raw(lr[k], dr[k], two);
-                            } else {
-                                float w[E];
-                                cpart += vec_weights(lr[k], dr[k], two, w);
-                            }
+                            cpart += unit_weights_raw(lr[k], dr[k], two);
                         }
                         if (++gcnt == g32 || st + 1 == nsub) {  // chunk `chunk` ends here
                             const float ct = warp_sum(cpart);
@@ -1302,7 +1264,7 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
                     }
                 }
             }
-            for (int64_t st0 = 0; st0 < (((DL && a.vec) || (TR && listed)) ? 0 : nsub);
+            for (int64_t st0 = 0; st0 < (((DL && a.vec) || listed) ? 0 : nsub);
                  st0 += kDepth) {
                 float l[kDepth][E], qv[kDepth][E];
                 bool have[kDepth];
@@ -1375,7 +1337,7 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
         if (state == SV_OK && owner == rank * kNW + warp) {
             const float tl = t - cum_before;
             int64_t tok = -1;
-            if (TR && listed) {
+            if (listed) {
                 // first survivor whose running weight passes the point, or
                 // (rounding) the last one with weight
                 float run = 0.f;
@@ -1437,19 +1399,8 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
                     for (int k = 0; k < E; ++k)
                         w[k] = 0.f;
                     const int64_t ui = w0 + st * 32 + lane;
-                    bool packed = false;  // the totals pass took vec_weights
-                    if constexpr (DL && !TR)
-                        packed = a.vec != 0;
-                    if (packed) {
-                        if (ui < w1) {
-                            const bool two = resid && !fallback;
-                            const uint4 lr = ld_stream(rp + ui);
-                            const uint4 dr = two ? ld_stream(dp + ui) : lr;
-                            lt = vec_weights(lr, dr, two, w);
-                        }
-                    } else if (load_unit(st, l, qv)) {
+                    if (load_unit(st, l, qv))
                         lt = unit_weights(l, qv, w, dummy);
-                    }
                     int lpos = -1;
                     for (int k = 0; k < U; ++k)
                         if (w[k] > 0.f)
@@ -1548,22 +1499,6 @@ __global__ void __launch_bounds__(kNT, TR ? sv::kTruncCtasPerSM : sv::kDraftCtas
 
 namespace sv {
 
-int trunc_set_attributes() {
-    const void* fns[6] = {(const void*)sv_trunc_kernel<2, false, true>,
-                          (const void*)sv_trunc_kernel<4, false, true>,
-                          (const void*)sv_trunc_kernel<2, true, true>,
-                          (const void*)sv_trunc_kernel<4, true, true>,
-                          (const void*)sv_trunc_kernel<2, true, false>,
-                          (const void*)sv_trunc_kernel<4, true, false>};
-    for (const void* f : fns)
-        if (cudaFuncSetAttribute(f, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
-            cudaSuccess) {
-            (void)cudaGetLastError();
-            return 1;
-        }
-    return 0;
-}
-
 int trunc_launch(const TruncLaunch& g, void* stream) {
     TArgs a;
     std::memset(&a, 0, sizeof a);
@@ -1605,17 +1540,15 @@ int trunc_launch(const TruncLaunch& g, void* stream) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    // q given: the truncated kernel; draft logits: with or without the filters
+    // q given, or draft logits (with a filter on: the untruncated draft-logit
+    // verify runs on the sampled verify's kernel)
     cudaError_t e;
     if (!g.dlogits)
-        e = g.es == 2 ? cudaLaunchKernelEx(&cfg, sv_trunc_kernel<2, false, true>, a)
-                      : cudaLaunchKernelEx(&cfg, sv_trunc_kernel<4, false, true>, a);
-    else if (g.filters)
-        e = g.es == 2 ? cudaLaunchKernelEx(&cfg, sv_trunc_kernel<2, true, true>, a)
-                      : cudaLaunchKernelEx(&cfg, sv_trunc_kernel<4, true, true>, a);
+        e = g.es == 2 ? cudaLaunchKernelEx(&cfg, sv_trunc_kernel<2, false>, a)
+                      : cudaLaunchKernelEx(&cfg, sv_trunc_kernel<4, false>, a);
     else
-        e = g.es == 2 ? cudaLaunchKernelEx(&cfg, sv_trunc_kernel<2, true, false>, a)
-                      : cudaLaunchKernelEx(&cfg, sv_trunc_kernel<4, true, false>, a);
+        e = g.es == 2 ? cudaLaunchKernelEx(&cfg, sv_trunc_kernel<2, true>, a)
+                      : cudaLaunchKernelEx(&cfg, sv_trunc_kernel<4, true>, a);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return 1;

@@ -163,18 +163,28 @@ def test_draft_logits_plan_invariants(sv, B, K, V, dtype, filters):
     per_sm = 4 if filters else 7  # resident CTAs per SM (launch bounds)
     if B <= 152 * per_sm:
         assert B * C <= 152 * per_sm
-    # with a filter on, the plan is the truncated kernel's
+    # with a filter on, the plan is the truncated kernel's; without, the
+    # sampled verify's mapping with room for the draft rows' partials
     if filters:
         assert p == sv.spec_verify_plan_truncated_for(152, 16, B, K, V, dtype, 0)[1]
+    else:
+        q = sv.spec_verify_plan_for(152, 232448, 16, B, K, V, dtype, 0, 0, 0)[1]
+        for k in ("cluster", "slice", "grid", "threads", "bulk_copy", "stages"):
+            assert p[k] == q[k], k
+        assert p["group"] <= q["group"] and p["smem_bytes"] >= q["smem_bytes"]
+        assert p["smem_bytes"] <= 232448
 
 
 def test_draft_logits_workload_plans(sv):
     assert dplan(sv, 256, 7, 128256, 1, 0)[1]["cluster"] == 4
     assert dplan(sv, 256, 7, 128256, 1, 1)[1]["cluster"] == 2
-    assert dplan(sv, 64, 3, 151936, 1, 0)[1]["cluster"] == 16
-    assert dplan(sv, 8, 4, 32000, 1, 0)[1]["cluster"] == 16
+    assert dplan(sv, 256, 7, 128256, 1, 0)[1]["stages"] == 3
+    assert dplan(sv, 64, 3, 151936, 1, 0)[1]["cluster"] == 8
+    assert dplan(sv, 64, 3, 151936, 1, 0)[1]["stages"] == 6
+    assert dplan(sv, 1, 4, 32000, 0, 0)[1]["cluster"] == 16
+    assert dplan(sv, 8, 4, 32000, 1, 0)[1]["cluster"] == 8
     assert dplan(sv, 8, 4, 32000, 1, 1)[1]["cluster"] == 8
-    assert dplan(sv, 8, 4, 32000, 1, 0, dev=dict(GB300, max_cluster=8))[1]["cluster"] == 8
+    assert dplan(sv, 1, 4, 32000, 0, 0, dev=dict(GB300, max_cluster=8))[1]["cluster"] == 8
     assert dplan(sv, 4, 2, 50000, 1, 0, oc=16, dev=dict(GB300, max_cluster=8))[0] == \
         sv.SV_ERR_UNSUPPORTED
     assert dplan(sv, 4, 2, 50000, 1, 1, oc=16)[0] == sv.SV_ERR_INVALID_ARG
