@@ -577,11 +577,14 @@ __device__ __forceinline__ uint4 load_vec_elems(const void* logits, int64_t gbas
 
 // Sum over this lane's vectors of one chunk (vector k*32 + lane of `buf`, for
 // k*32 + lane < nv) of 2^((l - a) c), with TRACK folding the raw values into
-// the NaN-propagating max `mx` on the way.  Two packed accumulators keep the
-// dependency chains short.
-template <int ES, bool FULL, bool TRACK>
-__device__ __forceinline__ float fold_chunk(const uint4* buf, int nv, float a, float c,
-                                            typename Elem<ES>::Max& mx) {
+// the NaN-propagating max `mx` on the way.  Returned as two parts: with SPLIT
+// the sums over the chunk's two halves (vectors k < kVecPerLane / 2, and the
+// rest: a bf16 chunk's two draw tiles), without it the sum and 0, taken in
+// two packed accumulators alternating within a vector (shorter dependency
+// chains; the draft-logit form measured faster with them).
+template <int ES, bool FULL, bool TRACK, bool SPLIT = true>
+__device__ __forceinline__ float2 fold_chunk(const uint4* buf, int nv, float a, float c,
+                                             typename Elem<ES>::Max& mx) {
     constexpr int E = Elem<ES>::E;
     const int lane = threadIdx.x & 31;
     const float2 c2 = make_float2(c, c);
@@ -599,15 +602,18 @@ __device__ __forceinline__ float fold_chunk(const uint4* buf, int nv, float a, f
             for (int h = 0; h < E / 2; ++h) {
                 const float2 y = __fmul2_rn(d[h], c2);
                 const float2 e = make_float2(ex2_approx(y.x), ex2_approx(y.y));
-                if (h & 1)
-                    s1 = __fadd2_rn(s1, e);
-                else
+                if (SPLIT ? k < kVecPerLane / 2 : !(h & 1))
                     s0 = __fadd2_rn(s0, e);
+                else
+                    s1 = __fadd2_rn(s1, e);
             }
         }
     }
-    const float2 t = __fadd2_rn(s0, s1);
-    return t.x + t.y;
+    if constexpr (!SPLIT) {
+        const float2 t = __fadd2_rn(s0, s1);
+        return make_float2(t.x + t.y, 0.f);
+    }
+    return make_float2(s0.x + s0.y, s1.x + s1.y);
 }
 
 // One lane's running partial of a row: offset a, sum s of 2^((l - a) c) over
@@ -625,8 +631,8 @@ __device__ __forceinline__ float fold_chunk(const uint4* buf, int nv, float a, f
 // against the row max); without it a chunk is accepted on its sum alone: a
 // sum of at most kFoldBound = (entries per lane per chunk) x 2^8 means every
 // term is at most kFoldBound, and a larger (or NaN / inf) sum sends the chunk
-// through the max and the rules above.
-template <int ES>
+// through the max and the rules above.  SPLIT: see fold_chunk.
+template <int ES, bool SPLIT = true>
 struct LaneSum {
     static constexpr float kFoldBound = (float)(kVecPerLane * Elem<ES>::E * 256);
     float a, s;
@@ -644,20 +650,26 @@ struct LaneSum {
         a = Elem<ES>::value(m0);
     }
 
-    __device__ __forceinline__ void chunk(const uint4* buf, int nv, float c, bool track) {
+    // Folds one chunk in; returns the lane's sums over the chunk's two halves
+    // (vectors k < kVecPerLane / 2 and the rest) against the offset `a` holds
+    // afterwards (zero when the chunk adds nothing).
+    __device__ __forceinline__ float2 chunk(const uint4* buf, int nv, float c, bool track) {
         typename Elem<ES>::Max cm = Elem<ES>::max_init();
+        float2 hs;
         float cs, m;
         if (track) {
-            cs = nv == kChunkVecs ? fold_chunk<ES, true, true>(buf, nv, a, c, cm)
-                                  : fold_chunk<ES, false, true>(buf, nv, a, c, cm);
+            hs = nv == kChunkVecs ? fold_chunk<ES, true, true, SPLIT>(buf, nv, a, c, cm)
+                                  : fold_chunk<ES, false, true, SPLIT>(buf, nv, a, c, cm);
+            cs = hs.x + hs.y;
             mx = Elem<ES>::mmax(mx, cm);
             m = Elem<ES>::value(cm);
         } else {
-            cs = nv == kChunkVecs ? fold_chunk<ES, true, false>(buf, nv, a, c, cm)
-                                  : fold_chunk<ES, false, false>(buf, nv, a, c, cm);
+            hs = nv == kChunkVecs ? fold_chunk<ES, true, false, SPLIT>(buf, nv, a, c, cm)
+                                  : fold_chunk<ES, false, false, SPLIT>(buf, nv, a, c, cm);
+            cs = hs.x + hs.y;
             if (cs <= kFoldBound) {  // false for NaN
                 s += cs;
-                return;
+                return hs;
             }
             const int lane = threadIdx.x & 31;
 #pragma unroll
@@ -668,19 +680,21 @@ struct LaneSum {
         }
         if ((m - a) * c <= 8.f) {  // false for NaN, +inf, or no offset yet
             s += cs;
-            return;
+            return hs;
         }
         if (!(m < INFINITY)) {  // NaN or +inf: the row is poisoned through mx; stop summing
             a = INFINITY;
             s = 0.f;
-            return;
+            return make_float2(0.f, 0.f);
         }
         if (!(m > -INFINITY))  // an all -inf chunk seen with no offset yet adds nothing
-            return;
+            return make_float2(0.f, 0.f);
         s = s > 0.f ? s * ex2_approx((a - m) * c) : 0.f;
         a = m;
         typename Elem<ES>::Max unused = Elem<ES>::max_init();
-        s += fold_chunk<ES, false, false>(buf, nv, a, c, unused);
+        hs = fold_chunk<ES, false, false, SPLIT>(buf, nv, a, c, unused);
+        s += hs.x + hs.y;
+        return hs;
     }
 };
 
@@ -798,7 +812,7 @@ __global__ void __launch_bounds__(NT, NS == sv::kStages ? sv::kThreadsPerSM / NT
     unsigned long long* bar = reinterpret_cast<unsigned long long*>(smem_raw + a.off_bar);
     unsigned long long* xbar = bar + NW * kStages;  // [0..1] row partials by parity, [2..3] draw rounds
     float4* part = reinterpret_cast<float4*>(smem_raw + a.off_part);  // [2][GG][C*NW] (a, S.hi, S.lo, max)
-    float* tt = reinterpret_cast<float*>(smem_raw + a.off_tt);          // [NW][ntw] draw tile totals
+    float* tt = reinterpret_cast<float*>(smem_raw + a.off_tt);          // [2][NW][ntw] draw tile totals, offsets
     unsigned char* ring = smem_raw + (size_t)warp * kStages * kChunkBytes;
     unsigned long long* wbar = bar + warp * kStages;
 
@@ -955,10 +969,36 @@ __global__ void __launch_bounds__(NT, NS == sv::kStages ? sv::kThreadsPerSM / NT
     // Streams this warp's stretch of row `row` into ls.  After every chunk
     // poll() may end the stream (returns false): a decision arrived that
     // makes the row unnecessary.
+    // The bonus row K also leaves, per draw tile of this warp's stretch, the
+    // warp's sum of 2^((l - a_w) c) and the offset a_w it is taken against
+    // (the lanes' largest offset when the tile's chunk was folded), so a
+    // bonus draw needs no second pass over the row.  (Not in the draft-logit
+    // form, which sums its chunks unsplit and keeps the pass.)
+    constexpr int kTilesPerChunk = kChunkVecs * E / sv::kDrawTile;  // 2 (bf16) or 1 (f32)
+    static_assert(kTilesPerChunk == 1 || kTilesPerChunk == 2, "draw tiles per chunk");
+    float* const tt_w = tt + warp * a.ntw;          // this warp's tile totals
+    float* const tta_w = tt + (NW + warp) * a.ntw;  // ... and their offsets
+    auto record_tiles = [&](int ch, float2 hs, float la, float cc) {
+        const float aw = warp_max_nan(la);
+        const float sc = (aw > -INFINITY && aw < INFINITY) ? ex2_approx((la - aw) * cc) : 0.f;
+        const float t0 = warp_sum_bcast((kTilesPerChunk == 2 ? hs.x : hs.x + hs.y) * sc);
+        const float t1 = kTilesPerChunk == 2 ? warp_sum_bcast(hs.y * sc) : 0.f;
+        const int t = ch * kTilesPerChunk;
+        if (lane == 0) {
+            tt_w[t] = t0;
+            tta_w[t] = aw;
+            if (kTilesPerChunk == 2 && t + 1 < a.ntw) {
+                tt_w[t + 1] = t1;
+                tta_w[t + 1] = aw;
+            }
+        }
+    };
+
     // (DL: half 1 streams the draft row of `row` at c_d, without the exact max)
-    auto stream_row = [&](int row, LaneSum<ES>& ls, auto&& poll, int half = 0) -> bool {
+    auto stream_row = [&](int row, LaneSum<ES, !DL>& ls, auto&& poll, int half = 0) -> bool {
         const float cc = half ? a.cd : c;
         const bool trk = half ? false : track;
+        const bool tiles = !DL && row == K && half == 0;
         ls.a = -INFINITY;
         ls.s = 0.f;
         ls.mx = Elem<ES>::max_init();
@@ -983,7 +1023,9 @@ __global__ void __launch_bounds__(NT, NS == sv::kStages ? sv::kThreadsPerSM / NT
             }
             if (ch == 0)
                 ls.start(buf, nv);
-            ls.chunk(buf, nv, cc, trk);
+            const float2 hs = ls.chunk(buf, nv, cc, trk);
+            if (tiles)
+                record_tiles(ch, hs, ls.a, cc);
             if (a.bulk)
                 release();
             else
@@ -998,7 +1040,7 @@ __global__ void __launch_bounds__(NT, NS == sv::kStages ? sv::kThreadsPerSM / NT
     // double-float, NaN-propagating max -- pushed into slot (par, r) of every
     // CTA of the cluster.
     // (DL: half 1 publishes the draft row's partial, at c_d, into slot r + G)
-    auto publish = [&](int par, int r, const LaneSum<ES>& ls, int half = 0) {
+    auto publish = [&](int par, int r, const LaneSum<ES, !DL>& ls, int half = 0) {
         const float aw = warp_max_nan(ls.a);
         const float mw = (track && !half) ? warp_max_nan(Elem<ES>::value(ls.mx)) : aw;
         FF sw = {0.f, 0.f};
@@ -1259,7 +1301,7 @@ __global__ void __launch_bounds__(NT, NS == sv::kStages ? sv::kThreadsPerSM / NT
             // than the ring's lookahead into its draft row is read)
             bool stopped = false;
             for (int h = 0; h < ((DL && cur < K) ? 2 : 1); ++h) {
-                LaneSum<ES> ls;
+                LaneSum<ES, !DL> ls;
                 if (!stream_row(cur, ls, poll, h)) {
                     stopped = true;
                     break;
@@ -1297,7 +1339,7 @@ __global__ void __launch_bounds__(NT, NS == sv::kStages ? sv::kThreadsPerSM / NT
             lim_row = g0 + ng - 1;
             for (int r = 0; r < ng; ++r)
                 for (int h = 0; h < (r < nd ? 2 : 1); ++h) {
-                    LaneSum<ES> ls;
+                    LaneSum<ES, !DL> ls;
                     (void)stream_row(g0 + r, ls, no_poll, h);
                     publish(par, r, ls, h);
                 }
@@ -1380,7 +1422,6 @@ __global__ void __launch_bounds__(NT, NS == sv::kStages ? sv::kThreadsPerSM / NT
         const unsigned char* lbase = lrow + e0 * ES;
         const float* qbase = qrow ? qrow + e0 : nullptr;
         const unsigned char* dbase = drow ? drow + e0 * ES : nullptr;
-        float* tt_w = tt + warp * a.ntw;
         uint32_t qbits = 0;
         auto load_logits = [&](int t, uint4 (&lv)[kDV]) {
 #pragma unroll
@@ -1544,10 +1585,31 @@ __global__ void __launch_bounds__(NT, NS == sv::kStages ? sv::kThreadsPerSM / NT
             }
             return wacc;
         };
+        // The bonus draw's tile totals from the row pass: each rescaled from
+        // its offset to the row's merged offset, summed in tile order.
+        auto bonus_from_tiles = [&]() -> FF {
+            __syncwarp();  // lane 0's records are visible to the warp
+            FF wacc = {0.f, 0.f};
+            for (int t0 = 0; t0 < ntile; t0 += 32) {
+                const int t = t0 + lane;
+                float v = 0.f;
+                if (t < ntile) {
+                    const float tv = tt_w[t];
+                    v = tv > 0.f ? tv * ex2_approx((tta_w[t] - rowA) * c) : 0.f;
+                    tt_w[t] = v;
+                }
+                const int n = min(32, ntile - t0);
+                for (int k = 0; k < n; ++k)
+                    wacc = ff_add(wacc, __shfl_sync(kFull, v, k));
+            }
+            return wacc;
+        };
         for (int round = 0; round < 2; ++round) {
             if (tid == 0)
                 mbar_arrive_expect_tx(&xbar[2 + sp], (uint32_t)(C * 16));
-            const FF wacc = mode == kModeResidual ? pass(std::true_type{}) : pass(std::false_type{});
+            const FF wacc = mode == kModeResidual ? pass(std::true_type{})
+                            : (!DL && mode == kModeBonus) ? bonus_from_tiles()
+                                                  : pass(std::false_type{});
             const bool badq = __any_sync(kFull, !q_bits_valid(qbits));
             const bool to = __any_sync(kFull, timed_out);
             if (lane == 0) {

@@ -45,7 +45,7 @@ inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 // parities, draw totals of the two draw rounds), the row partials pushed by
 // every warp of the cluster (offset, sum hi, sum lo, max: 16 bytes)
 // [2 parities][group rows][cluster CTAs x warps], and the draw's per-warp tile
-// totals.
+// totals with the offsets the bonus row's totals are taken against.
 struct Layout {
     int64_t wvec;       // 16-byte vectors per warp stretch
     int64_t ntw;        // draw tiles (kDrawTile entries) per warp stretch
@@ -65,7 +65,7 @@ inline Layout layout_for(int64_t slice, int elem_bytes, int group, int threads, 
     l.off_bar = l.off_fixed + kFixedSmem;
     l.off_part = l.off_bar + round_up((nw * stages + kExchangeBarriers) * 8, 16);
     l.off_tt = l.off_part + round_up(2 * (int64_t)group * cluster * nw * 16, 16);
-    l.total = l.off_tt + round_up(nw * l.ntw * 4, 16);
+    l.total = l.off_tt + round_up(2 * nw * l.ntw * 4, 16);  // tile totals, then their offsets
     return l;
 }
 

@@ -94,9 +94,16 @@ def test_overrides(sv):
 
 
 def test_shared_memory_does_not_grow_with_the_vocabulary(sv):
-    small = plan(sv, 1, 1, 32000, 1)[1]["smem_bytes"]
-    huge = plan(sv, 1, 1, 1 << 24, 1)[1]["smem_bytes"]
-    assert huge - small < 16 * 1024
+    """The rings are fixed and the exchange slots follow the cluster (at most
+    16 CTAs); only the draw's tile arrays (a total and an offset per 512
+    entries of a CTA's slice) follow V."""
+    small = plan(sv, 1, 1, 32000, 1)[1]
+    huge = plan(sv, 1, 1, 1 << 24, 1)[1]
+    tiles = lambda p: 2 * 4 * 4 * -(-p["slice"] // (4 * 512))  # [2][warps][tiles] floats
+    slots = lambda p: 2 * p["group"] * p["cluster"] * 4 * 16   # [2][group][C x warps] partials
+    grow = huge["smem_bytes"] - small["smem_bytes"]
+    assert grow <= tiles(huge) - tiles(small) + slots(huge) - slots(small) + 64
+    assert tiles(huge) <= 16 * 1024 + 64
     tiny = dict(GB300, smem=8 * 1024)
     assert plan(sv, 1, 1, 32000, 0, dev=tiny)[0] == sv.SV_ERR_UNSUPPORTED
 
