@@ -102,6 +102,17 @@ def test_random_shapes(dtype, V, T, Td, top_p, min_p, cluster):
            cluster)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_large_batch_on_three_stage_rings(dtype):
+    """Batches too large for the six-stage rings, one CTA per sequence: the
+    draft-logit form of the 128-thread kernel with three stages per warp."""
+    inp = workloads.make_random_draft_logits(800, 3, 3000, dtype, T=0.9, T_draft=1.2, seed=41)
+    p = gh.verifier().plan_draft_logits(inp.B, inp.K, inp.V, 1 if dtype == "bf16" else 0, 0)
+    assert p["stages"] == 3 and p["threads"] == 128 and p["group"] == 1
+    info, _, _ = _check(inp, label=f"{dtype} three stages")
+    assert info["exact"] + info["accept_ties"] + info["draw_ties"] == inp.B
+
+
 @pytest.mark.parametrize("K", [0, 1, 32])
 def test_depths(K):
     inp = workloads.make_random_draft_logits(12, K, 2048, "bf16", T=0.9, T_draft=1.1, seed=K + 5)

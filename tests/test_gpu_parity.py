@@ -75,6 +75,17 @@ def test_random_shapes_every_plan(shape, plan):
     gh.compare(g, o, K, label=f"{shape}/{plan}")
 
 
+def test_f32_batch_on_three_stage_rings():
+    """A float32 batch too large for the six-stage rings: the 128-thread
+    kernel with three stages per warp (one CTA per sequence)."""
+    inp = workloads.make_random(800, 3, 3000, dtype="f32", T=0.9, seed=31)
+    p = gh.verifier().plan(inp.B, inp.K, inp.V, 0)
+    assert p["stages"] == 3 and p["threads"] == 128 and p["group"] == 1
+    info = gh.compare(gh.gpu_verify_inputs(inp), oracle.verify_inputs(inp), inp.K,
+                      label="f32 three stages")
+    _record("f32_three_stages", info)
+
+
 def test_many_small_sequences_all_positions():
     """A batch large enough that every accepted length 1..K+1 occurs."""
     inp = workloads.make_random(3000, 6, 300, dtype="bf16", T=1.0, sigma=1.0, sigma_draft=0.3,
