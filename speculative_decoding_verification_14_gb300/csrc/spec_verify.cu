@@ -480,11 +480,17 @@ struct Elem<2> {
 
 // ------------------------------------------------------- warp helpers -----
 
+// Floats as ints in the same order (any NaN above +inf), so that one integer
+// warp reduction gives the float maximum.
+__device__ __forceinline__ int ord_key(float f) {
+    const int i = f != f ? 0x7fffffff : __float_as_int(f);
+    return i >= 0 ? i : i ^ 0x7fffffff;
+}
+__device__ __forceinline__ float ord_val(int k) { return __int_as_float(k >= 0 ? k : k ^ 0x7fffffff); }
+
+// NaN-propagating maximum over the warp, in every lane
 __device__ __forceinline__ float warp_max_nan(float v) {
-#pragma unroll
-    for (int o = 16; o; o >>= 1)
-        v = fmax_nan(v, __shfl_xor_sync(kFull, v, o));
-    return v;
+    return ord_val(__reduce_max_sync(kFull, ord_key(v)));
 }
 
 // Sums over the warp, reduced in one fixed order and broadcast from lane 0 so
@@ -1097,9 +1103,7 @@ __global__ void __launch_bounds__(NT, NS == sv::kStages ? sv::kThreadsPerSM / NT
             }
         }
         M = warp_max_nan(mloc);
-#pragma unroll
-        for (int sft = 16; sft; sft >>= 1)
-            amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, sft));
+        amax = ord_val(__reduce_max_sync(kFull, ord_key(amax)));  // (offsets are never NaN)
         // (a NaN or inf entry poisons its lane's offset to +inf, an all -inf
         // row leaves every offset at -inf: both show in the merged offset)
         FF acc = {0.f, 0.f};
