@@ -192,6 +192,36 @@ def test_device_errors_mark_only_their_sequence_and_clear():
     assert v.error() == (sv.SV_OK, 0)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("stats", [True, False])
+def test_nan_of_either_sign_is_nonfinite(dtype, stats):
+    """A NaN in a reached row is a sequence error whatever its sign bit (the
+    kernel's warp maxima order floats by integer keys); rows that are all
+    negative keep their ordinary parity."""
+    import speculative_decoding_verification_14_gb300 as sv
+    inp = workloads.make_random(5, 3, 4096, dtype=dtype, seed=21)
+    lg = inp.logits.copy()
+    if dtype == "f32":
+        bits = lg.view(np.uint32)
+        bits[0, 0, 100] = 0xFFC00000       # negative quiet NaN
+        bits[1, 0, 4095] = 0x7FC00000      # positive quiet NaN
+        bits[2, 0, 9] = 0xFF800001         # negative signalling NaN
+        lg[3] = lg[3] - np.float32(1e4)    # every logit negative
+    else:
+        lg[0, 0, 100] = 0xFFC0
+        lg[1, 0, 4095] = 0x7FC0
+        lg[2, 0, 9] = 0xFF81
+        f = workloads.logits_as_f64(lg[3:4], "bf16") - 1e4
+        lg[3:4] = workloads.f32_to_bf16_bits(f.astype(np.float32))
+    inp.logits = lg
+    o = oracle.verify_inputs(inp)
+    g = gh.gpu_verify_inputs(inp, stats=stats)
+    gh.compare(g, o, 3, check_stats=stats, label=f"nan {dtype} stats={stats}")
+    assert list(g["status"][:3]) == [sv.SV_ERR_NONFINITE] * 3
+    assert list(g["status"][3:]) == [sv.SV_OK] * 2
+    gh.verifier().error()  # clear the sticky word
+
+
 @pytest.mark.parametrize("name", workloads.CONFIG_ORDER)
 def test_without_row_stats_nothing_changes(name):
     """Without row_stats the kernel drops the exact running max from its fold
