@@ -143,7 +143,10 @@ int spec_verify_get_plan(sv_ctx* ctx, int B, int K, int64_t V, int logits_dtype,
 
 /* Force parts of the plan (0 = automatic): cluster size 1..16, rows per group
  * 1..K+1 (clamped), threads per CTA 128/256/512.  Used by tests to cover every
- * plan and by tuning sweeps.  Returns SV_ERR_INVALID_ARG on values outside those sets. */
+ * plan and by tuning sweeps.  The greedy, truncated and draft-logit calls take
+ * only the cluster size (the truncated kernel, also under a draft-logit call
+ * with a filter on, caps it at 8).  Returns
+ * SV_ERR_INVALID_ARG on values outside those sets. */
 int spec_verify_set_plan_override(sv_ctx* ctx, int cluster, int group, int threads);
 
 /* The planner as a pure host function of the device limits, for tests:
